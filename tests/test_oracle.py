@@ -1,0 +1,302 @@
+"""Pins for the fp64 CPU oracle, against things other than itself.
+
+Each test ties one oracle function to an independent fact: a library routine
+(torch / numpy / scipy conversions and products), brute force in plain
+Python, a closed form, or an algebraic identity of the exact product.  The
+set is chosen so that a dropped term, a wrong sign or index, or a transposed
+operand anywhere in the oracle fails at least one test.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from complexity_matmul_tcgen05_gb300 import inputs
+
+ALL16 = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+
+
+def _torch_values(bits, tdtype):
+    t = torch.from_numpy(bits.view(np.int16).copy()).view(tdtype)
+    return t.to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------- decoding
+
+@pytest.mark.parametrize("dtype,tdtype", [("f16", torch.float16), ("bf16", torch.bfloat16)])
+def test_decode_all_patterns_match_torch(dtype, tdtype):
+    ours = oracle.decode(ALL16, dtype)
+    ref = _torch_values(ALL16, tdtype)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_decode_special_values():
+    assert oracle.decode(np.array([0x3C00], np.uint16), "f16")[0] == 1.0
+    assert oracle.decode(np.array([0x0001], np.uint16), "f16")[0] == 2.0 ** -24
+    assert oracle.decode(np.array([0x7BFF], np.uint16), "f16")[0] == 65504.0
+    assert oracle.decode(np.array([0x3F80], np.uint16), "bf16")[0] == 1.0
+    assert oracle.decode(np.array([0x0001], np.uint16), "bf16")[0] == 2.0 ** -133
+    assert oracle.decode(np.array([0xC000], np.uint16), "bf16")[0] == -2.0
+
+
+# ---------------------------------------------------------------- encoding
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_encode_roundtrips_every_non_nan_pattern(dtype):
+    vals = oracle.decode(ALL16, dtype)
+    keep = ~np.isnan(vals)
+    back = oracle.encode(vals[keep], dtype)
+    assert np.array_equal(back, ALL16[keep])
+
+
+def test_encode_f16_matches_numpy_rne_from_double():
+    rng = np.random.default_rng(7)
+    mant = rng.random(200000) + 0.5
+    expo = rng.integers(-30, 18, 200000)
+    x = np.ldexp(mant, expo) * np.where(rng.random(200000) < 0.5, -1, 1)
+    # exact ties: midpoints between neighbouring fp16 values
+    base = oracle.decode(ALL16[(ALL16 & 0x7C00) != 0x7C00], "f16")
+    base = np.sort(base[np.isfinite(base)])
+    mids = (base[:-1] + base[1:]) / 2
+    x = np.concatenate([x, mids, [65519.0, 65520.0, 65536.0, 1e-9, -1e-9]])
+    ours = oracle.encode(x, "f16")
+    ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_encode_bf16_matches_torch_on_float32_values():
+    rng = np.random.default_rng(8)
+    mant = rng.random(200000) + 0.5
+    expo = rng.integers(-140, 120, 200000)
+    x = (np.ldexp(mant, expo) * np.where(rng.random(200000) < 0.5, -1, 1)).astype(np.float32)
+    x = x[np.isfinite(x)]
+    ours = oracle.encode(x.astype(np.float64), "bf16")
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_encode_bf16_ties_go_to_even():
+    one = 1.0
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: even is 1.0
+    assert oracle.encode(np.array([one + 2.0 ** -8]), "bf16")[0] == 0x3F80
+    # 1 + 3*2^-8 is halfway between 1+2^-7 (odd) and 1+2^-6 (even)
+    assert oracle.encode(np.array([one + 3 * 2.0 ** -8]), "bf16")[0] == 0x3F82
+    # just above a tie rounds up
+    assert oracle.encode(np.array([one + 2.0 ** -8 + 2.0 ** -30]), "bf16")[0] == 0x3F81
+
+
+# ----------------------------------------------------------- classical gemm
+
+def _brute(A, B):
+    M, K = len(A), len(A[0])
+    N = len(B[0])
+    C = [[0.0] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s = 0.0
+            for k in range(K):
+                s += A[i][k] * B[k][j]
+            C[i][j] = s
+    return C
+
+
+def test_gemm_equals_brute_force_bitwise():
+    rng = np.random.default_rng(1)
+    for (M, N, K) in [(1, 1, 1), (3, 5, 4), (7, 2, 9), (4, 4, 16)]:
+        A = rng.standard_normal((M, K))
+        B = rng.standard_normal((K, N))
+        ref = np.array(_brute(A.tolist(), B.tolist()))
+        assert np.array_equal(oracle.gemm(A, B), ref)
+
+
+@pytest.mark.parametrize("shape", [(17, 33, 65), (64, 1, 128), (1, 96, 31), (130, 70, 257)])
+def test_gemm_matches_numpy(shape):
+    M, N, K = shape
+    rng = np.random.default_rng(M * N + K)
+    A = rng.uniform(-1, 1, (M, K))
+    B = rng.uniform(-1, 1, (K, N))
+    C = oracle.gemm(A, B)
+    ref = A @ B
+    assert np.max(np.abs(C - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+def test_gemm_identity_zero_permutation_exact():
+    rng = np.random.default_rng(2)
+    X = rng.standard_normal((12, 12))
+    I = np.eye(12)
+    assert np.array_equal(oracle.gemm(I, X), X)
+    assert np.array_equal(oracle.gemm(X, I), X)
+    assert np.array_equal(oracle.gemm(np.zeros((12, 12)), X), np.zeros((12, 12)))
+    perm = rng.permutation(12)
+    P = I[perm]
+    assert np.array_equal(oracle.gemm(P, X), X[perm])
+    assert np.array_equal(oracle.gemm(X, P.T), X[:, perm])
+
+
+def test_gemm_transpose_identity():
+    rng = np.random.default_rng(3)
+    A = rng.standard_normal((9, 13))
+    B = rng.standard_normal((13, 6))
+    assert np.array_equal(oracle.gemm(A, B).T, oracle.gemm(B.T, A.T))
+
+
+def test_gemm_not_transposed_operand():
+    # a non-square case where A@B and A@B.T-like mistakes differ in shape/value
+    A = np.array([[1.0, 2.0, 3.0]])
+    B = np.array([[1.0, 0.0], [0.0, 10.0], [0.0, 100.0]])
+    assert np.array_equal(oracle.gemm(A, B), np.array([[1.0, 320.0]]))
+
+
+# ---------------------------------------------------------------- epilogue
+
+def test_epilogue_alpha_bias_closed_form():
+    X = np.array([[1.0, -2.0, 3.0], [0.5, 0.0, -4.0]])
+    bias = np.array([10.0, 20.0, 30.0])
+    out = oracle.epilogue(X, "scale_bias", 2.0, bias)
+    assert np.array_equal(out, 2.0 * X + bias[None, :])
+    assert np.array_equal(oracle.epilogue(X, "none", 1.0, None), X)
+
+
+def test_silu_against_scipy_and_limits():
+    from scipy.special import expit
+    xs = np.linspace(-30, 30, 1201)
+    ours = oracle.epilogue(xs.reshape(1, -1), "silu")[0]
+    ref = xs * expit(xs)
+    assert np.max(np.abs(ours - ref) / np.maximum(1e-300, np.abs(ref) + 1e-300)) < 1e-14
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12          # -> x for large x
+    assert abs(oracle.silu(-40.0)) < 1e-15                # -> 0 for very negative x
+    assert abs(oracle.silu(1e-8) / 1e-8 - 0.5) < 1e-8     # slope 1/2 at the origin
+    assert abs(oracle.silu(-1.0) - (-1.0 / (1.0 + math.e))) < 1e-16
+
+
+def test_swiglu_pairs_gate_with_up():
+    from scipy.special import expit
+    g = np.array([[1.0, -2.0]])
+    u = np.array([[3.0, 5.0]])
+    acc = np.concatenate([g, u], axis=1)             # gate | up
+    bias = np.array([0.5, 0.25, -1.0, 2.0])
+    out = oracle.epilogue(acc, "swiglu", 1.5, bias)
+    vg = 1.5 * g + bias[:2]
+    vu = 1.5 * u + bias[2:]
+    ref = vg * expit(vg) * vu
+    assert out.shape == (1, 2)
+    assert np.max(np.abs(out - ref)) < 1e-14
+
+
+# ----------------------------------------------------------------- Strassen
+
+@pytest.mark.parametrize("depth,shape", [(1, (2, 2, 2)), (1, (8, 6, 4)), (1, (34, 18, 50)),
+                                         (2, (4, 4, 4)), (2, (16, 24, 8)), (2, (36, 20, 44))])
+def test_strassen_equals_classical(depth, shape):
+    M, N, K = shape
+    rng = np.random.default_rng(M + 3 * N + 7 * K + depth)
+    A = rng.uniform(-1, 1, (M, K))
+    B = rng.uniform(-1, 1, (K, N))
+    ref = oracle.gemm(A, B)
+    S = oracle.strassen(A, B, depth)
+    assert np.linalg.norm(S - ref) <= 1e-12 * np.linalg.norm(ref)
+
+
+@pytest.mark.parametrize("depth", [1, 2])
+def test_strassen_exact_on_integers(depth):
+    rng = np.random.default_rng(11 + depth)
+    A = rng.integers(-3, 4, (16, 12)).astype(np.float64)
+    B = rng.integers(-3, 4, (12, 20)).astype(np.float64)
+    assert np.array_equal(oracle.strassen(A, B, depth), A @ B)
+
+
+def test_strassen_every_quadrant_depends_on_the_right_blocks():
+    # One nonzero block at a time: C = A B has a known block structure, so a
+    # wrong index or sign in any of the 7 products or 4 combinations shows.
+    n = 2
+    for ai in range(2):
+        for ak in range(2):
+            for bk in range(2):
+                for bj in range(2):
+                    A = np.zeros((2 * n, 2 * n))
+                    B = np.zeros((2 * n, 2 * n))
+                    A[ai * n:(ai + 1) * n, ak * n:(ak + 1) * n] = np.arange(1, n * n + 1).reshape(n, n)
+                    B[bk * n:(bk + 1) * n, bj * n:(bj + 1) * n] = np.arange(2, n * n + 2).reshape(n, n)
+                    assert np.array_equal(oracle.strassen(A, B, 1), A @ B)
+
+
+def test_strassen_rejects_indivisible():
+    with pytest.raises(ValueError):
+        oracle.strassen(np.ones((3, 4)), np.ones((4, 4)), 1)
+    with pytest.raises(ValueError):
+        oracle.strassen(np.ones((6, 4)), np.ones((4, 4)), 2)
+
+
+@pytest.mark.parametrize("depth", [1, 2])
+def test_emulated_without_rounding_is_exact_strassen(depth):
+    rng = np.random.default_rng(5)
+    A = rng.uniform(-1, 1, (16, 8))
+    B = rng.uniform(-1, 1, (8, 12))
+    assert np.array_equal(oracle.strassen_emulated(A, B, depth, "f64"), oracle.strassen(A, B, depth))
+
+
+@pytest.mark.parametrize("depth", [1, 2])
+def test_emulated_on_ternary_inputs_is_exact(depth):
+    # operand sums of {-1,0,1} values are small integers, exact in any 16-bit type
+    rng = np.random.default_rng(6)
+    A = rng.integers(-1, 2, (32, 16)).astype(np.float64)
+    B = rng.integers(-1, 2, (16, 24)).astype(np.float64)
+    assert np.array_equal(oracle.strassen_emulated(A, B, depth, "bf16"), A @ B)
+
+
+@pytest.mark.parametrize("dtype,depth,lo,hi", [("bf16", 1, 3e-4, 5e-3), ("bf16", 2, 6e-4, 1e-2),
+                                               ("f16", 1, 4e-5, 1e-3)])
+def test_emulated_rounding_error_is_in_the_expected_band(dtype, depth, lo, hi):
+    rng = np.random.default_rng(9)
+    n = 128
+    A = oracle.round_to(rng.uniform(-1, 1, (n, n)), dtype)
+    B = oracle.round_to(rng.uniform(-1, 1, (n, n)), dtype)
+    ref = oracle.gemm(A, B)
+    E = oracle.strassen_emulated(A, B, depth, dtype)
+    rel = np.linalg.norm(E - ref) / np.linalg.norm(ref)
+    assert lo < rel < hi, rel
+
+
+# ------------------------------------------------------------ sampled path
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_sampled_equals_full_bitwise(dtype):
+    A = inputs.matrix(40, 70, "uniform", dtype, 0)
+    B = inputs.matrix(70, 30, "uniform", dtype, 1)
+    Ab, Bb = inputs.bits(A), inputs.bits(B)
+    full = oracle.gemm(oracle.decode(Ab, dtype), oracle.decode(Bb, dtype))
+    rows, cols = inputs.sample_positions(40, 30, n=64, tile_m=16, tile_n=8)
+    rows, cols = rows.numpy(), cols.numpy()
+    s = oracle.gemm_sampled(Ab, Bb, dtype, rows, cols)
+    assert np.array_equal(s, full[rows, cols])
+
+
+@pytest.mark.parametrize("kind", ["scale_bias", "silu", "swiglu"])
+def test_reference_sampled_equals_full_reference(kind):
+    A = inputs.matrix(24, 48, "normal", "bf16", 0)
+    B = inputs.matrix(48, 32, "normal_inv_k", "bf16", 1, k=48)
+    bias = inputs.matrix(1, 32, "normal_0.02", "bf16", 2)[0]
+    Ab, Bb, bb = inputs.bits(A), inputs.bits(B), inputs.bits(bias)
+    full = oracle.reference(Ab, Bb, "bf16", kind, 0.75, bb)
+    Nout = full.shape[1]
+    rows, cols = inputs.sample_positions(24, Nout, n=40, tile_m=8, tile_n=8)
+    rows, cols = rows.numpy(), cols.numpy()
+    s = oracle.reference_sampled(Ab, Bb, "bf16", rows, cols, kind, 0.75, bb)
+    assert np.array_equal(s, full[rows, cols])
+
+
+def test_inputs_are_seeded_and_shaped():
+    a1 = inputs.matrix(8, 8, "uniform", "bf16", 0)
+    a2 = inputs.matrix(8, 8, "uniform", "bf16", 0)
+    a3 = inputs.matrix(8, 8, "uniform", "bf16", 1)
+    assert torch.equal(a1, a2) and not torch.equal(a1, a3)
+    assert a1.dtype == torch.bfloat16 and a1.abs().max() <= 1
+    t = inputs.matrix(64, 64, "ternary", "f16", 0)
+    assert set(torch.unique(t).tolist()) <= {-1.0, 0.0, 1.0}
