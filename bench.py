@@ -1,0 +1,426 @@
+"""Benchmark of fgemm on the proj_4096_bf16_bias workload (and others).
+
+Default run (N = 1): C = A @ B + bias, M = N = K = 4096, bf16, A ~ N(0,1),
+B ~ N(0,1/K), bias ~ N(0, 0.02^2), algorithm picked by the decision model,
+through the public binding (fgemm.matmul -> fgemm_matmul_ex).  Prints ONE
+JSON line.  Four rotating input/output sets (384 MB, more than the L2) are
+cycled so that every timed step streams its operands from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fgemm|reference]
+                    [--workload NAME] [--algo auto|classical|strassen1|strassen2]
+                    [--tile 0|64|128|256]
+
+--impl reference times the fp64 CPU oracle on host cores (a bounded sample
+of the same workload per step): the comparison arm; there is no installable
+reference implementation of this method.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on
+its own GPU (the product has no exchange step); value = total FLOPs of all
+ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "effective TFLOP/s (2*M*N*K/t) bf16 GEMM"
+UNIT = "TFLOP/s"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="fgemm", choices=["fgemm", "reference"])
+    ap.add_argument("--workload", default="proj_4096_bf16_bias")
+    ap.add_argument("--algo", default="auto")
+    ap.add_argument("--tile", type=int, default=0)
+    ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0 = auto)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------- distributed
+
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local % max(1, torch.cuda.device_count()))
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------- workload
+
+def workload_shape(name):
+    from complexity_matmul_tcgen05_gb300 import inputs
+    if name in inputs.WORKLOADS:
+        w = inputs.WORKLOADS[name]
+        return w["M"], w["N"], w["K"], w["dtype"], w["epi"]
+    m = re.fullmatch(r"sweep_(\d+)x(\d+)x(\d+)", name)
+    if m:
+        M, N, K = map(int, m.groups())
+        return M, N, K, "bf16", "none"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def make_inputs(name, device):
+    from complexity_matmul_tcgen05_gb300 import inputs
+    if name in inputs.WORKLOADS:
+        return inputs.workload_inputs(name, device)
+    M, N, K, _, _ = workload_shape(name)
+    A, B = inputs.sweep_inputs(M, N, K, device)
+    return A, B, None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------- peaks / ncu
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "complexity_matmul_tcgen05_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(workload, algo, tile):
+    """DRAM bytes per launch recorded under profiles/ for this workload, if
+    the counters were taken on the current kernel sources."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    want = kernel_source_hash()
+    pat = re.compile(r"traffic_bytes_per_launch\s*:\s*(\d+)\s+workload=(\S+)\s+algo=(\S+)\s+"
+                     r"tile=(\d+)\s+sources=(\w+)")
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, f)) as fh:
+            for line in fh:
+                m = pat.search(line)
+                if m and m.group(2) == workload and m.group(3) == algo and \
+                        int(m.group(4)) == tile and m.group(5) == want:
+                    return int(m.group(1))
+    return None
+
+
+# ----------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(name, target_s=10.0, device_inputs=None):
+    """Times the fp64 oracle on a bounded sample of the workload's output
+    entries (each a K-long dot product of decoded 16-bit inputs).  Returns
+    (TFLOP/s, seconds, entries, threads)."""
+    import numpy as np
+    import oracle
+    from complexity_matmul_tcgen05_gb300 import inputs
+    M, N, K, dtype, epi = workload_shape(name)
+    if device_inputs is None:
+        A, B, bias = make_inputs(name, "cpu")
+    else:
+        A, B, bias = (None if t is None else t.cpu() for t in device_inputs)
+    Ab, Bb = inputs.bits(A), inputs.bits(B)
+    bb = None if bias is None else inputs.bits(bias)
+    n_out = N // 2 if epi == "swiglu" else N
+    per_entry = 2.0 * K * (2 if epi == "swiglu" else 1)
+    n = 256
+    elapsed = 0.0
+    while True:
+        rows, cols = inputs.sample_positions(M, n_out, n=n)
+        t0 = time.perf_counter()
+        oracle.reference_sampled(Ab, Bb, dtype, rows.numpy(), cols.numpy(), epi, 1.0, bb)
+        elapsed = time.perf_counter() - t0
+        if elapsed >= target_s or n >= (1 << 26):
+            break
+        grow = max(2.0, min(16.0, target_s / max(elapsed, 1e-3)))
+        n = int(n * grow)
+    entries = rows.numel()
+    return per_entry * entries / elapsed / 1e12, elapsed, entries, oracle.num_threads()
+
+
+# --------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    """The comparison arm: the fp64 CPU oracle, as it stands, on host cores."""
+    if rank != 0:
+        return
+    M, N, K, dtype, epi = workload_shape(args.workload)
+    per_step = 3.0
+    for _ in range(max(0, args.warmup)):
+        cpu_oracle_sample(args.workload, target_s=0.2)
+    vals, secs, ents = [], 0.0, 0
+    for _ in range(args.steps):
+        v, s, e, thr = cpu_oracle_sample(args.workload, target_s=per_step)
+        vals.append(v)
+        secs += s
+        ents += e
+    value = 2.0 * K * (2 if epi == "swiglu" else 1) * ents / secs / 1e12
+    sample = (f"{ents} sampled output entries over {args.steps} steps, each a K={K} fp64 dot "
+              f"product of decoded {dtype} inputs (stratified, seed 3)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "epilogue": epi},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_fgemm(args, rank, world):
+    from complexity_matmul_tcgen05_gb300 import fgemm
+    M, N, K, dtype, epi = workload_shape(args.workload)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    A0, B0, bias0 = make_inputs(args.workload, dev)
+    n_out = N // 2 if epi == "swiglu" else N
+    set_bytes = 2 * (M * K + K * N + M * n_out)
+    l2 = 126 * 2 ** 20
+    sets = args.sets if args.sets > 0 else max(1, min(8, math.ceil(3 * l2 / set_bytes)))
+    As, Bs, Cs, biases = [A0], [B0], [], [bias0]
+    for i in range(1, sets):   # distinct copies so each step misses the L2
+        As.append(A0.clone())
+        Bs.append(B0.clone())
+        biases.append(None if bias0 is None else bias0.clone())
+    for i in range(sets):
+        Cs.append(torch.empty((M, n_out), dtype=A0.dtype, device=dev))
+    handle = fgemm.default_handle()
+    stream = torch.cuda.current_stream(dev)
+    algo, tile = args.algo, args.tile
+    if algo == "auto":
+        plan_algo, plan_tile, pred_us = handle.plan(M, N, K, fgemm._dtype_code(A0.dtype),
+                                                    fgemm.make_epilogue(epi))
+    else:
+        plan_algo, plan_tile, pred_us = algo, tile, None
+
+    def step(i):
+        fgemm.matmul(As[i % sets], Bs[i % sets], out=Cs[i % sets], epilogue=epi,
+                     bias=biases[i % sets], algo=algo, tile_n=tile, handle=handle)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    if handle.get_error() != fgemm.OK:
+        raise SystemExit(f"device error during warm-up: {handle.last_message()}")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if args.steps * 1.0 < 1e9:
+            time.sleep(0.25)  # at least one clock sample after the last step
+    barrier(world)
+    status = handle.get_error()
+    if status != fgemm.OK:
+        raise SystemExit(f"device error in the timed region: {handle.last_message()}")
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_avg_ms = statistics.mean(kern_ms)
+    flops = 2.0 * M * N * K
+    value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end: pinned host buffers -> device -> kernel -> host, every step
+    e2e = None
+    if not args.no_e2e:
+        hA = A0.cpu().pin_memory()
+        hB = B0.cpu().pin_memory()
+        hbias = None if bias0 is None else bias0.cpu().pin_memory()
+        hC = torch.empty((M, n_out), dtype=A0.dtype).pin_memory()
+        dA, dB = torch.empty_like(A0), torch.empty_like(B0)
+        dbias = None if bias0 is None else torch.empty_like(bias0)
+        dC = torch.empty((M, n_out), dtype=A0.dtype, device=dev)
+
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            if dbias is not None:
+                dbias.copy_(hbias, non_blocking=True)
+            fgemm.matmul(dA, dB, out=dC, epilogue=epi, bias=dbias, algo=algo, tile_n=tile,
+                         handle=handle)
+            hC.copy_(dC, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, min(args.steps, 20))
+        barrier(world)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        h2d = hA.numel() * 2 + hB.numel() * 2 + (0 if hbias is None else hbias.numel() * 2)
+        e2e = {"value": flops * world * n_e2e / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hC.numel() * 2}
+
+    if rank != 0:
+        return
+    burst, sustained, hbm, src = measured_peaks()
+    achieved = flops / (kern_avg_ms * 1e-3) / 1e12
+    executed = achieved * (7.0 / 8.0) ** {"classical": 0, "strassen1": 1, "strassen2": 2}[plan_algo]
+    roof = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": UNIT,
+            "frac": achieved / burst if burst else None,
+            "traffic": ncu_traffic(args.workload, plan_algo, plan_tile),
+            "peak_source": f"{src} bf16 dense (burst)", "executed_tflops": executed,
+            "kernel_ms": kern_avg_ms}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dtype == "bf16" else "f16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "epilogue": epi,
+                   "algo": plan_algo, "tile_m": 128, "tile_n": plan_tile,
+                   "predicted_us": pred_us, "l2": f"{sets} rotating input/output sets "
+                   f"({sets * set_bytes / 2 ** 20:.0f} MiB) cycled between steps",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline and world == 1:
+        v, s, e, thr = cpu_oracle_sample(args.workload, target_s=10.0,
+                                         device_inputs=(A0, B0, bias0))
+        line["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"{e} stratified output entries (seed 3) of the same workload, each a "
+                      f"K={K} fp64 dot product of decoded inputs, {s:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py --impl fgemm needs a CUDA device")
+        run_fgemm(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,787 @@
+// fgemm_api.cpp -- the C ABI (include/fgemm.h): handles, argument checks,
+// plan cache, tensor-map encoding, Strassen coefficient tables, launches and
+// calibration.  Host code only; kernels live in the fgemm_kern_*.cu files.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/fgemm.h"
+#include "fgemm_internal.h"
+
+namespace fgemm {
+bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo_t algo,
+                   int32_t tile_n);
+}
+
+using fgemm::KernelParams;
+using fgemm::StrassenTable;
+
+namespace {
+
+thread_local std::string g_thread_msg;
+
+// ------------------------------------------------------------------ helpers
+
+int depth_of(fgemm_algo_t a) {
+  return a == FGEMM_ALGO_STRASSEN1 ? 1 : (a == FGEMM_ALGO_STRASSEN2 ? 2 : 0);
+}
+
+fgemm_status_t fail(std::string* msg, fgemm_status_t s, const std::string& text) {
+  if (msg) *msg = text;
+  return s;
+}
+
+// One-level Strassen scheme (textbook form): for product k, the A blocks and
+// signs summed into its left operand, the B blocks into its right operand,
+// and the output blocks it is added into.  Block (r, c) of a 2 x 2 split.
+struct Term1 {
+  int r, c, sign;
+};
+struct Product1 {
+  int na;
+  Term1 a[2];
+  int nb;
+  Term1 b[2];
+  int nc;
+  Term1 c[2];
+};
+const Product1 kStrassen1[7] = {
+    // M1 = (A11 + A22)(B11 + B22) -> C11 +, C22 +
+    {2, {{0, 0, 1}, {1, 1, 1}}, 2, {{0, 0, 1}, {1, 1, 1}}, 2, {{0, 0, 1}, {1, 1, 1}}},
+    // M2 = (A21 + A22) B11 -> C21 +, C22 -
+    {2, {{1, 0, 1}, {1, 1, 1}}, 1, {{0, 0, 1}, {0, 0, 0}}, 2, {{1, 0, 1}, {1, 1, -1}}},
+    // M3 = A11 (B12 - B22) -> C12 +, C22 +
+    {1, {{0, 0, 1}, {0, 0, 0}}, 2, {{0, 1, 1}, {1, 1, -1}}, 2, {{0, 1, 1}, {1, 1, 1}}},
+    // M4 = A22 (B21 - B11) -> C11 +, C21 +
+    {1, {{1, 1, 1}, {0, 0, 0}}, 2, {{1, 0, 1}, {0, 0, -1}}, 2, {{0, 0, 1}, {1, 0, 1}}},
+    // M5 = (A11 + A12) B22 -> C11 -, C12 +
+    {2, {{0, 0, 1}, {0, 1, 1}}, 1, {{1, 1, 1}, {0, 0, 0}}, 2, {{0, 0, -1}, {0, 1, 1}}},
+    // M6 = (A21 - A11)(B11 + B12) -> C22 +
+    {2, {{1, 0, 1}, {0, 0, -1}}, 2, {{0, 0, 1}, {0, 1, 1}}, 1, {{1, 1, 1}, {0, 0, 0}}},
+    // M7 = (A12 - A22)(B21 + B22) -> C11 +
+    {2, {{0, 1, 1}, {1, 1, -1}}, 2, {{1, 0, 1}, {1, 1, 1}}, 1, {{0, 0, 1}, {0, 0, 0}}},
+};
+
+uint8_t term_code(int r, int c, int sign, int depth) {
+  const int idx = (r << depth) | c;
+  return static_cast<uint8_t>(idx | (sign < 0 ? fgemm::kTermNeg : 0));
+}
+
+// Table for `depth` levels: the depth-2 scheme applies the one-level scheme
+// to each of the seven products' half-size operands (outer product p, inner
+// product q), so block indices and signs multiply.
+StrassenTable build_table(int depth) {
+  StrassenTable t;
+  std::memset(&t, 0, sizeof(t));
+  if (depth == 0) {
+    t.na[0] = t.nb[0] = t.nc[0] = 1;
+    t.a[0][0] = t.b[0][0] = 0;
+    t.c[0][0] = fgemm::kTermFirst;
+    return t;
+  }
+  int np = 0;
+  if (depth == 1) {
+    for (int p = 0; p < 7; ++p, ++np) {
+      const Product1& P = kStrassen1[p];
+      t.na[np] = static_cast<uint8_t>(P.na);
+      t.nb[np] = static_cast<uint8_t>(P.nb);
+      t.nc[np] = static_cast<uint8_t>(P.nc);
+      for (int i = 0; i < P.na; ++i) t.a[np][i] = term_code(P.a[i].r, P.a[i].c, P.a[i].sign, 1);
+      for (int i = 0; i < P.nb; ++i) t.b[np][i] = term_code(P.b[i].r, P.b[i].c, P.b[i].sign, 1);
+      for (int i = 0; i < P.nc; ++i) t.c[np][i] = term_code(P.c[i].r, P.c[i].c, P.c[i].sign, 1);
+    }
+  } else {
+    for (int p = 0; p < 7; ++p) {
+      for (int q = 0; q < 7; ++q, ++np) {
+        const Product1& O = kStrassen1[p];
+        const Product1& I = kStrassen1[q];
+        int n = 0;
+        for (int i = 0; i < O.na; ++i)
+          for (int j = 0; j < I.na; ++j)
+            t.a[np][n++] = term_code(O.a[i].r * 2 + I.a[j].r, O.a[i].c * 2 + I.a[j].c,
+                                     O.a[i].sign * I.a[j].sign, 2);
+        t.na[np] = static_cast<uint8_t>(n);
+        n = 0;
+        for (int i = 0; i < O.nb; ++i)
+          for (int j = 0; j < I.nb; ++j)
+            t.b[np][n++] = term_code(O.b[i].r * 2 + I.b[j].r, O.b[i].c * 2 + I.b[j].c,
+                                     O.b[i].sign * I.b[j].sign, 2);
+        t.nb[np] = static_cast<uint8_t>(n);
+        n = 0;
+        for (int i = 0; i < O.nc; ++i)
+          for (int j = 0; j < I.nc; ++j)
+            t.c[np][n++] = term_code(O.c[i].r * 2 + I.c[j].r, O.c[i].c * 2 + I.c[j].c,
+                                     O.c[i].sign * I.c[j].sign, 2);
+        t.nc[np] = static_cast<uint8_t>(n);
+      }
+    }
+  }
+  // Mark the first contribution to each output block (it stores instead of
+  // adding), in product order.
+  bool seen[16] = {false};
+  for (int p = 0; p < np; ++p) {
+    for (int i = 0; i < t.nc[p]; ++i) {
+      const int idx = t.c[p][i] & fgemm::kTermIndexMask;
+      if (!seen[idx]) {
+        seen[idx] = true;
+        t.c[p][i] |= fgemm::kTermFirst;
+      }
+    }
+  }
+  return t;
+}
+
+const StrassenTable& table_for(int depth) {
+  static const StrassenTable t0 = build_table(0);
+  static const StrassenTable t1 = build_table(1);
+  static const StrassenTable t2 = build_table(2);
+  return depth == 0 ? t0 : (depth == 1 ? t1 : t2);
+}
+
+// ------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct TmapKey {
+  const void* ptr;
+  uint64_t inner, outer, ld;
+  uint32_t box_outer;
+  int bf16;
+  bool operator==(const TmapKey& o) const {
+    return ptr == o.ptr && inner == o.inner && outer == o.outer && ld == o.ld &&
+           box_outer == o.box_outer && bf16 == o.bf16;
+  }
+};
+struct TmapKeyHash {
+  size_t operator()(const TmapKey& k) const {
+    size_t h = std::hash<const void*>()(k.ptr);
+    h ^= std::hash<uint64_t>()(k.inner * 1000003u + k.outer) + 0x9e3779b97f4a7c15ull + (h << 6);
+    h ^= std::hash<uint64_t>()(k.ld * 31u + k.box_outer * 7u + k.bf16) + (h << 6) + (h >> 2);
+    return h;
+  }
+};
+
+struct PlanKey {
+  int64_t M, N, K;
+  int32_t epi, algo, tile;
+  bool operator==(const PlanKey& o) const {
+    return M == o.M && N == o.N && K == o.K && epi == o.epi && algo == o.algo && tile == o.tile;
+  }
+};
+struct PlanKeyHash {
+  size_t operator()(const PlanKey& k) const {
+    size_t h = std::hash<int64_t>()(k.M);
+    h = h * 1000003u ^ std::hash<int64_t>()(k.N);
+    h = h * 1000003u ^ std::hash<int64_t>()(k.K);
+    h = h * 1000003u ^ static_cast<size_t>(k.epi * 64 + k.algo * 8 + (k.tile >> 6));
+    return h;
+  }
+};
+struct Plan {
+  fgemm_algo_t algo;
+  int32_t tile_n;
+  double predicted_us;
+};
+
+}  // namespace
+
+struct fgemm_handle_s {
+  int device = 0;
+  int num_sms = 0;
+  cudaStream_t stream = nullptr;
+  unsigned int* d_err = nullptr;
+  float* workspace = nullptr;
+  size_t ws_bytes = 0;
+  unsigned long long spin_ns = 1000000000ull;
+  fgemm_device_model_t model{};
+  std::unordered_map<PlanKey, Plan, PlanKeyHash> plans;
+  std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> tmaps;
+  std::string msg;
+};
+
+namespace {
+
+fgemm_status_t set_msg(fgemm_handle_t h, fgemm_status_t s, const std::string& text) {
+  if (h)
+    h->msg = text;
+  else
+    g_thread_msg = text;
+  return s;
+}
+
+fgemm_status_t cuda_fail(fgemm_handle_t h, cudaError_t e, const char* what) {
+  std::string t = std::string(what) + ": " + cudaGetErrorString(e);
+  return set_msg(h, FGEMM_ERR_CUDA, t);
+}
+
+fgemm_status_t encode_tmap(fgemm_handle_t h, CUtensorMap* out, const void* ptr, uint64_t inner,
+                           uint64_t outer, uint64_t ld, uint32_t box_outer, int bf16) {
+  TmapKey key{ptr, inner, outer, ld, box_outer, bf16};
+  auto it = h->tmaps.find(key);
+  if (it != h->tmaps.end()) {
+    *out = it->second;
+    return FGEMM_OK;
+  }
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc) return set_msg(h, FGEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {64, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_msg(h, FGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(r) + ")");
+  if (h->tmaps.size() > 256) h->tmaps.clear();
+  h->tmaps.emplace(key, m);
+  *out = m;
+  return FGEMM_OK;
+}
+
+// The checks fgemm_matmul_ex makes before launching (see fgemm.h).
+fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                        int64_t ldb, const void* C, int64_t ldc, fgemm_dtype_t dtype,
+                        const fgemm_epilogue_t* epi, fgemm_algo_t algo, int32_t tile_n,
+                        std::string* msg) {
+  const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
+  if (dtype != FGEMM_F16 && dtype != FGEMM_BF16)
+    return fail(msg, FGEMM_ERR_INVALID_ARG, "dtype must be FGEMM_F16 or FGEMM_BF16");
+  if (kind < FGEMM_EPI_NONE || kind > FGEMM_EPI_SWIGLU)
+    return fail(msg, FGEMM_ERR_INVALID_ARG, "unknown epilogue kind");
+  if (algo < FGEMM_ALGO_AUTO || algo > FGEMM_ALGO_STRASSEN2)
+    return fail(msg, FGEMM_ERR_INVALID_ARG, "unknown algorithm");
+  if (tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 256)
+    return fail(msg, FGEMM_ERR_INVALID_ARG, "tile_n must be 0, 64, 128 or 256");
+  if (M < 0 || N < 0 || K < 0) return fail(msg, FGEMM_ERR_INVALID_ARG, "negative dimension");
+  const int64_t kMax = (int64_t{1} << 31) - 1;
+  if (M > kMax || N > kMax || K > kMax)
+    return fail(msg, FGEMM_ERR_INVALID_ARG, "dimension above 2^31 - 1");
+  if (kind == FGEMM_EPI_SWIGLU && (N % 2) != 0)
+    return fail(msg, FGEMM_ERR_INVALID_ARG, "SWIGLU needs an even N (gate | up)");
+  const int64_t n_out = kind == FGEMM_EPI_SWIGLU ? N / 2 : N;
+  if (kind == FGEMM_EPI_SCALE_BIAS && (!epi || !epi->bias))
+    return fail(msg, FGEMM_ERR_INVALID_ARG, "SCALE_BIAS needs a bias vector");
+  if (epi && epi->bias && (reinterpret_cast<uintptr_t>(epi->bias) & 1u))
+    return fail(msg, FGEMM_ERR_ALIGNMENT, "bias must be 2-byte aligned");
+  if (M == 0 || n_out == 0) return FGEMM_OK;  // nothing to compute
+  if (!C) return fail(msg, FGEMM_ERR_INVALID_ARG, "C is NULL");
+  if (ldc < n_out) return fail(msg, FGEMM_ERR_INVALID_ARG, "ldc < output width");
+  if ((reinterpret_cast<uintptr_t>(C) & 15u) || (ldc % 8) != 0)
+    return fail(msg, FGEMM_ERR_ALIGNMENT, "C must be 16-byte aligned with ldc a multiple of 8");
+  if (K == 0) return FGEMM_OK;  // C = epi(bias), A and B unused
+  if (!A || !B) return fail(msg, FGEMM_ERR_INVALID_ARG, "A or B is NULL");
+  if (lda < K) return fail(msg, FGEMM_ERR_INVALID_ARG, "lda < K");
+  if (ldb < N) return fail(msg, FGEMM_ERR_INVALID_ARG, "ldb < N");
+  if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u))
+    return fail(msg, FGEMM_ERR_ALIGNMENT, "A and B must be 16-byte aligned");
+  if ((lda % 8) != 0 || (ldb % 8) != 0)
+    return fail(msg, FGEMM_ERR_ALIGNMENT, "lda and ldb must be multiples of 8 elements");
+  if (kind == FGEMM_EPI_SWIGLU && (N % 16) != 0)
+    return fail(msg, FGEMM_ERR_ALIGNMENT, "SWIGLU needs N a multiple of 16 (up half 16-byte aligned)");
+  if (algo != FGEMM_ALGO_AUTO) {
+    const int32_t t = tile_n;
+    if (t != 0) {
+      if (!fgemm::form_is_legal(M, N, K, kind, algo, t))
+        return fail(msg, FGEMM_ERR_UNSUPPORTED, "forced form/tile is not legal for this shape");
+    } else {
+      bool any = false;
+      for (int32_t c : {64, 128, 256}) any = any || fgemm::form_is_legal(M, N, K, kind, algo, c);
+      if (!any)
+        return fail(msg, FGEMM_ERR_UNSUPPORTED,
+                    "Strassen form needs M, N, K divisible into 2^d blocks of whole tiles");
+    }
+  }
+  return FGEMM_OK;
+}
+
+fgemm_status_t choose_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, int32_t kind,
+                           fgemm_algo_t algo, int32_t tile_n, Plan* out) {
+  PlanKey key{M, N, K, kind, static_cast<int32_t>(algo), tile_n};
+  auto it = h->plans.find(key);
+  if (it != h->plans.end()) {
+    *out = it->second;
+    return FGEMM_OK;
+  }
+  Plan p{algo, tile_n, 0.0};
+  if (algo == FGEMM_ALGO_AUTO) {
+    int32_t tm = 0, tn = 0;
+    fgemm_status_t s = fgemm_model_plan(&h->model, M, N, K, kind, &p.algo, &tm, &tn, &p.predicted_us);
+    if (s != FGEMM_OK) return set_msg(h, s, "decision model found no legal form");
+    p.tile_n = tn;
+  } else if (tile_n == 0) {
+    double best = INFINITY;
+    for (int32_t c : {64, 128, 256}) {
+      double us;
+      if (fgemm_model_predict(&h->model, M, N, K, kind, algo, c, &us) == FGEMM_OK && us < best) {
+        best = us;
+        p.tile_n = c;
+      }
+    }
+    if (p.tile_n == 0) return set_msg(h, FGEMM_ERR_UNSUPPORTED, "no legal tile for this form");
+    p.predicted_us = best;
+  } else {
+    fgemm_model_predict(&h->model, M, N, K, kind, algo, tile_n, &p.predicted_us);
+  }
+  if (h->plans.size() > 4096) h->plans.clear();
+  h->plans.emplace(key, p);
+  *out = p;
+  return FGEMM_OK;
+}
+
+fgemm_status_t ensure_workspace(fgemm_handle_t h, size_t bytes) {
+  if (bytes <= h->ws_bytes) return FGEMM_OK;
+  if (h->workspace) {
+    cudaError_t e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+    cudaFree(h->workspace);
+    h->workspace = nullptr;
+    h->ws_bytes = 0;
+  }
+  cudaError_t e = cudaMalloc(&h->workspace, bytes);
+  if (e != cudaSuccess) {
+    h->workspace = nullptr;
+    return cuda_fail(h, e, "cudaMalloc(Strassen workspace)");
+  }
+  h->ws_bytes = bytes;
+  return FGEMM_OK;
+}
+
+double getenv_double(const char* name, double dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  char* end = nullptr;
+  double d = std::strtod(v, &end);
+  return (end && end != v) ? d : dflt;
+}
+
+// ------------------------------------------------- calibration JSON I/O
+
+bool json_number(const std::string& text, const char* key, double* out) {
+  const std::string pat = std::string("\"") + key + "\"";
+  size_t p = text.find(pat);
+  if (p == std::string::npos) return false;
+  p = text.find(':', p + pat.size());
+  if (p == std::string::npos) return false;
+  const char* s = text.c_str() + p + 1;
+  char* end = nullptr;
+  double d = std::strtod(s, &end);
+  if (end == s) return false;
+  *out = d;
+  return true;
+}
+
+fgemm_status_t load_calibration(fgemm_handle_t h, const char* path) {
+  FILE* f = std::fopen(path, "rb");
+  if (!f) return set_msg(h, FGEMM_ERR_CALIBRATION, std::string("cannot open ") + path);
+  std::string text;
+  char buf[4096];
+  size_t n;
+  while ((n = std::fread(buf, 1, sizeof(buf), f)) > 0) text.append(buf, n);
+  std::fclose(f);
+  fgemm_device_model_t m = h->model;
+  struct {
+    const char* key;
+    double* dst;
+  } fields[] = {
+      {"peak_tflops", &m.peak_tflops},         {"hbm_gbs", &m.hbm_gbs},
+      {"eff_classical_64", &m.eff_classical[0]}, {"eff_classical_128", &m.eff_classical[1]},
+      {"eff_classical_256", &m.eff_classical[2]}, {"eff_strassen1_128", &m.eff_strassen[0][0]},
+      {"eff_strassen1_256", &m.eff_strassen[0][1]}, {"eff_strassen2_128", &m.eff_strassen[1][0]},
+      {"eff_strassen2_256", &m.eff_strassen[1][1]}, {"launch_us", &m.launch_us},
+      {"tile_fill_us", &m.tile_fill_us},        {"l2_bytes", &m.l2_bytes},
+      {"l2_gbs", &m.l2_gbs},
+  };
+  int found = 0;
+  for (auto& fd : fields) found += json_number(text, fd.key, fd.dst) ? 1 : 0;
+  if (found == 0) return set_msg(h, FGEMM_ERR_CALIBRATION, std::string("no model fields in ") + path);
+  if (!(m.peak_tflops > 0) || !(m.hbm_gbs > 0))
+    return set_msg(h, FGEMM_ERR_CALIBRATION, "calibration has a non-positive peak or bandwidth");
+  h->model = m;
+  h->plans.clear();
+  return FGEMM_OK;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+
+extern "C" {
+
+const char* fgemm_status_string(fgemm_status_t s) {
+  switch (s) {
+    case FGEMM_OK: return "FGEMM_OK";
+    case FGEMM_ERR_INVALID_ARG: return "FGEMM_ERR_INVALID_ARG";
+    case FGEMM_ERR_ALIGNMENT: return "FGEMM_ERR_ALIGNMENT";
+    case FGEMM_ERR_UNSUPPORTED: return "FGEMM_ERR_UNSUPPORTED";
+    case FGEMM_ERR_CUDA: return "FGEMM_ERR_CUDA";
+    case FGEMM_ERR_TIMEOUT: return "FGEMM_ERR_TIMEOUT";
+    case FGEMM_ERR_NO_DEVICE: return "FGEMM_ERR_NO_DEVICE";
+    case FGEMM_ERR_CALIBRATION: return "FGEMM_ERR_CALIBRATION";
+  }
+  return "FGEMM_ERR_UNKNOWN";
+}
+
+const char* fgemm_last_message(fgemm_handle_t h) {
+  return h ? h->msg.c_str() : g_thread_msg.c_str();
+}
+
+fgemm_status_t fgemm_validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                              const void* B, int64_t ldb, const void* C, int64_t ldc,
+                              fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                              int32_t tile_n) {
+  std::string msg;
+  fgemm_status_t s = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_n, &msg);
+  g_thread_msg = msg;
+  return s;
+}
+
+fgemm_status_t fgemm_create(fgemm_handle_t* out) {
+  if (!out) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int dev = 0, count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+    cudaGetLastError();
+    return set_msg(nullptr, FGEMM_ERR_NO_DEVICE, "no CUDA device");
+  }
+  if (cudaGetDevice(&dev) != cudaSuccess) return set_msg(nullptr, FGEMM_ERR_NO_DEVICE, "cudaGetDevice failed");
+  int major = 0, minor = 0, sms = 0, l2 = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  if (major != 10 || minor != 3)
+    return set_msg(nullptr, FGEMM_ERR_NO_DEVICE,
+                   "device is sm_" + std::to_string(major) + std::to_string(minor) +
+                       "; this library is built for sm_103a only");
+  fgemm_handle_t h = new fgemm_handle_s();
+  h->device = dev;
+  h->num_sms = sms;
+  fgemm_model_default(&h->model, sms, getenv_double("FGEMM_PEAK_TFLOPS", 2250.0 * sms / 152.0),
+                      getenv_double("FGEMM_HBM_GBS", 7900.0));
+  if (l2 > 0) h->model.l2_bytes = l2;
+  const double spin_ms = getenv_double("FGEMM_SPIN_LIMIT_MS", 1000.0);
+  h->spin_ns = static_cast<unsigned long long>(std::max(1.0, spin_ms) * 1e6);
+  cudaError_t e = cudaMalloc(&h->d_err, sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(unsigned int));
+  if (e != cudaSuccess) {
+    fgemm_status_t s = cuda_fail(nullptr, e, "cudaMalloc(error word)");
+    if (h->d_err) cudaFree(h->d_err);
+    delete h;
+    return s;
+  }
+  if (const char* calib = std::getenv("FGEMM_CALIB")) {
+    if (*calib) {
+      fgemm_status_t s = load_calibration(h, calib);
+      if (s != FGEMM_OK) {
+        g_thread_msg = h->msg;
+        cudaFree(h->d_err);
+        delete h;
+        return s;
+      }
+    }
+  }
+  *out = h;
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_destroy(fgemm_handle_t h) {
+  if (!h) return FGEMM_OK;
+  cudaStreamSynchronize(h->stream);
+  if (h->workspace) cudaFree(h->workspace);
+  if (h->d_err) cudaFree(h->d_err);
+  delete h;
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_set_stream(fgemm_handle_t h, void* cuda_stream) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  h->stream = static_cast<cudaStream_t>(cuda_stream);
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_get_device_model(fgemm_handle_t h, fgemm_device_model_t* out) {
+  if (!h || !out) return set_msg(h, FGEMM_ERR_INVALID_ARG, "NULL argument");
+  *out = h->model;
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_set_device_model(fgemm_handle_t h, const fgemm_device_model_t* model) {
+  if (!h || !model) return set_msg(h, FGEMM_ERR_INVALID_ARG, "NULL argument");
+  if (model->num_sms <= 0 || !(model->peak_tflops > 0) || !(model->hbm_gbs > 0))
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "model needs positive SM count, peak and bandwidth");
+  h->model = *model;
+  h->plans.clear();
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, fgemm_dtype_t dtype,
+                          const fgemm_epilogue_t* epi, fgemm_algo_t* algo_out, int32_t* tile_m,
+                          int32_t* tile_n, double* predicted_us) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  if (dtype != FGEMM_F16 && dtype != FGEMM_BF16)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "dtype must be FGEMM_F16 or FGEMM_BF16");
+  const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
+  Plan p;
+  fgemm_status_t s = choose_plan(h, M, N, K, kind, FGEMM_ALGO_AUTO, 0, &p);
+  if (s != FGEMM_OK) return s;
+  if (algo_out) *algo_out = p.algo;
+  if (tile_m) *tile_m = fgemm::kBM;
+  if (tile_n) *tile_n = p.tile_n;
+  if (predicted_us) *predicted_us = p.predicted_us;
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                               int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                               fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                               int32_t tile_n) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  fgemm_status_t s = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_n, &h->msg);
+  if (s != FGEMM_OK) return s;
+  const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
+  const int64_t n_out = kind == FGEMM_EPI_SWIGLU ? N / 2 : N;
+  if (M == 0 || n_out == 0) return FGEMM_OK;
+
+  KernelParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.A = static_cast<const uint16_t*>(A);
+  p.B = static_cast<const uint16_t*>(B);
+  p.C = static_cast<uint16_t*>(C);
+  p.bias = epi ? static_cast<const uint16_t*>(epi->bias) : nullptr;
+  p.err = h->d_err;
+  p.lda = lda;
+  p.ldb = ldb;
+  p.ldc = ldc;
+  p.spin_ns = h->spin_ns;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.n_out = static_cast<int>(n_out);
+  p.epi = kind;
+  p.is_bf16 = dtype == FGEMM_BF16 ? 1 : 0;
+  p.alpha = epi ? epi->alpha : 1.0f;
+
+  if (K == 0) {
+    cudaError_t e = fgemm::launch_k0_fill(p, h->stream);
+    return e == cudaSuccess ? FGEMM_OK : cuda_fail(h, e, "K == 0 fill launch");
+  }
+
+  Plan plan;
+  s = choose_plan(h, M, N, K, kind, algo, algo == FGEMM_ALGO_AUTO ? 0 : tile_n, &plan);
+  if (s != FGEMM_OK) return s;
+  const int d = depth_of(plan.algo);
+  const int bn = plan.tile_n;
+
+  p.sub_m = static_cast<int>(M >> d);
+  p.sub_n = static_cast<int>(N >> d);
+  p.sub_k = static_cast<int>(K >> d);
+  p.tiles_m = static_cast<int>((p.sub_m + fgemm::kBM - 1) / fgemm::kBM);
+  if (d == 0 && kind == FGEMM_EPI_SWIGLU)
+    p.tiles_n = static_cast<int>((n_out + bn / 2 - 1) / (bn / 2));
+  else
+    p.tiles_n = (p.sub_n + bn - 1) / bn;
+  const long long units = static_cast<long long>(p.tiles_m) * p.tiles_n;
+  if (units > (1ll << 31) - 1) return set_msg(h, FGEMM_ERR_UNSUPPORTED, "too many tiles");
+  p.num_units = static_cast<int>(units);
+  p.k_blocks = (p.sub_k + fgemm::kBK - 1) / fgemm::kBK;
+  p.raster_group = 8;
+  const uint32_t fmt = p.is_bf16 ? 1u : 0u;
+  p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (1u << 16) |
+            (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>(fgemm::kBM >> 4) << 24);
+  p.num_products = d == 0 ? 1 : (d == 1 ? 7 : 49);
+  p.tab = table_for(d);
+
+  s = encode_tmap(h, &p.tmap_a, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                  static_cast<uint64_t>(lda), fgemm::kBM, p.is_bf16);
+  if (s != FGEMM_OK) return s;
+  s = encode_tmap(h, &p.tmap_b, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                  static_cast<uint64_t>(ldb), fgemm::kBK, p.is_bf16);
+  if (s != FGEMM_OK) return s;
+
+  const int grid = static_cast<int>(std::min<long long>(units, h->num_sms));
+  if (d > 0) {
+    const size_t per_cta = (size_t{1} << (2 * d)) * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float);
+    s = ensure_workspace(h, per_cta * static_cast<size_t>(grid));
+    if (s != FGEMM_OK) return s;
+    p.workspace = h->workspace;
+  }
+  cudaError_t e = fgemm::launch_gemm(bn, d, p, grid, h->stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "GEMM kernel launch");
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                            int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                            fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo) {
+  return fgemm_matmul_ex(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, 0);
+}
+
+fgemm_status_t fgemm_get_error(fgemm_handle_t h) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  cudaError_t e = cudaStreamSynchronize(h->stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, h->d_err, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpy(error word)");
+  if (word == 0) return FGEMM_OK;
+  cudaMemset(h->d_err, 0, sizeof(unsigned int));
+  static const char* roles[] = {"producer", "mma", "epilogue", "operand-sum"};
+  const unsigned role = (word >> 24) & 0xF;
+  char text[160];
+  std::snprintf(text, sizeof(text), "a bounded wait ran out in the %s role of block %u (word 0x%08x)",
+                role < 4 ? roles[role] : "?", word & 0xFFFFFFu, word);
+  return set_msg(h, FGEMM_ERR_TIMEOUT, text);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------- calibration
+
+namespace {
+
+__global__ void fill_pattern_kernel(uint16_t* x, long long n, uint32_t seed, int is_bf16) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    uint32_t v = static_cast<uint32_t>(i) * 2654435761u ^ seed;
+    v ^= v >> 15;
+    v *= 2246822519u;
+    v ^= v >> 13;
+    const float f = (static_cast<float>(v & 0xFFFF) / 32768.0f) - 1.0f;  // [-1, 1)
+    x[i] = is_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(f)) : __half_as_ushort(__float2half_rn(f));
+  }
+}
+
+}  // namespace
+
+extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out_path) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  const int64_t n = 8192;
+  uint16_t *A = nullptr, *B = nullptr, *C = nullptr, *Xa = nullptr, *Xb = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  fgemm_status_t status = FGEMM_OK;
+  fgemm_device_model_t m = h->model;
+  const size_t elems = static_cast<size_t>(n) * n;
+  const size_t copy_bytes = size_t{1} << 30;
+  auto check = [&](cudaError_t e, const char* what) {
+    if (e != cudaSuccess && status == FGEMM_OK) status = cuda_fail(h, e, what);
+    return e == cudaSuccess;
+  };
+  auto time_gemm = [&](int64_t M, int64_t N, int64_t K, fgemm_algo_t algo, int32_t tile, double* us) {
+    const int reps = 3;
+    for (int r = 0; r < reps + 1; ++r) {
+      if (r == 1) check(cudaEventRecord(e0, h->stream), "cudaEventRecord");
+      fgemm_status_t s = fgemm_matmul_ex(h, M, N, K, A, K, B, N, C, N, FGEMM_BF16, nullptr, algo, tile);
+      if (s != FGEMM_OK) {
+        if (status == FGEMM_OK) status = s;
+        return false;
+      }
+    }
+    check(cudaEventRecord(e1, h->stream), "cudaEventRecord");
+    if (!check(cudaEventSynchronize(e1), "cudaEventSynchronize")) return false;
+    float ms = 0;
+    check(cudaEventElapsedTime(&ms, e0, e1), "cudaEventElapsedTime");
+    *us = ms * 1e3 / reps;
+    return status == FGEMM_OK;
+  };
+  do {
+    if (!check(cudaMalloc(&A, elems * 2), "cudaMalloc")) break;
+    if (!check(cudaMalloc(&B, elems * 2), "cudaMalloc")) break;
+    if (!check(cudaMalloc(&C, elems * 2), "cudaMalloc")) break;
+    if (!check(cudaMalloc(&Xa, copy_bytes), "cudaMalloc")) break;
+    if (!check(cudaMalloc(&Xb, copy_bytes), "cudaMalloc")) break;
+    check(cudaEventCreate(&e0), "cudaEventCreate");
+    check(cudaEventCreate(&e1), "cudaEventCreate");
+    fill_pattern_kernel<<<1024, 256, 0, h->stream>>>(A, static_cast<long long>(elems), 1u, 1);
+    fill_pattern_kernel<<<1024, 256, 0, h->stream>>>(B, static_cast<long long>(elems), 2u, 1);
+    if (!check(cudaGetLastError(), "fill launch")) break;
+    const double flops = 2.0 * n * n * n;
+    const int32_t tiles[3] = {64, 128, 256};
+    for (int i = 0; i < 3 && status == FGEMM_OK; ++i) {
+      double us = 0;
+      if (!time_gemm(n, n, n, FGEMM_ALGO_CLASSICAL, tiles[i], &us)) break;
+      m.eff_classical[i] = flops / (us * 1e6) / m.peak_tflops;
+    }
+    for (int d = 1; d <= 2 && status == FGEMM_OK; ++d) {
+      for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
+        double us = 0;
+        if (!time_gemm(n, n, n, d == 1 ? FGEMM_ALGO_STRASSEN1 : FGEMM_ALGO_STRASSEN2, i == 0 ? 128 : 256, &us))
+          break;
+        const double executed = flops * std::pow(7.0 / 8.0, d);
+        m.eff_strassen[d - 1][i] = executed / (us * 1e6) / m.peak_tflops;
+      }
+    }
+    if (status != FGEMM_OK) break;
+    {  // launch + fill: one tiny tile
+      double us = 0;
+      if (!time_gemm(128, 128, 64, FGEMM_ALGO_CLASSICAL, 128, &us)) break;
+      m.launch_us = us;
+      m.tile_fill_us = std::max(0.2, us * 0.25);
+    }
+    {  // streaming bandwidth: device-to-device copy, read + write bytes
+      check(cudaMemcpyAsync(Xb, Xa, copy_bytes, cudaMemcpyDeviceToDevice, h->stream), "copy");
+      check(cudaEventRecord(e0, h->stream), "cudaEventRecord");
+      for (int r = 0; r < 3; ++r)
+        check(cudaMemcpyAsync(Xb, Xa, copy_bytes, cudaMemcpyDeviceToDevice, h->stream), "copy");
+      check(cudaEventRecord(e1, h->stream), "cudaEventRecord");
+      if (!check(cudaEventSynchronize(e1), "cudaEventSynchronize")) break;
+      float ms = 0;
+      check(cudaEventElapsedTime(&ms, e0, e1), "cudaEventElapsedTime");
+      if (ms > 0) m.hbm_gbs = 3.0 * 2.0 * copy_bytes / (ms * 1e-3) / 1e9;
+    }
+  } while (false);
+  cudaStreamSynchronize(h->stream);
+  if (A) cudaFree(A);
+  if (B) cudaFree(B);
+  if (C) cudaFree(C);
+  if (Xa) cudaFree(Xa);
+  if (Xb) cudaFree(Xb);
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (status != FGEMM_OK) return status;
+  h->model = m;
+  h->plans.clear();
+  if (json_out_path) {
+    FILE* f = std::fopen(json_out_path, "w");
+    if (!f) return set_msg(h, FGEMM_ERR_CALIBRATION, std::string("cannot write ") + json_out_path);
+    std::fprintf(f,
+                 "{\n  \"num_sms\": %d,\n  \"peak_tflops\": %.3f,\n  \"hbm_gbs\": %.3f,\n"
+                 "  \"eff_classical_64\": %.5f,\n  \"eff_classical_128\": %.5f,\n"
+                 "  \"eff_classical_256\": %.5f,\n  \"eff_strassen1_128\": %.5f,\n"
+                 "  \"eff_strassen1_256\": %.5f,\n  \"eff_strassen2_128\": %.5f,\n"
+                 "  \"eff_strassen2_256\": %.5f,\n  \"launch_us\": %.3f,\n  \"tile_fill_us\": %.3f,\n"
+                 "  \"l2_bytes\": %.0f,\n  \"l2_gbs\": %.1f\n}\n",
+                 m.num_sms, m.peak_tflops, m.hbm_gbs, m.eff_classical[0], m.eff_classical[1],
+                 m.eff_classical[2], m.eff_strassen[0][0], m.eff_strassen[0][1], m.eff_strassen[1][0],
+                 m.eff_strassen[1][1], m.launch_us, m.tile_fill_us, m.l2_bytes, m.l2_gbs);
+    std::fclose(f);
+  }
+  return FGEMM_OK;
+}

@@ -1,0 +1,14 @@
+// One-level Strassen instantiations of the persistent tcgen05 GEMM.
+#include "fgemm_kernel.cuh"
+
+namespace fgemm {
+
+cudaError_t launch_gemm_depth1(int bn, const KernelParams& p, int grid, cudaStream_t stream) {
+  switch (bn) {
+    case 128: return launch_gemm_t<128, 1>(p, grid, stream);
+    case 256: return launch_gemm_t<256, 1>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fgemm

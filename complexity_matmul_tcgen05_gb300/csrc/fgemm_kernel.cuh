@@ -1,0 +1,679 @@
+// fgemm_kernel.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// One kernel template covers both forms of the product:
+//   DEPTH == 0  classical: C tile = A row block x B column block.
+//   DEPTH >= 1  Strassen-like (FalconGEMM summary, "Methodology" items 1 and
+//               3): each output-tile position of the (M, N) >> DEPTH block
+//               space runs the 7^DEPTH block products one after another; the
+//               operand sums (e.g. A11 + A22, B12 - B22) are formed on chip
+//               by dedicated warps straight into the shared-memory operand
+//               buffers, and every product's accumulator is folded into the
+//               output blocks it contributes to by the epilogue (per-CTA fp32
+//               partial tiles), which also applies the final scale / bias /
+//               activation once the last product is in.
+//
+// Warp roles (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: raw operand tiles -> shared-memory ring
+//   warp 1      MMA issuer (one thread): tcgen05.mma into TMEM; owns TMEM
+//   warps 2,3   (Strassen) operand-sum warps, with warps 8..11
+//   warps 4..7  epilogue: tcgen05.ld -> fp32 math -> rounded stores
+// The TMEM accumulator is double-buffered, so the epilogue of one tile (or
+// product) runs while the MMAs of the next are in flight (the overlap the
+// PingPong GEMM note describes, done here with TMEM buffers instead of two
+// consumer warpgroups).
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry the kernel latches
+// an error code in p.err and every role leaves its loop, so the CTA still
+// reaches its teardown and frees its TMEM.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fgemm_internal.h"
+#include "fgemm_ptx.cuh"
+
+namespace fgemm {
+
+template <int BN>
+struct TileCfg {
+  static constexpr int kABytes = kBM * kBK * 2;  // 16 KB: 128 rows x 128 bytes
+  static constexpr int kBBytes = kBK * BN * 2;   // BN/64 boxes of 64 K-rows x 128 bytes
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int kTmemCols = BN == 256 ? 512 : (BN == 128 ? 256 : 128);
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static_assert(2 * BN <= kTmemCols, "two accumulator buffers must fit in TMEM");
+  static_assert((2 * kStages + 5) * 8 + 4 <= kBarBytes, "barrier area too small");
+};
+
+template <int DEPTH>
+struct RoleCfg {
+  static constexpr int kSumWarps = DEPTH == 0 ? 0 : 6;
+  static constexpr int kThreads = DEPTH == 0 ? 256 : 384;
+};
+
+// ------------------------------------------------------------ small helpers
+
+__device__ __forceinline__ uint32_t err_code(int role) {
+  return kErrTimeout | (static_cast<uint32_t>(role) << 24) | (blockIdx.x & 0xFFFFFFu);
+}
+
+// Bounded wait on one mbarrier phase by the calling thread.  Gives up when
+// the kernel's error word is set by another role (honor_err) or when
+// p.spin_ns elapses (then latches `code`).
+static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const KernelParams& p,
+                                          uint32_t code, bool honor_err) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+#pragma unroll 1
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (honor_err && *reinterpret_cast<volatile unsigned int*>(p.err) != 0u) return false;
+    if (ptx::globaltimer() - t0 > p.spin_ns) {
+      atomicCAS(p.err, 0u, code);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const KernelParams& p,
+                                         int role) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_bounded(bar, parity, p, err_code(role), true);
+}
+
+// Whole-warp wait; the outcome is made warp-uniform.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const KernelParams& p,
+                                          int role) {
+  bool ok = wait_one(bar, parity, p, role);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+__device__ __forceinline__ void unit_coords(const KernelParams& p, int unit, int& tm, int& tn) {
+  const int G = p.raster_group;
+  const int per_group = G * p.tiles_n;
+  const int g = unit / per_group;
+  const int first_m = g * G;
+  const int gsz = min(p.tiles_m - first_m, G);
+  const int r = unit - g * per_group;
+  tm = first_m + r % gsz;
+  tn = r / gsz;
+}
+
+__device__ __forceinline__ float h2f(uint32_t h, int is_bf16) {
+  return is_bf16 ? __uint_as_float(h << 16) : __half2float(__ushort_as_half((unsigned short)h));
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
+  if (is_bf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t pack1(float v, int is_bf16) {
+  return is_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
+                 : __half_as_ushort(__float2half_rn(v));
+}
+
+__device__ __forceinline__ float silu(float v) { return v / (1.0f + __expf(-v)); }
+
+__device__ __forceinline__ float ld_bias(const KernelParams& p, int col) {
+  return h2f(__ldg(p.bias + col), p.is_bf16);
+}
+
+// Writes 32 consecutive outputs of one row, clipping at n_out.
+__device__ __forceinline__ void store_row32(const KernelParams& p, int row, int col0,
+                                            const float (&v)[32]) {
+  uint16_t* dst = p.C + static_cast<long long>(row) * p.ldc + col0;
+  const int n = p.n_out - col0;
+  if (n >= 32) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      d4[q] = make_uint4(pack2(v[8 * q + 0], v[8 * q + 1], p.is_bf16),
+                         pack2(v[8 * q + 2], v[8 * q + 3], p.is_bf16),
+                         pack2(v[8 * q + 4], v[8 * q + 5], p.is_bf16),
+                         pack2(v[8 * q + 6], v[8 * q + 7], p.is_bf16));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n) dst[j] = pack1(v[j], p.is_bf16);
+  }
+}
+
+// v[j] = act(alpha * x[j] + bias[col0 + j]) for the non-gated epilogues.
+__device__ __forceinline__ void finish_plain(const KernelParams& p, int col0, float (&v)[32]) {
+  const int last = p.n_out - 1;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float x = p.alpha * v[j];
+    if (p.bias) x += ld_bias(p, min(col0 + j, last));
+    if (p.epi == kEpiSilu) x = silu(x);
+    v[j] = x;
+  }
+}
+
+// v[j] = silu(alpha * g + bias[col0 + j]) * (alpha * u + bias[n_out + col0 + j]).
+__device__ __forceinline__ void finish_swiglu(const KernelParams& p, int col0, float (&g)[32],
+                                              const float (&u)[32]) {
+  const int last = p.n_out - 1;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float gv = p.alpha * g[j];
+    float uv = p.alpha * u[j];
+    if (p.bias) {
+      const int cj = min(col0 + j, last);
+      gv += ld_bias(p, cj);
+      uv += ld_bias(p, p.n_out + cj);
+    }
+    g[j] = silu(gv) * uv;
+  }
+}
+
+// ------------------------------------------------------------ epilogues
+
+// Classical tile: the accumulator in TMEM columns [tbase, tbase + BN).  For
+// SwiGLU the tile's first BN/2 columns hold gate columns and the last BN/2
+// the matching up columns (the producer loads them side by side).
+template <int BN>
+__device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32_t tbase, int tm,
+                                                   int tn, int r) {
+  const int row = tm * kBM + r;
+  const bool row_ok = row < p.M;
+  if (p.epi == kEpiSwiglu) {
+    constexpr int HALF = BN / 2;
+#pragma unroll 1
+    for (int c = 0; c < HALF / 32; ++c) {
+      uint32_t gr[32], ur[32];
+      ptx::tmem_ld_32x32b_x32(tbase + c * 32, gr);
+      ptx::tmem_ld_32x32b_x32(tbase + HALF + c * 32, ur);
+      ptx::tmem_wait_ld();
+      const int col0 = tn * HALF + c * 32;
+      if (row_ok && col0 < p.n_out) {
+        float g[32], u[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          g[j] = __uint_as_float(gr[j]);
+          u[j] = __uint_as_float(ur[j]);
+        }
+        finish_swiglu(p, col0, g, u);
+        store_row32(p, row, col0, g);
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t ar[32];
+      ptx::tmem_ld_32x32b_x32(tbase + c * 32, ar);
+      ptx::tmem_wait_ld();
+      const int col0 = tn * BN + c * 32;
+      if (row_ok && col0 < p.n_out) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ar[j]);
+        finish_plain(p, col0, v);
+        store_row32(p, row, col0, v);
+      }
+    }
+  }
+}
+
+// Strassen product `pr` at tile (tm, tn): fold +-acc into the per-CTA fp32
+// partial tiles of the output blocks it feeds; after the last product, apply
+// the epilogue to every block and store C.  Workspace layout per CTA:
+// [block][32-column chunk][128 rows][32 floats], so a warp's 32 rows of one
+// chunk are 4 KB contiguous.  Every element is read and written only by the
+// thread that owns its row, in program order.
+template <int BN, int DEPTH>
+__device__ __forceinline__ void epilogue_strassen(const KernelParams& p, uint32_t tbase, int tm,
+                                                  int tn, int pr, int r, float* ws) {
+  constexpr int G = 1 << DEPTH;
+  constexpr int CH = BN / 32;
+  const int nc = p.tab.nc[pr];
+  const bool last = pr == p.num_products - 1;
+  auto slot_ptr = [&](int slot, int c) {
+    return reinterpret_cast<float4*>(ws + ((static_cast<size_t>(slot) * CH + c) * kBM + r) * 32);
+  };
+#pragma unroll 1
+  for (int c = 0; c < CH; ++c) {
+    uint32_t ar[32];
+    ptx::tmem_ld_32x32b_x32(tbase + c * 32, ar);
+    ptx::tmem_wait_ld();
+#pragma unroll 1
+    for (int t = 0; t < nc; ++t) {
+      const uint8_t code = p.tab.c[pr][t];
+      float4* w = slot_ptr(code & kTermIndexMask, c);
+      const float sg = (code & kTermNeg) ? -1.0f : 1.0f;
+      if (code & kTermFirst) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          w[q] = make_float4(sg * __uint_as_float(ar[4 * q + 0]), sg * __uint_as_float(ar[4 * q + 1]),
+                             sg * __uint_as_float(ar[4 * q + 2]), sg * __uint_as_float(ar[4 * q + 3]));
+      } else {
+        float4 x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = w[q];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          x[q].x += sg * __uint_as_float(ar[4 * q + 0]);
+          x[q].y += sg * __uint_as_float(ar[4 * q + 1]);
+          x[q].z += sg * __uint_as_float(ar[4 * q + 2]);
+          x[q].w += sg * __uint_as_float(ar[4 * q + 3]);
+          w[q] = x[q];
+        }
+      }
+    }
+    if (!last) continue;
+    if (p.epi == kEpiSwiglu) {
+#pragma unroll 1
+      for (int sr = 0; sr < G; ++sr) {
+#pragma unroll 1
+        for (int sc = 0; sc < G / 2; ++sc) {
+          const float4* wg = slot_ptr(sr * G + sc, c);
+          const float4* wu = slot_ptr(sr * G + sc + G / 2, c);
+          float g[32], u[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 a = wg[q], b = wu[q];
+            g[4 * q + 0] = a.x; g[4 * q + 1] = a.y; g[4 * q + 2] = a.z; g[4 * q + 3] = a.w;
+            u[4 * q + 0] = b.x; u[4 * q + 1] = b.y; u[4 * q + 2] = b.z; u[4 * q + 3] = b.w;
+          }
+          const int row = sr * p.sub_m + tm * kBM + r;
+          const int col0 = sc * p.sub_n + tn * BN + c * 32;
+          finish_swiglu(p, col0, g, u);
+          store_row32(p, row, col0, g);
+        }
+      }
+    } else {
+#pragma unroll 1
+      for (int s = 0; s < G * G; ++s) {
+        const float4* w = slot_ptr(s, c);
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 a = w[q];
+          v[4 * q + 0] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
+        }
+        const int row = (s >> DEPTH) * p.sub_m + tm * kBM + r;
+        const int col0 = (s & (G - 1)) * p.sub_n + tn * BN + c * 32;
+        finish_plain(p, col0, v);
+        store_row32(p, row, col0, v);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------- on-chip operand sums
+
+// 8 packed 16-bit values -> 8 floats.
+__device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8], int is_bf16) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i + 0] = h2f(w[i] & 0xFFFFu, is_bf16);
+    f[2 * i + 1] = h2f(w[i] >> 16, is_bf16);
+  }
+}
+
+// Forms sum_t sign_t * src_t over `nchunk` 16-byte chunks (8 elements each),
+// in fp32 with one final round-to-nearest-even, and writes each chunk into
+// the 128-byte-swizzled operand buffer.  `addr(ch, &goff, &soff)` maps a chunk
+// to its element offset from each source base and its shared-memory offset.
+template <typename AddrFn>
+__device__ __forceinline__ void form_sum(const uint16_t* const (&src)[kMaxTerms],
+                                         const float (&sg)[kMaxTerms], int nt, int nchunk,
+                                         int tid, int nthreads, uint8_t* dst, int is_bf16,
+                                         AddrFn addr) {
+  constexpr int U = 4;
+#pragma unroll 1
+  for (int ch0 = tid; ch0 < nchunk; ch0 += U * nthreads) {
+    uint4 v[U][kMaxTerms];
+    long long goff[U];
+    uint32_t soff[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int ch = ch0 + u * nthreads;
+      if (ch < nchunk) {
+        addr(ch, goff[u], soff[u]);
+#pragma unroll
+        for (int t = 0; t < kMaxTerms; ++t)
+          if (t < nt) v[u][t] = __ldg(reinterpret_cast<const uint4*>(src[t] + goff[u]));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int ch = ch0 + u * nthreads;
+      if (ch < nchunk) {
+        float acc[8], f[8];
+        unpack8(v[u][0], acc, is_bf16);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] *= sg[0];
+#pragma unroll
+        for (int t = 1; t < kMaxTerms; ++t) {
+          if (t < nt) {
+            unpack8(v[u][t], f, is_bf16);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] += sg[t] * f[i];
+          }
+        }
+        *reinterpret_cast<uint4*>(dst + soff[u]) =
+            make_uint4(pack2(acc[0], acc[1], is_bf16), pack2(acc[2], acc[3], is_bf16),
+                       pack2(acc[4], acc[5], is_bf16), pack2(acc[6], acc[7], is_bf16));
+      }
+    }
+  }
+}
+
+template <int DEPTH>
+__device__ __forceinline__ void form_a(const KernelParams& p, uint8_t* sA, int pr, int tm, int kb,
+                                       int tid, int nthreads) {
+  const int nt = p.tab.na[pr];
+  const uint16_t* src[kMaxTerms];
+  float sg[kMaxTerms];
+#pragma unroll
+  for (int t = 0; t < kMaxTerms; ++t) {
+    const uint8_t code = p.tab.a[pr][t < nt ? t : 0];
+    const int q = code & kTermIndexMask;
+    const int br = q >> DEPTH, bc = q & ((1 << DEPTH) - 1);
+    src[t] = p.A + static_cast<long long>(br * p.sub_m + tm * kBM) * p.lda + bc * p.sub_k + kb * kBK;
+    sg[t] = (code & kTermNeg) ? -1.0f : 1.0f;
+  }
+  const long long lda = p.lda;
+  // 128 rows x 8 chunks; row r, chunk c8 -> swizzled 16-byte slot c8 ^ (r & 7)
+  form_sum(src, sg, nt, kBM * 8, tid, nthreads, sA, p.is_bf16,
+           [lda](int ch, long long& goff, uint32_t& soff) {
+             const int row = ch >> 3, c8 = ch & 7;
+             goff = row * lda + c8 * 8;
+             soff = static_cast<uint32_t>(row * 128 + ((c8 ^ (row & 7)) << 4));
+           });
+}
+
+template <int BN, int DEPTH>
+__device__ __forceinline__ void form_b(const KernelParams& p, uint8_t* sB, int pr, int tn, int kb,
+                                       int tid, int nthreads) {
+  const int nt = p.tab.nb[pr];
+  const uint16_t* src[kMaxTerms];
+  float sg[kMaxTerms];
+#pragma unroll
+  for (int t = 0; t < kMaxTerms; ++t) {
+    const uint8_t code = p.tab.b[pr][t < nt ? t : 0];
+    const int q = code & kTermIndexMask;
+    const int br = q >> DEPTH, bc = q & ((1 << DEPTH) - 1);
+    src[t] = p.B + static_cast<long long>(br * p.sub_k + kb * kBK) * p.ldb + bc * p.sub_n + tn * BN;
+    sg[t] = (code & kTermNeg) ? -1.0f : 1.0f;
+  }
+  const long long ldb = p.ldb;
+  constexpr int CPR = BN / 8;  // 16-byte chunks per K-row of the tile
+  // K-row r, chunk c -> box c / 8 (64 columns each), swizzled slot (c % 8) ^ (r & 7)
+  form_sum(src, sg, nt, kBK * CPR, tid, nthreads, sB, p.is_bf16,
+           [ldb](int ch, long long& goff, uint32_t& soff) {
+             const int row = ch / CPR, c = ch % CPR;
+             goff = row * ldb + c * 8;
+             soff = static_cast<uint32_t>((c >> 3) * 8192 + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+           });
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int BN, int DEPTH>
+__global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
+    fgemm_kernel(const __grid_constant__ KernelParams p) {
+  using TC = TileCfg<BN>;
+  constexpr int S = TC::kStages;
+  constexpr int kSumWarps = RoleCfg<DEPTH>::kSumWarps;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw_addr);
+  const uint32_t sA0 = base;
+  const uint32_t sB0 = base + S * TC::kABytes;
+  const uint32_t bar0 = base + S * TC::kStageBytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + S * TC::kStageBytes + 8 * (2 * S + 5));
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull = [&](uint32_t b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * S + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int NP = DEPTH == 0 ? 1 : p.num_products;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(full(s), 1 + kSumWarps);
+      ptx::mbar_init(empty(s), 1);
+    }
+    for (uint32_t b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull(b), 1);
+      ptx::mbar_init(tempty(b), 4);
+    }
+    ptx::mbar_init(drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TC::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&p.tmap_a);
+      ptx::prefetch_tmap(&p.tmap_b);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+        int tm, tn;
+        unit_coords(p, unit, tm, tn);
+        for (int pr = 0; ok && pr < NP; ++pr) {
+          bool a_raw = true, b_raw = true;
+          int ax0 = 0, ay = tm * kBM, by0 = 0;
+          int bx[BN / 64];
+          if constexpr (DEPTH == 0) {
+            if (p.epi == kEpiSwiglu) {
+              constexpr int HALF = BN / 2;
+#pragma unroll
+              for (int q = 0; q < BN / 64; ++q) {
+                const int qc = q * 64;
+                bx[q] = qc < HALF ? tn * HALF + qc : p.n_out + tn * HALF + (qc - HALF);
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < BN / 64; ++q) bx[q] = tn * BN + q * 64;
+            }
+          } else {
+            a_raw = p.tab.na[pr] == 1;
+            b_raw = p.tab.nb[pr] == 1;
+            const int qa = p.tab.a[pr][0] & kTermIndexMask;
+            const int qb = p.tab.b[pr][0] & kTermIndexMask;
+            ay = (qa >> DEPTH) * p.sub_m + tm * kBM;
+            ax0 = (qa & ((1 << DEPTH) - 1)) * p.sub_k;
+            by0 = (qb >> DEPTH) * p.sub_k;
+            const int bxb = (qb & ((1 << DEPTH) - 1)) * p.sub_n + tn * BN;
+#pragma unroll
+            for (int q = 0; q < BN / 64; ++q) bx[q] = bxb + q * 64;
+          }
+          const uint32_t tx = (a_raw ? TC::kABytes : 0) + (b_raw ? TC::kBBytes : 0);
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_one(empty(s), ph ^ 1u, p, 0)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(full(s), tx);
+            if (a_raw) ptx::tma_load_2d(sA0 + s * TC::kABytes, &p.tmap_a, ax0 + kb * kBK, ay, full(s));
+            if (b_raw) {
+#pragma unroll
+              for (int q = 0; q < BN / 64; ++q)
+                ptx::tma_load_2d(sB0 + s * TC::kBBytes + q * 8192, &p.tmap_b, bx[q], by0 + kb * kBK,
+                                 full(s));
+            }
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Let copies already in flight land before the CTA leaves: the last
+        // S stages' full barriers (bounded, error word ignored).
+        for (int i = 0; i < S; ++i) {
+          if (--s < 0) {
+            s = S - 1;
+            ph ^= 1u;
+          }
+          wait_bounded(full(s), ph, p, err_code(0), false);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0, acc_it = 0;
+      bool ok = true;
+      const uint32_t b_lbo = 8192;  // 64-column boxes of B are 8 KB apart
+      for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+        for (int pr = 0; ok && pr < NP; ++pr) {
+          const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+          ++acc_it;
+          if (!wait_one(tempty(buf), aph ^ 1u, p, 1)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t dt = tmem_base + buf * BN;
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!wait_one(full(s), ph, p, 1)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t ad = ptx::sdesc(sA0 + s * TC::kABytes, 16, 1024);
+            const uint64_t bd = ptx::sdesc(sB0 + s * TC::kBBytes, b_lbo, 1024);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              // K step of 16: +32 bytes inside the A swizzle row, +16 K-rows (2 KB) of B
+              ptx::mma_f16(dt, ad + static_cast<uint64_t>(k * 2), bd + static_cast<uint64_t>(k * 128),
+                           p.idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(empty(s));
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          if (ok) ptx::mma_commit(tfull(buf));
+        }
+      }
+      // Every MMA this thread issued is complete before TMEM is released.
+      ptx::mma_commit(drain);
+      wait_bounded(drain, 0, p, err_code(1), false);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // --------------------------------------------------------- epilogue
+    const int ew = warp - 4;  // TMEM lane quarter this warp may access
+    const int r = ew * 32 + lane;
+    float* ws = nullptr;
+    if constexpr (DEPTH > 0)
+      ws = p.workspace + static_cast<size_t>(blockIdx.x) * (1 << (2 * DEPTH)) * kBM * BN;
+    uint32_t acc_it = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+      int tm, tn;
+      unit_coords(p, unit, tm, tn);
+      for (int pr = 0; pr < NP; ++pr) {
+        const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+        ++acc_it;
+        if (!wait_warp(tfull(buf), aph, p, 2)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * BN;
+        if constexpr (DEPTH == 0) {
+          epilogue_classical<BN>(p, tbase, tm, tn, r);
+        } else {
+          epilogue_strassen<BN, DEPTH>(p, tbase, tm, tn, pr, r, ws);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty(buf));
+      }
+    }
+  } else if (DEPTH > 0 && (warp == 2 || warp == 3 || warp >= 8)) {
+    // ------------------------------------------------ operand-sum warps
+    const int sw = warp < 4 ? warp - 2 : warp - 6;
+    const int tid = sw * 32 + lane;
+    constexpr int NT = kSumWarps * 32;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < p.num_units; unit += gridDim.x) {
+      int tm, tn;
+      unit_coords(p, unit, tm, tn);
+      for (int pr = 0; ok && pr < NP; ++pr) {
+        const bool a_sum = p.tab.na[pr] > 1;
+        const bool b_sum = p.tab.nb[pr] > 1;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_warp(empty(s), ph ^ 1u, p, 3)) {
+            ok = false;
+            break;
+          }
+          if (a_sum) form_a<DEPTH>(p, base_ptr + s * TC::kABytes, pr, tm, kb, tid, NT);
+          if (b_sum)
+            form_b<BN, DEPTH>(p, base_ptr + S * TC::kABytes + s * TC::kBBytes, pr, tn, kb, tid, NT);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(full(s));
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, TC::kTmemCols);
+}
+
+template <int BN, int DEPTH>
+cudaError_t launch_gemm_t(const KernelParams& p, int grid, cudaStream_t stream) {
+  auto kern = fgemm_kernel<BN, DEPTH>;
+  constexpr int smem = TileCfg<BN>::kSmemBytes;
+  static unsigned long long configured = 0;  // per-device bit
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured |= bit;
+  }
+  kern<<<grid, RoleCfg<DEPTH>::kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fgemm

@@ -1,0 +1,195 @@
+// fgemm_model.cpp -- the analytical decision model (host only).
+//
+// FalconGEMM summary, "Methodology" item 4: the runtime of each candidate
+// algorithm is estimated from compute throughput, memory bandwidth and the
+// extra cost that grows with the recursion depth, and the candidate with the
+// smallest predicted time (with its tiling) is chosen; item 5: the choice is
+// made at run time from the actual (M, N, K).
+//
+// The estimate for one (form, tile_n) candidate:
+//   tiles        = tile quantization of the output of one product: ceil(m/128)
+//                  * ceil(n/tile_n)  (CS336 Lecture 05 notes, "Page 43")
+//   waves        = ceil(tiles / SMs); the persistent kernel runs one tile per
+//                  SM at a time, so a partial last wave costs a full one
+//                  ("Page 48", wave quantization)
+//   t_tile       = products * (2 * 128 * tile_n * K_sub / (per-SM peak * eff)
+//                  + fill), eff measured per form and tile width
+//   t_compute    = waves * t_tile
+//   t_memory     = HBM bytes / bandwidth (operands and result once, plus the
+//                  Strassen partial tiles when they cannot stay in L2)
+//   t_operands   = operand elements streamed from L2 into the SMs (tiled
+//                  reads, "Page 42": tiles * (128 + tile_n) * K per source
+//                  term) * 2 bytes / L2 bandwidth
+//   t            = max(t_compute, t_memory, t_operands) + launch ("Page 21",
+//                  the roofline: time is the largest of compute and traffic)
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/fgemm.h"
+#include "fgemm_internal.h"
+
+namespace {
+
+int depth_of(fgemm_algo_t a) {
+  return a == FGEMM_ALGO_STRASSEN1 ? 1 : (a == FGEMM_ALGO_STRASSEN2 ? 2 : 0);
+}
+
+int tile_index(int tile_n) { return tile_n == 64 ? 0 : (tile_n == 128 ? 1 : 2); }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+namespace fgemm {
+
+// Shared with the API's validation: is (algo, tile_n) legal for the shape?
+bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo_t algo,
+                   int32_t tile_n) {
+  if (tile_n != 64 && tile_n != 128 && tile_n != 256) return false;
+  if (epi_kind == FGEMM_EPI_SWIGLU && tile_n == 64) return false;
+  const int d = depth_of(algo);
+  if (d == 0) return true;
+  if (tile_n == 64) return false;
+  const int64_t g = int64_t{1} << d;
+  if (M <= 0 || N <= 0 || K <= 0) return false;
+  return M % (g * kBM) == 0 && N % (g * tile_n) == 0 && K % (g * kBK) == 0;
+}
+
+}  // namespace fgemm
+
+extern "C" {
+
+void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak_tflops,
+                         double hbm_gbs) {
+  if (!out) return;
+  fgemm_device_model_t m{};
+  m.num_sms = num_sms > 0 ? num_sms : 1;
+  m.peak_tflops = peak_tflops > 0 ? peak_tflops : 2250.0;
+  m.hbm_gbs = hbm_gbs > 0 ? hbm_gbs : 7900.0;
+  m.eff_classical[0] = 0.50;
+  m.eff_classical[1] = 0.65;
+  m.eff_classical[2] = 0.75;
+  m.eff_strassen[0][0] = 0.45;
+  m.eff_strassen[0][1] = 0.55;
+  m.eff_strassen[1][0] = 0.35;
+  m.eff_strassen[1][1] = 0.45;
+  m.launch_us = 5.0;
+  m.tile_fill_us = 1.0;
+  m.l2_bytes = 126.0 * 1024 * 1024;
+  m.l2_gbs = 40000.0;
+  *out = m;
+}
+
+int64_t fgemm_model_tiles(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n) {
+  if (M <= 0 || N <= 0 || tile_m <= 0 || tile_n <= 0) return 0;
+  return ceil_div(M, tile_m) * ceil_div(N, tile_n);
+}
+
+int64_t fgemm_model_waves(int64_t tiles, int32_t slots, double* tail_util) {
+  if (tiles <= 0 || slots <= 0) {
+    if (tail_util) *tail_util = 0.0;
+    return 0;
+  }
+  const int64_t waves = ceil_div(tiles, slots);
+  if (tail_util) {
+    const int64_t rem = tiles % slots;
+    *tail_util = rem == 0 ? 1.0 : static_cast<double>(rem) / slots;
+  }
+  return waves;
+}
+
+double fgemm_model_tiled_reads(int64_t M, int64_t N, int64_t K, int32_t tile_m, int32_t tile_n) {
+  if (K <= 0) return 0.0;
+  return static_cast<double>(fgemm_model_tiles(M, N, tile_m, tile_n)) * (tile_m + tile_n) *
+         static_cast<double>(K);
+}
+
+double fgemm_model_roofline(double flops, double bytes, double peak_flops, double bandwidth) {
+  if (bytes <= 0) return peak_flops;
+  return std::min(peak_flops, flops / bytes * bandwidth);
+}
+
+fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, int64_t N,
+                                   int64_t K, int32_t epi_kind, fgemm_algo_t algo,
+                                   int32_t tile_n, double* predicted_us) {
+  if (!dev || M < 0 || N < 0 || K < 0) return FGEMM_ERR_INVALID_ARG;
+  if (algo == FGEMM_ALGO_AUTO) return FGEMM_ERR_INVALID_ARG;
+  if (!fgemm::form_is_legal(M, N, K, epi_kind, algo, tile_n)) return FGEMM_ERR_UNSUPPORTED;
+  const int d = depth_of(algo);
+  const bool swiglu = epi_kind == FGEMM_EPI_SWIGLU;
+  const int64_t n_out = swiglu ? N / 2 : N;
+  const int64_t sub_m = M >> d, sub_n = N >> d, sub_k = K >> d;
+  const int64_t products = d == 0 ? 1 : (d == 1 ? 7 : 49);
+  int64_t tiles;
+  if (d == 0 && swiglu)
+    tiles = fgemm_model_tiles(sub_m, n_out, fgemm::kBM, tile_n / 2);
+  else
+    tiles = fgemm_model_tiles(sub_m, sub_n, fgemm::kBM, tile_n);
+  const int64_t waves = fgemm_model_waves(tiles, dev->num_sms, nullptr);
+  const double eff = d == 0 ? dev->eff_classical[tile_index(tile_n)]
+                            : dev->eff_strassen[d - 1][tile_n == 128 ? 0 : 1];
+  const double per_sm_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms;
+  const double k_pad = static_cast<double>(ceil_div(sub_k, fgemm::kBK) * fgemm::kBK);
+  const double t_tile =
+      products * (2.0 * fgemm::kBM * tile_n * k_pad / (per_sm_flop_per_us * std::max(eff, 1e-3)) +
+                  dev->tile_fill_us);
+  const double t_compute = static_cast<double>(waves) * t_tile;
+  double bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
+                        static_cast<double>(M) * n_out);
+  if (d > 0) {
+    const double slot_bytes = 4.0 * fgemm::kBM * tile_n;
+    const double slots = std::pow(4.0, d);
+    const double live = std::min<double>(static_cast<double>(tiles), dev->num_sms) * slots * slot_bytes;
+    if (live > dev->l2_bytes) {
+      const double contributions = std::pow(12.0, d);  // nonzeros of the combination
+      bytes += static_cast<double>(tiles) * (2.0 * contributions) * slot_bytes;
+    }
+  }
+  const double t_memory = bytes / (dev->hbm_gbs * 1e3);
+  // Operand tiles streamed from L2 into the SMs: every product re-reads its
+  // source blocks (one or two per operand at depth 1, up to four at depth 2).
+  double op_elems;
+  if (d == 0) {
+    op_elems = static_cast<double>(tiles) * (fgemm::kBM + tile_n) * k_pad;
+  } else {
+    // sum over products of (a-terms * 128 + b-terms * tile_n): the scheme's
+    // term counts are 12 + 12 at depth 1 and 144 + 144 at depth 2
+    const double terms = d == 1 ? 12.0 : 144.0;
+    op_elems = static_cast<double>(tiles) * terms * (fgemm::kBM + tile_n) * k_pad;
+  }
+  const double t_operands = 2.0 * op_elems / (dev->l2_gbs * 1e3);
+  if (predicted_us)
+    *predicted_us = std::max(std::max(t_compute, t_memory), t_operands) + dev->launch_us;
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M, int64_t N, int64_t K,
+                                int32_t epi_kind, fgemm_algo_t* algo_out, int32_t* tile_m,
+                                int32_t* tile_n, double* predicted_us) {
+  if (!dev) return FGEMM_ERR_INVALID_ARG;
+  const fgemm_algo_t algos[3] = {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2};
+  const int32_t tiles[3] = {64, 128, 256};
+  double best = INFINITY;
+  fgemm_algo_t best_algo = FGEMM_ALGO_CLASSICAL;
+  int32_t best_tile = 0;
+  for (fgemm_algo_t a : algos) {
+    for (int32_t t : tiles) {
+      double us = 0;
+      if (fgemm_model_predict(dev, M, N, K, epi_kind, a, t, &us) != FGEMM_OK) continue;
+      if (us < best) {
+        best = us;
+        best_algo = a;
+        best_tile = t;
+      }
+    }
+  }
+  if (best_tile == 0) return FGEMM_ERR_UNSUPPORTED;
+  if (algo_out) *algo_out = best_algo;
+  if (tile_m) *tile_m = fgemm::kBM;
+  if (tile_n) *tile_n = best_tile;
+  if (predicted_us) *predicted_us = best;
+  return FGEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,279 @@
+"""Python binding of the fgemm C ABI (include/fgemm.h).
+
+Argument marshalling only: every step of the product runs in the CUDA
+library ``_build/libfgemm.so``.  If that library is missing, every call
+raises -- there is no fallback of any kind.
+
+``matmul`` takes torch CUDA tensors (fp16 or bf16, row-major, unit column
+stride) and enqueues on torch's current stream.  Given CPU tensors it copies
+them to the current device first and returns a CPU result (the end-to-end
+path: host -> device -> kernel -> host).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfgemm.so")
+
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_DEVICE, \
+    ERR_CALIBRATION = range(8)
+F16, BF16 = 0, 1
+ALGOS = {"auto": 0, "classical": 1, "strassen1": 2, "strassen2": 3}
+ALGO_NAMES = {v: k for k, v in ALGOS.items()}
+EPILOGUES = {"none": 0, "scale_bias": 1, "silu": 2, "swiglu": 3}
+
+
+class FgemmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(message)
+
+
+class Epilogue(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("alpha", ctypes.c_float), ("bias", ctypes.c_void_p)]
+
+
+class DeviceModel(ctypes.Structure):
+    _fields_ = [("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("peak_tflops", ctypes.c_double), ("hbm_gbs", ctypes.c_double),
+                ("eff_classical", ctypes.c_double * 3),
+                ("eff_strassen", (ctypes.c_double * 2) * 2),
+                ("launch_us", ctypes.c_double), ("tile_fill_us", ctypes.c_double),
+                ("l2_bytes", ctypes.c_double), ("l2_gbs", ctypes.c_double)]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise FgemmError(ERR_CUDA, f"fgemm CUDA library not built: {LIB_PATH} is missing "
+                                       "(run python -m complexity_matmul_tcgen05_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, i32, vp, st = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int
+        epi_p = ctypes.POINTER(Epilogue)
+        model_p = ctypes.POINTER(DeviceModel)
+        L.fgemm_create.argtypes = [ctypes.POINTER(vp)]
+        L.fgemm_destroy.argtypes = [vp]
+        L.fgemm_set_stream.argtypes = [vp, vp]
+        mm = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, st, epi_p, st]
+        L.fgemm_matmul.argtypes = mm
+        L.fgemm_matmul_ex.argtypes = mm + [i32]
+        L.fgemm_plan.argtypes = [vp, i64, i64, i64, st, epi_p, ctypes.POINTER(st),
+                                 ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                 ctypes.POINTER(ctypes.c_double)]
+        L.fgemm_get_error.argtypes = [vp]
+        L.fgemm_calibrate.argtypes = [vp, ctypes.c_char_p]
+        L.fgemm_status_string.argtypes = [st]
+        L.fgemm_status_string.restype = ctypes.c_char_p
+        L.fgemm_last_message.argtypes = [vp]
+        L.fgemm_last_message.restype = ctypes.c_char_p
+        L.fgemm_validate.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, st, epi_p, st, i32]
+        L.fgemm_model_default.argtypes = [model_p, i32, ctypes.c_double, ctypes.c_double]
+        L.fgemm_model_default.restype = None
+        L.fgemm_model_tiles.argtypes = [i64, i64, i32, i32]
+        L.fgemm_model_tiles.restype = i64
+        L.fgemm_model_waves.argtypes = [i64, i32, ctypes.POINTER(ctypes.c_double)]
+        L.fgemm_model_waves.restype = i64
+        L.fgemm_model_tiled_reads.argtypes = [i64, i64, i64, i32, i32]
+        L.fgemm_model_tiled_reads.restype = ctypes.c_double
+        L.fgemm_model_roofline.argtypes = [ctypes.c_double] * 4
+        L.fgemm_model_roofline.restype = ctypes.c_double
+        L.fgemm_model_predict.argtypes = [model_p, i64, i64, i64, i32, st, i32,
+                                          ctypes.POINTER(ctypes.c_double)]
+        L.fgemm_model_plan.argtypes = [model_p, i64, i64, i64, i32, ctypes.POINTER(st),
+                                       ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                       ctypes.POINTER(ctypes.c_double)]
+        L.fgemm_get_device_model.argtypes = [vp, model_p]
+        L.fgemm_set_device_model.argtypes = [vp, model_p]
+        for name in ("fgemm_create", "fgemm_destroy", "fgemm_set_stream", "fgemm_matmul",
+                     "fgemm_matmul_ex", "fgemm_plan", "fgemm_get_error", "fgemm_calibrate",
+                     "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
+                     "fgemm_get_device_model", "fgemm_set_device_model"):
+            getattr(L, name).restype = st
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().fgemm_status_string(status).decode()
+
+
+def _check(status: int, handle_ptr=None):
+    if status != OK:
+        msg = lib().fgemm_last_message(handle_ptr).decode()
+        raise FgemmError(status, f"{status_string(status)}: {msg}")
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float16:
+        return F16
+    if t == torch.bfloat16:
+        return BF16
+    raise FgemmError(ERR_INVALID_ARG, f"fgemm supports float16 and bfloat16, not {t}")
+
+
+def make_epilogue(kind: str = "none", alpha: float = 1.0, bias_ptr: int | None = None) -> Epilogue:
+    return Epilogue(EPILOGUES[kind], float(alpha), bias_ptr)
+
+
+def validate(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype: int, epilogue: Epilogue | None,
+             algo: str = "auto", tile_n: int = 0) -> int:
+    """Host-only argument check (no device): the status fgemm_matmul_ex would return."""
+    return lib().fgemm_validate(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype,
+                                ctypes.byref(epilogue) if epilogue is not None else None,
+                                ALGOS[algo], tile_n)
+
+
+class Handle:
+    """An fgemm handle on the current CUDA device."""
+
+    def __init__(self):
+        h = ctypes.c_void_p()
+        _check(lib().fgemm_create(ctypes.byref(h)))
+        self._h = h
+        self.device = torch.cuda.current_device()
+
+    @property
+    def ptr(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().fgemm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):  # pragma: no cover - interpreter teardown order
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_stream(self, stream_ptr: int):
+        _check(lib().fgemm_set_stream(self._h, ctypes.c_void_p(stream_ptr)), self._h)
+
+    def matmul_raw(self, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype: int,
+                   epilogue: Epilogue | None = None, algo: str = "auto", tile_n: int = 0) -> int:
+        """Direct C-ABI call on raw device pointers; returns the status."""
+        return lib().fgemm_matmul_ex(self._h, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype,
+                                     ctypes.byref(epilogue) if epilogue is not None else None,
+                                     ALGOS[algo], tile_n)
+
+    def plan(self, M, N, K, dtype: int = BF16, epilogue: Epilogue | None = None):
+        a = ctypes.c_int()
+        tm = ctypes.c_int32()
+        tn = ctypes.c_int32()
+        us = ctypes.c_double()
+        _check(lib().fgemm_plan(self._h, M, N, K, dtype,
+                                ctypes.byref(epilogue) if epilogue is not None else None,
+                                ctypes.byref(a), ctypes.byref(tm), ctypes.byref(tn),
+                                ctypes.byref(us)), self._h)
+        return ALGO_NAMES[a.value], tn.value, us.value
+
+    def get_error(self) -> int:
+        return lib().fgemm_get_error(self._h)
+
+    def last_message(self) -> str:
+        return lib().fgemm_last_message(self._h).decode()
+
+    def calibrate(self, json_path: str | None = None):
+        _check(lib().fgemm_calibrate(self._h, json_path.encode() if json_path else None), self._h)
+
+    def device_model(self) -> DeviceModel:
+        m = DeviceModel()
+        _check(lib().fgemm_get_device_model(self._h, ctypes.byref(m)), self._h)
+        return m
+
+    def set_device_model(self, m: DeviceModel):
+        _check(lib().fgemm_set_device_model(self._h, ctypes.byref(m)), self._h)
+
+
+_handles: dict[int, Handle] = {}
+
+
+def default_handle() -> Handle:
+    dev = torch.cuda.current_device()
+    h = _handles.get(dev)
+    if h is None:
+        h = Handle()
+        _handles[dev] = h
+    return h
+
+
+def _check_matrix(t: torch.Tensor, name: str):
+    if t.dim() != 2:
+        raise FgemmError(ERR_INVALID_ARG, f"{name} must be 2-D")
+    if t.size(1) > 1 and t.stride(1) != 1:
+        raise FgemmError(ERR_INVALID_ARG, f"{name} must be row-major with unit column stride")
+
+
+def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
+           epilogue: str = "none", alpha: float = 1.0, bias: torch.Tensor | None = None,
+           algo: str = "auto", tile_n: int = 0, handle: Handle | None = None) -> torch.Tensor:
+    """C = epi(alpha * A @ B + bias) through fgemm_matmul_ex.
+
+    A is M x K, B is K x N (row-major), bias has N entries; for
+    epilogue="swiglu" the output is M x N/2 (gate | up halves of B's columns).
+    """
+    if A.device.type == "cpu" and B.device.type == "cpu":
+        dev = torch.device("cuda", torch.cuda.current_device())
+        Ad = A.to(dev, non_blocking=True)
+        Bd = B.to(dev, non_blocking=True)
+        bd = None if bias is None else bias.to(dev, non_blocking=True)
+        Cd = matmul(Ad, Bd, epilogue=epilogue, alpha=alpha, bias=bd, algo=algo, tile_n=tile_n,
+                    handle=handle)
+        if out is not None:
+            out.copy_(Cd)
+            return out
+        return Cd.cpu()
+    _check_matrix(A, "A")
+    _check_matrix(B, "B")
+    if not (A.is_cuda and B.is_cuda):
+        raise FgemmError(ERR_INVALID_ARG, "A and B must both be CUDA tensors (or both CPU)")
+    if A.dtype != B.dtype:
+        raise FgemmError(ERR_INVALID_ARG, "A and B must have the same dtype")
+    dt = _dtype_code(A.dtype)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise FgemmError(ERR_INVALID_ARG, f"inner dimensions differ: {K} vs {K2}")
+    n_out = N // 2 if epilogue == "swiglu" else N
+    if out is None:
+        out = torch.empty((M, n_out), dtype=A.dtype, device=A.device)
+    else:
+        _check_matrix(out, "out")
+        if out.dtype != A.dtype or tuple(out.shape) != (M, n_out):
+            raise FgemmError(ERR_INVALID_ARG, "out has the wrong dtype or shape")
+    bias_ptr = None
+    if bias is not None:
+        if bias.dtype != A.dtype or bias.numel() != N or not bias.is_cuda:
+            raise FgemmError(ERR_INVALID_ARG, "bias must be a CUDA vector of N entries, same dtype")
+        bias = bias.contiguous()
+        bias_ptr = bias.data_ptr()
+    h = handle if handle is not None else default_handle()
+    h.set_stream(torch.cuda.current_stream(A.device).cuda_stream)
+    epi = make_epilogue(epilogue, alpha, bias_ptr)
+    lda = A.stride(0) if M > 1 else max(K, 1)
+    ldb = B.stride(0) if K > 1 else max(N, 1)
+    ldc = out.stride(0) if M > 1 else max(n_out, 1)
+    s = h.matmul_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, dt,
+                     epi, algo, tile_n)
+    _check(s, h.ptr)
+    return out
+
+
+def plan(M: int, N: int, K: int, dtype: torch.dtype = torch.bfloat16, epilogue: str = "none"):
+    """(algorithm, tile_n, predicted microseconds) the decision model picks."""
+    h = default_handle()
+    return h.plan(M, N, K, _dtype_code(dtype), make_epilogue(epilogue))

@@ -1,0 +1,255 @@
+/*
+ * fgemm.h -- C ABI of the fgemm library: dense half-precision matrix
+ * multiplication C = epi(alpha * A * B + bias) on one GB300 (sm_103a), in a
+ * classical form and in Strassen-like low-complexity forms (one or two
+ * recursion levels), with an analytical picker that chooses the algorithm
+ * and the tile per shape.
+ *
+ * Sources of the operations declared here:
+ *  - Low-complexity matrix multiplication (LCMA), Strassen-like, with a
+ *    recursion depth; a runtime model that picks algorithm and tiling from
+ *    compute throughput, memory bandwidth and the per-depth overhead; runtime
+ *    dispatch on the actual (M, N, K): FalconGEMM summary (arXiv 2605.06057),
+ *    "Methodology" items 1, 3, 4, 5 and "Results & Findings".
+ *  - Mainloop + epilogue split, epilogue fusion of scaling, elementwise ops
+ *    and SwiGLU: PingPong GEMM / CODA note (tilnote), opening section and
+ *    "How CODA applies it".
+ *  - 16-bit inputs with fp32 accumulation: CS336 Lecture 05 notes, "Page 26.
+ *    Low precision drives faster matrix multiplies".
+ *  - Tile and wave quantization, roofline: CS336 Lecture 05 notes, "Page 21",
+ *    "Page 43" and "Page 48".
+ *
+ * Conventions for every entry point:
+ *  - All matrices are row-major. Leading dimensions (lda, ldb, ldc) are in
+ *    elements. A is M x K, B is K x N, C is M x N_out with N_out = N, except
+ *    for FGEMM_EPI_SWIGLU where N_out = N / 2.
+ *  - Matrix and bias pointers are DEVICE pointers owned by the caller. The
+ *    library never frees, reads back or retains them beyond the call.
+ *  - Calls are asynchronous on the handle's stream: fgemm_matmul returns once
+ *    the kernel is enqueued. Errors found on the device (a bounded wait that
+ *    ran out) are latched in the handle and returned by fgemm_get_error.
+ *  - Argument errors are returned before anything is launched.
+ *  - A handle is used by one host thread at a time.
+ */
+#ifndef FGEMM_H
+#define FGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fgemm_handle_s* fgemm_handle_t;
+
+/* Element type of A, B, C and bias (all four share it). */
+typedef enum { FGEMM_F16 = 0, FGEMM_BF16 = 1 } fgemm_dtype_t;
+
+/* AUTO lets the decision model choose; the others force a form. */
+typedef enum {
+  FGEMM_ALGO_AUTO = 0,
+  FGEMM_ALGO_CLASSICAL = 1,
+  FGEMM_ALGO_STRASSEN1 = 2, /* one Strassen level: 7 half-size products */
+  FGEMM_ALGO_STRASSEN2 = 3  /* two levels: 49 quarter-size products */
+} fgemm_algo_t;
+
+/*
+ * Epilogue applied to the fp32 accumulator before the single rounding to the
+ * output type (PingPong GEMM / CODA note: the epilogue scales and applies
+ * elementwise operations before the write-back; CODA fuses SwiGLU there):
+ *   v = alpha * acc[i][j] + bias[j]            (bias term only if bias != NULL)
+ *   NONE, SCALE_BIAS : C[i][j] = v
+ *   SILU             : C[i][j] = v / (1 + exp(-v))
+ *   SWIGLU           : C[i][j] = silu(v[i][j]) * v[i][j + N/2], j < N/2
+ *                      (columns [0, N/2) of A*B are the gate, [N/2, N) the up
+ *                      projection; bias, if given, has N entries).
+ * SCALE_BIAS requires bias. bias has N entries of the element type, device
+ * memory, 2-byte aligned.
+ */
+typedef enum {
+  FGEMM_EPI_NONE = 0,
+  FGEMM_EPI_SCALE_BIAS = 1,
+  FGEMM_EPI_SILU = 2,
+  FGEMM_EPI_SWIGLU = 3
+} fgemm_epi_kind_t;
+
+typedef struct {
+  int32_t kind;     /* fgemm_epi_kind_t */
+  float alpha;      /* scale of the accumulator */
+  const void* bias; /* device pointer or NULL */
+} fgemm_epilogue_t;
+
+typedef enum {
+  FGEMM_OK = 0,
+  FGEMM_ERR_INVALID_ARG = 1, /* NULL pointer, bad size, ld too small, bad enum */
+  FGEMM_ERR_ALIGNMENT = 2,   /* pointer or row stride not 16-byte aligned */
+  FGEMM_ERR_UNSUPPORTED = 3, /* forced algorithm / tile not legal for shape */
+  FGEMM_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+  FGEMM_ERR_TIMEOUT = 5,     /* a bounded wait inside a kernel ran out */
+  FGEMM_ERR_NO_DEVICE = 6,   /* no usable sm_103 device */
+  FGEMM_ERR_CALIBRATION = 7  /* calibration file unreadable or malformed */
+} fgemm_status_t;
+
+/*
+ * Creates a handle on the CURRENT CUDA device. The handle owns: a device
+ * error word, a plan cache, a tensor-descriptor cache, the Strassen partial
+ * workspace (grown on demand) and the device model. The device model starts
+ * from the device's SM count and, if the environment variable FGEMM_CALIB
+ * names a calibration JSON written by fgemm_calibrate, from that file.
+ * Returns FGEMM_ERR_NO_DEVICE if no device is present or it is not sm_103,
+ * FGEMM_ERR_CALIBRATION if FGEMM_CALIB names a bad file.
+ */
+fgemm_status_t fgemm_create(fgemm_handle_t* out);
+
+/* Frees everything the handle owns. NULL is accepted. Synchronises the
+ * handle's stream first. */
+fgemm_status_t fgemm_destroy(fgemm_handle_t h);
+
+/* Sets the cudaStream_t (passed as void*) later calls are enqueued on.
+ * NULL selects the legacy default stream (the initial value). */
+fgemm_status_t fgemm_set_stream(fgemm_handle_t h, void* cuda_stream);
+
+/*
+ * C = epi(alpha * A * B + bias); see the conventions above.
+ *   M, N, K    >= 0. M == 0 or N_out == 0: nothing is done. K == 0: C = epi(bias).
+ *   A, lda     device pointer, M x K, lda >= K.
+ *   B, ldb     device pointer, K x N, ldb >= N.
+ *   C, ldc     device pointer, M x N_out, ldc >= N_out. C is only written.
+ *   epi        NULL means NONE with alpha = 1 and no bias.
+ *   algo       FGEMM_ALGO_AUTO or a forced form.
+ * Alignment: A, B, C 16-byte aligned and lda, ldb, ldc multiples of 8
+ * elements (the tensor-memory-access engine needs 16-byte rows), and for
+ * SWIGLU N a multiple of 16 -> else FGEMM_ERR_ALIGNMENT.
+ * Strassen forms need M, N, K (for SWIGLU: M, N/2, K) divisible into 2^d
+ * blocks that are whole numbers of tiles (128 rows, 128 or 256 columns, 64
+ * along K) -> else FGEMM_ERR_UNSUPPORTED; AUTO never picks an illegal form.
+ * Strassen forms use the handle's workspace (4^d partial tiles per SM).
+ */
+fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                            const void* A, int64_t lda, const void* B,
+                            int64_t ldb, void* C, int64_t ldc,
+                            fgemm_dtype_t dtype, const fgemm_epilogue_t* epi,
+                            fgemm_algo_t algo);
+
+/*
+ * As fgemm_matmul, with the output tile width forced: tile_n in {64, 128,
+ * 256} (classical), {128, 256} (Strassen forms, SWIGLU), or 0 to let the
+ * model choose. Used for exhaustive timing of the decision model's choices.
+ */
+fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N,
+                               int64_t K, const void* A, int64_t lda,
+                               const void* B, int64_t ldb, void* C, int64_t ldc,
+                               fgemm_dtype_t dtype, const fgemm_epilogue_t* epi,
+                               fgemm_algo_t algo, int32_t tile_n);
+
+/*
+ * Runs the decision model (no launch): the algorithm, tile and predicted
+ * time AUTO would use for this shape (FalconGEMM summary, "Methodology"
+ * items 4 and 5). Output pointers may be NULL.
+ */
+fgemm_status_t fgemm_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                          fgemm_dtype_t dtype, const fgemm_epilogue_t* epi,
+                          fgemm_algo_t* algo_out, int32_t* tile_m,
+                          int32_t* tile_n, double* predicted_us);
+
+/* Synchronises the handle's stream, then returns and clears the latched
+ * device error (FGEMM_OK, FGEMM_ERR_TIMEOUT or FGEMM_ERR_CUDA). */
+fgemm_status_t fgemm_get_error(fgemm_handle_t h);
+
+/*
+ * Measures the device (tensor throughput of each classical tile width and
+ * of each Strassen form, streaming bandwidth) with the library's own
+ * kernels, updates the handle's device model, and writes it as JSON to
+ * json_out_path if that is not NULL (FalconGEMM summary, "Methodology" item
+ * 4: the model is built from measured compute throughput and bandwidth).
+ * Allocates and frees its own scratch matrices. Takes about a second.
+ */
+fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out_path);
+
+/* Static string naming a status. */
+const char* fgemm_status_string(fgemm_status_t s);
+
+/* Text of the last error reported on this handle (or, for h == NULL, on this
+ * thread by a call without a handle). Valid until the next call. */
+const char* fgemm_last_message(fgemm_handle_t h);
+
+/*
+ * Host-only argument check used by fgemm_matmul_ex (no device needed):
+ * returns the status fgemm_matmul_ex would return before launching.
+ */
+fgemm_status_t fgemm_validate(int64_t M, int64_t N, int64_t K, const void* A,
+                              int64_t lda, const void* B, int64_t ldb,
+                              const void* C, int64_t ldc, fgemm_dtype_t dtype,
+                              const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                              int32_t tile_n);
+
+/* ------------------------------------------------------------------------
+ * Decision model, host only (no device needed). FalconGEMM summary,
+ * "Methodology" item 4 (analytical runtime model: compute throughput, memory
+ * bandwidth, overhead per recursion depth) with the tile and wave
+ * quantization terms of the CS336 Lecture 05 notes, "Page 43" and "Page 48",
+ * and the roofline of "Page 21".
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t num_sms;         /* concurrent tile slots (one persistent CTA per SM) */
+  int32_t reserved;
+  double peak_tflops;      /* dense 16-bit tensor peak, TFLOP/s */
+  double hbm_gbs;          /* streaming HBM bandwidth, GB/s */
+  double eff_classical[3]; /* mainloop fraction of peak for tile_n 64, 128, 256 */
+  double eff_strassen[2][2]; /* [depth-1][tile_n 128, 256]: executed-MAC rate
+                              * of the Strassen mainloop as a fraction of peak */
+  double launch_us;        /* fixed cost of one launch */
+  double tile_fill_us;     /* pipeline fill + drain cost per tile visit */
+  double l2_bytes;         /* L2 capacity (bytes) */
+  double l2_gbs;           /* L2 -> SM operand bandwidth, GB/s */
+} fgemm_device_model_t;
+
+/* Default model for a device with the given SM count, peak and bandwidth. */
+void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms,
+                         double peak_tflops, double hbm_gbs);
+
+/* Tile quantization: ceil(M / tile_m) * ceil(N / tile_n). */
+int64_t fgemm_model_tiles(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n);
+
+/* Wave quantization: number of waves ceil(tiles / slots); *tail_util (may be
+ * NULL) receives the occupancy of the last wave, (tiles mod slots) / slots,
+ * or 1 when tiles is a multiple of slots. */
+int64_t fgemm_model_waves(int64_t tiles, int32_t slots, double* tail_util);
+
+/* Elements a tiled product reads from global memory: each tile_m x tile_n
+ * output tile reads a tile_m x K block of A and a K x tile_n block of B, so
+ * tiles * (tile_m + tile_n) * K; for square N with T x T tiles that is
+ * 2 N^3 / T (CS336 Lecture 05 notes, "Page 42. Tiling math"). */
+double fgemm_model_tiled_reads(int64_t M, int64_t N, int64_t K, int32_t tile_m,
+                               int32_t tile_n);
+
+/* Roofline: min(peak_flops, (flops / bytes) * bandwidth) in FLOP/s. */
+double fgemm_model_roofline(double flops, double bytes, double peak_flops,
+                            double bandwidth);
+
+/* Predicted time (us) of one form and tile for a shape; returns
+ * FGEMM_ERR_UNSUPPORTED if that form/tile is illegal for the shape. */
+fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M,
+                                   int64_t N, int64_t K, int32_t epi_kind,
+                                   fgemm_algo_t algo, int32_t tile_n,
+                                   double* predicted_us);
+
+/* The argmin over every legal (form, tile): what AUTO launches. */
+fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M,
+                                int64_t N, int64_t K, int32_t epi_kind,
+                                fgemm_algo_t* algo_out, int32_t* tile_m,
+                                int32_t* tile_n, double* predicted_us);
+
+/* Copies the handle's current device model into *out. */
+fgemm_status_t fgemm_get_device_model(fgemm_handle_t h,
+                                      fgemm_device_model_t* out);
+
+/* Replaces the handle's device model (clears the plan cache). */
+fgemm_status_t fgemm_set_device_model(fgemm_handle_t h,
+                                      const fgemm_device_model_t* model);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FGEMM_H */

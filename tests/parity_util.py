@@ -1,0 +1,99 @@
+"""Helpers shared by the GPU parity tests: running the CUDA path through the
+C ABI and comparing with the oracle.  The comparison rules:
+
+* exact:     bit-for-bit equal to RNE_dtype(exact result) (ternary inputs).
+* normwise:  ||C_gpu - RNE(C_ref)||_F / ||C_ref||_F over the evaluated
+             entries, with C_ref the fp64 oracle.
+* elementwise (classical, no activation): each entry within 8 ulp of the
+             output type at C_ref, or within gamma_K * sum_k |a_ik b_kj| + ulp/2
+             (the standard bound of an fp32 dot product of length K).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from complexity_matmul_tcgen05_gb300 import fgemm, inputs
+
+TOL_NORMWISE = {"classical": 1e-3, "strassen1": 5e-3, "strassen2": 1e-2}
+TOL_EMULATED = 1e-4
+
+
+def dtype_name(t: torch.dtype) -> str:
+    return "bf16" if t == torch.bfloat16 else "f16"
+
+
+def gpu_bits(t: torch.Tensor) -> np.ndarray:
+    return inputs.bits(t.detach().cpu())
+
+
+def values(t: torch.Tensor) -> np.ndarray:
+    """Exact float64 values of a 16-bit tensor (decoded by the oracle)."""
+    return oracle.decode(gpu_bits(t), dtype_name(t.dtype))
+
+
+def ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Spacing of the 16-bit output format at |x| (subnormal spacing below)."""
+    mbits, emin = (7, -126) if dtype == "bf16" else (10, -14)
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    e = np.maximum(e, emin)
+    return np.ldexp(1.0, (e - mbits).astype(np.int64))
+
+
+def normwise(c_gpu: np.ndarray, c_ref: np.ndarray, dtype: str) -> float:
+    den = np.linalg.norm(c_ref)
+    if den == 0:
+        return float(np.linalg.norm(c_gpu))
+    return float(np.linalg.norm(c_gpu - oracle.round_to(c_ref, dtype)) / den)
+
+
+def elementwise_ok(c_gpu: np.ndarray, c_ref: np.ndarray, absdot: np.ndarray, K: int,
+                   dtype: str):
+    """(all entries pass, fraction that needed the dot-product-bound branch)."""
+    u = 2.0 ** -24
+    gamma = K * u / (1 - K * u)
+    diff = np.abs(c_gpu - c_ref)
+    ul = ulp(c_ref, dtype)
+    by_ulp = diff <= 8 * ul
+    by_bound = diff <= gamma * absdot + 0.5 * ul
+    ok = by_ulp | by_bound
+    return bool(ok.all()), float(np.mean(~by_ulp & by_bound))
+
+
+def abs_bits(b: np.ndarray) -> np.ndarray:
+    return (b & np.uint16(0x7FFF)).astype(np.uint16)
+
+
+def run(A, B, algo="classical", epilogue="none", alpha=1.0, bias=None, tile_n=0, out=None):
+    C = fgemm.matmul(A, B, out=out, epilogue=epilogue, alpha=alpha, bias=bias, algo=algo,
+                     tile_n=tile_n)
+    torch.cuda.synchronize()
+    assert fgemm.default_handle().get_error() == fgemm.OK, fgemm.default_handle().last_message()
+    return C
+
+
+def activation_condition(raw: np.ndarray, kind: str, alpha: float = 1.0,
+                         bias: np.ndarray | None = None) -> float:
+    """Normwise first-order condition number of the epilogue activation at
+    the reference product ``raw`` (M x N, pre-activation, without alpha/bias):
+    ||sum_x |d out/d x| * |x| || / ||out||, x ranging over the activation's
+    inputs (v for SiLU; gate and up for SwiGLU).  A relative perturbation
+    eps of the product becomes at most about kappa * eps in the output."""
+    v = alpha * raw + (0.0 if bias is None else bias[None, :])
+    sig = 1.0 / (1.0 + np.exp(-v))
+    silu = v * sig
+    dsilu = sig * (1.0 + v * (1.0 - sig))
+    if kind == "silu":
+        num = np.abs(dsilu * v)
+        out = silu
+    elif kind == "swiglu":
+        h = v.shape[1] // 2
+        g, u = v[:, :h], v[:, h:]
+        num = np.abs(dsilu[:, :h] * u * g) + np.abs(silu[:, :h] * u)
+        out = silu[:, :h] * u
+    else:
+        return 1.0
+    den = np.linalg.norm(out)
+    return float(np.linalg.norm(num) / den) if den > 0 else 1.0

@@ -1,0 +1,219 @@
+"""CPU tests of the C ABI: the library loads, exports every function the
+header declares, rejects bad arguments with the documented codes (host-only
+validation, nothing launched), and its decision model reproduces the worked
+numbers of the CS336 Lecture 05 notes."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from complexity_matmul_tcgen05_gb300 import fgemm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden", "cs336_quantization_examples.json")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from complexity_matmul_tcgen05_gb300 import build
+    build.build()
+    return fgemm.lib()
+
+
+def _declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(fgemm_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function(L):
+    names = _declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_create_without_device_reports_no_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    h = ctypes.c_void_p()
+    assert L.fgemm_create(ctypes.byref(h)) == fgemm.ERR_NO_DEVICE
+    assert h.value is None
+    assert L.fgemm_destroy(None) == fgemm.OK
+
+
+def test_status_strings(L):
+    for s in range(8):
+        assert fgemm.status_string(s).startswith("FGEMM_")
+
+
+def _v(M, N, K, A=16, lda=None, B=16, ldb=None, C=16, ldc=None, dtype=fgemm.BF16,
+       epi=None, algo="auto", tile=0):
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    n_out = N // 2 if (epi is not None and epi.kind == 3) else N
+    ldc = n_out if ldc is None else ldc
+    return fgemm.validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile)
+
+
+def test_validation_codes(L):
+    ok = fgemm.OK
+    assert _v(256, 256, 256) == ok
+    assert _v(0, 256, 256, A=0, B=0, C=0) == ok                    # empty: nothing to do
+    assert _v(8, 16, 0, A=0, B=0) == ok                            # K = 0: C = epi(bias)
+    assert _v(8, 16, 64, A=0) == fgemm.ERR_INVALID_ARG             # NULL A
+    assert _v(8, 16, 64, lda=32) == fgemm.ERR_INVALID_ARG          # lda < K
+    assert _v(8, 16, 64, ldb=8) == fgemm.ERR_INVALID_ARG           # ldb < N
+    assert _v(8, 16, 64, ldc=8) == fgemm.ERR_INVALID_ARG           # ldc < N
+    assert _v(-1, 16, 64) == fgemm.ERR_INVALID_ARG
+    assert _v(8, 16, 64, A=18) == fgemm.ERR_ALIGNMENT              # A not 16-byte aligned
+    assert _v(8, 16, 64, C=24) == fgemm.ERR_ALIGNMENT
+    assert _v(8, 16, 60, lda=60) == fgemm.ERR_ALIGNMENT            # 120-byte rows
+    assert _v(8, 16, 64, dtype=7) == fgemm.ERR_INVALID_ARG
+    assert _v(8, 16, 64, algo="classical", tile=96) == fgemm.ERR_INVALID_ARG
+    sb = fgemm.make_epilogue("scale_bias", 1.0, None)
+    assert _v(8, 16, 64, epi=sb) == fgemm.ERR_INVALID_ARG          # SCALE_BIAS without bias
+    sw = fgemm.make_epilogue("swiglu", 1.0, None)
+    assert _v(8, 24, 64, epi=sw) == fgemm.ERR_ALIGNMENT            # up half at column 12
+    assert _v(8, 32, 64, epi=sw) == ok
+    assert _v(8, 32, 64, epi=sw, algo="classical", tile=64) == fgemm.ERR_UNSUPPORTED
+    # Strassen legality: 2^d blocks of whole 128 x tile_n x 64 tiles
+    assert _v(256, 256, 128, algo="strassen1", tile=128) == ok
+    assert _v(256, 256, 128, algo="strassen1", tile=256) == fgemm.ERR_UNSUPPORTED
+    assert _v(384, 256, 128, algo="strassen1") == fgemm.ERR_UNSUPPORTED
+    assert _v(256, 256, 96, lda=96, algo="strassen1") == fgemm.ERR_UNSUPPORTED
+    assert _v(512, 512, 256, algo="strassen2", tile=128) == ok
+    assert _v(256, 512, 256, algo="strassen2") == fgemm.ERR_UNSUPPORTED
+
+
+def test_swiglu_odd_n_rejected(L):
+    sw = fgemm.make_epilogue("swiglu", 1.0, None)
+    assert fgemm.validate(8, 31, 64, 16, 64, 16, 32, 16, 16, fgemm.BF16, sw, "auto", 0) == \
+        fgemm.ERR_INVALID_ARG
+
+
+# ------------------------------------------------ decision model geometry
+
+def _model(L, sms=152, peak=2250.0, bw=7900.0):
+    m = fgemm.DeviceModel()
+    L.fgemm_model_default(ctypes.byref(m), sms, peak, bw)
+    return m
+
+
+def test_tile_quantization_page_example(L):
+    g = json.load(open(GOLDEN))["tile_quantization"]
+    T = g["tile"]
+    for n, tiles in g["cases"]:
+        assert L.fgemm_model_tiles(n, T, T, T) == tiles          # one dimension
+        assert L.fgemm_model_tiles(n, n, T, T) == tiles * tiles  # square
+
+
+def test_wave_quantization_page_example(L):
+    g = json.load(open(GOLDEN))["wave_quantization"]
+    for c in g["cases"]:
+        tiles = L.fgemm_model_tiles(c["n"], c["n"], g["tile_m"], g["tile_n"])
+        assert tiles == c["tiles"] == c["tiles_m"] * c["tiles_n"]
+        tail = ctypes.c_double()
+        waves = L.fgemm_model_waves(tiles, g["sms"], ctypes.byref(tail))
+        assert waves == c["waves"]
+        if "tail_tiles" in c:
+            assert abs(tail.value - c["tail_tiles"] / g["sms"]) < 1e-12
+            assert abs(tail.value - c["tail_utilization"]) < 1e-4
+
+
+def test_tiled_reads_page_formula(L):
+    g = json.load(open(GOLDEN))["tiled_reads"]
+    for c in g["cases"]:
+        n, t = c["n"], c["t"]
+        assert L.fgemm_model_tiled_reads(n, n, n, t, t) == 2 * n ** 3 / t
+        # the untiled limit (T = 1) reads 2 N^3 elements
+        assert L.fgemm_model_tiled_reads(n, n, n, 1, 1) == 2 * n ** 3
+
+
+def test_roofline_page_examples(L):
+    g = json.load(open(GOLDEN))["roofline"]
+    for c in g["cases"]:
+        got = L.fgemm_model_roofline(c["flops"], c["bytes"], c["peak_flops"], c["bw"])
+        assert abs(got - c["perf"]) <= 1e-9 * c["perf"]
+    r = json.load(open(GOLDEN))["relu_bytes_per_flop"]
+    # ReLU: 1 FLOP per element, read + write of the element
+    for bytes_per_elem, key in ((4, "fp32"), (2, "fp16")):
+        perf = L.fgemm_model_roofline(1.0, 2.0 * bytes_per_elem, 1e30, 1.0)
+        assert abs(1.0 / perf - r[key]) < 1e-12
+
+
+def _predict(L, m, M, N, K, algo, tile, epi=0):
+    us = ctypes.c_double()
+    s = L.fgemm_model_predict(ctypes.byref(m), M, N, K, epi, fgemm.ALGOS[algo], tile, ctypes.byref(us))
+    return s, us.value
+
+
+def test_model_wave_sawtooth_and_monotonicity(L):
+    m = _model(L)
+    # one more tile than the SM count costs a whole extra wave
+    s1, t1 = _predict(L, m, 128 * 152, 256, 4096, "classical", 256)
+    s2, t2 = _predict(L, m, 128 * 153, 256, 4096, "classical", 256)
+    assert s1 == s2 == fgemm.OK
+    assert t2 > 1.8 * (t1 - m.launch_us)
+    # more K never predicts less time
+    prev = 0
+    for K in (512, 1024, 2048, 4096):
+        _, t = _predict(L, m, 4096, 4096, K, "classical", 256)
+        assert t >= prev
+        prev = t
+
+
+def test_model_strassen_tradeoffs(L):
+    m = _model(L)
+    # illegal shapes are reported, never predicted
+    assert _predict(L, m, 384, 256, 128, "strassen1", 128)[0] == fgemm.ERR_UNSUPPORTED
+    # with equal efficiencies and ample L2 bandwidth the 7/8 work wins at
+    # large compute-bound sizes
+    m.l2_gbs = 1e9
+    m.eff_strassen[0][1] = m.eff_classical[2]
+    _, tc = _predict(L, m, 16384, 16384, 16384, "classical", 256)
+    _, ts = _predict(L, m, 16384, 16384, 16384, "strassen1", 256)
+    assert ts < tc
+    # and loses when its mainloop is much slower
+    m.eff_strassen[0][1] = 0.5 * m.eff_classical[2]
+    m.eff_strassen[0][0] = 0.5 * m.eff_classical[1]
+    _, ts = _predict(L, m, 16384, 16384, 16384, "strassen1", 256)
+    assert ts > tc
+    a = ctypes.c_int()
+    tm, tn, us = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+    assert L.fgemm_model_plan(ctypes.byref(m), 16384, 16384, 16384, 0, ctypes.byref(a),
+                              ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
+    assert fgemm.ALGO_NAMES[a.value] == "classical"
+
+
+def test_model_operand_traffic_term(L):
+    # with scarce L2 bandwidth, narrow tiles (which re-read A more often,
+    # tiled reads ~ (128 + tile_n) / (128 * tile_n)) predict more time
+    m = _model(L)
+    m.l2_gbs = 2000.0
+    _, t64 = _predict(L, m, 8192, 8192, 8192, "classical", 64)
+    _, t256 = _predict(L, m, 8192, 8192, 8192, "classical", 256)
+    assert t64 > 1.5 * t256
+    # and Strassen's extra source terms (24 vs 16 per 2x2 block) cost more
+    m.eff_strassen[0][1] = m.eff_classical[2]
+    _, tc = _predict(L, m, 16384, 16384, 16384, "classical", 256)
+    _, ts = _predict(L, m, 16384, 16384, 16384, "strassen1", 256)
+    assert ts > tc
+
+
+def test_model_plan_small_shapes_stay_classical(L):
+    m = _model(L)
+    a = ctypes.c_int()
+    tm, tn, us = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+    for (M, N, K) in [(16, 2048, 2048), (128, 4096, 4096), (256, 256, 256), (1000, 1000, 1000)]:
+        assert L.fgemm_model_plan(ctypes.byref(m), M, N, K, 0, ctypes.byref(a), ctypes.byref(tm),
+                                  ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
+        assert fgemm.ALGO_NAMES[a.value] == "classical"
+        assert tm.value == 128 and tn.value in (64, 128, 256)

@@ -1,0 +1,83 @@
+"""GPU parity at the full workload sizes, on 4096 stratified sampled output
+entries that the oracle computes one by one (K-long fp64 dot products of the
+decoded inputs), through the same binding call the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from complexity_matmul_tcgen05_gb300 import fgemm, inputs
+from parity_util import TOL_NORMWISE, elementwise_ok, gpu_bits, run, ulp
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+DEV = "cuda"
+
+
+def _picked(M, N, K, epi):
+    return fgemm.plan(M, N, K, epilogue=epi)[0]
+
+
+def _sampled_check(name, A, B, bias, run_algo, epi, dtype, tile=0):
+    """Runs `run_algo` and checks 4096 sampled entries against the oracle
+    with the tolerance of the form that actually ran."""
+    M, K = A.shape
+    N = B.shape[1]
+    n_out = N // 2 if epi == "swiglu" else N
+    algo = _picked(M, N, K, epi) if run_algo == "auto" else run_algo
+    depth_blocks = {"classical": 1, "strassen1": 2, "strassen2": 4}[algo]
+    C = run(A, B, algo=run_algo, epilogue=epi, bias=bias, tile_n=tile)
+    rows, cols = inputs.sample_positions(M, n_out, n=4096, row_blocks=depth_blocks,
+                                         col_blocks=depth_blocks)
+    rows, cols = rows.numpy(), cols.numpy()
+    Ab, Bb = gpu_bits(A), gpu_bits(B)
+    bb = None if bias is None else gpu_bits(bias)
+    ref = oracle.reference_sampled(Ab, Bb, dtype, rows, cols, epi, 1.0, bb)
+    got = oracle.decode(gpu_bits(C[torch.as_tensor(rows, device=DEV), torch.as_tensor(cols, device=DEV)]),
+                        dtype)
+    err = float(np.linalg.norm(got - oracle.round_to(ref, dtype)) / np.linalg.norm(ref))
+    kappa = 1.0
+    if epi == "swiglu":
+        g = oracle.gemm_sampled(Ab, Bb, dtype, rows, cols)
+        u = oracle.gemm_sampled(Ab, Bb, dtype, rows, cols + n_out)
+        if bb is not None:
+            bv = oracle.decode(bb, dtype)
+            g, u = g + bv[cols], u + bv[cols + n_out]
+        sig = 1 / (1 + np.exp(-g))
+        silu = g * sig
+        ds = sig * (1 + g * (1 - sig))
+        kappa = float(np.linalg.norm(np.abs(ds * u * g) + np.abs(silu * u)) / np.linalg.norm(silu * u))
+    assert err <= TOL_NORMWISE[algo] * max(1.0, kappa), (name, algo, err, kappa)
+    if algo == "classical" and epi in ("none", "scale_bias"):
+        absdot = oracle.gemm_sampled(Ab & np.uint16(0x7FFF), Bb & np.uint16(0x7FFF), dtype, rows, cols)
+        ok, _ = elementwise_ok(got, ref, absdot, K, dtype)
+        assert ok, name
+    return err
+
+
+@pytest.mark.parametrize("algo", ["auto", "classical"])
+def test_proj_4096_bias(algo):
+    A, B, bias = inputs.workload_inputs("proj_4096_bf16_bias", DEV)
+    _sampled_check("proj_4096", A, B, bias, algo, "scale_bias", "bf16")
+
+
+@pytest.mark.parametrize("algo", ["classical", "strassen1", "auto"])
+def test_ffn_up_swiglu(algo):
+    A, B, _ = inputs.workload_inputs("ffn_up_swiglu_bf16", DEV)
+    _sampled_check("ffn_up", A, B, None, algo, "swiglu", "bf16")
+
+
+@pytest.mark.parametrize("algo", ["classical", "strassen1", "strassen2", "auto"])
+def test_square_16384(algo):
+    A, B, _ = inputs.workload_inputs("square_16384_bf16", DEV)
+    _sampled_check("square_16384", A, B, None, algo, "none", "bf16")
+
+
+@pytest.mark.parametrize("shape", inputs.SWEEP_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_sweep_shapes_every_legal_form(shape):
+    M, N, K = shape
+    A, B = inputs.sweep_inputs(M, N, K, DEV)
+    for algo in ("classical", "strassen1", "strassen2", "auto"):
+        s = fgemm.validate(M, N, K, 16, K, 16, N, 16, N, fgemm.BF16, None, algo, 0)
+        if s == fgemm.ERR_UNSUPPORTED:
+            continue
+        _sampled_check(f"sweep {shape}", A, B, None, algo, "none", "bf16")

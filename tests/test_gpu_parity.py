@@ -1,0 +1,208 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small and mid sizes are checked on every output entry; the full-size
+workloads on 4096 stratified sampled entries computed one by one by the
+oracle, in the same launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from complexity_matmul_tcgen05_gb300 import fgemm, inputs
+from parity_util import (TOL_EMULATED, TOL_NORMWISE, activation_condition, elementwise_ok,
+                         gpu_bits, normwise, run, values)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _ternary(M, N, K, dtype, seed=10):
+    A = inputs.matrix(M, K, "ternary", dtype, seed, DEV)
+    B = inputs.matrix(K, N, "ternary", dtype, seed + 1, DEV)
+    bias = inputs.matrix(1, N, "ternary_bias", dtype, seed + 2, DEV)[0]
+    return A, B, bias
+
+
+def _exact_reference(A, B, bias, dtype):
+    ref = oracle.reference(gpu_bits(A), gpu_bits(B), dtype, "scale_bias", 1.0, gpu_bits(bias))
+    return oracle.encode(ref, dtype)
+
+
+# ------------------------------------------------- exact ternary parity
+
+EXACT_CASES = [
+    # (algo, M, N, K, tile_n)
+    ("classical", 128, 256, 64, 256),
+    ("classical", 128, 128, 64, 128),
+    ("classical", 128, 64, 64, 64),
+    ("classical", 1, 8, 8, 0),
+    ("classical", 200, 328, 136, 256),     # ragged M, N, K tails
+    ("classical", 257, 520, 1032, 128),
+    ("classical", 300, 72, 520, 64),
+    ("classical", 1000, 1000, 1000, 0),
+    ("strassen1", 256, 256, 128, 128),
+    ("strassen1", 256, 512, 128, 256),
+    ("strassen1", 512, 1024, 640, 256),
+    ("strassen2", 512, 512, 256, 128),
+    ("strassen2", 512, 1024, 512, 256),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("algo,M,N,K,tile", EXACT_CASES)
+def test_exact_ternary(algo, M, N, K, tile, dtype):
+    """Inputs in {-1,0,1}, integer bias: every form must equal RNE(exact C) bit for bit."""
+    A, B, bias = _ternary(M, N, K, dtype)
+    C = run(A, B, algo=algo, epilogue="scale_bias", bias=bias, tile_n=tile)
+    assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
+
+
+def test_exact_ternary_strided_and_guard_band():
+    """lda/ldb/ldc larger than the row length; C's padding and rows around it untouched."""
+    M, N, K = 130, 200, 136
+    A0, B0, bias = _ternary(M, N, K, "bf16", seed=20)
+    A = torch.zeros((M, K + 24), dtype=torch.bfloat16, device=DEV)[:, :K]
+    A.copy_(A0)
+    B = torch.zeros((K, N + 56), dtype=torch.bfloat16, device=DEV)[:, :N]
+    B.copy_(B0)
+    canary = 0x7F7B  # a bf16 NaN pattern never produced by the kernel
+    big = torch.full((M + 2, N + 40), canary, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    C = big[1:M + 1, :N]
+    run(A, B, epilogue="scale_bias", bias=bias, out=C, tile_n=128)
+    ref = _exact_reference(A0, B0, bias, "bf16")
+    assert np.array_equal(gpu_bits(C), ref)
+    raw = big.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (raw[0] == canary).all() and (raw[M + 1] == canary).all()
+    assert (raw[1:M + 1, N:] == canary).all()
+
+
+# ----------------------------------------- full-entry tolerance parity
+
+def _full_check(A, B, algo, dtype, epilogue="none", alpha=1.0, bias=None, tile=0, depth=0):
+    """Every entry: normwise bound (scaled by the activation's condition
+    number for SiLU / SwiGLU), the 8-ulp rule for classical without an
+    activation, and for Strassen the tight pin against the oracle's emulated
+    (rounded-operand) Strassen passed through the same epilogue."""
+    C = run(A, B, algo=algo, epilogue=epilogue, alpha=alpha, bias=bias, tile_n=tile)
+    Ab, Bb = gpu_bits(A), gpu_bits(B)
+    bb = None if bias is None else gpu_bits(bias)
+    Av, Bv = oracle.decode(Ab, dtype), oracle.decode(Bb, dtype)
+    bv = None if bb is None else oracle.decode(bb, dtype)
+    raw = oracle.gemm(Av, Bv)
+    ref = oracle.epilogue(raw, epilogue, alpha, bv)
+    c = values(C)
+    err = normwise(c, ref, dtype)
+    kappa = activation_condition(raw, epilogue, alpha, bv)
+    assert err <= TOL_NORMWISE[algo] * max(1.0, kappa), (err, kappa)
+    if algo == "classical" and epilogue in ("none", "scale_bias"):
+        absdot = abs(alpha) * oracle.gemm(np.abs(Av), np.abs(Bv))
+        ok, _ = elementwise_ok(c, ref, absdot, A.shape[1], dtype)
+        assert ok
+    if depth > 0:
+        emu = oracle.epilogue(oracle.strassen_emulated(Av, Bv, depth, dtype), epilogue, alpha, bv)
+        e2 = float(np.linalg.norm(c - oracle.round_to(emu, dtype)) / np.linalg.norm(emu))
+        assert e2 <= TOL_EMULATED * max(1.0, kappa), (e2, kappa)
+    return err
+
+
+@pytest.mark.parametrize("algo,depth", [("classical", 0), ("strassen1", 1)])
+def test_square_256_fp16_every_entry(algo, depth):
+    """fp16 256^3, A,B ~ U[-1,1] (seeds 0,1): all 65536 entries."""
+    A, B, _ = inputs.workload_inputs("square_256_f16", DEV)
+    _full_check(A, B, algo, "f16", depth=depth)
+
+
+@pytest.mark.parametrize("tile", [64, 128, 256])
+@pytest.mark.parametrize("epilogue,alpha", [("none", 1.0), ("scale_bias", 0.5), ("silu", 1.25)])
+def test_classical_epilogues_every_entry(epilogue, alpha, tile):
+    M, N, K = 384, 640, 320
+    A = inputs.matrix(M, K, "normal", "bf16", 0, DEV)
+    B = inputs.matrix(K, N, "normal_inv_k", "bf16", 1, DEV, k=K)
+    bias = inputs.matrix(1, N, "normal_0.02", "bf16", 2, DEV)[0] if epilogue != "none" else None
+    _full_check(A, B, "classical", "bf16", epilogue, alpha, bias, tile)
+
+
+@pytest.mark.parametrize("algo,tile,depth", [("classical", 128, 0), ("classical", 256, 0),
+                                             ("strassen1", 128, 1), ("strassen1", 256, 1),
+                                             ("strassen2", 128, 2)])
+def test_swiglu_every_entry(algo, tile, depth):
+    M, N, K = 512, 2048, 512
+    A = inputs.matrix(M, K, "normal", "bf16", 0, DEV)
+    B = inputs.matrix(K, N, "normal_inv_k", "bf16", 1, DEV, k=K)
+    bias = inputs.matrix(1, N, "normal_0.02", "bf16", 2, DEV)[0]
+    _full_check(A, B, algo, "bf16", "swiglu", 1.0, bias, tile, depth)
+
+
+@pytest.mark.parametrize("algo,tile,depth", [("strassen1", 128, 1), ("strassen1", 256, 1),
+                                             ("strassen2", 128, 2), ("strassen2", 256, 2)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_strassen_every_entry_and_emulation(algo, tile, depth, dtype):
+    """Normwise bound and the tighter pin: GPU Strassen vs the emulated
+    (rounded-operand) Strassen of the oracle."""
+    M, N, K = 512, 1024, 768
+    A = inputs.matrix(M, K, "uniform", dtype, 0, DEV)
+    B = inputs.matrix(K, N, "uniform", dtype, 1, DEV)
+    _full_check(A, B, algo, dtype, tile=tile, depth=depth)
+
+
+# -------------------------------------------------------------- edge cases
+
+def test_empty_and_k_zero():
+    A = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    B = torch.ones((64, 32), dtype=torch.bfloat16, device=DEV)
+    C = run(A, B)
+    assert C.shape == (0, 32)
+    A = torch.empty((5, 0), dtype=torch.bfloat16, device=DEV)
+    B = torch.empty((0, 16), dtype=torch.bfloat16, device=DEV)
+    bias = inputs.matrix(1, 16, "normal", "bf16", 3, DEV)[0]
+    C = run(A, B, epilogue="scale_bias", bias=bias)
+    ref = oracle.encode(np.tile(values(bias), (5, 1)), "bf16")
+    assert np.array_equal(gpu_bits(C), ref)
+
+
+def test_rejections_do_not_launch():
+    h = fgemm.default_handle()
+    A = torch.zeros((128, 72), dtype=torch.bfloat16, device=DEV)
+    B = torch.zeros((72, 64), dtype=torch.bfloat16, device=DEV)
+    C = torch.zeros((128, 64), dtype=torch.bfloat16, device=DEV)
+    s = h.matmul_raw(128, 64, 72, A.data_ptr() + 2, 72, B.data_ptr(), 64, C.data_ptr(), 64, fgemm.BF16)
+    assert s == fgemm.ERR_ALIGNMENT
+    s = h.matmul_raw(128, 64, 72, A.data_ptr(), 72, B.data_ptr(), 64, C.data_ptr(), 64, fgemm.BF16,
+                     None, "strassen1")
+    assert s == fgemm.ERR_UNSUPPORTED
+    s = h.matmul_raw(128, 64, 72, A.data_ptr(), 72, B.data_ptr(), 64, C.data_ptr(), 64, fgemm.BF16,
+                     fgemm.make_epilogue("scale_bias"))
+    assert s == fgemm.ERR_INVALID_ARG
+    assert h.get_error() == fgemm.OK
+
+
+def test_plan_is_legal_and_launchable():
+    for (M, N, K) in [(256, 256, 256), (4096, 4096, 4096), (16, 2048, 2048), (16384, 16384, 16384)]:
+        algo, tile, us = fgemm.plan(M, N, K)
+        assert algo in ("classical", "strassen1", "strassen2") and tile in (64, 128, 256)
+        assert us > 0
+
+
+def test_host_buffers_end_to_end():
+    A = inputs.matrix(256, 128, "ternary", "bf16", 30)
+    B = inputs.matrix(128, 192, "ternary", "bf16", 31)
+    C = fgemm.matmul(A.pin_memory(), B.pin_memory(), algo="classical")
+    assert C.device.type == "cpu"
+    ref = oracle.encode(oracle.gemm(values(A), values(B)), "bf16")
+    assert np.array_equal(gpu_bits(C), ref)
+
+
+def test_two_handles_two_streams():
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    A, B, bias = _ternary(256, 256, 128, "bf16", seed=40)
+    ref = _exact_reference(A, B, bias, "bf16")
+    h2 = fgemm.Handle()
+    with torch.cuda.stream(s1):
+        C1 = fgemm.matmul(A, B, epilogue="scale_bias", bias=bias, algo="strassen1")
+    with torch.cuda.stream(s2):
+        C2 = fgemm.matmul(A, B, epilogue="scale_bias", bias=bias, algo="classical", handle=h2)
+    torch.cuda.synchronize()
+    assert np.array_equal(gpu_bits(C1), ref) and np.array_equal(gpu_bits(C2), ref)
+    assert h2.get_error() == fgemm.OK
+    h2.close()
