@@ -15,7 +15,7 @@
 // Warp roles (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer: raw operand tiles -> shared-memory ring
 //   warp 1      MMA issuer (one thread): tcgen05.mma into TMEM; owns TMEM
-//   warps 2,3   (Strassen) operand-sum warps, with warps 8..11
+//   warps 2,3   (Strassen) operand-sum warps, with warps 8..15
 //   warps 4..7  epilogue: tcgen05.ld -> fp32 math -> rounded stores
 // The TMEM accumulator is double-buffered, so the epilogue of one tile (or
 // product) runs while the MMAs of the next are in flight (the overlap the
@@ -50,8 +50,9 @@ struct TileCfg {
 
 template <int DEPTH>
 struct RoleCfg {
-  static constexpr int kSumWarps = DEPTH == 0 ? 0 : 6;
-  static constexpr int kThreads = DEPTH == 0 ? 256 : 384;
+  // Strassen: warps 2, 3 and 8..15 form operand sums (10 warps).
+  static constexpr int kSumWarps = DEPTH == 0 ? 0 : 10;
+  static constexpr int kThreads = DEPTH == 0 ? 256 : 512;
 };
 
 // ------------------------------------------------------------ small helpers
@@ -323,102 +324,93 @@ __device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8], int is_bf
   }
 }
 
-// Forms sum_t sign_t * src_t over `nchunk` 16-byte chunks (8 elements each),
-// in fp32 with one final round-to-nearest-even, and writes each chunk into
-// the 128-byte-swizzled operand buffer.  `addr(ch, &goff, &soff)` maps a chunk
-// to its element offset from each source base and its shared-memory offset.
-template <typename AddrFn>
-__device__ __forceinline__ void form_sum(const uint16_t* const (&src)[kMaxTerms],
-                                         const float (&sg)[kMaxTerms], int nt, int nchunk,
-                                         int tid, int nthreads, uint8_t* dst, int is_bf16,
-                                         AddrFn addr) {
-  constexpr int U = 4;
+// Forms the product's summed operands for one K block: A sum (128 rows x 64)
+// and/or B sum (64 rows x BN), each element sum_t sign_t * src_t computed in
+// fp32 from the exact 16-bit inputs and rounded once (RNE), written into the
+// 128-byte-swizzled operand buffers.  A and B chunks (16 bytes = 8 elements)
+// form one work list so every thread keeps U chunks x terms loads in flight
+// before it stores anything (the loads come from L2; their latency, not
+// bandwidth, is what limits this stage).
+template <int BN, int DEPTH>
+__device__ __forceinline__ void form_operands(const KernelParams& p, uint8_t* sA, uint8_t* sB,
+                                              int pr, int tm, int tn, int kb, int tid,
+                                              int nthreads) {
+  constexpr int T = 1 << DEPTH;            // terms per formed operand (at most)
+  constexpr int U = DEPTH == 1 ? 8 : 4;    // chunks per thread in flight: U * T loads
+  constexpr int CPR = BN / 8;              // 16-byte chunks per K-row of the B tile
+  const int na = p.tab.na[pr], nb = p.tab.nb[pr];
+  const int nA = na > 1 ? kBM * 8 : 0;
+  const int nB = nb > 1 ? kBK * CPR : 0;
+  const int total = nA + nB;
+  if (total == 0) return;
+  const uint16_t* srcA[T];
+  const uint16_t* srcB[T];
+  float sgA[T], sgB[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    const uint8_t ca = p.tab.a[pr][t < na ? t : 0];
+    const int qa = ca & kTermIndexMask;
+    srcA[t] = p.A + static_cast<long long>((qa >> DEPTH) * p.sub_m + tm * kBM) * p.lda +
+              (qa & (T - 1)) * p.sub_k + kb * kBK;
+    sgA[t] = (ca & kTermNeg) ? -1.0f : 1.0f;
+    const uint8_t cb = p.tab.b[pr][t < nb ? t : 0];
+    const int qb = cb & kTermIndexMask;
+    srcB[t] = p.B + static_cast<long long>((qb >> DEPTH) * p.sub_k + kb * kBK) * p.ldb +
+              (qb & (T - 1)) * p.sub_n + tn * BN;
+    sgB[t] = (cb & kTermNeg) ? -1.0f : 1.0f;
+  }
+  const long long lda = p.lda, ldb = p.ldb;
+  const int is_bf16 = p.is_bf16;
 #pragma unroll 1
-  for (int ch0 = tid; ch0 < nchunk; ch0 += U * nthreads) {
-    uint4 v[U][kMaxTerms];
-    long long goff[U];
+  for (int ch0 = tid; ch0 < total; ch0 += U * nthreads) {
+    uint4 v[U][T];
     uint32_t soff[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int ch = ch0 + u * nthreads;
-      if (ch < nchunk) {
-        addr(ch, goff[u], soff[u]);
+      if (ch < nA) {
+        const int row = ch >> 3, c8 = ch & 7;
+        const long long goff = row * lda + c8 * 8;
+        soff[u] = static_cast<uint32_t>(row * 128 + ((c8 ^ (row & 7)) << 4));
 #pragma unroll
-        for (int t = 0; t < kMaxTerms; ++t)
-          if (t < nt) v[u][t] = __ldg(reinterpret_cast<const uint4*>(src[t] + goff[u]));
+        for (int t = 0; t < T; ++t)
+          if (t < na) v[u][t] = __ldg(reinterpret_cast<const uint4*>(srcA[t] + goff));
+      } else if (ch < total) {
+        const int cb = ch - nA;
+        const int row = cb / CPR, c = cb % CPR;
+        const long long goff = row * ldb + c * 8;
+        soff[u] = static_cast<uint32_t>((c >> 3) * 8192 + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+#pragma unroll
+        for (int t = 0; t < T; ++t)
+          if (t < nb) v[u][t] = __ldg(reinterpret_cast<const uint4*>(srcB[t] + goff));
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int ch = ch0 + u * nthreads;
-      if (ch < nchunk) {
+      if (ch < total) {
+        const bool is_a = ch < nA;
+        const int nt = is_a ? na : nb;
         float acc[8], f[8];
         unpack8(v[u][0], acc, is_bf16);
+        const float s0 = is_a ? sgA[0] : sgB[0];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] *= sg[0];
+        for (int i = 0; i < 8; ++i) acc[i] *= s0;
 #pragma unroll
-        for (int t = 1; t < kMaxTerms; ++t) {
+        for (int t = 1; t < T; ++t) {
           if (t < nt) {
+            const float st = is_a ? sgA[t] : sgB[t];
             unpack8(v[u][t], f, is_bf16);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] += sg[t] * f[i];
+            for (int i = 0; i < 8; ++i) acc[i] += st * f[i];
           }
         }
-        *reinterpret_cast<uint4*>(dst + soff[u]) =
+        *reinterpret_cast<uint4*>((is_a ? sA : sB) + soff[u]) =
             make_uint4(pack2(acc[0], acc[1], is_bf16), pack2(acc[2], acc[3], is_bf16),
                        pack2(acc[4], acc[5], is_bf16), pack2(acc[6], acc[7], is_bf16));
       }
     }
   }
-}
-
-template <int DEPTH>
-__device__ __forceinline__ void form_a(const KernelParams& p, uint8_t* sA, int pr, int tm, int kb,
-                                       int tid, int nthreads) {
-  const int nt = p.tab.na[pr];
-  const uint16_t* src[kMaxTerms];
-  float sg[kMaxTerms];
-#pragma unroll
-  for (int t = 0; t < kMaxTerms; ++t) {
-    const uint8_t code = p.tab.a[pr][t < nt ? t : 0];
-    const int q = code & kTermIndexMask;
-    const int br = q >> DEPTH, bc = q & ((1 << DEPTH) - 1);
-    src[t] = p.A + static_cast<long long>(br * p.sub_m + tm * kBM) * p.lda + bc * p.sub_k + kb * kBK;
-    sg[t] = (code & kTermNeg) ? -1.0f : 1.0f;
-  }
-  const long long lda = p.lda;
-  // 128 rows x 8 chunks; row r, chunk c8 -> swizzled 16-byte slot c8 ^ (r & 7)
-  form_sum(src, sg, nt, kBM * 8, tid, nthreads, sA, p.is_bf16,
-           [lda](int ch, long long& goff, uint32_t& soff) {
-             const int row = ch >> 3, c8 = ch & 7;
-             goff = row * lda + c8 * 8;
-             soff = static_cast<uint32_t>(row * 128 + ((c8 ^ (row & 7)) << 4));
-           });
-}
-
-template <int BN, int DEPTH>
-__device__ __forceinline__ void form_b(const KernelParams& p, uint8_t* sB, int pr, int tn, int kb,
-                                       int tid, int nthreads) {
-  const int nt = p.tab.nb[pr];
-  const uint16_t* src[kMaxTerms];
-  float sg[kMaxTerms];
-#pragma unroll
-  for (int t = 0; t < kMaxTerms; ++t) {
-    const uint8_t code = p.tab.b[pr][t < nt ? t : 0];
-    const int q = code & kTermIndexMask;
-    const int br = q >> DEPTH, bc = q & ((1 << DEPTH) - 1);
-    src[t] = p.B + static_cast<long long>(br * p.sub_k + kb * kBK) * p.ldb + bc * p.sub_n + tn * BN;
-    sg[t] = (code & kTermNeg) ? -1.0f : 1.0f;
-  }
-  const long long ldb = p.ldb;
-  constexpr int CPR = BN / 8;  // 16-byte chunks per K-row of the tile
-  // K-row r, chunk c -> box c / 8 (64 columns each), swizzled slot (c % 8) ^ (r & 7)
-  form_sum(src, sg, nt, kBK * CPR, tid, nthreads, sB, p.is_bf16,
-           [ldb](int ch, long long& goff, uint32_t& soff) {
-             const int row = ch / CPR, c = ch % CPR;
-             goff = row * ldb + c * 8;
-             soff = static_cast<uint32_t>((c >> 3) * 8192 + row * 128 + (((c & 7) ^ (row & 7)) << 4));
-           });
 }
 
 // ---------------------------------------------------------------- kernel
@@ -637,9 +629,10 @@ __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
             ok = false;
             break;
           }
-          if (a_sum) form_a<DEPTH>(p, base_ptr + s * TC::kABytes, pr, tm, kb, tid, NT);
-          if (b_sum)
-            form_b<BN, DEPTH>(p, base_ptr + S * TC::kABytes + s * TC::kBBytes, pr, tn, kb, tid, NT);
+          if (a_sum || b_sum)
+            form_operands<BN, DEPTH>(p, base_ptr + s * TC::kABytes,
+                                     base_ptr + S * TC::kABytes + s * TC::kBBytes, pr, tm, tn, kb,
+                                     tid, NT);
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(full(s));
