@@ -24,6 +24,7 @@ SOURCES = [
     "fgemm_kern_classical.cu",
     "fgemm_kern_strassen1.cu",
     "fgemm_kern_strassen2.cu",
+    "fgemm_static.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,

@@ -210,6 +210,14 @@ struct Plan {
 
 }  // namespace
 
+namespace fgemm {
+// Read-only access to the coefficient tables and the tensor-map encoder for
+// other host translation units.
+const StrassenTable& strassen_table(int depth) { return table_for(depth); }
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return get_encode_fn(); }
+void set_thread_message(const std::string& text) { g_thread_msg = text; }
+}  // namespace fgemm
+
 struct fgemm_handle_s {
   int device = 0;
   int num_sms = 0;

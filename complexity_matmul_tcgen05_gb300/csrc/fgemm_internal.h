@@ -74,6 +74,9 @@ int kernel_threads(int depth);
 cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, int grid,
                         cudaStream_t stream);
 
+// The Strassen coefficient table of `depth` levels (0: one trivial product).
+const StrassenTable& strassen_table(int depth);
+
 // C[i][j] = epi(bias[j]) for K == 0 (the product is empty).
 cudaError_t launch_k0_fill(const KernelParams& p, cudaStream_t stream);
 

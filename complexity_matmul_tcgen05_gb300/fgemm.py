@@ -95,12 +95,15 @@ def lib() -> ctypes.CDLL:
         L.fgemm_model_plan.argtypes = [model_p, i64, i64, i64, i32, ctypes.POINTER(st),
                                        ctypes.POINTER(i32), ctypes.POINTER(i32),
                                        ctypes.POINTER(ctypes.c_double)]
+        L.fgemm_strassen_matmul_static.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, st,
+                                                   epi_p, i32, i32, vp]
         L.fgemm_get_device_model.argtypes = [vp, model_p]
         L.fgemm_set_device_model.argtypes = [vp, model_p]
         for name in ("fgemm_create", "fgemm_destroy", "fgemm_set_stream", "fgemm_matmul",
                      "fgemm_matmul_ex", "fgemm_plan", "fgemm_get_error", "fgemm_calibrate",
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
-                     "fgemm_get_device_model", "fgemm_set_device_model"):
+                     "fgemm_get_device_model", "fgemm_set_device_model",
+                     "fgemm_strassen_matmul_static"):
             getattr(L, name).restype = st
         _lib = L
         return L

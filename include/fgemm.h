@@ -183,6 +183,41 @@ fgemm_status_t fgemm_validate(int64_t M, int64_t N, int64_t K, const void* A,
                               const fgemm_epilogue_t* epi, fgemm_algo_t algo,
                               int32_t tile_n);
 
+/*
+ * Strassen product (depth 1 or 2) that allocates no device memory. The paper
+ * has no counterpart; it exists for callers that may not call cudaMalloc:
+ * code running under a framework whose pool owns all device memory, serving
+ * loops that must not pay cudaMalloc's implicit device synchronisation, or
+ * plug-ins that are handed nothing but buffers and a stream.
+ *
+ * It computes what fgemm_matmul_ex(..., FGEMM_ALGO_STRASSEN1 or 2, tile_n)
+ * computes, with no handle: the scratch it needs (the kernel's error word and
+ * the fp32 partial tiles of the Strassen combination) lives in a 64 MiB
+ * array built into the library, which every device that loads the library
+ * keeps until the process exits.
+ *   depth      1 or 2.   tile_n  128 or 256 (0 = 128).
+ *   cuda_stream  the cudaStream_t (as void*) to enqueue on; NULL = legacy.
+ *   other arguments, layouts, alignment and legality: as fgemm_matmul_ex.
+ * Limit: the launch uses min(tiles, SMs) CTAs, each needing 4^depth partial
+ * tiles of 128 x tile_n floats (depth 1: 256 KiB at tile_n 128, 512 KiB at
+ * 256; depth 2: 1 or 2 MiB). A product that needs more than the array's
+ * 64 MiB returns FGEMM_ERR_UNSUPPORTED (message: how much it needs) before
+ * anything is enqueued.
+ * The first call on each device finds the array's device address
+ * (cudaGetSymbolAddress, which loads the library's device code): make that
+ * first call before capturing a stream. Every call shares the one array and
+ * leaves its contents behind; calls whose kernels overlap on the GPU (other
+ * streams, or other host threads) race on it and must be serialised by the
+ * caller. A bounded wait that runs out inside the kernel (it does not happen
+ * unless the GPU stalls for about a second) leaves C incomplete and is not
+ * reported by this call.
+ */
+fgemm_status_t fgemm_strassen_matmul_static(
+    int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+    int64_t ldb, void* C, int64_t ldc, fgemm_dtype_t dtype,
+    const fgemm_epilogue_t* epi, int32_t depth, int32_t tile_n,
+    void* cuda_stream);
+
 /* ------------------------------------------------------------------------
  * Decision model, host only (no device needed). FalconGEMM summary,
  * "Methodology" item 4 (analytical runtime model: compute throughput, memory
