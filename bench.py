@@ -53,7 +53,8 @@ def parse():
     ap.add_argument("--impl", default="fgemm", choices=["fgemm", "reference"])
     ap.add_argument("--workload", default="proj_4096_bf16_bias")
     ap.add_argument("--algo", default="auto")
-    ap.add_argument("--tile", type=int, default=0)
+    ap.add_argument("--tile", type=int, default=0, help="tile_n (0 = model)")
+    ap.add_argument("--tile-m", type=int, default=0, help="tile_m: 128 one CTA, 256 CTA pair")
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0 = auto)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -191,7 +192,7 @@ def kernel_source_hash():
     return h.hexdigest()[:12]
 
 
-def ncu_traffic(workload, algo, tile):
+def ncu_traffic(workload, algo, tile_m, tile):
     """DRAM bytes per launch recorded under profiles/ for this workload, if
     the counters were taken on the current kernel sources."""
     pdir = os.path.join(ROOT, "profiles")
@@ -199,7 +200,7 @@ def ncu_traffic(workload, algo, tile):
         return None
     want = kernel_source_hash()
     pat = re.compile(r"traffic_bytes_per_launch\s*:\s*(\d+)\s+workload=(\S+)\s+algo=(\S+)\s+"
-                     r"tile=(\d+)\s+sources=(\w+)")
+                     r"tile=(\d+)x(\d+)\s+sources=(\w+)")
     for f in sorted(os.listdir(pdir)):
         if not f.endswith((".md", ".txt")):
             continue
@@ -207,7 +208,8 @@ def ncu_traffic(workload, algo, tile):
             for line in fh:
                 m = pat.search(line)
                 if m and m.group(2) == workload and m.group(3) == algo and \
-                        int(m.group(4)) == tile and m.group(5) == want:
+                        int(m.group(4)) == tile_m and int(m.group(5)) == tile and \
+                        m.group(6) == want:
                     return int(m.group(1))
     return None
 
@@ -295,16 +297,16 @@ def run_fgemm(args, rank, world):
         Cs.append(torch.empty((M, n_out), dtype=A0.dtype, device=dev))
     handle = fgemm.default_handle()
     stream = torch.cuda.current_stream(dev)
-    algo, tile = args.algo, args.tile
+    algo, tile, tile_m = args.algo, args.tile, args.tile_m
     if algo == "auto":
-        plan_algo, plan_tile, pred_us = handle.plan(M, N, K, fgemm._dtype_code(A0.dtype),
-                                                    fgemm.make_epilogue(epi))
+        plan_algo, plan_tm, plan_tile, pred_us = handle.plan(M, N, K, fgemm._dtype_code(A0.dtype),
+                                                             fgemm.make_epilogue(epi))
     else:
-        plan_algo, plan_tile, pred_us = algo, tile, None
+        plan_algo, plan_tm, plan_tile, pred_us = algo, tile_m, tile, None
 
     def step(i):
         fgemm.matmul(As[i % sets], Bs[i % sets], out=Cs[i % sets], epilogue=epi,
-                     bias=biases[i % sets], algo=algo, tile_n=tile, handle=handle)
+                     bias=biases[i % sets], algo=algo, tile_n=tile, tile_m=tile_m, handle=handle)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -353,7 +355,7 @@ def run_fgemm(args, rank, world):
             if dbias is not None:
                 dbias.copy_(hbias, non_blocking=True)
             fgemm.matmul(dA, dB, out=dC, epilogue=epi, bias=dbias, algo=algo, tile_n=tile,
-                         handle=handle)
+                         tile_m=tile_m, handle=handle)
             hC.copy_(dC, non_blocking=True)
 
         for _ in range(2):
@@ -379,7 +381,7 @@ def run_fgemm(args, rank, world):
     executed = achieved * (7.0 / 8.0) ** {"classical": 0, "strassen1": 1, "strassen2": 2}[plan_algo]
     roof = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": UNIT,
             "frac": achieved / burst if burst else None,
-            "traffic": ncu_traffic(args.workload, plan_algo, plan_tile),
+            "traffic": ncu_traffic(args.workload, plan_algo, plan_tm, plan_tile),
             "peak_source": f"{src} bf16 dense (burst)", "executed_tflops": executed,
             "kernel_ms": kern_avg_ms}
     line = {
@@ -388,7 +390,7 @@ def run_fgemm(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dtype == "bf16" else "f16",
         "data": "synthetic",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K, "epilogue": epi,
-                   "algo": plan_algo, "tile_m": 128, "tile_n": plan_tile,
+                   "algo": plan_algo, "tile_m": plan_tm, "tile_n": plan_tile,
                    "predicted_us": pred_us, "l2": f"{sets} rotating input/output sets "
                    f"({sets * set_bytes / 2 ** 20:.0f} MiB) cycled between steps",
                    "parallelism": f"replicas x{world}"},

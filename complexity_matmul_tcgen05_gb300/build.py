@@ -25,6 +25,7 @@ SOURCES = [
     "fgemm_kern_strassen1.cu",
     "fgemm_kern_strassen2.cu",
     "fgemm_static.cu",
+    "fgemm_kern_pair.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,

@@ -23,7 +23,7 @@
 
 namespace fgemm {
 bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo_t algo,
-                   int32_t tile_n);
+                   int32_t tile_m, int32_t tile_n);
 }
 
 using fgemm::KernelParams;
@@ -188,9 +188,10 @@ struct TmapKeyHash {
 
 struct PlanKey {
   int64_t M, N, K;
-  int32_t epi, algo, tile;
+  int32_t epi, algo, tile_m, tile_n;
   bool operator==(const PlanKey& o) const {
-    return M == o.M && N == o.N && K == o.K && epi == o.epi && algo == o.algo && tile == o.tile;
+    return M == o.M && N == o.N && K == o.K && epi == o.epi && algo == o.algo &&
+           tile_m == o.tile_m && tile_n == o.tile_n;
   }
 };
 struct PlanKeyHash {
@@ -198,12 +199,13 @@ struct PlanKeyHash {
     size_t h = std::hash<int64_t>()(k.M);
     h = h * 1000003u ^ std::hash<int64_t>()(k.N);
     h = h * 1000003u ^ std::hash<int64_t>()(k.K);
-    h = h * 1000003u ^ static_cast<size_t>(k.epi * 64 + k.algo * 8 + (k.tile >> 6));
+    h = h * 1000003u ^ static_cast<size_t>(k.epi * 512 + k.algo * 64 + (k.tile_m >> 4) + (k.tile_n >> 6));
     return h;
   }
 };
 struct Plan {
   fgemm_algo_t algo;
+  int32_t tile_m;
   int32_t tile_n;
   double predicted_us;
 };
@@ -277,8 +279,8 @@ fgemm_status_t encode_tmap(fgemm_handle_t h, CUtensorMap* out, const void* ptr, 
 // The checks fgemm_matmul_ex makes before launching (see fgemm.h).
 fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                         int64_t ldb, const void* C, int64_t ldc, fgemm_dtype_t dtype,
-                        const fgemm_epilogue_t* epi, fgemm_algo_t algo, int32_t tile_n,
-                        std::string* msg) {
+                        const fgemm_epilogue_t* epi, fgemm_algo_t algo, int32_t tile_m,
+                        int32_t tile_n, std::string* msg) {
   const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
   if (dtype != FGEMM_F16 && dtype != FGEMM_BF16)
     return fail(msg, FGEMM_ERR_INVALID_ARG, "dtype must be FGEMM_F16 or FGEMM_BF16");
@@ -288,6 +290,8 @@ fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     return fail(msg, FGEMM_ERR_INVALID_ARG, "unknown algorithm");
   if (tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 256)
     return fail(msg, FGEMM_ERR_INVALID_ARG, "tile_n must be 0, 64, 128 or 256");
+  if (tile_m != 0 && tile_m != 128 && tile_m != 256)
+    return fail(msg, FGEMM_ERR_INVALID_ARG, "tile_m must be 0, 128 or 256");
   if (M < 0 || N < 0 || K < 0) return fail(msg, FGEMM_ERR_INVALID_ARG, "negative dimension");
   const int64_t kMax = (int64_t{1} << 31) - 1;
   if (M > kMax || N > kMax || K > kMax)
@@ -314,50 +318,51 @@ fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     return fail(msg, FGEMM_ERR_ALIGNMENT, "lda and ldb must be multiples of 8 elements");
   if (kind == FGEMM_EPI_SWIGLU && (N % 16) != 0)
     return fail(msg, FGEMM_ERR_ALIGNMENT, "SWIGLU needs N a multiple of 16 (up half 16-byte aligned)");
-  if (algo != FGEMM_ALGO_AUTO) {
-    const int32_t t = tile_n;
-    if (t != 0) {
-      if (!fgemm::form_is_legal(M, N, K, kind, algo, t))
-        return fail(msg, FGEMM_ERR_UNSUPPORTED, "forced form/tile is not legal for this shape");
-    } else {
-      bool any = false;
-      for (int32_t c : {64, 128, 256}) any = any || fgemm::form_is_legal(M, N, K, kind, algo, c);
-      if (!any)
-        return fail(msg, FGEMM_ERR_UNSUPPORTED,
-                    "Strassen form needs M, N, K divisible into 2^d blocks of whole tiles");
+  if (algo != FGEMM_ALGO_AUTO || tile_m != 0 || tile_n != 0) {
+    bool any = false;
+    for (fgemm_algo_t a : {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2}) {
+      if (algo != FGEMM_ALGO_AUTO && a != algo) continue;
+      for (int32_t tm : {128, 256}) {
+        if (tile_m != 0 && tm != tile_m) continue;
+        for (int32_t tn : {64, 128, 256}) {
+          if (tile_n != 0 && tn != tile_n) continue;
+          any = any || fgemm::form_is_legal(M, N, K, kind, a, tm, tn);
+        }
+      }
     }
+    if (!any)
+      return fail(msg, FGEMM_ERR_UNSUPPORTED,
+                  "no legal form/tile: Strassen forms need M, N, K divisible into 2^d blocks of "
+                  "whole 128 x tile_n x 64 tiles; 256-row tiles are classical only; SWIGLU needs "
+                  "tile_n >= 128");
   }
   return FGEMM_OK;
 }
 
 fgemm_status_t choose_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, int32_t kind,
-                           fgemm_algo_t algo, int32_t tile_n, Plan* out) {
-  PlanKey key{M, N, K, kind, static_cast<int32_t>(algo), tile_n};
+                           fgemm_algo_t algo, int32_t tile_m, int32_t tile_n, Plan* out) {
+  PlanKey key{M, N, K, kind, static_cast<int32_t>(algo), tile_m, tile_n};
   auto it = h->plans.find(key);
   if (it != h->plans.end()) {
     *out = it->second;
     return FGEMM_OK;
   }
-  Plan p{algo, tile_n, 0.0};
-  if (algo == FGEMM_ALGO_AUTO) {
-    int32_t tm = 0, tn = 0;
-    fgemm_status_t s = fgemm_model_plan(&h->model, M, N, K, kind, &p.algo, &tm, &tn, &p.predicted_us);
-    if (s != FGEMM_OK) return set_msg(h, s, "decision model found no legal form");
-    p.tile_n = tn;
-  } else if (tile_n == 0) {
-    double best = INFINITY;
-    for (int32_t c : {64, 128, 256}) {
-      double us;
-      if (fgemm_model_predict(&h->model, M, N, K, kind, algo, c, &us) == FGEMM_OK && us < best) {
-        best = us;
-        p.tile_n = c;
+  Plan p{FGEMM_ALGO_CLASSICAL, 0, 0, INFINITY};
+  for (fgemm_algo_t a : {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2}) {
+    if (algo != FGEMM_ALGO_AUTO && a != algo) continue;
+    for (int32_t tm : {128, 256}) {
+      if (tile_m != 0 && tm != tile_m) continue;
+      for (int32_t tn : {64, 128, 256}) {
+        if (tile_n != 0 && tn != tile_n) continue;
+        double us;
+        if (fgemm_model_predict(&h->model, M, N, K, kind, a, tm, tn, &us) == FGEMM_OK &&
+            us < p.predicted_us) {
+          p = Plan{a, tm, tn, us};
+        }
       }
     }
-    if (p.tile_n == 0) return set_msg(h, FGEMM_ERR_UNSUPPORTED, "no legal tile for this form");
-    p.predicted_us = best;
-  } else {
-    fgemm_model_predict(&h->model, M, N, K, kind, algo, tile_n, &p.predicted_us);
   }
+  if (p.tile_n == 0) return set_msg(h, FGEMM_ERR_UNSUPPORTED, "no legal form/tile for this shape");
   if (h->plans.size() > 4096) h->plans.clear();
   h->plans.emplace(key, p);
   *out = p;
@@ -421,7 +426,8 @@ fgemm_status_t load_calibration(fgemm_handle_t h, const char* path) {
   } fields[] = {
       {"peak_tflops", &m.peak_tflops},         {"hbm_gbs", &m.hbm_gbs},
       {"eff_classical_64", &m.eff_classical[0]}, {"eff_classical_128", &m.eff_classical[1]},
-      {"eff_classical_256", &m.eff_classical[2]}, {"eff_strassen1_128", &m.eff_strassen[0][0]},
+      {"eff_classical_256", &m.eff_classical[2]}, {"eff_pair_128", &m.eff_pair[0]},
+      {"eff_pair_256", &m.eff_pair[1]},         {"eff_strassen1_128", &m.eff_strassen[0][0]},
       {"eff_strassen1_256", &m.eff_strassen[0][1]}, {"eff_strassen2_128", &m.eff_strassen[1][0]},
       {"eff_strassen2_256", &m.eff_strassen[1][1]}, {"launch_us", &m.launch_us},
       {"tile_fill_us", &m.tile_fill_us},        {"l2_bytes", &m.l2_bytes},
@@ -464,9 +470,10 @@ const char* fgemm_last_message(fgemm_handle_t h) {
 fgemm_status_t fgemm_validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                               const void* B, int64_t ldb, const void* C, int64_t ldc,
                               fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
-                              int32_t tile_n) {
+                              int32_t tile_m, int32_t tile_n) {
   std::string msg;
-  fgemm_status_t s = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_n, &msg);
+  fgemm_status_t s =
+      validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_m, tile_n, &msg);
   g_thread_msg = msg;
   return s;
 }
@@ -558,10 +565,10 @@ fgemm_status_t fgemm_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, fge
     return set_msg(h, FGEMM_ERR_INVALID_ARG, "dtype must be FGEMM_F16 or FGEMM_BF16");
   const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
   Plan p;
-  fgemm_status_t s = choose_plan(h, M, N, K, kind, FGEMM_ALGO_AUTO, 0, &p);
+  fgemm_status_t s = choose_plan(h, M, N, K, kind, FGEMM_ALGO_AUTO, 0, 0, &p);
   if (s != FGEMM_OK) return s;
   if (algo_out) *algo_out = p.algo;
-  if (tile_m) *tile_m = fgemm::kBM;
+  if (tile_m) *tile_m = p.tile_m;
   if (tile_n) *tile_n = p.tile_n;
   if (predicted_us) *predicted_us = p.predicted_us;
   return FGEMM_OK;
@@ -570,9 +577,10 @@ fgemm_status_t fgemm_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, fge
 fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
                                int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
                                fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
-                               int32_t tile_n) {
+                               int32_t tile_m, int32_t tile_n) {
   if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
-  fgemm_status_t s = validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_n, &h->msg);
+  fgemm_status_t s =
+      validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_m, tile_n, &h->msg);
   if (s != FGEMM_OK) return s;
   const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
   const int64_t n_out = kind == FGEMM_EPI_SWIGLU ? N / 2 : N;
@@ -603,15 +611,16 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
   }
 
   Plan plan;
-  s = choose_plan(h, M, N, K, kind, algo, algo == FGEMM_ALGO_AUTO ? 0 : tile_n, &plan);
+  s = choose_plan(h, M, N, K, kind, algo, tile_m, tile_n, &plan);
   if (s != FGEMM_OK) return s;
   const int d = depth_of(plan.algo);
   const int bn = plan.tile_n;
+  const int bm = plan.tile_m;  // 256: CTA pair
 
   p.sub_m = static_cast<int>(M >> d);
   p.sub_n = static_cast<int>(N >> d);
   p.sub_k = static_cast<int>(K >> d);
-  p.tiles_m = static_cast<int>((p.sub_m + fgemm::kBM - 1) / fgemm::kBM);
+  p.tiles_m = static_cast<int>((p.sub_m + bm - 1) / bm);
   if (d == 0 && kind == FGEMM_EPI_SWIGLU)
     p.tiles_n = static_cast<int>((n_out + bn / 2 - 1) / (bn / 2));
   else
@@ -622,8 +631,10 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
   p.k_blocks = (p.sub_k + fgemm::kBK - 1) / fgemm::kBK;
   p.raster_group = 8;
   const uint32_t fmt = p.is_bf16 ? 1u : 0u;
+  // tcgen05 instruction descriptor: fp32 accumulator, A/B fp16 (0) or bf16
+  // (1), A K-major, B MN-major, N >> 3, M >> 4 (M = 256 on a CTA pair)
   p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (1u << 16) |
-            (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>(fgemm::kBM >> 4) << 24);
+            (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>(bm >> 4) << 24);
   p.num_products = d == 0 ? 1 : (d == 1 ? 7 : 49);
   p.tab = table_for(d);
 
@@ -634,6 +645,11 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
                   static_cast<uint64_t>(ldb), fgemm::kBK, p.is_bf16);
   if (s != FGEMM_OK) return s;
 
+  if (bm == 256) {
+    cudaError_t e = fgemm::launch_gemm_pair(bn, p, h->num_sms / 2, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "GEMM pair kernel launch");
+    return FGEMM_OK;
+  }
   const int grid = static_cast<int>(std::min<long long>(units, h->num_sms));
   if (d > 0) {
     const size_t per_cta = (size_t{1} << (2 * d)) * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float);
@@ -649,7 +665,7 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
 fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
                             int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
                             fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo) {
-  return fgemm_matmul_ex(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, 0);
+  return fgemm_matmul_ex(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, 0, 0);
 }
 
 fgemm_status_t fgemm_get_error(fgemm_handle_t h) {
@@ -702,11 +718,13 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
     if (e != cudaSuccess && status == FGEMM_OK) status = cuda_fail(h, e, what);
     return e == cudaSuccess;
   };
-  auto time_gemm = [&](int64_t M, int64_t N, int64_t K, fgemm_algo_t algo, int32_t tile, double* us) {
+  auto time_gemm = [&](int64_t M, int64_t N, int64_t K, fgemm_algo_t algo, int32_t tm, int32_t tile,
+                       double* us) {
     const int reps = 3;
     for (int r = 0; r < reps + 1; ++r) {
       if (r == 1) check(cudaEventRecord(e0, h->stream), "cudaEventRecord");
-      fgemm_status_t s = fgemm_matmul_ex(h, M, N, K, A, K, B, N, C, N, FGEMM_BF16, nullptr, algo, tile);
+      fgemm_status_t s =
+          fgemm_matmul_ex(h, M, N, K, A, K, B, N, C, N, FGEMM_BF16, nullptr, algo, tm, tile);
       if (s != FGEMM_OK) {
         if (status == FGEMM_OK) status = s;
         return false;
@@ -734,13 +752,19 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
     const int32_t tiles[3] = {64, 128, 256};
     for (int i = 0; i < 3 && status == FGEMM_OK; ++i) {
       double us = 0;
-      if (!time_gemm(n, n, n, FGEMM_ALGO_CLASSICAL, tiles[i], &us)) break;
+      if (!time_gemm(n, n, n, FGEMM_ALGO_CLASSICAL, 128, tiles[i], &us)) break;
       m.eff_classical[i] = flops / (us * 1e6) / m.peak_tflops;
+    }
+    for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
+      double us = 0;
+      if (!time_gemm(n, n, n, FGEMM_ALGO_CLASSICAL, 256, tiles[i + 1], &us)) break;
+      m.eff_pair[i] = flops / (us * 1e6) / m.peak_tflops;
     }
     for (int d = 1; d <= 2 && status == FGEMM_OK; ++d) {
       for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
         double us = 0;
-        if (!time_gemm(n, n, n, d == 1 ? FGEMM_ALGO_STRASSEN1 : FGEMM_ALGO_STRASSEN2, i == 0 ? 128 : 256, &us))
+        if (!time_gemm(n, n, n, d == 1 ? FGEMM_ALGO_STRASSEN1 : FGEMM_ALGO_STRASSEN2, 128,
+                       i == 0 ? 128 : 256, &us))
           break;
         const double executed = flops * std::pow(7.0 / 8.0, d);
         m.eff_strassen[d - 1][i] = executed / (us * 1e6) / m.peak_tflops;
@@ -749,7 +773,7 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
     if (status != FGEMM_OK) break;
     {  // launch + fill: one tiny tile
       double us = 0;
-      if (!time_gemm(128, 128, 64, FGEMM_ALGO_CLASSICAL, 128, &us)) break;
+      if (!time_gemm(128, 128, 64, FGEMM_ALGO_CLASSICAL, 128, 128, &us)) break;
       m.launch_us = us;
       m.tile_fill_us = std::max(0.2, us * 0.25);
     }
@@ -782,12 +806,13 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
     std::fprintf(f,
                  "{\n  \"num_sms\": %d,\n  \"peak_tflops\": %.3f,\n  \"hbm_gbs\": %.3f,\n"
                  "  \"eff_classical_64\": %.5f,\n  \"eff_classical_128\": %.5f,\n"
-                 "  \"eff_classical_256\": %.5f,\n  \"eff_strassen1_128\": %.5f,\n"
+                 "  \"eff_classical_256\": %.5f,\n  \"eff_pair_128\": %.5f,\n"
+                 "  \"eff_pair_256\": %.5f,\n  \"eff_strassen1_128\": %.5f,\n"
                  "  \"eff_strassen1_256\": %.5f,\n  \"eff_strassen2_128\": %.5f,\n"
                  "  \"eff_strassen2_256\": %.5f,\n  \"launch_us\": %.3f,\n  \"tile_fill_us\": %.3f,\n"
                  "  \"l2_bytes\": %.0f,\n  \"l2_gbs\": %.1f\n}\n",
                  m.num_sms, m.peak_tflops, m.hbm_gbs, m.eff_classical[0], m.eff_classical[1],
-                 m.eff_classical[2], m.eff_strassen[0][0], m.eff_strassen[0][1], m.eff_strassen[1][0],
+                 m.eff_classical[2], m.eff_pair[0], m.eff_pair[1], m.eff_strassen[0][0], m.eff_strassen[0][1], m.eff_strassen[1][0],
                  m.eff_strassen[1][1], m.launch_us, m.tile_fill_us, m.l2_bytes, m.l2_gbs);
     std::fclose(f);
   }

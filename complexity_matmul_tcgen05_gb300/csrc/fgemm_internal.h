@@ -50,7 +50,7 @@ struct KernelParams {
   int M, N, K;            // virtual GEMM: A is M x K, B is K x N
   int n_out;              // columns of C (N, or N/2 for SwiGLU)
   int sub_m, sub_n, sub_k;  // block sizes of one product (M, N, K >> depth)
-  int tiles_m, tiles_n;   // output tile grid of one product
+  int tiles_m, tiles_n;   // output tile grid of one product (256-row tiles on CTA pairs)
   int num_units;          // tiles_m * tiles_n
   int k_blocks;           // ceil(sub_k / 64)
   int epi;                // EpiKind
@@ -73,6 +73,10 @@ int kernel_threads(int depth);
 // Strassen depth (0 = classical) with `grid` CTAs on `stream`.
 cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, int grid,
                         cudaStream_t stream);
+
+// Classical kernel on CTA pairs: 256 x bn tiles (bn = 128 or 256), at most
+// `max_clusters` pairs (fewer if fewer fit on the device at once).
+cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int max_clusters, cudaStream_t stream);
 
 // The Strassen coefficient table of `depth` levels (0: one trivial product).
 const StrassenTable& strassen_table(int depth);

@@ -1,0 +1,16 @@
+// Classical instantiations on CTA pairs (256-row tiles, tcgen05 cta_group::2).
+#include <algorithm>
+
+#include "fgemm_kernel_pair.cuh"
+
+namespace fgemm {
+
+cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int max_clusters, cudaStream_t stream) {
+  switch (bn) {
+    case 128: return launch_gemm_pair_t<128>(p, max_clusters, stream);
+    case 256: return launch_gemm_pair_t<256>(p, max_clusters, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fgemm

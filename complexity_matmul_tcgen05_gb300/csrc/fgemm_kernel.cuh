@@ -185,9 +185,9 @@ __device__ __forceinline__ void finish_swiglu(const KernelParams& p, int col0, f
 // SwiGLU the tile's first BN/2 columns hold gate columns and the last BN/2
 // the matching up columns (the producer loads them side by side).
 template <int BN>
-__device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32_t tbase, int tm,
+__device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32_t tbase, int row0,
                                                    int tn, int r) {
-  const int row = tm * kBM + r;
+  const int row = row0 + r;
   const bool row_ok = row < p.M;
   if (p.epi == kEpiSwiglu) {
     constexpr int HALF = BN / 2;
@@ -601,7 +601,7 @@ __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * BN;
         if constexpr (DEPTH == 0) {
-          epilogue_classical<BN>(p, tbase, tm, tn, r);
+          epilogue_classical<BN>(p, tbase, tm * kBM, tn, r);
         } else {
           epilogue_strassen<BN, DEPTH>(p, tbase, tm, tn, pr, r, ws);
         }

@@ -7,13 +7,14 @@
 // made at run time from the actual (M, N, K).
 //
 // The estimate for one (form, tile_n) candidate:
-//   tiles        = tile quantization of the output of one product: ceil(m/128)
-//                  * ceil(n/tile_n)  (CS336 Lecture 05 notes, "Page 43")
-//   waves        = ceil(tiles / SMs); the persistent kernel runs one tile per
-//                  SM at a time, so a partial last wave costs a full one
+//   tiles        = tile quantization of the output of one product:
+//                  ceil(m/tile_m) * ceil(n/tile_n)  (CS336 Lecture 05 notes,
+//                  "Page 43")
+//   waves        = ceil(tiles / slots), slots = SMs (one tile per SM) or SM
+//                  pairs (256-row tiles); a partial last wave costs a full one
 //                  ("Page 48", wave quantization)
-//   t_tile       = products * (2 * 128 * tile_n * K_sub / (per-SM peak * eff)
-//                  + fill), eff measured per form and tile width
+//   t_tile       = products * (2 * tile_m * tile_n * K_sub / (slot peak * eff)
+//                  + fill), eff measured per form and tile
 //   t_compute    = waves * t_tile
 //   t_memory     = HBM bytes / bandwidth (operands and result once, plus the
 //                  Strassen partial tiles when they cannot stay in L2)
@@ -43,12 +44,14 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 namespace fgemm {
 
-// Shared with the API's validation: is (algo, tile_n) legal for the shape?
+// Shared with the API's validation: is (algo, tile_m x tile_n) legal?
 bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo_t algo,
-                   int32_t tile_n) {
+                   int32_t tile_m, int32_t tile_n) {
   if (tile_n != 64 && tile_n != 128 && tile_n != 256) return false;
+  if (tile_m != 128 && tile_m != 256) return false;
   if (epi_kind == FGEMM_EPI_SWIGLU && tile_n == 64) return false;
   const int d = depth_of(algo);
+  if (tile_m == 256) return d == 0 && tile_n >= 128;
   if (d == 0) return true;
   if (tile_n == 64) return false;
   const int64_t g = int64_t{1} << d;
@@ -70,6 +73,8 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   m.eff_classical[0] = 0.50;
   m.eff_classical[1] = 0.65;
   m.eff_classical[2] = 0.75;
+  m.eff_pair[0] = 0.75;
+  m.eff_pair[1] = 0.82;
   m.eff_strassen[0][0] = 0.45;
   m.eff_strassen[0][1] = 0.55;
   m.eff_strassen[1][0] = 0.35;
@@ -111,53 +116,56 @@ double fgemm_model_roofline(double flops, double bytes, double peak_flops, doubl
 }
 
 fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, int64_t N,
-                                   int64_t K, int32_t epi_kind, fgemm_algo_t algo,
+                                   int64_t K, int32_t epi_kind, fgemm_algo_t algo, int32_t tile_m,
                                    int32_t tile_n, double* predicted_us) {
   if (!dev || M < 0 || N < 0 || K < 0) return FGEMM_ERR_INVALID_ARG;
   if (algo == FGEMM_ALGO_AUTO) return FGEMM_ERR_INVALID_ARG;
-  if (!fgemm::form_is_legal(M, N, K, epi_kind, algo, tile_n)) return FGEMM_ERR_UNSUPPORTED;
+  if (!fgemm::form_is_legal(M, N, K, epi_kind, algo, tile_m, tile_n)) return FGEMM_ERR_UNSUPPORTED;
   const int d = depth_of(algo);
   const bool swiglu = epi_kind == FGEMM_EPI_SWIGLU;
+  const bool pair = tile_m == 256;
   const int64_t n_out = swiglu ? N / 2 : N;
   const int64_t sub_m = M >> d, sub_n = N >> d, sub_k = K >> d;
   const int64_t products = d == 0 ? 1 : (d == 1 ? 7 : 49);
   int64_t tiles;
   if (d == 0 && swiglu)
-    tiles = fgemm_model_tiles(sub_m, n_out, fgemm::kBM, tile_n / 2);
+    tiles = fgemm_model_tiles(sub_m, n_out, tile_m, tile_n / 2);
   else
-    tiles = fgemm_model_tiles(sub_m, sub_n, fgemm::kBM, tile_n);
-  const int64_t waves = fgemm_model_waves(tiles, dev->num_sms, nullptr);
-  const double eff = d == 0 ? dev->eff_classical[tile_index(tile_n)]
-                            : dev->eff_strassen[d - 1][tile_n == 128 ? 0 : 1];
-  const double per_sm_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms;
+    tiles = fgemm_model_tiles(sub_m, sub_n, tile_m, tile_n);
+  // a pair of SMs works on one 256-row tile
+  const int32_t slots = pair ? std::max(1, dev->num_sms / 2) : dev->num_sms;
+  const int64_t waves = fgemm_model_waves(tiles, slots, nullptr);
+  double eff;
+  if (d > 0)
+    eff = dev->eff_strassen[d - 1][tile_n == 128 ? 0 : 1];
+  else if (pair)
+    eff = dev->eff_pair[tile_n == 128 ? 0 : 1];
+  else
+    eff = dev->eff_classical[tile_index(tile_n)];
+  const double slot_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms * (pair ? 2.0 : 1.0);
   const double k_pad = static_cast<double>(ceil_div(sub_k, fgemm::kBK) * fgemm::kBK);
   const double t_tile =
-      products * (2.0 * fgemm::kBM * tile_n * k_pad / (per_sm_flop_per_us * std::max(eff, 1e-3)) +
+      products * (2.0 * tile_m * tile_n * k_pad / (slot_flop_per_us * std::max(eff, 1e-3)) +
                   dev->tile_fill_us);
   const double t_compute = static_cast<double>(waves) * t_tile;
   double bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
                         static_cast<double>(M) * n_out);
   if (d > 0) {
     const double slot_bytes = 4.0 * fgemm::kBM * tile_n;
-    const double slots = std::pow(4.0, d);
-    const double live = std::min<double>(static_cast<double>(tiles), dev->num_sms) * slots * slot_bytes;
+    const double nslots = std::pow(4.0, d);
+    const double live = std::min<double>(static_cast<double>(tiles), dev->num_sms) * nslots * slot_bytes;
     if (live > dev->l2_bytes) {
       const double contributions = std::pow(12.0, d);  // nonzeros of the combination
       bytes += static_cast<double>(tiles) * (2.0 * contributions) * slot_bytes;
     }
   }
   const double t_memory = bytes / (dev->hbm_gbs * 1e3);
-  // Operand tiles streamed from L2 into the SMs: every product re-reads its
-  // source blocks (one or two per operand at depth 1, up to four at depth 2).
-  double op_elems;
-  if (d == 0) {
-    op_elems = static_cast<double>(tiles) * (fgemm::kBM + tile_n) * k_pad;
-  } else {
-    // sum over products of (a-terms * 128 + b-terms * tile_n): the scheme's
-    // term counts are 12 + 12 at depth 1 and 144 + 144 at depth 2
-    const double terms = d == 1 ? 12.0 : 144.0;
-    op_elems = static_cast<double>(tiles) * terms * (fgemm::kBM + tile_n) * k_pad;
-  }
+  // Operand tiles streamed from L2 into the SMs (tiled reads): every product
+  // re-reads its source blocks; the scheme's term counts are 12 + 12 at depth
+  // 1 and 144 + 144 at depth 2 (against 8 + 8 for the four classical blocks).
+  double op_elems = static_cast<double>(tiles) * (tile_m + tile_n) * k_pad;
+  if (d == 1) op_elems *= 12.0;
+  if (d == 2) op_elems *= 144.0;
   const double t_operands = 2.0 * op_elems / (dev->l2_gbs * 1e3);
   if (predicted_us)
     *predicted_us = std::max(std::max(t_compute, t_memory), t_operands) + dev->launch_us;
@@ -169,25 +177,29 @@ fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M, int6
                                 int32_t* tile_n, double* predicted_us) {
   if (!dev) return FGEMM_ERR_INVALID_ARG;
   const fgemm_algo_t algos[3] = {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2};
-  const int32_t tiles[3] = {64, 128, 256};
+  const int32_t tms[2] = {128, 256};
+  const int32_t tns[3] = {64, 128, 256};
   double best = INFINITY;
   fgemm_algo_t best_algo = FGEMM_ALGO_CLASSICAL;
-  int32_t best_tile = 0;
+  int32_t best_m = 0, best_n = 0;
   for (fgemm_algo_t a : algos) {
-    for (int32_t t : tiles) {
-      double us = 0;
-      if (fgemm_model_predict(dev, M, N, K, epi_kind, a, t, &us) != FGEMM_OK) continue;
-      if (us < best) {
-        best = us;
-        best_algo = a;
-        best_tile = t;
+    for (int32_t tm : tms) {
+      for (int32_t tn : tns) {
+        double us = 0;
+        if (fgemm_model_predict(dev, M, N, K, epi_kind, a, tm, tn, &us) != FGEMM_OK) continue;
+        if (us < best) {
+          best = us;
+          best_algo = a;
+          best_m = tm;
+          best_n = tn;
+        }
       }
     }
   }
-  if (best_tile == 0) return FGEMM_ERR_UNSUPPORTED;
+  if (best_n == 0) return FGEMM_ERR_UNSUPPORTED;
   if (algo_out) *algo_out = best_algo;
-  if (tile_m) *tile_m = fgemm::kBM;
-  if (tile_n) *tile_n = best_tile;
+  if (tile_m) *tile_m = best_m;
+  if (tile_n) *tile_n = best_n;
   if (predicted_us) *predicted_us = best;
   return FGEMM_OK;
 }

@@ -98,7 +98,8 @@ extern "C" fgemm_status_t fgemm_strassen_matmul_static(
   if (depth != 1 && depth != 2) return fail(FGEMM_ERR_INVALID_ARG, "depth must be 1 or 2");
   if (tile_n == 0) tile_n = 128;
   const fgemm_algo_t algo = depth == 1 ? FGEMM_ALGO_STRASSEN1 : FGEMM_ALGO_STRASSEN2;
-  fgemm_status_t s = fgemm_validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_n);
+  fgemm_status_t s =
+      fgemm_validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, fgemm::kBM, tile_n);
   if (s != FGEMM_OK) return s;
   const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
   const int64_t n_out = kind == FGEMM_EPI_SWIGLU ? N / 2 : N;

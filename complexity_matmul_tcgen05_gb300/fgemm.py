@@ -42,6 +42,7 @@ class DeviceModel(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("peak_tflops", ctypes.c_double), ("hbm_gbs", ctypes.c_double),
                 ("eff_classical", ctypes.c_double * 3),
+                ("eff_pair", ctypes.c_double * 2),
                 ("eff_strassen", (ctypes.c_double * 2) * 2),
                 ("launch_us", ctypes.c_double), ("tile_fill_us", ctypes.c_double),
                 ("l2_bytes", ctypes.c_double), ("l2_gbs", ctypes.c_double)]
@@ -69,7 +70,7 @@ def lib() -> ctypes.CDLL:
         L.fgemm_set_stream.argtypes = [vp, vp]
         mm = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, st, epi_p, st]
         L.fgemm_matmul.argtypes = mm
-        L.fgemm_matmul_ex.argtypes = mm + [i32]
+        L.fgemm_matmul_ex.argtypes = mm + [i32, i32]
         L.fgemm_plan.argtypes = [vp, i64, i64, i64, st, epi_p, ctypes.POINTER(st),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(ctypes.c_double)]
@@ -79,7 +80,8 @@ def lib() -> ctypes.CDLL:
         L.fgemm_status_string.restype = ctypes.c_char_p
         L.fgemm_last_message.argtypes = [vp]
         L.fgemm_last_message.restype = ctypes.c_char_p
-        L.fgemm_validate.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, st, epi_p, st, i32]
+        L.fgemm_validate.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, st, epi_p, st, i32,
+                                     i32]
         L.fgemm_model_default.argtypes = [model_p, i32, ctypes.c_double, ctypes.c_double]
         L.fgemm_model_default.restype = None
         L.fgemm_model_tiles.argtypes = [i64, i64, i32, i32]
@@ -90,7 +92,7 @@ def lib() -> ctypes.CDLL:
         L.fgemm_model_tiled_reads.restype = ctypes.c_double
         L.fgemm_model_roofline.argtypes = [ctypes.c_double] * 4
         L.fgemm_model_roofline.restype = ctypes.c_double
-        L.fgemm_model_predict.argtypes = [model_p, i64, i64, i64, i32, st, i32,
+        L.fgemm_model_predict.argtypes = [model_p, i64, i64, i64, i32, st, i32, i32,
                                           ctypes.POINTER(ctypes.c_double)]
         L.fgemm_model_plan.argtypes = [model_p, i64, i64, i64, i32, ctypes.POINTER(st),
                                        ctypes.POINTER(i32), ctypes.POINTER(i32),
@@ -132,11 +134,11 @@ def make_epilogue(kind: str = "none", alpha: float = 1.0, bias_ptr: int | None =
 
 
 def validate(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype: int, epilogue: Epilogue | None,
-             algo: str = "auto", tile_n: int = 0) -> int:
+             algo: str = "auto", tile_n: int = 0, tile_m: int = 0) -> int:
     """Host-only argument check (no device): the status fgemm_matmul_ex would return."""
     return lib().fgemm_validate(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype,
                                 ctypes.byref(epilogue) if epilogue is not None else None,
-                                ALGOS[algo], tile_n)
+                                ALGOS[algo], tile_m, tile_n)
 
 
 class Handle:
@@ -167,11 +169,12 @@ class Handle:
         _check(lib().fgemm_set_stream(self._h, ctypes.c_void_p(stream_ptr)), self._h)
 
     def matmul_raw(self, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype: int,
-                   epilogue: Epilogue | None = None, algo: str = "auto", tile_n: int = 0) -> int:
+                   epilogue: Epilogue | None = None, algo: str = "auto", tile_n: int = 0,
+                   tile_m: int = 0) -> int:
         """Direct C-ABI call on raw device pointers; returns the status."""
         return lib().fgemm_matmul_ex(self._h, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype,
                                      ctypes.byref(epilogue) if epilogue is not None else None,
-                                     ALGOS[algo], tile_n)
+                                     ALGOS[algo], tile_m, tile_n)
 
     def plan(self, M, N, K, dtype: int = BF16, epilogue: Epilogue | None = None):
         a = ctypes.c_int()
@@ -182,7 +185,7 @@ class Handle:
                                 ctypes.byref(epilogue) if epilogue is not None else None,
                                 ctypes.byref(a), ctypes.byref(tm), ctypes.byref(tn),
                                 ctypes.byref(us)), self._h)
-        return ALGO_NAMES[a.value], tn.value, us.value
+        return ALGO_NAMES[a.value], tm.value, tn.value, us.value
 
     def get_error(self) -> int:
         return lib().fgemm_get_error(self._h)
@@ -223,7 +226,8 @@ def _check_matrix(t: torch.Tensor, name: str):
 
 def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
            epilogue: str = "none", alpha: float = 1.0, bias: torch.Tensor | None = None,
-           algo: str = "auto", tile_n: int = 0, handle: Handle | None = None) -> torch.Tensor:
+           algo: str = "auto", tile_n: int = 0, tile_m: int = 0,
+           handle: Handle | None = None) -> torch.Tensor:
     """C = epi(alpha * A @ B + bias) through fgemm_matmul_ex.
 
     A is M x K, B is K x N (row-major), bias has N entries; for
@@ -235,7 +239,7 @@ def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
         Bd = B.to(dev, non_blocking=True)
         bd = None if bias is None else bias.to(dev, non_blocking=True)
         Cd = matmul(Ad, Bd, epilogue=epilogue, alpha=alpha, bias=bd, algo=algo, tile_n=tile_n,
-                    handle=handle)
+                    tile_m=tile_m, handle=handle)
         if out is not None:
             out.copy_(Cd)
             return out
@@ -271,12 +275,12 @@ def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
     ldb = B.stride(0) if K > 1 else max(N, 1)
     ldc = out.stride(0) if M > 1 else max(n_out, 1)
     s = h.matmul_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, dt,
-                     epi, algo, tile_n)
+                     epi, algo, tile_n, tile_m)
     _check(s, h.ptr)
     return out
 
 
 def plan(M: int, N: int, K: int, dtype: torch.dtype = torch.bfloat16, epilogue: str = "none"):
-    """(algorithm, tile_n, predicted microseconds) the decision model picks."""
+    """(algorithm, tile_m, tile_n, predicted microseconds) the decision model picks."""
     h = default_handle()
     return h.plan(M, N, K, _dtype_code(dtype), make_epilogue(epilogue))

@@ -132,15 +132,20 @@ fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
                             fgemm_algo_t algo);
 
 /*
- * As fgemm_matmul, with the output tile width forced: tile_n in {64, 128,
- * 256} (classical), {128, 256} (Strassen forms, SWIGLU), or 0 to let the
- * model choose. Used for exhaustive timing of the decision model's choices.
+ * As fgemm_matmul, with the output tile forced (used for exhaustive timing of
+ * the decision model's choices). tile_m = 128: one CTA per tile, tile_n in
+ * {64, 128, 256}; tile_m = 256: a pair of CTAs (one M = 256 tensor-core
+ * operation across two SMs), tile_n in {128, 256}, classical form only.
+ * SWIGLU needs tile_n >= 128; the Strassen forms use tile_m = 128 and tile_n
+ * in {128, 256}. tile_m = tile_n = 0 lets the model choose; a zero in only
+ * one of them lets the model choose the other.
  */
 fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N,
                                int64_t K, const void* A, int64_t lda,
                                const void* B, int64_t ldb, void* C, int64_t ldc,
                                fgemm_dtype_t dtype, const fgemm_epilogue_t* epi,
-                               fgemm_algo_t algo, int32_t tile_n);
+                               fgemm_algo_t algo, int32_t tile_m,
+                               int32_t tile_n);
 
 /*
  * Runs the decision model (no launch): the algorithm, tile and predicted
@@ -181,7 +186,7 @@ fgemm_status_t fgemm_validate(int64_t M, int64_t N, int64_t K, const void* A,
                               int64_t lda, const void* B, int64_t ldb,
                               const void* C, int64_t ldc, fgemm_dtype_t dtype,
                               const fgemm_epilogue_t* epi, fgemm_algo_t algo,
-                              int32_t tile_n);
+                              int32_t tile_m, int32_t tile_n);
 
 /*
  * Strassen product (depth 1 or 2) that allocates no device memory. The paper
@@ -190,7 +195,7 @@ fgemm_status_t fgemm_validate(int64_t M, int64_t N, int64_t K, const void* A,
  * loops that must not pay cudaMalloc's implicit device synchronisation, or
  * plug-ins that are handed nothing but buffers and a stream.
  *
- * It computes what fgemm_matmul_ex(..., FGEMM_ALGO_STRASSEN1 or 2, tile_n)
+ * It computes what fgemm_matmul_ex(..., FGEMM_ALGO_STRASSEN1 or 2, 128, tile_n)
  * computes, with no handle: the scratch it needs (the kernel's error word and
  * the fp32 partial tiles of the Strassen combination) lives in a 64 MiB
  * array built into the library, which every device that loads the library
@@ -226,11 +231,12 @@ fgemm_status_t fgemm_strassen_matmul_static(
  * and the roofline of "Page 21".
  * ------------------------------------------------------------------------ */
 typedef struct {
-  int32_t num_sms;         /* concurrent tile slots (one persistent CTA per SM) */
+  int32_t num_sms;         /* SMs: one persistent CTA per SM, one pair per 2 */
   int32_t reserved;
   double peak_tflops;      /* dense 16-bit tensor peak, TFLOP/s */
   double hbm_gbs;          /* streaming HBM bandwidth, GB/s */
-  double eff_classical[3]; /* mainloop fraction of peak for tile_n 64, 128, 256 */
+  double eff_classical[3]; /* mainloop fraction of peak, 128 x {64, 128, 256} */
+  double eff_pair[2];      /* same for CTA-pair tiles 256 x {128, 256} */
   double eff_strassen[2][2]; /* [depth-1][tile_n 128, 256]: executed-MAC rate
                               * of the Strassen mainloop as a fraction of peak */
   double launch_us;        /* fixed cost of one launch */
@@ -266,8 +272,8 @@ double fgemm_model_roofline(double flops, double bytes, double peak_flops,
  * FGEMM_ERR_UNSUPPORTED if that form/tile is illegal for the shape. */
 fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M,
                                    int64_t N, int64_t K, int32_t epi_kind,
-                                   fgemm_algo_t algo, int32_t tile_n,
-                                   double* predicted_us);
+                                   fgemm_algo_t algo, int32_t tile_m,
+                                   int32_t tile_n, double* predicted_us);
 
 /* The argmin over every legal (form, tile): what AUTO launches. */
 fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M,

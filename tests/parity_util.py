@@ -66,9 +66,10 @@ def abs_bits(b: np.ndarray) -> np.ndarray:
     return (b & np.uint16(0x7FFF)).astype(np.uint16)
 
 
-def run(A, B, algo="classical", epilogue="none", alpha=1.0, bias=None, tile_n=0, out=None):
+def run(A, B, algo="classical", epilogue="none", alpha=1.0, bias=None, tile_n=0, out=None,
+        tile_m=0):
     C = fgemm.matmul(A, B, out=out, epilogue=epilogue, alpha=alpha, bias=bias, algo=algo,
-                     tile_n=tile_n)
+                     tile_n=tile_n, tile_m=tile_m)
     torch.cuda.synchronize()
     assert fgemm.default_handle().get_error() == fgemm.OK, fgemm.default_handle().last_message()
     return C

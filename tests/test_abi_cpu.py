@@ -55,12 +55,12 @@ def test_status_strings(L):
 
 
 def _v(M, N, K, A=16, lda=None, B=16, ldb=None, C=16, ldc=None, dtype=fgemm.BF16,
-       epi=None, algo="auto", tile=0):
+       epi=None, algo="auto", tile=0, tile_m=0):
     lda = K if lda is None else lda
     ldb = N if ldb is None else ldb
     n_out = N // 2 if (epi is not None and epi.kind == 3) else N
     ldc = n_out if ldc is None else ldc
-    return fgemm.validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile)
+    return fgemm.validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile, tile_m)
 
 
 def test_validation_codes(L):
@@ -91,6 +91,12 @@ def test_validation_codes(L):
     assert _v(256, 256, 96, lda=96, algo="strassen1") == fgemm.ERR_UNSUPPORTED
     assert _v(512, 512, 256, algo="strassen2", tile=128) == ok
     assert _v(256, 512, 256, algo="strassen2") == fgemm.ERR_UNSUPPORTED
+    # CTA-pair tiles: 256 x {128, 256}, classical only
+    assert _v(512, 512, 256, tile_m=256, tile=128) == ok
+    assert _v(512, 512, 256, tile_m=256, tile=64) == fgemm.ERR_UNSUPPORTED
+    assert _v(512, 512, 256, algo="strassen1", tile_m=256) == fgemm.ERR_UNSUPPORTED
+    assert _v(512, 512, 256, tile_m=192) == fgemm.ERR_INVALID_ARG
+    assert _v(100, 512, 256, tile_m=256) == ok                     # ragged rows are fine
 
 
 def test_swiglu_odd_n_rejected(L):
@@ -149,9 +155,10 @@ def test_roofline_page_examples(L):
         assert abs(1.0 / perf - r[key]) < 1e-12
 
 
-def _predict(L, m, M, N, K, algo, tile, epi=0):
+def _predict(L, m, M, N, K, algo, tile, epi=0, tile_m=128):
     us = ctypes.c_double()
-    s = L.fgemm_model_predict(ctypes.byref(m), M, N, K, epi, fgemm.ALGOS[algo], tile, ctypes.byref(us))
+    s = L.fgemm_model_predict(ctypes.byref(m), M, N, K, epi, fgemm.ALGOS[algo], tile_m, tile,
+                              ctypes.byref(us))
     return s, us.value
 
 
@@ -216,4 +223,17 @@ def test_model_plan_small_shapes_stay_classical(L):
         assert L.fgemm_model_plan(ctypes.byref(m), M, N, K, 0, ctypes.byref(a), ctypes.byref(tm),
                                   ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
         assert fgemm.ALGO_NAMES[a.value] == "classical"
-        assert tm.value == 128 and tn.value in (64, 128, 256)
+        assert tm.value in (128, 256) and tn.value in (64, 128, 256)
+
+
+def test_model_pair_tiles_fix_wave_quantization(L):
+    # 4096^2 output: 512 tiles of 128x256 on 152 SMs is 3.37 waves (the last
+    # runs 56 SMs); 512 pair tiles of 256x128 on 76 pairs is 6.74 waves.
+    m = _model(L)
+    m.eff_classical[2] = m.eff_pair[0] = 0.8
+    _, t_single = _predict(L, m, 4096, 4096, 4096, "classical", 256)
+    _, t_pair = _predict(L, m, 4096, 4096, 4096, "classical", 128, tile_m=256)
+    assert t_pair < t_single
+    tail = ctypes.c_double()
+    assert L.fgemm_model_waves(L.fgemm_model_tiles(4096, 4096, 128, 256), 152, ctypes.byref(tail)) == 4
+    assert L.fgemm_model_waves(L.fgemm_model_tiles(4096, 4096, 256, 128), 76, ctypes.byref(tail)) == 7

@@ -82,7 +82,7 @@ def test_sweep_shapes_every_legal_form(shape):
     M, N, K = shape
     A, B = inputs.sweep_inputs(M, N, K, DEV)
     for algo in ("classical", "strassen1", "strassen2", "auto"):
-        s = fgemm.validate(M, N, K, 16, K, 16, N, 16, N, fgemm.BF16, None, algo, 0)
+        s = fgemm.validate(M, N, K, 16, K, 16, N, 16, N, fgemm.BF16, None, algo)
         if s == fgemm.ERR_UNSUPPORTED:
             continue
         _sampled_check(f"sweep {shape}", A, B, None, algo, "none", "bf16")

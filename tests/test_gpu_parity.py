@@ -47,6 +47,15 @@ EXACT_CASES = [
     ("strassen2", 512, 512, 256, 128),
     ("strassen2", 512, 1024, 512, 256),
 ]
+# CTA-pair tiles (256 rows over two SMs): (M, N, K, tile_n)
+EXACT_PAIR_CASES = [
+    (256, 256, 64, 256),
+    (256, 128, 64, 128),
+    (100, 256, 128, 256),      # the odd CTA's rows are all past M
+    (300, 520, 1032, 128),     # ragged M, N, K
+    (1000, 1000, 1000, 256),
+    (2048, 1024, 512, 128),
+]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
@@ -55,6 +64,14 @@ def test_exact_ternary(algo, M, N, K, tile, dtype):
     """Inputs in {-1,0,1}, integer bias: every form must equal RNE(exact C) bit for bit."""
     A, B, bias = _ternary(M, N, K, dtype)
     C = run(A, B, algo=algo, epilogue="scale_bias", bias=bias, tile_n=tile)
+    assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K,tile", EXACT_PAIR_CASES)
+def test_exact_ternary_cta_pair(M, N, K, tile, dtype):
+    A, B, bias = _ternary(M, N, K, dtype)
+    C = run(A, B, algo="classical", epilogue="scale_bias", bias=bias, tile_n=tile, tile_m=256)
     assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
 
 
@@ -79,12 +96,13 @@ def test_exact_ternary_strided_and_guard_band():
 
 # ----------------------------------------- full-entry tolerance parity
 
-def _full_check(A, B, algo, dtype, epilogue="none", alpha=1.0, bias=None, tile=0, depth=0):
+def _full_check(A, B, algo, dtype, epilogue="none", alpha=1.0, bias=None, tile=0, depth=0,
+                tile_m=0):
     """Every entry: normwise bound (scaled by the activation's condition
     number for SiLU / SwiGLU), the 8-ulp rule for classical without an
     activation, and for Strassen the tight pin against the oracle's emulated
     (rounded-operand) Strassen passed through the same epilogue."""
-    C = run(A, B, algo=algo, epilogue=epilogue, alpha=alpha, bias=bias, tile_n=tile)
+    C = run(A, B, algo=algo, epilogue=epilogue, alpha=alpha, bias=bias, tile_n=tile, tile_m=tile_m)
     Ab, Bb = gpu_bits(A), gpu_bits(B)
     bb = None if bias is None else gpu_bits(bias)
     Av, Bv = oracle.decode(Ab, dtype), oracle.decode(Bb, dtype)
@@ -113,25 +131,26 @@ def test_square_256_fp16_every_entry(algo, depth):
     _full_check(A, B, algo, "f16", depth=depth)
 
 
-@pytest.mark.parametrize("tile", [64, 128, 256])
+@pytest.mark.parametrize("tile_m,tile", [(128, 64), (128, 128), (128, 256), (256, 128), (256, 256)])
 @pytest.mark.parametrize("epilogue,alpha", [("none", 1.0), ("scale_bias", 0.5), ("silu", 1.25)])
-def test_classical_epilogues_every_entry(epilogue, alpha, tile):
+def test_classical_epilogues_every_entry(epilogue, alpha, tile_m, tile):
     M, N, K = 384, 640, 320
     A = inputs.matrix(M, K, "normal", "bf16", 0, DEV)
     B = inputs.matrix(K, N, "normal_inv_k", "bf16", 1, DEV, k=K)
     bias = inputs.matrix(1, N, "normal_0.02", "bf16", 2, DEV)[0] if epilogue != "none" else None
-    _full_check(A, B, "classical", "bf16", epilogue, alpha, bias, tile)
+    _full_check(A, B, "classical", "bf16", epilogue, alpha, bias, tile, tile_m=tile_m)
 
 
-@pytest.mark.parametrize("algo,tile,depth", [("classical", 128, 0), ("classical", 256, 0),
-                                             ("strassen1", 128, 1), ("strassen1", 256, 1),
-                                             ("strassen2", 128, 2)])
-def test_swiglu_every_entry(algo, tile, depth):
+@pytest.mark.parametrize("algo,tile_m,tile,depth", [
+    ("classical", 128, 128, 0), ("classical", 128, 256, 0), ("classical", 256, 128, 0),
+    ("classical", 256, 256, 0), ("strassen1", 128, 128, 1), ("strassen1", 128, 256, 1),
+    ("strassen2", 128, 128, 2)])
+def test_swiglu_every_entry(algo, tile_m, tile, depth):
     M, N, K = 512, 2048, 512
     A = inputs.matrix(M, K, "normal", "bf16", 0, DEV)
     B = inputs.matrix(K, N, "normal_inv_k", "bf16", 1, DEV, k=K)
     bias = inputs.matrix(1, N, "normal_0.02", "bf16", 2, DEV)[0]
-    _full_check(A, B, algo, "bf16", "swiglu", 1.0, bias, tile, depth)
+    _full_check(A, B, algo, "bf16", "swiglu", 1.0, bias, tile, depth, tile_m=tile_m)
 
 
 @pytest.mark.parametrize("algo,tile,depth", [("strassen1", 128, 1), ("strassen1", 256, 1),
@@ -179,8 +198,9 @@ def test_rejections_do_not_launch():
 
 def test_plan_is_legal_and_launchable():
     for (M, N, K) in [(256, 256, 256), (4096, 4096, 4096), (16, 2048, 2048), (16384, 16384, 16384)]:
-        algo, tile, us = fgemm.plan(M, N, K)
+        algo, tile_m, tile, us = fgemm.plan(M, N, K)
         assert algo in ("classical", "strassen1", "strassen2") and tile in (64, 128, 256)
+        assert tile_m in (128, 256)
         assert us > 0
 
 
