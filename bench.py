@@ -58,6 +58,9 @@ def parse():
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0 = auto)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="decision-model check: every legal form/tile vs auto on the sweep shapes")
+    ap.add_argument("--out", default=None, help="JSON-lines file for --sweep")
     return ap.parse_args()
 
 
@@ -182,13 +185,19 @@ def measured_peaks():
     return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ("fgemm_kernel.cuh", "fgemm_kernel_pair.cuh", "fgemm_ptx.cuh",
+                  "fgemm_internal.h", "fgemm_kern_classical.cu", "fgemm_kern_pair.cu",
+                  "fgemm_kern_strassen1.cu", "fgemm_kern_strassen2.cu")
+
+
 def kernel_source_hash():
+    """Hash of the device-code sources: recorded ncu counters are used only
+    while the kernels they were taken on are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "complexity_matmul_tcgen05_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:12]
 
 
@@ -410,8 +419,86 @@ def run_fgemm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+CANDIDATES = [("classical", 128, 64), ("classical", 128, 128), ("classical", 128, 256),
+              ("classical", 256, 128), ("classical", 256, 256), ("strassen1", 128, 128),
+              ("strassen1", 128, 256), ("strassen2", 128, 128), ("strassen2", 128, 256)]
+
+
+def run_sweep(args):
+    """Times every legal (form, tile) and AUTO on each sweep shape (CUDA
+    events, median of 5 after 2 warm-ups, a 512 MiB buffer written between
+    runs to flush the L2) and the host cost of the decision (a fresh model
+    evaluation, and a whole cached call).  One JSON line per shape."""
+    from complexity_matmul_tcgen05_gb300 import fgemm, inputs
+    dev = torch.device("cuda", torch.cuda.current_device())
+    handle = fgemm.default_handle()
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    out = open(args.out, "w") if args.out else None
+    model = handle.device_model()
+    L = fgemm.lib()
+    import ctypes
+
+    def time_one(A, B, C, algo, tm, tn):
+        ts = []
+        for r in range(7):
+            flush.fill_(r & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fgemm.matmul(A, B, out=C, algo=algo, tile_m=tm, tile_n=tn, handle=handle)
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    for (M, N, K) in inputs.SWEEP_SHAPES:
+        A, B = inputs.sweep_inputs(M, N, K, dev)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        times = {}
+        for algo, tm, tn in CANDIDATES:
+            if fgemm.validate(M, N, K, 16, K, 16, N, 16, N, fgemm.BF16, None, algo, tn, tm) != fgemm.OK:
+                continue
+            times[f"{algo}:{tm}x{tn}"] = time_one(A, B, C, algo, tm, tn)
+        a_algo, a_tm, a_tn, pred = handle.plan(M, N, K)
+        t_auto = time_one(A, B, C, "auto", 0, 0)
+        best = min(times, key=times.get)
+        # host cost of one fresh model evaluation (every form and tile)
+        a = ctypes.c_int()
+        x, y, us = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+        t0 = time.perf_counter()
+        for _ in range(1000):
+            L.fgemm_model_plan(ctypes.byref(model), M, N, K, 0, ctypes.byref(a), ctypes.byref(x),
+                               ctypes.byref(y), ctypes.byref(us))
+        plan_us = (time.perf_counter() - t0) * 1e3
+        # host cost of a whole cached call (checks, plan lookup, launch)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(50):
+            handle.matmul_raw(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N,
+                              fgemm.BF16, None, "auto", 0, 0)
+        call_us = (time.perf_counter() - t0) / 50 * 1e6
+        torch.cuda.synchronize()
+        rec = {"M": M, "N": N, "K": K, "times_us": times, "best": best, "best_us": times[best],
+               "auto": f"{a_algo}:{a_tm}x{a_tn}", "auto_us": t_auto, "predicted_us": pred,
+               "regret": t_auto / times[best] - 1.0,
+               "auto_tflops": 2.0 * M * N * K / (t_auto * 1e-6) / 1e12,
+               "model_eval_us": plan_us, "host_call_us": call_us,
+               "decision_share": plan_us / t_auto}
+        line = json.dumps(rec)
+        print(line, flush=True)
+        if out:
+            out.write(line + "\n")
+            out.flush()
+        del A, B, C
+    if handle.get_error() != fgemm.OK:
+        raise SystemExit(f"device error: {handle.last_message()}")
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     rank, world = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)

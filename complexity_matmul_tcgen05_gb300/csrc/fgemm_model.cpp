@@ -70,17 +70,21 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   m.num_sms = num_sms > 0 ? num_sms : 1;
   m.peak_tflops = peak_tflops > 0 ? peak_tflops : 2250.0;
   m.hbm_gbs = hbm_gbs > 0 ? hbm_gbs : 7900.0;
-  m.eff_classical[0] = 0.50;
-  m.eff_classical[1] = 0.65;
-  m.eff_classical[2] = 0.75;
-  m.eff_pair[0] = 0.75;
-  m.eff_pair[1] = 0.82;
-  m.eff_strassen[0][0] = 0.45;
-  m.eff_strassen[0][1] = 0.55;
-  m.eff_strassen[1][0] = 0.35;
-  m.eff_strassen[1][1] = 0.45;
-  m.launch_us = 5.0;
-  m.tile_fill_us = 1.0;
+  // Mainloop efficiencies and fixed costs measured on GB300 by fgemm_calibrate
+  // (8192^3 bf16, every form and tile), as fractions of the 2250 TFLOP/s
+  // nominal dense peak the model starts from; fgemm_calibrate re-measures them
+  // on the device at hand.
+  m.eff_classical[0] = 0.257;  // 128 x 64
+  m.eff_classical[1] = 0.501;  // 128 x 128
+  m.eff_classical[2] = 0.700;  // 128 x 256
+  m.eff_pair[0] = 0.499;       // 256 x 128
+  m.eff_pair[1] = 0.850;       // 256 x 256
+  m.eff_strassen[0][0] = 0.072;
+  m.eff_strassen[0][1] = 0.082;
+  m.eff_strassen[1][0] = 0.034;
+  m.eff_strassen[1][1] = 0.047;
+  m.launch_us = 9.1;
+  m.tile_fill_us = 2.3;
   m.l2_bytes = 126.0 * 1024 * 1024;
   m.l2_gbs = 40000.0;
   *out = m;
