@@ -428,6 +428,8 @@ fgemm_status_t load_calibration(fgemm_handle_t h, const char* path) {
       {"eff_classical_64", &m.eff_classical[0]}, {"eff_classical_128", &m.eff_classical[1]},
       {"eff_classical_256", &m.eff_classical[2]}, {"eff_pair_128", &m.eff_pair[0]},
       {"eff_pair_256", &m.eff_pair[1]},         {"eff_strassen1_128", &m.eff_strassen[0][0]},
+      {"eff_strassen1_pair_128", &m.eff_strassen_pair[0]},
+      {"eff_strassen1_pair_256", &m.eff_strassen_pair[1]},
       {"eff_strassen1_256", &m.eff_strassen[0][1]}, {"eff_strassen2_128", &m.eff_strassen[1][0]},
       {"eff_strassen2_256", &m.eff_strassen[1][1]}, {"launch_us", &m.launch_us},
       {"tile_fill_us", &m.tile_fill_us},        {"l2_bytes", &m.l2_bytes},
@@ -645,6 +647,16 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
                   static_cast<uint64_t>(ldb), fgemm::kBK, p.is_bf16);
   if (s != FGEMM_OK) return s;
 
+  if (bm == 256 && d == 1) {
+    // one persistent CTA per SM at most: 4 partial tiles of 128 x bn each
+    const size_t per_cta = 4 * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float);
+    s = ensure_workspace(h, per_cta * static_cast<size_t>(h->num_sms));
+    if (s != FGEMM_OK) return s;
+    p.workspace = h->workspace;
+    cudaError_t e = fgemm::launch_strassen_pair(bn, p, h->num_sms / 2, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "Strassen pair kernel launch");
+    return FGEMM_OK;
+  }
   if (bm == 256) {
     cudaError_t e = fgemm::launch_gemm_pair(bn, p, h->num_sms / 2, h->stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM pair kernel launch");
@@ -770,6 +782,11 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
         m.eff_strassen[d - 1][i] = executed / (us * 1e6) / m.peak_tflops;
       }
     }
+    for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
+      double us = 0;
+      if (!time_gemm(n, n, n, FGEMM_ALGO_STRASSEN1, 256, i == 0 ? 128 : 256, &us)) break;
+      m.eff_strassen_pair[i] = flops * 7.0 / 8.0 / (us * 1e6) / m.peak_tflops;
+    }
     if (status != FGEMM_OK) break;
     {  // launch + fill: one tiny tile
       double us = 0;
@@ -809,11 +826,13 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
                  "  \"eff_classical_256\": %.5f,\n  \"eff_pair_128\": %.5f,\n"
                  "  \"eff_pair_256\": %.5f,\n  \"eff_strassen1_128\": %.5f,\n"
                  "  \"eff_strassen1_256\": %.5f,\n  \"eff_strassen2_128\": %.5f,\n"
-                 "  \"eff_strassen2_256\": %.5f,\n  \"launch_us\": %.3f,\n  \"tile_fill_us\": %.3f,\n"
+                 "  \"eff_strassen2_256\": %.5f,\n  \"eff_strassen1_pair_128\": %.5f,\n"
+                 "  \"eff_strassen1_pair_256\": %.5f,\n  \"launch_us\": %.3f,\n  \"tile_fill_us\": %.3f,\n"
                  "  \"l2_bytes\": %.0f,\n  \"l2_gbs\": %.1f\n}\n",
                  m.num_sms, m.peak_tflops, m.hbm_gbs, m.eff_classical[0], m.eff_classical[1],
                  m.eff_classical[2], m.eff_pair[0], m.eff_pair[1], m.eff_strassen[0][0], m.eff_strassen[0][1], m.eff_strassen[1][0],
-                 m.eff_strassen[1][1], m.launch_us, m.tile_fill_us, m.l2_bytes, m.l2_gbs);
+                 m.eff_strassen[1][1], m.eff_strassen_pair[0], m.eff_strassen_pair[1], m.launch_us,
+                 m.tile_fill_us, m.l2_bytes, m.l2_gbs);
     std::fclose(f);
   }
   return FGEMM_OK;

@@ -78,6 +78,10 @@ cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, int grid,
 // `max_clusters` pairs (fewer if fewer fit on the device at once).
 cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int max_clusters, cudaStream_t stream);
 
+// One-level Strassen on CTA pairs (256 x bn tiles of the half-size block space).
+cudaError_t launch_strassen_pair(int bn, const KernelParams& p, int max_clusters,
+                                 cudaStream_t stream);
+
 // The Strassen coefficient table of `depth` levels (0: one trivial product).
 const StrassenTable& strassen_table(int depth);
 

@@ -13,4 +13,13 @@ cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int max_clusters, cu
   }
 }
 
+cudaError_t launch_strassen_pair(int bn, const KernelParams& p, int max_clusters,
+                                 cudaStream_t stream) {
+  switch (bn) {
+    case 128: return launch_strassen_pair_t<128>(p, max_clusters, stream);
+    case 256: return launch_strassen_pair_t<256>(p, max_clusters, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace fgemm

@@ -227,14 +227,15 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
   }
 }
 
-// Strassen product `pr` at tile (tm, tn): fold +-acc into the per-CTA fp32
+// Strassen product `pr` for the 128 rows starting at row0 (inside each
+// output block) of column tile tn: fold +-acc into the per-CTA fp32
 // partial tiles of the output blocks it feeds; after the last product, apply
 // the epilogue to every block and store C.  Workspace layout per CTA:
 // [block][32-column chunk][128 rows][32 floats], so a warp's 32 rows of one
 // chunk are 4 KB contiguous.  Every element is read and written only by the
 // thread that owns its row, in program order.
 template <int BN, int DEPTH>
-__device__ __forceinline__ void epilogue_strassen(const KernelParams& p, uint32_t tbase, int tm,
+__device__ __forceinline__ void epilogue_strassen(const KernelParams& p, uint32_t tbase, int row0,
                                                   int tn, int pr, int r, float* ws) {
   constexpr int G = 1 << DEPTH;
   constexpr int CH = BN / 32;
@@ -287,7 +288,7 @@ __device__ __forceinline__ void epilogue_strassen(const KernelParams& p, uint32_
             g[4 * q + 0] = a.x; g[4 * q + 1] = a.y; g[4 * q + 2] = a.z; g[4 * q + 3] = a.w;
             u[4 * q + 0] = b.x; u[4 * q + 1] = b.y; u[4 * q + 2] = b.z; u[4 * q + 3] = b.w;
           }
-          const int row = sr * p.sub_m + tm * kBM + r;
+          const int row = sr * p.sub_m + row0 + r;
           const int col0 = sc * p.sub_n + tn * BN + c * 32;
           finish_swiglu(p, col0, g, u);
           store_row32(p, row, col0, g);
@@ -303,7 +304,7 @@ __device__ __forceinline__ void epilogue_strassen(const KernelParams& p, uint32_
           const float4 a = w[q];
           v[4 * q + 0] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
         }
-        const int row = (s >> DEPTH) * p.sub_m + tm * kBM + r;
+        const int row = (s >> DEPTH) * p.sub_m + row0 + r;
         const int col0 = (s & (G - 1)) * p.sub_n + tn * BN + c * 32;
         finish_plain(p, col0, v);
         store_row32(p, row, col0, v);
@@ -603,7 +604,7 @@ __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
         if constexpr (DEPTH == 0) {
           epilogue_classical<BN>(p, tbase, tm * kBM, tn, r);
         } else {
-          epilogue_strassen<BN, DEPTH>(p, tbase, tm, tn, pr, r, ws);
+          epilogue_strassen<BN, DEPTH>(p, tbase, tm * kBM, tn, pr, r, ws);
         }
         ptx::tc_fence_before();
         __syncwarp();

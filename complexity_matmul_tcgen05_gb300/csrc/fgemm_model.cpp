@@ -51,12 +51,12 @@ bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo
   if (tile_m != 128 && tile_m != 256) return false;
   if (epi_kind == FGEMM_EPI_SWIGLU && tile_n == 64) return false;
   const int d = depth_of(algo);
-  if (tile_m == 256) return d == 0 && tile_n >= 128;
+  if (tile_m == 256 && (tile_n < 128 || d == 2)) return false;
   if (d == 0) return true;
   if (tile_n == 64) return false;
   const int64_t g = int64_t{1} << d;
   if (M <= 0 || N <= 0 || K <= 0) return false;
-  return M % (g * kBM) == 0 && N % (g * tile_n) == 0 && K % (g * kBK) == 0;
+  return M % (g * tile_m) == 0 && N % (g * tile_n) == 0 && K % (g * kBK) == 0;
 }
 
 }  // namespace fgemm
@@ -83,6 +83,8 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   m.eff_strassen[0][1] = 0.082;
   m.eff_strassen[1][0] = 0.034;
   m.eff_strassen[1][1] = 0.047;
+  m.eff_strassen_pair[0] = 0.097;  // 256 x 128 (8192^3: 250 TFLOP/s effective)
+  m.eff_strassen_pair[1] = 0.146;  // 256 x 256 (8192^3: 376 TFLOP/s effective)
   m.launch_us = 9.1;
   m.tile_fill_us = 2.3;
   m.l2_bytes = 126.0 * 1024 * 1024;
@@ -140,7 +142,9 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
   const int32_t slots = pair ? std::max(1, dev->num_sms / 2) : dev->num_sms;
   const int64_t waves = fgemm_model_waves(tiles, slots, nullptr);
   double eff;
-  if (d > 0)
+  if (d > 0 && pair)
+    eff = dev->eff_strassen_pair[tile_n == 128 ? 0 : 1];
+  else if (d > 0)
     eff = dev->eff_strassen[d - 1][tile_n == 128 ? 0 : 1];
   else if (pair)
     eff = dev->eff_pair[tile_n == 128 ? 0 : 1];

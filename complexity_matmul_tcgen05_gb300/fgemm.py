@@ -44,6 +44,7 @@ class DeviceModel(ctypes.Structure):
                 ("eff_classical", ctypes.c_double * 3),
                 ("eff_pair", ctypes.c_double * 2),
                 ("eff_strassen", (ctypes.c_double * 2) * 2),
+                ("eff_strassen_pair", ctypes.c_double * 2),
                 ("launch_us", ctypes.c_double), ("tile_fill_us", ctypes.c_double),
                 ("l2_bytes", ctypes.c_double), ("l2_gbs", ctypes.c_double)]
 

@@ -135,9 +135,9 @@ fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * As fgemm_matmul, with the output tile forced (used for exhaustive timing of
  * the decision model's choices). tile_m = 128: one CTA per tile, tile_n in
  * {64, 128, 256}; tile_m = 256: a pair of CTAs (one M = 256 tensor-core
- * operation across two SMs), tile_n in {128, 256}, classical form only.
- * SWIGLU needs tile_n >= 128; the Strassen forms use tile_m = 128 and tile_n
- * in {128, 256}. tile_m = tile_n = 0 lets the model choose; a zero in only
+ * operation across two SMs), tile_n in {128, 256}, classical and one-level
+ * Strassen forms. SWIGLU needs tile_n >= 128; the Strassen forms use tile_n
+ * in {128, 256}, two levels only with tile_m = 128. tile_m = tile_n = 0 lets the model choose; a zero in only
  * one of them lets the model choose the other.
  */
 fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N,
@@ -239,6 +239,7 @@ typedef struct {
   double eff_pair[2];      /* same for CTA-pair tiles 256 x {128, 256} */
   double eff_strassen[2][2]; /* [depth-1][tile_n 128, 256]: executed-MAC rate
                               * of the Strassen mainloop as a fraction of peak */
+  double eff_strassen_pair[2]; /* one level on CTA pairs, 256 x {128, 256} */
   double launch_us;        /* fixed cost of one launch */
   double tile_fill_us;     /* pipeline fill + drain cost per tile visit */
   double l2_bytes;         /* L2 capacity (bytes) */

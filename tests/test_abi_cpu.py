@@ -91,10 +91,12 @@ def test_validation_codes(L):
     assert _v(256, 256, 96, lda=96, algo="strassen1") == fgemm.ERR_UNSUPPORTED
     assert _v(512, 512, 256, algo="strassen2", tile=128) == ok
     assert _v(256, 512, 256, algo="strassen2") == fgemm.ERR_UNSUPPORTED
-    # CTA-pair tiles: 256 x {128, 256}, classical only
+    # CTA-pair tiles: 256 x {128, 256}, classical and one-level Strassen
     assert _v(512, 512, 256, tile_m=256, tile=128) == ok
     assert _v(512, 512, 256, tile_m=256, tile=64) == fgemm.ERR_UNSUPPORTED
-    assert _v(512, 512, 256, algo="strassen1", tile_m=256) == fgemm.ERR_UNSUPPORTED
+    assert _v(512, 512, 256, algo="strassen1", tile_m=256) == ok
+    assert _v(256, 512, 256, algo="strassen1", tile_m=256) == fgemm.ERR_UNSUPPORTED  # 2 x 256 rows
+    assert _v(1024, 1024, 512, algo="strassen2", tile_m=256) == fgemm.ERR_UNSUPPORTED
     assert _v(512, 512, 256, tile_m=192) == fgemm.ERR_INVALID_ARG
     assert _v(100, 512, 256, tile_m=256) == ok                     # ragged rows are fine
 

@@ -68,6 +68,16 @@ def test_exact_ternary(algo, M, N, K, tile, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K,tile", [(512, 512, 128, 128), (512, 1024, 256, 256),
+                                        (1024, 2048, 640, 256), (1536, 768, 384, 128)])
+def test_exact_ternary_strassen_cta_pair(M, N, K, tile, dtype):
+    """One-level Strassen on CTA pairs (TMA-staged operand sums): bit-exact."""
+    A, B, bias = _ternary(M, N, K, dtype)
+    C = run(A, B, algo="strassen1", epilogue="scale_bias", bias=bias, tile_n=tile, tile_m=256)
+    assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("M,N,K,tile", EXACT_PAIR_CASES)
 def test_exact_ternary_cta_pair(M, N, K, tile, dtype):
     A, B, bias = _ternary(M, N, K, dtype)
@@ -144,7 +154,7 @@ def test_classical_epilogues_every_entry(epilogue, alpha, tile_m, tile):
 @pytest.mark.parametrize("algo,tile_m,tile,depth", [
     ("classical", 128, 128, 0), ("classical", 128, 256, 0), ("classical", 256, 128, 0),
     ("classical", 256, 256, 0), ("strassen1", 128, 128, 1), ("strassen1", 128, 256, 1),
-    ("strassen2", 128, 128, 2)])
+    ("strassen1", 256, 256, 1), ("strassen2", 128, 128, 2)])
 def test_swiglu_every_entry(algo, tile_m, tile, depth):
     M, N, K = 512, 2048, 512
     A = inputs.matrix(M, K, "normal", "bf16", 0, DEV)
@@ -153,16 +163,17 @@ def test_swiglu_every_entry(algo, tile_m, tile, depth):
     _full_check(A, B, algo, "bf16", "swiglu", 1.0, bias, tile, depth, tile_m=tile_m)
 
 
-@pytest.mark.parametrize("algo,tile,depth", [("strassen1", 128, 1), ("strassen1", 256, 1),
-                                             ("strassen2", 128, 2), ("strassen2", 256, 2)])
+@pytest.mark.parametrize("algo,tile_m,tile,depth", [
+    ("strassen1", 128, 128, 1), ("strassen1", 128, 256, 1), ("strassen1", 256, 128, 1),
+    ("strassen1", 256, 256, 1), ("strassen2", 128, 128, 2), ("strassen2", 128, 256, 2)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_strassen_every_entry_and_emulation(algo, tile, depth, dtype):
+def test_strassen_every_entry_and_emulation(algo, tile_m, tile, depth, dtype):
     """Normwise bound and the tighter pin: GPU Strassen vs the emulated
     (rounded-operand) Strassen of the oracle."""
     M, N, K = 512, 1024, 768
     A = inputs.matrix(M, K, "uniform", dtype, 0, DEV)
     B = inputs.matrix(K, N, "uniform", dtype, 1, DEV)
-    _full_check(A, B, algo, dtype, tile=tile, depth=depth)
+    _full_check(A, B, algo, dtype, tile=tile, depth=depth, tile_m=tile_m)
 
 
 # -------------------------------------------------------------- edge cases
