@@ -24,6 +24,7 @@
 namespace fgemm {
 bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo_t algo,
                    int32_t tile_m, int32_t tile_n);
+
 }
 
 using fgemm::KernelParams;
@@ -678,6 +679,18 @@ fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, c
                             int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
                             fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo) {
   return fgemm_matmul_ex(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, 0, 0);
+}
+
+fgemm_status_t fgemm_selftest_wait_timeout(fgemm_handle_t h, int32_t limit_ms) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  if (limit_ms < 1 || limit_ms > 10000)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "limit_ms must be in 1..10000");
+  KernelParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.err = h->d_err;
+  p.spin_ns = static_cast<unsigned long long>(limit_ms) * 1000000ull;
+  cudaError_t e = fgemm::launch_selftest_wait(p, h->stream);
+  return e == cudaSuccess ? FGEMM_OK : cuda_fail(h, e, "self-test launch");
 }
 
 fgemm_status_t fgemm_get_error(fgemm_handle_t h) {

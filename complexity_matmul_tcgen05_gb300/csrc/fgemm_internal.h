@@ -85,6 +85,9 @@ cudaError_t launch_strassen_pair(int bn, const KernelParams& p, int max_clusters
 // The Strassen coefficient table of `depth` levels (0: one trivial product).
 const StrassenTable& strassen_table(int depth);
 
+// One block whose bounded wait on a never-completed mbarrier runs out.
+cudaError_t launch_selftest_wait(const KernelParams& p, cudaStream_t stream);
+
 // C[i][j] = epi(bias[j]) for K == 0 (the product is empty).
 cudaError_t launch_k0_fill(const KernelParams& p, cudaStream_t stream);
 

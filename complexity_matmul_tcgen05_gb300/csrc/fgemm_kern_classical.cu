@@ -51,6 +51,24 @@ __global__ void k0_fill_kernel(const __grid_constant__ KernelParams p) {
   }
 }
 
+// Nothing ever arrives on `bar`, so the wait for its phase 0 can only end
+// by its time limit; the helper then latches the timeout in p.err.
+__global__ void selftest_wait_kernel(const __grid_constant__ KernelParams p) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_one(ptx::smem_u32(&bar), 0, p, 0);
+  __syncthreads();
+}
+
+cudaError_t launch_selftest_wait(const KernelParams& p, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_k0_fill(const KernelParams& p, cudaStream_t stream) {
   const long long total = static_cast<long long>(p.M) * p.n_out;
   const int threads = 256;

@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
                                  ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(ctypes.c_double)]
         L.fgemm_get_error.argtypes = [vp]
+        L.fgemm_selftest_wait_timeout.argtypes = [vp, i32]
         L.fgemm_calibrate.argtypes = [vp, ctypes.c_char_p]
         L.fgemm_status_string.argtypes = [st]
         L.fgemm_status_string.restype = ctypes.c_char_p
@@ -106,7 +107,7 @@ def lib() -> ctypes.CDLL:
                      "fgemm_matmul_ex", "fgemm_plan", "fgemm_get_error", "fgemm_calibrate",
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
-                     "fgemm_strassen_matmul_static"):
+                     "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout"):
             getattr(L, name).restype = st
         _lib = L
         return L

@@ -171,6 +171,16 @@ fgemm_status_t fgemm_get_error(fgemm_handle_t h);
  */
 fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out_path);
 
+/*
+ * Failure-detection self-test. Launches a one-block kernel that waits on an
+ * mbarrier nothing will ever complete, through the same bounded wait every
+ * GEMM kernel uses, with the limit set to limit_ms (1..10000) for this
+ * launch. The wait gives up, the kernel latches a timeout in the handle's
+ * error word and exits normally: no fault, no trap, and the handle stays
+ * usable. Asynchronous; fgemm_get_error then returns FGEMM_ERR_TIMEOUT.
+ */
+fgemm_status_t fgemm_selftest_wait_timeout(fgemm_handle_t h, int32_t limit_ms);
+
 /* Static string naming a status. */
 const char* fgemm_status_string(fgemm_status_t s);
 

@@ -237,3 +237,28 @@ def test_two_handles_two_streams():
     assert np.array_equal(gpu_bits(C1), ref) and np.array_equal(gpu_bits(C2), ref)
     assert h2.get_error() == fgemm.OK
     h2.close()
+
+
+# ------------------------------------------------------- failure detection
+
+def test_bounded_wait_reports_timeout_and_handle_survives():
+    """A wait that nothing will complete gives up after its limit, the kernel
+    exits, fgemm_get_error reports the timeout (role and block), and the same
+    handle then computes a correct product."""
+    import time
+    h = fgemm.Handle()
+    assert h.get_error() == fgemm.OK
+    t0 = time.perf_counter()
+    assert fgemm.lib().fgemm_selftest_wait_timeout(h.ptr, 50) == fgemm.OK
+    status = h.get_error()
+    elapsed = time.perf_counter() - t0
+    assert status == fgemm.ERR_TIMEOUT
+    assert "producer" in h.last_message()
+    assert 0.045 <= elapsed < 5.0
+    assert h.get_error() == fgemm.OK            # the word was cleared
+    A, B, bias = _ternary(256, 256, 128, "bf16", seed=80)
+    C = fgemm.matmul(A, B, epilogue="scale_bias", bias=bias, algo="classical", handle=h)
+    torch.cuda.synchronize()
+    assert h.get_error() == fgemm.OK
+    assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, "bf16"))
+    h.close()
