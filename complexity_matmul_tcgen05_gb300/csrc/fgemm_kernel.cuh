@@ -150,33 +150,51 @@ __device__ __forceinline__ void store_row32(const KernelParams& p, int row, int 
   }
 }
 
-// v[j] = act(alpha * x[j] + bias[col0 + j]) for the non-gated epilogues.
-__device__ __forceinline__ void finish_plain(const KernelParams& p, int col0, float (&v)[32]) {
-  const int last = p.n_out - 1;
+// b[j] = bias[base + min(col0 + j, n_out - 1)] (0 without a bias), for every
+// lane of the warp: each lane loads one entry and the warp exchanges them by
+// shuffles.  Warp-collective: call it outside row-dependent branches.
+__device__ __forceinline__ void bias32(const KernelParams& p, int base, int col0, float (&b)[32]) {
+  if (!p.bias) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) b[j] = 0.0f;
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const float mine = ld_bias(p, base + min(col0 + lane, p.n_out - 1));
+#pragma unroll
+  for (int j = 0; j < 32; ++j) b[j] = __shfl_sync(0xFFFFFFFFu, mine, j);
+}
+
+// v[j] = act(alpha * x[j] + b[j]) for the non-gated epilogues.
+__device__ __forceinline__ void finish_plain(const KernelParams& p, const float (&b)[32],
+                                             float (&v)[32]) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    float x = p.alpha * v[j];
-    if (p.bias) x += ld_bias(p, min(col0 + j, last));
+    float x = p.alpha * v[j] + b[j];
     if (p.epi == kEpiSilu) x = silu(x);
     v[j] = x;
   }
 }
 
-// v[j] = silu(alpha * g + bias[col0 + j]) * (alpha * u + bias[n_out + col0 + j]).
-__device__ __forceinline__ void finish_swiglu(const KernelParams& p, int col0, float (&g)[32],
+// g[j] = silu(alpha * g + bg[j]) * (alpha * u + bu[j]).
+__device__ __forceinline__ void finish_swiglu(const KernelParams& p, const float (&bg)[32],
+                                              const float (&bu)[32], float (&g)[32],
                                               const float (&u)[32]) {
-  const int last = p.n_out - 1;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    float gv = p.alpha * g[j];
-    float uv = p.alpha * u[j];
-    if (p.bias) {
-      const int cj = min(col0 + j, last);
-      gv += ld_bias(p, cj);
-      uv += ld_bias(p, p.n_out + cj);
-    }
-    g[j] = silu(gv) * uv;
-  }
+  for (int j = 0; j < 32; ++j) g[j] = silu(p.alpha * g[j] + bg[j]) * (p.alpha * u[j] + bu[j]);
+}
+
+// finish_swiglu with one bias array live at a time (for the 128-register
+// Strassen kernels).  Warp-collective like bias32.
+__device__ __forceinline__ void finish_swiglu_warp(const KernelParams& p, int col0, float (&g)[32],
+                                                   const float (&u)[32]) {
+  float b[32];
+  bias32(p, 0, col0, b);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) g[j] = silu(p.alpha * g[j] + b[j]);
+  bias32(p, p.n_out, col0, b);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) g[j] *= p.alpha * u[j] + b[j];
 }
 
 // ------------------------------------------------------------ epilogues
@@ -198,6 +216,9 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
       ptx::tmem_ld_32x32b_x32(tbase + HALF + c * 32, ur);
       ptx::tmem_wait_ld();
       const int col0 = tn * HALF + c * 32;
+      float bg[32], bu[32];
+      bias32(p, 0, col0, bg);
+      bias32(p, p.n_out, col0, bu);
       if (row_ok && col0 < p.n_out) {
         float g[32], u[32];
 #pragma unroll
@@ -205,7 +226,7 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
           g[j] = __uint_as_float(gr[j]);
           u[j] = __uint_as_float(ur[j]);
         }
-        finish_swiglu(p, col0, g, u);
+        finish_swiglu(p, bg, bu, g, u);
         store_row32(p, row, col0, g);
       }
     }
@@ -216,11 +237,13 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
       ptx::tmem_ld_32x32b_x32(tbase + c * 32, ar);
       ptx::tmem_wait_ld();
       const int col0 = tn * BN + c * 32;
+      float b[32];
+      bias32(p, 0, col0, b);
       if (row_ok && col0 < p.n_out) {
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ar[j]);
-        finish_plain(p, col0, v);
+        finish_plain(p, b, v);
         store_row32(p, row, col0, v);
       }
     }
@@ -290,7 +313,7 @@ __device__ __forceinline__ void epilogue_strassen(const KernelParams& p, uint32_
           }
           const int row = sr * p.sub_m + row0 + r;
           const int col0 = sc * p.sub_n + tn * BN + c * 32;
-          finish_swiglu(p, col0, g, u);
+          finish_swiglu_warp(p, col0, g, u);
           store_row32(p, row, col0, g);
         }
       }
@@ -306,7 +329,9 @@ __device__ __forceinline__ void epilogue_strassen(const KernelParams& p, uint32_
         }
         const int row = (s >> DEPTH) * p.sub_m + row0 + r;
         const int col0 = (s & (G - 1)) * p.sub_n + tn * BN + c * 32;
-        finish_plain(p, col0, v);
+        float b[32];
+        bias32(p, 0, col0, b);
+        finish_plain(p, b, v);
         store_row32(p, row, col0, v);
       }
     }
