@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--tile", type=int, default=0, help="tile_n (0 = model)")
     ap.add_argument("--tile-m", type=int, default=0, help="tile_m: 128 one CTA, 256 CTA pair")
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0 = auto)")
+    ap.add_argument("--split", default="auto", choices=["off", "auto", "force"],
+                    help="K split of the last wave of CTA-pair tiles")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
@@ -305,6 +307,7 @@ def run_fgemm(args, rank, world):
     for i in range(sets):
         Cs.append(torch.empty((M, n_out), dtype=A0.dtype, device=dev))
     handle = fgemm.default_handle()
+    handle.set_split_mode(args.split)
     stream = torch.cuda.current_stream(dev)
     algo, tile, tile_m = args.algo, args.tile, args.tile_m
     if algo == "auto":
@@ -427,6 +430,7 @@ def run_fgemm(args, rank, world):
         "data": "synthetic",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K, "epilogue": epi,
                    "algo": plan_algo, "tile_m": plan_tm, "tile_n": plan_tile,
+                   "k_split": args.split,
                    "predicted_us": pred_us, "l2": f"{sets} rotating input/output sets "
                    f"({sets * set_bytes / 2 ** 20:.0f} MiB) cycled between steps",
                    "parallelism": f"replicas x{world}"},

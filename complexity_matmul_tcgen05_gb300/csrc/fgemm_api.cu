@@ -228,6 +228,10 @@ struct fgemm_handle_s {
   unsigned int* d_err = nullptr;
   float* workspace = nullptr;
   size_t ws_bytes = 0;
+  unsigned int* split_ctr = nullptr;  // K-split arrival counters (zeroed once)
+  size_t split_ctr_count = 0;
+  unsigned int split_gen = 0;         // generation of the last split launch
+  int split_mode = 1;                 // 0 never, 1 auto, 2 whenever possible
   unsigned long long spin_ns = 1000000000ull;
   fgemm_device_model_t model{};
   std::unordered_map<PlanKey, Plan, PlanKeyHash> plans;
@@ -382,9 +386,52 @@ fgemm_status_t ensure_workspace(fgemm_handle_t h, size_t bytes) {
   cudaError_t e = cudaMalloc(&h->workspace, bytes);
   if (e != cudaSuccess) {
     h->workspace = nullptr;
-    return cuda_fail(h, e, "cudaMalloc(Strassen workspace)");
+    return cuda_fail(h, e, "cudaMalloc(partial-tile workspace)");
   }
   h->ws_bytes = bytes;
+  return FGEMM_OK;
+}
+
+// Workspace, counters and generation of a K-split pair launch.
+fgemm_status_t prepare_split(fgemm_handle_t h, KernelParams* p, int split, int pieces, int bn) {
+  const size_t slots = static_cast<size_t>(split) * pieces * 2;
+  fgemm_status_t s =
+      ensure_workspace(h, slots * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float));
+  if (s != FGEMM_OK) return s;
+  const size_t ctrs = static_cast<size_t>(split) * 8;  // 2 CTAs x 4 epilogue warps
+  if (ctrs > h->split_ctr_count) {
+    if (h->split_ctr) {
+      cudaError_t e = cudaStreamSynchronize(h->stream);
+      if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+      cudaFree(h->split_ctr);
+      h->split_ctr = nullptr;
+      h->split_ctr_count = 0;
+    }
+    const size_t n = std::max<size_t>(ctrs, static_cast<size_t>(8) * h->num_sms);
+    cudaError_t e = cudaMalloc(&h->split_ctr, n * sizeof(unsigned int));
+    if (e != cudaSuccess) {
+      h->split_ctr = nullptr;
+      return cuda_fail(h, e, "cudaMalloc(split counters)");
+    }
+    e = cudaMemset(h->split_ctr, 0, n * sizeof(unsigned int));
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemset(split counters)");
+    h->split_ctr_count = n;
+    h->split_gen = 0;
+  }
+  // Counters hold gen << 8 | arrivals; a counter tagged with an older
+  // generation (e.g. left by a launch that ended on an error) reads as zero
+  // arrivals.  When the 24-bit generation wraps, clear them all.
+  if (++h->split_gen >= (1u << 24)) {
+    cudaError_t e =
+        cudaMemsetAsync(h->split_ctr, 0, h->split_ctr_count * sizeof(unsigned int), h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync(split counters)");
+    h->split_gen = 1;
+  }
+  p->split_tiles = split;
+  p->split_pieces = pieces;
+  p->split_gen = h->split_gen;
+  p->split_ctr = h->split_ctr;
+  p->split_ws = h->workspace;
   return FGEMM_OK;
 }
 
@@ -434,7 +481,7 @@ fgemm_status_t load_calibration(fgemm_handle_t h, const char* path) {
       {"eff_strassen1_256", &m.eff_strassen[0][1]}, {"eff_strassen2_128", &m.eff_strassen[1][0]},
       {"eff_strassen2_256", &m.eff_strassen[1][1]}, {"launch_us", &m.launch_us},
       {"tile_fill_us", &m.tile_fill_us},        {"l2_bytes", &m.l2_bytes},
-      {"l2_gbs", &m.l2_gbs},
+      {"l2_gbs", &m.l2_gbs},                    {"split_fix_us", &m.split_fix_us},
   };
   int found = 0;
   for (auto& fd : fields) found += json_number(text, fd.key, fd.dst) ? 1 : 0;
@@ -534,8 +581,16 @@ fgemm_status_t fgemm_destroy(fgemm_handle_t h) {
   if (!h) return FGEMM_OK;
   cudaStreamSynchronize(h->stream);
   if (h->workspace) cudaFree(h->workspace);
+  if (h->split_ctr) cudaFree(h->split_ctr);
   if (h->d_err) cudaFree(h->d_err);
   delete h;
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_set_split_mode(fgemm_handle_t h, int32_t mode) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  if (mode < 0 || mode > 2) return set_msg(h, FGEMM_ERR_INVALID_ARG, "split mode must be 0, 1 or 2");
+  h->split_mode = mode;
   return FGEMM_OK;
 }
 
@@ -659,7 +714,18 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
     return FGEMM_OK;
   }
   if (bm == 256) {
-    cudaError_t e = fgemm::launch_gemm_pair(bn, p, h->num_sms / 2, h->stream);
+    const int fit = fgemm::gemm_pair_clusters_fit(bn);
+    if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the CTA-pair launch");
+    int32_t pieces = 1;
+    const int split =
+        fgemm_model_split_tail(&h->model, units, fit, p.k_blocks, bn, h->split_mode, &pieces);
+    int clusters = static_cast<int>(std::min<long long>(fit, units));
+    if (split > 0) {
+      clusters = fit;  // the schedule is planned for every pair that fits
+      s = prepare_split(h, &p, split, pieces, bn);
+      if (s != FGEMM_OK) return s;
+    }
+    cudaError_t e = fgemm::launch_gemm_pair(bn, p, clusters, h->stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "GEMM pair kernel launch");
     return FGEMM_OK;
   }
@@ -780,11 +846,34 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
       if (!time_gemm(n, n, n, FGEMM_ALGO_CLASSICAL, 128, tiles[i], &us)) break;
       m.eff_classical[i] = flops / (us * 1e6) / m.peak_tflops;
     }
+    const int saved_split = h->split_mode;
+    h->split_mode = 0;  // mainloop efficiencies are taken on whole waves
+    double pair256_us = 0;
     for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
       double us = 0;
       if (!time_gemm(n, n, n, FGEMM_ALGO_CLASSICAL, 256, tiles[i + 1], &us)) break;
       m.eff_pair[i] = flops / (us * 1e6) / m.peak_tflops;
+      if (i == 1) pair256_us = us;
     }
+    if (status == FGEMM_OK) {
+      // split_fix_us: the split form's time against whole waves, less the
+      // idle share of the last wave it removes
+      h->split_mode = 2;
+      double us = 0;
+      const int fit = fgemm::gemm_pair_clusters_fit(256);
+      const int64_t pair_tiles = (n / 256) * (n / 256);
+      int32_t pieces = 1;
+      const int split =
+          fgemm_model_split_tail(nullptr, pair_tiles, fit, static_cast<int32_t>(n / 64), 256, 2, &pieces);
+      if (split > 0 && time_gemm(n, n, n, FGEMM_ALGO_CLASSICAL, 256, 256, &us)) {
+        // whole waves: W + 1 tile times; split: W + 1/S tile times + (S-1) * fix
+        const int64_t waves = (pair_tiles + fit - 1) / fit;
+        const double t_tile = pair256_us / static_cast<double>(waves);
+        const double saved = (1.0 - 1.0 / pieces) * t_tile;
+        m.split_fix_us = std::min(50.0, std::max(0.5, (us - pair256_us + saved) / (pieces - 1)));
+      }
+    }
+    h->split_mode = saved_split;
     for (int d = 1; d <= 2 && status == FGEMM_OK; ++d) {
       for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
         double us = 0;
@@ -841,11 +930,11 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
                  "  \"eff_strassen1_256\": %.5f,\n  \"eff_strassen2_128\": %.5f,\n"
                  "  \"eff_strassen2_256\": %.5f,\n  \"eff_strassen1_pair_128\": %.5f,\n"
                  "  \"eff_strassen1_pair_256\": %.5f,\n  \"launch_us\": %.3f,\n  \"tile_fill_us\": %.3f,\n"
-                 "  \"l2_bytes\": %.0f,\n  \"l2_gbs\": %.1f\n}\n",
+                 "  \"l2_bytes\": %.0f,\n  \"l2_gbs\": %.1f,\n  \"split_fix_us\": %.3f\n}\n",
                  m.num_sms, m.peak_tflops, m.hbm_gbs, m.eff_classical[0], m.eff_classical[1],
                  m.eff_classical[2], m.eff_pair[0], m.eff_pair[1], m.eff_strassen[0][0], m.eff_strassen[0][1], m.eff_strassen[1][0],
                  m.eff_strassen[1][1], m.eff_strassen_pair[0], m.eff_strassen_pair[1], m.launch_us,
-                 m.tile_fill_us, m.l2_bytes, m.l2_gbs);
+                 m.tile_fill_us, m.l2_bytes, m.l2_gbs, m.split_fix_us);
     std::fclose(f);
   }
   return FGEMM_OK;

@@ -14,6 +14,7 @@ constexpr int kBK = 64;           // K per pipeline stage = one 128-byte swizzle
 constexpr int kMaxDepth = 2;      // Strassen recursion levels supported
 constexpr int kMaxProducts = 49;  // 7^2
 constexpr int kMaxTerms = 4;      // 2^depth source blocks per formed operand
+constexpr int kMaxSplitPieces = 4;  // K pieces per split tile (each last piece reads S - 1)
 
 // Term codes in the Strassen tables: bits [0,5) block index
 // (row_block << depth | col_block) in the 2^depth x 2^depth block grid,
@@ -35,6 +36,62 @@ struct StrassenTable {
 };
 
 enum EpiKind : int { kEpiNone = 0, kEpiScaleBias = 1, kEpiSilu = 2, kEpiSwiglu = 3 };
+
+#ifdef __CUDACC__
+#define FGEMM_HD __host__ __device__
+#else
+#define FGEMM_HD
+#endif
+
+// ---------------------------------------------------------------------------
+// Work schedule of the persistent CTA-pair kernel, with the last partial
+// wave split along K.
+//
+// With T output tiles on P clusters, R = T mod P tiles would run alone in a
+// last, partly idle wave.  When 2R <= P, those R tiles (the FIRST R units in
+// the rasterised order, so that they share row blocks of A with the first
+// wave of whole tiles) are each cut into S = floor(P / R) pieces of equal K
+// range; piece s of split tile t runs on cluster t * S + s, as that
+// cluster's first work item.  Every cluster then runs its (T - R) / P whole
+// tiles, units R + c, R + c + P, ...  The kernel takes W + 1/S tile times
+// instead of W + 1.
+//
+// Every piece stores its fp32 partial tile; the piece that finishes last
+// (per 32-row warp slice, decided by a counter) sums the pieces in piece
+// order, so the result does not depend on which finished last, and applies
+// the epilogue.  No CTA waits for another.  Its sum overlaps the MMAs of the
+// cluster's first whole tile.
+struct WorkItem {
+  int unit;     // output tile (unit_coords order)
+  int k0, k1;   // K blocks [k0, k1) of the tile
+  int piece;    // index of this piece among the tile's pieces
+  int npieces;  // 1 for a whole tile
+};
+
+// The n-th work item of `cluster` (false once its list is exhausted).
+FGEMM_HD inline bool work_item(int num_units, int split_tiles, int split_pieces, int clusters,
+                               int k_blocks, int cluster, int n, WorkItem& w) {
+  const bool has_piece = split_tiles > 0 && cluster < split_tiles * split_pieces;
+  if (has_piece && n == 0) {
+    const int s = cluster % split_pieces;
+    w.unit = cluster / split_pieces;
+    w.k0 = static_cast<int>(static_cast<long long>(s) * k_blocks / split_pieces);
+    w.k1 = static_cast<int>(static_cast<long long>(s + 1) * k_blocks / split_pieces);
+    w.piece = s;
+    w.npieces = split_pieces;
+    return true;
+  }
+  const int i = n - (has_piece ? 1 : 0);
+  const int whole = num_units - split_tiles;
+  const int count = cluster < whole ? (whole - cluster + clusters - 1) / clusters : 0;
+  if (i >= count) return false;
+  w.unit = split_tiles + cluster + i * clusters;
+  w.k0 = 0;
+  w.k1 = k_blocks;
+  w.piece = 0;
+  w.npieces = 1;
+  return true;
+}
 
 struct KernelParams {
   CUtensorMap tmap_a;  // A: inner dim K, outer M, box {64, 128}, 128B swizzle
@@ -60,6 +117,12 @@ struct KernelParams {
   float alpha;
   int num_products;
   StrassenTable tab;
+  // K split of the last partial wave (CTA-pair classical kernel only)
+  int split_tiles;          // tiles split along K (0: none), units [0, split_tiles)
+  int split_pieces;         // pieces per split tile (>= 2 when split_tiles > 0)
+  unsigned int split_gen;   // launch generation tagging the counters, 1 .. 2^24 - 1
+  unsigned int* split_ctr;  // per (split tile, CTA rank, epilogue warp): gen << 8 | arrivals
+  float* split_ws;          // per (split tile, piece, CTA rank): 128 x BN fp32, [col/4][row][4]
 };
 
 // Error word layout written by a kernel whose bounded wait ran out.
@@ -74,9 +137,14 @@ int kernel_threads(int depth);
 cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, int grid,
                         cudaStream_t stream);
 
-// Classical kernel on CTA pairs: 256 x bn tiles (bn = 128 or 256), at most
-// `max_clusters` pairs (fewer if fewer fit on the device at once).
-cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int max_clusters, cudaStream_t stream);
+// Classical kernel on CTA pairs: 256 x bn tiles (bn = 128 or 256) on exactly
+// `clusters` pairs, which must not exceed gemm_pair_clusters_fit(bn) and must
+// equal the cluster count p's split schedule was planned for.
+cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int clusters, cudaStream_t stream);
+
+// How many clusters of the classical pair kernel fit on the current device
+// at once (0 on error).
+int gemm_pair_clusters_fit(int bn);
 
 // One-level Strassen on CTA pairs (256 x bn tiles of the half-size block space).
 cudaError_t launch_strassen_pair(int bn, const KernelParams& p, int max_clusters,

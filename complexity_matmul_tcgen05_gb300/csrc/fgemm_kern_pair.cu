@@ -5,11 +5,19 @@
 
 namespace fgemm {
 
-cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int max_clusters, cudaStream_t stream) {
+cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int clusters, cudaStream_t stream) {
   switch (bn) {
-    case 128: return launch_gemm_pair_t<128>(p, max_clusters, stream);
-    case 256: return launch_gemm_pair_t<256>(p, max_clusters, stream);
+    case 128: return launch_gemm_pair_t<128>(p, clusters, stream);
+    case 256: return launch_gemm_pair_t<256>(p, clusters, stream);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+int gemm_pair_clusters_fit(int bn) {
+  switch (bn) {
+    case 128: return gemm_pair_clusters_fit_t<128>();
+    case 256: return gemm_pair_clusters_fit_t<256>();
+    default: return 0;
   }
 }
 

@@ -201,50 +201,76 @@ __device__ __forceinline__ void finish_swiglu_warp(const KernelParams& p, int co
 
 // Classical tile: the accumulator in TMEM columns [tbase, tbase + BN).  For
 // SwiGLU the tile's first BN/2 columns hold gate columns and the last BN/2
-// the matching up columns (the producer loads them side by side).
+// the matching up columns (the producer loads them side by side).  Every
+// bias entry the tile needs is loaded up front (one per lane per 32-column
+// chunk, broadcast by shuffles), and for the plain epilogues the TMEM load of
+// the next chunk is in flight while the current one is finished and stored.
 template <int BN>
 __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32_t tbase, int row0,
                                                    int tn, int r) {
+  const int lane = threadIdx.x & 31;
   const int row = row0 + r;
   const bool row_ok = row < p.M;
   if (p.epi == kEpiSwiglu) {
     constexpr int HALF = BN / 2;
-#pragma unroll 1
-    for (int c = 0; c < HALF / 32; ++c) {
+    constexpr int CH = HALF / 32;
+    float bg[CH], bu[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int col = min(tn * HALF + c * 32 + lane, p.n_out - 1);
+      bg[c] = p.bias ? ld_bias(p, col) : 0.0f;
+      bu[c] = p.bias ? ld_bias(p, p.n_out + col) : 0.0f;
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
       uint32_t gr[32], ur[32];
       ptx::tmem_ld_32x32b_x32(tbase + c * 32, gr);
       ptx::tmem_ld_32x32b_x32(tbase + HALF + c * 32, ur);
       ptx::tmem_wait_ld();
+      ptx::tmem_regs_ready(gr);
+      ptx::tmem_regs_ready(ur);
       const int col0 = tn * HALF + c * 32;
-      float bg[32], bu[32];
-      bias32(p, 0, col0, bg);
-      bias32(p, p.n_out, col0, bu);
-      if (row_ok && col0 < p.n_out) {
-        float g[32], u[32];
+      float g[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          g[j] = __uint_as_float(gr[j]);
-          u[j] = __uint_as_float(ur[j]);
-        }
-        finish_swiglu(p, bg, bu, g, u);
-        store_row32(p, row, col0, g);
+      for (int j = 0; j < 32; ++j) {
+        const float gv = p.alpha * __uint_as_float(gr[j]) + __shfl_sync(0xFFFFFFFFu, bg[c], j);
+        const float uv = p.alpha * __uint_as_float(ur[j]) + __shfl_sync(0xFFFFFFFFu, bu[c], j);
+        g[j] = silu(gv) * uv;
       }
+      if (row_ok && col0 < p.n_out) store_row32(p, row, col0, g);
     }
   } else {
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t ar[32];
-      ptx::tmem_ld_32x32b_x32(tbase + c * 32, ar);
-      ptx::tmem_wait_ld();
-      const int col0 = tn * BN + c * 32;
-      float b[32];
-      bias32(p, 0, col0, b);
-      if (row_ok && col0 < p.n_out) {
-        float v[32];
+    constexpr int CH = BN / 32;
+    float bl[CH];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ar[j]);
-        finish_plain(p, b, v);
-        store_row32(p, row, col0, v);
+    for (int c = 0; c < CH; ++c)
+      bl[c] = p.bias ? ld_bias(p, min(tn * BN + c * 32 + lane, p.n_out - 1)) : 0.0f;
+    auto finish = [&](int c, const uint32_t (&ar)[32]) {
+      const int col0 = tn * BN + c * 32;
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float x = p.alpha * __uint_as_float(ar[j]) + __shfl_sync(0xFFFFFFFFu, bl[c], j);
+        if (p.epi == kEpiSilu) x = silu(x);
+        v[j] = x;
+      }
+      if (row_ok && col0 < p.n_out) store_row32(p, row, col0, v);
+    };
+    uint32_t ra[32], rb[32];
+    ptx::tmem_ld_32x32b_x32(tbase, ra);
+    ptx::tmem_wait_ld();
+    ptx::tmem_regs_ready(ra);
+#pragma unroll
+    for (int c = 0; c < CH; c += 2) {  // CH is even for every tile width
+      ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, rb);
+      finish(c, ra);
+      ptx::tmem_wait_ld();
+      ptx::tmem_regs_ready(rb);
+      if (c + 2 < CH) ptx::tmem_ld_32x32b_x32(tbase + (c + 2) * 32, ra);
+      finish(c + 1, rb);
+      if (c + 2 < CH) {
+        ptx::tmem_wait_ld();
+        ptx::tmem_regs_ready(ra);
       }
     }
   }

@@ -38,6 +38,124 @@ struct PairCfg {
   static_assert((2 * kStages + 5) * 8 + 4 <= kBarBytes, "barrier area too small");
 };
 
+// One piece of a K-split tile, for this thread's row r of the CTA's 128 rows:
+// store the piece's fp32 partial (layout [col/4][row][4]: a lane moves 16
+// bytes of its row, a warp 512 contiguous bytes), then count the arrival on
+// the (tile, rank, warp) counter.  A warp that is not the last for its 32
+// rows hands the TMEM buffer back at once.  The last one sums the pieces in
+// piece order (its own from TMEM, the others from the workspace), applies the
+// ordinary epilogue to the sum, then hands the buffer back.  Hands the buffer
+// back itself (arrives on `tempty_remote`).
+template <int BN>
+__device__ __forceinline__ void epilogue_split_piece(const KernelParams& p, uint32_t tbase, int row0,
+                                                     int tn, int r, const WorkItem& w,
+                                                     uint32_t rank, int ew,
+                                                     uint32_t tempty_remote) {
+  const int lane = threadIdx.x & 31;
+  const int t = w.unit;  // the split region is units [0, split_tiles)
+  constexpr size_t kSlot = static_cast<size_t>(kBM) * BN;
+  const size_t piece_stride = 2 * kSlot;  // slots are [tile][piece][rank]
+  float* tile_ws = p.split_ws + (static_cast<size_t>(t) * p.split_pieces * 2 + rank) * kSlot;
+  float4* mine = reinterpret_cast<float4*>(tile_ws + static_cast<size_t>(w.piece) * piece_stride);
+  auto release = [&]() {
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive_cluster(tempty_remote);
+  };
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t ar[32];
+    ptx::tmem_ld_32x32b_x32(tbase + c * 32, ar);
+    ptx::tmem_wait_ld();
+    ptx::tmem_regs_ready(ar);
+    float4* dst = mine + static_cast<size_t>(c * 8) * kBM + r;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      __stcg(dst + q * kBM, make_float4(__uint_as_float(ar[4 * q + 0]), __uint_as_float(ar[4 * q + 1]),
+                                        __uint_as_float(ar[4 * q + 2]), __uint_as_float(ar[4 * q + 3])));
+  }
+  __threadfence();
+  __syncwarp();
+  unsigned int count = 0;
+  if (lane == 0) {
+    unsigned int* ctr = p.split_ctr + (static_cast<size_t>(t) * 2 + rank) * 4 + ew;
+    const unsigned int gen = p.split_gen;
+    unsigned int cur = *reinterpret_cast<volatile unsigned int*>(ctr);
+#pragma unroll 1
+    for (int it = 0; it < (1 << 20); ++it) {
+      const unsigned int next = (cur >> 8) == gen ? cur + 1u : ((gen << 8) | 1u);
+      const unsigned int prev = atomicCAS(ctr, cur, next);
+      if (prev == cur) {
+        count = next & 0xFFu;
+        break;
+      }
+      cur = prev;
+    }
+    if (count == 0) atomicCAS(p.err, 0u, err_code(2));
+  }
+  count = __shfl_sync(0xFFFFFFFFu, count, 0);
+  if (count != static_cast<unsigned int>(w.npieces)) {
+    release();
+    return;
+  }
+  __threadfence();
+  const int row = row0 + r;
+  const bool row_ok = row < p.M;
+  // v = sum over pieces q = 0 .. npieces-1 (in that order) of TMEM column
+  // block [col, col + 32) of piece q; this piece's own values come from TMEM.
+  auto load_sum = [&](int col, float (&v)[32]) {
+    uint32_t ar[32];
+    ptx::tmem_ld_32x32b_x32(tbase + col, ar);
+    ptx::tmem_wait_ld();
+    ptx::tmem_regs_ready(ar);
+#pragma unroll 1
+    for (int q = 0; q < w.npieces; ++q) {
+      float x[32];
+      if (q == w.piece) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(ar[j]);
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(tile_ws + static_cast<size_t>(q) * piece_stride) +
+                            static_cast<size_t>(col / 4) * kBM + r;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 f = __ldcg(src + i * kBM);
+          x[4 * i + 0] = f.x;
+          x[4 * i + 1] = f.y;
+          x[4 * i + 2] = f.z;
+          x[4 * i + 3] = f.w;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = q == 0 ? x[j] : v[j] + x[j];
+    }
+  };
+  if (p.epi == kEpiSwiglu) {
+    constexpr int HALF = BN / 2;
+#pragma unroll 1
+    for (int c = 0; c < HALF / 32; ++c) {
+      const int col0 = tn * HALF + c * 32;
+      float g[32], u[32];
+      load_sum(c * 32, g);
+      load_sum(HALF + c * 32, u);
+      finish_swiglu_warp(p, col0, g, u);
+      if (row_ok && col0 < p.n_out) store_row32(p, row, col0, g);
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col0 = tn * BN + c * 32;
+      float v[32];
+      load_sum(c * 32, v);
+      float b[32];
+      bias32(p, 0, col0, b);
+      finish_plain(p, b, v);
+      if (row_ok && col0 < p.n_out) store_row32(p, row, col0, v);
+    }
+  }
+  release();
+}
+
 template <int BN>
 __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constant__ KernelParams p) {
   using PC = PairCfg<BN>;
@@ -94,9 +212,11 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
       uint32_t ph = 0;
       bool ok = true;
       constexpr int HALF = BN / 2;
-      for (int unit = cluster; ok && unit < p.num_units; unit += nclusters) {
+      WorkItem w;
+      for (int n = 0; ok && work_item(p.num_units, p.split_tiles, p.split_pieces, nclusters, p.k_blocks, cluster, n, w);
+           ++n) {
         int tm, tn;
-        unit_coords(p, unit, tm, tn);
+        unit_coords(p, w.unit, tm, tn);
         const int ay = tm * (2 * kBM) + static_cast<int>(rank) * kBM;
         int bx[BN / 128];
 #pragma unroll
@@ -107,7 +227,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
           else
             bx[q] = tn * BN + qc;
         }
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!wait_one(empty(s), ph ^ 1u, p, 0)) {
             ok = false;
             break;
@@ -141,7 +261,9 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
       int s = 0;
       uint32_t ph = 0, acc_it = 0;
       bool ok = true;
-      for (int unit = cluster; ok && unit < p.num_units; unit += nclusters) {
+      WorkItem w;
+      for (int n = 0; ok && work_item(p.num_units, p.split_tiles, p.split_pieces, nclusters, p.k_blocks, cluster, n, w);
+           ++n) {
         const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
         ++acc_it;
         if (!wait_one(tempty(buf), aph ^ 1u, p, 1)) {
@@ -150,7 +272,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
         }
         ptx::tc_fence_after();
         const uint32_t dt = tmem_base + buf * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = w.k0; kb < w.k1; ++kb) {
           if (!wait_one(full(s), ph, p, 1)) {
             ok = false;
             break;
@@ -161,7 +283,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
             ptx::mma_f16_pair(dt, ad + static_cast<uint64_t>(k * 2), bd + static_cast<uint64_t>(k * 128),
-                              p.idesc, (kb | k) != 0 ? 1u : 0u);
+                              p.idesc, (kb != w.k0 || k != 0) ? 1u : 0u);
           ptx::mma_commit_pair(empty(s), 0x3);
           if (++s == S) {
             s = 0;
@@ -180,9 +302,11 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
     const int r = ew * 32 + lane;
     uint32_t acc_it = 0;
     bool ok = true;
-    for (int unit = cluster; ok && unit < p.num_units; unit += nclusters) {
+    WorkItem w;
+    for (int n = 0; ok && work_item(p.num_units, p.split_tiles, p.split_pieces, nclusters, p.k_blocks, cluster, n, w);
+         ++n) {
       int tm, tn;
-      unit_coords(p, unit, tm, tn);
+      unit_coords(p, w.unit, tm, tn);
       const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
       ++acc_it;
       if (!wait_warp(tfull(buf), aph, p, 2)) {
@@ -191,7 +315,12 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
       }
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * BN;
-      epilogue_classical<BN>(p, tbase, tm * (2 * kBM) + static_cast<int>(rank) * kBM, tn, r);
+      const int row0 = tm * (2 * kBM) + static_cast<int>(rank) * kBM;
+      if (w.npieces > 1) {  // arrives on tempty itself, before the pieces' sum
+        epilogue_split_piece<BN>(p, tbase, row0, tn, r, w, rank, ew, ptx::mapa(tempty(buf), 0));
+        continue;
+      }
+      epilogue_classical<BN>(p, tbase, row0, tn, r);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty(buf), 0));
@@ -510,8 +639,11 @@ cudaError_t launch_strassen_pair_t(const KernelParams& p, int max_clusters, cuda
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// Launch configuration of the classical pair kernel; on first use per device
+// it also sets the shared-memory limit and records how many clusters fit.
 template <int BN>
-cudaError_t launch_gemm_pair_t(const KernelParams& p, int max_clusters, cudaStream_t stream) {
+cudaError_t pair_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1], int& fit,
+                        cudaStream_t stream) {
   auto kern = fgemm_kernel_pair<BN>;
   constexpr int smem = PairCfg<BN>::kSmemBytes;
   static unsigned long long configured = 0;
@@ -520,8 +652,7 @@ cudaError_t launch_gemm_pair_t(const KernelParams& p, int max_clusters, cudaStre
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cfg = cudaLaunchConfig_t{};
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -534,16 +665,38 @@ cudaError_t launch_gemm_pair_t(const KernelParams& p, int max_clusters, cudaStre
   if (!(configured & bit)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(2 * std::max(max_clusters, 1), 1, 1);
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2 * std::max(sms / 2, 1), 1, 1);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) return e;
-    clusters_fit[dev & 63] = n > 0 ? n : 1;
+    clusters_fit[dev & 63] = std::min(n > 0 ? n : 1, std::max(sms / 2, 1));
     configured |= bit;
   }
-  const int clusters = std::min(std::min(max_clusters, clusters_fit[dev & 63]), p.num_units);
-  cfg.gridDim = dim3(2 * std::max(clusters, 1), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  fit = clusters_fit[dev & 63];
+  return cudaSuccess;
+}
+
+template <int BN>
+int gemm_pair_clusters_fit_t() {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  int fit = 0;
+  return pair_config<BN>(cfg, attr, fit, nullptr) == cudaSuccess ? fit : 0;
+}
+
+template <int BN>
+cudaError_t launch_gemm_pair_t(const KernelParams& p, int clusters, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  int fit = 0;
+  cudaError_t e = pair_config<BN>(cfg, attr, fit, stream);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1 || clusters > fit) return cudaErrorInvalidValue;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, fgemm_kernel_pair<BN>, p);
 }
 
 }  // namespace fgemm

@@ -15,7 +15,11 @@
 //                  ("Page 48", wave quantization)
 //   t_tile       = products * (2 * tile_m * tile_n * K_sub / (slot peak * eff)
 //                  + fill), eff measured per form and tile
-//   t_compute    = waves * t_tile
+//   t_compute    = waves * t_tile; for the classical CTA-pair kernel whose
+//                  last wave holds R <= slots / 2 tiles, those tiles may run
+//                  as S = slots / R pieces of K each (S <= 4), and then
+//                  t_compute = (floor(tiles / slots) + 1/S) * t_tile
+//                  + (S - 1) * split_fix_us, when that is less
 //   t_memory     = HBM bytes / bandwidth (operands and result once, plus the
 //                  Strassen partial tiles when they cannot stay in L2)
 //   t_operands   = operand elements streamed from L2 into the SMs (tiled
@@ -89,6 +93,7 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   m.tile_fill_us = 2.3;
   m.l2_bytes = 126.0 * 1024 * 1024;
   m.l2_gbs = 40000.0;
+  m.split_fix_us = 4.0;
   *out = m;
 }
 
@@ -119,6 +124,49 @@ double fgemm_model_tiled_reads(int64_t M, int64_t N, int64_t K, int32_t tile_m, 
 double fgemm_model_roofline(double flops, double bytes, double peak_flops, double bandwidth) {
   if (bytes <= 0) return peak_flops;
   return std::min(peak_flops, flops / bytes * bandwidth);
+}
+
+int32_t fgemm_model_split_tail(const fgemm_device_model_t* dev, int64_t tiles, int32_t clusters,
+                               int32_t k_blocks, int32_t tile_n, int32_t mode, int32_t* pieces) {
+  if (pieces) *pieces = 1;
+  if (mode <= 0 || tiles <= 0 || clusters < 2 || clusters > 255 || k_blocks <= 0) return 0;
+  const int64_t rem = tiles % clusters;
+  if (rem == 0 || 2 * rem > clusters) return 0;
+  const int32_t s = static_cast<int32_t>(
+      std::min<int64_t>(std::min<int64_t>(clusters / rem, k_blocks), fgemm::kMaxSplitPieces));
+  if (s < 2) return 0;
+  if (mode == 1) {
+    // auto: split when the part of a tile time it saves, (1 - 1/S) * t_tile,
+    // outweighs its cost, split_fix_us per other piece each last piece reads
+    if (!dev || dev->num_sms <= 0) return 0;
+    const double eff = std::max(dev->eff_pair[tile_n == 128 ? 0 : 1], 1e-3);
+    const double pair_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms * 2.0;
+    const double t_tile = 2.0 * 256.0 * tile_n * fgemm::kBK * k_blocks / (pair_flop_per_us * eff);
+    if ((1.0 - 1.0 / s) * t_tile <= dev->split_fix_us * (s - 1)) return 0;
+  }
+  if (pieces) *pieces = s;
+  return static_cast<int32_t>(rem);
+}
+
+int32_t fgemm_split_work_item(int64_t tiles, int32_t split_tiles, int32_t split_pieces,
+                              int32_t clusters, int32_t k_blocks, int32_t cluster, int32_t n,
+                              int32_t* out5) {
+  if (tiles <= 0 || tiles > (1ll << 31) - 1 || clusters <= 0 || k_blocks <= 0 || cluster < 0 ||
+      cluster >= clusters || n < 0 || split_tiles < 0 || split_tiles > tiles || !out5)
+    return 0;
+  if (split_tiles > 0 && (split_pieces < 2 || split_pieces > k_blocks ||
+                          static_cast<int64_t>(split_tiles) * split_pieces > clusters))
+    return 0;
+  fgemm::WorkItem w;
+  if (!fgemm::work_item(static_cast<int>(tiles), split_tiles, split_pieces, clusters, k_blocks,
+                        cluster, n, w))
+    return 0;
+  out5[0] = w.unit;
+  out5[1] = w.k0;
+  out5[2] = w.k1;
+  out5[3] = w.piece;
+  out5[4] = w.npieces;
+  return 1;
 }
 
 fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, int64_t N,
@@ -155,7 +203,14 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
   const double t_tile =
       products * (2.0 * tile_m * tile_n * k_pad / (slot_flop_per_us * std::max(eff, 1e-3)) +
                   dev->tile_fill_us);
-  const double t_compute = static_cast<double>(waves) * t_tile;
+  double t_compute = static_cast<double>(waves) * t_tile;
+  if (pair && d == 0) {
+    // the tiles of the last partial wave may be split along K into S pieces
+    const int32_t kb = static_cast<int32_t>(std::min<int64_t>(ceil_div(sub_k, fgemm::kBK), 1 << 30));
+    int32_t s = 1;
+    if (fgemm_model_split_tail(dev, tiles, slots, kb, tile_n, 1, &s) > 0)
+      t_compute = (static_cast<double>(tiles / slots) + 1.0 / s) * t_tile + dev->split_fix_us * (s - 1);
+  }
   double bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
                         static_cast<double>(M) * n_out);
   if (d > 0) {

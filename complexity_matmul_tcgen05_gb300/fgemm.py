@@ -46,7 +46,8 @@ class DeviceModel(ctypes.Structure):
                 ("eff_strassen", (ctypes.c_double * 2) * 2),
                 ("eff_strassen_pair", ctypes.c_double * 2),
                 ("launch_us", ctypes.c_double), ("tile_fill_us", ctypes.c_double),
-                ("l2_bytes", ctypes.c_double), ("l2_gbs", ctypes.c_double)]
+                ("l2_bytes", ctypes.c_double), ("l2_gbs", ctypes.c_double),
+                ("split_fix_us", ctypes.c_double)]
 
 
 _lib = None
@@ -101,16 +102,39 @@ def lib() -> ctypes.CDLL:
                                        ctypes.POINTER(ctypes.c_double)]
         L.fgemm_strassen_matmul_static.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, st,
                                                    epi_p, i32, i32, vp]
+        L.fgemm_model_split_tail.argtypes = [model_p, i64, i32, i32, i32, i32, ctypes.POINTER(i32)]
+        L.fgemm_model_split_tail.restype = i32
+        L.fgemm_split_work_item.argtypes = [i64, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
+        L.fgemm_split_work_item.restype = i32
+        L.fgemm_set_split_mode.argtypes = [vp, i32]
         L.fgemm_get_device_model.argtypes = [vp, model_p]
         L.fgemm_set_device_model.argtypes = [vp, model_p]
         for name in ("fgemm_create", "fgemm_destroy", "fgemm_set_stream", "fgemm_matmul",
                      "fgemm_matmul_ex", "fgemm_plan", "fgemm_get_error", "fgemm_calibrate",
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
-                     "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout"):
+                     "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout",
+                     "fgemm_set_split_mode"):
             getattr(L, name).restype = st
         _lib = L
         return L
+
+
+SPLIT_MODES = {"off": 0, "auto": 1, "force": 2}
+
+
+def split_work_items(tiles: int, split_tiles: int, split_pieces: int, clusters: int,
+                     k_blocks: int, cluster: int):
+    """The work list of one pair in the K-split schedule, as (unit, k0, k1,
+    piece, npieces) tuples (host-side copy of what the kernel runs)."""
+    out = (ctypes.c_int32 * 5)()
+    items = []
+    n = 0
+    while lib().fgemm_split_work_item(tiles, split_tiles, split_pieces, clusters, k_blocks,
+                                      cluster, n, out):
+        items.append(tuple(out))
+        n += 1
+    return items
 
 
 def status_string(status: int) -> str:
@@ -169,6 +193,12 @@ class Handle:
 
     def set_stream(self, stream_ptr: int):
         _check(lib().fgemm_set_stream(self._h, ctypes.c_void_p(stream_ptr)), self._h)
+
+    def set_split_mode(self, mode):
+        """K split of the last wave of CTA-pair tiles: "off" (0), "auto" (1,
+        the default) or "force" (2, whenever possible)."""
+        code = SPLIT_MODES[mode] if isinstance(mode, str) else int(mode)
+        _check(lib().fgemm_set_split_mode(self._h, code), self._h)
 
     def matmul_raw(self, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype: int,
                    epilogue: Epilogue | None = None, algo: str = "auto", tile_n: int = 0,

@@ -92,8 +92,8 @@ typedef enum {
 
 /*
  * Creates a handle on the CURRENT CUDA device. The handle owns: a device
- * error word, a plan cache, a tensor-descriptor cache, the Strassen partial
- * workspace (grown on demand) and the device model. The device model starts
+ * error word, a plan cache, a tensor-descriptor cache, the partial-tile
+ * workspace (grown on demand), the split-piece counters and the device model. The device model starts
  * from the device's SM count and, if the environment variable FGEMM_CALIB
  * names a calibration JSON written by fgemm_calibrate, from that file.
  * Returns FGEMM_ERR_NO_DEVICE if no device is present or it is not sm_103,
@@ -123,7 +123,10 @@ fgemm_status_t fgemm_set_stream(fgemm_handle_t h, void* cuda_stream);
  * Strassen forms need M, N, K (for SWIGLU: M, N/2, K) divisible into 2^d
  * blocks that are whole numbers of tiles (128 rows, 128 or 256 columns, 64
  * along K) -> else FGEMM_ERR_UNSUPPORTED; AUTO never picks an illegal form.
- * Strassen forms use the handle's workspace (4^d partial tiles per SM).
+ * Strassen forms use the handle's workspace (4^d partial tiles per SM); a
+ * classical CTA-pair launch whose last wave is split along K (see
+ * fgemm_set_split_mode) uses it for the pieces' fp32 partial tiles and a
+ * small counter buffer the handle allocates once.
  */
 fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
                             const void* A, int64_t lda, const void* B,
@@ -254,6 +257,9 @@ typedef struct {
   double tile_fill_us;     /* pipeline fill + drain cost per tile visit */
   double l2_bytes;         /* L2 capacity (bytes) */
   double l2_gbs;           /* L2 -> SM operand bandwidth, GB/s */
+  double split_fix_us;     /* fixed cost of splitting the last wave of CTA-pair
+                            * tiles along K (partial stores, the sum by the last
+                            * piece, its exposed epilogue) */
 } fgemm_device_model_t;
 
 /* Default model for a device with the given SM count, peak and bandwidth. */
@@ -291,6 +297,47 @@ fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M,
                                 int64_t N, int64_t K, int32_t epi_kind,
                                 fgemm_algo_t* algo_out, int32_t* tile_m,
                                 int32_t* tile_n, double* predicted_us);
+
+/*
+ * Last-wave K split of the classical CTA-pair kernel (no counterpart on the
+ * pages, which quantize waves but do not split them; the pages' own remedy
+ * for wave quantization, CS336 Lecture 05 notes "Page 48", is choosing tile
+ * sizes). With `tiles` output tiles on `clusters` pairs, the last wave would
+ * run R = tiles % clusters tiles on R pairs while the rest idle. When
+ * 2R <= clusters, the first R tiles (in rasterised order) are each cut into
+ * S = min(clusters / R, k_blocks, 4) pieces of equal K range; piece s of
+ * split tile t is the first work item of pair t * S + s, and every pair then
+ * runs its (tiles - R) / clusters whole tiles. Each piece stores an fp32
+ * partial; the last piece to finish sums the pieces in piece order
+ * (deterministic) and applies the epilogue.
+ *
+ * fgemm_model_split_tail returns R (0 = no split) and writes S to *pieces
+ * (1 when no split; pieces may be NULL). mode 0: never; 1 (auto): when
+ * (1 - 1/S) * tile time > (S - 1) * dev->split_fix_us; 2: whenever the
+ * conditions above allow. Requires 2 <= clusters <= 255; dev may be NULL for
+ * modes 0 and 2.
+ */
+int32_t fgemm_model_split_tail(const fgemm_device_model_t* dev, int64_t tiles,
+                               int32_t clusters, int32_t k_blocks, int32_t tile_n,
+                               int32_t mode, int32_t* pieces);
+
+/*
+ * The n-th work item (n = 0, 1, ...) of pair `cluster` in the schedule
+ * above: writes {unit, k0, k1, piece, npieces} (tile index, K blocks
+ * [k0, k1), piece index among the tile's npieces; whole tiles have
+ * npieces = 1) to out5 and returns 1, or returns 0 past the end of the list
+ * (or on invalid arguments). Host-only; the kernel runs the same function.
+ */
+int32_t fgemm_split_work_item(int64_t tiles, int32_t split_tiles, int32_t split_pieces,
+                              int32_t clusters, int32_t k_blocks, int32_t cluster,
+                              int32_t n, int32_t* out5);
+
+/*
+ * K-split mode of the handle's classical CTA-pair launches: 0 never, 1 auto
+ * (the default: fgemm_model_split_tail with the handle's device model), 2
+ * whenever possible. Returns FGEMM_ERR_INVALID_ARG for other modes.
+ */
+fgemm_status_t fgemm_set_split_mode(fgemm_handle_t h, int32_t mode);
 
 /* Copies the handle's current device model into *out. */
 fgemm_status_t fgemm_get_device_model(fgemm_handle_t h,

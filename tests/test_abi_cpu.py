@@ -239,3 +239,86 @@ def test_model_pair_tiles_fix_wave_quantization(L):
     tail = ctypes.c_double()
     assert L.fgemm_model_waves(L.fgemm_model_tiles(4096, 4096, 128, 256), 152, ctypes.byref(tail)) == 4
     assert L.fgemm_model_waves(L.fgemm_model_tiles(4096, 4096, 256, 128), 76, ctypes.byref(tail)) == 7
+
+
+# ----------------------------------------------------------- K-split schedule
+
+def _split(L, tiles, clusters, kb, mode=2, m=None):
+    pieces = ctypes.c_int32()
+    r = L.fgemm_model_split_tail(None if m is None else ctypes.byref(m), tiles, clusters, kb, 256,
+                                 mode, ctypes.byref(pieces))
+    return r, pieces.value
+
+
+@pytest.mark.parametrize("tiles,clusters,kb", [
+    (256, 76, 64),    # 4096^2 in 256x256 pair tiles on 76 pairs, K = 4096: R = 28, S = 2
+    (1024, 76, 128),  # 8192^3: R = 36, S = 2
+    (77, 76, 76),     # one tail tile: S capped at 4
+    (96, 76, 64),     # R = 20: S = 3
+    (64, 76, 32),     # R = 64 > 76/2: no split
+    (10, 76, 1),      # one K block: a piece needs at least one
+    (5, 3, 7),        # R = 2 > 3/2: no split
+    (13, 4, 3),       # R = 1, S = min(4, 3) = 3
+    (200, 7, 9),      # R = 4 > 7/2: no split
+])
+def test_split_schedule_covers_every_k_block_once(L, tiles, clusters, kb):
+    split, pieces = _split(L, tiles, clusters, kb)
+    rem = tiles % clusters
+    if rem == 0 or 2 * rem > clusters or min(clusters // rem, kb, 4) < 2:
+        assert (split, pieces) == (0, 1)
+    else:
+        assert split == rem and pieces == min(clusters // rem, kb, 4)
+        assert split * pieces <= clusters
+    sched = [fgemm.split_work_items(tiles, split, pieces, clusters, kb, c) for c in range(clusters)]
+    seen = {}
+    for c, items in enumerate(sched):
+        for n, (unit, k0, k1, piece, npieces) in enumerate(items):
+            assert 0 <= unit < tiles and 0 <= k0 < k1 <= kb
+            if unit >= split:
+                assert (k0, k1, piece, npieces) == (0, kb, 0, 1)
+                assert (unit - split) % clusters == c
+            else:  # a piece: the pair's first item, pair = tile * S + piece
+                assert n == 0 and npieces == pieces and c == unit * pieces + piece
+            for k in range(k0, k1):
+                assert (unit, k) not in seen, (unit, k)
+                seen[(unit, k)] = piece
+    assert len(seen) == tiles * kb
+    # the pieces of a split tile are numbered 0.. in K order
+    for t in range(split):
+        order = [seen[(t, k)] for k in range(kb)]
+        assert order == sorted(order) and order[0] == 0 and order[-1] == pieces - 1
+    # every pair runs the same whole tiles count; the split adds at most one
+    # piece of ceil(kb / S) K blocks
+    work = [sum(k1 - k0 for (_, k0, k1, _, _) in items) for items in sched]
+    whole = (tiles - split) // clusters * kb
+    assert all(whole <= w <= whole + (kb + pieces - 1) // pieces for w in work) if split else True
+
+
+def test_split_rule(L):
+    m = _model(L)
+    # 4096^3 + bias: 256 pair tiles on 76 pairs, the last wave 28/76 busy
+    assert _split(L, 256, 76, 64, 1, m) == (28, 2)
+    assert _split(L, 256, 76, 64, 0, m) == (0, 1)
+    # full waves: nothing to split
+    assert _split(L, 152, 76, 64, 2) == (0, 1)
+    # a short K makes the saved time smaller than the split's cost
+    assert _split(L, 256, 76, 2, 1, m) == (0, 1)
+    m.split_fix_us = 1e9
+    assert _split(L, 256, 76, 64, 1, m) == (0, 1)
+    # invalid cluster counts are never split
+    assert _split(L, 256, 1, 64, 2) == (0, 1)
+    assert _split(L, 1000, 300, 64, 2) == (0, 1)
+
+
+def test_model_split_removes_the_pair_sawtooth(L):
+    # 77 pair tiles on 76 pairs: whole waves cost two tile times; split, the
+    # one extra tile runs as 4 pieces on 4 pairs: 1 + 1/4 tile times
+    m = _model(L)
+    _, t76 = _predict(L, m, 256 * 76, 256, 8192, "classical", 256, tile_m=256)
+    _, t77 = _predict(L, m, 256 * 77, 256, 8192, "classical", 256, tile_m=256)
+    t_tile = t76 - m.launch_us
+    assert abs(t77 - (m.launch_us + 1.25 * t_tile + 3 * m.split_fix_us)) < 1e-6 * t77
+    m.split_fix_us = 1e9  # split never pays: back to the whole-wave sawtooth
+    _, t77w = _predict(L, m, 256 * 77, 256, 8192, "classical", 256, tile_m=256)
+    assert abs(t77w - (m.launch_us + 2 * t_tile)) < 1e-6 * t77w
+    assert t77 < 0.8 * t77w

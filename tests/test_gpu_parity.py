@@ -262,3 +262,59 @@ def test_bounded_wait_reports_timeout_and_handle_survives():
     assert h.get_error() == fgemm.OK
     assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, "bf16"))
     h.close()
+
+
+# ------------------------------------- K split of the last wave (CTA pairs)
+
+@pytest.fixture
+def split_mode():
+    """Sets the default handle's K-split mode for one test, then restores auto."""
+    h = fgemm.default_handle()
+    yield h.set_split_mode
+    h.set_split_mode("auto")
+
+
+SPLIT_CASES = [
+    # (M, N, K, tile_n): tiles on the pairs that fit, with a partial last wave
+    (256, 256, 4096, 256),     # one tile shared by every pair
+    (256, 256, 64, 256),       # one K block: too short to share, whole-tile path
+    (2304, 2048, 1032, 256),   # 72 tiles (fewer than the pairs), ragged K
+    (4096, 4096, 512, 256),    # 256 tiles: a full wave count plus a tail
+    (300, 520, 1032, 128),     # ragged M, N, K
+    (5000, 640, 776, 128),     # 20 x 5 = 100 tiles, ragged M and K
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K,tile", SPLIT_CASES)
+def test_exact_ternary_cta_pair_split(M, N, K, tile, dtype, split_mode):
+    """Split pieces summed by the last one: still RNE(exact C) bit for bit."""
+    split_mode("force")
+    A, B, bias = _ternary(M, N, K, dtype, seed=30)
+    C = run(A, B, algo="classical", epilogue="scale_bias", bias=bias, tile_n=tile, tile_m=256)
+    assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
+
+
+@pytest.mark.parametrize("epilogue,alpha,tile", [("scale_bias", 0.75, 256), ("silu", 1.0, 128),
+                                                 ("swiglu", 1.0, 256), ("swiglu", 1.0, 128)])
+def test_split_every_entry_and_deterministic(epilogue, alpha, tile, split_mode):
+    """Forced split on random inputs: every entry within the classical bounds,
+    and two runs give the same bits (the pieces are summed in a fixed order)."""
+    split_mode("force")
+    M, N, K = 1280, 2048, 2112  # 5 x 8 = 40 pair tiles (SwiGLU: 5 x 8 or 5 x 16), K ragged
+    A = inputs.matrix(M, K, "normal", "bf16", 40, DEV)
+    B = inputs.matrix(K, N, "normal_inv_k", "bf16", 41, DEV, k=K)
+    bias = inputs.matrix(1, N, "normal_0.02", "bf16", 42, DEV)[0] if epilogue != "swiglu" else None
+    _full_check(A, B, "classical", "bf16", epilogue=epilogue, alpha=alpha, bias=bias, tile=tile,
+                tile_m=256)
+    C1 = run(A, B, algo="classical", epilogue=epilogue, alpha=alpha, bias=bias, tile_n=tile,
+             tile_m=256)
+    C2 = run(A, B, algo="classical", epilogue=epilogue, alpha=alpha, bias=bias, tile_n=tile,
+             tile_m=256)
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+    # and the whole-wave form agrees within the classical tolerance
+    split_mode("off")
+    C0 = run(A, B, algo="classical", epilogue=epilogue, alpha=alpha, bias=bias, tile_n=tile,
+             tile_m=256)
+    d = values(C1) - values(C0)
+    assert np.linalg.norm(d) <= 1e-3 * max(np.linalg.norm(values(C0)), 1e-30)
