@@ -203,8 +203,10 @@ __device__ __forceinline__ void finish_swiglu_warp(const KernelParams& p, int co
 // SwiGLU the tile's first BN/2 columns hold gate columns and the last BN/2
 // the matching up columns (the producer loads them side by side).  Every
 // bias entry the tile needs is loaded up front (one per lane per 32-column
-// chunk, broadcast by shuffles), and for the plain epilogues the TMEM load of
-// the next chunk is in flight while the current one is finished and stored.
+// chunk, kept as raw 16-bit values and converted when used, so no wait on
+// them precedes the first TMEM load; broadcast by shuffles), and for the
+// plain epilogues the TMEM load of the next chunk is in flight while the
+// current one is finished and stored.
 template <int BN>
 __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32_t tbase, int row0,
                                                    int tn, int r) {
@@ -241,16 +243,17 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
     }
   } else {
     constexpr int CH = BN / 32;
-    float bl[CH];
+    uint32_t bl[CH];  // raw 16-bit bias values, converted when used
 #pragma unroll
     for (int c = 0; c < CH; ++c)
-      bl[c] = p.bias ? ld_bias(p, min(tn * BN + c * 32 + lane, p.n_out - 1)) : 0.0f;
+      bl[c] = p.bias ? __ldg(p.bias + min(tn * BN + c * 32 + lane, p.n_out - 1)) : 0u;
     auto finish = [&](int c, const uint32_t (&ar)[32]) {
       const int col0 = tn * BN + c * 32;
+      const float bf = h2f(bl[c], p.is_bf16);
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float x = p.alpha * __uint_as_float(ar[j]) + __shfl_sync(0xFFFFFFFFu, bl[c], j);
+        float x = p.alpha * __uint_as_float(ar[j]) + __shfl_sync(0xFFFFFFFFu, bf, j);
         if (p.epi == kEpiSilu) x = silu(x);
         v[j] = x;
       }
