@@ -8,9 +8,9 @@ gcc into ``oracle/_build/liboracle.so``.
 
 Every function follows the definition stated in ``oracle.c``'s header:
 classical product (CS336 Lecture 05 notes, "Page 40. Trick 5: tiling"),
-epilogue (PingPong GEMM / CODA note), Strassen recursion (FalconGEMM
-summary, "Methodology" items 1 and 4; textbook identities, since the pages
-print none).  Arrays are numpy, row-major.
+epilogue (PingPong GEMM / CODA note), Strassen and Winograd recursions
+(FalconGEMM summary, "Methodology" items 1 and 4; textbook identities, since
+the pages print none).  Arrays are numpy, row-major.
 """
 from __future__ import annotations
 
@@ -69,6 +69,11 @@ def _load():
         lib.oracle_strassen_emulated.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, i64, dp,
                                                  i64, dp, i64, dp, i64]
         lib.oracle_strassen_emulated.restype = ctypes.c_int
+        lib.oracle_winograd_f64.argtypes = [ctypes.c_int, i64, i64, i64, dp, i64, dp, i64, dp, i64]
+        lib.oracle_winograd_f64.restype = ctypes.c_int
+        lib.oracle_winograd_emulated.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, i64, dp,
+                                                 i64, dp, i64, dp, i64]
+        lib.oracle_winograd_emulated.restype = ctypes.c_int
         lib.oracle_silu.argtypes = [ctypes.c_double]
         lib.oracle_silu.restype = ctypes.c_double
         _lib = lib
@@ -201,6 +206,36 @@ def strassen_emulated(A: np.ndarray, B: np.ndarray, depth: int, dtype) -> np.nda
                                           _ptr(C, ctypes.c_double), N)
     if rc != 0:
         raise ValueError("Strassen needs M, N, K divisible by 2**depth")
+    return C
+
+
+def winograd(A: np.ndarray, B: np.ndarray, depth: int) -> np.ndarray:
+    """Recursive Winograd variant of Strassen in fp64 (depth levels)."""
+    A, B = _f64(A), _f64(B)
+    M, K = A.shape
+    _, N = B.shape
+    C = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_winograd_f64(depth, M, N, K, _ptr(A, ctypes.c_double), K,
+                                     _ptr(B, ctypes.c_double), N,
+                                     _ptr(C, ctypes.c_double), N)
+    if rc != 0:
+        raise ValueError("Winograd needs M, N, K divisible by 2**depth")
+    return C
+
+
+def winograd_emulated(A: np.ndarray, B: np.ndarray, depth: int, dtype) -> np.ndarray:
+    """Winograd variant with every leaf operand rounded (fp32, then ``dtype``)
+    once from the exact signed sum of source blocks it stands for."""
+    code = F64 if str(dtype) in ("f64", "float64") else _dtype_code(dtype)
+    A, B = _f64(A), _f64(B)
+    M, K = A.shape
+    _, N = B.shape
+    C = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_winograd_emulated(depth, code, M, N, K, _ptr(A, ctypes.c_double), K,
+                                          _ptr(B, ctypes.c_double), N,
+                                          _ptr(C, ctypes.c_double), N)
+    if rc != 0:
+        raise ValueError("Winograd needs M, N, K divisible by 2**depth")
     return C
 
 

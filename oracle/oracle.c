@@ -40,6 +40,21 @@
  *    applied recursively `depth` times, classical at the leaves.  In exact
  *    arithmetic it equals the classical product.
  *
+ *  - Winograd's variant of Strassen (named beside Strassen among the
+ *    Strassen-like LCMAs of the FalconGEMM summary, "Methodology" item 1; the
+ *    pages print no formulas, so the oracle uses the standard variant).  It
+ *    still multiplies seven half-size products but builds its operands and
+ *    the output from shared partial sums:
+ *        S1 = A21 + A22   S2 = S1 - A11   S3 = A11 - A21   S4 = A12 - S2
+ *        T1 = B12 - B11   T2 = B22 - T1   T3 = B22 - B12   T4 = T2 - B21
+ *        P1 = A11 B11   P2 = A12 B21   P3 = S4 B22   P4 = A22 T4
+ *        P5 = S1 T1     P6 = S2 T2     P7 = S3 T3
+ *        U1 = P1 + P2   U2 = P1 + P6   U3 = U2 + P7   U4 = U2 + P5
+ *        U5 = U4 + P3   U6 = U3 - P4   U7 = U3 + P5
+ *        C11 = U1   C12 = U5   C21 = U6   C22 = U7
+ *    applied recursively `depth` times, classical at the leaves (15 block
+ *    additions per level against Strassen's 18).
+ *
  *  - Emulated Strassen: the same recursion, except that every leaf operand
  *    (an exact signed sum of source blocks) is rounded first to fp32 and then
  *    to the 16-bit input type, round-to-nearest-even, because a tensor core
@@ -329,6 +344,107 @@ static void strassen_rec(int depth, int round_dtype, int64_t M, int64_t N,
   for (int q = 0; q < 7; ++q) free(P[q]);
   free(S);
   free(T);
+}
+
+/*
+ * Recursive Winograd variant, in the notation of the header.  The partial
+ * sums S1..S4 and T1..T4 are formed exactly (fp64) at every level, so with
+ * `round_dtype` >= 0 a leaf operand is rounded once, from the exact signed
+ * sum of source blocks it stands for (S2 = A21 + A22 - A11, ...).
+ */
+static void winograd_rec(int depth, int round_dtype, int64_t M, int64_t N,
+                         int64_t K, const double* A, int64_t lda,
+                         const double* B, int64_t ldb, double* C,
+                         int64_t ldc) {
+  if (depth == 0) {
+    strassen_rec(0, round_dtype, M, N, K, A, lda, B, ldb, C, ldc);
+    return;
+  }
+  const int64_t m = M / 2, n = N / 2, k = K / 2;
+  const double* A11 = A;
+  const double* A12 = A + k;
+  const double* A21 = A + m * lda;
+  const double* A22 = A + m * lda + k;
+  const double* B11 = B;
+  const double* B12 = B + n;
+  const double* B21 = B + k * ldb;
+  const double* B22 = B + k * ldb + n;
+  double* S1 = (double*)malloc(sizeof(double) * (size_t)(m * k));
+  double* S2 = (double*)malloc(sizeof(double) * (size_t)(m * k));
+  double* S3 = (double*)malloc(sizeof(double) * (size_t)(m * k));
+  double* S4 = (double*)malloc(sizeof(double) * (size_t)(m * k));
+  double* T1 = (double*)malloc(sizeof(double) * (size_t)(k * n));
+  double* T2 = (double*)malloc(sizeof(double) * (size_t)(k * n));
+  double* T3 = (double*)malloc(sizeof(double) * (size_t)(k * n));
+  double* T4 = (double*)malloc(sizeof(double) * (size_t)(k * n));
+  double* P[7];
+  for (int q = 0; q < 7; ++q)
+    P[q] = (double*)malloc(sizeof(double) * (size_t)(m * n));
+
+  combine(m, k, 1, A21, lda, 1, A22, lda, S1, k);  /* S1 = A21 + A22 */
+  combine(m, k, 1, S1, k, -1, A11, lda, S2, k);    /* S2 = S1 - A11 */
+  combine(m, k, 1, A11, lda, -1, A21, lda, S3, k); /* S3 = A11 - A21 */
+  combine(m, k, 1, A12, lda, -1, S2, k, S4, k);    /* S4 = A12 - S2 */
+  combine(k, n, 1, B12, ldb, -1, B11, ldb, T1, n); /* T1 = B12 - B11 */
+  combine(k, n, 1, B22, ldb, -1, T1, n, T2, n);    /* T2 = B22 - T1 */
+  combine(k, n, 1, B22, ldb, -1, B12, ldb, T3, n); /* T3 = B22 - B12 */
+  combine(k, n, 1, T2, n, -1, B21, ldb, T4, n);    /* T4 = T2 - B21 */
+
+  winograd_rec(depth - 1, round_dtype, m, n, k, A11, lda, B11, ldb, P[0], n); /* P1 */
+  winograd_rec(depth - 1, round_dtype, m, n, k, A12, lda, B21, ldb, P[1], n); /* P2 */
+  winograd_rec(depth - 1, round_dtype, m, n, k, S4, k, B22, ldb, P[2], n);    /* P3 */
+  winograd_rec(depth - 1, round_dtype, m, n, k, A22, lda, T4, n, P[3], n);    /* P4 */
+  winograd_rec(depth - 1, round_dtype, m, n, k, S1, k, T1, n, P[4], n);       /* P5 */
+  winograd_rec(depth - 1, round_dtype, m, n, k, S2, k, T2, n, P[5], n);       /* P6 */
+  winograd_rec(depth - 1, round_dtype, m, n, k, S3, k, T3, n, P[6], n);       /* P7 */
+
+  for (int64_t i = 0; i < m; ++i) {
+    for (int64_t j = 0; j < n; ++j) {
+      const int64_t t = i * n + j;
+      const double u1 = P[0][t] + P[1][t];
+      const double u2 = P[0][t] + P[5][t];
+      const double u3 = u2 + P[6][t];
+      const double u4 = u2 + P[4][t];
+      const double u5 = u4 + P[2][t];
+      const double u6 = u3 - P[3][t];
+      const double u7 = u3 + P[4][t];
+      C[i * ldc + j] = u1;                 /* C11 */
+      C[i * ldc + j + n] = u5;             /* C12 */
+      C[(i + m) * ldc + j] = u6;           /* C21 */
+      C[(i + m) * ldc + j + n] = u7;       /* C22 */
+    }
+  }
+  for (int q = 0; q < 7; ++q) free(P[q]);
+  free(S1);
+  free(S2);
+  free(S3);
+  free(S4);
+  free(T1);
+  free(T2);
+  free(T3);
+  free(T4);
+}
+
+/* Returns 0, or -1 if M, N, K are not divisible by 2^depth. */
+int oracle_winograd_f64(int depth, int64_t M, int64_t N, int64_t K,
+                        const double* A, int64_t lda, const double* B,
+                        int64_t ldb, double* C, int64_t ldc) {
+  const int64_t g = (int64_t)1 << depth;
+  if (depth < 0 || M % g || N % g || K % g) return -1;
+  winograd_rec(depth, -1, M, N, K, A, lda, B, ldb, C, ldc);
+  return 0;
+}
+
+/* Same recursion with leaf operands rounded to `dtype` (0 f16, 1 bf16, 2 none). */
+int oracle_winograd_emulated(int depth, int dtype, int64_t M, int64_t N,
+                             int64_t K, const double* A, int64_t lda,
+                             const double* B, int64_t ldb, double* C,
+                             int64_t ldc) {
+  const int64_t g = (int64_t)1 << depth;
+  if (depth < 0 || M % g || N % g || K % g) return -1;
+  if (dtype < 0 || dtype > 2) return -1;
+  winograd_rec(depth, dtype, M, N, K, A, lda, B, ldb, C, ldc);
+  return 0;
 }
 
 /* Returns 0, or -1 if M, N, K are not divisible by 2^depth. */

@@ -264,6 +264,109 @@ def test_emulated_rounding_error_is_in_the_expected_band(dtype, depth, lo, hi):
     assert lo < rel < hi, rel
 
 
+# ----------------------------------------------------------------- Winograd
+
+@pytest.mark.parametrize("depth,shape", [(1, (2, 2, 2)), (1, (8, 6, 4)), (1, (34, 18, 50)),
+                                         (2, (4, 4, 4)), (2, (16, 24, 8)), (2, (36, 20, 44))])
+def test_winograd_equals_classical(depth, shape):
+    M, N, K = shape
+    rng = np.random.default_rng(2 * M + 5 * N + 3 * K + depth)
+    A = rng.uniform(-1, 1, (M, K))
+    B = rng.uniform(-1, 1, (K, N))
+    ref = oracle.gemm(A, B)
+    W = oracle.winograd(A, B, depth)
+    assert np.linalg.norm(W - ref) <= 1e-12 * np.linalg.norm(ref)
+
+
+@pytest.mark.parametrize("depth", [1, 2])
+def test_winograd_exact_on_integers(depth):
+    rng = np.random.default_rng(21 + depth)
+    A = rng.integers(-3, 4, (16, 12)).astype(np.float64)
+    B = rng.integers(-3, 4, (12, 20)).astype(np.float64)
+    assert np.array_equal(oracle.winograd(A, B, depth), A @ B)
+
+
+def test_winograd_every_quadrant_depends_on_the_right_blocks():
+    # one nonzero block of A and one of B at a time: any wrong block, sign or
+    # partial sum in the seven products or the output sums shows
+    n = 2
+    for ai in range(2):
+        for ak in range(2):
+            for bk in range(2):
+                for bj in range(2):
+                    A = np.zeros((2 * n, 2 * n))
+                    B = np.zeros((2 * n, 2 * n))
+                    A[ai * n:(ai + 1) * n, ak * n:(ak + 1) * n] = np.arange(1, n * n + 1).reshape(n, n)
+                    B[bk * n:(bk + 1) * n, bj * n:(bj + 1) * n] = np.arange(3, n * n + 3).reshape(n, n)
+                    assert np.array_equal(oracle.winograd(A, B, 1), A @ B)
+
+
+def test_winograd_rejects_indivisible():
+    with pytest.raises(ValueError):
+        oracle.winograd(np.ones((3, 4)), np.ones((4, 4)), 1)
+    with pytest.raises(ValueError):
+        oracle.winograd_emulated(np.ones((6, 4)), np.ones((4, 4)), 2, "bf16")
+
+
+@pytest.mark.parametrize("depth", [1, 2])
+def test_winograd_emulated_without_rounding_is_exact_winograd(depth):
+    rng = np.random.default_rng(15)
+    A = rng.uniform(-1, 1, (16, 8))
+    B = rng.uniform(-1, 1, (8, 12))
+    assert np.array_equal(oracle.winograd_emulated(A, B, depth, "f64"), oracle.winograd(A, B, depth))
+
+
+def test_winograd_emulated_on_ternary_inputs_is_exact():
+    # operands are signed sums of up to four {-1,0,1} values: exact in bf16
+    rng = np.random.default_rng(16)
+    A = rng.integers(-1, 2, (32, 16)).astype(np.float64)
+    B = rng.integers(-1, 2, (16, 24)).astype(np.float64)
+    assert np.array_equal(oracle.winograd_emulated(A, B, 1, "bf16"), A @ B)
+
+
+def test_winograd_emulated_rounds_each_operand_once_from_its_blocks():
+    # 2 x 2 scalars, B = I: the products' operands are the expanded sums
+    #   P3: a + b - c - d   P5: (c + d) * (-1)   P6: (c + d - a) * 2
+    #   P7: a - c           P4: d * 2             P1: a, P2: 0
+    # and the emulation must round each of them once (fp32, then bf16), not
+    # the partial sums they are built from.  With a = 1, c = 2^-9, d = 2^-10,
+    # c + d - a is a bf16 tie (rounded to even), so the rounding shows in C.
+    a, b, c, d = 1.0, 2.0 ** -8, 2.0 ** -9, 2.0 ** -10
+    A = np.array([[a, b], [c, d]])
+    B = np.eye(2)
+
+    def r(x):  # fp32, then bf16, both round-to-nearest-even (torch casts)
+        return float(torch.tensor(x, dtype=torch.float64).to(torch.float32).to(torch.bfloat16)
+                     .to(torch.float64))
+
+    p1, p2 = r(a) * 1.0, r(b) * 0.0
+    p3 = r(a + b - c - d) * 1.0
+    p4 = r(d) * r(2.0)
+    p5 = r(c + d) * r(-1.0)
+    p6 = r(c + d - a) * r(2.0)
+    p7 = r(a - c) * r(1.0)
+    expect = np.array([[p1 + p2, p1 + p6 + p5 + p3],
+                       [p1 + p6 + p7 - p4, p1 + p6 + p7 + p5]])
+    got = oracle.winograd_emulated(A, B, 1, "bf16")
+    assert np.allclose(got, expect, rtol=0, atol=1e-15)
+    assert not np.allclose(got, A, rtol=0, atol=1e-6)  # the tie is visible
+
+
+@pytest.mark.parametrize("dtype,depth,lo,hi", [("bf16", 1, 1e-3, 1e-2), ("bf16", 2, 3e-3, 3e-2),
+                                               ("f16", 1, 1e-4, 2e-3)])
+def test_winograd_emulated_rounding_error_is_in_the_expected_band(dtype, depth, lo, hi):
+    # rounding up to four-term operand sums to an 8-bit (bf16) or 11-bit (f16)
+    # significand: well above zero, and below 2^-7 / 2^-10 per level
+    rng = np.random.default_rng(9)
+    n = 128
+    A = oracle.round_to(rng.uniform(-1, 1, (n, n)), dtype)
+    B = oracle.round_to(rng.uniform(-1, 1, (n, n)), dtype)
+    ref = oracle.gemm(A, B)
+    E = oracle.winograd_emulated(A, B, depth, dtype)
+    rel = np.linalg.norm(E - ref) / np.linalg.norm(ref)
+    assert lo < rel < hi, rel
+
+
 # ------------------------------------------------------------ sampled path
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
