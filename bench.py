@@ -7,7 +7,7 @@ JSON line.  Four rotating input/output sets (384 MB, more than the L2) are
 cycled so that every timed step streams its operands from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fgemm|reference]
-                    [--workload NAME] [--algo auto|classical|strassen1|strassen2]
+                    [--workload NAME] [--algo auto|classical|strassen1|strassen2|winograd1]
                     [--tile 0|64|128|256]
 
 --impl reference times the fp64 CPU oracle on host cores (a bounded sample
@@ -189,7 +189,7 @@ def measured_peaks():
 
 KERNEL_SOURCES = ("fgemm_kernel.cuh", "fgemm_kernel_pair.cuh", "fgemm_ptx.cuh",
                   "fgemm_internal.h", "fgemm_kern_classical.cu", "fgemm_kern_pair.cu",
-                  "fgemm_kern_strassen1.cu", "fgemm_kern_strassen2.cu")
+                  "fgemm_kern_strassen1.cu", "fgemm_kern_strassen2.cu", "fgemm_kern_winograd1.cu")
 
 
 def kernel_source_hash():
@@ -417,7 +417,7 @@ def run_fgemm(args, rank, world):
         return
     burst, sustained, hbm, src = measured_peaks()
     achieved = flops / (kern_avg_ms * 1e-3) / 1e12
-    executed = achieved * (7.0 / 8.0) ** {"classical": 0, "strassen1": 1, "strassen2": 2}[plan_algo]
+    executed = achieved * (7.0 / 8.0) ** {"classical": 0, "strassen1": 1, "strassen2": 2, "winograd1": 1}[plan_algo]
     roof = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": UNIT,
             "frac": achieved / burst if burst else None,
             "traffic": ncu_traffic(args.workload, plan_algo, plan_tm, plan_tile),
@@ -453,7 +453,8 @@ def run_fgemm(args, rank, world):
 CANDIDATES = [("classical", 128, 64), ("classical", 128, 128), ("classical", 128, 256),
               ("classical", 256, 128), ("classical", 256, 256), ("strassen1", 128, 128),
               ("strassen1", 128, 256), ("strassen1", 256, 128), ("strassen1", 256, 256),
-              ("strassen2", 128, 128), ("strassen2", 128, 256)]
+              ("strassen2", 128, 128), ("strassen2", 128, 256), ("winograd1", 128, 128),
+              ("winograd1", 128, 256)]
 
 
 def run_sweep(args):

@@ -26,6 +26,7 @@ SOURCES = [
     "fgemm_kern_strassen2.cu",
     "fgemm_static.cu",
     "fgemm_kern_pair.cu",
+    "fgemm_kern_winograd1.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,

@@ -37,8 +37,12 @@ thread_local std::string g_thread_msg;
 // ------------------------------------------------------------------ helpers
 
 int depth_of(fgemm_algo_t a) {
-  return a == FGEMM_ALGO_STRASSEN1 ? 1 : (a == FGEMM_ALGO_STRASSEN2 ? 2 : 0);
+  return (a == FGEMM_ALGO_STRASSEN1 || a == FGEMM_ALGO_WINOGRAD1) ? 1
+                                                                 : (a == FGEMM_ALGO_STRASSEN2 ? 2 : 0);
 }
+
+constexpr fgemm_algo_t kForms[4] = {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2,
+                                    FGEMM_ALGO_WINOGRAD1};
 
 fgemm_status_t fail(std::string* msg, fgemm_status_t s, const std::string& text) {
   if (msg) *msg = text;
@@ -152,6 +156,72 @@ const StrassenTable& table_for(int depth) {
   return depth == 0 ? t0 : (depth == 1 ? t1 : t2);
 }
 
+// One level of Winograd's variant, its shared partial sums expanded into
+// signed sums of source blocks (the kernel forms every operand from the
+// blocks themselves, in fp32, rounded once):
+//   S1 = A21 + A22, S2 = S1 - A11, S3 = A11 - A21, S4 = A12 - S2
+//   T1 = B12 - B11, T2 = B22 - T1, T3 = B22 - B12, T4 = T2 - B21
+//   P1 = A11 B11, P2 = A12 B21, P3 = S4 B22, P4 = A22 T4,
+//   P5 = S1 T1, P6 = S2 T2, P7 = S3 T3
+//   C11 = P1 + P2, C12 = P1 + P6 + P5 + P3, C21 = P1 + P6 + P7 - P4,
+//   C22 = P1 + P6 + P7 + P5
+struct TermW {
+  int r, c, sign;
+};
+struct ProductW {
+  int na;
+  TermW a[4];
+  int nb;
+  TermW b[4];
+  int nc;
+  TermW c[4];
+};
+const ProductW kWinograd1[7] = {
+    // P1 = A11 B11 -> every output block
+    {1, {{0, 0, 1}}, 1, {{0, 0, 1}}, 4, {{0, 0, 1}, {0, 1, 1}, {1, 0, 1}, {1, 1, 1}}},
+    // P2 = A12 B21 -> C11
+    {1, {{0, 1, 1}}, 1, {{1, 0, 1}}, 1, {{0, 0, 1}}},
+    // P3 = (A11 + A12 - A21 - A22) B22 -> C12
+    {4, {{0, 0, 1}, {0, 1, 1}, {1, 0, -1}, {1, 1, -1}}, 1, {{1, 1, 1}}, 1, {{0, 1, 1}}},
+    // P4 = A22 (B11 - B12 - B21 + B22) -> C21 -
+    {1, {{1, 1, 1}}, 4, {{0, 0, 1}, {0, 1, -1}, {1, 0, -1}, {1, 1, 1}}, 1, {{1, 0, -1}}},
+    // P5 = (A21 + A22)(B12 - B11) -> C12, C22
+    {2, {{1, 0, 1}, {1, 1, 1}}, 2, {{0, 1, 1}, {0, 0, -1}}, 2, {{0, 1, 1}, {1, 1, 1}}},
+    // P6 = (A21 + A22 - A11)(B22 - B12 + B11) -> C12, C21, C22
+    {3, {{1, 0, 1}, {1, 1, 1}, {0, 0, -1}}, 3, {{1, 1, 1}, {0, 1, -1}, {0, 0, 1}}, 3,
+     {{0, 1, 1}, {1, 0, 1}, {1, 1, 1}}},
+    // P7 = (A11 - A21)(B22 - B12) -> C21, C22
+    {2, {{0, 0, 1}, {1, 0, -1}}, 2, {{1, 1, 1}, {0, 1, -1}}, 2, {{1, 0, 1}, {1, 1, 1}}},
+};
+
+StrassenTable build_winograd_table() {
+  StrassenTable t;
+  std::memset(&t, 0, sizeof(t));
+  bool seen[4] = {false};
+  for (int p = 0; p < 7; ++p) {
+    const ProductW& P = kWinograd1[p];
+    t.na[p] = static_cast<uint8_t>(P.na);
+    t.nb[p] = static_cast<uint8_t>(P.nb);
+    t.nc[p] = static_cast<uint8_t>(P.nc);
+    for (int i = 0; i < P.na; ++i) t.a[p][i] = term_code(P.a[i].r, P.a[i].c, P.a[i].sign, 1);
+    for (int i = 0; i < P.nb; ++i) t.b[p][i] = term_code(P.b[i].r, P.b[i].c, P.b[i].sign, 1);
+    for (int i = 0; i < P.nc; ++i) {
+      t.c[p][i] = term_code(P.c[i].r, P.c[i].c, P.c[i].sign, 1);
+      const int idx = t.c[p][i] & fgemm::kTermIndexMask;
+      if (!seen[idx]) {  // the first contribution to a block stores
+        seen[idx] = true;
+        t.c[p][i] |= fgemm::kTermFirst;
+      }
+    }
+  }
+  return t;
+}
+
+const StrassenTable& winograd_table_ref() {
+  static const StrassenTable t = build_winograd_table();
+  return t;
+}
+
 // ------------------------------------------------------- tensor maps
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -218,6 +288,7 @@ namespace fgemm {
 // other host translation units.
 const StrassenTable& strassen_table(int depth) { return table_for(depth); }
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return get_encode_fn(); }
+const StrassenTable& winograd_table() { return winograd_table_ref(); }
 void set_thread_message(const std::string& text) { g_thread_msg = text; }
 }  // namespace fgemm
 
@@ -291,7 +362,7 @@ fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     return fail(msg, FGEMM_ERR_INVALID_ARG, "dtype must be FGEMM_F16 or FGEMM_BF16");
   if (kind < FGEMM_EPI_NONE || kind > FGEMM_EPI_SWIGLU)
     return fail(msg, FGEMM_ERR_INVALID_ARG, "unknown epilogue kind");
-  if (algo < FGEMM_ALGO_AUTO || algo > FGEMM_ALGO_STRASSEN2)
+  if (algo < FGEMM_ALGO_AUTO || algo > FGEMM_ALGO_WINOGRAD1)
     return fail(msg, FGEMM_ERR_INVALID_ARG, "unknown algorithm");
   if (tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 256)
     return fail(msg, FGEMM_ERR_INVALID_ARG, "tile_n must be 0, 64, 128 or 256");
@@ -325,7 +396,7 @@ fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     return fail(msg, FGEMM_ERR_ALIGNMENT, "SWIGLU needs N a multiple of 16 (up half 16-byte aligned)");
   if (algo != FGEMM_ALGO_AUTO || tile_m != 0 || tile_n != 0) {
     bool any = false;
-    for (fgemm_algo_t a : {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2}) {
+    for (fgemm_algo_t a : kForms) {
       if (algo != FGEMM_ALGO_AUTO && a != algo) continue;
       for (int32_t tm : {128, 256}) {
         if (tile_m != 0 && tm != tile_m) continue;
@@ -337,9 +408,9 @@ fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     }
     if (!any)
       return fail(msg, FGEMM_ERR_UNSUPPORTED,
-                  "no legal form/tile: Strassen forms need M, N, K divisible into 2^d blocks of "
-                  "whole 128 x tile_n x 64 tiles; 256-row tiles are classical only; SWIGLU needs "
-                  "tile_n >= 128");
+                  "no legal form/tile: Strassen and Winograd forms need M, N, K divisible into "
+                  "2^d blocks of whole 128 x tile_n x 64 tiles; 256-row tiles are classical or "
+                  "one Strassen level only; SWIGLU needs tile_n >= 128");
   }
   return FGEMM_OK;
 }
@@ -353,7 +424,7 @@ fgemm_status_t choose_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, in
     return FGEMM_OK;
   }
   Plan p{FGEMM_ALGO_CLASSICAL, 0, 0, INFINITY};
-  for (fgemm_algo_t a : {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2}) {
+  for (fgemm_algo_t a : kForms) {
     if (algo != FGEMM_ALGO_AUTO && a != algo) continue;
     for (int32_t tm : {128, 256}) {
       if (tile_m != 0 && tm != tile_m) continue;
@@ -482,6 +553,7 @@ fgemm_status_t load_calibration(fgemm_handle_t h, const char* path) {
       {"eff_strassen2_256", &m.eff_strassen[1][1]}, {"launch_us", &m.launch_us},
       {"tile_fill_us", &m.tile_fill_us},        {"l2_bytes", &m.l2_bytes},
       {"l2_gbs", &m.l2_gbs},                    {"split_fix_us", &m.split_fix_us},
+      {"eff_winograd1_128", &m.eff_winograd[0]}, {"eff_winograd1_256", &m.eff_winograd[1]},
   };
   int found = 0;
   for (auto& fd : fields) found += json_number(text, fd.key, fd.dst) ? 1 : 0;
@@ -694,7 +766,8 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
   p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (1u << 16) |
             (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>(bm >> 4) << 24);
   p.num_products = d == 0 ? 1 : (d == 1 ? 7 : 49);
-  p.tab = table_for(d);
+  const bool wino = plan.algo == FGEMM_ALGO_WINOGRAD1;
+  p.tab = wino ? winograd_table_ref() : table_for(d);
 
   s = encode_tmap(h, &p.tmap_a, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                   static_cast<uint64_t>(lda), fgemm::kBM, p.is_bf16);
@@ -736,7 +809,8 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
     if (s != FGEMM_OK) return s;
     p.workspace = h->workspace;
   }
-  cudaError_t e = fgemm::launch_gemm(bn, d, p, grid, h->stream);
+  cudaError_t e = wino ? fgemm::launch_gemm_winograd1(bn, p, grid, h->stream)
+                       : fgemm::launch_gemm(bn, d, p, grid, h->stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "GEMM kernel launch");
   return FGEMM_OK;
 }
@@ -889,6 +963,11 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
       if (!time_gemm(n, n, n, FGEMM_ALGO_STRASSEN1, 256, i == 0 ? 128 : 256, &us)) break;
       m.eff_strassen_pair[i] = flops * 7.0 / 8.0 / (us * 1e6) / m.peak_tflops;
     }
+    for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
+      double us = 0;
+      if (!time_gemm(n, n, n, FGEMM_ALGO_WINOGRAD1, 128, i == 0 ? 128 : 256, &us)) break;
+      m.eff_winograd[i] = flops * 7.0 / 8.0 / (us * 1e6) / m.peak_tflops;
+    }
     if (status != FGEMM_OK) break;
     {  // launch + fill: one tiny tile
       double us = 0;
@@ -930,11 +1009,13 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
                  "  \"eff_strassen1_256\": %.5f,\n  \"eff_strassen2_128\": %.5f,\n"
                  "  \"eff_strassen2_256\": %.5f,\n  \"eff_strassen1_pair_128\": %.5f,\n"
                  "  \"eff_strassen1_pair_256\": %.5f,\n  \"launch_us\": %.3f,\n  \"tile_fill_us\": %.3f,\n"
-                 "  \"l2_bytes\": %.0f,\n  \"l2_gbs\": %.1f,\n  \"split_fix_us\": %.3f\n}\n",
+                 "  \"l2_bytes\": %.0f,\n  \"l2_gbs\": %.1f,\n  \"split_fix_us\": %.3f,\n"
+                 "  \"eff_winograd1_128\": %.5f,\n  \"eff_winograd1_256\": %.5f\n}\n",
                  m.num_sms, m.peak_tflops, m.hbm_gbs, m.eff_classical[0], m.eff_classical[1],
                  m.eff_classical[2], m.eff_pair[0], m.eff_pair[1], m.eff_strassen[0][0], m.eff_strassen[0][1], m.eff_strassen[1][0],
                  m.eff_strassen[1][1], m.eff_strassen_pair[0], m.eff_strassen_pair[1], m.launch_us,
-                 m.tile_fill_us, m.l2_bytes, m.l2_gbs, m.split_fix_us);
+                 m.tile_fill_us, m.l2_bytes, m.l2_gbs, m.split_fix_us, m.eff_winograd[0],
+                 m.eff_winograd[1]);
     std::fclose(f);
   }
   return FGEMM_OK;

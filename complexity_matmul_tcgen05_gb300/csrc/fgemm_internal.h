@@ -137,6 +137,11 @@ int kernel_threads(int depth);
 cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, int grid,
                         cudaStream_t stream);
 
+// One-level Winograd variant on the single-CTA kernel (bn = 128 or 256): the
+// Strassen kernel with up to four source blocks per formed operand; p.tab
+// must be the Winograd table.
+cudaError_t launch_gemm_winograd1(int bn, const KernelParams& p, int grid, cudaStream_t stream);
+
 // Classical kernel on CTA pairs: 256 x bn tiles (bn = 128 or 256) on exactly
 // `clusters` pairs, which must not exceed gemm_pair_clusters_fit(bn) and must
 // equal the cluster count p's split schedule was planned for.
@@ -152,6 +157,10 @@ cudaError_t launch_strassen_pair(int bn, const KernelParams& p, int max_clusters
 
 // The Strassen coefficient table of `depth` levels (0: one trivial product).
 const StrassenTable& strassen_table(int depth);
+
+// The one-level Winograd-variant table (seven products, operands of up to
+// four blocks, outputs fed by up to four products).
+const StrassenTable& winograd_table();
 
 // One block whose bounded wait on a never-completed mbarrier runs out.
 cudaError_t launch_selftest_wait(const KernelParams& p, cudaStream_t stream);

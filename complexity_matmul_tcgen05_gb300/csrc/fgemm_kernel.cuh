@@ -385,13 +385,16 @@ __device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8], int is_bf
 // 128-byte-swizzled operand buffers.  A and B chunks (16 bytes = 8 elements)
 // form one work list so every thread keeps U chunks x terms loads in flight
 // before it stores anything (the loads come from L2; their latency, not
-// bandwidth, is what limits this stage).
-template <int BN, int DEPTH>
+// bandwidth, is what limits this stage).  TERMS bounds the source blocks of
+// one formed operand: 2^DEPTH for the Strassen tables, 4 for the one-level
+// Winograd table (whose expanded operands have up to four blocks).
+template <int BN, int DEPTH, int TERMS>
 __device__ __forceinline__ void form_operands(const KernelParams& p, uint8_t* sA, uint8_t* sB,
                                               int pr, int tm, int tn, int kb, int tid,
                                               int nthreads) {
-  constexpr int T = 1 << DEPTH;            // terms per formed operand (at most)
-  constexpr int U = DEPTH == 1 ? 8 : 4;    // chunks per thread in flight: U * T loads
+  constexpr int T = TERMS;                 // terms per formed operand (at most)
+  constexpr int G = 1 << DEPTH;            // blocks per dimension
+  constexpr int U = T == 2 ? 8 : 4;        // chunks per thread in flight: U * T loads
   constexpr int CPR = BN / 8;              // 16-byte chunks per K-row of the B tile
   const int na = p.tab.na[pr], nb = p.tab.nb[pr];
   const int nA = na > 1 ? kBM * 8 : 0;
@@ -406,12 +409,12 @@ __device__ __forceinline__ void form_operands(const KernelParams& p, uint8_t* sA
     const uint8_t ca = p.tab.a[pr][t < na ? t : 0];
     const int qa = ca & kTermIndexMask;
     srcA[t] = p.A + static_cast<long long>((qa >> DEPTH) * p.sub_m + tm * kBM) * p.lda +
-              (qa & (T - 1)) * p.sub_k + kb * kBK;
+              (qa & (G - 1)) * p.sub_k + kb * kBK;
     sgA[t] = (ca & kTermNeg) ? -1.0f : 1.0f;
     const uint8_t cb = p.tab.b[pr][t < nb ? t : 0];
     const int qb = cb & kTermIndexMask;
     srcB[t] = p.B + static_cast<long long>((qb >> DEPTH) * p.sub_k + kb * kBK) * p.ldb +
-              (qb & (T - 1)) * p.sub_n + tn * BN;
+              (qb & (G - 1)) * p.sub_n + tn * BN;
     sgB[t] = (cb & kTermNeg) ? -1.0f : 1.0f;
   }
   const long long lda = p.lda, ldb = p.ldb;
@@ -470,7 +473,7 @@ __device__ __forceinline__ void form_operands(const KernelParams& p, uint8_t* sA
 
 // ---------------------------------------------------------------- kernel
 
-template <int BN, int DEPTH>
+template <int BN, int DEPTH, int TERMS = (1 << DEPTH)>
 __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
     fgemm_kernel(const __grid_constant__ KernelParams p) {
   using TC = TileCfg<BN>;
@@ -685,7 +688,7 @@ __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
             break;
           }
           if (a_sum || b_sum)
-            form_operands<BN, DEPTH>(p, base_ptr + s * TC::kABytes,
+            form_operands<BN, DEPTH, TERMS>(p, base_ptr + s * TC::kABytes,
                                      base_ptr + S * TC::kABytes + s * TC::kBBytes, pr, tm, tn, kb,
                                      tid, NT);
           ptx::fence_proxy_async_smem();
@@ -706,9 +709,9 @@ __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem_base, TC::kTmemCols);
 }
 
-template <int BN, int DEPTH>
+template <int BN, int DEPTH, int TERMS = (1 << DEPTH)>
 cudaError_t launch_gemm_t(const KernelParams& p, int grid, cudaStream_t stream) {
-  auto kern = fgemm_kernel<BN, DEPTH>;
+  auto kern = fgemm_kernel<BN, DEPTH, TERMS>;
   constexpr int smem = TileCfg<BN>::kSmemBytes;
   static unsigned long long configured = 0;  // per-device bit
   int dev = 0;

@@ -4,7 +4,8 @@
 // algorithm is estimated from compute throughput, memory bandwidth and the
 // extra cost that grows with the recursion depth, and the candidate with the
 // smallest predicted time (with its tiling) is chosen; item 5: the choice is
-// made at run time from the actual (M, N, K).
+// made at run time from the actual (M, N, K).  Candidates: classical, Strassen at one or
+// two levels, and one level of Winograd's variant (single-CTA tiles).
 //
 // The estimate for one (form, tile_n) candidate:
 //   tiles        = tile quantization of the output of one product:
@@ -37,7 +38,8 @@
 namespace {
 
 int depth_of(fgemm_algo_t a) {
-  return a == FGEMM_ALGO_STRASSEN1 ? 1 : (a == FGEMM_ALGO_STRASSEN2 ? 2 : 0);
+  return (a == FGEMM_ALGO_STRASSEN1 || a == FGEMM_ALGO_WINOGRAD1) ? 1
+                                                                 : (a == FGEMM_ALGO_STRASSEN2 ? 2 : 0);
 }
 
 int tile_index(int tile_n) { return tile_n == 64 ? 0 : (tile_n == 128 ? 1 : 2); }
@@ -55,7 +57,7 @@ bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo
   if (tile_m != 128 && tile_m != 256) return false;
   if (epi_kind == FGEMM_EPI_SWIGLU && tile_n == 64) return false;
   const int d = depth_of(algo);
-  if (tile_m == 256 && (tile_n < 128 || d == 2)) return false;
+  if (tile_m == 256 && (tile_n < 128 || d == 2 || algo == FGEMM_ALGO_WINOGRAD1)) return false;
   if (d == 0) return true;
   if (tile_n == 64) return false;
   const int64_t g = int64_t{1} << d;
@@ -94,6 +96,8 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   m.l2_bytes = 126.0 * 1024 * 1024;
   m.l2_gbs = 40000.0;
   m.split_fix_us = 4.0;
+  m.eff_winograd[0] = 0.065;  // 128 x 128 (below Strassen's: 14 + 14 source terms, not 12 + 12)
+  m.eff_winograd[1] = 0.074;  // 128 x 256
   *out = m;
 }
 
@@ -189,8 +193,11 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
   // a pair of SMs works on one 256-row tile
   const int32_t slots = pair ? std::max(1, dev->num_sms / 2) : dev->num_sms;
   const int64_t waves = fgemm_model_waves(tiles, slots, nullptr);
+  const bool wino = algo == FGEMM_ALGO_WINOGRAD1;
   double eff;
-  if (d > 0 && pair)
+  if (wino)
+    eff = dev->eff_winograd[tile_n == 128 ? 0 : 1];
+  else if (d > 0 && pair)
     eff = dev->eff_strassen_pair[tile_n == 128 ? 0 : 1];
   else if (d > 0)
     eff = dev->eff_strassen[d - 1][tile_n == 128 ? 0 : 1];
@@ -218,7 +225,8 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     const double nslots = std::pow(4.0, d);
     const double live = std::min<double>(static_cast<double>(tiles), dev->num_sms) * nslots * slot_bytes;
     if (live > dev->l2_bytes) {
-      const double contributions = std::pow(12.0, d);  // nonzeros of the combination
+      // nonzeros of the output combination: 12 per Strassen level, 14 for Winograd
+      const double contributions = wino ? 14.0 : std::pow(12.0, d);
       bytes += static_cast<double>(tiles) * (2.0 * contributions) * slot_bytes;
     }
   }
@@ -227,7 +235,7 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
   // re-reads its source blocks; the scheme's term counts are 12 + 12 at depth
   // 1 and 144 + 144 at depth 2 (against 8 + 8 for the four classical blocks).
   double op_elems = static_cast<double>(tiles) * (tile_m + tile_n) * k_pad;
-  if (d == 1) op_elems *= 12.0;
+  if (d == 1) op_elems *= wino ? 14.0 : 12.0;
   if (d == 2) op_elems *= 144.0;
   const double t_operands = 2.0 * op_elems / (dev->l2_gbs * 1e3);
   if (predicted_us)
@@ -239,7 +247,8 @@ fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M, int6
                                 int32_t epi_kind, fgemm_algo_t* algo_out, int32_t* tile_m,
                                 int32_t* tile_n, double* predicted_us) {
   if (!dev) return FGEMM_ERR_INVALID_ARG;
-  const fgemm_algo_t algos[3] = {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2};
+  const fgemm_algo_t algos[4] = {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2,
+                                 FGEMM_ALGO_WINOGRAD1};
   const int32_t tms[2] = {128, 256};
   const int32_t tns[3] = {64, 128, 256};
   double best = INFINITY;

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libfgemm.so")
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_NO_DEVICE, \
     ERR_CALIBRATION = range(8)
 F16, BF16 = 0, 1
-ALGOS = {"auto": 0, "classical": 1, "strassen1": 2, "strassen2": 3}
+ALGOS = {"auto": 0, "classical": 1, "strassen1": 2, "strassen2": 3, "winograd1": 4}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 EPILOGUES = {"none": 0, "scale_bias": 1, "silu": 2, "swiglu": 3}
 
@@ -47,7 +47,8 @@ class DeviceModel(ctypes.Structure):
                 ("eff_strassen_pair", ctypes.c_double * 2),
                 ("launch_us", ctypes.c_double), ("tile_fill_us", ctypes.c_double),
                 ("l2_bytes", ctypes.c_double), ("l2_gbs", ctypes.c_double),
-                ("split_fix_us", ctypes.c_double)]
+                ("split_fix_us", ctypes.c_double),
+                ("eff_winograd", ctypes.c_double * 2)]
 
 
 _lib = None

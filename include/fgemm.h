@@ -50,7 +50,12 @@ typedef enum {
   FGEMM_ALGO_AUTO = 0,
   FGEMM_ALGO_CLASSICAL = 1,
   FGEMM_ALGO_STRASSEN1 = 2, /* one Strassen level: 7 half-size products */
-  FGEMM_ALGO_STRASSEN2 = 3  /* two levels: 49 quarter-size products */
+  FGEMM_ALGO_STRASSEN2 = 3, /* two levels: 49 quarter-size products */
+  FGEMM_ALGO_WINOGRAD1 = 4  /* one level of Winograd's variant: 7 half-size
+                             * products whose operands are sums of up to four
+                             * blocks (FalconGEMM summary, "Methodology" item 1
+                             * names it; standard identities). One-CTA tiles
+                             * only (tile_m 128, tile_n 128 or 256). */
 } fgemm_algo_t;
 
 /*
@@ -260,6 +265,8 @@ typedef struct {
   double split_fix_us;     /* fixed cost of splitting the last wave of CTA-pair
                             * tiles along K (partial stores, the sum by the last
                             * piece, its exposed epilogue) */
+  double eff_winograd[2];  /* one Winograd level, 128 x {128, 256}: executed-MAC
+                            * rate of its mainloop as a fraction of peak */
 } fgemm_device_model_t;
 
 /* Default model for a device with the given SM count, peak and bandwidth. */

@@ -16,7 +16,11 @@ import torch
 import oracle
 from complexity_matmul_tcgen05_gb300 import fgemm, inputs
 
-TOL_NORMWISE = {"classical": 1e-3, "strassen1": 5e-3, "strassen2": 1e-2}
+# Winograd's variant is not among the forms the budgets were set for; its
+# operands are rounded sums of up to four blocks, and the oracle's emulation
+# puts its inherent error at 6.0e-3 on U[-1,1] bf16 inputs (Strassen-1: 4.4e-3).
+# Its budget keeps Strassen-1's ratio of budget to inherent error (5e-3 / 4.4e-3).
+TOL_NORMWISE = {"classical": 1e-3, "strassen1": 5e-3, "strassen2": 1e-2, "winograd1": 7e-3}
 TOL_EMULATED = 1e-4
 
 

@@ -322,3 +322,25 @@ def test_model_split_removes_the_pair_sawtooth(L):
     _, t77w = _predict(L, m, 256 * 77, 256, 8192, "classical", 256, tile_m=256)
     assert abs(t77w - (m.launch_us + 2 * t_tile)) < 1e-6 * t77w
     assert t77 < 0.8 * t77w
+
+
+def test_winograd_legality_and_model(L):
+    # one level on single-CTA tiles of 128 x {128, 256}; never on CTA pairs
+    ep = fgemm.make_epilogue("none")
+    ok = lambda M, N, K, tm, tn: fgemm.validate(M, N, K, 16, K, 16, N, 16, N, fgemm.BF16, ep,
+                                                "winograd1", tn, tm)
+    assert ok(512, 512, 256, 128, 128) == fgemm.OK
+    assert ok(512, 1024, 256, 128, 256) == fgemm.OK
+    assert ok(512, 512, 256, 256, 256) == fgemm.ERR_UNSUPPORTED
+    assert ok(512, 512, 256, 128, 64) == fgemm.ERR_UNSUPPORTED
+    assert ok(384, 512, 256, 128, 128) == fgemm.ERR_UNSUPPORTED   # 192-row blocks
+    m = _model(L)
+    s, tw = _predict(L, m, 16384, 16384, 16384, "winograd1", 256)
+    assert s == fgemm.OK and tw > 0
+    assert _predict(L, m, 16384, 16384, 16384, "winograd1", 256, tile_m=256)[0] == fgemm.ERR_UNSUPPORTED
+    # with the Strassen mainloop rate, the extra source terms (14 + 14 vs
+    # 12 + 12) make it predict no faster than Strassen-1
+    m.eff_winograd[1] = m.eff_strassen[0][1]
+    _, ts = _predict(L, m, 16384, 16384, 16384, "strassen1", 256)
+    _, tw = _predict(L, m, 16384, 16384, 16384, "winograd1", 256)
+    assert tw >= ts

@@ -24,7 +24,7 @@ def _sampled_check(name, A, B, bias, run_algo, epi, dtype, tile=0):
     N = B.shape[1]
     n_out = N // 2 if epi == "swiglu" else N
     algo = _picked(M, N, K, epi) if run_algo == "auto" else run_algo
-    depth_blocks = {"classical": 1, "strassen1": 2, "strassen2": 4}[algo]
+    depth_blocks = {"classical": 1, "strassen1": 2, "strassen2": 4, "winograd1": 2}[algo]
     C = run(A, B, algo=run_algo, epilogue=epi, bias=bias, tile_n=tile)
     # Strassen forms sit within a few percent of their normwise budgets (the
     # rounded operand sums alone give 4.7e-3 and 9.7e-3 on these inputs), so
@@ -65,13 +65,13 @@ def test_proj_4096_bias(algo):
     _sampled_check("proj_4096", A, B, bias, algo, "scale_bias", "bf16")
 
 
-@pytest.mark.parametrize("algo", ["classical", "strassen1", "auto"])
+@pytest.mark.parametrize("algo", ["classical", "strassen1", "winograd1", "auto"])
 def test_ffn_up_swiglu(algo):
     A, B, _ = inputs.workload_inputs("ffn_up_swiglu_bf16", DEV)
     _sampled_check("ffn_up", A, B, None, algo, "swiglu", "bf16")
 
 
-@pytest.mark.parametrize("algo", ["classical", "strassen1", "strassen2", "auto"])
+@pytest.mark.parametrize("algo", ["classical", "strassen1", "strassen2", "winograd1", "auto"])
 def test_square_16384(algo):
     A, B, _ = inputs.workload_inputs("square_16384_bf16", DEV)
     _sampled_check("square_16384", A, B, None, algo, "none", "bf16")

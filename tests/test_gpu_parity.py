@@ -46,6 +46,10 @@ EXACT_CASES = [
     ("strassen1", 512, 1024, 640, 256),
     ("strassen2", 512, 512, 256, 128),
     ("strassen2", 512, 1024, 512, 256),
+    ("winograd1", 256, 256, 128, 128),
+    ("winograd1", 256, 512, 128, 256),
+    ("winograd1", 512, 1024, 640, 256),
+    ("winograd1", 1024, 512, 384, 128),
 ]
 # CTA-pair tiles (256 rows over two SMs): (M, N, K, tile_n)
 EXACT_PAIR_CASES = [
@@ -128,7 +132,8 @@ def _full_check(A, B, algo, dtype, epilogue="none", alpha=1.0, bias=None, tile=0
         ok, _ = elementwise_ok(c, ref, absdot, A.shape[1], dtype)
         assert ok
     if depth > 0:
-        emu = oracle.epilogue(oracle.strassen_emulated(Av, Bv, depth, dtype), epilogue, alpha, bv)
+        emulated = oracle.winograd_emulated if algo == "winograd1" else oracle.strassen_emulated
+        emu = oracle.epilogue(emulated(Av, Bv, depth, dtype), epilogue, alpha, bv)
         e2 = float(np.linalg.norm(c - oracle.round_to(emu, dtype)) / np.linalg.norm(emu))
         assert e2 <= TOL_EMULATED * max(1.0, kappa), (e2, kappa)
     return err
@@ -154,7 +159,7 @@ def test_classical_epilogues_every_entry(epilogue, alpha, tile_m, tile):
 @pytest.mark.parametrize("algo,tile_m,tile,depth", [
     ("classical", 128, 128, 0), ("classical", 128, 256, 0), ("classical", 256, 128, 0),
     ("classical", 256, 256, 0), ("strassen1", 128, 128, 1), ("strassen1", 128, 256, 1),
-    ("strassen1", 256, 256, 1), ("strassen2", 128, 128, 2)])
+    ("strassen1", 256, 256, 1), ("strassen2", 128, 128, 2), ("winograd1", 128, 256, 1)])
 def test_swiglu_every_entry(algo, tile_m, tile, depth):
     M, N, K = 512, 2048, 512
     A = inputs.matrix(M, K, "normal", "bf16", 0, DEV)
@@ -165,7 +170,8 @@ def test_swiglu_every_entry(algo, tile_m, tile, depth):
 
 @pytest.mark.parametrize("algo,tile_m,tile,depth", [
     ("strassen1", 128, 128, 1), ("strassen1", 128, 256, 1), ("strassen1", 256, 128, 1),
-    ("strassen1", 256, 256, 1), ("strassen2", 128, 128, 2), ("strassen2", 128, 256, 2)])
+    ("strassen1", 256, 256, 1), ("strassen2", 128, 128, 2), ("strassen2", 128, 256, 2),
+    ("winograd1", 128, 128, 1), ("winograd1", 128, 256, 1)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_strassen_every_entry_and_emulation(algo, tile_m, tile, depth, dtype):
     """Normwise bound and the tighter pin: GPU Strassen vs the emulated
