@@ -189,7 +189,8 @@ def measured_peaks():
 
 KERNEL_SOURCES = ("fgemm_kernel.cuh", "fgemm_kernel_pair.cuh", "fgemm_ptx.cuh",
                   "fgemm_internal.h", "fgemm_kern_classical.cu", "fgemm_kern_pair.cu",
-                  "fgemm_kern_strassen1.cu", "fgemm_kern_strassen2.cu", "fgemm_kern_winograd1.cu")
+                  "fgemm_kern_strassen1.cu", "fgemm_kern_strassen2.cu", "fgemm_kern_winograd1.cu",
+                  "fgemm_kern_skinny.cu")
 
 
 def kernel_source_hash():
@@ -450,7 +451,8 @@ def run_fgemm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-CANDIDATES = [("classical", 128, 64), ("classical", 128, 128), ("classical", 128, 256),
+CANDIDATES = [("classical", 16, 128), ("classical", 32, 128), ("classical", 64, 128),
+              ("classical", 128, 64), ("classical", 128, 128), ("classical", 128, 256),
               ("classical", 256, 128), ("classical", 256, 256), ("strassen1", 128, 128),
               ("strassen1", 128, 256), ("strassen1", 256, 128), ("strassen1", 256, 256),
               ("strassen2", 128, 128), ("strassen2", 128, 256), ("winograd1", 128, 128),

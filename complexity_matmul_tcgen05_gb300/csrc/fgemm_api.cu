@@ -366,8 +366,8 @@ fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     return fail(msg, FGEMM_ERR_INVALID_ARG, "unknown algorithm");
   if (tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 256)
     return fail(msg, FGEMM_ERR_INVALID_ARG, "tile_n must be 0, 64, 128 or 256");
-  if (tile_m != 0 && tile_m != 128 && tile_m != 256)
-    return fail(msg, FGEMM_ERR_INVALID_ARG, "tile_m must be 0, 128 or 256");
+  if (tile_m != 0 && tile_m != 16 && tile_m != 32 && tile_m != 64 && tile_m != 128 && tile_m != 256)
+    return fail(msg, FGEMM_ERR_INVALID_ARG, "tile_m must be 0, 16, 32, 64, 128 or 256");
   if (M < 0 || N < 0 || K < 0) return fail(msg, FGEMM_ERR_INVALID_ARG, "negative dimension");
   const int64_t kMax = (int64_t{1} << 31) - 1;
   if (M > kMax || N > kMax || K > kMax)
@@ -398,7 +398,7 @@ fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     bool any = false;
     for (fgemm_algo_t a : kForms) {
       if (algo != FGEMM_ALGO_AUTO && a != algo) continue;
-      for (int32_t tm : {128, 256}) {
+      for (int32_t tm : {16, 32, 64, 128, 256}) {
         if (tile_m != 0 && tm != tile_m) continue;
         for (int32_t tn : {64, 128, 256}) {
           if (tile_n != 0 && tn != tile_n) continue;
@@ -410,7 +410,8 @@ fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
       return fail(msg, FGEMM_ERR_UNSUPPORTED,
                   "no legal form/tile: Strassen and Winograd forms need M, N, K divisible into "
                   "2^d blocks of whole 128 x tile_n x 64 tiles; 256-row tiles are classical or "
-                  "one Strassen level only; SWIGLU needs tile_n >= 128");
+                  "one Strassen level only; tile_m 16/32/64 (small M) needs M <= tile_m, "
+                  "tile_n 128, classical, no SWIGLU; SWIGLU needs tile_n >= 128");
   }
   return FGEMM_OK;
 }
@@ -426,7 +427,7 @@ fgemm_status_t choose_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, in
   Plan p{FGEMM_ALGO_CLASSICAL, 0, 0, INFINITY};
   for (fgemm_algo_t a : kForms) {
     if (algo != FGEMM_ALGO_AUTO && a != algo) continue;
-    for (int32_t tm : {128, 256}) {
+    for (int32_t tm : {16, 32, 64, 128, 256}) {
       if (tile_m != 0 && tm != tile_m) continue;
       for (int32_t tn : {64, 128, 256}) {
         if (tile_n != 0 && tn != tile_n) continue;
@@ -463,13 +464,9 @@ fgemm_status_t ensure_workspace(fgemm_handle_t h, size_t bytes) {
   return FGEMM_OK;
 }
 
-// Workspace, counters and generation of a K-split pair launch.
-fgemm_status_t prepare_split(fgemm_handle_t h, KernelParams* p, int split, int pieces, int bn) {
-  const size_t slots = static_cast<size_t>(split) * pieces * 2;
-  fgemm_status_t s =
-      ensure_workspace(h, slots * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float));
-  if (s != FGEMM_OK) return s;
-  const size_t ctrs = static_cast<size_t>(split) * 8;  // 2 CTAs x 4 epilogue warps
+// Arrival counters for pieces (at least `ctrs`), zeroed when (re)allocated,
+// and the next launch generation (1 .. 2^24 - 1) in h->split_gen.
+fgemm_status_t ensure_counters(fgemm_handle_t h, size_t ctrs) {
   if (ctrs > h->split_ctr_count) {
     if (h->split_ctr) {
       cudaError_t e = cudaStreamSynchronize(h->stream);
@@ -498,11 +495,64 @@ fgemm_status_t prepare_split(fgemm_handle_t h, KernelParams* p, int split, int p
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync(split counters)");
     h->split_gen = 1;
   }
+  return FGEMM_OK;
+}
+
+// Workspace, counters and generation of a K-split pair launch.
+fgemm_status_t prepare_split(fgemm_handle_t h, KernelParams* p, int split, int pieces, int bn) {
+  const size_t slots = static_cast<size_t>(split) * pieces * 2;
+  fgemm_status_t s =
+      ensure_workspace(h, slots * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float));
+  if (s != FGEMM_OK) return s;
+  s = ensure_counters(h, static_cast<size_t>(split) * 8);  // 2 CTAs x 4 epilogue warps
+  if (s != FGEMM_OK) return s;
   p->split_tiles = split;
   p->split_pieces = pieces;
   p->split_gen = h->split_gen;
   p->split_ctr = h->split_ctr;
   p->split_ws = h->workspace;
+  return FGEMM_OK;
+}
+
+
+// The small-M kernel (tile_m = mp in {16, 32, 64}, M <= mp): C^T = B^T A^T
+// over 128-column tiles of C, the K blocks of all tiles shared out over the
+// SMs.  A's descriptor uses an {64, mp} box; partial slots and counters are
+// two and eight per CTA.
+fgemm_status_t launch_small_m(fgemm_handle_t h, KernelParams& p, int64_t M, int64_t N, int64_t K,
+                              const void* A, int64_t lda, const void* B, int64_t ldb, int mp) {
+  const long long tiles = (static_cast<long long>(p.n_out) + 127) / 128;
+  if (tiles > (1ll << 30)) return set_msg(h, FGEMM_ERR_UNSUPPORTED, "too many tiles");
+  p.num_units = static_cast<int>(tiles);
+  p.tiles_m = 1;
+  p.tiles_n = p.num_units;
+  p.k_blocks = static_cast<int>((K + fgemm::kBK - 1) / fgemm::kBK);
+  const uint32_t fmt = p.is_bf16 ? 1u : 0u;
+  // tcgen05 instruction descriptor: fp32 accumulator, A = B^T (MN-major, bit
+  // 15), B = A^T (K-major), N = mp, M = 128
+  p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (1u << 15) |
+            (static_cast<uint32_t>(mp >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+  fgemm_status_t s = encode_tmap(h, &p.tmap_a, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                                 static_cast<uint64_t>(lda), static_cast<uint32_t>(mp), p.is_bf16);
+  if (s != FGEMM_OK) return s;
+  s = encode_tmap(h, &p.tmap_b, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                  static_cast<uint64_t>(ldb), fgemm::kBK, p.is_bf16);
+  if (s != FGEMM_OK) return s;
+  // every CTA streams at least kMinShare K blocks, so that a tile is not cut
+  // into more pieces than its sum can absorb cheaply
+  constexpr long long kMinShare = 8;
+  const long long iters = tiles * p.k_blocks;
+  const int ctas = static_cast<int>(
+      std::max<long long>(1, std::min<long long>(h->num_sms, (iters + kMinShare - 1) / kMinShare)));
+  s = ensure_workspace(h, static_cast<size_t>(ctas) * 2 * 128 * static_cast<size_t>(mp) * sizeof(float));
+  if (s != FGEMM_OK) return s;
+  s = ensure_counters(h, static_cast<size_t>(ctas) * 8);
+  if (s != FGEMM_OK) return s;
+  p.split_ws = h->workspace;
+  p.split_ctr = h->split_ctr;
+  p.split_gen = h->split_gen;
+  cudaError_t e = fgemm::launch_gemm_skinny(mp, p, ctas, h->stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "small-M kernel launch");
   return FGEMM_OK;
 }
 
@@ -745,7 +795,8 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
   if (s != FGEMM_OK) return s;
   const int d = depth_of(plan.algo);
   const int bn = plan.tile_n;
-  const int bm = plan.tile_m;  // 256: CTA pair
+  const int bm = plan.tile_m;  // 256: CTA pair; 16, 32, 64: the small-M kernel
+  if (bm < fgemm::kBM) return launch_small_m(h, p, M, N, K, A, lda, B, ldb, bm);
 
   p.sub_m = static_cast<int>(M >> d);
   p.sub_n = static_cast<int>(N >> d);

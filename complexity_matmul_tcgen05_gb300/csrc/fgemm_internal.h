@@ -93,6 +93,55 @@ FGEMM_HD inline bool work_item(int num_units, int split_tiles, int split_pieces,
   return true;
 }
 
+// ---------------------------------------------------------------------------
+// Work schedule of the small-M kernel (stream-K).  Its tiles are 128 columns
+// of C (all M <= 64 rows); the K blocks of all tiles, laid end to end tile
+// after tile (tiles * k_blocks iterations), are cut into `ctas` contiguous
+// shares of equal size (+-1), one per CTA.  A share meets each tile in one
+// contiguous K range (a piece); the pieces of a tile run on consecutive CTAs
+// and are numbered from 0 in K order.  As in the CTA-pair split, every piece
+// of a tile with several pieces stores an fp32 partial and the last to finish
+// sums them in piece order.
+
+// The CTA whose share holds flat iteration x.
+FGEMM_HD inline int stream_k_owner(long long x, long long total, int ctas) {
+  return static_cast<int>(((x + 1) * ctas - 1) / total);
+}
+
+// The n-th work item of CTA `cta` (false once its share is exhausted).
+FGEMM_HD inline bool stream_k_item(int tiles, int k_blocks, int ctas, int cta, int n, WorkItem& w) {
+  const long long total = static_cast<long long>(tiles) * k_blocks;
+  const long long lo = static_cast<long long>(cta) * total / ctas;
+  const long long hi = static_cast<long long>(cta + 1) * total / ctas;
+  if (hi <= lo) return false;
+  const long long start = n == 0 ? lo : (lo / k_blocks + n) * k_blocks;
+  if (start >= hi) return false;
+  const long long t = start / k_blocks;
+  const long long tile_lo = t * k_blocks;
+  const long long end = hi < tile_lo + k_blocks ? hi : tile_lo + k_blocks;
+  const int first = stream_k_owner(tile_lo, total, ctas);
+  const int last = stream_k_owner(tile_lo + k_blocks - 1, total, ctas);
+  w.unit = static_cast<int>(t);
+  w.k0 = static_cast<int>(start - tile_lo);
+  w.k1 = static_cast<int>(end - tile_lo);
+  w.piece = cta - first;
+  w.npieces = last - first + 1;
+  return true;
+}
+
+// Partial slot of the piece of tile `unit` that runs on CTA c.  Only a
+// CTA's first and last work items can be pieces of a shared tile (the items
+// between are whole tiles), so each CTA owns two slots: 2c for its first item
+// and 2c + 1 for its last.  A piece is its CTA's first item exactly when the
+// CTA's share starts inside the tile.  The tile's arrival counters sit with
+// the slot of its piece 0.
+FGEMM_HD inline long long stream_k_slot(int tiles, int k_blocks, int ctas, int unit, int c) {
+  const long long total = static_cast<long long>(tiles) * k_blocks;
+  const long long tile_lo = static_cast<long long>(unit) * k_blocks;
+  const long long lo = static_cast<long long>(c) * total / ctas;
+  return static_cast<long long>(c) * 2 + (lo >= tile_lo ? 0 : 1);
+}
+
 struct KernelParams {
   CUtensorMap tmap_a;  // A: inner dim K, outer M, box {64, 128}, 128B swizzle
   CUtensorMap tmap_b;  // B: inner dim N, outer K, box {64, 64},  128B swizzle
@@ -136,6 +185,13 @@ int kernel_threads(int depth);
 // Strassen depth (0 = classical) with `grid` CTAs on `stream`.
 cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, int grid,
                         cudaStream_t stream);
+
+// Small-M kernel: C (M <= mp rows, mp = 16, 32 or 64) computed as
+// C^T = B^T A^T in tiles of 128 columns of C, K split over `grid` CTAs by
+// stream_k_item.  p.tmap_a has a {64, mp} box; p.split_ws holds 2 * grid
+// partial slots of 128 x mp fp32 and p.split_ctr 8 * grid counters tagged
+// with p.split_gen.
+cudaError_t launch_gemm_skinny(int mp, const KernelParams& p, int grid, cudaStream_t stream);
 
 // One-level Winograd variant on the single-CTA kernel (bn = 128 or 256): the
 // Strassen kernel with up to four source blocks per formed operand; p.tab

@@ -94,6 +94,38 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const K
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
+// Counts one arrival of a split piece on `ctr` (by lane 0 of the calling
+// warp) and tells the whole warp whether it was the last of `npieces`.  The
+// counter holds gen << 8 | arrivals.  A counter tagged with another
+// generation (left by a launch that ended on an error) counts as zero
+// arrivals, and the last arrival resets the counter to zero arrivals of this
+// generation, so a replay of the same launch (a CUDA graph) counts from zero
+// again.  Warp-collective.
+__device__ __forceinline__ bool count_arrival(const KernelParams& p, unsigned int* ctr, int npieces) {
+  const int lane = threadIdx.x & 31;
+  unsigned int count = 0;
+  if (lane == 0) {
+    const unsigned int gen = p.split_gen;
+    unsigned int cur = *reinterpret_cast<volatile unsigned int*>(ctr);
+#pragma unroll 1
+    for (int it = 0; it < (1 << 20); ++it) {
+      const unsigned int next = (cur >> 8) == gen ? cur + 1u : ((gen << 8) | 1u);
+      const unsigned int prev = atomicCAS(ctr, cur, next);
+      if (prev == cur) {
+        count = next & 0xFFu;
+        break;
+      }
+      cur = prev;
+    }
+    if (count == 0)
+      atomicCAS(p.err, 0u, err_code(2));
+    else if (count == static_cast<unsigned int>(npieces))
+      atomicExch(ctr, gen << 8);
+  }
+  count = __shfl_sync(0xFFFFFFFFu, count, 0);
+  return count == static_cast<unsigned int>(npieces);
+}
+
 __device__ __forceinline__ void unit_coords(const KernelParams& p, int unit, int& tm, int& tn) {
   const int G = p.raster_group;
   const int per_group = G * p.tiles_n;

@@ -76,25 +76,8 @@ __device__ __forceinline__ void epilogue_split_piece(const KernelParams& p, uint
   }
   __threadfence();
   __syncwarp();
-  unsigned int count = 0;
-  if (lane == 0) {
-    unsigned int* ctr = p.split_ctr + (static_cast<size_t>(t) * 2 + rank) * 4 + ew;
-    const unsigned int gen = p.split_gen;
-    unsigned int cur = *reinterpret_cast<volatile unsigned int*>(ctr);
-#pragma unroll 1
-    for (int it = 0; it < (1 << 20); ++it) {
-      const unsigned int next = (cur >> 8) == gen ? cur + 1u : ((gen << 8) | 1u);
-      const unsigned int prev = atomicCAS(ctr, cur, next);
-      if (prev == cur) {
-        count = next & 0xFFu;
-        break;
-      }
-      cur = prev;
-    }
-    if (count == 0) atomicCAS(p.err, 0u, err_code(2));
-  }
-  count = __shfl_sync(0xFFFFFFFFu, count, 0);
-  if (count != static_cast<unsigned int>(w.npieces)) {
+  const bool last = count_arrival(p, p.split_ctr + (static_cast<size_t>(t) * 2 + rank) * 4 + ew, w.npieces);
+  if (!last) {
     release();
     return;
   }

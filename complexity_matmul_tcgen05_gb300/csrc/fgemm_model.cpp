@@ -21,8 +21,9 @@
 //                  as S = slots / R pieces of K each (S <= 4), and then
 //                  t_compute = (floor(tiles / slots) + 1/S) * t_tile
 //                  + (S - 1) * split_fix_us, when that is less
-//   t_memory     = HBM bytes / bandwidth (operands and result once, plus the
-//                  Strassen partial tiles when they cannot stay in L2)
+//   t_memory     = HBM bytes / (bandwidth * streaming efficiency * share of
+//                  the SMs the launch keeps busy) (operands and result once,
+//                  plus the Strassen partial tiles when they cannot stay in L2)
 //   t_operands   = operand elements streamed from L2 into the SMs (tiled
 //                  reads, "Page 42": tiles * (128 + tile_n) * K per source
 //                  term) * 2 bytes / L2 bandwidth
@@ -54,6 +55,9 @@ namespace fgemm {
 bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo_t algo,
                    int32_t tile_m, int32_t tile_n) {
   if (tile_n != 64 && tile_n != 128 && tile_n != 256) return false;
+  if (tile_m == 16 || tile_m == 32 || tile_m == 64)  // the small-M kernel
+    return algo == FGEMM_ALGO_CLASSICAL && tile_n == 128 && epi_kind != FGEMM_EPI_SWIGLU &&
+           M <= tile_m;
   if (tile_m != 128 && tile_m != 256) return false;
   if (epi_kind == FGEMM_EPI_SWIGLU && tile_n == 64) return false;
   const int d = depth_of(algo);
@@ -98,6 +102,10 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   m.split_fix_us = 4.0;
   m.eff_winograd[0] = 0.065;  // 128 x 128 (below Strassen's: 14 + 14 source terms, not 12 + 12)
   m.eff_winograd[1] = 0.074;  // 128 x 256
+  m.eff_small_m[0] = 0.056;   // tile_m 16: an N = 16 MMA, 16/256 of the full rate, x 0.9
+  m.eff_small_m[1] = 0.11;    // tile_m 32
+  m.eff_small_m[2] = 0.22;    // tile_m 64
+  m.hbm_stream_eff = 0.9;
   *out = m;
 }
 
@@ -173,12 +181,46 @@ int32_t fgemm_split_work_item(int64_t tiles, int32_t split_tiles, int32_t split_
   return 1;
 }
 
+int32_t fgemm_stream_k_work_item(int64_t tiles, int32_t k_blocks, int32_t ctas, int32_t cta,
+                                 int32_t n, int64_t* out6) {
+  if (tiles <= 0 || tiles > (1ll << 30) || k_blocks <= 0 || ctas <= 0 || cta < 0 || cta >= ctas ||
+      n < 0 || !out6 || static_cast<long long>(ctas) > tiles * k_blocks)
+    return 0;
+  fgemm::WorkItem w;
+  if (!fgemm::stream_k_item(static_cast<int>(tiles), k_blocks, ctas, cta, n, w)) return 0;
+  out6[0] = w.unit;
+  out6[1] = w.k0;
+  out6[2] = w.k1;
+  out6[3] = w.piece;
+  out6[4] = w.npieces;
+  out6[5] = fgemm::stream_k_slot(static_cast<int>(tiles), k_blocks, ctas, w.unit, cta);
+  return 1;
+}
+
 fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, int64_t N,
                                    int64_t K, int32_t epi_kind, fgemm_algo_t algo, int32_t tile_m,
                                    int32_t tile_n, double* predicted_us) {
   if (!dev || M < 0 || N < 0 || K < 0) return FGEMM_ERR_INVALID_ARG;
   if (algo == FGEMM_ALGO_AUTO) return FGEMM_ERR_INVALID_ARG;
   if (!fgemm::form_is_legal(M, N, K, epi_kind, algo, tile_m, tile_n)) return FGEMM_ERR_UNSUPPORTED;
+  if (tile_m < 128) {
+    // small-M kernel: every SM streams an equal share of the K blocks of all
+    // 128-column tiles; bound by B from HBM or by the narrow MMAs
+    const int64_t tiles = ceil_div(N, 128), kb = ceil_div(K, fgemm::kBK);
+    const int64_t iters = tiles * kb;
+    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(dev->num_sms, ceil_div(iters, 8)));
+    const double eff = std::max(dev->eff_small_m[tile_m == 16 ? 0 : (tile_m == 32 ? 1 : 2)], 1e-3);
+    const double sm_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms;
+    const double t_kb = 2.0 * 128.0 * tile_m * fgemm::kBK / (sm_flop_per_us * eff);
+    const double t_compute = static_cast<double>(ceil_div(iters, ctas)) * t_kb + dev->tile_fill_us;
+    const double bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
+                                static_cast<double>(M) * N);
+    const double sm_share = std::min(1.0, static_cast<double>(ctas) / std::max(1, dev->num_sms));
+    const double t_memory =
+        bytes / (dev->hbm_gbs * 1e3 * std::max(dev->hbm_stream_eff, 1e-3) * sm_share);
+    if (predicted_us) *predicted_us = std::max(t_compute, t_memory) + dev->launch_us;
+    return FGEMM_OK;
+  }
   const int d = depth_of(algo);
   const bool swiglu = epi_kind == FGEMM_EPI_SWIGLU;
   const bool pair = tile_m == 256;
@@ -230,7 +272,12 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
       bytes += static_cast<double>(tiles) * (2.0 * contributions) * slot_bytes;
     }
   }
-  const double t_memory = bytes / (dev->hbm_gbs * 1e3);
+  // a launch that keeps s SMs busy streams at most s / num_sms of the device
+  // bandwidth (each SM has a bounded number of copies in flight)
+  const double busy_sms = static_cast<double>(std::min<int64_t>(tiles, slots)) * (pair ? 2.0 : 1.0);
+  const double sm_share = std::min(1.0, busy_sms / std::max(1, dev->num_sms));
+  const double t_memory =
+      bytes / (dev->hbm_gbs * 1e3 * std::max(dev->hbm_stream_eff, 1e-3) * std::max(sm_share, 1e-3));
   // Operand tiles streamed from L2 into the SMs (tiled reads): every product
   // re-reads its source blocks; the scheme's term counts are 12 + 12 at depth
   // 1 and 144 + 144 at depth 2 (against 8 + 8 for the four classical blocks).
@@ -249,7 +296,7 @@ fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M, int6
   if (!dev) return FGEMM_ERR_INVALID_ARG;
   const fgemm_algo_t algos[4] = {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2,
                                  FGEMM_ALGO_WINOGRAD1};
-  const int32_t tms[2] = {128, 256};
+  const int32_t tms[5] = {16, 32, 64, 128, 256};
   const int32_t tns[3] = {64, 128, 256};
   double best = INFINITY;
   fgemm_algo_t best_algo = FGEMM_ALGO_CLASSICAL;

@@ -48,7 +48,8 @@ class DeviceModel(ctypes.Structure):
                 ("launch_us", ctypes.c_double), ("tile_fill_us", ctypes.c_double),
                 ("l2_bytes", ctypes.c_double), ("l2_gbs", ctypes.c_double),
                 ("split_fix_us", ctypes.c_double),
-                ("eff_winograd", ctypes.c_double * 2)]
+                ("eff_winograd", ctypes.c_double * 2),
+                ("eff_small_m", ctypes.c_double * 3), ("hbm_stream_eff", ctypes.c_double)]
 
 
 _lib = None
@@ -108,6 +109,8 @@ def lib() -> ctypes.CDLL:
         L.fgemm_split_work_item.argtypes = [i64, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
         L.fgemm_split_work_item.restype = i32
         L.fgemm_set_split_mode.argtypes = [vp, i32]
+        L.fgemm_stream_k_work_item.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(i64)]
+        L.fgemm_stream_k_work_item.restype = i32
         L.fgemm_get_device_model.argtypes = [vp, model_p]
         L.fgemm_set_device_model.argtypes = [vp, model_p]
         for name in ("fgemm_create", "fgemm_destroy", "fgemm_set_stream", "fgemm_matmul",
@@ -133,6 +136,18 @@ def split_work_items(tiles: int, split_tiles: int, split_pieces: int, clusters: 
     n = 0
     while lib().fgemm_split_work_item(tiles, split_tiles, split_pieces, clusters, k_blocks,
                                       cluster, n, out):
+        items.append(tuple(out))
+        n += 1
+    return items
+
+
+def stream_k_work_items(tiles: int, k_blocks: int, ctas: int, cta: int):
+    """The work list of one CTA of the small-M kernel, as (unit, k0, k1,
+    piece, npieces, slot) tuples (host-side copy of what the kernel runs)."""
+    out = (ctypes.c_int64 * 6)()
+    items = []
+    n = 0
+    while lib().fgemm_stream_k_work_item(tiles, k_blocks, ctas, cta, n, out):
         items.append(tuple(out))
         n += 1
     return items

@@ -144,9 +144,14 @@ fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * the decision model's choices). tile_m = 128: one CTA per tile, tile_n in
  * {64, 128, 256}; tile_m = 256: a pair of CTAs (one M = 256 tensor-core
  * operation across two SMs), tile_n in {128, 256}, classical and one-level
- * Strassen forms. SWIGLU needs tile_n >= 128; the Strassen forms use tile_n
- * in {128, 256}, two levels only with tile_m = 128. tile_m = tile_n = 0 lets the model choose; a zero in only
- * one of them lets the model choose the other.
+ * Strassen forms; tile_m = 16, 32 or 64: the small-M kernel for M <= tile_m
+ * (classical, no SWIGLU, tile_n = 128 columns of C per tile): it computes
+ * C^T = B^T A^T so that the tensor-core rows run over N, and shares the K
+ * blocks of all tiles evenly over the SMs (pieces of a tile are summed in a
+ * fixed order). SWIGLU needs tile_n >= 128; the Strassen forms use tile_n in
+ * {128, 256}, two levels only with tile_m = 128. tile_m = tile_n = 0 lets
+ * the model choose; a zero in only one of them lets the model choose the
+ * other.
  */
 fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N,
                                int64_t K, const void* A, int64_t lda,
@@ -267,6 +272,10 @@ typedef struct {
                             * piece, its exposed epilogue) */
   double eff_winograd[2];  /* one Winograd level, 128 x {128, 256}: executed-MAC
                             * rate of its mainloop as a fraction of peak */
+  double eff_small_m[3];   /* small-M tiles (tile_m 16, 32, 64): MMA rate as a
+                            * fraction of peak (an N = tile_m MMA runs at most
+                            * tile_m / 256 of the full rate) */
+  double hbm_stream_eff;   /* fraction of hbm_gbs a kernel streaming B reaches */
 } fgemm_device_model_t;
 
 /* Default model for a device with the given SM count, peak and bandwidth. */
@@ -338,6 +347,18 @@ int32_t fgemm_model_split_tail(const fgemm_device_model_t* dev, int64_t tiles,
 int32_t fgemm_split_work_item(int64_t tiles, int32_t split_tiles, int32_t split_pieces,
                               int32_t clusters, int32_t k_blocks, int32_t cluster,
                               int32_t n, int32_t* out5);
+
+/*
+ * The n-th work item of CTA `cta` of the small-M kernel (tile_m 16/32/64):
+ * the K blocks of all `tiles` 128-column tiles, laid end to end, are cut into
+ * `ctas` equal contiguous shares (stream-K). Writes {unit, k0, k1, piece,
+ * npieces, slot} to out6 and returns 1, or returns 0 past the end of the
+ * share (or on invalid arguments; ctas must not exceed tiles * k_blocks).
+ * `slot` is the partial slot (0 .. 2 ctas - 1) the piece stores to when the
+ * tile has more than one piece. Host-only; the kernel runs the same code.
+ */
+int32_t fgemm_stream_k_work_item(int64_t tiles, int32_t k_blocks, int32_t ctas, int32_t cta,
+                                 int32_t n, int64_t* out6);
 
 /*
  * K-split mode of the handle's classical CTA-pair launches: 0 never, 1 auto

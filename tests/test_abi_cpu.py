@@ -225,7 +225,8 @@ def test_model_plan_small_shapes_stay_classical(L):
         assert L.fgemm_model_plan(ctypes.byref(m), M, N, K, 0, ctypes.byref(a), ctypes.byref(tm),
                                   ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
         assert fgemm.ALGO_NAMES[a.value] == "classical"
-        assert tm.value in (128, 256) and tn.value in (64, 128, 256)
+        assert tm.value in (16, 32, 64, 128, 256) and tn.value in (64, 128, 256)
+        assert tm.value >= 128 or M <= tm.value   # the small-M tiles only where M fits
 
 
 def test_model_pair_tiles_fix_wave_quantization(L):
@@ -314,6 +315,7 @@ def test_model_split_removes_the_pair_sawtooth(L):
     # 77 pair tiles on 76 pairs: whole waves cost two tile times; split, the
     # one extra tile runs as 4 pieces on 4 pairs: 1 + 1/4 tile times
     m = _model(L)
+    m.hbm_gbs = 1e9  # compute-bound: the sawtooth is in the compute term
     _, t76 = _predict(L, m, 256 * 76, 256, 8192, "classical", 256, tile_m=256)
     _, t77 = _predict(L, m, 256 * 77, 256, 8192, "classical", 256, tile_m=256)
     t_tile = t76 - m.launch_us
@@ -344,3 +346,75 @@ def test_winograd_legality_and_model(L):
     _, ts = _predict(L, m, 16384, 16384, 16384, "strassen1", 256)
     _, tw = _predict(L, m, 16384, 16384, 16384, "winograd1", 256)
     assert tw >= ts
+
+
+# ------------------------------------------------------- small-M stream-K
+
+@pytest.mark.parametrize("tiles,kb,ctas", [
+    (128, 256, 152),   # 16 x 16384 x 16384: 128 column tiles, K = 16384
+    (16, 32, 152),     # 16 x 2048 x 2048
+    (64, 128, 152),    # 16 x 8192 x 8192
+    (1, 1, 1),
+    (3, 5, 7),         # fewer iterations per CTA than one tile
+    (200, 3, 152),     # more tiles than CTAs, short K
+    (1, 400, 152),     # one tile over every CTA
+])
+def test_stream_k_schedule_covers_and_slots_are_unique(L, tiles, kb, ctas):
+    ctas = min(ctas, tiles * kb)
+    seen = {}
+    slots = {}
+    counters = {}
+    per_cta = []
+    for c in range(ctas):
+        items = fgemm.stream_k_work_items(tiles, kb, ctas, c)
+        per_cta.append(sum(k1 - k0 for (_, k0, k1, _, _, _) in items))
+        for n, (unit, k0, k1, piece, npieces, slot) in enumerate(items):
+            assert 0 <= unit < tiles and 0 <= k0 < k1 <= kb
+            for k in range(k0, k1):
+                assert (unit, k) not in seen
+                seen[(unit, k)] = (c, piece, npieces)
+            if npieces == 1:
+                assert (k0, k1) == (0, kb)
+                continue
+            # only a CTA's first and last items are pieces of a shared tile
+            assert n == 0 or n == len(items) - 1
+            assert 0 <= slot < 2 * ctas and slot // 2 == c
+            assert slot not in slots, "two pieces share a partial slot"
+            slots[slot] = (unit, piece)
+            if piece == 0:
+                assert unit not in counters
+                counters[unit] = slot
+    assert len(seen) == tiles * kb
+    assert max(per_cta) - min(per_cta) <= 1   # equal shares
+    for t in range(tiles):
+        pieces = [seen[(t, k)][1] for k in range(kb)]
+        assert pieces == sorted(pieces) and pieces[0] == 0
+        n = seen[(t, 0)][2]
+        assert pieces[-1] == n - 1
+        if n > 1:
+            assert t in counters
+
+
+def test_small_m_legality_and_model(L):
+    ep = fgemm.make_epilogue("none")
+    ok = lambda M, N, K, tm, tn, epi=ep: fgemm.validate(M, N, K, 16, K, 16, N, 16, N, fgemm.BF16, epi,
+                                                        "classical", tn, tm)
+    assert ok(16, 4096, 4096, 16, 128) == fgemm.OK
+    assert ok(7, 1000, 520, 16, 128) == fgemm.OK
+    assert ok(17, 4096, 4096, 16, 128) == fgemm.ERR_UNSUPPORTED      # M > tile_m
+    assert ok(16, 4096, 4096, 16, 256) == fgemm.ERR_UNSUPPORTED      # 128-column tiles only
+    assert ok(64, 4096, 4096, 64, 128, fgemm.make_epilogue("swiglu")) == fgemm.ERR_UNSUPPORTED
+    assert fgemm.validate(16, 4096, 4096, 16, 4096, 16, 4096, 16, 4096, fgemm.BF16, ep,
+                          "strassen1", 128, 16) == fgemm.ERR_UNSUPPORTED
+    m = _model(L)
+    # 16 x 16384 x 16384 streams 512 MiB of B: the small-M form predicts the
+    # HBM time, well under the 128-row tiles' prediction
+    _, t_small = _predict(L, m, 16, 16384, 16384, "classical", 128, tile_m=16)
+    _, t_wide = _predict(L, m, 16, 16384, 16384, "classical", 64, tile_m=128)
+    hbm_us = 2.0 * 16384 * 16384 / (m.hbm_gbs * 1e3 * m.hbm_stream_eff)
+    assert hbm_us <= t_small <= hbm_us + m.launch_us + 1.0
+    assert t_small < t_wide
+    a, tm, tn, us = ctypes.c_int(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+    assert L.fgemm_model_plan(ctypes.byref(m), 16, 16384, 16384, 0, ctypes.byref(a), ctypes.byref(tm),
+                              ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
+    assert (fgemm.ALGO_NAMES[a.value], tm.value, tn.value) == ("classical", 16, 128)

@@ -17,7 +17,7 @@ def _picked(M, N, K, epi):
     return fgemm.plan(M, N, K, epilogue=epi)[0]
 
 
-def _sampled_check(name, A, B, bias, run_algo, epi, dtype, tile=0):
+def _sampled_check(name, A, B, bias, run_algo, epi, dtype, tile=0, tile_m=0):
     """Runs `run_algo` and checks 4096 sampled entries against the oracle
     with the tolerance of the form that actually ran."""
     M, K = A.shape
@@ -25,7 +25,7 @@ def _sampled_check(name, A, B, bias, run_algo, epi, dtype, tile=0):
     n_out = N // 2 if epi == "swiglu" else N
     algo = _picked(M, N, K, epi) if run_algo == "auto" else run_algo
     depth_blocks = {"classical": 1, "strassen1": 2, "strassen2": 4, "winograd1": 2}[algo]
-    C = run(A, B, algo=run_algo, epilogue=epi, bias=bias, tile_n=tile)
+    C = run(A, B, algo=run_algo, epilogue=epi, bias=bias, tile_n=tile, tile_m=tile_m)
     # Strassen forms sit within a few percent of their normwise budgets (the
     # rounded operand sums alone give 4.7e-3 and 9.7e-3 on these inputs), so
     # they get 8x more samples: the sampled estimate's relative noise drops
@@ -81,8 +81,12 @@ def test_square_16384(algo):
 def test_sweep_shapes_every_legal_form(shape):
     M, N, K = shape
     A, B = inputs.sweep_inputs(M, N, K, DEV)
-    for algo in ("classical", "strassen1", "strassen2", "auto"):
+    for algo in ("classical", "strassen1", "strassen2", "winograd1", "auto"):
         s = fgemm.validate(M, N, K, 16, K, 16, N, 16, N, fgemm.BF16, None, algo)
         if s == fgemm.ERR_UNSUPPORTED:
             continue
         _sampled_check(f"sweep {shape}", A, B, None, algo, "none", "bf16")
+    for tm in (16, 32, 64):  # the small-M kernel, where M fits
+        if M <= tm:
+            _sampled_check(f"sweep {shape} small-M {tm}", A, B, None, "classical", "none", "bf16",
+                           tile=128, tile_m=tm)

@@ -216,9 +216,15 @@ def test_rejections_do_not_launch():
 def test_plan_is_legal_and_launchable():
     for (M, N, K) in [(256, 256, 256), (4096, 4096, 4096), (16, 2048, 2048), (16384, 16384, 16384)]:
         algo, tile_m, tile, us = fgemm.plan(M, N, K)
-        assert algo in ("classical", "strassen1", "strassen2") and tile in (64, 128, 256)
-        assert tile_m in (128, 256)
+        assert algo in ("classical", "strassen1", "strassen2", "winograd1") and tile in (64, 128, 256)
+        assert tile_m in (128, 256) or (tile_m in (16, 32, 64) and M <= tile_m and tile == 128)
         assert us > 0
+        A = inputs.matrix(M, K, "ternary", "bf16", 32, DEV)
+        B = inputs.matrix(K, N, "ternary", "bf16", 33, DEV)
+        if M * N * K <= 2 ** 33:  # launch what the plan chose
+            C = run(A, B, algo=algo, tile_n=tile, tile_m=tile_m)
+            ref = A.float() @ B.float()
+            assert torch.equal(C.float(), ref.to(torch.bfloat16).float())
 
 
 def test_host_buffers_end_to_end():
@@ -324,3 +330,82 @@ def test_split_every_entry_and_deterministic(epilogue, alpha, tile, split_mode):
              tile_m=256)
     d = values(C1) - values(C0)
     assert np.linalg.norm(d) <= 1e-3 * max(np.linalg.norm(values(C0)), 1e-30)
+
+
+# --------------------------------------------- small-M kernel (C^T = B^T A^T)
+
+SMALL_M_CASES = [
+    # (M, N, K, tile_m)
+    (1, 8, 64, 16),          # one row, one ragged column tile
+    (16, 4096, 4096, 16),    # 32 tiles x 64 K blocks over every SM
+    (7, 1000, 520, 16),      # ragged M, N, K
+    (32, 520, 64, 32),       # one K block: whole tiles only
+    (33, 2048, 1032, 64),
+    (64, 4096, 8192, 64),
+    (16, 16384, 256, 16),    # more tiles than SMs
+    (16, 128, 32768, 16),    # one tile shared by 64 CTAs (64 pieces)
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K,tm", SMALL_M_CASES)
+def test_exact_ternary_small_m(M, N, K, tm, dtype):
+    A, B, bias = _ternary(M, N, K, dtype, seed=50)
+    C = run(A, B, algo="classical", epilogue="scale_bias", bias=bias, tile_n=128, tile_m=tm)
+    assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
+
+
+@pytest.mark.parametrize("tm", [16, 32, 64])
+@pytest.mark.parametrize("epilogue,alpha", [("none", 1.0), ("scale_bias", 0.5), ("silu", 1.25)])
+def test_small_m_every_entry_and_deterministic(tm, epilogue, alpha):
+    M, N, K = tm - 3, 1536, 3080  # ragged M, N and K; 12 tiles shared over the SMs
+    A = inputs.matrix(M, K, "normal", "bf16", 60, DEV)
+    B = inputs.matrix(K, N, "normal_inv_k", "bf16", 61, DEV, k=K)
+    bias = inputs.matrix(1, N, "normal_0.02", "bf16", 62, DEV)[0]
+    _full_check(A, B, "classical", "bf16", epilogue=epilogue, alpha=alpha, bias=bias, tile=128,
+                tile_m=tm)
+    C1 = run(A, B, algo="classical", epilogue=epilogue, alpha=alpha, bias=bias, tile_n=128, tile_m=tm)
+    C2 = run(A, B, algo="classical", epilogue=epilogue, alpha=alpha, bias=bias, tile_n=128, tile_m=tm)
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
+def test_small_m_strided_and_guard_band():
+    """lda/ldb/ldc beyond the row length; rows past M and C's padding untouched."""
+    M, N, K = 12, 300, 200
+    A0, B0, bias = _ternary(M, N, K, "bf16", seed=70)
+    A = torch.zeros((M, K + 40), dtype=torch.bfloat16, device=DEV)[:, :K]
+    A.copy_(A0)
+    B = torch.zeros((K, N + 20), dtype=torch.bfloat16, device=DEV)[:, :N]
+    B.copy_(B0)
+    canary = 0x7F7B
+    big = torch.full((M + 2, N + 28), canary, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    C = big[1:M + 1, :N]
+    run(A, B, epilogue="scale_bias", bias=bias, out=C, tile_n=128, tile_m=16)
+    assert np.array_equal(gpu_bits(C), _exact_reference(A0, B0, bias, "bf16"))
+    raw = big.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (raw[0] == canary).all() and (raw[M + 1] == canary).all()
+    assert (raw[1:M + 1, N:] == canary).all()
+
+
+@pytest.mark.parametrize("M,N,K,tm,tn", [(4096, 4096, 512, 256, 256),   # CTA pairs, split last wave
+                                         (16, 4096, 4096, 16, 128),     # small-M stream-K
+                                         (2560, 2048, 512, 256, 256)])  # 80 tiles: 4 split in 4
+def test_graph_replays_recount_split_pieces(M, N, K, tm, tn, split_mode):
+    """A CUDA graph replays the same launch parameters; the pieces' arrival
+    counters must start from zero on every replay, or tiles go unwritten."""
+    split_mode("force")
+    A, B, bias = _ternary(M, N, K, "bf16", seed=80)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    kw = dict(out=C, epilogue="scale_bias", bias=bias, algo="classical", tile_n=tn, tile_m=tm)
+    fgemm.matmul(A, B, **kw)  # allocations and launch set-up happen outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fgemm.matmul(A, B, **kw)
+    ref = _exact_reference(A, B, bias, "bf16")
+    for _ in range(3):
+        C.view(torch.int16).fill_(0x7F7B)  # a NaN pattern the kernel never writes
+        g.replay()
+        torch.cuda.synchronize()
+        assert fgemm.default_handle().get_error() == fgemm.OK
+        assert np.array_equal(gpu_bits(C), ref)
