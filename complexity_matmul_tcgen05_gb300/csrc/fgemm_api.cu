@@ -604,6 +604,8 @@ fgemm_status_t load_calibration(fgemm_handle_t h, const char* path) {
       {"tile_fill_us", &m.tile_fill_us},        {"l2_bytes", &m.l2_bytes},
       {"l2_gbs", &m.l2_gbs},                    {"split_fix_us", &m.split_fix_us},
       {"eff_winograd1_128", &m.eff_winograd[0]}, {"eff_winograd1_256", &m.eff_winograd[1]},
+      {"hbm_stream_eff", &m.hbm_stream_eff},     {"small_m_stream_eff", &m.small_m_stream_eff},
+      {"small_m_fix_us", &m.small_m_fix_us},
   };
   int found = 0;
   for (auto& fd : fields) found += json_number(text, fd.key, fd.dst) ? 1 : 0;

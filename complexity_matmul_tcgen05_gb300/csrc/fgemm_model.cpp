@@ -106,6 +106,8 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   m.eff_small_m[1] = 0.11;    // tile_m 32
   m.eff_small_m[2] = 0.22;    // tile_m 64
   m.hbm_stream_eff = 0.9;
+  m.small_m_stream_eff = 0.75;  // 16 x 16384^2: 537 MB in ~101-106 us inside the kernel
+  m.small_m_fix_us = 4.0;
   *out = m;
 }
 
@@ -149,8 +151,10 @@ int32_t fgemm_model_split_tail(const fgemm_device_model_t* dev, int64_t tiles, i
   if (s < 2) return 0;
   if (mode == 1) {
     // auto: split when the part of a tile time it saves, (1 - 1/S) * t_tile,
-    // outweighs its cost, split_fix_us per other piece each last piece reads
-    if (!dev || dev->num_sms <= 0) return 0;
+    // outweighs its cost, split_fix_us per other piece each last piece reads;
+    // and only with at least one wave of whole tiles, whose MMAs hide the
+    // pieces' partial stores and sums (with none, they are all exposed)
+    if (!dev || dev->num_sms <= 0 || tiles < clusters) return 0;
     const double eff = std::max(dev->eff_pair[tile_n == 128 ? 0 : 1], 1e-3);
     const double pair_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms * 2.0;
     const double t_tile = 2.0 * 256.0 * tile_n * fgemm::kBK * k_blocks / (pair_flop_per_us * eff);
@@ -217,8 +221,9 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
                                 static_cast<double>(M) * N);
     const double sm_share = std::min(1.0, static_cast<double>(ctas) / std::max(1, dev->num_sms));
     const double t_memory =
-        bytes / (dev->hbm_gbs * 1e3 * std::max(dev->hbm_stream_eff, 1e-3) * sm_share);
-    if (predicted_us) *predicted_us = std::max(t_compute, t_memory) + dev->launch_us;
+        bytes / (dev->hbm_gbs * 1e3 * std::max(dev->small_m_stream_eff, 1e-3) * sm_share);
+    if (predicted_us)
+      *predicted_us = std::max(t_compute, t_memory) + dev->small_m_fix_us + dev->launch_us;
     return FGEMM_OK;
   }
   const int d = depth_of(algo);

@@ -49,7 +49,8 @@ class DeviceModel(ctypes.Structure):
                 ("l2_bytes", ctypes.c_double), ("l2_gbs", ctypes.c_double),
                 ("split_fix_us", ctypes.c_double),
                 ("eff_winograd", ctypes.c_double * 2),
-                ("eff_small_m", ctypes.c_double * 3), ("hbm_stream_eff", ctypes.c_double)]
+                ("eff_small_m", ctypes.c_double * 3), ("hbm_stream_eff", ctypes.c_double),
+                ("small_m_stream_eff", ctypes.c_double), ("small_m_fix_us", ctypes.c_double)]
 
 
 _lib = None

@@ -276,6 +276,10 @@ typedef struct {
                             * fraction of peak (an N = tile_m MMA runs at most
                             * tile_m / 256 of the full rate) */
   double hbm_stream_eff;   /* fraction of hbm_gbs a kernel streaming B reaches */
+  double small_m_stream_eff; /* the same for the small-M kernel, whose CTAs read
+                              * B at different K (less DRAM page locality) */
+  double small_m_fix_us;   /* its per-launch cost beyond the stream: the pieces'
+                            * partial store, count and sum, and the slowest CTA */
 } fgemm_device_model_t;
 
 /* Default model for a device with the given SM count, peak and bandwidth. */
@@ -328,9 +332,9 @@ fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M,
  * (deterministic) and applies the epilogue.
  *
  * fgemm_model_split_tail returns R (0 = no split) and writes S to *pieces
- * (1 when no split; pieces may be NULL). mode 0: never; 1 (auto): when
- * (1 - 1/S) * tile time > (S - 1) * dev->split_fix_us; 2: whenever the
- * conditions above allow. Requires 2 <= clusters <= 255; dev may be NULL for
+ * (1 when no split; pieces may be NULL). mode 0: never; 1 (auto): when at
+ * least one whole wave remains (tiles >= clusters) and (1 - 1/S) * tile time
+ * > (S - 1) * dev->split_fix_us; 2: whenever the conditions above allow. Requires 2 <= clusters <= 255; dev may be NULL for
  * modes 0 and 2.
  */
 int32_t fgemm_model_split_tail(const fgemm_device_model_t* dev, int64_t tiles,

@@ -407,14 +407,14 @@ def test_small_m_legality_and_model(L):
     assert fgemm.validate(16, 4096, 4096, 16, 4096, 16, 4096, 16, 4096, fgemm.BF16, ep,
                           "strassen1", 128, 16) == fgemm.ERR_UNSUPPORTED
     m = _model(L)
-    # 16 x 16384 x 16384 streams 512 MiB of B: the small-M form predicts the
-    # HBM time, well under the 128-row tiles' prediction
+    # 16 x 16384 x 16384 streams 512 MiB of B: the small-M form predicts that
+    # stream at its own efficiency, plus its fixed cost and the launch
     _, t_small = _predict(L, m, 16, 16384, 16384, "classical", 128, tile_m=16)
-    _, t_wide = _predict(L, m, 16, 16384, 16384, "classical", 64, tile_m=128)
-    hbm_us = 2.0 * 16384 * 16384 / (m.hbm_gbs * 1e3 * m.hbm_stream_eff)
-    assert hbm_us <= t_small <= hbm_us + m.launch_us + 1.0
+    b = 2.0 * (16 * 16384 + 16384 * 16384 + 16 * 16384)
+    stream_us = b / (m.hbm_gbs * 1e3 * m.small_m_stream_eff)
+    assert abs(t_small - (stream_us + m.small_m_fix_us + m.launch_us)) < 1e-6 * t_small
+    # 16 x 8192 x 8192 as 128 x 64 tiles keeps 128 of 152 SMs streaming: the
+    # small-M form, on every SM, predicts less
+    _, t_small = _predict(L, m, 16, 8192, 8192, "classical", 128, tile_m=16)
+    _, t_wide = _predict(L, m, 16, 8192, 8192, "classical", 64, tile_m=128)
     assert t_small < t_wide
-    a, tm, tn, us = ctypes.c_int(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
-    assert L.fgemm_model_plan(ctypes.byref(m), 16, 16384, 16384, 0, ctypes.byref(a), ctypes.byref(tm),
-                              ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
-    assert (fgemm.ALGO_NAMES[a.value], tm.value, tn.value) == ("classical", 16, 128)
