@@ -74,6 +74,9 @@ def _load():
         lib.oracle_winograd_emulated.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, i64, dp,
                                                  i64, dp, i64, dp, i64]
         lib.oracle_winograd_emulated.restype = ctypes.c_int
+        lib.oracle_rmsnorm.argtypes = [i64, i64, dp, i64, dp, ctypes.c_double, dp, i64]
+        lib.oracle_block_sumsq.argtypes = [i64, i64, dp, i64, dp]
+        lib.oracle_row_scale.argtypes = [i64, i64, dp, ctypes.c_double, ctypes.c_double, dp]
         lib.oracle_silu.argtypes = [ctypes.c_double]
         lib.oracle_silu.restype = ctypes.c_double
         _lib = lib
@@ -171,6 +174,39 @@ def epilogue(acc: np.ndarray, kind: str = "none", alpha: float = 1.0,
                             None if b is None else _ptr(b, ctypes.c_double),
                             _ptr(out, ctypes.c_double), Nout)
     return out
+
+
+def rmsnorm(x: np.ndarray, g: np.ndarray | None = None, eps: float = 1e-6) -> np.ndarray:
+    """RMSNorm of every row: x_ij * g_j / sqrt(mean_j x_ij^2 + eps)."""
+    x = _f64(x)
+    M, N = x.shape
+    y = np.empty((M, N), dtype=np.float64)
+    gg = None if g is None else _f64(g)
+    if gg is not None:
+        assert gg.shape == (N,)
+    _load().oracle_rmsnorm(M, N, _ptr(x, ctypes.c_double), N,
+                           None if gg is None else _ptr(gg, ctypes.c_double), float(eps),
+                           _ptr(y, ctypes.c_double), N)
+    return y
+
+
+def block_sumsq(x: np.ndarray) -> np.ndarray:
+    """[ceil(N/64), M]: per row, the sum of squares of each block of 64 columns."""
+    x = _f64(x)
+    M, N = x.shape
+    out = np.empty(((N + 63) // 64, M), dtype=np.float64)
+    _load().oracle_block_sumsq(M, N, _ptr(x, ctypes.c_double), N, _ptr(out, ctypes.c_double))
+    return out
+
+
+def row_scale(sumsq: np.ndarray, n: int, eps: float) -> np.ndarray:
+    """r_i = 1 / sqrt(sum_p sumsq[p, i] / n + eps) for a [parts, M] array."""
+    s = _f64(sumsq)
+    parts, M = s.shape
+    r = np.empty(M, dtype=np.float64)
+    _load().oracle_row_scale(M, parts, _ptr(s, ctypes.c_double), float(n), float(eps),
+                             _ptr(r, ctypes.c_double))
+    return r
 
 
 def silu(v: float) -> float:

@@ -40,6 +40,16 @@
  *    applied recursively `depth` times, classical at the leaves.  In exact
  *    arithmetic it equals the classical product.
  *
+ *  - RMSNorm statistics carried by the epilogue (PingPong GEMM / CODA note,
+ *    CODA section: the epilogue also produces what the following
+ *    normalisation needs).  RMSNorm of a row x of width n with gain g:
+ *        y_j = x_j * g_j / sqrt(mean_j(x_j^2) + eps)
+ *    The producing GEMM emits, per row and per block of 64 output columns,
+ *    the sum of squares of its (rounded) outputs; the consuming GEMM forms
+ *        r_i = 1 / sqrt(sum over blocks / n + eps)
+ *    and since  y W = diag(r) x diag(g) W,  it multiplies its accumulator
+ *    row i by r_i, with g folded into its weights once.
+ *
  *  - Winograd's variant of Strassen (named beside Strassen among the
  *    Strassen-like LCMAs of the FalconGEMM summary, "Methodology" item 1; the
  *    pages print no formulas, so the oracle uses the standard variant).  It
@@ -240,6 +250,45 @@ void oracle_epilogue(int kind, int64_t M, int64_t N, const double* acc,
       }
       out[i * ldo + j] = o;
     }
+  }
+}
+
+/* ------------------------------------------------------- RMSNorm pieces */
+
+/* y = RMSNorm(x) row by row: y_ij = x_ij * g_j / sqrt(mean_j x_ij^2 + eps)
+ * (g may be NULL: all ones). */
+void oracle_rmsnorm(int64_t M, int64_t N, const double* x, int64_t ldx,
+                    const double* g, double eps, double* y, int64_t ldy) {
+  for (int64_t i = 0; i < M; ++i) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < N; ++j) ss += x[i * ldx + j] * x[i * ldx + j];
+    const double r = 1.0 / sqrt(ss / (double)N + eps);
+    for (int64_t j = 0; j < N; ++j)
+      y[i * ldy + j] = x[i * ldx + j] * r * (g ? g[j] : 1.0);
+  }
+}
+
+/* Per row i and block p of 64 columns: out[p * M + i] = sum of x_ij^2 over
+ * the block's columns j < N (the last block may be partial). */
+void oracle_block_sumsq(int64_t M, int64_t N, const double* x, int64_t ldx,
+                        double* out) {
+  const int64_t parts = (N + 63) / 64;
+  for (int64_t p = 0; p < parts; ++p)
+    for (int64_t i = 0; i < M; ++i) {
+      double ss = 0.0;
+      for (int64_t j = p * 64; j < N && j < (p + 1) * 64; ++j)
+        ss += x[i * ldx + j] * x[i * ldx + j];
+      out[p * M + i] = ss;
+    }
+}
+
+/* r_i = 1 / sqrt(sum_p sumsq[p * M + i] / n + eps). */
+void oracle_row_scale(int64_t M, int64_t parts, const double* sumsq, double n,
+                      double eps, double* r) {
+  for (int64_t i = 0; i < M; ++i) {
+    double ss = 0.0;
+    for (int64_t p = 0; p < parts; ++p) ss += sumsq[p * M + i];
+    r[i] = 1.0 / sqrt(ss / n + eps);
   }
 }
 

@@ -367,6 +367,50 @@ def test_winograd_emulated_rounding_error_is_in_the_expected_band(dtype, depth, 
     assert lo < rel < hi, rel
 
 
+# ------------------------------------------------------------------ RMSNorm
+
+def test_rmsnorm_matches_torch():
+    rng = np.random.default_rng(31)
+    x = rng.normal(0, 3, (7, 300))
+    g = rng.uniform(0.5, 1.5, 300)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (300,), torch.from_numpy(g), eps=1e-5)
+    assert np.allclose(oracle.rmsnorm(x, g, 1e-5), ref.numpy(), rtol=1e-13, atol=0)
+
+
+def test_rmsnorm_closed_forms_and_invariance():
+    # a constant row c: mean(x^2) = c^2, so y = c / sqrt(c^2 + eps)
+    x = np.full((3, 64), 2.5)
+    assert np.allclose(oracle.rmsnorm(x, None, 0.25), 2.5 / np.sqrt(6.25 + 0.25), rtol=1e-15)
+    # scaling a row by s leaves it unchanged when eps = 0; a row of +-1 is fixed
+    rng = np.random.default_rng(32)
+    x = rng.normal(size=(5, 96))
+    assert np.allclose(oracle.rmsnorm(7.0 * x, None, 0.0), oracle.rmsnorm(x, None, 0.0), rtol=1e-13)
+    pm = np.where(rng.normal(size=(4, 128)) > 0, 1.0, -1.0)
+    assert np.array_equal(oracle.rmsnorm(pm, None, 0.0), pm)
+
+
+def test_block_sumsq_and_row_scale():
+    x = np.arange(1.0, 1 + 3 * 130).reshape(3, 130)   # last block has 2 columns
+    s = oracle.block_sumsq(x)
+    assert s.shape == (3, 3)
+    for p, (a, b) in enumerate([(0, 64), (64, 128), (128, 130)]):
+        assert np.array_equal(s[p], (x[:, a:b] ** 2).sum(axis=1))
+    r = oracle.row_scale(s, 130, 1e-3)
+    assert np.allclose(r, 1 / np.sqrt((x ** 2).mean(axis=1) + 1e-3), rtol=1e-15)
+
+
+def test_rms_scale_folded_into_the_next_product():
+    # RMSNorm(x) W == diag(r) x (diag(g) W): what the consumer's epilogue uses
+    rng = np.random.default_rng(33)
+    x = rng.normal(size=(6, 192))
+    g = rng.uniform(0.5, 1.5, 192)
+    W = rng.normal(size=(192, 40))
+    r = oracle.row_scale(oracle.block_sumsq(x), 192, 1e-6)
+    lhs = oracle.gemm(oracle.rmsnorm(x, g, 1e-6), W)
+    rhs = r[:, None] * oracle.gemm(x, g[:, None] * W)
+    assert np.allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
+
+
 # ------------------------------------------------------------ sampled path
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
