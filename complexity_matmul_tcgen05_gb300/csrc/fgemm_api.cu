@@ -260,9 +260,10 @@ struct TmapKeyHash {
 struct PlanKey {
   int64_t M, N, K;
   int32_t epi, algo, tile_m, tile_n;
+  int32_t wide_classical;  // plans restricted to classical 128/256-row tiles
   bool operator==(const PlanKey& o) const {
     return M == o.M && N == o.N && K == o.K && epi == o.epi && algo == o.algo &&
-           tile_m == o.tile_m && tile_n == o.tile_n;
+           tile_m == o.tile_m && tile_n == o.tile_n && wide_classical == o.wide_classical;
   }
 };
 struct PlanKeyHash {
@@ -270,7 +271,8 @@ struct PlanKeyHash {
     size_t h = std::hash<int64_t>()(k.M);
     h = h * 1000003u ^ std::hash<int64_t>()(k.N);
     h = h * 1000003u ^ std::hash<int64_t>()(k.K);
-    h = h * 1000003u ^ static_cast<size_t>(k.epi * 512 + k.algo * 64 + (k.tile_m >> 4) + (k.tile_n >> 6));
+    h = h * 1000003u ^ static_cast<size_t>(k.epi * 512 + k.algo * 64 + (k.tile_m >> 4) + (k.tile_n >> 6) +
+                                           k.wide_classical * 4096);
     return h;
   }
 };
@@ -417,8 +419,9 @@ fgemm_status_t validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
 }
 
 fgemm_status_t choose_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, int32_t kind,
-                           fgemm_algo_t algo, int32_t tile_m, int32_t tile_n, Plan* out) {
-  PlanKey key{M, N, K, kind, static_cast<int32_t>(algo), tile_m, tile_n};
+                           fgemm_algo_t algo, int32_t tile_m, int32_t tile_n, Plan* out,
+                           bool wide_classical = false) {
+  PlanKey key{M, N, K, kind, static_cast<int32_t>(algo), tile_m, tile_n, wide_classical ? 1 : 0};
   auto it = h->plans.find(key);
   if (it != h->plans.end()) {
     *out = it->second;
@@ -427,8 +430,10 @@ fgemm_status_t choose_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, in
   Plan p{FGEMM_ALGO_CLASSICAL, 0, 0, INFINITY};
   for (fgemm_algo_t a : kForms) {
     if (algo != FGEMM_ALGO_AUTO && a != algo) continue;
+    if (wide_classical && a != FGEMM_ALGO_CLASSICAL) continue;
     for (int32_t tm : {16, 32, 64, 128, 256}) {
       if (tile_m != 0 && tm != tile_m) continue;
+      if (wide_classical && tm < 128) continue;
       for (int32_t tn : {64, 128, 256}) {
         if (tile_n != 0 && tn != tile_n) continue;
         double us;
@@ -756,14 +761,16 @@ fgemm_status_t fgemm_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, fge
   return FGEMM_OK;
 }
 
-fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
-                               int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
-                               fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
-                               int32_t tile_m, int32_t tile_n) {
-  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+namespace {
+
+fgemm_status_t matmul_impl(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                           int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                           fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                           int32_t tile_m, int32_t tile_n, const fgemm_rms_t* rms) {
   fgemm_status_t s =
       validate(M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_m, tile_n, &h->msg);
   if (s != FGEMM_OK) return s;
+  const bool with_rms = rms && (rms->sumsq_out || rms->sumsq_in);
   const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
   const int64_t n_out = kind == FGEMM_EPI_SWIGLU ? N / 2 : N;
   if (M == 0 || n_out == 0) return FGEMM_OK;
@@ -786,14 +793,23 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
   p.epi = kind;
   p.is_bf16 = dtype == FGEMM_BF16 ? 1 : 0;
   p.alpha = epi ? epi->alpha : 1.0f;
+  if (with_rms) {
+    p.sumsq_out = rms->sumsq_out;
+    p.sumsq_in = rms->sumsq_in;
+    p.sumsq_parts = rms->sumsq_in ? rms->sumsq_parts : 0;
+    p.rms_inv_n = rms->sumsq_in ? static_cast<float>(1.0 / static_cast<double>(rms->norm_width)) : 0.0f;
+    p.rms_eps = rms->eps;
+  }
 
   if (K == 0) {
+    if (with_rms) return set_msg(h, FGEMM_ERR_UNSUPPORTED, "RMSNorm statistics need K >= 1");
     cudaError_t e = fgemm::launch_k0_fill(p, h->stream);
     return e == cudaSuccess ? FGEMM_OK : cuda_fail(h, e, "K == 0 fill launch");
   }
 
   Plan plan;
-  s = choose_plan(h, M, N, K, kind, algo, tile_m, tile_n, &plan);
+  s = choose_plan(h, M, N, K, kind, with_rms ? FGEMM_ALGO_CLASSICAL : algo, tile_m, tile_n, &plan,
+                  with_rms);
   if (s != FGEMM_OK) return s;
   const int d = depth_of(plan.algo);
   const int bn = plan.tile_n;
@@ -843,8 +859,9 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
     const int fit = fgemm::gemm_pair_clusters_fit(bn);
     if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the CTA-pair launch");
     int32_t pieces = 1;
-    const int split =
-        fgemm_model_split_tail(&h->model, units, fit, p.k_blocks, bn, h->split_mode, &pieces);
+    const int split = with_rms ? 0
+                               : fgemm_model_split_tail(&h->model, units, fit, p.k_blocks, bn,
+                                                        h->split_mode, &pieces);
     int clusters = static_cast<int>(std::min<long long>(fit, units));
     if (split > 0) {
       clusters = fit;  // the schedule is planned for every pair that fits
@@ -866,6 +883,37 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
                        : fgemm::launch_gemm(bn, d, p, grid, h->stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "GEMM kernel launch");
   return FGEMM_OK;
+}
+
+}  // namespace
+
+fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                               int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                               fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                               int32_t tile_m, int32_t tile_n) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  return matmul_impl(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_m, tile_n, nullptr);
+}
+
+fgemm_status_t fgemm_matmul_rms(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                                int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                                fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                                int32_t tile_m, int32_t tile_n, const fgemm_rms_t* rms) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  if (rms && (rms->sumsq_out || rms->sumsq_in)) {
+    if (algo != FGEMM_ALGO_AUTO && algo != FGEMM_ALGO_CLASSICAL)
+      return set_msg(h, FGEMM_ERR_UNSUPPORTED, "RMSNorm statistics: classical form only");
+    if (tile_m != 0 && tile_m != 128 && tile_m != 256)
+      return set_msg(h, FGEMM_ERR_UNSUPPORTED, "RMSNorm statistics: tile_m 128 or 256 only");
+    if ((reinterpret_cast<uintptr_t>(rms->sumsq_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(rms->sumsq_in) & 3u))
+      return set_msg(h, FGEMM_ERR_ALIGNMENT, "sumsq buffers must be 4-byte aligned");
+    if (rms->sumsq_in && (rms->sumsq_parts < 1 || rms->norm_width < 1 || !(rms->eps >= 0.0f) ||
+                          !std::isfinite(rms->eps)))
+      return set_msg(h, FGEMM_ERR_INVALID_ARG,
+                     "sumsq_in needs sumsq_parts >= 1, norm_width >= 1 and a finite eps >= 0");
+  }
+  return matmul_impl(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_m, tile_n, rms);
 }
 
 fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,

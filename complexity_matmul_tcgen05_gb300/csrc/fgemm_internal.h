@@ -172,6 +172,12 @@ struct KernelParams {
   unsigned int split_gen;   // launch generation tagging the counters, 1 .. 2^24 - 1
   unsigned int* split_ctr;  // per (split tile, CTA rank, epilogue warp): gen << 8 | arrivals
   float* split_ws;          // per (split tile, piece, CTA rank): 128 x BN fp32, [col/4][row][4]
+  // RMSNorm statistics (classical one-CTA and CTA-pair kernels, no K split)
+  float* sumsq_out;         // [ceil(n_out / 64)][M]: sums of squares of stored outputs, or null
+  const float* sumsq_in;    // [sumsq_parts][M] from an earlier product, or null
+  int sumsq_parts;
+  float rms_inv_n;          // 1 / width of the normalised rows
+  float rms_eps;
 };
 
 // Error word layout written by a kernel whose bounded wait ran out.

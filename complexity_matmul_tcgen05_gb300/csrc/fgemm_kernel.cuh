@@ -157,6 +157,20 @@ __device__ __forceinline__ uint16_t pack1(float v, int is_bf16) {
 
 __device__ __forceinline__ float silu(float v) { return v / (1.0f + __expf(-v)); }
 
+// The value a float becomes when stored in the output type.
+__device__ __forceinline__ float round_out(float v, int is_bf16) {
+  return h2f(pack1(v, is_bf16), is_bf16);
+}
+
+// RMSNorm row scale from an earlier product's block sums of squares:
+// 1 / sqrt(sum_p sumsq_in[p][row] / n + eps), summed in block order.
+__device__ __forceinline__ float rms_row_scale(const KernelParams& p, int row) {
+  float ss = 0.0f;
+#pragma unroll 4
+  for (int q = 0; q < p.sumsq_parts; ++q) ss += __ldg(p.sumsq_in + static_cast<size_t>(q) * p.M + row);
+  return 1.0f / sqrtf(ss * p.rms_inv_n + p.rms_eps);
+}
+
 __device__ __forceinline__ float ld_bias(const KernelParams& p, int col) {
   return h2f(__ldg(p.bias + col), p.is_bf16);
 }
@@ -238,13 +252,33 @@ __device__ __forceinline__ void finish_swiglu_warp(const KernelParams& p, int co
 // chunk, kept as raw 16-bit values and converted when used, so no wait on
 // them precedes the first TMEM load; broadcast by shuffles), and for the
 // plain epilogues the TMEM load of the next chunk is in flight while the
-// current one is finished and stored.
+// current one is finished and stored.  RMSNorm statistics (CODA section of
+// the PingPong GEMM / CODA note): with p.sumsq_in the accumulator row is first
+// scaled by 1 / sqrt(mean of squares + eps) of an earlier product's row; with
+// p.sumsq_out the sums of squares of the stored values of each 64-column
+// block are written out, in column order within the block.
 template <int BN>
 __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32_t tbase, int row0,
                                                    int tn, int r) {
   const int lane = threadIdx.x & 31;
   const int row = row0 + r;
   const bool row_ok = row < p.M;
+  // RMSNorm: the scale of this row (1 without statistics in), and the
+  // running sum of squares of the stored outputs of one 64-column block
+  const float rs = (p.sumsq_in && row_ok) ? rms_row_scale(p, row) : 1.0f;
+  float ss = 0.0f;
+  auto add_sumsq = [&](int c, int col0, const float (&v)[32]) {
+    if (!p.sumsq_out) return;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float q = round_out(v[j], p.is_bf16);
+      if (col0 + j < p.n_out) ss += q * q;
+    }
+    if ((c & 1) && row_ok && col0 - 32 < p.n_out) {  // end of the block [col0 - 32, col0 + 32)
+      p.sumsq_out[static_cast<size_t>((col0 - 32) >> 6) * p.M + row] = ss;
+      ss = 0.0f;
+    }
+  };
   if (p.epi == kEpiSwiglu) {
     constexpr int HALF = BN / 2;
     constexpr int CH = HALF / 32;
@@ -267,11 +301,12 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
       float g[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float gv = p.alpha * __uint_as_float(gr[j]) + __shfl_sync(0xFFFFFFFFu, bg[c], j);
-        const float uv = p.alpha * __uint_as_float(ur[j]) + __shfl_sync(0xFFFFFFFFu, bu[c], j);
+        const float gv = p.alpha * (rs * __uint_as_float(gr[j])) + __shfl_sync(0xFFFFFFFFu, bg[c], j);
+        const float uv = p.alpha * (rs * __uint_as_float(ur[j])) + __shfl_sync(0xFFFFFFFFu, bu[c], j);
         g[j] = silu(gv) * uv;
       }
       if (row_ok && col0 < p.n_out) store_row32(p, row, col0, g);
+      add_sumsq(c, col0, g);
     }
   } else {
     constexpr int CH = BN / 32;
@@ -285,11 +320,12 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float x = p.alpha * __uint_as_float(ar[j]) + __shfl_sync(0xFFFFFFFFu, bf, j);
+        float x = p.alpha * (rs * __uint_as_float(ar[j])) + __shfl_sync(0xFFFFFFFFu, bf, j);
         if (p.epi == kEpiSilu) x = silu(x);
         v[j] = x;
       }
       if (row_ok && col0 < p.n_out) store_row32(p, row, col0, v);
+      add_sumsq(c, col0, v);
     };
     uint32_t ra[32], rb[32];
     ptx::tmem_ld_32x32b_x32(tbase, ra);

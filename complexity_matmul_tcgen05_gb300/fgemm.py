@@ -28,6 +28,12 @@ ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 EPILOGUES = {"none": 0, "scale_bias": 1, "silu": 2, "swiglu": 3}
 
 
+class Rms(ctypes.Structure):
+    _fields_ = [("sumsq_out", ctypes.c_void_p), ("sumsq_in", ctypes.c_void_p),
+                ("sumsq_parts", ctypes.c_int32), ("norm_width", ctypes.c_int64),
+                ("eps", ctypes.c_float)]
+
+
 class FgemmError(RuntimeError):
     def __init__(self, status: int, message: str):
         self.status = status
@@ -76,6 +82,7 @@ def lib() -> ctypes.CDLL:
         mm = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, st, epi_p, st]
         L.fgemm_matmul.argtypes = mm
         L.fgemm_matmul_ex.argtypes = mm + [i32, i32]
+        L.fgemm_matmul_rms.argtypes = mm + [i32, i32, ctypes.POINTER(Rms)]
         L.fgemm_plan.argtypes = [vp, i64, i64, i64, st, epi_p, ctypes.POINTER(st),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(ctypes.c_double)]
@@ -119,7 +126,7 @@ def lib() -> ctypes.CDLL:
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
                      "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout",
-                     "fgemm_set_split_mode"):
+                     "fgemm_set_split_mode", "fgemm_matmul_rms"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -225,6 +232,14 @@ class Handle:
                                      ctypes.byref(epilogue) if epilogue is not None else None,
                                      ALGOS[algo], tile_m, tile_n)
 
+    def matmul_rms_raw(self, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype: int,
+                       epilogue: Epilogue | None, algo: str, tile_n: int, tile_m: int,
+                       rms: Rms) -> int:
+        """fgemm_matmul_rms on raw device pointers; returns the status."""
+        return lib().fgemm_matmul_rms(self._h, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype,
+                                      ctypes.byref(epilogue) if epilogue is not None else None,
+                                      ALGOS[algo], tile_m, tile_n, ctypes.byref(rms))
+
     def plan(self, M, N, K, dtype: int = BF16, epilogue: Epilogue | None = None):
         a = ctypes.c_int()
         tm = ctypes.c_int32()
@@ -276,11 +291,18 @@ def _check_matrix(t: torch.Tensor, name: str):
 def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
            epilogue: str = "none", alpha: float = 1.0, bias: torch.Tensor | None = None,
            algo: str = "auto", tile_n: int = 0, tile_m: int = 0,
-           handle: Handle | None = None) -> torch.Tensor:
+           handle: Handle | None = None, sumsq_out: torch.Tensor | None = None,
+           sumsq_in: torch.Tensor | None = None, norm_width: int = 0,
+           rms_eps: float = 1e-6) -> torch.Tensor:
     """C = epi(alpha * A @ B + bias) through fgemm_matmul_ex.
 
     A is M x K, B is K x N (row-major), bias has N entries; for
     epilogue="swiglu" the output is M x N/2 (gate | up halves of B's columns).
+
+    RMSNorm statistics (fgemm_matmul_rms): ``sumsq_out`` (fp32, shape
+    [ceil(N_out/64), M]) receives each row's sums of squares of the stored
+    outputs per 64-column block; ``sumsq_in`` (fp32 [parts, M], from an earlier
+    call) scales accumulator row i by 1/sqrt(sum / norm_width + rms_eps).
     """
     if A.device.type == "cpu" and B.device.type == "cpu":
         dev = torch.device("cuda", torch.cuda.current_device())
@@ -323,8 +345,25 @@ def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
     lda = A.stride(0) if M > 1 else max(K, 1)
     ldb = B.stride(0) if K > 1 else max(N, 1)
     ldc = out.stride(0) if M > 1 else max(n_out, 1)
-    s = h.matmul_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, dt,
-                     epi, algo, tile_n, tile_m)
+    if sumsq_out is None and sumsq_in is None:
+        s = h.matmul_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, dt,
+                         epi, algo, tile_n, tile_m)
+    else:
+        parts = 0
+        for t, name in ((sumsq_out, "sumsq_out"), (sumsq_in, "sumsq_in")):
+            if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()):
+                raise FgemmError(ERR_INVALID_ARG, f"{name} must be a contiguous CUDA float32 tensor")
+        if sumsq_out is not None and tuple(sumsq_out.shape) != ((n_out + 63) // 64, M):
+            raise FgemmError(ERR_INVALID_ARG, "sumsq_out must have shape [ceil(N_out / 64), M]")
+        if sumsq_in is not None:
+            if sumsq_in.dim() != 2 or sumsq_in.shape[1] != M:
+                raise FgemmError(ERR_INVALID_ARG, "sumsq_in must have shape [parts, M]")
+            parts = sumsq_in.shape[0]
+        rms = Rms(None if sumsq_out is None else sumsq_out.data_ptr(),
+                  None if sumsq_in is None else sumsq_in.data_ptr(), parts, int(norm_width),
+                  float(rms_eps))
+        s = h.matmul_rms_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, dt,
+                             epi, algo, tile_n, tile_m, rms)
     _check(s, h.ptr)
     return out
 

@@ -161,6 +161,48 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N,
                                int32_t tile_n);
 
 /*
+ * RMSNorm statistics carried by the epilogue (PingPong GEMM / CODA note,
+ * CODA section: the epilogue also produces what the following normalisation
+ * needs). RMSNorm of a row x of width n with gain g is
+ *   y_j = x_j g_j / sqrt(mean_j x_j^2 + eps),
+ * and y W = diag(r) x (diag(g) W) with r = 1 / sqrt(mean_j x_j^2 + eps), so
+ * a product can hand the next one its rows' sums of squares and the next one
+ * scales its accumulator rows by r (g folded into its weights by the caller).
+ *   sumsq_out   NULL, or device fp32 [ceil(N_out / 64)][M] (row-major: block
+ *               p's M sums are contiguous): for each row and block of 64
+ *               output columns, the sum of squares of the values as stored in
+ *               C (after rounding), accumulated in column order in fp32.
+ *   sumsq_in    NULL, or device fp32 [sumsq_parts][M] written by an earlier
+ *               call: the accumulator of row i is multiplied by
+ *               r_i = 1 / sqrt(sum_p sumsq_in[p][i] / norm_width + eps)
+ *               (blocks summed in order, fp32) before alpha, bias and the
+ *               activation.
+ *   sumsq_parts blocks in sumsq_in (>= 1 with sumsq_in); norm_width >= 1 the
+ *               normalised width; eps >= 0.
+ * Both pointers 4-byte aligned, else FGEMM_ERR_ALIGNMENT.
+ */
+typedef struct {
+  float* sumsq_out;
+  const float* sumsq_in;
+  int32_t sumsq_parts;
+  int64_t norm_width;
+  float eps;
+} fgemm_rms_t;
+
+/*
+ * As fgemm_matmul_ex, with RMSNorm statistics (rms may be NULL). Classical
+ * form on one-CTA or CTA-pair tiles only (tile_m 128 or 256; AUTO chooses
+ * among those), never with the last-wave K split; K >= 1. Other forced forms
+ * or tiles return FGEMM_ERR_UNSUPPORTED.
+ */
+fgemm_status_t fgemm_matmul_rms(fgemm_handle_t h, int64_t M, int64_t N,
+                                int64_t K, const void* A, int64_t lda,
+                                const void* B, int64_t ldb, void* C, int64_t ldc,
+                                fgemm_dtype_t dtype, const fgemm_epilogue_t* epi,
+                                fgemm_algo_t algo, int32_t tile_m, int32_t tile_n,
+                                const fgemm_rms_t* rms);
+
+/*
  * Runs the decision model (no launch): the algorithm, tile and predicted
  * time AUTO would use for this shape (FalconGEMM summary, "Methodology"
  * items 4 and 5). Output pointers may be NULL.

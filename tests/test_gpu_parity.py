@@ -409,3 +409,73 @@ def test_graph_replays_recount_split_pieces(M, N, K, tm, tn, split_mode):
         torch.cuda.synchronize()
         assert fgemm.default_handle().get_error() == fgemm.OK
         assert np.array_equal(gpu_bits(C), ref)
+
+
+# ------------------------------------------ RMSNorm statistics in the epilogue
+
+@pytest.mark.parametrize("tm,tn,epilogue", [(128, 64, "none"), (128, 128, "scale_bias"),
+                                            (128, 256, "silu"), (256, 128, "none"),
+                                            (256, 256, "scale_bias"), (128, 256, "swiglu"),
+                                            (256, 256, "swiglu")])
+def test_rms_sums_of_squares_out(tm, tn, epilogue):
+    """The producer's block sums of squares equal the oracle's over the values
+    C actually holds (fp32 sums of 64 squares against fp64)."""
+    M, N, K = 300, 1000, 520          # ragged rows, a partial last block
+    if epilogue == "swiglu":
+        N = 2064                      # output width 1032: 17 blocks, the last of 8 columns
+    A = inputs.matrix(M, K, "normal", "bf16", 90, DEV)
+    B = inputs.matrix(K, N, "normal_inv_k", "bf16", 91, DEV, k=K)
+    bias = inputs.matrix(1, N, "normal_0.02", "bf16", 92, DEV)[0] if epilogue == "scale_bias" else None
+    n_out = N // 2 if epilogue == "swiglu" else N
+    S = torch.full(((n_out + 63) // 64, M), float("nan"), dtype=torch.float32, device=DEV)
+    C = fgemm.matmul(A, B, epilogue=epilogue, bias=bias, tile_m=tm, tile_n=tn, sumsq_out=S)
+    torch.cuda.synchronize()
+    assert fgemm.default_handle().get_error() == fgemm.OK
+    ref = oracle.block_sumsq(values(C))
+    got = S.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    assert np.allclose(got, ref, rtol=1e-5, atol=0), np.max(np.abs(got - ref) / np.maximum(ref, 1e-30))
+
+
+@pytest.mark.parametrize("tm,tn", [(128, 128), (256, 256)])
+def test_rms_scale_in_chain(tm, tn):
+    """x = A W1 (+ its sums of squares); y = RMSNorm(x; g) W2 computed as
+    diag(r) x (g W2) by the second product: against the oracle's chain on the
+    same bf16 inputs (x as stored, g W2 as rounded), and against the plain
+    definition RMSNorm(x) W2 within the rounding of g W2."""
+    M, D, F, K = 512, 1024, 768, 640
+    eps = 1e-5
+    A = inputs.matrix(M, K, "normal", "bf16", 93, DEV)
+    W1 = inputs.matrix(K, D, "normal_inv_k", "bf16", 94, DEV, k=K)
+    W2 = inputs.matrix(D, F, "normal_inv_k", "bf16", 95, DEV, k=D)
+    g = (1.0 + 0.1 * torch.randn(D, generator=torch.Generator().manual_seed(96))).to(torch.float64)
+    S = torch.empty(((D + 63) // 64, M), dtype=torch.float32, device=DEV)
+    X = fgemm.matmul(A, W1, tile_m=tm, tile_n=tn, sumsq_out=S)
+    W2g = (g[:, None] * W2.double().cpu()).to(torch.bfloat16).to(DEV)   # g folded, rounded once
+    Y = fgemm.matmul(X, W2g, tile_m=tm, tile_n=tn, sumsq_in=S, norm_width=D, rms_eps=eps)
+    torch.cuda.synchronize()
+    assert fgemm.default_handle().get_error() == fgemm.OK
+    xv = values(X)
+    r = oracle.row_scale(oracle.block_sumsq(xv), D, eps)
+    acc = oracle.gemm(xv, values(W2g))
+    ref = r[:, None] * acc
+    y = values(Y)
+    assert normwise(y, ref, "bf16") <= TOL_NORMWISE["classical"]
+    absdot = r[:, None] * oracle.gemm(np.abs(xv), np.abs(values(W2g)))
+    ok, _ = elementwise_ok(y, ref, absdot, D, "bf16")
+    assert ok
+    # the definition, with the exact gain: off only by the rounding of g W2
+    defn = oracle.gemm(oracle.rmsnorm(xv, g.numpy(), eps), values(W2))
+    assert float(np.linalg.norm(y - defn) / np.linalg.norm(defn)) <= 5e-3
+
+
+def test_rms_rejections():
+    A = torch.zeros((256, 128), dtype=torch.bfloat16, device=DEV)
+    B = torch.zeros((128, 256), dtype=torch.bfloat16, device=DEV)
+    S = torch.zeros((4, 256), dtype=torch.float32, device=DEV)
+    with pytest.raises(fgemm.FgemmError):   # Strassen forms carry no statistics
+        fgemm.matmul(A, B, algo="strassen1", sumsq_out=S)
+    with pytest.raises(fgemm.FgemmError):   # nor does the small-M kernel
+        fgemm.matmul(A[:16], B, tile_m=16, tile_n=128, sumsq_out=S[:, :16].contiguous())
+    with pytest.raises(fgemm.FgemmError):   # eps must be finite and >= 0
+        fgemm.matmul(A, B, sumsq_in=S, norm_width=256, rms_eps=-1.0)
