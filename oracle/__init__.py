@@ -74,6 +74,10 @@ def _load():
         lib.oracle_winograd_emulated.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, i64, dp,
                                                  i64, dp, i64, dp, i64]
         lib.oracle_winograd_emulated.restype = ctypes.c_int
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_fp8_decode.argtypes = [ctypes.c_int, i64, u8p, dp]
+        lib.oracle_e8m0_decode.argtypes = [i64, u8p, dp]
+        lib.oracle_mx_values.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, u8p, i64, u8p, i64, dp]
         lib.oracle_rmsnorm.argtypes = [i64, i64, dp, i64, dp, ctypes.c_double, dp, i64]
         lib.oracle_block_sumsq.argtypes = [i64, i64, dp, i64, dp]
         lib.oracle_row_scale.argtypes = [i64, i64, dp, ctypes.c_double, ctypes.c_double, dp]
@@ -173,6 +177,39 @@ def epilogue(acc: np.ndarray, kind: str = "none", alpha: float = 1.0,
     _load().oracle_epilogue(k, M, N, _ptr(acc, ctypes.c_double), N, float(alpha),
                             None if b is None else _ptr(b, ctypes.c_double),
                             _ptr(out, ctypes.c_double), Nout)
+    return out
+
+
+FP8 = {"e4m3": 0, "e5m2": 1}
+
+
+def fp8_decode(bits: np.ndarray, fmt: str) -> np.ndarray:
+    """Exact value of every 8-bit float pattern (uint8 array) as float64."""
+    b = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_fp8_decode(FP8[fmt], b.size, _ptr(b, ctypes.c_uint8), _ptr(out, ctypes.c_double))
+    return out
+
+
+def e8m0_decode(bits: np.ndarray) -> np.ndarray:
+    """2^(e - 127) for every E8M0 pattern (255: NaN)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_e8m0_decode(b.size, _ptr(b, ctypes.c_uint8), _ptr(out, ctypes.c_double))
+    return out
+
+
+def mx_values(X: np.ndarray, S: np.ndarray, fmt: str, along: str) -> np.ndarray:
+    """Values of a block-scaled matrix: X (rows x cols, uint8 8-bit floats)
+    times the E8M0 scale of its block of 32.  along="row": S is rows x
+    ceil(cols/32); along="col": S is ceil(rows/32) x cols."""
+    X = np.ascontiguousarray(X, dtype=np.uint8)
+    S = np.ascontiguousarray(S, dtype=np.uint8)
+    rows, cols = X.shape
+    out = np.empty((rows, cols), dtype=np.float64)
+    _load().oracle_mx_values(FP8[fmt], 0 if along == "row" else 1, rows, cols,
+                             _ptr(X, ctypes.c_uint8), cols, _ptr(S, ctypes.c_uint8), S.shape[1],
+                             _ptr(out, ctypes.c_double))
     return out
 
 

@@ -50,6 +50,15 @@
  *    and since  y W = diag(r) x diag(g) W,  it multiplies its accumulator
  *    row i by r_i, with g folded into its weights once.
  *
+ *  - Block-scaled 8-bit inputs (MX: CS336 Lecture 05 notes, "Page 27.
+ *    Frontiers in low precision - FP8 and MXFP8").  An element is an 8-bit
+ *    float, E4M3
+ *    (bias 7, S.1111.111 is NaN, no infinity) or E5M2 (bias 15, IEEE-like
+ *    infinities and NaNs), and every 32 consecutive elements along K share a
+ *    power-of-two scale stored as E8M0 (value 2^(e - 127), e = 255 is NaN).
+ *    Its value is element * scale; the MX product is the classical product
+ *    of those values.
+ *
  *  - Winograd's variant of Strassen (named beside Strassen among the
  *    Strassen-like LCMAs of the FalconGEMM summary, "Methodology" item 1; the
  *    pages print no formulas, so the oracle uses the standard variant).  It
@@ -251,6 +260,54 @@ void oracle_epilogue(int kind, int64_t M, int64_t N, const double* acc,
       out[i * ldo + j] = o;
     }
   }
+}
+
+/* ------------------------------------------------------ 8-bit MX inputs */
+
+/* fmt 0: E4M3 (1 sign, 4 exponent bits, bias 7, 3 mantissa bits; exponent
+ * and mantissa all ones is NaN, no infinity).  fmt 1: E5M2 (5 exponent bits,
+ * bias 15, 2 mantissa bits; exponent all ones: infinity if the mantissa is 0,
+ * else NaN).  Exponent 0: subnormal, mantissa * 2^(1 - bias - mbits). */
+static double fp8_value(int fmt, uint8_t x) {
+  const int ebits = fmt == 0 ? 4 : 5, mbits = fmt == 0 ? 3 : 2;
+  const int bias = fmt == 0 ? 7 : 15;
+  const int sign = x >> 7;
+  const int e = (x >> mbits) & ((1 << ebits) - 1);
+  const int m = x & ((1 << mbits) - 1);
+  double v;
+  if (fmt == 0 && e == 15 && m == 7) return NAN;
+  if (fmt == 1 && e == 31) {
+    if (m != 0) return NAN;
+    v = INFINITY;
+  } else if (e == 0) {
+    v = ldexp((double)m, 1 - bias - mbits);
+  } else {
+    v = ldexp(1.0 + (double)m / (double)(1 << mbits), e - bias);
+  }
+  return sign ? -v : v;
+}
+
+void oracle_fp8_decode(int fmt, int64_t n, const uint8_t* in, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = fp8_value(fmt, in[i]);
+}
+
+/* E8M0 scale: 2^(e - 127); e = 255 is NaN. */
+static double e8m0_value(uint8_t e) { return e == 255 ? NAN : ldexp(1.0, (int)e - 127); }
+
+void oracle_e8m0_decode(int64_t n, const uint8_t* in, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e8m0_value(in[i]);
+}
+
+/* Value of a block-scaled matrix X (rows x cols, 8-bit elements, ld ldx).
+ * along == 0: blocks of 32 run along a row, S[r * lds + c / 32];
+ * along == 1: blocks of 32 run down a column, S[(r / 32) * lds + c]. */
+void oracle_mx_values(int fmt, int along, int64_t rows, int64_t cols, const uint8_t* X,
+                      int64_t ldx, const uint8_t* S, int64_t lds, double* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      const uint8_t e = along == 0 ? S[r * lds + c / 32] : S[(r / 32) * lds + c];
+      out[r * cols + c] = fp8_value(fmt, X[r * ldx + c]) * e8m0_value(e);
+    }
 }
 
 /* ------------------------------------------------------- RMSNorm pieces */

@@ -367,6 +367,61 @@ def test_winograd_emulated_rounding_error_is_in_the_expected_band(dtype, depth, 
     assert lo < rel < hi, rel
 
 
+# ------------------------------------------------------- 8-bit MX inputs
+
+@pytest.mark.parametrize("fmt,tdtype", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_fp8_decode_all_patterns_match_torch(fmt, tdtype):
+    bits = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(bits).view(tdtype).to(torch.float64).numpy()
+    got = oracle.fp8_decode(bits, fmt)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def test_fp8_special_values():
+    e4 = oracle.fp8_decode(np.array([0x38, 0x7E, 0x7F, 0x01, 0x80], dtype=np.uint8), "e4m3")
+    assert e4[0] == 1.0 and e4[1] == 448.0 and np.isnan(e4[2]) and e4[3] == 2.0 ** -9
+    assert e4[4] == 0.0 and np.signbit(e4[4])
+    e5 = oracle.fp8_decode(np.array([0x3C, 0x7B, 0x7C, 0xFC, 0x7D, 0x01], dtype=np.uint8), "e5m2")
+    assert e5[0] == 1.0 and e5[1] == 57344.0 and e5[2] == np.inf and e5[3] == -np.inf
+    assert np.isnan(e5[4]) and e5[5] == 2.0 ** -16
+
+
+def test_e8m0_decode_all_patterns_match_torch():
+    bits = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(bits).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = oracle.e8m0_decode(bits)
+    assert np.isnan(got[255]) and np.isnan(ref[255])
+    assert np.array_equal(got[:255], ref[:255])
+    assert got[127] == 1.0 and got[0] == 2.0 ** -127 and got[254] == 2.0 ** 127
+
+
+def test_mx_values_blocks_along_rows_and_columns():
+    rng = np.random.default_rng(40)
+    X = rng.integers(0, 256, (40, 70)).astype(np.uint8)
+    X[(X & 0x7F) == 0x7F] = 0x38                        # no NaN patterns
+    Sr = rng.integers(120, 135, (40, 3)).astype(np.uint8)   # blocks of 32 along a row
+    Sc = rng.integers(120, 135, (2, 70)).astype(np.uint8)   # blocks of 32 down a column
+    v = oracle.fp8_decode(X, "e4m3")
+    rowscale = 2.0 ** (np.repeat(Sr.astype(np.int64), 32, axis=1)[:, :70] - 127)
+    colscale = 2.0 ** (np.repeat(Sc.astype(np.int64), 32, axis=0)[:40, :] - 127)
+    assert np.array_equal(oracle.mx_values(X, Sr, "e4m3", "row"), v * rowscale)
+    assert np.array_equal(oracle.mx_values(X, Sc, "e4m3", "col"), v * colscale)
+
+
+def test_mx_product_closed_form():
+    # A = 1.0 everywhere with row scales 2^1, B = 0.5 with column scales 2^-2:
+    # every entry of the product is K * 2 * 0.5 * 0.25
+    M, N, K = 4, 6, 64
+    A = np.full((M, K), 0x38, dtype=np.uint8)              # E4M3 1.0
+    B = np.full((K, N), 0x38, dtype=np.uint8)              # E5M2 0.5 is 0x38 as well
+    SA = np.full((M, K // 32), 128, dtype=np.uint8)
+    SB = np.full((K // 32, N), 125, dtype=np.uint8)
+    C = oracle.gemm(oracle.mx_values(A, SA, "e4m3", "row"), oracle.mx_values(B, SB, "e5m2", "col"))
+    assert np.array_equal(C, np.full((M, N), K * 2.0 * 0.5 * 0.25))
+
+
 # ------------------------------------------------------------------ RMSNorm
 
 def test_rmsnorm_matches_torch():
