@@ -301,6 +301,8 @@ struct fgemm_handle_s {
   unsigned int* d_err = nullptr;
   float* workspace = nullptr;
   size_t ws_bytes = 0;
+  void* mx_buf = nullptr;             // bf16 values of MX inputs
+  size_t mx_bytes = 0;
   unsigned int* split_ctr = nullptr;  // K-split arrival counters (zeroed once)
   size_t split_ctr_count = 0;
   unsigned int split_gen = 0;         // generation of the last split launch
@@ -711,6 +713,7 @@ fgemm_status_t fgemm_destroy(fgemm_handle_t h) {
   cudaStreamSynchronize(h->stream);
   if (h->workspace) cudaFree(h->workspace);
   if (h->split_ctr) cudaFree(h->split_ctr);
+  if (h->mx_buf) cudaFree(h->mx_buf);
   if (h->d_err) cudaFree(h->d_err);
   delete h;
   return FGEMM_OK;
@@ -914,6 +917,85 @@ fgemm_status_t fgemm_matmul_rms(fgemm_handle_t h, int64_t M, int64_t N, int64_t 
                      "sumsq_in needs sumsq_parts >= 1, norm_width >= 1 and a finite eps >= 0");
   }
   return matmul_impl(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_m, tile_n, rms);
+}
+
+fgemm_status_t fgemm_mx_to_bf16(fgemm_handle_t h, int64_t rows, int64_t cols, const void* X,
+                                int64_t ldx, const void* S, int64_t lds, int32_t format,
+                                int32_t along, void* Y, int64_t ldy) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  if (format != FGEMM_FP8_E4M3 && format != FGEMM_FP8_E5M2)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "format must be FGEMM_FP8_E4M3 or FGEMM_FP8_E5M2");
+  if (along != 0 && along != 1) return set_msg(h, FGEMM_ERR_INVALID_ARG, "along must be 0 or 1");
+  if (rows < 0 || cols < 0) return set_msg(h, FGEMM_ERR_INVALID_ARG, "negative dimension");
+  if (rows == 0 || cols == 0) return FGEMM_OK;
+  if (!X || !S || !Y) return set_msg(h, FGEMM_ERR_INVALID_ARG, "X, S and Y must not be NULL");
+  const int64_t need_s = along == 0 ? (cols + 31) / 32 : cols;
+  if (ldx < cols || ldy < cols || lds < need_s)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "ldx, ldy >= cols and lds >= the scales per row");
+  if (reinterpret_cast<uintptr_t>(Y) & 1u) return set_msg(h, FGEMM_ERR_ALIGNMENT, "Y must be 2-byte aligned");
+  cudaError_t e = fgemm::launch_mx_dequant(static_cast<const uint8_t*>(X), ldx,
+                                           static_cast<const uint8_t*>(S), lds, format, along, rows, cols,
+                                           static_cast<uint16_t*>(Y), ldy, h->num_sms, h->stream);
+  return e == cudaSuccess ? FGEMM_OK : cuda_fail(h, e, "MX to bf16 launch");
+}
+
+fgemm_status_t fgemm_matmul_mx(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                               int64_t lda, const void* scale_a, int64_t ld_sa, int32_t a_format,
+                               const void* B, int64_t ldb, const void* scale_b, int64_t ld_sb,
+                               int32_t b_format, void* C, int64_t ldc, const fgemm_epilogue_t* epi,
+                               fgemm_algo_t algo, int32_t tile_m, int32_t tile_n) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  if ((a_format != FGEMM_FP8_E4M3 && a_format != FGEMM_FP8_E5M2) ||
+      (b_format != FGEMM_FP8_E4M3 && b_format != FGEMM_FP8_E5M2))
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "8-bit formats must be FGEMM_FP8_E4M3 or FGEMM_FP8_E5M2");
+  if (M < 0 || N < 0 || K < 0) return set_msg(h, FGEMM_ERR_INVALID_ARG, "negative dimension");
+  const int64_t kMax = (int64_t{1} << 31) - 1;
+  if (M > kMax || N > kMax || K > kMax)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "dimension above 2^31 - 1");
+  const int64_t kblocks = (K + 31) / 32;
+  if (M > 0 && N > 0 && K > 0) {
+    if (!A || !B || !scale_a || !scale_b)
+      return set_msg(h, FGEMM_ERR_INVALID_ARG, "A, B and their scales must not be NULL");
+    if (lda < K || ldb < N || ld_sa < kblocks || ld_sb < N)
+      return set_msg(h, FGEMM_ERR_INVALID_ARG, "lda >= K, ldb >= N, ld_sa >= ceil(K/32), ld_sb >= N");
+  }
+  const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
+  if (M == 0 || N == 0 || K == 0) {  // no 8-bit operand is read
+    return matmul_impl(h, M, N, K, A, lda, B, ldb, C, ldc, FGEMM_BF16, epi, algo, tile_m, tile_n,
+                       nullptr);
+  }
+  (void)kind;
+  // bf16 copies, rows padded to 8 elements (16-byte rows for the copy engine)
+  const int64_t kp = (K + 7) / 8 * 8, np = (N + 7) / 8 * 8;
+  const size_t a_bytes = (static_cast<size_t>(M) * kp * 2 + 255) / 256 * 256;
+  const size_t need = a_bytes + static_cast<size_t>(K) * np * 2;
+  if (need > h->mx_bytes) {
+    if (h->mx_buf) {
+      cudaError_t e = cudaStreamSynchronize(h->stream);
+      if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+      cudaFree(h->mx_buf);
+      h->mx_buf = nullptr;
+      h->mx_bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&h->mx_buf, need);
+    if (e != cudaSuccess) {
+      h->mx_buf = nullptr;
+      return cuda_fail(h, e, "cudaMalloc(MX bf16 values)");
+    }
+    h->mx_bytes = need;
+  }
+  uint16_t* Ab = static_cast<uint16_t*>(h->mx_buf);
+  uint16_t* Bb = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(h->mx_buf) + a_bytes);
+  cudaError_t e = fgemm::launch_mx_dequant(static_cast<const uint8_t*>(A), lda,
+                                           static_cast<const uint8_t*>(scale_a), ld_sa, a_format, 0, M,
+                                           K, Ab, kp, h->num_sms, h->stream);
+  if (e == cudaSuccess)
+    e = fgemm::launch_mx_dequant(static_cast<const uint8_t*>(B), ldb,
+                                 static_cast<const uint8_t*>(scale_b), ld_sb, b_format, 1, K, N, Bb,
+                                 np, h->num_sms, h->stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "MX to bf16 launch");
+  return matmul_impl(h, M, N, K, Ab, kp, Bb, np, C, ldc, FGEMM_BF16, epi, algo, tile_m, tile_n,
+                     nullptr);
 }
 
 fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,

@@ -83,6 +83,9 @@ def lib() -> ctypes.CDLL:
         L.fgemm_matmul.argtypes = mm
         L.fgemm_matmul_ex.argtypes = mm + [i32, i32]
         L.fgemm_matmul_rms.argtypes = mm + [i32, i32, ctypes.POINTER(Rms)]
+        L.fgemm_matmul_mx.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64,
+                                      i32, vp, i64, epi_p, st, i32, i32]
+        L.fgemm_mx_to_bf16.argtypes = [vp, i64, i64, vp, i64, vp, i64, i32, i32, vp, i64]
         L.fgemm_plan.argtypes = [vp, i64, i64, i64, st, epi_p, ctypes.POINTER(st),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(ctypes.c_double)]
@@ -126,7 +129,8 @@ def lib() -> ctypes.CDLL:
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
                      "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout",
-                     "fgemm_set_split_mode", "fgemm_matmul_rms"):
+                     "fgemm_set_split_mode", "fgemm_matmul_rms", "fgemm_matmul_mx",
+                     "fgemm_mx_to_bf16"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -366,6 +370,67 @@ def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
                              epi, algo, tile_n, tile_m, rms)
     _check(s, h.ptr)
     return out
+
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def matmul_mx(A: torch.Tensor, scale_a: torch.Tensor, B: torch.Tensor, scale_b: torch.Tensor, *,
+              a_format: str = "e4m3", b_format: str = "e4m3", out: torch.Tensor | None = None,
+              epilogue: str = "none", alpha: float = 1.0, bias: torch.Tensor | None = None,
+              algo: str = "auto", tile_n: int = 0, tile_m: int = 0,
+              handle: Handle | None = None) -> torch.Tensor:
+    """C = epi(alpha * A @ B + bias) for block-scaled 8-bit A (M x K) and B
+    (K x N), given as uint8 (or float8) CUDA tensors, with E8M0 scales
+    scale_a (M x ceil(K/32)) and scale_b (ceil(K/32) x N) as uint8; C is bf16."""
+    for t, name in ((A, "A"), (B, "B"), (scale_a, "scale_a"), (scale_b, "scale_b")):
+        if not t.is_cuda or t.dim() != 2 or t.element_size() != 1 or t.stride(1) != 1:
+            raise FgemmError(ERR_INVALID_ARG, f"{name} must be a 2-D CUDA byte tensor with unit column stride")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise FgemmError(ERR_INVALID_ARG, f"inner dimensions differ: {K} vs {K2}")
+    kb = (K + 31) // 32
+    if tuple(scale_a.shape) != (M, kb) or tuple(scale_b.shape) != (kb, N):
+        raise FgemmError(ERR_INVALID_ARG, "scales must be M x ceil(K/32) and ceil(K/32) x N")
+    n_out = N // 2 if epilogue == "swiglu" else N
+    if out is None:
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=A.device)
+    bias_ptr = None
+    if bias is not None:
+        if bias.dtype != torch.bfloat16 or bias.numel() != N or not bias.is_cuda:
+            raise FgemmError(ERR_INVALID_ARG, "bias must be a CUDA bf16 vector of N entries")
+        bias = bias.contiguous()
+        bias_ptr = bias.data_ptr()
+    h = handle if handle is not None else default_handle()
+    h.set_stream(torch.cuda.current_stream(A.device).cuda_stream)
+    epi = make_epilogue(epilogue, alpha, bias_ptr)
+    s = lib().fgemm_matmul_mx(h.ptr, M, N, K, A.data_ptr(), A.stride(0) if M > 1 else max(K, 1),
+                              scale_a.data_ptr(), scale_a.stride(0) if M > 1 else max(kb, 1),
+                              FP8_FORMATS[a_format], B.data_ptr(), B.stride(0) if K > 1 else max(N, 1),
+                              scale_b.data_ptr(), scale_b.stride(0) if kb > 1 else max(N, 1),
+                              FP8_FORMATS[b_format], out.data_ptr(),
+                              out.stride(0) if M > 1 else max(n_out, 1), ctypes.byref(epi),
+                              ALGOS[algo], tile_m, tile_n)
+    _check(s, h.ptr)
+    return out
+
+
+def mx_to_bf16(X: torch.Tensor, S: torch.Tensor, fmt: str = "e4m3", along: str = "row",
+               handle: Handle | None = None) -> torch.Tensor:
+    """bf16 values of a block-scaled 8-bit matrix X (uint8, rows x cols) with
+    E8M0 scales S: blocks of 32 along each row (S rows x ceil(cols/32)) or
+    down each column (S ceil(rows/32) x cols)."""
+    rows, cols = X.shape
+    Y = torch.empty((rows, cols), dtype=torch.bfloat16, device=X.device)
+    h = handle if handle is not None else default_handle()
+    h.set_stream(torch.cuda.current_stream(X.device).cuda_stream)
+    s = lib().fgemm_mx_to_bf16(h.ptr, rows, cols, X.data_ptr(), X.stride(0) if rows > 1 else max(cols, 1),
+                               S.data_ptr(), S.stride(0) if S.shape[0] > 1 else max(S.shape[1], 1),
+                               FP8_FORMATS[fmt], 0 if along == "row" else 1, Y.data_ptr(),
+                               Y.stride(0) if rows > 1 else max(cols, 1))
+    _check(s, h.ptr)
+    return Y
 
 
 def plan(M: int, N: int, K: int, dtype: torch.dtype = torch.bfloat16, epilogue: str = "none"):

@@ -203,6 +203,47 @@ fgemm_status_t fgemm_matmul_rms(fgemm_handle_t h, int64_t M, int64_t N,
                                 const fgemm_rms_t* rms);
 
 /*
+ * Block-scaled 8-bit inputs (MX; CS336 Lecture 05 notes, "Page 27. Frontiers
+ * in low precision - FP8 and MXFP8" and "Page 28. MXFP8 training in
+ * practice"): C = epi(alpha * A * B + bias) where every element of A and B is
+ * an 8-bit float times the E8M0 scale (2^(e - 127), e = 255 NaN) of its block
+ * of 32 values along K.
+ *   A, lda          device, M x K bytes, lda >= K.
+ *   scale_a, ld_sa  device, M x ceil(K/32) E8M0 bytes: row i, block k/32.
+ *   B, ldb          device, K x N bytes, ldb >= N.
+ *   scale_b, ld_sb  device, ceil(K/32) x N E8M0 bytes: block k/32, column j.
+ *   a_format, b_format  FGEMM_FP8_E4M3 or FGEMM_FP8_E5M2.
+ *   C, ldc, epi     as fgemm_matmul_ex, in bf16 (bias bf16 too).
+ * Each value is written to bf16 first, which is exact while it lies in
+ * bf16's normal range; outside it the exact value is rounded once (RNE, to
+ * a subnormal or infinity). Those bf16 matrices live in a handle-owned
+ * buffer (grown on demand), and the product then runs as fgemm_matmul_ex
+ * with algo / tile_m / tile_n. This function has no fused 8-bit tensor-core
+ * path: the product runs at the bf16 rate.
+ */
+typedef enum { FGEMM_FP8_E4M3 = 0, FGEMM_FP8_E5M2 = 1 } fgemm_fp8_format_t;
+
+/*
+ * The first step of fgemm_matmul_mx on its own: Y (rows x cols bf16, ld ldy,
+ * 16-byte aligned rows for the fast path) = the values of the block-scaled
+ * matrix X (rows x cols bytes, ld ldx) with E8M0 scales S (ld lds): blocks of
+ * 32 along each row (along 0, S is rows x ceil(cols/32)) or down each column
+ * (along 1, S is ceil(rows/32) x cols). Each value is rounded once to bf16
+ * (exact while in bf16's normal range). Asynchronous on the handle's stream.
+ */
+fgemm_status_t fgemm_mx_to_bf16(fgemm_handle_t h, int64_t rows, int64_t cols,
+                                const void* X, int64_t ldx, const void* S, int64_t lds,
+                                int32_t format, int32_t along, void* Y, int64_t ldy);
+
+fgemm_status_t fgemm_matmul_mx(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                               const void* A, int64_t lda, const void* scale_a,
+                               int64_t ld_sa, int32_t a_format, const void* B,
+                               int64_t ldb, const void* scale_b, int64_t ld_sb,
+                               int32_t b_format, void* C, int64_t ldc,
+                               const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                               int32_t tile_m, int32_t tile_n);
+
+/*
  * Runs the decision model (no launch): the algorithm, tile and predicted
  * time AUTO would use for this shape (FalconGEMM summary, "Methodology"
  * items 4 and 5). Output pointers may be NULL.

@@ -479,3 +479,103 @@ def test_rms_rejections():
         fgemm.matmul(A[:16], B, tile_m=16, tile_n=128, sumsq_out=S[:, :16].contiguous())
     with pytest.raises(fgemm.FgemmError):   # eps must be finite and >= 0
         fgemm.matmul(A, B, sumsq_in=S, norm_width=256, rms_eps=-1.0)
+
+
+# ----------------------------------------------- block-scaled 8-bit (MX) inputs
+
+def _mx_random(rows, cols, fmt, along, seed, lo=118, hi=136):
+    """Random 8-bit floats (no NaN or infinity patterns) and E8M0 scales in
+    [lo, hi) (2^-9 .. 2^8): uint8 tensors on the device."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randint(0, 256, (rows, cols), generator=g, dtype=torch.int32).to(torch.uint8)
+    special = (x & 0x7F) == 0x7F if fmt == "e4m3" else (x & 0x7C) == 0x7C
+    x[special] = 0x38
+    kb = (cols + 31) // 32 if along == "row" else (rows + 31) // 32
+    shape = (rows, kb) if along == "row" else (kb, cols)
+    s = torch.randint(lo, hi, shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    return x.to(DEV), s.to(DEV)
+
+
+def _np(t):
+    return t.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("along", ["row", "col"])
+def test_mx_to_bf16_every_pattern_and_scale(fmt, along):
+    """Every 8-bit pattern (NaNs and infinities included) under every E8M0
+    scale: the bf16 value equals the exact value rounded once (subnormal
+    results, overflow to infinity, NaN scales)."""
+    x = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    if along == "row":   # 256 rows = one per scale; each row is all 256 patterns
+        X = x.repeat(256, 1).to(DEV)
+        S = torch.arange(256, dtype=torch.int32).to(torch.uint8)[:, None].repeat(1, 8).to(DEV)
+    else:                # 256 columns per pattern block, scales down each column
+        X = x[:, None].repeat(1, 256).to(DEV)
+        S = torch.arange(256, dtype=torch.int32).to(torch.uint8)[None, :].repeat(8, 1).to(DEV)
+    Y = fgemm.mx_to_bf16(X, S, fmt, along)
+    torch.cuda.synchronize()
+    ref = oracle.mx_values(_np(X), _np(S), fmt, along)
+    got = values(Y)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(gpu_bits(Y)[ok], oracle.encode(ref[ok], "bf16"))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_mx_values_exact_through_identity(fmt):
+    """C = A x I through the whole MX product: every entry is A's value rounded
+    once to bf16, bit for bit (scales that keep the values in bf16's normal
+    range; how the tensor core treats subnormal inputs is not this test's)."""
+    M, K = 130, 96
+    A, SA = _mx_random(M, K, fmt, "row", 100, lo=20, hi=240)
+    B = torch.zeros((K, K), dtype=torch.uint8, device=DEV)
+    B.fill_diagonal_(0x38 if fmt == "e4m3" else 0x3C)         # 1.0
+    SB = torch.full(((K + 31) // 32, K), 127, dtype=torch.uint8, device=DEV)
+    C = fgemm.matmul_mx(A, SA, B, SB, a_format=fmt, b_format=fmt)
+    torch.cuda.synchronize()
+    assert fgemm.default_handle().get_error() == fgemm.OK
+    ref = oracle.encode(oracle.mx_values(_np(A), _np(SA), fmt, "row"), "bf16")
+    got = gpu_bits(C)
+    # -0 in A meets +0 products from the rest of the row: the sum is +0
+    zero = ((got & 0x7FFF) == 0) & ((ref & 0x7FFF) == 0)
+    assert np.array_equal(np.where(zero, 0, got), np.where(zero, 0, ref))
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e4m3", "e5m2"), ("e5m2", "e5m2")])
+@pytest.mark.parametrize("M,N,K,epilogue", [(256, 512, 1024, "none"), (300, 520, 1000, "scale_bias"),
+                                            (1024, 1024, 2048, "silu")])
+def test_mx_product_every_entry(fa, fb, M, N, K, epilogue):
+    A, SA = _mx_random(M, K, fa, "row", 101)
+    B, SB = _mx_random(K, N, fb, "col", 102)
+    bias = inputs.matrix(1, N, "normal_0.02", "bf16", 103, DEV)[0] if epilogue == "scale_bias" else None
+    C = fgemm.matmul_mx(A, SA, B, SB, a_format=fa, b_format=fb, epilogue=epilogue, bias=bias)
+    torch.cuda.synchronize()
+    assert fgemm.default_handle().get_error() == fgemm.OK
+    Av = oracle.mx_values(_np(A), _np(SA), fa, "row")
+    Bv = oracle.mx_values(_np(B), _np(SB), fb, "col")
+    bv = None if bias is None else values(bias)
+    raw = oracle.gemm(Av, Bv)
+    ref = oracle.epilogue(raw, epilogue, 1.0, bv)
+    c = values(C)
+    kappa = activation_condition(raw, epilogue, 1.0, bv)
+    assert normwise(c, ref, "bf16") <= TOL_NORMWISE["classical"] * max(1.0, kappa)
+    if epilogue in ("none", "scale_bias"):
+        absdot = oracle.gemm(np.abs(Av), np.abs(Bv))
+        ok, _ = elementwise_ok(c, ref, absdot, K, "bf16")
+        assert ok
+
+
+def test_mx_exact_ternary():
+    """Elements in {-1, 0, 1} with unit scales: integer products, exact."""
+    M, N, K = 256, 384, 520
+    g = torch.Generator().manual_seed(104)
+    pick = torch.tensor([0x00, 0x38, 0xB8], dtype=torch.uint8)     # 0, 1, -1 in E4M3
+    A = pick[torch.randint(0, 3, (M, K), generator=g)].to(DEV)
+    B = pick[torch.randint(0, 3, (K, N), generator=g)].to(DEV)
+    SA = torch.full((M, (K + 31) // 32), 127, dtype=torch.uint8, device=DEV)
+    SB = torch.full(((K + 31) // 32, N), 127, dtype=torch.uint8, device=DEV)
+    C = fgemm.matmul_mx(A, SA, B, SB)
+    ref = oracle.encode(oracle.gemm(oracle.fp8_decode(_np(A), "e4m3"), oracle.fp8_decode(_np(B), "e4m3")),
+                        "bf16")
+    assert np.array_equal(gpu_bits(C), ref)
