@@ -256,19 +256,21 @@ __device__ __forceinline__ void finish_swiglu_warp(const KernelParams& p, int co
 // the PingPong GEMM / CODA note): with p.sumsq_in the accumulator row is first
 // scaled by 1 / sqrt(mean of squares + eps) of an earlier product's row; with
 // p.sumsq_out the sums of squares of the stored values of each 64-column
-// block are written out, in column order within the block.
-template <int BN>
-__device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32_t tbase, int row0,
-                                                   int tn, int r) {
+// block are written out, in column order within the block.  RMS selects the
+// variant with those statistics at compile time, so the plain epilogue pays
+// nothing for them.
+template <int BN, bool RMS>
+__device__ __forceinline__ void epilogue_classical_t(const KernelParams& p, uint32_t tbase, int row0,
+                                                     int tn, int r) {
   const int lane = threadIdx.x & 31;
   const int row = row0 + r;
   const bool row_ok = row < p.M;
   // RMSNorm: the scale of this row (1 without statistics in), and the
   // running sum of squares of the stored outputs of one 64-column block
-  const float rs = (p.sumsq_in && row_ok) ? rms_row_scale(p, row) : 1.0f;
+  const float rs = (RMS && p.sumsq_in && row_ok) ? rms_row_scale(p, row) : 1.0f;
   float ss = 0.0f;
   auto add_sumsq = [&](int c, int col0, const float (&v)[32]) {
-    if (!p.sumsq_out) return;
+    if (!RMS || !p.sumsq_out) return;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const float q = round_out(v[j], p.is_bf16);
@@ -301,8 +303,10 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
       float g[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float gv = p.alpha * (rs * __uint_as_float(gr[j])) + __shfl_sync(0xFFFFFFFFu, bg[c], j);
-        const float uv = p.alpha * (rs * __uint_as_float(ur[j])) + __shfl_sync(0xFFFFFFFFu, bu[c], j);
+        const float ga = RMS ? rs * __uint_as_float(gr[j]) : __uint_as_float(gr[j]);
+        const float ua = RMS ? rs * __uint_as_float(ur[j]) : __uint_as_float(ur[j]);
+        const float gv = p.alpha * ga + __shfl_sync(0xFFFFFFFFu, bg[c], j);
+        const float uv = p.alpha * ua + __shfl_sync(0xFFFFFFFFu, bu[c], j);
         g[j] = silu(gv) * uv;
       }
       if (row_ok && col0 < p.n_out) store_row32(p, row, col0, g);
@@ -320,7 +324,8 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float x = p.alpha * (rs * __uint_as_float(ar[j])) + __shfl_sync(0xFFFFFFFFu, bf, j);
+        const float a = RMS ? rs * __uint_as_float(ar[j]) : __uint_as_float(ar[j]);
+        float x = p.alpha * a + __shfl_sync(0xFFFFFFFFu, bf, j);
         if (p.epi == kEpiSilu) x = silu(x);
         v[j] = x;
       }
@@ -345,6 +350,15 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
       }
     }
   }
+}
+
+template <int BN>
+__device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32_t tbase, int row0,
+                                                   int tn, int r) {
+  if (p.sumsq_in || p.sumsq_out)
+    epilogue_classical_t<BN, true>(p, tbase, row0, tn, r);
+  else
+    epilogue_classical_t<BN, false>(p, tbase, row0, tn, r);
 }
 
 // Strassen product `pr` for the 128 rows starting at row0 (inside each
