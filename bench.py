@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="decision-model check: every legal form/tile vs auto on the sweep shapes")
     ap.add_argument("--out", default=None, help="JSON-lines file for --sweep")
+    ap.add_argument("--mx", default=None, choices=["e4m3", "e5m2"],
+                    help="time the block-scaled 8-bit (MX) product on the workload's shape")
     return ap.parse_args()
 
 
@@ -529,10 +531,80 @@ def run_sweep(args):
         raise SystemExit(f"device error: {handle.last_message()}")
 
 
+def run_mx(args):
+    """Times fgemm_matmul_mx (8-bit elements, E8M0 scales per 32 values of
+    K) on the workload's shape: the whole call, its 8-bit-to-bf16 step alone
+    and the bf16 product alone.  Each is captured `steps` times in a CUDA
+    graph over four rotating input sets and timed by CUDA events around a
+    replay, so host launch costs do not count.  One JSON line."""
+    from complexity_matmul_tcgen05_gb300 import fgemm
+    dev = torch.device("cuda", torch.cuda.current_device())
+    M, N, K, _, _ = workload_shape(args.workload)
+    kb = (K + 31) // 32
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    sets = 4
+    # Elements as block-scaled quantisation leaves them: Gaussian values whose
+    # block maxima sit near the top of the 8-bit range (sigma 64 of E4M3's
+    # 448, 8192 of E5M2's 57344), cast by torch; scales spread around 2^0.
+    sigma, f8 = (64.0, torch.float8_e4m3fn) if args.mx == "e4m3" else (8192.0, torch.float8_e5m2)
+    def fp8(rows, cols):
+        x = torch.randn((rows, cols), generator=g, device=dev) * sigma
+        return x.to(f8).view(torch.uint8)
+    def scales(rows, cols):
+        return torch.randint(120, 135, (rows, cols), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    As = [fp8(M, K) for _ in range(sets)]
+    Bs = [fp8(K, N) for _ in range(sets)]
+    SA = scales(M, kb)
+    SB = scales(kb, N)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    Ab = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    Bb = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+    h = fgemm.default_handle()
+
+    def timed(fn):
+        for i in range(max(3, args.warmup)):
+            fn(i)  # allocations and launch set-up happen before the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                fn(i)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / args.steps
+
+    full = timed(lambda i: fgemm.matmul_mx(As[i % sets], SA, Bs[i % sets], SB, a_format=args.mx,
+                                           b_format=args.mx, out=C, handle=h))
+    conv = timed(lambda i: (fgemm.mx_to_bf16(As[i % sets], SA, args.mx, "row", handle=h, out=Ab),
+                            fgemm.mx_to_bf16(Bs[i % sets], SB, args.mx, "col", handle=h, out=Bb)))
+    prod = timed(lambda i: fgemm.matmul(Ab, Bb, out=C, handle=h))
+    if h.get_error() != fgemm.OK:
+        raise SystemExit(f"device error: {h.last_message()}")
+    flops = 2.0 * M * N * K
+    mx_bytes = M * K + K * N + M * kb + kb * N
+    print(json.dumps({
+        "metric": METRIC, "value": flops / (full * 1e-6) / 1e12, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full / 1e3,
+        "higher_is_better": True, "dtype": f"mx-{args.mx} -> bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "mx_format": args.mx,
+                   "l2": f"{sets} rotating 8-bit input sets", "timing": "CUDA graph replay"},
+        "mx_to_bf16_us": conv, "mx_to_bf16_gbs": (mx_bytes + 2 * (M * K + K * N)) / (conv * 1e3),
+        "bf16_product_us": prod, "whole_call_us": full}), flush=True)
+
+
 def main():
     args = parse()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.mx:
+        run_mx(args)
         return
     rank, world = dist_setup(args.gpus)
     if args.impl == "reference":

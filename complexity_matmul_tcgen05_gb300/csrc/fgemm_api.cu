@@ -933,9 +933,9 @@ fgemm_status_t fgemm_mx_to_bf16(fgemm_handle_t h, int64_t rows, int64_t cols, co
   if (ldx < cols || ldy < cols || lds < need_s)
     return set_msg(h, FGEMM_ERR_INVALID_ARG, "ldx, ldy >= cols and lds >= the scales per row");
   if (reinterpret_cast<uintptr_t>(Y) & 1u) return set_msg(h, FGEMM_ERR_ALIGNMENT, "Y must be 2-byte aligned");
-  cudaError_t e = fgemm::launch_mx_dequant(static_cast<const uint8_t*>(X), ldx,
-                                           static_cast<const uint8_t*>(S), lds, format, along, rows, cols,
-                                           static_cast<uint16_t*>(Y), ldy, h->num_sms, h->stream);
+  const fgemm::MxJob job{static_cast<const uint8_t*>(X), ldx, static_cast<const uint8_t*>(S), lds, format,
+                         along, rows, cols, static_cast<uint16_t*>(Y), ldy};
+  cudaError_t e = fgemm::launch_mx_dequant(&job, 1, h->num_sms, h->stream);
   return e == cudaSuccess ? FGEMM_OK : cuda_fail(h, e, "MX to bf16 launch");
 }
 
@@ -986,13 +986,12 @@ fgemm_status_t fgemm_matmul_mx(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
   }
   uint16_t* Ab = static_cast<uint16_t*>(h->mx_buf);
   uint16_t* Bb = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(h->mx_buf) + a_bytes);
-  cudaError_t e = fgemm::launch_mx_dequant(static_cast<const uint8_t*>(A), lda,
-                                           static_cast<const uint8_t*>(scale_a), ld_sa, a_format, 0, M,
-                                           K, Ab, kp, h->num_sms, h->stream);
-  if (e == cudaSuccess)
-    e = fgemm::launch_mx_dequant(static_cast<const uint8_t*>(B), ldb,
-                                 static_cast<const uint8_t*>(scale_b), ld_sb, b_format, 1, K, N, Bb,
-                                 np, h->num_sms, h->stream);
+  const fgemm::MxJob jobs[2] = {
+      {static_cast<const uint8_t*>(A), lda, static_cast<const uint8_t*>(scale_a), ld_sa, a_format, 0, M, K, Ab,
+       kp},
+      {static_cast<const uint8_t*>(B), ldb, static_cast<const uint8_t*>(scale_b), ld_sb, b_format, 1, K, N, Bb,
+       np}};
+  cudaError_t e = fgemm::launch_mx_dequant(jobs, 2, h->num_sms, h->stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "MX to bf16 launch");
   return matmul_impl(h, M, N, K, Ab, kp, Bb, np, C, ldc, FGEMM_BF16, epi, algo, tile_m, tile_n,
                      nullptr);

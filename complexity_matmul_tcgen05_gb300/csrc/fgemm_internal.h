@@ -199,11 +199,22 @@ cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, int grid,
 // with p.split_gen.
 cudaError_t launch_gemm_skinny(int mp, const KernelParams& p, int grid, cudaStream_t stream);
 
-// Block-scaled 8-bit matrix (fmt 0 E4M3, 1 E5M2; E8M0 scales of blocks of 32
-// along rows (along 0) or down columns (along 1)) to bf16 values Y.
-cudaError_t launch_mx_dequant(const uint8_t* X, long long ldx, const uint8_t* S, long long lds, int fmt,
-                              int along, long long rows, long long cols, uint16_t* Y, long long ldy,
-                              int num_sms, cudaStream_t stream);
+// A block-scaled 8-bit matrix X (rows x cols, fmt 0 E4M3, 1 E5M2) with E8M0
+// scales S of blocks of 32 along rows (along 0) or down columns (along 1),
+// and the bf16 matrix Y its values go to.
+struct MxJob {
+  const uint8_t* X;
+  long long ldx;
+  const uint8_t* S;
+  long long lds;
+  int fmt, along;
+  long long rows, cols;
+  uint16_t* Y;
+  long long ldy;
+};
+
+// Converts one or two such matrices (njobs 1 or 2) in a single launch.
+cudaError_t launch_mx_dequant(const MxJob* jobs, int njobs, int num_sms, cudaStream_t stream);
 
 // One-level Winograd variant on the single-CTA kernel (bn = 128 or 256): the
 // Strassen kernel with up to four source blocks per formed operand; p.tab

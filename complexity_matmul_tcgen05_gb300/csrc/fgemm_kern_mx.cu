@@ -15,8 +15,10 @@
 // (round-to-nearest-even), so the value equals the exact value rounded once.
 // NaN elements or scales give NaN; E5M2 infinities stay infinite.
 //
-// Memory-bound: each thread converts 16 consecutive bytes of a row (one
-// 16-byte load, two 16-byte stores), grid-strided over the matrix.
+// Memory-bound: a thread converts a group of 16 consecutive bytes (one
+// 16-byte load, two 16-byte stores, the group's scales in one load).  Groups
+// with no special element or scale (the usual case) take a packed integer
+// path, two elements per 32-bit word; the rest go through fp32.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -30,13 +32,8 @@ namespace fgemm {
 
 namespace {
 
-__device__ __forceinline__ float fp8_to_float(uint8_t x, int fmt) {
-  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(x),
-                                               fmt == 0 ? __NV_E4M3 : __NV_E5M2);
-  return __half2float(__half(h));
-}
 
-// x * 2^(e - 127) rounded once to bf16.
+// x * 2^(e - 127) rounded once to bf16 (the general path).
 __device__ __forceinline__ uint16_t scaled_bf16(float x, uint8_t e) {
   if (e == 255u) return 0x7FC0u;  // NaN scale
   // 2^(e - 127) as fp32 (normal for e >= 1, the subnormal 2^-127 for e = 0)
@@ -51,66 +48,247 @@ __device__ __forceinline__ uint16_t scaled_bf16(float x, uint8_t e) {
   return __bfloat16_as_ushort(__double2bfloat16(d));
 }
 
-// along == 0: scale blocks run along a row (S[r * lds + c / 32]);
-// along == 1: they run down a column (S[(r / 32) * lds + c]).
-__global__ void __launch_bounds__(256) mx_dequant_kernel(const uint8_t* __restrict__ X, long long ldx,
-                                                         const uint8_t* __restrict__ S, long long lds,
-                                                         int fmt, int along, long long rows,
-                                                         long long cols, uint16_t* __restrict__ Y,
-                                                         long long ldy) {
-  const long long groups_per_row = (cols + 15) / 16;
-  const long long total = rows * groups_per_row;
-  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
-       g += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = g / groups_per_row;
-    const long long c0 = (g - r * groups_per_row) * 16;
-    const uint8_t* src = X + r * ldx + c0;
-    uint16_t* dst = Y + r * ldy + c0;
-    const bool whole = c0 + 16 <= cols && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) &&
-                       ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0);
-    uint8_t b[16];
-    if (whole) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// The bit layouts (CS336 Lecture 05 notes, "Page 27"): E4M3 has 4 exponent
+// bits with bias 7 and 3 mantissa bits, and its only specials are the NaNs
+// 0x7F / 0xFF; E5M2 has 5 exponent bits with bias 15 and 2 mantissa bits, and
+// exponent 31 holds infinities and NaNs.  A bf16 has 8 exponent bits (bias
+// 127) and 7 mantissa bits.
+template <int FMT>
+struct Fp8Layout {
+  static constexpr uint32_t kBias = FMT == 0 ? 7u : 15u;
+  static constexpr int kShift = FMT == 0 ? 4 : 5;  // 7 - mantissa bits
+  static constexpr uint32_t kExpMask4 = FMT == 0 ? 0x78787878u : 0x7C7C7C7Cu;
+  static constexpr uint32_t kManMask4 = FMT == 0 ? 0x07070707u : 0x03030303u;
+  // Scales e for which every normal element lands on a bf16 normal:
+  // exponent x_exp - bias + e in [1, 254] for x_exp over the normal range
+  // (E4M3 1..15, E5M2 1..30).
+  static constexpr uint32_t kScaleLo = FMT == 0 ? 7u : 15u;
+  static constexpr uint32_t kScaleHi = FMT == 0 ? 246u : 239u;
+};
+
+// Bit 7 of each byte of the result is set where that byte of `w` is an
+// 8-bit subnormal or a NaN / infinity pattern (the elements the integer path
+// below does not take); the other bits are junk.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8_specials4(uint32_t w) {
+  using L = Fp8Layout<FMT>;
+  const uint32_t exp_nz = (w & L::kExpMask4) + L::kExpMask4;
+  const uint32_t man_nz = (w & L::kManMask4) + 0x7F7F7F7Fu;
+  const uint32_t top = FMT == 0 ? (w & 0x7F7F7F7Fu) + 0x01010101u : (w & 0x7C7C7C7Cu) + 0x04040404u;
+  return (man_nz & ~exp_nz) | top;
+}
+
+// Bit 7 of each byte set where that byte of `s` lies outside [lo, hi]
+// (lo < 128 <= hi); the other bits are junk.
+__device__ __forceinline__ uint32_t bytes_outside4(uint32_t s, uint32_t lo, uint32_t hi) {
+  const uint32_t ge_lo = ((s | 0x80808080u) - lo * 0x01010101u) | s;
+  const uint32_t ns = ~s;
+  const uint32_t le_hi = ((ns | 0x80808080u) - (255u - hi) * 0x01010101u) | ns;
+  return ~(ge_lo & le_hi);
+}
+
+// Two elements in the low bytes of the 16-bit lanes of `p`, their bf16
+// exponent offsets ((e - bias) << 7) in the lanes of `eb`: a normal element
+// keeps its sign and mantissa and has its exponent re-biased by the scale
+// (bf16 exponent = x_exp - bias + e), a zero keeps only its sign.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t p, uint32_t eb) {
+  const uint32_t mag = p & 0x007F007Fu;
+  const uint32_t nonzero = (((mag + 0x007F007Fu) & 0x00800080u) * 0xFFu);  // 0x7F80 per nonzero lane
+  return ((mag << Fp8Layout<FMT>::kShift) + (eb & nonzero)) | ((p & 0x00800080u) << 8);
+}
+
+// One 16-column group: its 16 bytes and the 16 scales that apply to them,
+// both packed four to a word.
+struct MxGroup {
+  uint32_t w[4];
+  uint32_t s[4];
+};
+
+__device__ __forceinline__ void mx_load(const uint8_t* __restrict__ src, const uint8_t* __restrict__ S,
+                                        long long lds, int along, long long r, long long c0,
+                                        long long cols, bool whole, MxGroup& g) {
+  if (whole) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+    g.w[0] = v.x;
+    g.w[1] = v.y;
+    g.w[2] = v.z;
+    g.w[3] = v.w;
+  } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) b[i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
-    } else {
+    for (int q = 0; q < 4; ++q) {
+      g.w[q] = 0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) b[i] = c0 + i < cols ? src[i] : 0;
+      for (int i = 0; i < 4; ++i)
+        if (c0 + 4 * q + i < cols) g.w[q] |= static_cast<uint32_t>(src[4 * q + i]) << (8 * i);
     }
-    uint16_t o[16];
+  }
+  // one byte (a 16-column group lies in one 32-block of its row) or 16
+  // consecutive bytes (one per column)
+  if (along == 0) {
+    const uint32_t ev = __ldg(S + r * lds + (c0 >> 5));
+    const uint32_t rep = ev * 0x01010101u;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const long long c = c0 + i;
-      const uint8_t e = along == 0 ? S[r * lds + (c >> 5)] : S[(r >> 5) * lds + c];
-      o[i] = c < cols ? scaled_bf16(fp8_to_float(b[i], fmt), e) : 0;
-    }
-    if (whole) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-      d4[0] = make_uint4(o[0] | (static_cast<uint32_t>(o[1]) << 16), o[2] | (static_cast<uint32_t>(o[3]) << 16),
-                         o[4] | (static_cast<uint32_t>(o[5]) << 16), o[6] | (static_cast<uint32_t>(o[7]) << 16));
-      d4[1] = make_uint4(o[8] | (static_cast<uint32_t>(o[9]) << 16), o[10] | (static_cast<uint32_t>(o[11]) << 16),
-                         o[12] | (static_cast<uint32_t>(o[13]) << 16), o[14] | (static_cast<uint32_t>(o[15]) << 16));
+    for (int q = 0; q < 4; ++q) g.s[q] = rep;
+  } else {
+    const uint8_t* srow = S + (r >> 5) * lds + c0;
+    if (whole && ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0)) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(srow));
+      g.s[0] = v.x;
+      g.s[1] = v.y;
+      g.s[2] = v.z;
+      g.s[3] = v.w;
     } else {
+      // columns past the end get scale 127 (2^0): their elements are zero
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (c0 + i < cols) dst[i] = o[i];
+      for (int q = 0; q < 4; ++q) {
+        g.s[q] = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t e = c0 + 4 * q + i < cols ? __ldg(srow + 4 * q + i) : 127u;
+          g.s[q] |= e << (8 * i);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mx_store(uint16_t* dst, long long c0, long long cols, bool whole,
+                                         const uint32_t (&o)[8]) {
+  if (whole) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    d4[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (c0 + i < cols) dst[i] = static_cast<uint16_t>(o[i >> 1] >> (16 * (i & 1)));
+  }
+}
+
+// The general path for a group that holds a special element or scale: each
+// value through fp32 (or fp64 near the ends of bf16's range).  Kept out of
+// line so that the common path stays small.
+__device__ __noinline__ void mx_group_general(uint16_t* dst, long long c0, long long cols, bool whole,
+                                              MxGroup g, int fmt) {
+  const __nv_fp8_interpretation_t interp = fmt == 0 ? __NV_E4M3 : __NV_E5M2;
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t x = (g.w[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+    const uint8_t e = static_cast<uint8_t>(g.s[i >> 2] >> (8 * (i & 3)));
+    const float f = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(x), interp)));
+    const uint32_t v = scaled_bf16(f, e);
+    if (i & 1)
+      o[i >> 1] |= v << 16;
+    else
+      o[i >> 1] = v;
+  }
+  mx_store(dst, c0, cols, whole, o);
+}
+
+// One group: the integer path when no element is special and every scale
+// lies in the range where all results are bf16 normals, else the general one.
+template <int FMT>
+__device__ __forceinline__ void mx_group(uint16_t* dst, long long c0, long long cols, bool whole,
+                                         const MxGroup& g, int along) {
+  using L = Fp8Layout<FMT>;
+  uint32_t bad = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) bad |= fp8_specials4<FMT>(g.w[q]);
+  if (along == 0) {
+    const uint32_t e = g.s[0] & 0xFFu;
+    if (e < L::kScaleLo || e > L::kScaleHi) bad |= 0x80u;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) bad |= bytes_outside4(g.s[q], L::kScaleLo, L::kScaleHi);
+  }
+  if (bad & 0x80808080u) {
+    mx_group_general(dst, c0, cols, whole, g, FMT);
+    return;
+  }
+  uint32_t o[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t sel = h == 0 ? 0x4140u : 0x4342u;  // bytes 2h, 2h+1 into the two lanes
+      const uint32_t p = __byte_perm(g.w[q], 0, sel);
+      const uint32_t eb = (__byte_perm(g.s[q], 0, sel) << 7) - (L::kBias << 7) * 0x00010001u;
+      o[2 * q + h] = fp8x2_to_bf16x2<FMT>(p, eb);
+    }
+  }
+  mx_store(dst, c0, cols, whole, o);
+}
+
+constexpr int kMxRows = 1;  // rows per thread (more held more registers and ran slower)
+
+// Up to two matrices in one launch.  Block b of the flat grid works on job 0
+// while b < blocks0, else on job 1; within a job, blocks walk column chunks
+// of 256 groups (x) inside row chunks of kMxRows rows.  Thread t takes group
+// (chunk * 256 + t) of each of the chunk's rows: coalesced 16-byte loads
+// along a row.  along == 0: scale blocks run along a row
+// (S[r * lds + c / 32]); along == 1: down a column (S[(r / 32) * lds + c]).
+struct MxJobs {
+  MxJob job[2];
+  long long blocks0, blocks;  // blocks of job 0, of both
+};
+
+__host__ __device__ __forceinline__ long long mx_chunks_x(const MxJob& j) { return ((j.cols + 15) / 16 + 255) / 256; }
+
+__global__ void __launch_bounds__(256) mx_dequant_kernel(const __grid_constant__ MxJobs jobs) {
+  for (long long b = blockIdx.x; b < jobs.blocks; b += gridDim.x) {
+    const bool second = b >= jobs.blocks0;
+    const MxJob& j = jobs.job[second ? 1 : 0];
+    const long long lb = second ? b - jobs.blocks0 : b;
+    const long long cx = mx_chunks_x(j);
+    const long long r0 = (lb / cx) * kMxRows;
+    const long long gi = (lb % cx) * 256 + threadIdx.x;
+    const long long c0 = gi * 16;
+    if (c0 >= j.cols) continue;
+    MxGroup g[kMxRows];
+    bool whole[kMxRows];
+#pragma unroll
+    for (int k = 0; k < kMxRows; ++k) {
+      const long long r = r0 + k;
+      whole[k] = false;
+      if (r < j.rows) {
+        const uint8_t* src = j.X + r * j.ldx + c0;
+        whole[k] = c0 + 16 <= j.cols && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(j.Y + r * j.ldy + c0) & 15u) == 0);
+        mx_load(src, j.S, j.lds, j.along, r, c0, j.cols, whole[k], g[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kMxRows; ++k) {
+      if (r0 + k >= j.rows) break;
+      uint16_t* dst = j.Y + (r0 + k) * j.ldy + c0;
+      if (j.fmt == 0)
+        mx_group<0>(dst, c0, j.cols, whole[k], g[k], j.along);
+      else
+        mx_group<1>(dst, c0, j.cols, whole[k], g[k], j.along);
     }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_mx_dequant(const uint8_t* X, long long ldx, const uint8_t* S, long long lds, int fmt,
-                              int along, long long rows, long long cols, uint16_t* Y, long long ldy,
-                              int num_sms, cudaStream_t stream) {
-  const long long groups = rows * ((cols + 15) / 16);
-  if (groups == 0) return cudaSuccess;
-  // a few waves of resident blocks (8 x 256 threads per SM), grid-strided
-  const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 1) * 8 * 4;
-  const long long want = (groups + 255) / 256;
-  const int grid = static_cast<int>(want < cap ? want : cap);
-  mx_dequant_kernel<<<grid, 256, 0, stream>>>(X, ldx, S, lds, fmt, along, rows, cols, Y, ldy);
+cudaError_t launch_mx_dequant(const MxJob* jobs, int njobs, int num_sms, cudaStream_t stream) {
+  MxJobs p{};
+  long long counts[2] = {0, 0};
+  for (int i = 0; i < njobs && i < 2; ++i) {
+    p.job[i] = jobs[i];
+    if (jobs[i].rows > 0 && jobs[i].cols > 0)
+      counts[i] = (jobs[i].rows + kMxRows - 1) / kMxRows * mx_chunks_x(jobs[i]);
+  }
+  p.blocks0 = counts[0];
+  p.blocks = counts[0] + counts[1];
+  if (p.blocks == 0) return cudaSuccess;
+  // eight resident blocks of 256 threads per SM; up to 16 waves of them in
+  // one grid, block-strided beyond
+  const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 1) * 8 * 16;
+  const unsigned grid = static_cast<unsigned>(p.blocks < cap ? p.blocks : cap);
+  mx_dequant_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -417,12 +417,16 @@ def matmul_mx(A: torch.Tensor, scale_a: torch.Tensor, B: torch.Tensor, scale_b: 
 
 
 def mx_to_bf16(X: torch.Tensor, S: torch.Tensor, fmt: str = "e4m3", along: str = "row",
-               handle: Handle | None = None) -> torch.Tensor:
+               handle: Handle | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
     """bf16 values of a block-scaled 8-bit matrix X (uint8, rows x cols) with
     E8M0 scales S: blocks of 32 along each row (S rows x ceil(cols/32)) or
-    down each column (S ceil(rows/32) x cols)."""
+    down each column (S ceil(rows/32) x cols).  `out`, if given, is a bf16
+    rows x cols tensor on X's device with unit column stride."""
     rows, cols = X.shape
-    Y = torch.empty((rows, cols), dtype=torch.bfloat16, device=X.device)
+    if out is not None and (out.dtype != torch.bfloat16 or tuple(out.shape) != (rows, cols)
+                            or out.device != X.device or (cols > 1 and out.stride(1) != 1)):
+        raise ValueError("out must be a bf16 tensor of X's shape and device with unit column stride")
+    Y = out if out is not None else torch.empty((rows, cols), dtype=torch.bfloat16, device=X.device)
     h = handle if handle is not None else default_handle()
     h.set_stream(torch.cuda.current_stream(X.device).cuda_stream)
     s = lib().fgemm_mx_to_bf16(h.ptr, rows, cols, X.data_ptr(), X.stride(0) if rows > 1 else max(cols, 1),
