@@ -928,6 +928,7 @@ fgemm_status_t fgemm_mx_to_bf16(fgemm_handle_t h, int64_t rows, int64_t cols, co
   if (along != 0 && along != 1) return set_msg(h, FGEMM_ERR_INVALID_ARG, "along must be 0 or 1");
   if (rows < 0 || cols < 0) return set_msg(h, FGEMM_ERR_INVALID_ARG, "negative dimension");
   if (rows == 0 || cols == 0) return FGEMM_OK;
+  if (cols > (int64_t{1} << 31) - 1) return set_msg(h, FGEMM_ERR_INVALID_ARG, "cols above 2^31 - 1");
   if (!X || !S || !Y) return set_msg(h, FGEMM_ERR_INVALID_ARG, "X, S and Y must not be NULL");
   const int64_t need_s = along == 0 ? (cols + 31) / 32 : cols;
   if (ldx < cols || ldy < cols || lds < need_s)

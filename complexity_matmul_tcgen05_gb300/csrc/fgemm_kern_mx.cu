@@ -98,16 +98,31 @@ __device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t p, uint32_t eb) {
   return ((mag << Fp8Layout<FMT>::kShift) + (eb & nonzero)) | ((p & 0x00800080u) << 8);
 }
 
-// One 16-column group: its 16 bytes and the 16 scales that apply to them,
-// both packed four to a word.
+// One 16-column group: its 16 bytes and the scales that apply to them, both
+// packed four to a word (scales along rows: only s[0], the group's one scale).
 struct MxGroup {
   uint32_t w[4];
   uint32_t s[4];
 };
 
-__device__ __forceinline__ void mx_load(const uint8_t* __restrict__ src, const uint8_t* __restrict__ S,
-                                        long long lds, int along, long long r, long long c0,
-                                        long long cols, bool whole, MxGroup& g) {
+// A job as the kernel sees it: the matrix, whether every full group's
+// element, output and (down columns) scale rows are 16-byte aligned, and its
+// count of 16-column groups per row.
+struct MxJobDev {
+  const uint8_t* X;
+  const uint8_t* S;
+  uint16_t* Y;
+  long long ldx, lds, ldy, rows;
+  int cols, groups, fmt, along, vec, svec;
+};
+
+struct MxLaunch {
+  MxJobDev job[2];
+};
+
+template <int ALONG>
+__device__ __forceinline__ void mx_load(const MxJobDev& j, long long r, int c0, bool whole, MxGroup& g) {
+  const uint8_t* src = j.X + r * j.ldx + c0;
   if (whole) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
     g.w[0] = v.x;
@@ -120,19 +135,14 @@ __device__ __forceinline__ void mx_load(const uint8_t* __restrict__ src, const u
       g.w[q] = 0;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        if (c0 + 4 * q + i < cols) g.w[q] |= static_cast<uint32_t>(src[4 * q + i]) << (8 * i);
+        if (c0 + 4 * q + i < j.cols) g.w[q] |= static_cast<uint32_t>(src[4 * q + i]) << (8 * i);
     }
   }
-  // one byte (a 16-column group lies in one 32-block of its row) or 16
-  // consecutive bytes (one per column)
-  if (along == 0) {
-    const uint32_t ev = __ldg(S + r * lds + (c0 >> 5));
-    const uint32_t rep = ev * 0x01010101u;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) g.s[q] = rep;
-  } else {
-    const uint8_t* srow = S + (r >> 5) * lds + c0;
-    if (whole && ((reinterpret_cast<uintptr_t>(srow) & 15u) == 0)) {
+  if (ALONG == 0) {  // a 16-column group lies in one 32-block of its row
+    g.s[0] = __ldg(j.S + r * j.lds + (c0 >> 5));
+  } else {           // one scale per column, from the row of the 32-block
+    const uint8_t* srow = j.S + (r >> 5) * j.lds + c0;
+    if (whole && j.svec) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(srow));
       g.s[0] = v.x;
       g.s[1] = v.y;
@@ -145,7 +155,7 @@ __device__ __forceinline__ void mx_load(const uint8_t* __restrict__ src, const u
         g.s[q] = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint32_t e = c0 + 4 * q + i < cols ? __ldg(srow + 4 * q + i) : 127u;
+          const uint32_t e = c0 + 4 * q + i < j.cols ? __ldg(srow + 4 * q + i) : 127u;
           g.s[q] |= e << (8 * i);
         }
       }
@@ -153,8 +163,7 @@ __device__ __forceinline__ void mx_load(const uint8_t* __restrict__ src, const u
   }
 }
 
-__device__ __forceinline__ void mx_store(uint16_t* dst, long long c0, long long cols, bool whole,
-                                         const uint32_t (&o)[8]) {
+__device__ __forceinline__ void mx_store(uint16_t* dst, int c0, int cols, bool whole, const uint32_t (&o)[8]) {
   if (whole) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
     d4[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -169,14 +178,14 @@ __device__ __forceinline__ void mx_store(uint16_t* dst, long long c0, long long 
 // The general path for a group that holds a special element or scale: each
 // value through fp32 (or fp64 near the ends of bf16's range).  Kept out of
 // line so that the common path stays small.
-__device__ __noinline__ void mx_group_general(uint16_t* dst, long long c0, long long cols, bool whole,
-                                              MxGroup g, int fmt) {
+__device__ __noinline__ void mx_group_general(uint16_t* dst, int c0, int cols, bool whole, MxGroup g, int fmt,
+                                              int along) {
   const __nv_fp8_interpretation_t interp = fmt == 0 ? __NV_E4M3 : __NV_E5M2;
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint32_t x = (g.w[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-    const uint8_t e = static_cast<uint8_t>(g.s[i >> 2] >> (8 * (i & 3)));
+    const uint8_t e = static_cast<uint8_t>(along == 0 ? g.s[0] : g.s[i >> 2] >> (8 * (i & 3)));
     const float f = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(x), interp)));
     const uint32_t v = scaled_bf16(f, e);
     if (i & 1)
@@ -189,22 +198,23 @@ __device__ __noinline__ void mx_group_general(uint16_t* dst, long long c0, long 
 
 // One group: the integer path when no element is special and every scale
 // lies in the range where all results are bf16 normals, else the general one.
-template <int FMT>
-__device__ __forceinline__ void mx_group(uint16_t* dst, long long c0, long long cols, bool whole,
-                                         const MxGroup& g, int along) {
+template <int FMT, int ALONG>
+__device__ __forceinline__ void mx_group(uint16_t* dst, int c0, int cols, bool whole, const MxGroup& g) {
   using L = Fp8Layout<FMT>;
   uint32_t bad = 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) bad |= fp8_specials4<FMT>(g.w[q]);
-  if (along == 0) {
-    const uint32_t e = g.s[0] & 0xFFu;
-    if (e < L::kScaleLo || e > L::kScaleHi) bad |= 0x80u;
+  uint32_t eb_row = 0;  // along rows: the group's exponent offset in both lanes
+  if (ALONG == 0) {
+    const uint32_t e = g.s[0];
+    if (e - L::kScaleLo > L::kScaleHi - L::kScaleLo) bad |= 0x80u;
+    eb_row = ((e - L::kBias) << 7) * 0x00010001u;
   } else {
 #pragma unroll
     for (int q = 0; q < 4; ++q) bad |= bytes_outside4(g.s[q], L::kScaleLo, L::kScaleHi);
   }
   if (bad & 0x80808080u) {
-    mx_group_general(dst, c0, cols, whole, g, FMT);
+    mx_group_general(dst, c0, cols, whole, g, FMT, ALONG);
     return;
   }
   uint32_t o[8];
@@ -214,80 +224,77 @@ __device__ __forceinline__ void mx_group(uint16_t* dst, long long c0, long long 
     for (int h = 0; h < 2; ++h) {
       const uint32_t sel = h == 0 ? 0x4140u : 0x4342u;  // bytes 2h, 2h+1 into the two lanes
       const uint32_t p = __byte_perm(g.w[q], 0, sel);
-      const uint32_t eb = (__byte_perm(g.s[q], 0, sel) << 7) - (L::kBias << 7) * 0x00010001u;
+      const uint32_t eb =
+          ALONG == 0 ? eb_row : (__byte_perm(g.s[q], 0, sel) << 7) - (L::kBias << 7) * 0x00010001u;
       o[2 * q + h] = fp8x2_to_bf16x2<FMT>(p, eb);
     }
   }
   mx_store(dst, c0, cols, whole, o);
 }
 
-constexpr int kMxRows = 1;  // rows per thread (more held more registers and ran slower)
+// Thread t of block (x, y, z) converts 16-column group x * 256 + t of rows
+// y, y + gridDim.y, ... of job z: coalesced 16-byte loads along each row.
+// along == 0: scale blocks run along a row (S[r * lds + c / 32]);
+// along == 1: they run down a column (S[(r / 32) * lds + c]).
+template <int FMT, int ALONG>
+__device__ __forceinline__ void mx_rows(const MxJobDev& j, int gi) {
+  const int c0 = gi * 16;
+  const bool whole = j.vec && c0 + 16 <= j.cols;
+  for (long long r = blockIdx.y; r < j.rows; r += gridDim.y) {
+    MxGroup g;
+    mx_load<ALONG>(j, r, c0, whole, g);
+    mx_group<FMT, ALONG>(j.Y + r * j.ldy + c0, c0, j.cols, whole, g);
+  }
+}
 
-// Up to two matrices in one launch.  Block b of the flat grid works on job 0
-// while b < blocks0, else on job 1; within a job, blocks walk column chunks
-// of 256 groups (x) inside row chunks of kMxRows rows.  Thread t takes group
-// (chunk * 256 + t) of each of the chunk's rows: coalesced 16-byte loads
-// along a row.  along == 0: scale blocks run along a row
-// (S[r * lds + c / 32]); along == 1: down a column (S[(r / 32) * lds + c]).
-struct MxJobs {
-  MxJob job[2];
-  long long blocks0, blocks;  // blocks of job 0, of both
-};
-
-__host__ __device__ __forceinline__ long long mx_chunks_x(const MxJob& j) { return ((j.cols + 15) / 16 + 255) / 256; }
-
-__global__ void __launch_bounds__(256) mx_dequant_kernel(const __grid_constant__ MxJobs jobs) {
-  for (long long b = blockIdx.x; b < jobs.blocks; b += gridDim.x) {
-    const bool second = b >= jobs.blocks0;
-    const MxJob& j = jobs.job[second ? 1 : 0];
-    const long long lb = second ? b - jobs.blocks0 : b;
-    const long long cx = mx_chunks_x(j);
-    const long long r0 = (lb / cx) * kMxRows;
-    const long long gi = (lb % cx) * 256 + threadIdx.x;
-    const long long c0 = gi * 16;
-    if (c0 >= j.cols) continue;
-    MxGroup g[kMxRows];
-    bool whole[kMxRows];
-#pragma unroll
-    for (int k = 0; k < kMxRows; ++k) {
-      const long long r = r0 + k;
-      whole[k] = false;
-      if (r < j.rows) {
-        const uint8_t* src = j.X + r * j.ldx + c0;
-        whole[k] = c0 + 16 <= j.cols && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) &&
-                   ((reinterpret_cast<uintptr_t>(j.Y + r * j.ldy + c0) & 15u) == 0);
-        mx_load(src, j.S, j.lds, j.along, r, c0, j.cols, whole[k], g[k]);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kMxRows; ++k) {
-      if (r0 + k >= j.rows) break;
-      uint16_t* dst = j.Y + (r0 + k) * j.ldy + c0;
-      if (j.fmt == 0)
-        mx_group<0>(dst, c0, j.cols, whole[k], g[k], j.along);
-      else
-        mx_group<1>(dst, c0, j.cols, whole[k], g[k], j.along);
-    }
+// Six resident blocks per SM (at most 40 registers a thread) keep more loads
+// in flight than the unconstrained 56-register build.
+__global__ void __launch_bounds__(256, 6) mx_dequant_kernel(const __grid_constant__ MxLaunch L) {
+  const MxJobDev& j = L.job[blockIdx.z];
+  const int gi = blockIdx.x * 256 + threadIdx.x;
+  if (gi >= j.groups) return;
+  switch (j.fmt * 2 + j.along) {
+    case 0: mx_rows<0, 0>(j, gi); break;
+    case 1: mx_rows<0, 1>(j, gi); break;
+    case 2: mx_rows<1, 0>(j, gi); break;
+    default: mx_rows<1, 1>(j, gi); break;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_mx_dequant(const MxJob* jobs, int njobs, int num_sms, cudaStream_t stream) {
-  MxJobs p{};
-  long long counts[2] = {0, 0};
+  (void)num_sms;
+  MxLaunch p{};
+  int n = 0;
+  long long max_groups = 0, max_rows = 0;
   for (int i = 0; i < njobs && i < 2; ++i) {
-    p.job[i] = jobs[i];
-    if (jobs[i].rows > 0 && jobs[i].cols > 0)
-      counts[i] = (jobs[i].rows + kMxRows - 1) / kMxRows * mx_chunks_x(jobs[i]);
+    const MxJob& a = jobs[i];
+    if (a.rows <= 0 || a.cols <= 0) continue;
+    if (a.cols > (1LL << 31) - 1) return cudaErrorInvalidValue;
+    MxJobDev& d = p.job[n++];
+    d.X = a.X;
+    d.S = a.S;
+    d.Y = a.Y;
+    d.ldx = a.ldx;
+    d.lds = a.lds;
+    d.ldy = a.ldy;
+    d.rows = a.rows;
+    d.cols = static_cast<int>(a.cols);
+    d.groups = static_cast<int>((a.cols + 15) / 16);
+    d.fmt = a.fmt;
+    d.along = a.along;
+    d.vec = (reinterpret_cast<uintptr_t>(a.X) % 16 == 0) && (a.ldx % 16 == 0) &&
+            (reinterpret_cast<uintptr_t>(a.Y) % 16 == 0) && (a.ldy % 8 == 0);
+    d.svec = (reinterpret_cast<uintptr_t>(a.S) % 16 == 0) && (a.lds % 16 == 0);
+    max_groups = d.groups > max_groups ? d.groups : max_groups;
+    max_rows = a.rows > max_rows ? a.rows : max_rows;
   }
-  p.blocks0 = counts[0];
-  p.blocks = counts[0] + counts[1];
-  if (p.blocks == 0) return cudaSuccess;
-  // eight resident blocks of 256 threads per SM; up to 16 waves of them in
-  // one grid, block-strided beyond
-  const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 1) * 8 * 16;
-  const unsigned grid = static_cast<unsigned>(p.blocks < cap ? p.blocks : cap);
+  if (n == 0) return cudaSuccess;
+  // x: 256 groups per block; y: one row per block row, at most 65535
+  // (row-strided beyond); z: the job
+  const dim3 grid(static_cast<unsigned>((max_groups + 255) / 256),
+                  static_cast<unsigned>(max_rows < 65535 ? max_rows : 65535), static_cast<unsigned>(n));
   mx_dequant_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -230,6 +230,9 @@ typedef enum { FGEMM_FP8_E4M3 = 0, FGEMM_FP8_E5M2 = 1 } fgemm_fp8_format_t;
  * 32 along each row (along 0, S is rows x ceil(cols/32)) or down each column
  * (along 1, S is ceil(rows/32) x cols). Each value is rounded once to bf16
  * (exact while in bf16's normal range). Asynchronous on the handle's stream.
+ * Errors: FGEMM_ERR_INVALID_ARG for a bad format or along, a negative size,
+ * cols above 2^31 - 1, NULL pointers or leading dimensions below the row
+ * lengths; FGEMM_ERR_ALIGNMENT for an odd Y address.
  */
 fgemm_status_t fgemm_mx_to_bf16(fgemm_handle_t h, int64_t rows, int64_t cols,
                                 const void* X, int64_t ldx, const void* S, int64_t lds,
