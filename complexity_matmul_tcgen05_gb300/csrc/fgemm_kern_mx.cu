@@ -8,17 +8,18 @@
 // that step: it writes every value x * 2^(e - 127) as bf16, which the bf16
 // tensor-core GEMM then consumes.
 //
-// Exactness: an 8-bit float has at most 4 significant bits, so while
-// x * 2^(e - 127) stays in bf16's normal range the fp32 product and its bf16
-// cast are exact.  Outside it (a subnormal or an overflowing result) the
-// product is formed in double precision and rounded to bf16 once
-// (round-to-nearest-even), so the value equals the exact value rounded once.
-// NaN elements or scales give NaN; E5M2 infinities stay infinite.
+// Exactness: an 8-bit float has at most 4 significant bits and a magnitude
+// in [2^-16, 2^16) or zero, so its fp16 and fp32 forms are exact, and so is
+// the fp32 product x * 2^(e - 127) for every scale below 255: the smallest,
+// 2^-143, is a multiple of fp32's subnormal step 2^-149, and a product of
+// 2^128 or more is infinite in fp32 and rounds to infinity in bf16 as well.
+// The cast to bf16 (round to nearest even) is therefore the one rounding:
+// each value is the exact value rounded once.  NaN elements or scales give
+// NaN, E5M2 infinities stay infinite, zeros keep their sign.
 //
 // Memory-bound: a thread converts a group of 16 consecutive bytes (one
-// 16-byte load, two 16-byte stores, the group's scales in one load).  Groups
-// with no special element or scale (the usual case) take a packed integer
-// path, two elements per 32-bit word; the rest go through fp32.
+// 16-byte load, two 16-byte stores, the group's scales in one load), two
+// elements at a time through fp16 and fp32 and one packed rounding to bf16.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -32,50 +33,12 @@ namespace fgemm {
 
 namespace {
 
-
-// x * 2^(e - 127) rounded once to bf16 (the general path).
+// x * 2^(e - 127) rounded once to bf16, for any scale (the general path).
 __device__ __forceinline__ uint16_t scaled_bf16(float x, uint8_t e) {
   if (e == 255u) return 0x7FC0u;  // NaN scale
-  // 2^(e - 127) as fp32 (normal for e >= 1, the subnormal 2^-127 for e = 0)
+  // 2^(e - 127) as fp32: normal for e >= 1, the subnormal 2^-127 for e = 0
   const float s = e == 0 ? __int_as_float(1 << 22) : __int_as_float(static_cast<int>(e) << 23);
-  const float f = x * s;
-  const float af = fabsf(f);
-  if (x == 0.0f || (af >= 1.1754943508222875e-38f && af <= 3.3895313892515355e+38f) || !isfinite(x)) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(f));  // exact: at most 4 significant bits
-  }
-  // subnormal or overflowing result: the exact product, rounded once
-  const double d = static_cast<double>(x) * __longlong_as_double(static_cast<long long>(e - 127 + 1023) << 52);
-  return __bfloat16_as_ushort(__double2bfloat16(d));
-}
-
-// The bit layouts (CS336 Lecture 05 notes, "Page 27"): E4M3 has 4 exponent
-// bits with bias 7 and 3 mantissa bits, and its only specials are the NaNs
-// 0x7F / 0xFF; E5M2 has 5 exponent bits with bias 15 and 2 mantissa bits, and
-// exponent 31 holds infinities and NaNs.  A bf16 has 8 exponent bits (bias
-// 127) and 7 mantissa bits.
-template <int FMT>
-struct Fp8Layout {
-  static constexpr uint32_t kBias = FMT == 0 ? 7u : 15u;
-  static constexpr int kShift = FMT == 0 ? 4 : 5;  // 7 - mantissa bits
-  static constexpr uint32_t kExpMask4 = FMT == 0 ? 0x78787878u : 0x7C7C7C7Cu;
-  static constexpr uint32_t kManMask4 = FMT == 0 ? 0x07070707u : 0x03030303u;
-  // Scales e for which every normal element lands on a bf16 normal:
-  // exponent x_exp - bias + e in [1, 254] for x_exp over the normal range
-  // (E4M3 1..15, E5M2 1..30).
-  static constexpr uint32_t kScaleLo = FMT == 0 ? 7u : 15u;
-  static constexpr uint32_t kScaleHi = FMT == 0 ? 246u : 239u;
-};
-
-// Bit 7 of each byte of the result is set where that byte of `w` is an
-// 8-bit subnormal or a NaN / infinity pattern (the elements the integer path
-// below does not take); the other bits are junk.
-template <int FMT>
-__device__ __forceinline__ uint32_t fp8_specials4(uint32_t w) {
-  using L = Fp8Layout<FMT>;
-  const uint32_t exp_nz = (w & L::kExpMask4) + L::kExpMask4;
-  const uint32_t man_nz = (w & L::kManMask4) + 0x7F7F7F7Fu;
-  const uint32_t top = FMT == 0 ? (w & 0x7F7F7F7Fu) + 0x01010101u : (w & 0x7C7C7C7Cu) + 0x04040404u;
-  return (man_nz & ~exp_nz) | top;
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x * s));  // x * s is exact
 }
 
 // Bit 7 of each byte set where that byte of `s` lies outside [lo, hi]
@@ -85,17 +48,6 @@ __device__ __forceinline__ uint32_t bytes_outside4(uint32_t s, uint32_t lo, uint
   const uint32_t ns = ~s;
   const uint32_t le_hi = ((ns | 0x80808080u) - (255u - hi) * 0x01010101u) | ns;
   return ~(ge_lo & le_hi);
-}
-
-// Two elements in the low bytes of the 16-bit lanes of `p`, their bf16
-// exponent offsets ((e - bias) << 7) in the lanes of `eb`: a normal element
-// keeps its sign and mantissa and has its exponent re-biased by the scale
-// (bf16 exponent = x_exp - bias + e), a zero keeps only its sign.
-template <int FMT>
-__device__ __forceinline__ uint32_t fp8x2_to_bf16x2(uint32_t p, uint32_t eb) {
-  const uint32_t mag = p & 0x007F007Fu;
-  const uint32_t nonzero = (((mag + 0x007F007Fu) & 0x00800080u) * 0xFFu);  // 0x7F80 per nonzero lane
-  return ((mag << Fp8Layout<FMT>::kShift) + (eb & nonzero)) | ((p & 0x00800080u) << 8);
 }
 
 // One 16-column group: its 16 bytes and the scales that apply to them, both
@@ -175,9 +127,8 @@ __device__ __forceinline__ void mx_store(uint16_t* dst, int c0, int cols, bool w
   }
 }
 
-// The general path for a group that holds a special element or scale: each
-// value through fp32 (or fp64 near the ends of bf16's range).  Kept out of
-// line so that the common path stays small.
+// The general path, for a group with a scale of 0 or 255: one value at a
+// time.  Kept out of line so that the common path stays small.
 __device__ __noinline__ void mx_group_general(uint16_t* dst, int c0, int cols, bool whole, MxGroup g, int fmt,
                                               int along) {
   const __nv_fp8_interpretation_t interp = fmt == 0 ? __NV_E4M3 : __NV_E5M2;
@@ -196,37 +147,43 @@ __device__ __noinline__ void mx_group_general(uint16_t* dst, int c0, int cols, b
   mx_store(dst, c0, cols, whole, o);
 }
 
-// One group: the integer path when no element is special and every scale
-// lies in the range where all results are bf16 normals, else the general one.
+// One group through fp32: every 8-bit value (at most 4 significant bits) is
+// exact in fp16 and fp32, and x * 2^(e - 127) is exact in fp32 for e in
+// [1, 254] (the smallest product 2^-142 lies above fp32's subnormal step and
+// an overflow is infinite in both fp32 and bf16), so the one rounding to bf16
+// is the only one.  Zeros, infinities and NaNs pass through the multiply.
+// Scales 0 and 255 take the general path.
 template <int FMT, int ALONG>
 __device__ __forceinline__ void mx_group(uint16_t* dst, int c0, int cols, bool whole, const MxGroup& g) {
-  using L = Fp8Layout<FMT>;
-  uint32_t bad = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) bad |= fp8_specials4<FMT>(g.w[q]);
-  uint32_t eb_row = 0;  // along rows: the group's exponent offset in both lanes
+  uint32_t bad;
   if (ALONG == 0) {
-    const uint32_t e = g.s[0];
-    if (e - L::kScaleLo > L::kScaleHi - L::kScaleLo) bad |= 0x80u;
-    eb_row = ((e - L::kBias) << 7) * 0x00010001u;
+    bad = (g.s[0] - 1u > 253u) ? 1u : 0u;
   } else {
+    bad = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) bad |= bytes_outside4(g.s[q], L::kScaleLo, L::kScaleHi);
+    for (int q = 0; q < 4; ++q) bad |= bytes_outside4(g.s[q], 1u, 254u);
+    bad &= 0x80808080u;
   }
-  if (bad & 0x80808080u) {
+  if (bad) {
     mx_group_general(dst, c0, cols, whole, g, FMT, ALONG);
     return;
   }
+  const __nv_fp8_interpretation_t interp = FMT == 0 ? __NV_E4M3 : __NV_E5M2;
+  const float s_row = __uint_as_float(g.s[0] << 23);
   uint32_t o[8];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint32_t sel = h == 0 ? 0x4140u : 0x4342u;  // bytes 2h, 2h+1 into the two lanes
-      const uint32_t p = __byte_perm(g.w[q], 0, sel);
-      const uint32_t eb =
-          ALONG == 0 ? eb_row : (__byte_perm(g.s[q], 0, sel) << 7) - (L::kBias << 7) * 0x00010001u;
-      o[2 * q + h] = fp8x2_to_bf16x2<FMT>(p, eb);
+      const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>(g.w[q] >> (16 * h));
+      const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, interp)));
+      float s0 = s_row, s1 = s_row;
+      if (ALONG == 1) {
+        s0 = __uint_as_float(((g.s[q] >> (16 * h)) & 0xFFu) << 23);
+        s1 = __uint_as_float(((g.s[q] >> (16 * h + 8)) & 0xFFu) << 23);
+      }
+      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s0, f.y * s1);
+      o[2 * q + h] = *reinterpret_cast<const uint32_t*>(&b);
     }
   }
   mx_store(dst, c0, cols, whole, o);
@@ -247,10 +204,7 @@ __device__ __forceinline__ void mx_rows(const MxJobDev& j, int gi) {
   }
 }
 
-// Six resident blocks per SM (at most 40 registers a thread) keep more loads
-// in flight than the unconstrained 56-register build.
-__global__ void __launch_bounds__(256, 6) mx_dequant_kernel(const __grid_constant__ MxLaunch L) {
-  const MxJobDev& j = L.job[blockIdx.z];
+__device__ __forceinline__ void mx_job(const MxJobDev& j) {
   const int gi = blockIdx.x * 256 + threadIdx.x;
   if (gi >= j.groups) return;
   switch (j.fmt * 2 + j.along) {
@@ -259,6 +213,17 @@ __global__ void __launch_bounds__(256, 6) mx_dequant_kernel(const __grid_constan
     case 2: mx_rows<1, 0>(j, gi); break;
     default: mx_rows<1, 1>(j, gi); break;
   }
+}
+
+// Six resident blocks per SM (at most 40 registers a thread) keep more loads
+// in flight than the unconstrained 56-register build.  The job is picked by
+// a branch rather than an index so that its fields are read at fixed
+// parameter offsets.
+__global__ void __launch_bounds__(256, 6) mx_dequant_kernel(const __grid_constant__ MxLaunch L) {
+  if (blockIdx.z == 0)
+    mx_job(L.job[0]);
+  else
+    mx_job(L.job[1]);
 }
 
 }  // namespace

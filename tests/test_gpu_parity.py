@@ -523,6 +523,44 @@ def test_mx_to_bf16_every_pattern_and_scale(fmt, along):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("along", ["row", "col"])
+@pytest.mark.parametrize("rows,cols,offset", [(96, 1024, 0), (70, 1000, 0), (65, 515, 1)])
+def test_mx_to_bf16_quantised_data_with_planted_specials(fmt, along, rows, cols, offset):
+    """Gaussian values cast to 8 bits (almost every 16-column group is plain
+    normals and zeros) with a few planted subnormals, NaN / infinity patterns,
+    zeros of both signs and out-of-range scales; ragged column counts and
+    (offset 1) rows that are not 16-byte aligned.  Bit for bit against the
+    oracle."""
+    g = torch.Generator().manual_seed(105)
+    sigma, f8 = (64.0, torch.float8_e4m3fn) if fmt == "e4m3" else (8192.0, torch.float8_e5m2)
+    full = (torch.randn((rows, cols + offset), generator=g) * sigma).to(f8).view(torch.uint8)
+    n = rows * (cols + offset)
+    flat = full.view(-1)
+    idx = torch.randint(0, n, (40,), generator=g)
+    sub = 0x05 if fmt == "e4m3" else 0x02            # 8-bit subnormals
+    nan = 0x7F if fmt == "e4m3" else 0x7E
+    plant = torch.tensor([sub, sub | 0x80, nan, 0x00, 0x80] * 8, dtype=torch.uint8)
+    flat[idx] = plant
+    if fmt == "e5m2":
+        flat[idx[:4]] = torch.tensor([0x7C, 0xFC, 0x7F, 0x01], dtype=torch.uint8)   # +-inf, NaN, subnormal
+    X = full.to(DEV)[:, offset:]
+    kb = (cols + 31) // 32 if along == "row" else (rows + 31) // 32
+    shape = (rows, kb) if along == "row" else (kb, cols)
+    S = torch.randint(100, 150, shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    sflat = S.view(-1)
+    sidx = torch.randint(0, sflat.numel(), (6,), generator=g)
+    sflat[sidx] = torch.tensor([0, 3, 250, 255, 254, 1], dtype=torch.uint8)
+    S = S.to(DEV)
+    Y = fgemm.mx_to_bf16(X, S, fmt, along)
+    torch.cuda.synchronize()
+    ref = oracle.mx_values(_np(X), _np(S), fmt, along)
+    got = values(Y)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(gpu_bits(Y)[ok], oracle.encode(ref[ok], "bf16"))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 def test_mx_values_exact_through_identity(fmt):
     """C = A x I through the whole MX product: every entry is A's value rounded
     once to bf16, bit for bit (scales that keep the values in bf16's normal
