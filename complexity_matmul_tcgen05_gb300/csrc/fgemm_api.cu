@@ -241,18 +241,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 struct TmapKey {
   const void* ptr;
   uint64_t inner, outer, ld;
-  uint32_t box_outer;
+  uint32_t box_inner, box_outer;
   int bf16;
   bool operator==(const TmapKey& o) const {
     return ptr == o.ptr && inner == o.inner && outer == o.outer && ld == o.ld &&
-           box_outer == o.box_outer && bf16 == o.bf16;
+           box_inner == o.box_inner && box_outer == o.box_outer && bf16 == o.bf16;
   }
 };
 struct TmapKeyHash {
   size_t operator()(const TmapKey& k) const {
     size_t h = std::hash<const void*>()(k.ptr);
     h ^= std::hash<uint64_t>()(k.inner * 1000003u + k.outer) + 0x9e3779b97f4a7c15ull + (h << 6);
-    h ^= std::hash<uint64_t>()(k.ld * 31u + k.box_outer * 7u + k.bf16) + (h << 6) + (h >> 2);
+    h ^= std::hash<uint64_t>()(k.ld * 31u + k.box_outer * 7u + k.box_inner * 131u + k.bf16) + (h << 6) +
+         (h >> 2);
     return h;
   }
 };
@@ -329,9 +330,13 @@ fgemm_status_t cuda_fail(fgemm_handle_t h, cudaError_t e, const char* what) {
   return set_msg(h, FGEMM_ERR_CUDA, t);
 }
 
+// A 2D map of 16-bit elements (inner x outer, row pitch ld elements) with
+// boxes of box_inner x box_outer.  Boxes 64 elements wide (128-byte rows)
+// use the 128-byte swizzle, 32 wide the 64-byte one.
 fgemm_status_t encode_tmap(fgemm_handle_t h, CUtensorMap* out, const void* ptr, uint64_t inner,
-                           uint64_t outer, uint64_t ld, uint32_t box_outer, int bf16) {
-  TmapKey key{ptr, inner, outer, ld, box_outer, bf16};
+                           uint64_t outer, uint64_t ld, uint32_t box_outer, int bf16,
+                           uint32_t box_inner = 64) {
+  TmapKey key{ptr, inner, outer, ld, box_inner, box_outer, bf16};
   auto it = h->tmaps.find(key);
   if (it != h->tmaps.end()) {
     *out = it->second;
@@ -342,12 +347,12 @@ fgemm_status_t encode_tmap(fgemm_handle_t h, CUtensorMap* out, const void* ptr, 
   CUtensorMap m;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {ld * 2};
-  const cuuint32_t box[2] = {64, box_outer};
+  const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(&m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   box_inner == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return set_msg(h, FGEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(r) + ")");
   if (h->tmaps.size() > 256) h->tmaps.clear();
@@ -861,6 +866,10 @@ fgemm_status_t matmul_impl(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, co
   if (bm == 256) {
     const int fit = fgemm::gemm_pair_clusters_fit(bn);
     if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the CTA-pair launch");
+    // C leaves this kernel by TMA stores of 32 x 32 boxes
+    s = encode_tmap(h, &p.tmap_c, C, static_cast<uint64_t>(p.n_out), static_cast<uint64_t>(M),
+                    static_cast<uint64_t>(ldc), 32, p.is_bf16, 32);
+    if (s != FGEMM_OK) return s;
     int32_t pieces = 1;
     const int split = with_rms ? 0
                                : fgemm_model_split_tail(&h->model, units, fit, p.k_blocks, bn,

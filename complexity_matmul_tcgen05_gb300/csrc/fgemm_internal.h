@@ -93,6 +93,15 @@ FGEMM_HD inline bool work_item(int num_units, int split_tiles, int split_pieces,
   return true;
 }
 
+// How many work items `cluster` runs under the schedule of work_item.
+FGEMM_HD inline int work_item_count(int num_units, int split_tiles, int split_pieces, int clusters,
+                                    int cluster) {
+  const bool has_piece = split_tiles > 0 && cluster < split_tiles * split_pieces;
+  const int whole = num_units - split_tiles;
+  const int count = cluster < whole ? (whole - cluster + clusters - 1) / clusters : 0;
+  return count + (has_piece ? 1 : 0);
+}
+
 // ---------------------------------------------------------------------------
 // Work schedule of the small-M kernel (stream-K).  Its tiles are 128 columns
 // of C (all M <= 64 rows); the K blocks of all tiles, laid end to end tile
@@ -145,6 +154,7 @@ FGEMM_HD inline long long stream_k_slot(int tiles, int k_blocks, int ctas, int u
 struct KernelParams {
   CUtensorMap tmap_a;  // A: inner dim K, outer M, box {64, 128}, 128B swizzle
   CUtensorMap tmap_b;  // B: inner dim N, outer K, box {64, 64},  128B swizzle
+  CUtensorMap tmap_c;  // C (CTA-pair classical kernel): inner n_out, outer M, box {32, 32}, 64B swizzle
   const uint16_t* A;
   const uint16_t* B;
   uint16_t* C;

@@ -196,6 +196,47 @@ __device__ __forceinline__ void store_row32(const KernelParams& p, int row, int 
   }
 }
 
+// A warp's staging area for TMA stores of C: two 2 KB buffers of 32 rows x
+// 32 columns (64-byte rows, 16-byte chunk j of row t at chunk j ^ ((t >> 1) & 3),
+// the 64-byte swizzle of p.tmap_c), used in turn.
+struct StageOut {
+  uint8_t* ptr;   // generic address of the first buffer
+  uint32_t addr;  // shared-space address of the first buffer (1024-aligned)
+  uint32_t it;    // buffers filled so far
+};
+
+// Stores the warp's 32 rows x 32 columns (row wrow0 + lane holds v) through
+// the staging area: wait until the buffer's previous store has read it,
+// write this lane's row, then lane 0 issues the TMA store.  The tensor map
+// clips rows >= M and columns >= n_out.  Warp-collective.
+__device__ __forceinline__ void stage_store32(const KernelParams& p, StageOut& so, int wrow0, int col0,
+                                              const float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t off = (so.it & 1u) * 2048u;
+  if (lane == 0) ptx::bulk_wait_read<1>();
+  __syncwarp();
+  uint8_t* row = so.ptr + off + lane * 64;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(row + ((q ^ sw) << 4)) =
+        make_uint4(pack2(v[8 * q + 0], v[8 * q + 1], p.is_bf16), pack2(v[8 * q + 2], v[8 * q + 3], p.is_bf16),
+                   pack2(v[8 * q + 4], v[8 * q + 5], p.is_bf16), pack2(v[8 * q + 6], v[8 * q + 7], p.is_bf16));
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_2d(&p.tmap_c, so.addr + off, col0, wrow0);
+    ptx::bulk_commit();
+  }
+  ++so.it;
+}
+
+// Waits until every TMA store of the staging area has completed.
+__device__ __forceinline__ void stage_drain() {
+  if ((threadIdx.x & 31) == 0) ptx::bulk_wait<0>();
+  __syncwarp();
+}
+
 // b[j] = bias[base + min(col0 + j, n_out - 1)] (0 without a bias), for every
 // lane of the warp: each lane loads one entry and the warp exchanges them by
 // shuffles.  Warp-collective: call it outside row-dependent branches.
@@ -259,40 +300,55 @@ __device__ __forceinline__ void finish_swiglu_warp(const KernelParams& p, int co
 // block are written out, in column order within the block.  RMS selects the
 // variant with those statistics at compile time, so the plain epilogue pays
 // nothing for them.
-template <int BN, bool RMS>
+// PART selects the 32-column chunks this warp finishes: 0 all of them, 1 the
+// first half, 2 the second half (two warps sharing one tile's rows).  With a
+// staging area (so != nullptr) C goes out by TMA stores, else by each lane
+// storing its row.
+template <int BN, bool RMS, int PART>
 __device__ __forceinline__ void epilogue_classical_t(const KernelParams& p, uint32_t tbase, int row0,
-                                                     int tn, int r) {
+                                                     int tn, int r, StageOut* so) {
   const int lane = threadIdx.x & 31;
   const int row = row0 + r;
   const bool row_ok = row < p.M;
+  const int wrow0 = row - lane;
+  auto emit = [&](int col0, const float (&v)[32]) {
+    if (so) {
+      if (wrow0 < p.M && col0 < p.n_out) stage_store32(p, *so, wrow0, col0, v);
+    } else if (row_ok && col0 < p.n_out) {
+      store_row32(p, row, col0, v);
+    }
+  };
   // RMSNorm: the scale of this row (1 without statistics in), and the
   // running sum of squares of the stored outputs of one 64-column block
   const float rs = (RMS && p.sumsq_in && row_ok) ? rms_row_scale(p, row) : 1.0f;
   float ss = 0.0f;
   auto add_sumsq = [&](int c, int col0, const float (&v)[32]) {
-    if (!RMS || !p.sumsq_out) return;
+    if constexpr (RMS) {
+      if (!p.sumsq_out) return;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float q = round_out(v[j], p.is_bf16);
-      if (col0 + j < p.n_out) ss += q * q;
-    }
-    if ((c & 1) && row_ok && col0 - 32 < p.n_out) {  // end of the block [col0 - 32, col0 + 32)
-      p.sumsq_out[static_cast<size_t>((col0 - 32) >> 6) * p.M + row] = ss;
-      ss = 0.0f;
+      for (int j = 0; j < 32; ++j) {
+        const float q = round_out(v[j], p.is_bf16);
+        if (col0 + j < p.n_out) ss += q * q;
+      }
+      if ((c & 1) && row_ok && col0 - 32 < p.n_out) {  // end of the block [col0 - 32, col0 + 32)
+        p.sumsq_out[static_cast<size_t>((col0 - 32) >> 6) * p.M + row] = ss;
+        ss = 0.0f;
+      }
     }
   };
   if (p.epi == kEpiSwiglu) {
     constexpr int HALF = BN / 2;
     constexpr int CH = HALF / 32;
+    constexpr int CB = PART == 2 ? CH / 2 : 0, CE = PART == 1 ? CH / 2 : CH;
     float bg[CH], bu[CH];
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
+    for (int c = CB; c < CE; ++c) {
       const int col = min(tn * HALF + c * 32 + lane, p.n_out - 1);
       bg[c] = p.bias ? ld_bias(p, col) : 0.0f;
       bu[c] = p.bias ? ld_bias(p, p.n_out + col) : 0.0f;
     }
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
+    for (int c = CB; c < CE; ++c) {
       uint32_t gr[32], ur[32];
       ptx::tmem_ld_32x32b_x32(tbase + c * 32, gr);
       ptx::tmem_ld_32x32b_x32(tbase + HALF + c * 32, ur);
@@ -309,14 +365,15 @@ __device__ __forceinline__ void epilogue_classical_t(const KernelParams& p, uint
         const float uv = p.alpha * ua + __shfl_sync(0xFFFFFFFFu, bu[c], j);
         g[j] = silu(gv) * uv;
       }
-      if (row_ok && col0 < p.n_out) store_row32(p, row, col0, g);
+      emit(col0, g);
       add_sumsq(c, col0, g);
     }
   } else {
     constexpr int CH = BN / 32;
+    constexpr int CB = PART == 2 ? CH / 2 : 0, CE = PART == 1 ? CH / 2 : CH;
     uint32_t bl[CH];  // raw 16-bit bias values, converted when used
 #pragma unroll
-    for (int c = 0; c < CH; ++c)
+    for (int c = CB; c < CE; ++c)
       bl[c] = p.bias ? __ldg(p.bias + min(tn * BN + c * 32 + lane, p.n_out - 1)) : 0u;
     auto finish = [&](int c, const uint32_t (&ar)[32]) {
       const int col0 = tn * BN + c * 32;
@@ -329,22 +386,22 @@ __device__ __forceinline__ void epilogue_classical_t(const KernelParams& p, uint
         if (p.epi == kEpiSilu) x = silu(x);
         v[j] = x;
       }
-      if (row_ok && col0 < p.n_out) store_row32(p, row, col0, v);
+      emit(col0, v);
       add_sumsq(c, col0, v);
     };
     uint32_t ra[32], rb[32];
-    ptx::tmem_ld_32x32b_x32(tbase, ra);
+    ptx::tmem_ld_32x32b_x32(tbase + CB * 32, ra);
     ptx::tmem_wait_ld();
     ptx::tmem_regs_ready(ra);
 #pragma unroll
-    for (int c = 0; c < CH; c += 2) {  // CH is even for every tile width
+    for (int c = CB; c < CE; c += 2) {  // CB and CE are even for every tile width
       ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, rb);
       finish(c, ra);
       ptx::tmem_wait_ld();
       ptx::tmem_regs_ready(rb);
-      if (c + 2 < CH) ptx::tmem_ld_32x32b_x32(tbase + (c + 2) * 32, ra);
+      if (c + 2 < CE) ptx::tmem_ld_32x32b_x32(tbase + (c + 2) * 32, ra);
       finish(c + 1, rb);
-      if (c + 2 < CH) {
+      if (c + 2 < CE) {
         ptx::tmem_wait_ld();
         ptx::tmem_regs_ready(ra);
       }
@@ -352,13 +409,13 @@ __device__ __forceinline__ void epilogue_classical_t(const KernelParams& p, uint
   }
 }
 
-template <int BN>
+template <int BN, int PART = 0>
 __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32_t tbase, int row0,
-                                                   int tn, int r) {
+                                                   int tn, int r, StageOut* so = nullptr) {
   if (p.sumsq_in || p.sumsq_out)
-    epilogue_classical_t<BN, true>(p, tbase, row0, tn, r);
+    epilogue_classical_t<BN, true, PART>(p, tbase, row0, tn, r, so);
   else
-    epilogue_classical_t<BN, false>(p, tbase, row0, tn, r);
+    epilogue_classical_t<BN, false, PART>(p, tbase, row0, tn, r, so);
 }
 
 // Strassen product `pr` for the 128 rows starting at row0 (inside each

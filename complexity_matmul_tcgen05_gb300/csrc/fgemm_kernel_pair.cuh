@@ -27,15 +27,19 @@ struct PairCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = BN == 256 ? 6 : 8;
   static constexpr int kTmemCols = BN == 256 ? 512 : 256;
-  static constexpr int kBarBytes = 256;
-  // One extra B half after the barriers: the MMA reads BN/2 columns of B per
-  // CTA; the slack keeps even a full-width read of the last stage inside this
-  // CTA's shared memory.
-  static constexpr int kSlackBytes = kBBytes;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kSlackBytes;
+  static constexpr int kBarBytes = 1024;  // barriers, padded to keep what follows 1024-aligned
+  // After the barriers: the epilogue warps' staging areas for TMA stores of
+  // C (4 KB each).  The region is at least one B half long: the MMA reads
+  // BN/2 columns of B per CTA, and this keeps even a full-width read of the
+  // last stage inside this CTA's shared memory.
+  static constexpr int kStagingOff = kStages * kStageBytes + kBarBytes;
+  static constexpr int kStagingBytes = 4 * 4096;
+  static constexpr int kSlackBytes = kBBytes > kStagingBytes ? kBBytes : kStagingBytes;
+  static constexpr int kSmemBytes = 1024 + kStagingOff + kSlackBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(2 * BN <= kTmemCols, "two accumulator buffers must fit in TMEM");
   static_assert((2 * kStages + 5) * 8 + 4 <= kBarBytes, "barrier area too small");
+  static_assert(kStageBytes >= 4096, "the last tile's second half stages in the pipeline buffers");
 };
 
 // One piece of a K-split tile, for this thread's row r of the CTA's 128 rows:
@@ -164,6 +168,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
   const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
+  const int n_items = work_item_count(p.num_units, p.split_tiles, p.split_pieces, nclusters, cluster);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -286,6 +291,8 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
     uint32_t acc_it = 0;
     bool ok = true;
     WorkItem w;
+    const int last_n = n_items - 1;
+    StageOut so{base_ptr + PC::kStagingOff + ew * 4096, base + PC::kStagingOff + ew * 4096, 0};
     for (int n = 0; ok && work_item(p.num_units, p.split_tiles, p.split_pieces, nclusters, p.k_blocks, cluster, n, w);
          ++n) {
       int tm, tn;
@@ -303,10 +310,40 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
         epilogue_split_piece<BN>(p, tbase, row0, tn, r, w, rank, ew, ptx::mapa(tempty(buf), 0));
         continue;
       }
-      epilogue_classical<BN>(p, tbase, row0, tn, r);
+      if (n == last_n)  // warps 0-3 finish the other half of the columns
+        epilogue_classical<BN, 1>(p, tbase, row0, tn, r, &so);
+      else
+        epilogue_classical<BN>(p, tbase, row0, tn, r, &so);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty(buf), 0));
+    }
+    stage_drain();
+  }
+
+  // ------------------------------------------- last tile, second half
+  // Nothing overlaps the last tile's epilogue, so the producer, MMA and
+  // spare warps (one per TMEM lane quarter, like warps 4-7) take half of its
+  // columns.  They meet first, so that the spare warps start their bounded
+  // wait only once the producer and the MMA issuer are done.
+  if (warp < 4) ptx::named_bar_sync(1, 128);
+  if (warp < 4 && n_items > 0) {
+    WorkItem w;
+    work_item(p.num_units, p.split_tiles, p.split_pieces, nclusters, p.k_blocks, cluster, n_items - 1, w);
+    if (w.npieces == 1) {
+      const uint32_t it = static_cast<uint32_t>(n_items - 1);
+      const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+      if (wait_warp(tfull(buf), aph, p, 2)) {
+        ptx::tc_fence_after();
+        int tm, tn;
+        unit_coords(p, w.unit, tm, tn);
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(warp * 32) << 16) + buf * BN;
+        const int row0 = tm * (2 * kBM) + static_cast<int>(rank) * kBM;
+        // every MMA has read its operands by now: stage in the pipeline buffers
+        StageOut so{base_ptr + warp * 4096, base + warp * 4096, 0};
+        epilogue_classical<BN, 2>(p, tbase, row0, tn, warp * 32 + lane, &so);
+        stage_drain();
+      }
     }
   }
 
