@@ -89,8 +89,10 @@ def test_exact_ternary_cta_pair(M, N, K, tile, dtype):
     assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
 
 
-def test_exact_ternary_strided_and_guard_band():
-    """lda/ldb/ldc larger than the row length; C's padding and rows around it untouched."""
+@pytest.mark.parametrize("tile_m,tile_n", [(0, 128), (256, 128), (256, 256)])
+def test_exact_ternary_strided_and_guard_band(tile_m, tile_n):
+    """lda/ldb/ldc larger than the row length; C's padding and rows around it
+    untouched (on CTA pairs C leaves by TMA stores, clipped at M and N)."""
     M, N, K = 130, 200, 136
     A0, B0, bias = _ternary(M, N, K, "bf16", seed=20)
     A = torch.zeros((M, K + 24), dtype=torch.bfloat16, device=DEV)[:, :K]
@@ -100,12 +102,32 @@ def test_exact_ternary_strided_and_guard_band():
     canary = 0x7F7B  # a bf16 NaN pattern never produced by the kernel
     big = torch.full((M + 2, N + 40), canary, dtype=torch.int16, device=DEV).view(torch.bfloat16)
     C = big[1:M + 1, :N]
-    run(A, B, epilogue="scale_bias", bias=bias, out=C, tile_n=128)
+    run(A, B, epilogue="scale_bias", bias=bias, out=C, tile_n=tile_n, tile_m=tile_m)
     ref = _exact_reference(A0, B0, bias, "bf16")
     assert np.array_equal(gpu_bits(C), ref)
     raw = big.view(torch.int16).cpu().numpy().view(np.uint16)
     assert (raw[0] == canary).all() and (raw[M + 1] == canary).all()
     assert (raw[1:M + 1, N:] == canary).all()
+
+
+def test_pair_swiglu_padded_output_guard_band():
+    """SwiGLU on CTA pairs into an output with a padded row pitch: every entry
+    of the valid region within the classical bounds, the padding untouched."""
+    M, N, K = 600, 1040, 520     # 3 x 5 pair tiles (128 output columns each), ragged
+    A = inputs.matrix(M, K, "normal", "bf16", 21, DEV)
+    B = inputs.matrix(K, N, "normal_inv_k", "bf16", 22, DEV, k=K)
+    canary = 0x7F7B
+    big = torch.full((M + 2, N // 2 + 24), canary, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    C = big[1:M + 1, :N // 2]
+    run(A, B, epilogue="swiglu", out=C, tile_n=256, tile_m=256)
+    raw = big.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (raw[0] == canary).all() and (raw[M + 1] == canary).all()
+    assert (raw[1:M + 1, N // 2:] == canary).all()
+    Av, Bv = oracle.decode(gpu_bits(A), "bf16"), oracle.decode(gpu_bits(B), "bf16")
+    prod = oracle.gemm(Av, Bv)
+    ref = oracle.epilogue(prod, "swiglu", 1.0, None)
+    kappa = activation_condition(prod, "swiglu")
+    assert normwise(values(C), ref, "bf16") <= TOL_NORMWISE["classical"] * max(1.0, kappa)
 
 
 # ----------------------------------------- full-entry tolerance parity
