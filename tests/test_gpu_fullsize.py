@@ -90,3 +90,36 @@ def test_sweep_shapes_every_legal_form(shape):
         if M <= tm:
             _sampled_check(f"sweep {shape} small-M {tm}", A, B, None, "classical", "none", "bf16",
                            tile=128, tile_m=tm)
+
+
+@pytest.mark.parametrize("fa,fb", [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e5m2")])
+def test_mx_4096_sampled(fa, fb):
+    """The block-scaled 8-bit product at the size `bench.py --mx` times, on its
+    input recipe (Gaussian values cast to 8 bits by torch, scales around 2^0):
+    4096 sampled entries against the oracle's decoded values (every entry a
+    K-long fp64 dot product), with the classical normwise and per-entry
+    bounds."""
+    n = 4096
+    kb = n // 32
+    g = torch.Generator().manual_seed(7)
+    def fp8(fmt):
+        sigma, f8 = (64.0, torch.float8_e4m3fn) if fmt == "e4m3" else (8192.0, torch.float8_e5m2)
+        return (torch.randn((n, n), generator=g) * sigma).to(f8).view(torch.uint8)
+    A, B = fp8(fa), fp8(fb)
+    SA = torch.randint(120, 135, (n, kb), generator=g, dtype=torch.int32).to(torch.uint8)
+    SB = torch.randint(120, 135, (kb, n), generator=g, dtype=torch.int32).to(torch.uint8)
+    C = fgemm.matmul_mx(A.to(DEV), SA.to(DEV), B.to(DEV), SB.to(DEV), a_format=fa, b_format=fb)
+    torch.cuda.synchronize()
+    assert fgemm.default_handle().get_error() == fgemm.OK
+    rows, cols = inputs.sample_positions(n, n, n=4096, tile_m=256, tile_n=256)
+    rows, cols = rows.numpy(), cols.numpy()
+    Av = oracle.mx_values(A.numpy(), SA.numpy(), fa, "row")[rows]          # sampled rows of A
+    Bv = oracle.mx_values(B.numpy(), SB.numpy(), fb, "col")[:, cols]       # sampled columns of B
+    ref = np.einsum("ik,ki->i", Av, Bv)
+    absdot = np.einsum("ik,ki->i", np.abs(Av), np.abs(Bv))
+    got = oracle.decode(gpu_bits(C[torch.as_tensor(rows, device=DEV), torch.as_tensor(cols, device=DEV)]),
+                        "bf16")
+    err = float(np.linalg.norm(got - oracle.round_to(ref, "bf16")) / np.linalg.norm(ref))
+    assert err <= TOL_NORMWISE["classical"], err
+    ok, _ = elementwise_ok(got, ref, absdot, n, "bf16")
+    assert ok
