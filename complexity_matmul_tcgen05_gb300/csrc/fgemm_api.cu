@@ -844,7 +844,7 @@ fgemm_status_t matmul_impl(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, co
             (static_cast<uint32_t>(bn >> 3) << 17) | (static_cast<uint32_t>(bm >> 4) << 24);
   p.num_products = d == 0 ? 1 : (d == 1 ? 7 : 49);
   const bool wino = plan.algo == FGEMM_ALGO_WINOGRAD1;
-  p.tab = wino ? winograd_table_ref() : table_for(d);
+  const StrassenTable& tab = wino ? winograd_table_ref() : table_for(d);
 
   s = encode_tmap(h, &p.tmap_a, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                   static_cast<uint64_t>(lda), fgemm::kBM, p.is_bf16);
@@ -859,7 +859,7 @@ fgemm_status_t matmul_impl(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, co
     s = ensure_workspace(h, per_cta * static_cast<size_t>(h->num_sms));
     if (s != FGEMM_OK) return s;
     p.workspace = h->workspace;
-    cudaError_t e = fgemm::launch_strassen_pair(bn, p, h->num_sms / 2, h->stream);
+    cudaError_t e = fgemm::launch_strassen_pair(bn, p, tab, h->num_sms / 2, h->stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "Strassen pair kernel launch");
     return FGEMM_OK;
   }
@@ -891,8 +891,8 @@ fgemm_status_t matmul_impl(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, co
     if (s != FGEMM_OK) return s;
     p.workspace = h->workspace;
   }
-  cudaError_t e = wino ? fgemm::launch_gemm_winograd1(bn, p, grid, h->stream)
-                       : fgemm::launch_gemm(bn, d, p, grid, h->stream);
+  cudaError_t e = wino ? fgemm::launch_gemm_winograd1(bn, p, tab, grid, h->stream)
+                       : fgemm::launch_gemm(bn, d, p, &tab, grid, h->stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "GEMM kernel launch");
   return FGEMM_OK;
 }

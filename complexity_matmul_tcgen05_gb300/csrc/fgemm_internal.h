@@ -175,7 +175,6 @@ struct KernelParams {
   uint32_t idesc;         // tcgen05 instruction descriptor
   float alpha;
   int num_products;
-  StrassenTable tab;
   // K split of the last partial wave (CTA-pair classical kernel only)
   int split_tiles;          // tiles split along K (0: none), units [0, split_tiles)
   int split_pieces;         // pieces per split tile (>= 2 when split_tiles > 0)
@@ -190,6 +189,14 @@ struct KernelParams {
   float rms_eps;
 };
 
+// The launch arguments of the Strassen / Winograd kernels: the common
+// parameters and the scheme's table.  The classical kernels take
+// KernelParams alone (a smaller parameter block is a cheaper launch).
+struct StrassenParams {
+  KernelParams k;
+  StrassenTable tab;
+};
+
 // Error word layout written by a kernel whose bounded wait ran out.
 constexpr unsigned int kErrTimeout = 0x80000000u;
 // bits [24,28): role (0 producer, 1 mma, 2 epilogue, 3 operand-sum), [0,24): block
@@ -198,8 +205,9 @@ size_t kernel_smem_bytes(int bn, int depth);
 int kernel_threads(int depth);
 
 // Launches the persistent GEMM kernel for tile width bn (64/128/256) and
-// Strassen depth (0 = classical) with `grid` CTAs on `stream`.
-cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, int grid,
+// Strassen depth (0 = classical) with `grid` CTAs on `stream`; `tab` is the
+// Strassen table of that depth (unused, may be null, for depth 0).
+cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, const StrassenTable* tab, int grid,
                         cudaStream_t stream);
 
 // Small-M kernel: C (M <= mp rows, mp = 16, 32 or 64) computed as
@@ -227,9 +235,10 @@ struct MxJob {
 cudaError_t launch_mx_dequant(const MxJob* jobs, int njobs, int num_sms, cudaStream_t stream);
 
 // One-level Winograd variant on the single-CTA kernel (bn = 128 or 256): the
-// Strassen kernel with up to four source blocks per formed operand; p.tab
+// Strassen kernel with up to four source blocks per formed operand; `tab`
 // must be the Winograd table.
-cudaError_t launch_gemm_winograd1(int bn, const KernelParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_winograd1(int bn, const KernelParams& p, const StrassenTable& tab, int grid,
+                                  cudaStream_t stream);
 
 // Classical kernel on CTA pairs: 256 x bn tiles (bn = 128 or 256) on exactly
 // `clusters` pairs, which must not exceed gemm_pair_clusters_fit(bn) and must
@@ -241,7 +250,7 @@ cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int clusters, cudaSt
 int gemm_pair_clusters_fit(int bn);
 
 // One-level Strassen on CTA pairs (256 x bn tiles of the half-size block space).
-cudaError_t launch_strassen_pair(int bn, const KernelParams& p, int max_clusters,
+cudaError_t launch_strassen_pair(int bn, const KernelParams& p, const StrassenTable& tab, int max_clusters,
                                  cudaStream_t stream);
 
 // The Strassen coefficient table of `depth` levels (0: one trivial product).

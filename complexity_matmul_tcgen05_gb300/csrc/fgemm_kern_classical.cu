@@ -4,8 +4,10 @@
 
 namespace fgemm {
 
-cudaError_t launch_gemm_depth1(int bn, const KernelParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_gemm_depth2(int bn, const KernelParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_depth1(int bn, const KernelParams& p, const StrassenTable& tab, int grid,
+                               cudaStream_t stream);
+cudaError_t launch_gemm_depth2(int bn, const KernelParams& p, const StrassenTable& tab, int grid,
+                               cudaStream_t stream);
 
 size_t kernel_smem_bytes(int bn, int depth) {
   (void)depth;
@@ -21,14 +23,15 @@ int kernel_threads(int depth) {
   return depth == 0 ? RoleCfg<0>::kThreads : RoleCfg<1>::kThreads;
 }
 
-cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, int grid, cudaStream_t stream) {
-  if (depth == 1) return launch_gemm_depth1(bn, p, grid, stream);
-  if (depth == 2) return launch_gemm_depth2(bn, p, grid, stream);
+cudaError_t launch_gemm(int bn, int depth, const KernelParams& p, const StrassenTable* tab, int grid,
+                        cudaStream_t stream) {
+  if (depth == 1) return tab ? launch_gemm_depth1(bn, p, *tab, grid, stream) : cudaErrorInvalidValue;
+  if (depth == 2) return tab ? launch_gemm_depth2(bn, p, *tab, grid, stream) : cudaErrorInvalidValue;
   if (depth != 0) return cudaErrorInvalidValue;
   switch (bn) {
-    case 64: return launch_gemm_t<64, 0>(p, grid, stream);
-    case 128: return launch_gemm_t<128, 0>(p, grid, stream);
-    case 256: return launch_gemm_t<256, 0>(p, grid, stream);
+    case 64: return launch_gemm_t<64, 0>(p, nullptr, grid, stream);
+    case 128: return launch_gemm_t<128, 0>(p, nullptr, grid, stream);
+    case 256: return launch_gemm_t<256, 0>(p, nullptr, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

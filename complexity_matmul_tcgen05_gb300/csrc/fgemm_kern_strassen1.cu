@@ -3,10 +3,11 @@
 
 namespace fgemm {
 
-cudaError_t launch_gemm_depth1(int bn, const KernelParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm_depth1(int bn, const KernelParams& p, const StrassenTable& tab, int grid,
+                               cudaStream_t stream) {
   switch (bn) {
-    case 128: return launch_gemm_t<128, 1>(p, grid, stream);
-    case 256: return launch_gemm_t<256, 1>(p, grid, stream);
+    case 128: return launch_gemm_t<128, 1>(p, &tab, grid, stream);
+    case 256: return launch_gemm_t<256, 1>(p, &tab, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -426,11 +426,12 @@ __device__ __forceinline__ void epilogue_classical(const KernelParams& p, uint32
 // chunk are 4 KB contiguous.  Every element is read and written only by the
 // thread that owns its row, in program order.
 template <int BN, int DEPTH>
-__device__ __forceinline__ void epilogue_strassen(const KernelParams& p, uint32_t tbase, int row0,
+__device__ __forceinline__ void epilogue_strassen(const KernelParams& p, const StrassenTable& tab,
+                                                  uint32_t tbase, int row0,
                                                   int tn, int pr, int r, float* ws) {
   constexpr int G = 1 << DEPTH;
   constexpr int CH = BN / 32;
-  const int nc = p.tab.nc[pr];
+  const int nc = tab.nc[pr];
   const bool last = pr == p.num_products - 1;
   auto slot_ptr = [&](int slot, int c) {
     return reinterpret_cast<float4*>(ws + ((static_cast<size_t>(slot) * CH + c) * kBM + r) * 32);
@@ -442,7 +443,7 @@ __device__ __forceinline__ void epilogue_strassen(const KernelParams& p, uint32_
     ptx::tmem_wait_ld();
 #pragma unroll 1
     for (int t = 0; t < nc; ++t) {
-      const uint8_t code = p.tab.c[pr][t];
+      const uint8_t code = tab.c[pr][t];
       float4* w = slot_ptr(code & kTermIndexMask, c);
       const float sg = (code & kTermNeg) ? -1.0f : 1.0f;
       if (code & kTermFirst) {
@@ -528,14 +529,15 @@ __device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8], int is_bf
 // one formed operand: 2^DEPTH for the Strassen tables, 4 for the one-level
 // Winograd table (whose expanded operands have up to four blocks).
 template <int BN, int DEPTH, int TERMS>
-__device__ __forceinline__ void form_operands(const KernelParams& p, uint8_t* sA, uint8_t* sB,
+__device__ __forceinline__ void form_operands(const KernelParams& p, const StrassenTable& tab, uint8_t* sA,
+                                              uint8_t* sB,
                                               int pr, int tm, int tn, int kb, int tid,
                                               int nthreads) {
   constexpr int T = TERMS;                 // terms per formed operand (at most)
   constexpr int G = 1 << DEPTH;            // blocks per dimension
   constexpr int U = T == 2 ? 8 : 4;        // chunks per thread in flight: U * T loads
   constexpr int CPR = BN / 8;              // 16-byte chunks per K-row of the B tile
-  const int na = p.tab.na[pr], nb = p.tab.nb[pr];
+  const int na = tab.na[pr], nb = tab.nb[pr];
   const int nA = na > 1 ? kBM * 8 : 0;
   const int nB = nb > 1 ? kBK * CPR : 0;
   const int total = nA + nB;
@@ -545,12 +547,12 @@ __device__ __forceinline__ void form_operands(const KernelParams& p, uint8_t* sA
   float sgA[T], sgB[T];
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    const uint8_t ca = p.tab.a[pr][t < na ? t : 0];
+    const uint8_t ca = tab.a[pr][t < na ? t : 0];
     const int qa = ca & kTermIndexMask;
     srcA[t] = p.A + static_cast<long long>((qa >> DEPTH) * p.sub_m + tm * kBM) * p.lda +
               (qa & (G - 1)) * p.sub_k + kb * kBK;
     sgA[t] = (ca & kTermNeg) ? -1.0f : 1.0f;
-    const uint8_t cb = p.tab.b[pr][t < nb ? t : 0];
+    const uint8_t cb = tab.b[pr][t < nb ? t : 0];
     const int qb = cb & kTermIndexMask;
     srcB[t] = p.B + static_cast<long long>((qb >> DEPTH) * p.sub_k + kb * kBK) * p.ldb +
               (qb & (G - 1)) * p.sub_n + tn * BN;
@@ -612,9 +614,28 @@ __device__ __forceinline__ void form_operands(const KernelParams& p, uint8_t* sA
 
 // ---------------------------------------------------------------- kernel
 
+// Launch arguments by depth: the classical kernel takes KernelParams, the
+// Strassen kernels StrassenParams.  A classical instantiation gets an unused
+// table reference so that the shared code compiles.
+template <int DEPTH>
+struct KernelArgs {
+  using type = StrassenParams;
+};
+template <>
+struct KernelArgs<0> {
+  using type = KernelParams;
+};
+static __device__ StrassenTable g_no_table;
+__device__ __forceinline__ const KernelParams& kernel_params(const KernelParams& a) { return a; }
+__device__ __forceinline__ const KernelParams& kernel_params(const StrassenParams& a) { return a.k; }
+__device__ __forceinline__ const StrassenTable& kernel_table(const KernelParams&) { return g_no_table; }
+__device__ __forceinline__ const StrassenTable& kernel_table(const StrassenParams& a) { return a.tab; }
+
 template <int BN, int DEPTH, int TERMS = (1 << DEPTH)>
 __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
-    fgemm_kernel(const __grid_constant__ KernelParams p) {
+    fgemm_kernel(const __grid_constant__ typename KernelArgs<DEPTH>::type args) {
+  const KernelParams& p = kernel_params(args);
+  const StrassenTable& tab = kernel_table(args);
   using TC = TileCfg<BN>;
   constexpr int S = TC::kStages;
   constexpr int kSumWarps = RoleCfg<DEPTH>::kSumWarps;
@@ -686,10 +707,10 @@ __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
               for (int q = 0; q < BN / 64; ++q) bx[q] = tn * BN + q * 64;
             }
           } else {
-            a_raw = p.tab.na[pr] == 1;
-            b_raw = p.tab.nb[pr] == 1;
-            const int qa = p.tab.a[pr][0] & kTermIndexMask;
-            const int qb = p.tab.b[pr][0] & kTermIndexMask;
+            a_raw = tab.na[pr] == 1;
+            b_raw = tab.nb[pr] == 1;
+            const int qa = tab.a[pr][0] & kTermIndexMask;
+            const int qb = tab.b[pr][0] & kTermIndexMask;
             ay = (qa >> DEPTH) * p.sub_m + tm * kBM;
             ax0 = (qa & ((1 << DEPTH) - 1)) * p.sub_k;
             by0 = (qb >> DEPTH) * p.sub_k;
@@ -800,7 +821,7 @@ __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
         if constexpr (DEPTH == 0) {
           epilogue_classical<BN>(p, tbase, tm * kBM, tn, r);
         } else {
-          epilogue_strassen<BN, DEPTH>(p, tbase, tm * kBM, tn, pr, r, ws);
+          epilogue_strassen<BN, DEPTH>(p, tab, tbase, tm * kBM, tn, pr, r, ws);
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -819,15 +840,15 @@ __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
       int tm, tn;
       unit_coords(p, unit, tm, tn);
       for (int pr = 0; ok && pr < NP; ++pr) {
-        const bool a_sum = p.tab.na[pr] > 1;
-        const bool b_sum = p.tab.nb[pr] > 1;
+        const bool a_sum = tab.na[pr] > 1;
+        const bool b_sum = tab.nb[pr] > 1;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_warp(empty(s), ph ^ 1u, p, 3)) {
             ok = false;
             break;
           }
           if (a_sum || b_sum)
-            form_operands<BN, DEPTH, TERMS>(p, base_ptr + s * TC::kABytes,
+            form_operands<BN, DEPTH, TERMS>(p, tab, base_ptr + s * TC::kABytes,
                                      base_ptr + S * TC::kABytes + s * TC::kBBytes, pr, tm, tn, kb,
                                      tid, NT);
           ptx::fence_proxy_async_smem();
@@ -849,7 +870,7 @@ __global__ void __launch_bounds__(RoleCfg<DEPTH>::kThreads, 1)
 }
 
 template <int BN, int DEPTH, int TERMS = (1 << DEPTH)>
-cudaError_t launch_gemm_t(const KernelParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm_t(const KernelParams& p, const StrassenTable* tab, int grid, cudaStream_t stream) {
   auto kern = fgemm_kernel<BN, DEPTH, TERMS>;
   constexpr int smem = TileCfg<BN>::kSmemBytes;
   static unsigned long long configured = 0;  // per-device bit
@@ -862,7 +883,14 @@ cudaError_t launch_gemm_t(const KernelParams& p, int grid, cudaStream_t stream) 
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
-  kern<<<grid, RoleCfg<DEPTH>::kThreads, smem, stream>>>(p);
+  if constexpr (DEPTH == 0) {
+    (void)tab;
+    kern<<<grid, RoleCfg<DEPTH>::kThreads, smem, stream>>>(p);
+  } else {
+    if (!tab) return cudaErrorInvalidValue;
+    const StrassenParams args{p, *tab};
+    kern<<<grid, RoleCfg<DEPTH>::kThreads, smem, stream>>>(args);
+  }
   return cudaGetLastError();
 }
 

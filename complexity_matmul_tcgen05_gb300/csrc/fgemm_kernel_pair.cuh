@@ -400,7 +400,9 @@ __device__ __forceinline__ void add_staged(uint8_t* dst, const uint8_t* src, int
 
 template <int BN>
 __global__ void __launch_bounds__(PairStrassenCfg<BN>::kThreads, 1)
-    fgemm_kernel_pair_strassen(const __grid_constant__ KernelParams p) {
+    fgemm_kernel_pair_strassen(const __grid_constant__ StrassenParams args) {
+  const KernelParams& p = args.k;
+  const StrassenTable& tab = args.tab;
   using PC = PairStrassenCfg<BN>;
   constexpr int S = PC::kStages;
   constexpr int NSW = PC::kSumWarps;
@@ -467,11 +469,11 @@ __global__ void __launch_bounds__(PairStrassenCfg<BN>::kThreads, 1)
         const int row_in_block = tm * (2 * kBM) + static_cast<int>(rank) * kBM;
         const int col_in_block = tn * BN + static_cast<int>(rank) * (BN / 2);
         for (int pr = 0; ok && pr < NP; ++pr) {
-          const int na = p.tab.na[pr], nb = p.tab.nb[pr];
+          const int na = tab.na[pr], nb = tab.nb[pr];
           int ay[2], ax[2], by[2], bx[2];
           for (int t = 0; t < 2; ++t) {
-            const int qa = p.tab.a[pr][t < na ? t : 0] & kTermIndexMask;
-            const int qb = p.tab.b[pr][t < nb ? t : 0] & kTermIndexMask;
+            const int qa = tab.a[pr][t < na ? t : 0] & kTermIndexMask;
+            const int qb = tab.b[pr][t < nb ? t : 0] & kTermIndexMask;
             ay[t] = (qa >> 1) * p.sub_m + row_in_block;
             ax[t] = (qa & 1) * p.sub_k;
             by[t] = (qb >> 1) * p.sub_k;
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(PairStrassenCfg<BN>::kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * BN;
-        epilogue_strassen<BN, 1>(p, tbase, row0, tn, pr, r, ws);
+        epilogue_strassen<BN, 1>(p, tab, tbase, row0, tn, pr, r, ws);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty(buf), 0));
@@ -589,11 +591,11 @@ __global__ void __launch_bounds__(PairStrassenCfg<BN>::kThreads, 1)
     bool ok = true;
     for (int unit = cluster; ok && unit < p.num_units; unit += nclusters) {
       for (int pr = 0; ok && pr < NP; ++pr) {
-        const int na = p.tab.na[pr], nb = p.tab.nb[pr];
-        const float sa0 = (p.tab.a[pr][0] & kTermNeg) ? -1.0f : 1.0f;
-        const float sa1 = (p.tab.a[pr][1] & kTermNeg) ? -1.0f : 1.0f;
-        const float sb0 = (p.tab.b[pr][0] & kTermNeg) ? -1.0f : 1.0f;
-        const float sb1 = (p.tab.b[pr][1] & kTermNeg) ? -1.0f : 1.0f;
+        const int na = tab.na[pr], nb = tab.nb[pr];
+        const float sa0 = (tab.a[pr][0] & kTermNeg) ? -1.0f : 1.0f;
+        const float sa1 = (tab.a[pr][1] & kTermNeg) ? -1.0f : 1.0f;
+        const float sb0 = (tab.b[pr][0] & kTermNeg) ? -1.0f : 1.0f;
+        const float sb1 = (tab.b[pr][1] & kTermNeg) ? -1.0f : 1.0f;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_warp(loaded(s), ph, p, 3)) {
             ok = false;
@@ -624,7 +626,8 @@ __global__ void __launch_bounds__(PairStrassenCfg<BN>::kThreads, 1)
 }
 
 template <int BN>
-cudaError_t launch_strassen_pair_t(const KernelParams& p, int max_clusters, cudaStream_t stream) {
+cudaError_t launch_strassen_pair_t(const KernelParams& p, const StrassenTable& tab, int max_clusters,
+                                   cudaStream_t stream) {
   auto kern = fgemm_kernel_pair_strassen<BN>;
   constexpr int smem = PairStrassenCfg<BN>::kSmemBytes;
   static unsigned long long configured = 0;
@@ -656,7 +659,8 @@ cudaError_t launch_strassen_pair_t(const KernelParams& p, int max_clusters, cuda
   }
   const int clusters = std::min(std::min(max_clusters, clusters_fit[dev & 63]), p.num_units);
   cfg.gridDim = dim3(2 * std::max(clusters, 1), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  const StrassenParams args{p, tab};
+  return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 // Launch configuration of the classical pair kernel; on first use per device

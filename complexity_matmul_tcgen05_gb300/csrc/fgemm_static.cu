@@ -156,7 +156,7 @@ extern "C" fgemm_status_t fgemm_strassen_matmul_static(
             (static_cast<uint32_t>(tile_n >> 3) << 17) |
             (static_cast<uint32_t>(fgemm::kBM >> 4) << 24);
   p.num_products = depth == 1 ? 7 : 49;
-  p.tab = fgemm::strassen_table(depth);
+  const fgemm::StrassenTable& tab = fgemm::strassen_table(depth);
 
   const int grid = static_cast<int>(std::min<long long>(units, sms));
   const size_t per_cta = (size_t{1} << (2 * depth)) * fgemm::kBM * static_cast<size_t>(tile_n) * 4;
@@ -180,7 +180,7 @@ extern "C" fgemm_status_t fgemm_strassen_matmul_static(
   e = cudaMemsetAsync(p.err, 0, sizeof(unsigned int), stream);
   if (e != cudaSuccess)
     return fail(FGEMM_ERR_CUDA, std::string("clearing the error word: ") + cudaGetErrorString(e));
-  e = fgemm::launch_gemm(tile_n, depth, p, grid, stream);
+  e = fgemm::launch_gemm(tile_n, depth, p, &tab, grid, stream);
   if (e != cudaSuccess) return fail(FGEMM_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e));
   return FGEMM_OK;
 }
