@@ -230,10 +230,11 @@ def ncu_traffic(workload, algo, tile_m, tile):
 
 # ----------------------------------------------------------- CPU oracle
 
-def cpu_oracle_sample(name, target_s=10.0, device_inputs=None):
+def cpu_oracle_sample(name, target_s=10.0, device_inputs=None, entries=None):
     """Times the fp64 oracle on a bounded sample of the workload's output
-    entries (each a K-long dot product of decoded 16-bit inputs).  Returns
-    (TFLOP/s, seconds, entries, threads)."""
+    entries (each a K-long dot product of decoded 16-bit inputs): `entries`
+    of them, or as many as take about target_s.  Returns (TFLOP/s, seconds,
+    entries, threads)."""
     import numpy as np
     import oracle
     from complexity_matmul_tcgen05_gb300 import inputs
@@ -246,14 +247,14 @@ def cpu_oracle_sample(name, target_s=10.0, device_inputs=None):
     bb = None if bias is None else inputs.bits(bias)
     n_out = N // 2 if epi == "swiglu" else N
     per_entry = 2.0 * K * (2 if epi == "swiglu" else 1)
-    n = 256
+    n = entries if entries else 256
     elapsed = 0.0
     while True:
         rows, cols = inputs.sample_positions(M, n_out, n=n)
         t0 = time.perf_counter()
         oracle.reference_sampled(Ab, Bb, dtype, rows.numpy(), cols.numpy(), epi, 1.0, bb)
         elapsed = time.perf_counter() - t0
-        if elapsed >= target_s or n >= (1 << 26):
+        if entries or elapsed >= target_s or n >= (1 << 26):
             break
         grow = max(2.0, min(16.0, target_s / max(elapsed, 1e-3)))
         n = int(n * grow)
@@ -268,12 +269,18 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     M, N, K, dtype, epi = workload_shape(args.workload)
-    per_step = 3.0
+    # inputs drawn once; the sample size fixed in the warm-up so that each
+    # step takes about per_step seconds and the whole run about two minutes
+    per_step = min(3.0, 100.0 / max(1, args.steps))
+    host_inputs = make_inputs(args.workload, "cpu")
+    _, t_probe, n_probe, _ = cpu_oracle_sample(args.workload, target_s=per_step / 4,
+                                               device_inputs=host_inputs)
+    n_step = max(256, int(n_probe * per_step / max(t_probe, 1e-6)))
     for _ in range(max(0, args.warmup)):
-        cpu_oracle_sample(args.workload, target_s=0.2)
+        cpu_oracle_sample(args.workload, device_inputs=host_inputs, entries=max(256, n_step // 16))
     vals, secs, ents = [], 0.0, 0
     for _ in range(args.steps):
-        v, s, e, thr = cpu_oracle_sample(args.workload, target_s=per_step)
+        v, s, e, thr = cpu_oracle_sample(args.workload, device_inputs=host_inputs, entries=n_step)
         vals.append(v)
         secs += s
         ents += e
