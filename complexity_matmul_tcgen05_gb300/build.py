@@ -21,6 +21,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = [
     "fgemm_api.cu",
     "fgemm_model.cpp",
+    "fgemm_tables.cpp",
     "fgemm_kern_classical.cu",
     "fgemm_kern_strassen1.cu",
     "fgemm_kern_strassen2.cu",
