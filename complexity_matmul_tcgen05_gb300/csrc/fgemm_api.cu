@@ -374,12 +374,12 @@ fgemm_status_t launch_small_m(fgemm_handle_t h, KernelParams& p, int64_t M, int6
   s = encode_tmap(h, &p.tmap_b, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
                   static_cast<uint64_t>(ldb), fgemm::kBK, p.is_bf16);
   if (s != FGEMM_OK) return s;
-  // every CTA streams at least kMinShare K blocks, so that a tile is not cut
-  // into more pieces than its sum can absorb cheaply
-  constexpr long long kMinShare = 8;
-  const long long iters = tiles * p.k_blocks;
-  const int ctas = static_cast<int>(
-      std::max<long long>(1, std::min<long long>(h->num_sms, (iters + kMinShare - 1) / kMinShare)));
+  // every CTA streams at least 8 K blocks, so that a tile is not cut into
+  // more pieces than its sum can absorb cheaply; among such grids, one whose
+  // shares start at few K offsets of a tile, so that the CTAs read the same
+  // rows of B together
+  const int ctas = fgemm_small_m_grid(tiles, p.k_blocks, h->num_sms, nullptr);
+  if (ctas <= 0) return set_msg(h, FGEMM_ERR_UNSUPPORTED, "cannot size the small-M grid");
   s = ensure_workspace(h, static_cast<size_t>(ctas) * 2 * 128 * static_cast<size_t>(mp) * sizeof(float));
   if (s != FGEMM_OK) return s;
   s = ensure_counters(h, static_cast<size_t>(ctas) * 8);
@@ -441,7 +441,7 @@ fgemm_status_t load_calibration(fgemm_handle_t h, const char* path) {
       {"l2_gbs", &m.l2_gbs},                    {"split_fix_us", &m.split_fix_us},
       {"eff_winograd1_128", &m.eff_winograd[0]}, {"eff_winograd1_256", &m.eff_winograd[1]},
       {"hbm_stream_eff", &m.hbm_stream_eff},     {"small_m_stream_eff", &m.small_m_stream_eff},
-      {"small_m_fix_us", &m.small_m_fix_us},
+      {"small_m_fix_us", &m.small_m_fix_us},     {"small_m_aligned_eff", &m.small_m_aligned_eff},
   };
   int found = 0;
   for (auto& fd : fields) found += json_number(text, fd.key, fd.dst) ? 1 : 0;

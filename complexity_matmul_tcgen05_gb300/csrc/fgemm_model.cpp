@@ -30,6 +30,7 @@
 //   t            = max(t_compute, t_memory, t_operands) + launch ("Page 21",
 //                  the roofline: time is the largest of compute and traffic)
 #include <algorithm>
+#include <numeric>
 #include <cmath>
 #include <cstdint>
 
@@ -102,12 +103,18 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   m.split_fix_us = 4.0;
   m.eff_winograd[0] = 0.065;  // 128 x 128 (below Strassen's: 14 + 14 source terms, not 12 + 12)
   m.eff_winograd[1] = 0.074;  // 128 x 256
-  m.eff_small_m[0] = 0.056;   // tile_m 16: an N = 16 MMA, 16/256 of the full rate, x 0.9
-  m.eff_small_m[1] = 0.11;    // tile_m 32
-  m.eff_small_m[2] = 0.22;    // tile_m 64
+  // small-M tiles: an N = tile_m MMA runs at most tile_m / 256 of the full
+  // rate.  These are lower bounds from streams that stayed memory-bound:
+  // 16 x 16384^2 at 6.4 TB/s, and tile_m 64 only 5 % slower than tile_m 16
+  m.eff_small_m[0] = 0.07;    // tile_m 16
+  m.eff_small_m[1] = 0.14;    // tile_m 32
+  m.eff_small_m[2] = 0.27;    // tile_m 64
   m.hbm_stream_eff = 0.9;
   m.small_m_stream_eff = 0.75;  // 16 x 16384^2: 537 MB in ~101-106 us inside the kernel
   m.small_m_fix_us = 4.0;
+  // 16 x 16384^2 on 128 CTAs of one whole tile each: 537 MB in 83.7 us, and
+  // 16 x 8192^2 on 128 CTAs of half a tile: 32.7 us (CUDA events)
+  m.small_m_aligned_eff = 0.97;
   *out = m;
 }
 
@@ -201,6 +208,29 @@ int32_t fgemm_stream_k_work_item(int64_t tiles, int32_t k_blocks, int32_t ctas, 
   return 1;
 }
 
+int32_t fgemm_small_m_grid(int64_t tiles, int32_t k_blocks, int32_t num_sms, int32_t* phases_out) {
+  if (tiles <= 0 || tiles > (1ll << 30) || k_blocks <= 0 || num_sms <= 0) return 0;
+  const int64_t iters = tiles * k_blocks;
+  const int64_t most = std::max<int64_t>(1, std::min<int64_t>(num_sms, ceil_div(iters, 8)));
+  const int64_t least = std::max<int64_t>(1, ceil_div(most * 3, 4));
+  int64_t best = most, best_phases = most;
+  for (int64_t c = most; c >= least; --c) {
+    if (iters % c) continue;
+    const int64_t share = iters / c;
+    const int64_t phases = std::min<int64_t>(c, k_blocks / std::gcd<int64_t>(share, k_blocks));
+    if (phases < best_phases) {
+      best = c;
+      best_phases = phases;
+    }
+  }
+  if (best_phases > 4) {
+    best = most;
+    best_phases = most;
+  }
+  if (phases_out) *phases_out = static_cast<int32_t>(best_phases);
+  return static_cast<int32_t>(best);
+}
+
 fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, int64_t N,
                                    int64_t K, int32_t epi_kind, fgemm_algo_t algo, int32_t tile_m,
                                    int32_t tile_n, double* predicted_us) {
@@ -212,16 +242,21 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     // 128-column tiles; bound by B from HBM or by the narrow MMAs
     const int64_t tiles = ceil_div(N, 128), kb = ceil_div(K, fgemm::kBK);
     const int64_t iters = tiles * kb;
-    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(dev->num_sms, ceil_div(iters, 8)));
+    int32_t phases = 0;
+    const int64_t ctas = std::max(1, fgemm_small_m_grid(tiles, static_cast<int32_t>(kb), dev->num_sms, &phases));
+    const bool aligned = phases <= 4;
     const double eff = std::max(dev->eff_small_m[tile_m == 16 ? 0 : (tile_m == 32 ? 1 : 2)], 1e-3);
     const double sm_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms;
     const double t_kb = 2.0 * 128.0 * tile_m * fgemm::kBK / (sm_flop_per_us * eff);
     const double t_compute = static_cast<double>(ceil_div(iters, ctas)) * t_kb + dev->tile_fill_us;
     const double bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
                                 static_cast<double>(M) * N);
-    const double sm_share = std::min(1.0, static_cast<double>(ctas) / std::max(1, dev->num_sms));
-    const double t_memory =
-        bytes / (dev->hbm_gbs * 1e3 * std::max(dev->small_m_stream_eff, 1e-3) * sm_share);
+    // CTAs reading B in step stream at the full rate from 3/4 of the SMs on;
+    // otherwise the rate scales with the SMs in use
+    const double sm_share = std::min(
+        1.0, static_cast<double>(ctas) / std::max(1.0, (aligned ? 0.75 : 1.0) * dev->num_sms));
+    const double stream_eff = aligned ? dev->small_m_aligned_eff : dev->small_m_stream_eff;
+    const double t_memory = bytes / (dev->hbm_gbs * 1e3 * std::max(stream_eff, 1e-3) * sm_share);
     if (predicted_us)
       *predicted_us = std::max(t_compute, t_memory) + dev->small_m_fix_us + dev->launch_us;
     return FGEMM_OK;

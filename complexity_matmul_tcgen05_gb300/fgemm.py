@@ -56,7 +56,8 @@ class DeviceModel(ctypes.Structure):
                 ("split_fix_us", ctypes.c_double),
                 ("eff_winograd", ctypes.c_double * 2),
                 ("eff_small_m", ctypes.c_double * 3), ("hbm_stream_eff", ctypes.c_double),
-                ("small_m_stream_eff", ctypes.c_double), ("small_m_fix_us", ctypes.c_double)]
+                ("small_m_stream_eff", ctypes.c_double), ("small_m_fix_us", ctypes.c_double),
+                ("small_m_aligned_eff", ctypes.c_double)]
 
 
 _lib = None
@@ -122,6 +123,8 @@ def lib() -> ctypes.CDLL:
         L.fgemm_set_split_mode.argtypes = [vp, i32]
         L.fgemm_stream_k_work_item.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(i64)]
         L.fgemm_stream_k_work_item.restype = i32
+        L.fgemm_small_m_grid.argtypes = [i64, i32, i32, ctypes.POINTER(i32)]
+        L.fgemm_small_m_grid.restype = i32
         L.fgemm_get_device_model.argtypes = [vp, model_p]
         L.fgemm_set_device_model.argtypes = [vp, model_p]
         for name in ("fgemm_create", "fgemm_destroy", "fgemm_set_stream", "fgemm_matmul",
@@ -163,6 +166,12 @@ def stream_k_work_items(tiles: int, k_blocks: int, ctas: int, cta: int):
         items.append(tuple(out))
         n += 1
     return items
+
+
+def small_m_grid(tiles: int, k_blocks: int, num_sms: int):
+    """(CTA count, phases) of the small-M kernel's grid (fgemm_small_m_grid)."""
+    ph = ctypes.c_int32()
+    return lib().fgemm_small_m_grid(tiles, k_blocks, num_sms, ctypes.byref(ph)), ph.value
 
 
 def status_string(status: int) -> str:

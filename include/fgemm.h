@@ -366,7 +366,26 @@ typedef struct {
                               * B at different K (less DRAM page locality) */
   double small_m_fix_us;   /* its per-launch cost beyond the stream: the pieces'
                             * partial store, count and sum, and the slowest CTA */
+  double small_m_aligned_eff; /* fraction of hbm_gbs the small-M kernel reaches when
+                               * its shares start at no more than 4 K offsets of a
+                               * tile (fgemm_small_m_grid), so that its CTAs read the
+                               * same rows of B together */
 } fgemm_device_model_t;
+
+/*
+ * Grid of the small-M kernel for `tiles` 128-column tiles of `k_blocks` K
+ * blocks each on `num_sms` SMs. The K blocks of all tiles, laid end to end,
+ * are cut into equal shares, one per CTA. Among the CTA counts from 3/4 of
+ * the largest grid (every SM, each CTA at least 8 blocks) up to that grid,
+ * the ones that divide tiles * k_blocks exactly are scored by their phases:
+ * the number of distinct K offsets inside a tile at which shares start. The
+ * count with the fewest phases wins (the larger count on a tie). Fewer
+ * phases mean the CTAs read fewer distinct rows of B at a time. If no count
+ * has 4 phases or fewer, the largest grid is returned with phases set to its
+ * CTA count. Returns the CTA count (0 on invalid arguments) and writes the
+ * phases to *phases_out when it is not NULL. Host-only.
+ */
+int32_t fgemm_small_m_grid(int64_t tiles, int32_t k_blocks, int32_t num_sms, int32_t* phases_out);
 
 /* Default model for a device with the given SM count, peak and bandwidth. */
 void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms,

@@ -7,6 +7,7 @@ import json
 import os
 import re
 
+import numpy as np
 import pytest
 
 from complexity_matmul_tcgen05_gb300 import fgemm
@@ -407,14 +408,67 @@ def test_small_m_legality_and_model(L):
     assert fgemm.validate(16, 4096, 4096, 16, 4096, 16, 4096, 16, 4096, fgemm.BF16, ep,
                           "strassen1", 128, 16) == fgemm.ERR_UNSUPPORTED
     m = _model(L)
-    # 16 x 16384 x 16384 streams 512 MiB of B: the small-M form predicts that
-    # stream at its own efficiency, plus its fixed cost and the launch
+    # 16 x 16384 x 16384 streams 512 MiB of B on 128 CTAs of one whole tile
+    # each (every share starts at K offset 0): the aligned rate, plus the
+    # fixed cost and the launch
     _, t_small = _predict(L, m, 16, 16384, 16384, "classical", 128, tile_m=16)
     b = 2.0 * (16 * 16384 + 16384 * 16384 + 16 * 16384)
-    stream_us = b / (m.hbm_gbs * 1e3 * m.small_m_stream_eff)
+    stream_us = b / (m.hbm_gbs * 1e3 * m.small_m_aligned_eff)
     assert abs(t_small - (stream_us + m.small_m_fix_us + m.launch_us)) < 1e-6 * t_small
+    # 16 x 20480 x 8128: 160 tiles of 127 K blocks; of 114..152 CTAs only 127
+    # divides the 20320 iterations, and its shares start at 127 offsets, so
+    # every SM streams at the misaligned rate
+    assert fgemm.small_m_grid(160, 127, 152) == (152, 152)
+    _, t_mis = _predict(L, m, 16, 20480, 8128, "classical", 128, tile_m=16)
+    b = 2.0 * (16 * 8128 + 8128 * 20480 + 16 * 20480)
+    stream_us = b / (m.hbm_gbs * 1e3 * m.small_m_stream_eff)
+    assert abs(t_mis - (stream_us + m.small_m_fix_us + m.launch_us)) < 1e-6 * t_mis
+    # and AUTO takes the small-M form for 16 x 16384^2
+    a = ctypes.c_int()
+    tm, tn, us = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+    assert L.fgemm_model_plan(ctypes.byref(m), 16, 16384, 16384, 0, ctypes.byref(a), ctypes.byref(tm),
+                              ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
+    assert (fgemm.ALGO_NAMES[a.value], tm.value, tn.value) == ("classical", 16, 128)
     # 16 x 8192 x 8192 as 128 x 64 tiles keeps 128 of 152 SMs streaming: the
     # small-M form, on every SM, predicts less
     _, t_small = _predict(L, m, 16, 8192, 8192, "classical", 128, tile_m=16)
     _, t_wide = _predict(L, m, 16, 8192, 8192, "classical", 64, tile_m=128)
     assert t_small < t_wide
+
+
+@pytest.mark.parametrize("tiles,kb,sms,want", [
+    (128, 256, 152, (128, 1)),   # 16 x 16384^2: one whole tile per CTA
+    (64, 128, 152, (128, 2)),    # 16 x 8192^2: half a tile per CTA, shares start at 0 or 64
+    (96, 192, 152, (144, 3)),    # 16 x 12288^2: 2/3 of a tile, shares start at 0, 128, 64
+    (32, 256, 152, (128, 4)),    # 16 x 4096 x 16384: a quarter tile
+    (128, 64, 152, (128, 1)),    # 16 x 16384 x 4096
+    (16, 32, 152, (64, 4)),      # 16 x 2048^2: 512 iterations, at most 64 CTAs of 8 blocks
+    (1, 1, 152, (1, 1)),         # one block
+])
+def test_small_m_grid_picks(tiles, kb, sms, want):
+    assert fgemm.small_m_grid(tiles, kb, sms) == want
+
+
+def test_small_m_grid_invariants():
+    rng = np.random.default_rng(7)
+    for _ in range(400):
+        tiles = int(rng.integers(1, 400))
+        kb = int(rng.integers(1, 600))
+        sms = int(rng.choice([8, 76, 132, 148, 152]))
+        ctas, phases = fgemm.small_m_grid(tiles, kb, sms)
+        iters = tiles * kb
+        most = max(1, min(sms, -(-iters // 8)))
+        assert 1 <= ctas <= most
+        if phases <= 4:
+            assert iters % ctas == 0 and ctas >= -(-most * 3 // 4)
+            share = iters // ctas
+            starts = {(i * share) % kb for i in range(ctas)}   # brute force
+            assert phases == len(starts)
+            # no grid in range with fewer phases (ties go to the larger grid)
+            for c in range(-(-most * 3 // 4), most + 1):
+                if iters % c == 0:
+                    other = len({(i * (iters // c)) % kb for i in range(c)})
+                    assert other > phases or (other == phases and c <= ctas)
+        else:
+            assert ctas == most and phases == most
+    assert fgemm.small_m_grid(0, 4, 152) == (0, 0)

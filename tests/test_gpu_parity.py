@@ -366,6 +366,8 @@ SMALL_M_CASES = [
     (64, 4096, 8192, 64),
     (16, 16384, 256, 16),    # more tiles than SMs
     (16, 128, 32768, 16),    # one tile shared by 64 CTAs (64 pieces)
+    (16, 16384, 4096, 16),   # 128 CTAs of one whole tile each
+    (16, 4096, 16384, 16),   # 128 CTAs of a quarter tile: 4 pieces a tile
 ]
 
 
