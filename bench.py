@@ -194,6 +194,15 @@ def measured_peaks():
     return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def roofline_bound(M, N, K, n_out, bias_elems, tflops, gbs):
+    """(algorithmic bytes, memory-bound?) of one 16-bit product: A, B, C and
+    the bias read or written once, against 2MNK flops; memory-bound when those
+    bytes at `gbs` take longer than the flops at `tflops`."""
+    alg_bytes = 2.0 * (M * K + K * N + M * n_out + bias_elems)
+    flops = 2.0 * M * N * K
+    return alg_bytes, bool(tflops and gbs) and alg_bytes / (gbs * 1e9) > flops / (tflops * 1e12)
+
+
 KERNEL_SOURCES = ("fgemm_kernel.cuh", "fgemm_kernel_pair.cuh", "fgemm_ptx.cuh",
                   "fgemm_internal.h", "fgemm_kern_classical.cu", "fgemm_kern_pair.cu",
                   "fgemm_kern_strassen1.cu", "fgemm_kern_strassen2.cu", "fgemm_kern_winograd1.cu",
@@ -433,10 +442,8 @@ def run_fgemm(args, rank, world):
     burst, sustained, hbm, src = measured_peaks()
     achieved = flops / (kern_avg_ms * 1e-3) / 1e12
     executed = achieved * (7.0 / 8.0) ** {"classical": 0, "strassen1": 1, "strassen2": 2, "winograd1": 1}[plan_algo]
-    # the bound: the algorithmic bytes (A, B, C and the bias, once each) at
-    # the measured copy rate against the flops at the measured bf16 peak
-    alg_bytes = 2.0 * (M * K + K * N + M * n_out) + (0 if bias0 is None else 2.0 * bias0.numel())
-    memory_bound = bool(hbm and burst) and alg_bytes / (hbm * 1e9) > flops / (burst * 1e12)
+    alg_bytes, memory_bound = roofline_bound(M, N, K, n_out, 0 if bias0 is None else bias0.numel(),
+                                             burst, hbm)
     traffic = ncu_traffic(args.workload, plan_algo, plan_tm, plan_tile)
     if memory_bound:
         gbs = alg_bytes / (kern_avg_ms * 1e-3) / 1e9

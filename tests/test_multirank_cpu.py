@@ -59,3 +59,20 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_roofline_bound_follows_arithmetic_intensity():
+    """The bench's roofline is tensor-bound for 4096^3 + bias and HBM-bound
+    for 16 x 16384^2, at the measured peaks of a GB300 (1951 TFLOP/s bf16,
+    6791 GB/s copy)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    b, mem = bench.roofline_bound(4096, 4096, 4096, 4096, 4096, 1951.4, 6791.4)
+    assert b == 2.0 * (3 * 4096 * 4096 + 4096) and not mem      # 14.8 us of bytes, 70 us of flops
+    b, mem = bench.roofline_bound(16, 16384, 16384, 16384, 0, 1951.4, 6791.4)
+    assert b == 2.0 * (16 * 16384 * 2 + 16384 * 16384) and mem  # 79 us of bytes, 4.4 us of flops
+    # SwiGLU writes half the columns
+    b, _ = bench.roofline_bound(8192, 28672, 4096, 14336, 0, 1951.4, 6791.4)
+    assert b == 2.0 * (8192 * 4096 + 4096 * 28672 + 8192 * 14336)
+    # no peaks known: never claims a memory bound
+    assert bench.roofline_bound(16, 16384, 16384, 16384, 0, None, None)[1] is False
