@@ -238,8 +238,9 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
   if (algo == FGEMM_ALGO_AUTO) return FGEMM_ERR_INVALID_ARG;
   if (!fgemm::form_is_legal(M, N, K, epi_kind, algo, tile_m, tile_n)) return FGEMM_ERR_UNSUPPORTED;
   if (tile_m < 128) {
-    // small-M kernel: every SM streams an equal share of the K blocks of all
-    // 128-column tiles; bound by B from HBM or by the narrow MMAs
+    // small-M kernel: every CTA of the grid fgemm_small_m_grid picks streams
+    // an equal share of the K blocks of all 128-column tiles; bound by B from
+    // HBM or by the narrow MMAs
     const int64_t tiles = ceil_div(N, 128), kb = ceil_div(K, fgemm::kBK);
     const int64_t iters = tiles * kb;
     int32_t phases = 0;

@@ -147,8 +147,8 @@ fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * Strassen forms; tile_m = 16, 32 or 64: the small-M kernel for M <= tile_m
  * (classical, no SWIGLU, tile_n = 128 columns of C per tile): it computes
  * C^T = B^T A^T so that the tensor-core rows run over N, and shares the K
- * blocks of all tiles evenly over the SMs (pieces of a tile are summed in a
- * fixed order). SWIGLU needs tile_n >= 128; the Strassen forms use tile_n in
+ * blocks of all tiles evenly over the CTAs of the grid fgemm_small_m_grid
+ * picks (pieces of a tile are summed in a fixed order). SWIGLU needs tile_n >= 128; the Strassen forms use tile_n in
  * {128, 256}, two levels only with tile_m = 128. tile_m = tile_n = 0 lets
  * the model choose; a zero in only one of them lets the model choose the
  * other.
@@ -362,14 +362,14 @@ typedef struct {
                             * fraction of peak (an N = tile_m MMA runs at most
                             * tile_m / 256 of the full rate) */
   double hbm_stream_eff;   /* fraction of hbm_gbs a kernel streaming B reaches */
-  double small_m_stream_eff; /* the same for the small-M kernel, whose CTAs read
-                              * B at different K (less DRAM page locality) */
+  double small_m_stream_eff; /* the same for the small-M kernel on a grid of more
+                              * than 4 phases: its CTAs draw unequal shares of
+                              * the bandwidth and the slowest sets the time */
   double small_m_fix_us;   /* its per-launch cost beyond the stream: the pieces'
                             * partial store, count and sum, and the slowest CTA */
-  double small_m_aligned_eff; /* fraction of hbm_gbs the small-M kernel reaches when
-                               * its shares start at no more than 4 K offsets of a
-                               * tile (fgemm_small_m_grid), so that its CTAs read the
-                               * same rows of B together */
+  double small_m_aligned_eff; /* fraction of hbm_gbs the small-M kernel reaches on
+                               * a grid whose shares start at no more than 4 K
+                               * offsets of a tile (fgemm_small_m_grid) */
 } fgemm_device_model_t;
 
 /*
