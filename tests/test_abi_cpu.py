@@ -359,6 +359,12 @@ def test_winograd_legality_and_model(L):
     (3, 5, 7),         # fewer iterations per CTA than one tile
     (200, 3, 152),     # more tiles than CTAs, short K
     (1, 400, 152),     # one tile over every CTA
+    # the grids fgemm_small_m_grid picks on 152 SMs
+    (128, 256, 128),   # 16 x 16384^2: one whole tile per CTA
+    (64, 128, 128),    # 16 x 8192^2: half a tile per CTA
+    (96, 192, 144),    # 16 x 12288^2: 2/3 of a tile per CTA
+    (32, 256, 128),    # 16 x 4096 x 16384: a quarter tile per CTA
+    (224, 64, 128),    # 16 x 28672 x 4096: 1.75 tiles per CTA
 ])
 def test_stream_k_schedule_covers_and_slots_are_unique(L, tiles, kb, ctas):
     ctas = min(ctas, tiles * kb)
