@@ -368,6 +368,8 @@ SMALL_M_CASES = [
     (16, 128, 32768, 16),    # one tile shared by 64 CTAs (64 pieces)
     (16, 16384, 4096, 16),   # 128 CTAs of one whole tile each
     (16, 4096, 16384, 16),   # 128 CTAs of a quarter tile: 4 pieces a tile
+    (16, 28672, 4096, 16),   # 224 tiles on 128 CTAs: shares of 1.75 tiles cross tile ends
+    (48, 16384, 8192, 64),   # ragged M in 64-row tiles, one whole tile per CTA
 ]
 
 
