@@ -53,10 +53,10 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=250)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="fgemm", choices=["fgemm", "reference"])
-    ap.add_argument("--workload", default="proj_4096_bf16_bias")
+    ap.add_argument("--workload", default="square_16384_bf16")
     ap.add_argument("--algo", default="auto")
     ap.add_argument("--tile", type=int, default=0, help="tile_n (0 = model)")
     ap.add_argument("--tile-m", type=int, default=0, help="tile_m: 128 one CTA, 256 CTA pair")
@@ -65,6 +65,8 @@ def parse():
                     help="K split of the last wave of CTA-pair tiles")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-forms", action="store_true",
+                    help="skip the same-run timing of the other forms and of the 256^3 case")
     ap.add_argument("--sweep", action="store_true",
                     help="decision-model check: every legal form/tile vs auto on the sweep shapes")
     ap.add_argument("--out", default=None, help="JSON-lines file for --sweep")
@@ -278,6 +280,12 @@ def cpu_oracle_sample(name, target_s=10.0, device_inputs=None, entries=None):
 
 # --------------------------------------------------------------- arms
 
+def workload_config(name):
+    """The workload's identity, the same in both arms: what the numbers are on."""
+    M, N, K, dtype, epi = workload_shape(name)
+    return {"workload": name, "M": M, "N": N, "K": K, "dtype": dtype, "epilogue": epi}
+
+
 def run_reference(args, rank, world):
     """The comparison arm: the fp64 CPU oracle, as it stands, on host cores."""
     if rank != 0:
@@ -306,12 +314,53 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "epilogue": epi},
+        "config": workload_config(args.workload),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def launches_per_call(algo, tile_m):
+    """Kernels of this library one fgemm_matmul_ex call launches."""
+    return 1
+
+
+def time_calls(fn, n, stream):
+    """Mean ms of n back-to-back calls of fn(i) (CUDA events around each on
+    `stream`), and the ms of the whole run."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(n):
+        ev[i][0].record(stream)
+        fn(i)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev), t0.elapsed_time(t1)
+
+
+def time_form(A, B, C, bias, epi, algo, handle, stream, target_ms=400.0, max_calls=50):
+    """One LCMA or classical form on the workload: the model's best tile of
+    that form, timed over enough calls for about target_ms (at least 3)."""
+    from complexity_matmul_tcgen05_gb300 import fgemm
+
+    def call(i):
+        fgemm.matmul(A, B, out=C, epilogue=epi, bias=bias, algo=algo, handle=handle)
+
+    call(0)
+    call(1)
+    torch.cuda.synchronize()
+    one, _ = time_calls(call, 1, stream)
+    n = int(max(3, min(max_calls, math.ceil(target_ms / max(one, 1e-3)))))
+    mean_ms, _ = time_calls(call, n, stream)
+    if handle.get_error() != fgemm.OK:
+        raise SystemExit(f"device error timing {algo}: {handle.last_message()}")
+    return mean_ms, n
 
 
 def run_fgemm(args, rank, world):
@@ -330,6 +379,12 @@ def run_fgemm(args, rank, world):
         biases.append(None if bias0 is None else bias0.clone())
     for i in range(sets):
         Cs.append(torch.empty((M, n_out), dtype=A0.dtype, device=dev))
+    if sets == 1:
+        l2_note = (f"inputs larger than the L2: A {M * K * 2 / 2 ** 20:.0f} MiB, "
+                   f"B {K * N * 2 / 2 ** 20:.0f} MiB, C {M * n_out * 2 / 2 ** 20:.0f} MiB")
+    else:
+        l2_note = (f"{sets} rotating input/output sets ({sets * set_bytes / 2 ** 20:.0f} MiB) "
+                   f"cycled between steps")
     handle = fgemm.default_handle()
     handle.set_split_mode(args.split)
     stream = torch.cuda.current_stream(dev)
@@ -362,8 +417,7 @@ def run_fgemm(args, rank, world):
             ev[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
-        if args.steps * 1.0 < 1e9:
-            time.sleep(0.25)  # at least one clock sample after the last step
+        time.sleep(0.25)  # at least one clock sample after the last step
     barrier(world)
     status = handle.get_error()
     if status != fgemm.OK:
@@ -374,74 +428,93 @@ def run_fgemm(args, rank, world):
     flops = 2.0 * M * N * K
     value = flops * world * args.steps / (total_ms * 1e-3) / 1e12
 
-    # End to end: every step uploads its inputs from pinned host memory,
-    # runs fgemm.matmul and downloads its result.  Uploads, products and
-    # downloads run on three streams with two device buffer sets, so step
-    # i+1's upload and step i-1's download overlap step i's product (a
-    # pipeline of products, as a serving loop runs it).
+    # The other forms on the same inputs in the same run (the classical
+    # kernel and the Strassen-like forms, each with the model's best tile of
+    # that form), after the timed region.
+    depth = {"classical": 0, "strassen1": 1, "strassen2": 2, "winograd1": 1}
+    burst, sustained, hbm, src = measured_peaks()
+    long_step = total_ms >= 500.0
+    peak = sustained if (long_step and sustained) else burst
+    peak_kind = "sustained" if (long_step and sustained) else "burst"
+    forms = {}
+    if rank == 0 and not args.no_forms:
+        w = inputs_mod().WORKLOADS.get(args.workload, {})
+        for form in ("classical", "strassen1", "strassen2", "winograd1"):
+            if form not in w.get("algos", ()) and not (form == "classical"):
+                continue
+            if fgemm.validate(M, N, K, 16, K, 16, N, 16, n_out, fgemm._dtype_code(A0.dtype),
+                              fgemm.make_epilogue(epi, 1.0, 16 if bias0 is not None else None),
+                              form) != fgemm.OK:
+                continue
+            f_algo, f_tm, f_tn, _ = handle.plan(M, N, K, fgemm._dtype_code(A0.dtype),
+                                                fgemm.make_epilogue(epi), algo=form)
+            ms, n = time_form(As[0], Bs[0], Cs[0], biases[0], epi, form, handle, stream)
+            eff = flops / (ms * 1e-3) / 1e12
+            executed = eff * (7.0 / 8.0) ** depth[form]
+            forms[form] = {"tile_m": f_tm, "tile_n": f_tn, "ms_per_call": ms, "calls": n,
+                           "effective_tflops": eff, "executed_tflops": executed,
+                           "executed_frac_of_peak": executed / peak if peak else None}
+        if "classical" in forms:
+            for f, d in forms.items():
+                d["vs_classical"] = d["effective_tflops"] / forms["classical"]["effective_tflops"]
+
+    # The small fp16 case (256^3, classical and one-level Strassen): launch-
+    # bound, so it is reported as time per call, back to back and as one
+    # launch alone.
+    small = None
+    if rank == 0 and not args.no_forms and args.workload != "square_256_f16":
+        sA, sB, _ = make_inputs("square_256_f16", dev)
+        sC = torch.empty((256, 256), dtype=sA.dtype, device=dev)
+        small = {"workload": "square_256_f16"}
+        for form in ("classical", "strassen1"):
+            def call(i, form=form):
+                fgemm.matmul(sA, sB, out=sC, algo=form, handle=handle)
+            for i in range(5):
+                call(i)
+            back_to_back, _ = time_calls(call, 200, stream)
+            alone = statistics.median(time_calls(call, 1, stream)[0] for _ in range(20))
+            f_algo, f_tm, f_tn, pred = handle.plan(256, 256, 256, fgemm.F16, None, algo=form)
+            small[form] = {"tile_m": f_tm, "tile_n": f_tn, "us_back_to_back": back_to_back * 1e3,
+                           "us_alone": alone * 1e3, "predicted_us": pred}
+        if handle.get_error() != fgemm.OK:
+            raise SystemExit(f"device error in the 256^3 case: {handle.last_message()}")
+
+    # End to end through the library's host-buffer path: fgemm.matmul on
+    # pinned CPU tensors uploads A, B (and the bias), runs the product and
+    # downloads C into a pinned host tensor, every step.
     e2e = None
     if not args.no_e2e:
         hA = A0.cpu().pin_memory()
         hB = B0.cpu().pin_memory()
         hbias = None if bias0 is None else bias0.cpu().pin_memory()
-        hC = [torch.empty((M, n_out), dtype=A0.dtype).pin_memory() for _ in range(2)]
-        dA = [torch.empty_like(A0) for _ in range(2)]
-        dB = [torch.empty_like(B0) for _ in range(2)]
-        dbias = [None if bias0 is None else torch.empty_like(bias0) for _ in range(2)]
-        dC = [torch.empty((M, n_out), dtype=A0.dtype, device=dev) for _ in range(2)]
-        s_up, s_mm, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        up_done = [torch.cuda.Event() for _ in range(2)]
-        mm_done = [torch.cuda.Event() for _ in range(2)]
-        down_done = [torch.cuda.Event() for _ in range(2)]
-        for b in range(2):   # all buffers start free
-            mm_done[b].record(s_mm)
-            down_done[b].record(s_down)
+        hC = torch.empty((M, n_out), dtype=A0.dtype).pin_memory()
 
         def e2e_step(i):
-            b = i % 2
-            with torch.cuda.stream(s_up):
-                s_up.wait_event(mm_done[b])          # product i-2 has read set b
-                dA[b].copy_(hA, non_blocking=True)
-                dB[b].copy_(hB, non_blocking=True)
-                if dbias[b] is not None:
-                    dbias[b].copy_(hbias, non_blocking=True)
-                up_done[b].record(s_up)
-            with torch.cuda.stream(s_mm):
-                s_mm.wait_event(up_done[b])
-                s_mm.wait_event(down_done[b])        # result i-2 has left set b
-                fgemm.matmul(dA[b], dB[b], out=dC[b], epilogue=epi, bias=dbias[b], algo=algo,
-                             tile_n=tile, tile_m=tile_m, handle=handle)
-                mm_done[b].record(s_mm)
-            with torch.cuda.stream(s_down):
-                s_down.wait_event(mm_done[b])
-                hC[b].copy_(dC[b], non_blocking=True)
-                down_done[b].record(s_down)
+            fgemm.matmul(hA, hB, out=hC, epilogue=epi, bias=hbias, algo=algo, tile_n=tile,
+                         tile_m=tile_m, handle=handle)
 
         for i in range(2):
             e2e_step(i)
         torch.cuda.synchronize()
-        n_e2e = max(3, min(args.steps, 20))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, min(args.steps, 40))
         barrier(world)
         torch.cuda.synchronize()
-        e0.record(s_up)
+        w0 = time.perf_counter()
         for i in range(n_e2e):
             e2e_step(i)
-        s_up.wait_stream(s_down)
-        e1.record(s_up)
         torch.cuda.synchronize()
+        e2e_ms = max_over_ranks((time.perf_counter() - w0) * 1e3, world)
         handle.set_stream(torch.cuda.current_stream(dev).cuda_stream)
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
         h2d = hA.numel() * 2 + hB.numel() * 2 + (0 if hbias is None else hbias.numel() * 2)
         e2e = {"value": flops * world * n_e2e / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hC[0].numel() * 2,
-               "pipeline": "upload / product / download on three streams, two buffer sets"}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hC.numel() * 2,
+               "steps": n_e2e, "path": "fgemm.matmul on pinned host tensors (upload, product, "
+               "download each step, host wall clock)"}
 
     if rank != 0:
         return
-    burst, sustained, hbm, src = measured_peaks()
     achieved = flops / (kern_avg_ms * 1e-3) / 1e12
-    executed = achieved * (7.0 / 8.0) ** {"classical": 0, "strassen1": 1, "strassen2": 2, "winograd1": 1}[plan_algo]
+    executed = achieved * (7.0 / 8.0) ** depth[plan_algo]
     alg_bytes, memory_bound = roofline_bound(M, N, K, n_out, 0 if bias0 is None else bias0.numel(),
                                              burst, hbm)
     traffic = ncu_traffic(args.workload, plan_algo, plan_tm, plan_tile)
@@ -451,25 +524,30 @@ def run_fgemm(args, rank, world):
                 "traffic": traffic, "algorithmic_bytes": alg_bytes,
                 "peak_source": f"{src} copy bandwidth", "tflops": achieved, "kernel_ms": kern_avg_ms}
     else:
-        roof = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": UNIT,
-                "frac": achieved / burst if burst else None, "traffic": traffic,
-                "peak_source": f"{src} bf16 dense (burst)", "executed_tflops": executed,
+        roof = {"bound": "tensor", "achieved": executed, "peak": peak, "unit": UNIT,
+                "frac": executed / peak if peak else None, "traffic": traffic,
+                "peak_source": f"{src} bf16 dense ({peak_kind}: the timed region is "
+                               f"{total_ms / 1e3:.2f} s of back-to-back launches)",
+                "effective_tflops": achieved, "executed_tflops": executed,
+                "algorithmic_flops": flops * (7.0 / 8.0) ** depth[plan_algo],
                 "kernel_ms": kern_avg_ms}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dtype == "bf16" else "f16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "M": M, "N": N, "K": K, "epilogue": epi,
-                   "algo": plan_algo, "tile_m": plan_tm, "tile_n": plan_tile,
-                   "k_split": args.split,
-                   "predicted_us": pred_us, "l2": f"{sets} rotating input/output sets "
-                   f"({sets * set_bytes / 2 ** 20:.0f} MiB) cycled between steps",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(args.workload),
+        "plan": {"algo": plan_algo, "tile_m": plan_tm, "tile_n": plan_tile, "k_split": args.split,
+                 "predicted_us": pred_us},
+        "l2": l2_note,
+        "parallelism": f"replicas x{world}",
         "roofline": roof,
-        "gpu_launches": args.steps,
+        "forms": forms,
+        "gpu_launches": args.steps * launches_per_call(plan_algo, plan_tm),
         "clocks": clk.summary(),
     }
+    if small is not None:
+        line["small_case"] = small
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline and world == 1:
@@ -480,6 +558,11 @@ def run_fgemm(args, rank, world):
             "sample": f"{e} stratified output entries (seed 3) of the same workload, each a "
                       f"K={K} fp64 dot product of decoded inputs, {s:.1f} s"}
     print(json.dumps(line), flush=True)
+
+
+def inputs_mod():
+    from complexity_matmul_tcgen05_gb300 import inputs
+    return inputs
 
 
 CANDIDATES = [("classical", 16, 128), ("classical", 32, 128), ("classical", 64, 128),

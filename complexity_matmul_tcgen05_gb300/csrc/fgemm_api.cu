@@ -579,12 +579,22 @@ fgemm_status_t fgemm_set_device_model(fgemm_handle_t h, const fgemm_device_model
 fgemm_status_t fgemm_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, fgemm_dtype_t dtype,
                           const fgemm_epilogue_t* epi, fgemm_algo_t* algo_out, int32_t* tile_m,
                           int32_t* tile_n, double* predicted_us) {
+  return fgemm_plan_ex(h, M, N, K, dtype, epi, FGEMM_ALGO_AUTO, 0, 0, algo_out, tile_m, tile_n,
+                       predicted_us);
+}
+
+fgemm_status_t fgemm_plan_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                             fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                             int32_t tile_m_in, int32_t tile_n_in, fgemm_algo_t* algo_out,
+                             int32_t* tile_m, int32_t* tile_n, double* predicted_us) {
   if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
   if (dtype != FGEMM_F16 && dtype != FGEMM_BF16)
     return set_msg(h, FGEMM_ERR_INVALID_ARG, "dtype must be FGEMM_F16 or FGEMM_BF16");
+  if (algo < FGEMM_ALGO_AUTO || algo > FGEMM_ALGO_WINOGRAD1)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "unknown algorithm");
   const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
   Plan p;
-  fgemm_status_t s = choose_plan(h, M, N, K, kind, FGEMM_ALGO_AUTO, 0, 0, &p);
+  fgemm_status_t s = choose_plan(h, M, N, K, kind, algo, tile_m_in, tile_n_in, &p);
   if (s != FGEMM_OK) return s;
   if (algo_out) *algo_out = p.algo;
   if (tile_m) *tile_m = p.tile_m;

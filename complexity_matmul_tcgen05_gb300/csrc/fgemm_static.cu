@@ -14,6 +14,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -175,12 +176,60 @@ extern "C" fgemm_status_t fgemm_strassen_matmul_static(
   s = encode(&p.tmap_b, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
              static_cast<uint64_t>(ldb), fgemm::kBK, p.is_bf16);
   if (s != FGEMM_OK) return s;
-  // The partial tiles need no clearing (each product's first contribution
-  // stores); the error word must start at zero.
-  e = cudaMemsetAsync(p.err, 0, sizeof(unsigned int), stream);
-  if (e != cudaSuccess)
-    return fail(FGEMM_ERR_CUDA, std::string("clearing the error word: ") + cudaGetErrorString(e));
+  // The partial tiles need no clearing: each product's first contribution to
+  // a block stores instead of adding.  The error word is not cleared here: it
+  // starts at zero when the library is loaded, a timeout latches into it and
+  // stays until fgemm_strassen_static_get_error reads and clears it, so a
+  // failed call cannot be hidden by a later one.
   e = fgemm::launch_gemm(tile_n, depth, p, &tab, grid, stream);
   if (e != cudaSuccess) return fail(FGEMM_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e));
   return FGEMM_OK;
+}
+
+extern "C" fgemm_status_t fgemm_strassen_static_get_error(void* cuda_stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FGEMM_ERR_NO_DEVICE, "cudaGetDevice failed");
+  void* scratch = nullptr;
+  int sms = 0;
+  fgemm_status_t s = setup_device(dev, &scratch, &sms);
+  if (s != FGEMM_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess)
+    return fail(FGEMM_ERR_CUDA, std::string("cudaStreamSynchronize: ") + cudaGetErrorString(e));
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess)
+    return fail(FGEMM_ERR_CUDA, std::string("reading the error word: ") + cudaGetErrorString(e));
+  if (word == 0) {
+    fgemm::set_thread_message("");
+    return FGEMM_OK;
+  }
+  e = cudaMemset(scratch, 0, sizeof(unsigned int));
+  if (e != cudaSuccess)
+    return fail(FGEMM_ERR_CUDA, std::string("clearing the error word: ") + cudaGetErrorString(e));
+  static const char* roles[] = {"producer", "mma", "epilogue", "operand-sum"};
+  const unsigned role = (word >> 24) & 0xF;
+  char text[160];
+  std::snprintf(text, sizeof(text),
+                "a bounded wait ran out in the %s role of block %u (word 0x%08x)",
+                role < 4 ? roles[role] : "?", word & 0xFFFFFFu, word);
+  return fail(FGEMM_ERR_TIMEOUT, text);
+}
+
+extern "C" fgemm_status_t fgemm_strassen_static_selftest_timeout(int32_t limit_ms,
+                                                                 void* cuda_stream) {
+  if (limit_ms < 1 || limit_ms > 10000) return fail(FGEMM_ERR_INVALID_ARG, "limit_ms must be in 1..10000");
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(FGEMM_ERR_NO_DEVICE, "cudaGetDevice failed");
+  void* scratch = nullptr;
+  int sms = 0;
+  fgemm_status_t s = setup_device(dev, &scratch, &sms);
+  if (s != FGEMM_OK) return s;
+  fgemm::KernelParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.err = static_cast<unsigned int*>(scratch);
+  p.spin_ns = static_cast<unsigned long long>(limit_ms) * 1000000ull;
+  const cudaError_t e = fgemm::launch_selftest_wait(p, static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? FGEMM_OK
+                          : fail(FGEMM_ERR_CUDA, std::string("self-test launch: ") + cudaGetErrorString(e));
 }

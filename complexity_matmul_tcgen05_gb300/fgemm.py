@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
         L.fgemm_plan.argtypes = [vp, i64, i64, i64, st, epi_p, ctypes.POINTER(st),
                                  ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(ctypes.c_double)]
+        L.fgemm_plan_ex.argtypes = [vp, i64, i64, i64, st, epi_p, st, i32, i32, ctypes.POINTER(st),
+                                    ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                    ctypes.POINTER(ctypes.c_double)]
         L.fgemm_get_error.argtypes = [vp]
         L.fgemm_selftest_wait_timeout.argtypes = [vp, i32]
         L.fgemm_calibrate.argtypes = [vp, ctypes.c_char_p]
@@ -116,6 +119,8 @@ def lib() -> ctypes.CDLL:
                                        ctypes.POINTER(ctypes.c_double)]
         L.fgemm_strassen_matmul_static.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, st,
                                                    epi_p, i32, i32, vp]
+        L.fgemm_strassen_static_get_error.argtypes = [vp]
+        L.fgemm_strassen_static_selftest_timeout.argtypes = [i32, vp]
         L.fgemm_model_split_tail.argtypes = [model_p, i64, i32, i32, i32, i32, ctypes.POINTER(i32)]
         L.fgemm_model_split_tail.restype = i32
         L.fgemm_split_work_item.argtypes = [i64, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
@@ -128,12 +133,13 @@ def lib() -> ctypes.CDLL:
         L.fgemm_get_device_model.argtypes = [vp, model_p]
         L.fgemm_set_device_model.argtypes = [vp, model_p]
         for name in ("fgemm_create", "fgemm_destroy", "fgemm_set_stream", "fgemm_matmul",
-                     "fgemm_matmul_ex", "fgemm_plan", "fgemm_get_error", "fgemm_calibrate",
+                     "fgemm_matmul_ex", "fgemm_plan", "fgemm_plan_ex", "fgemm_get_error", "fgemm_calibrate",
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
                      "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout",
                      "fgemm_set_split_mode", "fgemm_matmul_rms", "fgemm_matmul_mx",
-                     "fgemm_mx_to_bf16"):
+                     "fgemm_mx_to_bf16", "fgemm_strassen_static_get_error",
+                     "fgemm_strassen_static_selftest_timeout"):
             getattr(L, name).restype = st
         _lib = L
         return L
@@ -253,15 +259,18 @@ class Handle:
                                       ctypes.byref(epilogue) if epilogue is not None else None,
                                       ALGOS[algo], tile_m, tile_n, ctypes.byref(rms))
 
-    def plan(self, M, N, K, dtype: int = BF16, epilogue: Epilogue | None = None):
+    def plan(self, M, N, K, dtype: int = BF16, epilogue: Epilogue | None = None,
+             algo: str = "auto", tile_m: int = 0, tile_n: int = 0):
+        """(algorithm, tile_m, tile_n, predicted us) of the model's choice,
+        restricted to a form / tile when those are given."""
         a = ctypes.c_int()
         tm = ctypes.c_int32()
         tn = ctypes.c_int32()
         us = ctypes.c_double()
-        _check(lib().fgemm_plan(self._h, M, N, K, dtype,
-                                ctypes.byref(epilogue) if epilogue is not None else None,
-                                ctypes.byref(a), ctypes.byref(tm), ctypes.byref(tn),
-                                ctypes.byref(us)), self._h)
+        _check(lib().fgemm_plan_ex(self._h, M, N, K, dtype,
+                                   ctypes.byref(epilogue) if epilogue is not None else None,
+                                   ALGOS[algo], tile_m, tile_n, ctypes.byref(a), ctypes.byref(tm),
+                                   ctypes.byref(tn), ctypes.byref(us)), self._h)
         return ALGO_NAMES[a.value], tm.value, tn.value, us.value
 
     def get_error(self) -> int:

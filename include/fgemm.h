@@ -256,6 +256,18 @@ fgemm_status_t fgemm_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
                           fgemm_algo_t* algo_out, int32_t* tile_m,
                           int32_t* tile_n, double* predicted_us);
 
+/*
+ * As fgemm_plan, with the choice restricted: algo (FGEMM_ALGO_AUTO: any
+ * form), tile_m_in and tile_n_in (0: any) constrain the candidates the model
+ * ranks, as a forced form or tile in fgemm_matmul_ex does; the result is
+ * what that call would launch. FGEMM_ERR_UNSUPPORTED if no candidate is
+ * legal for the shape.
+ */
+fgemm_status_t fgemm_plan_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                             fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                             int32_t tile_m_in, int32_t tile_n_in, fgemm_algo_t* algo_out,
+                             int32_t* tile_m, int32_t* tile_n, double* predicted_us);
+
 /* Synchronises the handle's stream, then returns and clears the latched
  * device error (FGEMM_OK, FGEMM_ERR_TIMEOUT or FGEMM_ERR_CUDA). */
 fgemm_status_t fgemm_get_error(fgemm_handle_t h);
@@ -323,14 +335,34 @@ fgemm_status_t fgemm_validate(int64_t M, int64_t N, int64_t K, const void* A,
  * leaves its contents behind; calls whose kernels overlap on the GPU (other
  * streams, or other host threads) race on it and must be serialised by the
  * caller. A bounded wait that runs out inside the kernel (it does not happen
- * unless the GPU stalls for about a second) leaves C incomplete and is not
- * reported by this call.
+ * unless the GPU stalls for about a second) leaves C incomplete; the kernel
+ * latches a code in the array's error word, which stays set until
+ * fgemm_strassen_static_get_error reads and clears it. While it is set,
+ * later calls on the same device give up their waits early (as a handle's
+ * calls do until fgemm_get_error), so check it before trusting results.
  */
 fgemm_status_t fgemm_strassen_matmul_static(
     int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
     int64_t ldb, void* C, int64_t ldc, fgemm_dtype_t dtype,
     const fgemm_epilogue_t* epi, int32_t depth, int32_t tile_n,
     void* cuda_stream);
+
+/*
+ * The error word of fgemm_strassen_matmul_static on the current device:
+ * synchronises cuda_stream (NULL = legacy stream), then returns FGEMM_OK, or
+ * FGEMM_ERR_TIMEOUT (fgemm_last_message(NULL) names the role and block)
+ * after clearing the word. Allocates nothing.
+ */
+fgemm_status_t fgemm_strassen_static_get_error(void* cuda_stream);
+
+/*
+ * Failure-detection self-test of the allocation-free path: one block waits
+ * on an mbarrier nothing completes, through the bounded wait of the GEMM
+ * kernels, with the limit limit_ms (1..10000); it gives up, latches a timeout
+ * in the static error word and exits normally (no fault, no trap).
+ * Asynchronous on cuda_stream. Allocates nothing.
+ */
+fgemm_status_t fgemm_strassen_static_selftest_timeout(int32_t limit_ms, void* cuda_stream);
 
 /* ------------------------------------------------------------------------
  * Decision model, host only (no device needed). FalconGEMM summary,

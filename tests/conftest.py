@@ -25,3 +25,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Prints every error a parity check measured, with the bound it was held
+    to (tests record them through parity_util.record)."""
+    mod = sys.modules.get("parity_util")
+    recs = getattr(mod, "RECORDS", None) if mod else None
+    if not recs:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", f"measured errors ({len(recs)} checks): measured / bound")
+    worst = max(recs, key=lambda r: r[2] / r[3] if r[3] > 0 else 0.0)
+    for name, qty, got, bound in recs:
+        ratio = got / bound if bound > 0 else float("nan")
+        tr.write_line(f"{got:10.3e} / {bound:8.1e} ({ratio:5.2f})  {qty:28s} {name}")
+    tr.write_line(f"closest to its bound: {worst[1]} of {worst[0]}: {worst[2]:.3e} / {worst[3]:.1e}")

@@ -251,6 +251,79 @@ def test_emulated_on_ternary_inputs_is_exact(depth):
     assert np.array_equal(oracle.strassen_emulated(A, B, depth, "bf16"), A @ B)
 
 
+# Textbook one-level Strassen as coefficient matrices over the 2 x 2 blocks
+# [X11, X12, X21, X22]: product p multiplies (U[p] . A-blocks) by (V[p] .
+# B-blocks), and output block q collects W[q] . (M1 .. M7).  Two levels are
+# the Kronecker squares of U, V and W (written out independently of the
+# oracle's recursion).
+_U = np.array([[1, 0, 0, 1], [0, 0, 1, 1], [1, 0, 0, 0], [0, 0, 0, 1],
+               [1, 1, 0, 0], [-1, 0, 1, 0], [0, 1, 0, -1]], dtype=np.float64)
+_V = np.array([[1, 0, 0, 1], [1, 0, 0, 0], [0, 1, 0, -1], [-1, 0, 1, 0],
+               [0, 0, 0, 1], [1, 1, 0, 0], [0, 0, 1, 1]], dtype=np.float64)
+_W = np.array([[1, 0, 0, 1, -1, 0, 1], [0, 0, 1, 0, 1, 0, 0],
+               [0, 1, 0, 1, 0, 0, 0], [1, -1, 1, 0, 0, 1, 0]], dtype=np.float64)
+
+
+def _blocks2(X):
+    """The 16 scalar entries of a 4 x 4 matrix in two-level block order:
+    index 4 * outer + inner, each of outer / inner = 2 * row_half + col_half."""
+    out = np.empty(16)
+    for o in range(4):
+        for i in range(4):
+            r = 2 * (o >> 1) + (i >> 1)
+            c = 2 * (o & 1) + (i & 1)
+            out[4 * o + i] = X[r, c]
+    return out
+
+
+def _bf16_once(x):
+    """fp64 -> fp32 -> bf16 (both round-to-nearest-even), as torch casts."""
+    return torch.tensor(x, dtype=torch.float64).to(torch.float32).to(torch.bfloat16) \
+        .to(torch.float64).numpy()
+
+
+def test_strassen_coefficients_reproduce_the_product():
+    # the coefficient matrices above are the textbook scheme: exact on random 2 x 2
+    rng = np.random.default_rng(21)
+    A, B = rng.uniform(-1, 1, (2, 2)), rng.uniform(-1, 1, (2, 2))
+    m = (_U @ A.reshape(4)) * (_V @ B.reshape(4))
+    assert np.allclose((_W @ m).reshape(2, 2), A @ B, rtol=0, atol=1e-15)
+    assert np.allclose(oracle.strassen(A, B, 1), (_W @ m).reshape(2, 2), rtol=0, atol=1e-15)
+
+
+def test_strassen_emulated_depth2_rounds_each_leaf_once_from_its_quarter_blocks():
+    # 4 x 4 scalars, B = I: every leaf operand of the 49 products is a signed
+    # sum of up to four scalar quarter blocks.  The leaf of (M1, M1) sums
+    # A00 + A11 + A22 + A33 (outer A11 + A22, then inner X11 + X22).  With
+    # A00 = 1, A22 = 2^-10, A11 = 2^-8, A33 = 0 the exact sum 1 + 2^-8 + 2^-10
+    # is above the bf16 midpoint and rounds to 1 + 2^-7.  Rounding at the
+    # outer level first (1 + 2^-10 -> 1, then 1 + 2^-8 is a tie -> 1) or
+    # rounding the running sum would give 1, and that shows in C.
+    A = np.zeros((4, 4))
+    A[0, 0], A[2, 2], A[1, 1], A[3, 3] = 1.0, 2.0 ** -10, 2.0 ** -8, 0.0
+    A[0, 3], A[3, 0], A[1, 2] = 0.375, -0.5, 0.25
+    B = np.eye(4)
+    U2, V2, W2 = np.kron(_U, _U), np.kron(_V, _V), np.kron(_W, _W)
+    a, b = _blocks2(A), _blocks2(B)
+    S = _bf16_once(U2 @ a)               # every leaf rounded once from its exact sum
+    T = _bf16_once(V2 @ b)
+    c = W2 @ (S * T)
+    expect = np.empty((4, 4))
+    for o in range(4):
+        for i in range(4):
+            expect[2 * (o >> 1) + (i >> 1), 2 * (o & 1) + (i & 1)] = c[4 * o + i]
+    got = oracle.strassen_emulated(A, B, 2, "bf16")
+    assert np.allclose(got, expect, rtol=0, atol=1e-15)
+    # the wrong placement: round the outer sums first, then the leaf sums
+    outer_a = _bf16_once(np.kron(_U, np.eye(4)) @ a)        # 7 outer sums x 4 inner entries
+    wrong_S = _bf16_once(np.kron(np.eye(7), _U) @ outer_a)
+    assert not np.allclose(wrong_S, S)
+    wrong = W2 @ (wrong_S * T)
+    assert not np.allclose(c, wrong, rtol=0, atol=1e-6)    # the tie is visible in C
+    # no rounding at all gives A exactly (B = I), so the rounding shows too
+    assert not np.allclose(got, A, rtol=0, atol=1e-6)
+
+
 @pytest.mark.parametrize("dtype,depth,lo,hi", [("bf16", 1, 3e-4, 5e-3), ("bf16", 2, 6e-4, 1e-2),
                                                ("f16", 1, 4e-5, 1e-3)])
 def test_emulated_rounding_error_is_in_the_expected_band(dtype, depth, lo, hi):
