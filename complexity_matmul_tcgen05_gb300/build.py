@@ -30,6 +30,7 @@ SOURCES = [
     "fgemm_kern_winograd1.cu",
     "fgemm_kern_skinny.cu",
     "fgemm_kern_mx.cu",
+    "fgemm_kern_lcma.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,

@@ -351,6 +351,106 @@ fgemm_status_t prepare_split(fgemm_handle_t h, KernelParams* p, int split, int p
 }
 
 
+// One Strassen-like level on CTA pairs with the summed operands streamed
+// through HBM: the scheme's distinct summed operands become temporaries
+// (formed by one pre-pass launch), the product kernel reads every operand
+// through a tensor map of A, B or the temporaries.  Workspace layout: the
+// product kernel's partial tiles, then the A and the B temporaries.
+fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTable& tab, int bn,
+                           const void* A, int64_t lda, const void* B, int64_t ldb) {
+  using fgemm::LcmaFormParams;
+  using fgemm::LcmaParams;
+  LcmaParams L;
+  std::memset(&L, 0, sizeof(L));
+  LcmaFormParams F;
+  std::memset(&F, 0, sizeof(F));
+  const int np = 7;
+  // the distinct summed operands of each side (a single positive term is a
+  // raw block of A or B, read in place)
+  auto operand = [&](int n, const uint8_t* codes, fgemm::LcmaFormJob& J, uint8_t* is_temp,
+                     uint8_t* idx) {
+    if (n == 1 && !(codes[0] & fgemm::kTermNeg)) {
+      *is_temp = 0;
+      *idx = codes[0] & fgemm::kTermIndexMask;
+      return;
+    }
+    int8_t coef[16] = {0};
+    for (int i = 0; i < n; ++i)
+      coef[codes[i] & fgemm::kTermIndexMask] += (codes[i] & fgemm::kTermNeg) ? -1 : 1;
+    int t = 0;
+    while (t < J.ntemp && std::memcmp(J.coef[t], coef, sizeof(coef)) != 0) ++t;
+    if (t == J.ntemp) {
+      std::memcpy(J.coef[t], coef, sizeof(coef));
+      for (int q = 0; q < 16; ++q)
+        if (coef[q] != 0) J.block_mask |= 1u << q;
+      ++J.ntemp;
+    }
+    *is_temp = 1;
+    *idx = static_cast<uint8_t>(t);
+  };
+  for (int pr = 0; pr < np; ++pr) {
+    fgemm::LcmaProduct& P = L.prod[pr];
+    operand(tab.na[pr], tab.a[pr], F.job[0], &P.a_temp, &P.a_idx);
+    operand(tab.nb[pr], tab.b[pr], F.job[1], &P.b_temp, &P.b_idx);
+    P.nc = tab.nc[pr];
+    for (int t = 0; t < P.nc; ++t)
+      P.c[t] = static_cast<uint8_t>(tab.c[pr][t] & (fgemm::kTermIndexMask | fgemm::kTermNeg));
+  }
+  const int ntA = F.job[0].ntemp, ntB = F.job[1].ntemp;
+  const int fit = fgemm::lcma_pair_clusters_fit(bn);
+  if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the Strassen pair launch");
+  const long long positions = p.num_units;
+  L.units = positions * np;
+  const int clusters = static_cast<int>(std::min<long long>(fit, L.units));
+  const size_t slot_bytes = static_cast<size_t>(2) * clusters * fgemm::lcma_slot_floats(bn, 1) * sizeof(float);
+  const size_t ta_elems = static_cast<size_t>(ntA) * p.sub_m * p.sub_k;
+  const size_t tb_elems = static_cast<size_t>(ntB) * p.sub_k * p.sub_n;
+  auto align = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t ta_off = align(slot_bytes), tb_off = ta_off + align(ta_elems * 2);
+  fgemm_status_t s = ensure_workspace(h, tb_off + align(tb_elems * 2));
+  if (s != FGEMM_OK) return s;
+  s = ensure_counters(h, static_cast<size_t>(positions) * 8);  // 2 CTAs x 4 epilogue warps
+  if (s != FGEMM_OK) return s;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(h->workspace);
+  uint16_t* TA = reinterpret_cast<uint16_t*>(ws + ta_off);
+  uint16_t* TB = reinterpret_cast<uint16_t*>(ws + tb_off);
+  p.workspace = h->workspace;
+  p.split_ctr = h->split_ctr;
+  p.split_gen = h->split_gen;
+  p.num_products = np;
+  L.tmap_ta = p.tmap_a;
+  L.tmap_tb = p.tmap_b;
+  if (ntA > 0) {
+    s = encode_tmap(h, &L.tmap_ta, TA, static_cast<uint64_t>(p.sub_k),
+                    static_cast<uint64_t>(ntA) * p.sub_m, static_cast<uint64_t>(p.sub_k), fgemm::kBM,
+                    p.is_bf16);
+    if (s != FGEMM_OK) return s;
+  }
+  if (ntB > 0) {
+    s = encode_tmap(h, &L.tmap_tb, TB, static_cast<uint64_t>(p.sub_n),
+                    static_cast<uint64_t>(ntB) * p.sub_k, static_cast<uint64_t>(p.sub_n), fgemm::kBK,
+                    p.is_bf16);
+    if (s != FGEMM_OK) return s;
+  }
+  L.k = p;
+  F.is_bf16 = p.is_bf16;
+  F.job[0].src = static_cast<const uint16_t*>(A);
+  F.job[0].ld = lda;
+  F.job[0].dst = TA;
+  F.job[0].rows = p.sub_m;
+  F.job[0].cols = p.sub_k;
+  F.job[1].src = static_cast<const uint16_t*>(B);
+  F.job[1].ld = ldb;
+  F.job[1].dst = TB;
+  F.job[1].rows = p.sub_k;
+  F.job[1].cols = p.sub_n;
+  cudaError_t e = fgemm::launch_lcma_form(F, h->num_sms, h->stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "operand-sum pre-pass launch");
+  e = fgemm::launch_lcma_pair(bn, L, clusters, h->stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "Strassen pair kernel launch");
+  return FGEMM_OK;
+}
+
 // The small-M kernel (tile_m = mp in {16, 32, 64}, M <= mp): C^T = B^T A^T
 // over 128-column tiles of C, the K blocks of all tiles shared out over the
 // SMs.  A's descriptor uses an {64, mp} box; partial slots and counters are
@@ -402,52 +502,12 @@ double getenv_double(const char* name, double dflt) {
 
 // ------------------------------------------------- calibration JSON I/O
 
-bool json_number(const std::string& text, const char* key, double* out) {
-  const std::string pat = std::string("\"") + key + "\"";
-  size_t p = text.find(pat);
-  if (p == std::string::npos) return false;
-  p = text.find(':', p + pat.size());
-  if (p == std::string::npos) return false;
-  const char* s = text.c_str() + p + 1;
-  char* end = nullptr;
-  double d = std::strtod(s, &end);
-  if (end == s) return false;
-  *out = d;
-  return true;
-}
-
 fgemm_status_t load_calibration(fgemm_handle_t h, const char* path) {
-  FILE* f = std::fopen(path, "rb");
-  if (!f) return set_msg(h, FGEMM_ERR_CALIBRATION, std::string("cannot open ") + path);
-  std::string text;
-  char buf[4096];
-  size_t n;
-  while ((n = std::fread(buf, 1, sizeof(buf), f)) > 0) text.append(buf, n);
-  std::fclose(f);
   fgemm_device_model_t m = h->model;
-  struct {
-    const char* key;
-    double* dst;
-  } fields[] = {
-      {"peak_tflops", &m.peak_tflops},         {"hbm_gbs", &m.hbm_gbs},
-      {"eff_classical_64", &m.eff_classical[0]}, {"eff_classical_128", &m.eff_classical[1]},
-      {"eff_classical_256", &m.eff_classical[2]}, {"eff_pair_128", &m.eff_pair[0]},
-      {"eff_pair_256", &m.eff_pair[1]},         {"eff_strassen1_128", &m.eff_strassen[0][0]},
-      {"eff_strassen1_pair_128", &m.eff_strassen_pair[0]},
-      {"eff_strassen1_pair_256", &m.eff_strassen_pair[1]},
-      {"eff_strassen1_256", &m.eff_strassen[0][1]}, {"eff_strassen2_128", &m.eff_strassen[1][0]},
-      {"eff_strassen2_256", &m.eff_strassen[1][1]}, {"launch_us", &m.launch_us},
-      {"tile_fill_us", &m.tile_fill_us},        {"l2_bytes", &m.l2_bytes},
-      {"l2_gbs", &m.l2_gbs},                    {"split_fix_us", &m.split_fix_us},
-      {"eff_winograd1_128", &m.eff_winograd[0]}, {"eff_winograd1_256", &m.eff_winograd[1]},
-      {"hbm_stream_eff", &m.hbm_stream_eff},     {"small_m_stream_eff", &m.small_m_stream_eff},
-      {"small_m_fix_us", &m.small_m_fix_us},     {"small_m_aligned_eff", &m.small_m_aligned_eff},
-  };
-  int found = 0;
-  for (auto& fd : fields) found += json_number(text, fd.key, fd.dst) ? 1 : 0;
-  if (found == 0) return set_msg(h, FGEMM_ERR_CALIBRATION, std::string("no model fields in ") + path);
-  if (!(m.peak_tflops > 0) || !(m.hbm_gbs > 0))
-    return set_msg(h, FGEMM_ERR_CALIBRATION, "calibration has a non-positive peak or bandwidth");
+  const fgemm_status_t s = fgemm_model_load_json(path, &m);
+  if (s != FGEMM_OK)
+    return set_msg(h, s == FGEMM_ERR_CALIBRATION ? s : FGEMM_ERR_CALIBRATION,
+                   std::string("calibration file unreadable or malformed: ") + path);
   h->model = m;
   h->plans.clear();
   return FGEMM_OK;
@@ -509,8 +569,8 @@ fgemm_status_t fgemm_create(fgemm_handle_t* out) {
   fgemm_handle_t h = new fgemm_handle_s();
   h->device = dev;
   h->num_sms = sms;
-  fgemm_model_default(&h->model, sms, getenv_double("FGEMM_PEAK_TFLOPS", 2250.0 * sms / 152.0),
-                      getenv_double("FGEMM_HBM_GBS", 7900.0));
+  fgemm_model_default(&h->model, sms, getenv_double("FGEMM_PEAK_TFLOPS", 0.0),
+                      getenv_double("FGEMM_HBM_GBS", 0.0));
   if (l2 > 0) h->model.l2_bytes = l2;
   const double spin_ms = getenv_double("FGEMM_SPIN_LIMIT_MS", 1000.0);
   h->spin_ns = static_cast<unsigned long long>(std::max(1.0, spin_ms) * 1e6);
@@ -687,16 +747,7 @@ fgemm_status_t matmul_impl(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, co
                   static_cast<uint64_t>(ldb), fgemm::kBK, p.is_bf16);
   if (s != FGEMM_OK) return s;
 
-  if (bm == 256 && d == 1) {
-    // one persistent CTA per SM at most: 4 partial tiles of 128 x bn each
-    const size_t per_cta = 4 * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float);
-    s = ensure_workspace(h, per_cta * static_cast<size_t>(h->num_sms));
-    if (s != FGEMM_OK) return s;
-    p.workspace = h->workspace;
-    cudaError_t e = fgemm::launch_strassen_pair(bn, p, tab, h->num_sms / 2, h->stream);
-    if (e != cudaSuccess) return cuda_fail(h, e, "Strassen pair kernel launch");
-    return FGEMM_OK;
-  }
+  if (bm == 256 && d == 1) return launch_lcma(h, p, tab, bn, A, lda, B, ldb);
   if (bm == 256) {
     const int fit = fgemm::gemm_pair_clusters_fit(bn);
     if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the CTA-pair launch");
@@ -897,8 +948,13 @@ __global__ void fill_pattern_kernel(uint16_t* x, long long n, uint32_t seed, int
 }  // namespace
 
 extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out_path) {
+  return fgemm_calibrate_ex(h, 8192, json_out_path);
+}
+
+extern "C" fgemm_status_t fgemm_calibrate_ex(fgemm_handle_t h, int64_t n, const char* json_out_path) {
   if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
-  const int64_t n = 8192;
+  if (n < 1024 || n > 16384 || n % 1024 != 0)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "calibration size must be a multiple of 1024 in [1024, 16384]");
   uint16_t *A = nullptr, *B = nullptr, *C = nullptr, *Xa = nullptr, *Xb = nullptr;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   fgemm_status_t status = FGEMM_OK;
@@ -995,11 +1051,17 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
       m.eff_winograd[i] = flops * 7.0 / 8.0 / (us * 1e6) / m.peak_tflops;
     }
     if (status != FGEMM_OK) break;
-    {  // launch + fill: one tiny tile
+    {  // launch cost: back-to-back K = 0 products (one trivial kernel each)
       double us = 0;
-      if (!time_gemm(128, 128, 64, FGEMM_ALGO_CLASSICAL, 128, 128, &us)) break;
-      m.launch_us = us;
-      m.tile_fill_us = std::max(0.2, us * 0.25);
+      if (!time_gemm(128, 128, 0, FGEMM_ALGO_AUTO, 0, 0, &us)) break;
+      m.launch_us = std::max(0.5, us);
+      // pipeline fill and drain: one 128 x 128 tile at two K lengths, the
+      // intercept of its time in K less the launch
+      double t1 = 0, t2 = 0;
+      if (!time_gemm(128, 128, 1024, FGEMM_ALGO_CLASSICAL, 128, 128, &t1)) break;
+      if (!time_gemm(128, 128, 4096, FGEMM_ALGO_CLASSICAL, 128, 128, &t2)) break;
+      const double intercept = t1 - (t2 - t1) / 3.0;
+      m.tile_fill_us = std::max(0.5, intercept - m.launch_us);
     }
     {  // streaming bandwidth: device-to-device copy, read + write bytes
       check(cudaMemcpyAsync(Xb, Xa, copy_bytes, cudaMemcpyDeviceToDevice, h->stream), "copy");
@@ -1024,25 +1086,7 @@ extern "C" fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out
   if (status != FGEMM_OK) return status;
   h->model = m;
   h->plans.clear();
-  if (json_out_path) {
-    FILE* f = std::fopen(json_out_path, "w");
-    if (!f) return set_msg(h, FGEMM_ERR_CALIBRATION, std::string("cannot write ") + json_out_path);
-    std::fprintf(f,
-                 "{\n  \"num_sms\": %d,\n  \"peak_tflops\": %.3f,\n  \"hbm_gbs\": %.3f,\n"
-                 "  \"eff_classical_64\": %.5f,\n  \"eff_classical_128\": %.5f,\n"
-                 "  \"eff_classical_256\": %.5f,\n  \"eff_pair_128\": %.5f,\n"
-                 "  \"eff_pair_256\": %.5f,\n  \"eff_strassen1_128\": %.5f,\n"
-                 "  \"eff_strassen1_256\": %.5f,\n  \"eff_strassen2_128\": %.5f,\n"
-                 "  \"eff_strassen2_256\": %.5f,\n  \"eff_strassen1_pair_128\": %.5f,\n"
-                 "  \"eff_strassen1_pair_256\": %.5f,\n  \"launch_us\": %.3f,\n  \"tile_fill_us\": %.3f,\n"
-                 "  \"l2_bytes\": %.0f,\n  \"l2_gbs\": %.1f,\n  \"split_fix_us\": %.3f,\n"
-                 "  \"eff_winograd1_128\": %.5f,\n  \"eff_winograd1_256\": %.5f\n}\n",
-                 m.num_sms, m.peak_tflops, m.hbm_gbs, m.eff_classical[0], m.eff_classical[1],
-                 m.eff_classical[2], m.eff_pair[0], m.eff_pair[1], m.eff_strassen[0][0], m.eff_strassen[0][1], m.eff_strassen[1][0],
-                 m.eff_strassen[1][1], m.eff_strassen_pair[0], m.eff_strassen_pair[1], m.launch_us,
-                 m.tile_fill_us, m.l2_bytes, m.l2_gbs, m.split_fix_us, m.eff_winograd[0],
-                 m.eff_winograd[1]);
-    std::fclose(f);
-  }
+  if (json_out_path && fgemm_model_save_json(&m, json_out_path) != FGEMM_OK)
+    return set_msg(h, FGEMM_ERR_CALIBRATION, std::string("cannot write ") + json_out_path);
   return FGEMM_OK;
 }

@@ -197,6 +197,68 @@ struct StrassenParams {
   StrassenTable tab;
 };
 
+// ---------------------------------------------------------------------------
+// Low-complexity forms on CTA pairs with the summed operands streamed
+// through HBM: a streaming pre-pass forms each summed operand of the scheme
+// once (fp32 sum of the exact blocks, one rounding) into temporaries, then
+// one persistent launch runs the block products on the classical pair
+// mainloop and folds each product into the output blocks it feeds.
+
+// Product p of a scheme as the product kernel reads it: its A operand is
+// raw block a_idx of A (a_temp == 0) or temporary a_idx (a_temp == 1), the
+// same for B; its accumulator is added, with the codes' signs, into output
+// blocks c[0 .. nc) (codes as in StrassenTable: block index | kTermNeg).
+struct LcmaProduct {
+  uint8_t a_temp, a_idx, b_temp, b_idx;
+  uint8_t nc;
+  uint8_t c[kMaxTerms];
+};
+
+struct LcmaParams {
+  KernelParams k;        // tmap_a / tmap_b map A and B; k.workspace holds the partial tiles
+  CUtensorMap tmap_ta;   // A temporaries: inner sub_k, outer ntemp_a * sub_m, box {64, 128}
+  CUtensorMap tmap_tb;   // B temporaries: inner sub_n, outer ntemp_b * sub_k, box {64, 64}
+  long long units;       // output positions * num_products
+  LcmaProduct prod[kMaxProducts];
+};
+
+// One matrix of the pre-pass: the `rows` x `cols` blocks of src (block q at
+// block row q >> depth, block column q & (2^depth - 1)) are combined into
+// ntemp temporaries, temporary t = sum_q coef[t][q] * block_q (coef in
+// {-1, 0, 1}), stored one after another, each rows x cols with pitch cols.
+struct LcmaFormJob {
+  const uint16_t* src;
+  long long ld;
+  uint16_t* dst;
+  int rows, cols;
+  int ntemp;
+  uint32_t block_mask;  // blocks some temporary reads
+  int8_t coef[kMaxProducts][16];
+};
+
+struct LcmaFormParams {
+  LcmaFormJob job[2];  // A and B
+  int is_bf16;
+};
+
+// Per-CTA partial tiles of the product kernel: three slots (a pair's first
+// output position, its last, and the ones between) of 4^depth blocks of
+// 128 x bn fp32.
+inline size_t lcma_slot_floats(int bn, int depth) {
+  return static_cast<size_t>(3) * (size_t{1} << (2 * depth)) * 128 * static_cast<size_t>(bn);
+}
+
+// The pre-pass (depth 1) over both jobs in one launch.
+cudaError_t launch_lcma_form(const LcmaFormParams& f, int num_sms, cudaStream_t stream);
+
+// The product kernel for one Strassen-like level on `clusters` CTA pairs
+// (bn = 128 or 256); p.k.split_ctr / split_gen carry the position counters
+// (8 per output position) for positions whose products span two pairs.
+cudaError_t launch_lcma_pair(int bn, const LcmaParams& p, int clusters, cudaStream_t stream);
+
+// How many clusters of the product kernel fit on the current device.
+int lcma_pair_clusters_fit(int bn);
+
 // Error word layout written by a kernel whose bounded wait ran out.
 constexpr unsigned int kErrTimeout = 0x80000000u;
 // bits [24,28): role (0 producer, 1 mma, 2 epilogue, 3 operand-sum), [0,24): block
@@ -248,10 +310,6 @@ cudaError_t launch_gemm_pair(int bn, const KernelParams& p, int clusters, cudaSt
 // How many clusters of the classical pair kernel fit on the current device
 // at once (0 on error).
 int gemm_pair_clusters_fit(int bn);
-
-// One-level Strassen on CTA pairs (256 x bn tiles of the half-size block space).
-cudaError_t launch_strassen_pair(int bn, const KernelParams& p, const StrassenTable& tab, int max_clusters,
-                                 cudaStream_t stream);
 
 // The Strassen coefficient table of `depth` levels (0: one trivial product).
 const StrassenTable& strassen_table(int depth);

@@ -21,13 +21,4 @@ int gemm_pair_clusters_fit(int bn) {
   }
 }
 
-cudaError_t launch_strassen_pair(int bn, const KernelParams& p, const StrassenTable& tab, int max_clusters,
-                                 cudaStream_t stream) {
-  switch (bn) {
-    case 128: return launch_strassen_pair_t<128>(p, tab, max_clusters, stream);
-    case 256: return launch_strassen_pair_t<256>(p, tab, max_clusters, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 }  // namespace fgemm

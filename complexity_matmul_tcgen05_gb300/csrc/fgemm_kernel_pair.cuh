@@ -353,316 +353,6 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
   if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, PC::kTmemCols);
 }
 
-// ------------------------------------------------------------------------
-// One-level Strassen on CTA pairs (256 x BN tiles of the half-size block
-// space, tcgen05 cta_group::2).  Operand sums are formed on chip in two
-// steps: each CTA's producer loads a summed operand's first source tile by
-// TMA straight into the operand buffer and its second source tile into a
-// staging buffer of the same layout; the operand-sum warps then add the two
-// in place (fp32, one round-to-nearest-even), element by element at equal
-// byte offsets, since both tiles carry the same 128-byte swizzle.  The TMA
-// engine carries the load latency; the sum warps only touch shared memory.
-// A CTA holds 128 rows of each A operand and BN/2 columns of each B operand,
-// which halves its B-side sum work against a 128-row tile.
-template <int BN>
-struct PairStrassenCfg {
-  static constexpr int kABytes = kBM * kBK * 2;        // 16 KB
-  static constexpr int kBBytes = kBK * (BN / 2) * 2;   // this CTA's half of B
-  static constexpr int kStageBytes = 2 * (kABytes + kBBytes);  // operands + staging
-  static constexpr int kStages = BN == 256 ? 3 : 4;
-  static constexpr int kTmemCols = BN == 256 ? 512 : 256;
-  static constexpr int kBarBytes = 256;
-  static constexpr int kSlackBytes = kBBytes;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kSlackBytes;
-  static constexpr int kSumWarps = 10;  // warps 2, 3 and 8..15
-  static constexpr int kThreads = 512;
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static_assert((3 * kStages + 5) * 8 + 4 <= kBarBytes, "barrier area too small");
-};
-
-// dst = sg0 * dst + sg1 * src over `bytes` of 16-bit values (same layout).
-__device__ __forceinline__ void add_staged(uint8_t* dst, const uint8_t* src, int bytes, float sg0,
-                                           float sg1, int tid, int nthreads, int is_bf16) {
-#pragma unroll 4
-  for (int off = tid * 16; off < bytes; off += nthreads * 16) {
-    const uint4 a = *reinterpret_cast<const uint4*>(dst + off);
-    const uint4 b = *reinterpret_cast<const uint4*>(src + off);
-    float fa[8], fb[8];
-    unpack8(a, fa, is_bf16);
-    unpack8(b, fb, is_bf16);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) fa[i] = sg0 * fa[i] + sg1 * fb[i];
-    *reinterpret_cast<uint4*>(dst + off) =
-        make_uint4(pack2(fa[0], fa[1], is_bf16), pack2(fa[2], fa[3], is_bf16),
-                   pack2(fa[4], fa[5], is_bf16), pack2(fa[6], fa[7], is_bf16));
-  }
-}
-
-template <int BN>
-__global__ void __launch_bounds__(PairStrassenCfg<BN>::kThreads, 1)
-    fgemm_kernel_pair_strassen(const __grid_constant__ StrassenParams args) {
-  const KernelParams& p = args.k;
-  const StrassenTable& tab = args.tab;
-  using PC = PairStrassenCfg<BN>;
-  constexpr int S = PC::kStages;
-  constexpr int NSW = PC::kSumWarps;
-
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
-  const uint32_t base = (raw_addr + 1023u) & ~1023u;
-  uint8_t* base_ptr = smem_raw + (base - raw_addr);
-  // stage s: [A operand][B operand][A staging][B staging]
-  auto sA = [&](int s) { return base + s * PC::kStageBytes; };
-  auto sB = [&](int s) { return base + s * PC::kStageBytes + PC::kABytes; };
-  auto xA = [&](int s) { return base + s * PC::kStageBytes + PC::kABytes + PC::kBBytes; };
-  auto xB = [&](int s) { return base + s * PC::kStageBytes + 2 * PC::kABytes + PC::kBBytes; };
-  const uint32_t bar0 = base + S * PC::kStageBytes;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + S * PC::kStageBytes + 8 * (3 * S + 5));
-  auto loaded = [&](int s) { return bar0 + 8u * s; };        // TMA bytes of this CTA
-  auto full = [&](int s) { return bar0 + 8u * (S + s); };    // even CTA: sums of both CTAs done
-  auto empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
-  auto tfull = [&](uint32_t b) { return bar0 + 8u * (3 * S + b); };
-  auto tempty = [&](uint32_t b) { return bar0 + 8u * (3 * S + 2 + b); };
-  const uint32_t drain = bar0 + 8u * (3 * S + 4);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = ptx::cluster_ctarank();
-  const bool leader = rank == 0;
-  const int cluster = blockIdx.x >> 1;
-  const int nclusters = gridDim.x >> 1;
-  const int NP = p.num_products;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(loaded(s), 1);
-      ptx::mbar_init(full(s), 2 * NSW);
-      ptx::mbar_init(empty(s), 1);
-    }
-    for (uint32_t b = 0; b < 2; ++b) {
-      ptx::mbar_init(tfull(b), 1);
-      ptx::mbar_init(tempty(b), 8);
-    }
-    ptx::mbar_init(drain, 1);
-    ptx::fence_mbar_init();
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), PC::kTmemCols);
-    ptx::tmem_relinquish_pair();
-  }
-  ptx::tc_fence_before();
-  ptx::cluster_sync();
-  ptx::tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp == 0) {
-    // ----------------------------------- TMA producer: operands + staging
-    if (lane == 0) {
-      ptx::prefetch_tmap(&p.tmap_a);
-      ptx::prefetch_tmap(&p.tmap_b);
-      int s = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      for (int unit = cluster; ok && unit < p.num_units; unit += nclusters) {
-        int tm, tn;
-        unit_coords(p, unit, tm, tn);
-        const int row_in_block = tm * (2 * kBM) + static_cast<int>(rank) * kBM;
-        const int col_in_block = tn * BN + static_cast<int>(rank) * (BN / 2);
-        for (int pr = 0; ok && pr < NP; ++pr) {
-          const int na = tab.na[pr], nb = tab.nb[pr];
-          int ay[2], ax[2], by[2], bx[2];
-          for (int t = 0; t < 2; ++t) {
-            const int qa = tab.a[pr][t < na ? t : 0] & kTermIndexMask;
-            const int qb = tab.b[pr][t < nb ? t : 0] & kTermIndexMask;
-            ay[t] = (qa >> 1) * p.sub_m + row_in_block;
-            ax[t] = (qa & 1) * p.sub_k;
-            by[t] = (qb >> 1) * p.sub_k;
-            bx[t] = (qb & 1) * p.sub_n + col_in_block;
-          }
-          const uint32_t tx = static_cast<uint32_t>(na * PC::kABytes + nb * PC::kBBytes);
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!wait_one(empty(s), ph ^ 1u, p, 0)) {
-              ok = false;
-              break;
-            }
-            ptx::mbar_arrive_expect_tx(loaded(s), tx);
-            const int k0 = kb * kBK;
-            ptx::tma_load_2d(sA(s), &p.tmap_a, ax[0] + k0, ay[0], loaded(s));
-            if (na > 1) ptx::tma_load_2d(xA(s), &p.tmap_a, ax[1] + k0, ay[1], loaded(s));
-#pragma unroll
-            for (int q = 0; q < BN / 128; ++q) {
-              ptx::tma_load_2d(sB(s) + q * 8192, &p.tmap_b, bx[0] + q * 64, by[0] + k0, loaded(s));
-              if (nb > 1)
-                ptx::tma_load_2d(xB(s) + q * 8192, &p.tmap_b, bx[1] + q * 64, by[1] + k0, loaded(s));
-            }
-            if (++s == S) {
-              s = 0;
-              ph ^= 1u;
-            }
-          }
-        }
-      }
-      if (!ok) {
-        for (int i = 0; i < S; ++i) {
-          if (--s < 0) {
-            s = S - 1;
-            ph ^= 1u;
-          }
-          wait_bounded(loaded(s), ph, p, err_code(0), false);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ----------------------------------- MMA issuer (even CTA only)
-    if (lane == 0 && leader) {
-      int s = 0;
-      uint32_t ph = 0, acc_it = 0;
-      bool ok = true;
-      for (int unit = cluster; ok && unit < p.num_units; unit += nclusters) {
-        for (int pr = 0; ok && pr < NP; ++pr) {
-          const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
-          ++acc_it;
-          if (!wait_one(tempty(buf), aph ^ 1u, p, 1)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t dt = tmem_base + buf * BN;
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!wait_one(full(s), ph, p, 1)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint64_t ad = ptx::sdesc(sA(s), 16, 1024);
-            const uint64_t bd = ptx::sdesc(sB(s), 8192, 1024);
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              ptx::mma_f16_pair(dt, ad + static_cast<uint64_t>(k * 2),
-                                bd + static_cast<uint64_t>(k * 128), p.idesc,
-                                (kb | k) != 0 ? 1u : 0u);
-            ptx::mma_commit_pair(empty(s), 0x3);
-            if (++s == S) {
-              s = 0;
-              ph ^= 1u;
-            }
-          }
-          if (ok) ptx::mma_commit_pair(tfull(buf), 0x3);
-        }
-      }
-      ptx::mma_commit_pair(drain, 0x1);
-      wait_bounded(drain, 0, p, err_code(1), false);
-    }
-    __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
-    // ----------------------------------- epilogue (both CTAs)
-    const int ew = warp - 4;
-    const int r = ew * 32 + lane;
-    float* ws = p.workspace + static_cast<size_t>(blockIdx.x) * 4 * kBM * BN;
-    uint32_t acc_it = 0;
-    bool ok = true;
-    for (int unit = cluster; ok && unit < p.num_units; unit += nclusters) {
-      int tm, tn;
-      unit_coords(p, unit, tm, tn);
-      const int row0 = tm * (2 * kBM) + static_cast<int>(rank) * kBM;
-      for (int pr = 0; pr < NP; ++pr) {
-        const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
-        ++acc_it;
-        if (!wait_warp(tfull(buf), aph, p, 2)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * BN;
-        epilogue_strassen<BN, 1>(p, tab, tbase, row0, tn, pr, r, ws);
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty(buf), 0));
-      }
-    }
-  } else if (warp == 2 || warp == 3 || warp >= 8) {
-    // ----------------------------------- operand-sum warps (both CTAs)
-    const int sw = warp < 4 ? warp - 2 : warp - 6;
-    const int tid = sw * 32 + lane;
-    constexpr int NT = NSW * 32;
-    int s = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int unit = cluster; ok && unit < p.num_units; unit += nclusters) {
-      for (int pr = 0; ok && pr < NP; ++pr) {
-        const int na = tab.na[pr], nb = tab.nb[pr];
-        const float sa0 = (tab.a[pr][0] & kTermNeg) ? -1.0f : 1.0f;
-        const float sa1 = (tab.a[pr][1] & kTermNeg) ? -1.0f : 1.0f;
-        const float sb0 = (tab.b[pr][0] & kTermNeg) ? -1.0f : 1.0f;
-        const float sb1 = (tab.b[pr][1] & kTermNeg) ? -1.0f : 1.0f;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_warp(loaded(s), ph, p, 3)) {
-            ok = false;
-            break;
-          }
-          if (na > 1)
-            add_staged(base_ptr + (sA(s) - base), base_ptr + (xA(s) - base), PC::kABytes, sa0, sa1,
-                       tid, NT, p.is_bf16);
-          if (nb > 1)
-            add_staged(base_ptr + (sB(s) - base), base_ptr + (xB(s) - base), PC::kBBytes, sb0, sb1,
-                       tid, NT, p.is_bf16);
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(full(s), 0));
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-    }
-  }
-
-  ptx::tc_fence_before();
-  ptx::cluster_sync();
-  ptx::tc_fence_after();
-  if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, PC::kTmemCols);
-}
-
-template <int BN>
-cudaError_t launch_strassen_pair_t(const KernelParams& p, const StrassenTable& tab, int max_clusters,
-                                   cudaStream_t stream) {
-  auto kern = fgemm_kernel_pair_strassen<BN>;
-  constexpr int smem = PairStrassenCfg<BN>::kSmemBytes;
-  static unsigned long long configured = 0;
-  static int clusters_fit[64] = {0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(PairStrassenCfg<BN>::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (!(configured & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(2 * std::max(max_clusters, 1), 1, 1);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    clusters_fit[dev & 63] = n > 0 ? n : 1;
-    configured |= bit;
-  }
-  const int clusters = std::min(std::min(max_clusters, clusters_fit[dev & 63]), p.num_units);
-  cfg.gridDim = dim3(2 * std::max(clusters, 1), 1, 1);
-  const StrassenParams args{p, tab};
-  return cudaLaunchKernelEx(&cfg, kern, args);
-}
-
 // Launch configuration of the classical pair kernel; on first use per device
 // it also sets the shared-memory limit and records how many clusters fit.
 template <int BN>

@@ -14,9 +14,11 @@
 //   waves        = ceil(tiles / slots), slots = SMs (one tile per SM) or SM
 //                  pairs (256-row tiles); a partial last wave costs a full one
 //                  ("Page 48", wave quantization)
-//   t_tile       = products * (2 * tile_m * tile_n * K_sub / (slot peak * eff)
-//                  + fill), eff measured per form and tile
-//   t_compute    = waves * t_tile; for the classical CTA-pair kernel whose
+//   t_tile       = products * 2 * tile_m * tile_n * K_sub / (slot peak * eff),
+//                  eff measured per form and tile
+//   t_compute    = waves * t_tile + fill (the pipeline fill and the last
+//                  tile's epilogue, once per launch: every other epilogue
+//                  overlaps the next tile's MMAs); for the classical CTA-pair kernel whose
 //                  last wave holds R <= slots / 2 tiles, those tiles may run
 //                  as S = slots / R pieces of K each (S <= 4), and then
 //                  t_compute = (floor(tiles / slots) + 1/S) * t_tile
@@ -31,8 +33,14 @@
 //                  the roofline: time is the largest of compute and traffic)
 #include <algorithm>
 #include <numeric>
+#include <utility>
+#include <vector>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
 
 #include "../../include/fgemm.h"
 #include "fgemm_internal.h"
@@ -62,7 +70,7 @@ bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo
   if (tile_m != 128 && tile_m != 256) return false;
   if (epi_kind == FGEMM_EPI_SWIGLU && tile_n == 64) return false;
   const int d = depth_of(algo);
-  if (tile_m == 256 && (tile_n < 128 || d == 2 || algo == FGEMM_ALGO_WINOGRAD1)) return false;
+  if (tile_m == 256 && (tile_n < 128 || d == 2)) return false;
   if (d == 0) return true;
   if (tile_n == 64) return false;
   const int64_t g = int64_t{1} << d;
@@ -79,42 +87,57 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   if (!out) return;
   fgemm_device_model_t m{};
   m.num_sms = num_sms > 0 ? num_sms : 1;
-  m.peak_tflops = peak_tflops > 0 ? peak_tflops : 2250.0;
-  m.hbm_gbs = hbm_gbs > 0 ? hbm_gbs : 7900.0;
-  // Mainloop efficiencies and fixed costs measured on GB300 by fgemm_calibrate
-  // (8192^3 bf16, every form and tile), as fractions of the 2250 TFLOP/s
-  // nominal dense peak the model starts from; fgemm_calibrate re-measures them
-  // on the device at hand.
-  m.eff_classical[0] = 0.257;  // 128 x 64
-  m.eff_classical[1] = 0.501;  // 128 x 128
-  m.eff_classical[2] = 0.700;  // 128 x 256
-  m.eff_pair[0] = 0.499;       // 256 x 128
-  m.eff_pair[1] = 0.850;       // 256 x 256
-  m.eff_strassen[0][0] = 0.072;
-  m.eff_strassen[0][1] = 0.082;
-  m.eff_strassen[1][0] = 0.034;
-  m.eff_strassen[1][1] = 0.047;
-  m.eff_strassen_pair[0] = 0.097;  // 256 x 128 (8192^3: 250 TFLOP/s effective)
-  m.eff_strassen_pair[1] = 0.146;  // 256 x 256 (8192^3: 376 TFLOP/s effective)
-  m.launch_us = 9.1;
-  m.tile_fill_us = 2.3;
+  // The denominators: a GB300's measured dense bf16 GEMM rate (cuBLAS,
+  // 8192^3, burst) and its measured streaming copy bandwidth, unless the
+  // caller gives others.
+  m.peak_tflops = peak_tflops > 0 ? peak_tflops : 1891.3 * m.num_sms / 152.0;
+  m.hbm_gbs = hbm_gbs > 0 ? hbm_gbs : 6789.0;
+  // Mainloop rates measured on GB300 by fgemm_calibrate (8192^3 bf16, every
+  // form and tile), in TFLOP/s for 152 SMs; each efficiency is that rate as a
+  // fraction of the peak above, so the model predicts the measured rates
+  // whatever denominator it is given.  fgemm_calibrate re-measures them on
+  // the device at hand.
+  const double sm_scale = m.num_sms / 152.0;
+  auto rate = [&](double tflops_152) { return tflops_152 * sm_scale / m.peak_tflops; };
+  m.eff_classical[0] = rate(578.3);   // 128 x 64
+  m.eff_classical[1] = rate(1127.3);  // 128 x 128
+  m.eff_classical[2] = rate(1575.0);  // 128 x 256
+  m.eff_pair[0] = rate(1122.8);       // 256 x 128
+  m.eff_pair[1] = rate(1912.5);       // 256 x 256
+  // Strassen on one-CTA tiles (operand sums formed on chip from registers):
+  // executed-MAC rates
+  m.eff_strassen[0][0] = rate(162.0);
+  m.eff_strassen[0][1] = rate(184.5);
+  m.eff_strassen[1][0] = rate(76.5);
+  m.eff_strassen[1][1] = rate(105.8);
+  // one level on CTA pairs, summed operands streamed through HBM: the rate
+  // of its product kernel (executed MACs)
+  m.eff_strassen_pair[0] = rate(675.0);   // 256 x 128
+  m.eff_strassen_pair[1] = rate(675.0);   // 256 x 256
+  // launch: back-to-back calls of a one-kernel product; fill: the first
+  // MMA about 1.5 us after the start, the last 256 x 256 tile's epilogue
+  // about 5 us after the last MMA (timestamps of an instrumented build)
+  m.launch_us = 4.0;
+  m.tile_fill_us = 6.5;
   m.l2_bytes = 126.0 * 1024 * 1024;
   m.l2_gbs = 40000.0;
   m.split_fix_us = 4.0;
-  m.eff_winograd[0] = 0.065;  // 128 x 128 (below Strassen's: 14 + 14 source terms, not 12 + 12)
-  m.eff_winograd[1] = 0.074;  // 128 x 256
+  m.eff_winograd[0] = rate(146.3);  // 128 x 128 (below Strassen's: 14 + 14 source terms, not 12 + 12)
+  m.eff_winograd[1] = rate(166.5);  // 128 x 256
   // small-M tiles: an N = tile_m MMA runs at most tile_m / 256 of the full
   // rate.  These are lower bounds from streams that stayed memory-bound:
   // 16 x 16384^2 at 6.4 TB/s, and tile_m 64 only 5 % slower than tile_m 16
-  m.eff_small_m[0] = 0.07;    // tile_m 16
-  m.eff_small_m[1] = 0.14;    // tile_m 32
-  m.eff_small_m[2] = 0.27;    // tile_m 64
-  m.hbm_stream_eff = 0.9;
-  m.small_m_stream_eff = 0.75;  // 16 x 16384^2: 537 MB in ~101-106 us inside the kernel
+  m.eff_small_m[0] = rate(157.5);   // tile_m 16
+  m.eff_small_m[1] = rate(315.0);   // tile_m 32
+  m.eff_small_m[2] = rate(607.5);   // tile_m 64
+  // streaming rates, as fractions of the copy bandwidth above (fitted as
+  // 7110, 5925 and 7663 GB/s)
+  m.hbm_stream_eff = 7110.0 / m.hbm_gbs;
+  m.small_m_stream_eff = 5925.0 / m.hbm_gbs;  // 16 x 16384^2: 537 MB in ~101-106 us inside the kernel
   m.small_m_fix_us = 4.0;
   // 16 x 16384^2 on 128 CTAs of one whole tile each: 537 MB in 83.7 us, and
   // 16 x 8192^2 on 128 CTAs of half a tile: 32.7 us (CUDA events)
-  m.small_m_aligned_eff = 0.97;
+  m.small_m_aligned_eff = 7663.0 / m.hbm_gbs;
   *out = m;
 }
 
@@ -249,7 +272,8 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     const double eff = std::max(dev->eff_small_m[tile_m == 16 ? 0 : (tile_m == 32 ? 1 : 2)], 1e-3);
     const double sm_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms;
     const double t_kb = 2.0 * 128.0 * tile_m * fgemm::kBK / (sm_flop_per_us * eff);
-    const double t_compute = static_cast<double>(ceil_div(iters, ctas)) * t_kb + dev->tile_fill_us;
+    // (its pipeline fill and last sum are in small_m_fix_us)
+    const double t_compute = static_cast<double>(ceil_div(iters, ctas)) * t_kb;
     const double bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
                                 static_cast<double>(M) * N);
     // CTAs reading B in step stream at the full rate from 3/4 of the SMs on;
@@ -265,6 +289,32 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
   const int d = depth_of(algo);
   const bool swiglu = epi_kind == FGEMM_EPI_SWIGLU;
   const bool pair = tile_m == 256;
+  if (pair && d == 1) {
+    // One level on CTA pairs with the summed operands streamed through HBM:
+    // a pre-pass reads A and B once and writes each summed operand once
+    // (Strassen: 5 + 5 of the 4 + 4 blocks, Winograd: 4 + 4), then the seven
+    // block products run on the classical pair mainloop, their (position,
+    // product) units shared out evenly over the pairs.
+    const bool wino = algo == FGEMM_ALGO_WINOGRAD1;
+    const int64_t sub_m = M / 2, sub_n = N / 2, sub_k = K / 2;
+    const double temps = wino ? 4.0 : 5.0;
+    const double pre_bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
+                                    temps * (static_cast<double>(sub_m) * sub_k +
+                                             static_cast<double>(sub_k) * sub_n));
+    const double t_pre = pre_bytes / (dev->hbm_gbs * 1e3 * std::max(dev->hbm_stream_eff, 1e-3)) +
+                         dev->launch_us;
+    const int64_t positions = fgemm_model_tiles(sub_m, sub_n, 256, tile_n);
+    const int32_t pairs = std::max(1, dev->num_sms / 2);
+    const int64_t units = positions * 7;
+    const double eff = std::max(dev->eff_strassen_pair[tile_n == 128 ? 0 : 1], 1e-3);
+    const double pair_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms * 2.0;
+    const double k_pad = static_cast<double>(ceil_div(sub_k, fgemm::kBK) * fgemm::kBK);
+    const double t_unit = 2.0 * 256.0 * tile_n * k_pad / (pair_flop_per_us * eff);
+    const double t_compute = static_cast<double>(ceil_div(units, std::min<int64_t>(pairs, units))) * t_unit +
+                             dev->tile_fill_us;
+    if (predicted_us) *predicted_us = t_pre + t_compute + dev->launch_us;
+    return FGEMM_OK;
+  }
   const int64_t n_out = swiglu ? N / 2 : N;
   const int64_t sub_m = M >> d, sub_n = N >> d, sub_k = K >> d;
   const int64_t products = d == 0 ? 1 : (d == 1 ? 7 : 49);
@@ -290,9 +340,11 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     eff = dev->eff_classical[tile_index(tile_n)];
   const double slot_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms * (pair ? 2.0 : 1.0);
   const double k_pad = static_cast<double>(ceil_div(sub_k, fgemm::kBK) * fgemm::kBK);
+  // a tile's (or a Strassen position's) MMA time; the epilogue of one tile
+  // overlaps the next tile's MMAs, so the pipeline fill and the last
+  // epilogue are paid once per launch
   const double t_tile =
-      products * (2.0 * tile_m * tile_n * k_pad / (slot_flop_per_us * std::max(eff, 1e-3)) +
-                  dev->tile_fill_us);
+      products * (2.0 * tile_m * tile_n * k_pad / (slot_flop_per_us * std::max(eff, 1e-3)));
   double t_compute = static_cast<double>(waves) * t_tile;
   if (pair && d == 0) {
     // the tiles of the last partial wave may be split along K into S pieces
@@ -301,6 +353,7 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     if (fgemm_model_split_tail(dev, tiles, slots, kb, tile_n, 1, &s) > 0)
       t_compute = (static_cast<double>(tiles / slots) + 1.0 / s) * t_tile + dev->split_fix_us * (s - 1);
   }
+  t_compute += dev->tile_fill_us;
   double bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
                         static_cast<double>(M) * n_out);
   if (d > 0) {
@@ -365,3 +418,114 @@ fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M, int6
 }
 
 }  // extern "C"
+
+// ------------------------------------------------ device model as JSON
+
+namespace {
+
+// Every field of the model that a calibration file carries (key, member).
+std::vector<std::pair<const char*, double*>> model_fields(fgemm_device_model_t& m) {
+  return {
+      {"peak_tflops", &m.peak_tflops},
+      {"hbm_gbs", &m.hbm_gbs},
+      {"eff_classical_64", &m.eff_classical[0]},
+      {"eff_classical_128", &m.eff_classical[1]},
+      {"eff_classical_256", &m.eff_classical[2]},
+      {"eff_pair_128", &m.eff_pair[0]},
+      {"eff_pair_256", &m.eff_pair[1]},
+      {"eff_strassen1_128", &m.eff_strassen[0][0]},
+      {"eff_strassen1_256", &m.eff_strassen[0][1]},
+      {"eff_strassen2_128", &m.eff_strassen[1][0]},
+      {"eff_strassen2_256", &m.eff_strassen[1][1]},
+      {"eff_strassen1_pair_128", &m.eff_strassen_pair[0]},
+      {"eff_strassen1_pair_256", &m.eff_strassen_pair[1]},
+      {"launch_us", &m.launch_us},
+      {"tile_fill_us", &m.tile_fill_us},
+      {"l2_bytes", &m.l2_bytes},
+      {"l2_gbs", &m.l2_gbs},
+      {"split_fix_us", &m.split_fix_us},
+      {"eff_winograd1_128", &m.eff_winograd[0]},
+      {"eff_winograd1_256", &m.eff_winograd[1]},
+      {"eff_small_m_16", &m.eff_small_m[0]},
+      {"eff_small_m_32", &m.eff_small_m[1]},
+      {"eff_small_m_64", &m.eff_small_m[2]},
+      {"hbm_stream_eff", &m.hbm_stream_eff},
+      {"small_m_stream_eff", &m.small_m_stream_eff},
+      {"small_m_fix_us", &m.small_m_fix_us},
+      {"small_m_aligned_eff", &m.small_m_aligned_eff},
+  };
+}
+
+// The number after "key": in a flat JSON object (false if absent or not a
+// number).
+bool json_number(const std::string& text, const char* key, double* out) {
+  const std::string pat = std::string("\"") + key + "\"";
+  size_t p = text.find(pat);
+  if (p == std::string::npos) return false;
+  p = text.find_first_not_of(" \t\r\n", p + pat.size());
+  if (p == std::string::npos || text[p] != ':') return false;
+  const char* s = text.c_str() + p + 1;
+  char* end = nullptr;
+  const double d = std::strtod(s, &end);
+  if (end == s || !std::isfinite(d)) return false;
+  *out = d;
+  return true;
+}
+
+}  // namespace
+
+extern "C" fgemm_status_t fgemm_model_load_json(const char* path, fgemm_device_model_t* model) {
+  if (!path || !model) return FGEMM_ERR_INVALID_ARG;
+  FILE* f = std::fopen(path, "rb");
+  if (!f) return FGEMM_ERR_CALIBRATION;
+  std::string text;
+  char buf[4096];
+  size_t n;
+  while ((n = std::fread(buf, 1, sizeof(buf), f)) > 0 && text.size() < (1u << 20)) text.append(buf, n);
+  std::fclose(f);
+  fgemm_device_model_t m = *model;
+  const double old_peak = m.peak_tflops, old_bw = m.hbm_gbs;
+  double v = 0, tf = 0;
+  // A file of measured peaks (a dense bf16 GEMM rate "bf16_tflops" and a
+  // copy bandwidth "hbm_gbs", without the model's own "peak_tflops"): the
+  // denominators change and every efficiency is rescaled, so that the rates
+  // the model predicts stay the ones it was fitted to.
+  const bool peaks_file = !json_number(text, "peak_tflops", &v) && json_number(text, "bf16_tflops", &tf);
+  int found = 0;
+  for (auto& fd : model_fields(m)) found += json_number(text, fd.first, fd.second) ? 1 : 0;
+  if (json_number(text, "num_sms", &v) && v >= 1 && v <= 4096) {
+    m.num_sms = static_cast<int32_t>(v);
+    ++found;
+  }
+  if (peaks_file) {
+    if (!(tf > 0) || !(m.hbm_gbs > 0)) return FGEMM_ERR_CALIBRATION;
+    const double r = old_peak / tf;
+    for (double* e : {&m.eff_classical[0], &m.eff_classical[1], &m.eff_classical[2], &m.eff_pair[0],
+                      &m.eff_pair[1], &m.eff_strassen[0][0], &m.eff_strassen[0][1],
+                      &m.eff_strassen[1][0], &m.eff_strassen[1][1], &m.eff_strassen_pair[0],
+                      &m.eff_strassen_pair[1], &m.eff_winograd[0], &m.eff_winograd[1],
+                      &m.eff_small_m[0], &m.eff_small_m[1], &m.eff_small_m[2]})
+      *e *= r;
+    const double rb = old_bw / m.hbm_gbs;
+    for (double* e : {&m.hbm_stream_eff, &m.small_m_stream_eff, &m.small_m_aligned_eff}) *e *= rb;
+    m.peak_tflops = tf;
+    ++found;
+  }
+  if (!found) return FGEMM_ERR_CALIBRATION;
+  if (!(m.peak_tflops > 0) || !(m.hbm_gbs > 0) || !(m.launch_us >= 0) || !(m.tile_fill_us >= 0))
+    return FGEMM_ERR_CALIBRATION;
+  *model = m;
+  return FGEMM_OK;
+}
+
+extern "C" fgemm_status_t fgemm_model_save_json(const fgemm_device_model_t* model, const char* path) {
+  if (!path || !model) return FGEMM_ERR_INVALID_ARG;
+  FILE* f = std::fopen(path, "w");
+  if (!f) return FGEMM_ERR_CALIBRATION;
+  fgemm_device_model_t m = *model;
+  std::fprintf(f, "{\n  \"num_sms\": %d", m.num_sms);
+  for (auto& fd : model_fields(m)) std::fprintf(f, ",\n  \"%s\": %.9g", fd.first, *fd.second);
+  std::fprintf(f, "\n}\n");
+  const bool ok = std::fclose(f) == 0;
+  return ok ? FGEMM_OK : FGEMM_ERR_CALIBRATION;
+}

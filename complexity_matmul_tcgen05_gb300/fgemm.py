@@ -96,6 +96,9 @@ def lib() -> ctypes.CDLL:
         L.fgemm_get_error.argtypes = [vp]
         L.fgemm_selftest_wait_timeout.argtypes = [vp, i32]
         L.fgemm_calibrate.argtypes = [vp, ctypes.c_char_p]
+        L.fgemm_calibrate_ex.argtypes = [vp, i64, ctypes.c_char_p]
+        L.fgemm_model_load_json.argtypes = [ctypes.c_char_p, model_p]
+        L.fgemm_model_save_json.argtypes = [model_p, ctypes.c_char_p]
         L.fgemm_status_string.argtypes = [st]
         L.fgemm_status_string.restype = ctypes.c_char_p
         L.fgemm_last_message.argtypes = [vp]
@@ -134,6 +137,7 @@ def lib() -> ctypes.CDLL:
         L.fgemm_set_device_model.argtypes = [vp, model_p]
         for name in ("fgemm_create", "fgemm_destroy", "fgemm_set_stream", "fgemm_matmul",
                      "fgemm_matmul_ex", "fgemm_plan", "fgemm_plan_ex", "fgemm_get_error", "fgemm_calibrate",
+                     "fgemm_calibrate_ex", "fgemm_model_load_json", "fgemm_model_save_json",
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
                      "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout",
@@ -279,8 +283,9 @@ class Handle:
     def last_message(self) -> str:
         return lib().fgemm_last_message(self._h).decode()
 
-    def calibrate(self, json_path: str | None = None):
-        _check(lib().fgemm_calibrate(self._h, json_path.encode() if json_path else None), self._h)
+    def calibrate(self, json_path: str | None = None, n: int = 8192):
+        _check(lib().fgemm_calibrate_ex(self._h, n, json_path.encode() if json_path else None),
+               self._h)
 
     def device_model(self) -> DeviceModel:
         m = DeviceModel()

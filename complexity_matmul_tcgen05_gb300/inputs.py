@@ -36,7 +36,7 @@ WORKLOADS = {
                                algos=("classical", "strassen1", "auto")),
     "square_16384_bf16": dict(M=16384, N=16384, K=16384, dtype="bf16", a="uniform",
                               b="uniform", epi="none", bias=None,
-                              algos=("classical", "strassen1", "strassen2", "auto")),
+                              algos=("classical", "strassen1", "strassen2", "winograd1", "auto")),
 }
 
 SWEEP_SHAPES = [(m, nk, nk) for m in (16, 128, 1024, 8192)

@@ -98,9 +98,11 @@ typedef enum {
 /*
  * Creates a handle on the CURRENT CUDA device. The handle owns: a device
  * error word, a plan cache, a tensor-descriptor cache, the partial-tile
- * workspace (grown on demand), the split-piece counters and the device model. The device model starts
- * from the device's SM count and, if the environment variable FGEMM_CALIB
- * names a calibration JSON written by fgemm_calibrate, from that file.
+ * workspace (grown on demand), the split-piece counters and the device model.
+ * The device model starts from the device's SM count and the rates measured
+ * on a GB300 (fgemm_model_default) and, if the environment variable
+ * FGEMM_CALIB names a JSON file, from that file (fgemm_model_load_json: a
+ * calibration written by fgemm_calibrate, or measured peaks).
  * Returns FGEMM_ERR_NO_DEVICE if no device is present or it is not sm_103,
  * FGEMM_ERR_CALIBRATION if FGEMM_CALIB names a bad file.
  */
@@ -283,6 +285,15 @@ fgemm_status_t fgemm_get_error(fgemm_handle_t h);
 fgemm_status_t fgemm_calibrate(fgemm_handle_t h, const char* json_out_path);
 
 /*
+ * fgemm_calibrate on n x n x n products (n a multiple of 1024 in [1024,
+ * 16384]; fgemm_calibrate uses 8192). Besides the mainloop rates it
+ * measures the launch cost (back-to-back K = 0 calls) and the pipeline fill
+ * and drain (the intercept in K of a one-tile product's time, less the
+ * launch). FGEMM_ERR_INVALID_ARG for another n.
+ */
+fgemm_status_t fgemm_calibrate_ex(fgemm_handle_t h, int64_t n, const char* json_out_path);
+
+/*
  * Failure-detection self-test. Launches a one-block kernel that waits on an
  * mbarrier nothing will ever complete, through the same bounded wait every
  * GEMM kernel uses, with the limit set to limit_ms (1..10000) for this
@@ -419,9 +430,34 @@ typedef struct {
  */
 int32_t fgemm_small_m_grid(int64_t tiles, int32_t k_blocks, int32_t num_sms, int32_t* phases_out);
 
-/* Default model for a device with the given SM count, peak and bandwidth. */
+/*
+ * Default model for a device with the given SM count: the mainloop, launch
+ * and streaming rates fgemm_calibrate measured on a GB300 (for 152 SMs,
+ * scaled by the SM count), expressed as efficiencies against peak_tflops
+ * (<= 0: 1891.3 TFLOP/s, the dense bf16 rate a GB300 measured, scaled by the
+ * SM count) and hbm_gbs (<= 0: 6789 GB/s, its measured copy bandwidth). The
+ * predicted times do not depend on the two denominators.
+ */
 void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms,
                          double peak_tflops, double hbm_gbs);
+
+/*
+ * Reads a flat JSON object into *model (host only), starting from its
+ * current contents. Either a calibration as fgemm_model_save_json writes it
+ * (keys named after the fields, e.g. "peak_tflops", "eff_pair_256",
+ * "launch_us"; absent keys keep their values), or measured peaks: a dense
+ * bf16 GEMM rate "bf16_tflops" and a copy bandwidth "hbm_gbs" with no
+ * "peak_tflops", which become the model's denominators with every
+ * efficiency rescaled so that the predicted rates do not change.
+ * FGEMM_ERR_CALIBRATION if the file cannot be read, holds no known key, or
+ * gives a non-positive peak or bandwidth or a negative fixed cost (then
+ * *model is unchanged); FGEMM_ERR_INVALID_ARG for NULL arguments.
+ */
+fgemm_status_t fgemm_model_load_json(const char* path, fgemm_device_model_t* model);
+
+/* Writes *model as the flat JSON object fgemm_model_load_json reads (host
+ * only). FGEMM_ERR_CALIBRATION if the file cannot be written. */
+fgemm_status_t fgemm_model_save_json(const fgemm_device_model_t* model, const char* path);
 
 /* Tile quantization: ceil(M / tile_m) * ceil(N / tile_n). */
 int64_t fgemm_model_tiles(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n);

@@ -319,28 +319,33 @@ def test_model_split_removes_the_pair_sawtooth(L):
     m.hbm_gbs = 1e9  # compute-bound: the sawtooth is in the compute term
     _, t76 = _predict(L, m, 256 * 76, 256, 8192, "classical", 256, tile_m=256)
     _, t77 = _predict(L, m, 256 * 77, 256, 8192, "classical", 256, tile_m=256)
-    t_tile = t76 - m.launch_us
-    assert abs(t77 - (m.launch_us + 1.25 * t_tile + 3 * m.split_fix_us)) < 1e-6 * t77
+    fixed = m.launch_us + m.tile_fill_us   # once per launch
+    t_tile = t76 - fixed
+    assert abs(t77 - (fixed + 1.25 * t_tile + 3 * m.split_fix_us)) < 1e-6 * t77
     m.split_fix_us = 1e9  # split never pays: back to the whole-wave sawtooth
     _, t77w = _predict(L, m, 256 * 77, 256, 8192, "classical", 256, tile_m=256)
-    assert abs(t77w - (m.launch_us + 2 * t_tile)) < 1e-6 * t77w
+    assert abs(t77w - (fixed + 2 * t_tile)) < 1e-6 * t77w
     assert t77 < 0.8 * t77w
 
 
 def test_winograd_legality_and_model(L):
-    # one level on single-CTA tiles of 128 x {128, 256}; never on CTA pairs
+    # one level on single-CTA tiles of 128 x {128, 256} and on CTA pairs of
+    # 256 x {128, 256} (whole tiles in every block), never 64 wide
     ep = fgemm.make_epilogue("none")
     ok = lambda M, N, K, tm, tn: fgemm.validate(M, N, K, 16, K, 16, N, 16, N, fgemm.BF16, ep,
                                                 "winograd1", tn, tm)
     assert ok(512, 512, 256, 128, 128) == fgemm.OK
     assert ok(512, 1024, 256, 128, 256) == fgemm.OK
-    assert ok(512, 512, 256, 256, 256) == fgemm.ERR_UNSUPPORTED
+    assert ok(512, 512, 256, 256, 256) == fgemm.OK                 # one pair tile per block
+    assert ok(512, 768, 256, 256, 256) == fgemm.ERR_UNSUPPORTED    # 384-column blocks
+    assert ok(768, 512, 256, 256, 128) == fgemm.ERR_UNSUPPORTED    # 384-row blocks
     assert ok(512, 512, 256, 128, 64) == fgemm.ERR_UNSUPPORTED
     assert ok(384, 512, 256, 128, 128) == fgemm.ERR_UNSUPPORTED   # 192-row blocks
     m = _model(L)
     s, tw = _predict(L, m, 16384, 16384, 16384, "winograd1", 256)
     assert s == fgemm.OK and tw > 0
-    assert _predict(L, m, 16384, 16384, 16384, "winograd1", 256, tile_m=256)[0] == fgemm.ERR_UNSUPPORTED
+    s, twp = _predict(L, m, 16384, 16384, 16384, "winograd1", 256, tile_m=256)
+    assert s == fgemm.OK and twp > 0
     # with the Strassen mainloop rate, the extra source terms (14 + 14 vs
     # 12 + 12) make it predict no faster than Strassen-1
     m.eff_winograd[1] = m.eff_strassen[0][1]
@@ -478,3 +483,74 @@ def test_small_m_grid_invariants():
         else:
             assert ctas == most and phases == most
     assert fgemm.small_m_grid(0, 4, 152) == (0, 0)
+
+
+# ------------------------------------------------- calibration files (host)
+
+def _flat(m):
+    """Every number of a device model, by field name."""
+    out = {}
+    for name, ct in fgemm.DeviceModel._fields_:
+        v = getattr(m, name)
+        if hasattr(v, "__len__"):
+            flat = np.array([list(x) if hasattr(x, "__len__") else x for x in v], dtype=float).ravel()
+            for i, x in enumerate(flat):
+                out[f"{name}[{i}]"] = float(x)
+        else:
+            out[name] = float(v)
+    return out
+
+
+def test_model_json_round_trip(L, tmp_path):
+    m = _model(L)
+    m.eff_pair[1] = 0.777
+    m.launch_us = 3.25
+    m.small_m_fix_us = 5.5
+    m.eff_strassen[1][0] = 0.0123
+    path = str(tmp_path / "calib.json").encode()
+    assert L.fgemm_model_save_json(ctypes.byref(m), path) == fgemm.OK
+    d = json.load(open(path))                     # valid JSON, one key per field
+    assert d["eff_pair_256"] == 0.777 and d["launch_us"] == 3.25 and d["num_sms"] == 152
+    assert d["eff_strassen2_128"] == 0.0123 and d["small_m_fix_us"] == 5.5
+    m2 = _model(L, sms=100, peak=1.0, bw=1.0)     # everything different before the load
+    assert L.fgemm_model_load_json(path, ctypes.byref(m2)) == fgemm.OK
+    a, b = _flat(m), _flat(m2)
+    for k in a:
+        if k != "reserved":
+            assert abs(a[k] - b[k]) <= 1e-8 * max(1.0, abs(a[k])), k
+
+
+def test_model_json_measured_peaks_change_only_the_denominators(L, tmp_path):
+    # a file of measured peaks (the format the driver's peak measurement
+    # writes): the peak and bandwidth become the denominators, the efficiencies
+    # are rescaled, and every predicted time stays the same
+    m = _model(L)
+    shapes = [(16384, 16384, 16384, "classical", 256, 256), (4096, 4096, 4096, "classical", 128, 128),
+              (16, 16384, 16384, "classical", 16, 128), (8192, 8192, 8192, "strassen1", 256, 256),
+              (8192, 8192, 8192, "strassen2", 128, 256)]
+    before = [_predict(L, m, M, N, K, a, tn, tile_m=tm)[1] for (M, N, K, a, tm, tn) in shapes]
+    path = tmp_path / "peaks.json"
+    path.write_text(json.dumps({"hbm_gbs": 6000.0, "bf16_tflops": 1700.0,
+                                "bf16_tflops_sustained": 1600.0, "gpu_name": "NVIDIA GB300"}))
+    assert L.fgemm_model_load_json(str(path).encode(), ctypes.byref(m)) == fgemm.OK
+    assert m.peak_tflops == 1700.0 and m.hbm_gbs == 6000.0
+    after = [_predict(L, m, M, N, K, a, tn, tile_m=tm)[1] for (M, N, K, a, tm, tn) in shapes]
+    for b, a in zip(before, after):
+        assert abs(a - b) <= 1e-9 * b
+
+
+def test_model_json_rejects_bad_files_and_keeps_the_model(L, tmp_path):
+    m = _model(L)
+    ref = _flat(m)
+    cases = {"garbage.json": "this is not a calibration", "negative.json": '{"peak_tflops": -5}',
+             "zero_bw.json": '{"hbm_gbs": 0}', "neg_launch.json": '{"launch_us": -1.0}',
+             "empty.json": "{}"}
+    for name, text in cases.items():
+        p = tmp_path / name
+        p.write_text(text)
+        assert L.fgemm_model_load_json(str(p).encode(), ctypes.byref(m)) == fgemm.ERR_CALIBRATION, name
+        assert _flat(m) == ref, name
+    assert L.fgemm_model_load_json(str(tmp_path / "missing.json").encode(), ctypes.byref(m)) == \
+        fgemm.ERR_CALIBRATION
+    assert L.fgemm_model_load_json(None, ctypes.byref(m)) == fgemm.ERR_INVALID_ARG
+    assert _flat(m) == ref

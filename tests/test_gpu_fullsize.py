@@ -100,16 +100,19 @@ def test_proj_4096_bias(algo):
     _sampled_check("proj_4096", A, B, bias, algo, "scale_bias", "bf16")
 
 
-@pytest.mark.parametrize("algo", ["classical", "strassen1", "winograd1", "auto"])
-def test_ffn_up_swiglu(algo):
+@pytest.mark.parametrize("algo,tile_m", [("classical", 0), ("strassen1", 256), ("strassen1", 128),
+                                         ("winograd1", 256), ("auto", 0)])
+def test_ffn_up_swiglu(algo, tile_m):
     A, B, _ = inputs.workload_inputs("ffn_up_swiglu_bf16", DEV)
-    _sampled_check("ffn_up", A, B, None, algo, "swiglu", "bf16")
+    _sampled_check("ffn_up", A, B, None, algo, "swiglu", "bf16", tile_m=tile_m)
 
 
-@pytest.mark.parametrize("algo", ["classical", "strassen1", "strassen2", "winograd1", "auto"])
-def test_square_16384(algo):
+@pytest.mark.parametrize("algo,tile_m", [("classical", 0), ("strassen1", 256), ("strassen1", 128),
+                                         ("strassen2", 128), ("winograd1", 256), ("winograd1", 128),
+                                         ("auto", 0)])
+def test_square_16384(algo, tile_m):
     A, B, _ = inputs.workload_inputs("square_16384_bf16", DEV)
-    _sampled_check("square_16384", A, B, None, algo, "none", "bf16")
+    _sampled_check("square_16384", A, B, None, algo, "none", "bf16", tile_m=tile_m)
 
 
 @pytest.mark.parametrize("shape", inputs.SWEEP_SHAPES, ids=lambda s: "x".join(map(str, s)))

@@ -71,14 +71,50 @@ def test_exact_ternary(algo, M, N, K, tile, dtype):
     assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
 
 
+# One level on CTA pairs (summed operands streamed through HBM by a pre-pass,
+# products on the pair mainloop).  Each shape's (position, product) units are
+# shared out over the pairs: 512 x 512 x 128 has 1 position (7 units, one per
+# pair, so all 7 pairs finish it together); 512 x 1024 has 2 (14 units);
+# 2048^2 at 256 has 16 (112 units over 76 pairs); 4096 x 4096 x 512 has 64
+# (448 units: about 6 per pair, positions shared at every range boundary).
+LCMA_PAIR_CASES = [(512, 512, 128, 128), (512, 1024, 256, 256), (1024, 2048, 640, 256),
+                   (1536, 768, 384, 128), (2048, 2048, 256, 256), (4096, 4096, 512, 256)]
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-@pytest.mark.parametrize("M,N,K,tile", [(512, 512, 128, 128), (512, 1024, 256, 256),
-                                        (1024, 2048, 640, 256), (1536, 768, 384, 128)])
-def test_exact_ternary_strassen_cta_pair(M, N, K, tile, dtype):
-    """One-level Strassen on CTA pairs (TMA-staged operand sums): bit-exact."""
+@pytest.mark.parametrize("algo", ["strassen1", "winograd1"])
+@pytest.mark.parametrize("M,N,K,tile", LCMA_PAIR_CASES)
+def test_exact_ternary_lcma_cta_pair(M, N, K, tile, algo, dtype):
+    """One Strassen / Winograd level on CTA pairs: RNE(exact C) bit for bit."""
     A, B, bias = _ternary(M, N, K, dtype)
-    C = run(A, B, algo="strassen1", epilogue="scale_bias", bias=bias, tile_n=tile, tile_m=256)
+    C = run(A, B, algo=algo, epilogue="scale_bias", bias=bias, tile_n=tile, tile_m=256)
     assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
+
+
+@pytest.mark.parametrize("algo", ["strassen1", "winograd1"])
+def test_lcma_cta_pair_deterministic_and_graph_replay(algo):
+    """Positions shared by two pairs are summed in pair order: two launches
+    give the same bits; a captured graph replays the launch (its arrival
+    counters count from zero each time) with the same result."""
+    M, N, K = 4096, 2048, 1024
+    A = inputs.matrix(M, K, "uniform", "bf16", 70, DEV)
+    B = inputs.matrix(K, N, "uniform", "bf16", 71, DEV)
+    kw = dict(algo=algo, tile_n=256, tile_m=256)
+    C1 = run(A, B, **kw)
+    C2 = run(A, B, **kw)
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+    C = torch.empty_like(C1)
+    fgemm.matmul(A, B, out=C, **kw)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fgemm.matmul(A, B, out=C, **kw)
+    for _ in range(3):
+        C.view(torch.int16).fill_(0x7F7B)
+        g.replay()
+        torch.cuda.synchronize()
+        assert fgemm.default_handle().get_error() == fgemm.OK
+        assert torch.equal(C.view(torch.int16), C1.view(torch.int16))
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
@@ -231,7 +267,8 @@ def test_classical_epilogues_every_entry(epilogue, alpha, tile_m, tile):
 @pytest.mark.parametrize("algo,tile_m,tile,depth", [
     ("classical", 128, 128, 0), ("classical", 128, 256, 0), ("classical", 256, 128, 0),
     ("classical", 256, 256, 0), ("strassen1", 128, 128, 1), ("strassen1", 128, 256, 1),
-    ("strassen1", 256, 256, 1), ("strassen2", 128, 128, 2), ("winograd1", 128, 256, 1)])
+    ("strassen1", 256, 256, 1), ("strassen1", 256, 128, 1), ("strassen2", 128, 128, 2),
+    ("winograd1", 128, 256, 1), ("winograd1", 256, 256, 1)])
 def test_swiglu_every_entry(algo, tile_m, tile, depth):
     M, N, K = 512, 2048, 512
     A = inputs.matrix(M, K, "normal", "bf16", 0, DEV)
@@ -243,7 +280,8 @@ def test_swiglu_every_entry(algo, tile_m, tile, depth):
 @pytest.mark.parametrize("algo,tile_m,tile,depth", [
     ("strassen1", 128, 128, 1), ("strassen1", 128, 256, 1), ("strassen1", 256, 128, 1),
     ("strassen1", 256, 256, 1), ("strassen2", 128, 128, 2), ("strassen2", 128, 256, 2),
-    ("winograd1", 128, 128, 1), ("winograd1", 128, 256, 1)])
+    ("winograd1", 128, 128, 1), ("winograd1", 128, 256, 1), ("winograd1", 256, 128, 1),
+    ("winograd1", 256, 256, 1)])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_strassen_every_entry_and_emulation(algo, tile_m, tile, depth, dtype):
     """Normwise bound and the tighter pin: GPU Strassen vs the emulated
@@ -696,3 +734,45 @@ def test_mx_exact_ternary():
     ref = oracle.encode(oracle.gemm(oracle.fp8_decode(_np(A), "e4m3"), oracle.fp8_decode(_np(B), "e4m3")),
                         "bf16")
     assert np.array_equal(gpu_bits(C), ref)
+
+
+# ------------------------------------------------------------ calibration
+
+def test_calibrate_reduced_size_and_reload(tmp_path, monkeypatch):
+    """fgemm_calibrate at 2048^3 on a handle of its own: every rate it
+    measures is finite and positive, the JSON it writes reloads into a fresh
+    handle (FGEMM_CALIB) as the same model, and AUTO's picks under it stay
+    legal and compute the right product."""
+    import json
+    import math
+    h = fgemm.Handle()
+    path = tmp_path / "calib.json"
+    h.calibrate(str(path), n=2048)
+    m = h.device_model()
+    effs = list(m.eff_classical) + list(m.eff_pair) + [x for row in m.eff_strassen for x in row] + \
+        list(m.eff_strassen_pair) + list(m.eff_winograd)
+    for e in effs:
+        assert math.isfinite(e) and 0 < e < 2.0, effs
+    assert 0.5 <= m.launch_us < 100 and 0.5 <= m.tile_fill_us < 200
+    assert 1000 < m.hbm_gbs < 20000
+    d = json.load(open(path))
+    assert abs(d["eff_pair_256"] - m.eff_pair[1]) <= 1e-8 and abs(d["launch_us"] - m.launch_us) <= 1e-8
+    monkeypatch.setenv("FGEMM_CALIB", str(path))
+    h2 = fgemm.Handle()
+    m2 = h2.device_model()
+    assert abs(m2.eff_pair[1] - m.eff_pair[1]) <= 1e-8 and abs(m2.tile_fill_us - m.tile_fill_us) <= 1e-8
+    for (M, N, K) in [(256, 256, 256), (4096, 4096, 1024), (16, 2048, 2048), (2048, 2048, 2048)]:
+        algo, tm, tn, us = h2.plan(M, N, K)
+        assert fgemm.validate(M, N, K, 16, K, 16, N, 16, N, fgemm.BF16, None, algo, tn, tm) == fgemm.OK
+        assert math.isfinite(us) and us > 0
+        A = inputs.matrix(M, K, "ternary", "bf16", 34, DEV)
+        B = inputs.matrix(K, N, "ternary", "bf16", 35, DEV)
+        C = fgemm.matmul(A, B, handle=h2)
+        torch.cuda.synchronize()
+        assert h2.get_error() == fgemm.OK
+        assert torch.equal(C.float(), (A.float() @ B.float()).to(torch.bfloat16).float())
+    monkeypatch.setenv("FGEMM_CALIB", str(tmp_path / "missing.json"))
+    with pytest.raises(fgemm.FgemmError):
+        fgemm.Handle()
+    h.close()
+    h2.close()
