@@ -388,13 +388,43 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
     *is_temp = 1;
     *idx = static_cast<uint8_t>(t);
   };
+  int first_of[4] = {-1, -1, -1, -1}, last_of[4] = {-1, -1, -1, -1};  // product per output block
   for (int pr = 0; pr < np; ++pr) {
     fgemm::LcmaProduct& P = L.prod[pr];
     operand(tab.na[pr], tab.a[pr], F.job[0], &P.a_temp, &P.a_idx);
     operand(tab.nb[pr], tab.b[pr], F.job[1], &P.b_temp, &P.b_idx);
     P.nc = tab.nc[pr];
-    for (int t = 0; t < P.nc; ++t)
+    for (int t = 0; t < P.nc; ++t) {
       P.c[t] = static_cast<uint8_t>(tab.c[pr][t] & (fgemm::kTermIndexMask | fgemm::kTermNeg));
+      const int blk = P.c[t] & fgemm::kTermIndexMask;
+      if (first_of[blk] < 0) first_of[blk] = pr;
+      last_of[blk] = pr;
+    }
+  }
+  // first and last contribution to each block, and where each output is complete
+  for (int pr = 0; pr < np; ++pr) {
+    fgemm::LcmaProduct& P = L.prod[pr];
+    for (int t = 0; t < P.nc; ++t) {
+      const int blk = P.c[t] & fgemm::kTermIndexMask;
+      if (first_of[blk] == pr) P.c[t] |= fgemm::kTermFirst;
+      if (last_of[blk] == pr) P.c[t] |= fgemm::kTermLast;
+    }
+    P.fin = 0;
+    P.groups = 0;
+    for (int b = 0; b < 4; ++b)
+      if (p.epi != FGEMM_EPI_SWIGLU && last_of[b] == pr) P.fin |= static_cast<uint8_t>(1u << b);
+    for (int sr = 0; sr < 2; ++sr)
+      if (p.epi == FGEMM_EPI_SWIGLU && std::max(last_of[2 * sr], last_of[2 * sr + 1]) == pr)
+        P.fin |= static_cast<uint8_t>(1u << sr);
+    for (int t = 0; t < P.nc; ++t) {
+      const int blk = P.c[t] & fgemm::kTermIndexMask;
+      P.groups |= static_cast<uint8_t>(1u << (p.epi == FGEMM_EPI_SWIGLU ? blk >> 1 : blk));
+    }
+  }
+  for (int g = 0; g < 4; ++g) {
+    int n = 0;
+    for (int pr = 0; pr < np; ++pr) n += (L.prod[pr].groups >> g) & 1u;
+    L.group_pieces[g] = static_cast<uint8_t>(n);
   }
   const int ntA = F.job[0].ntemp, ntB = F.job[1].ntemp;
   const int fit = fgemm::lcma_pair_clusters_fit(bn);
@@ -402,19 +432,26 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   const long long positions = p.num_units;
   L.units = positions * np;
   const int clusters = static_cast<int>(std::min<long long>(fit, L.units));
-  const size_t slot_bytes = static_cast<size_t>(2) * clusters * fgemm::lcma_slot_floats(bn, 1) * sizeof(float);
+  // the positions of the partial last wave run as separate product units
+  const long long tail_positions = positions % clusters;
+  const size_t slot_bytes = static_cast<size_t>(2) * clusters * fgemm::lcma_slot_floats(bn) * sizeof(float);
+  const size_t tail_bytes =
+      static_cast<size_t>(tail_positions) * np * 2 * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float);
   const size_t ta_elems = static_cast<size_t>(ntA) * p.sub_m * p.sub_k;
   const size_t tb_elems = static_cast<size_t>(ntB) * p.sub_k * p.sub_n;
   auto align = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-  const size_t ta_off = align(slot_bytes), tb_off = ta_off + align(ta_elems * 2);
+  const size_t tail_off = align(slot_bytes);
+  const size_t ta_off = tail_off + align(tail_bytes), tb_off = ta_off + align(ta_elems * 2);
   fgemm_status_t s = ensure_workspace(h, tb_off + align(tb_elems * 2));
   if (s != FGEMM_OK) return s;
-  s = ensure_counters(h, static_cast<size_t>(positions) * 8);  // 2 CTAs x 4 epilogue warps
+  // 4 output groups x 2 CTAs x 4 epilogue warps per tail position
+  s = ensure_counters(h, static_cast<size_t>(std::max<long long>(tail_positions, 1)) * 32);
   if (s != FGEMM_OK) return s;
   uint8_t* ws = reinterpret_cast<uint8_t*>(h->workspace);
   uint16_t* TA = reinterpret_cast<uint16_t*>(ws + ta_off);
   uint16_t* TB = reinterpret_cast<uint16_t*>(ws + tb_off);
   p.workspace = h->workspace;
+  p.split_ws = reinterpret_cast<float*>(ws + tail_off);
   p.split_ctr = h->split_ctr;
   p.split_gen = h->split_gen;
   p.num_products = np;

@@ -18,8 +18,10 @@ constexpr int kMaxSplitPieces = 4;  // K pieces per split tile (each last piece 
 
 // Term codes in the Strassen tables: bits [0,5) block index
 // (row_block << depth | col_block) in the 2^depth x 2^depth block grid,
-// bit 6 = first contribution to that output block, bit 7 = negative sign.
+// bit 5 = last contribution to that output block (product kernel on CTA
+// pairs only), bit 6 = first contribution, bit 7 = negative sign.
 constexpr uint8_t kTermIndexMask = 0x1F;
+constexpr uint8_t kTermLast = 0x20;
 constexpr uint8_t kTermFirst = 0x40;
 constexpr uint8_t kTermNeg = 0x80;
 
@@ -207,19 +209,26 @@ struct StrassenParams {
 // Product p of a scheme as the product kernel reads it: its A operand is
 // raw block a_idx of A (a_temp == 0) or temporary a_idx (a_temp == 1), the
 // same for B; its accumulator is added, with the codes' signs, into output
-// blocks c[0 .. nc) (codes as in StrassenTable: block index | kTermNeg).
+// blocks c[0 .. nc) (codes as in StrassenTable, with kTermFirst / kTermLast
+// marking the first and the last contribution to each block in product
+// order).  fin: the output blocks (bit b) whose value is complete once this
+// product is in, or for SwiGLU the block rows (bit r: gate block 2r, up
+// block 2r + 1) complete with it.
 struct LcmaProduct {
   uint8_t a_temp, a_idx, b_temp, b_idx;
   uint8_t nc;
   uint8_t c[kMaxTerms];
+  uint8_t fin;
+  uint8_t groups;  // output groups it feeds (bit g: block g, or for SwiGLU block row g)
 };
 
 struct LcmaParams {
   KernelParams k;        // tmap_a / tmap_b map A and B; k.workspace holds the partial tiles
   CUtensorMap tmap_ta;   // A temporaries: inner sub_k, outer ntemp_a * sub_m, box {64, 128}
   CUtensorMap tmap_tb;   // B temporaries: inner sub_n, outer ntemp_b * sub_k, box {64, 64}
-  long long units;       // output positions * num_products
+  long long units;       // output positions * num_products (informational)
   LcmaProduct prod[kMaxProducts];
+  uint8_t group_pieces[4];  // products feeding each output group
 };
 
 // One matrix of the pre-pass: the `rows` x `cols` blocks of src (block q at
@@ -241,19 +250,20 @@ struct LcmaFormParams {
   int is_bf16;
 };
 
-// Per-CTA partial tiles of the product kernel: three slots (a pair's first
-// output position, its last, and the ones between) of 4^depth blocks of
-// 128 x bn fp32.
-inline size_t lcma_slot_floats(int bn, int depth) {
-  return static_cast<size_t>(3) * (size_t{1} << (2 * depth)) * 128 * static_cast<size_t>(bn);
-}
+// Per-CTA partial tiles of the product kernel's whole positions: the four
+// output blocks of one level, 128 x bn fp32 each.
+inline size_t lcma_slot_floats(int bn) { return static_cast<size_t>(4) * 128 * static_cast<size_t>(bn); }
 
 // The pre-pass (depth 1) over both jobs in one launch.
 cudaError_t launch_lcma_form(const LcmaFormParams& f, int num_sms, cudaStream_t stream);
 
 // The product kernel for one Strassen-like level on `clusters` CTA pairs
-// (bn = 128 or 256); p.k.split_ctr / split_gen carry the position counters
-// (8 per output position) for positions whose products span two pairs.
+// (bn = 128 or 256).  p.k.workspace holds 2 * clusters * lcma_slot_floats
+// partials; the T = positions mod clusters positions of the partial last
+// wave run as 7 T separate product units, whose accumulators (128 x bn fp32
+// per unit and CTA) go to p.k.split_ws, with 32 counters per such position
+// (4 output groups x 2 CTAs x 4 epilogue warps) in p.k.split_ctr tagged with
+// p.k.split_gen.
 cudaError_t launch_lcma_pair(int bn, const LcmaParams& p, int clusters, cudaStream_t stream);
 
 // How many clusters of the product kernel fit on the current device.

@@ -12,17 +12,22 @@
 //     launch on CTA pairs: 256 x BN tiles of the half-size block space, on
 //     the classical pair mainloop (TMA -> 128-byte-swizzled shared-memory ring
 //     -> tcgen05.mma cta_group::2 -> double-buffered TMEM), so the tensor
-//     pipe sees the same operand stream as a classical product.  The work
-//     units (output position, product), position-major, are shared out in
-//     equal contiguous ranges over the pairs.  The epilogue warps fold each
-//     product's accumulator into per-CTA fp32 partial tiles of the output
-//     blocks it feeds (C11 = M1 + M4 - M5 + M7, ...) with TMA bulk stores
-//     (first contribution) and bulk reduce-adds performed at the L2, so no
-//     load latency sits in the fold.  After the last product of a position
-//     they apply alpha / bias / activation to every block and store C.  A
-//     position whose products fall in two pairs' ranges is finished by the
-//     last pair to arrive (a generation-tagged counter), which adds the
-//     pairs' partials in pair order: the result does not depend on timing.
+//     pipe sees the same operand stream as a classical product.  Each pair
+//     runs whole output positions in waves (all seven products of one
+//     position, the pairs in step on the same product, so neighbouring
+//     positions share its operand panels in the L2).  The epilogue warps
+//     fold each product's accumulator into per-CTA fp32 partial tiles of the
+//     output blocks it feeds (C11 = M1 + M4 - M5 + M7, ...): the first
+//     contribution to a block is stored, the next ones are added by vector
+//     atomic reductions performed at the L2 (no load latency in the fold),
+//     and at a block's last contribution the epilogue reads the partial,
+//     adds the accumulator, applies alpha / bias / activation and stores C.
+//     The
+//     partial last wave's positions run as separate (product, position)
+//     units shared out evenly over the pairs: each stores its accumulator,
+//     and the last of a position's seven to finish (a generation-tagged
+//     counter) combines them in product order, so the result does not
+//     depend on timing.
 //
 // Why the sums go through HBM on this chip: the classical 256 x 256 pair
 // mainloop already keeps the shared-memory port and the tensor pipe near
@@ -48,7 +53,9 @@ __device__ __forceinline__ const uint4* form_src(const LcmaFormJob& J, int q, in
 
 // One warp per row and 32 column groups of 8 elements (16 bytes) per warp:
 // the four blocks' 16 bytes are loaded once, every temporary's 16 bytes
-// formed and stored.  blockIdx.z selects the matrix (A or B).
+// formed and stored.  blockIdx.z selects the matrix (A or B).  The source
+// blocks are read through the read-only path and the temporaries written
+// once; the sums of a row's group are independent of every other group.
 __global__ void __launch_bounds__(256) lcma_form_kernel(const __grid_constant__ LcmaFormParams P) {
   const LcmaFormJob& J = P.job[blockIdx.z];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -56,31 +63,43 @@ __global__ void __launch_bounds__(256) lcma_form_kernel(const __grid_constant__ 
   const int c8 = blockIdx.x * 32 + lane;
   if (J.ntemp == 0 || c8 >= cols8) return;
   const long long plane = static_cast<long long>(J.rows) * J.cols;
+  // two rows per iteration: eight 16-byte loads in flight per thread
+  const int step = gridDim.y * 8;
 #pragma unroll 1
-  for (int r = blockIdx.y * 8 + warp; r < J.rows; r += gridDim.y * 8) {
-    uint4 raw[4];
+  for (int r0 = blockIdx.y * 8 + warp; r0 < J.rows; r0 += 2 * step) {
+    uint4 raw[2][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      raw[q] = (J.block_mask >> q) & 1u ? __ldg(form_src(J, q, r) + c8) : make_uint4(0, 0, 0, 0);
-    uint16_t* dst = J.dst + static_cast<long long>(r) * J.cols + c8 * 8;
+    for (int h = 0; h < 2; ++h) {
+      const int r = r0 + h * step;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        raw[h][q] = (r < J.rows && ((J.block_mask >> q) & 1u)) ? __ldg(form_src(J, q, r) + c8)
+                                                               : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = r0 + h * step;
+      if (r >= J.rows) break;
+      uint16_t* dst = J.dst + static_cast<long long>(r) * J.cols + c8 * 8;
 #pragma unroll 1
-    for (int t = 0; t < J.ntemp; ++t) {
-      float acc[8];
+      for (int t = 0; t < J.ntemp; ++t) {
+        float acc[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int cf = J.coef[t][q];
-        if (cf != 0) {
-          float f[8];
-          unpack8(raw[q], f, P.is_bf16);
+        for (int q = 0; q < 4; ++q) {
+          const int cf = J.coef[t][q];
+          if (cf != 0) {
+            float f[8];
+            unpack8(raw[h][q], f, P.is_bf16);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] += cf > 0 ? f[i] : -f[i];
+            for (int i = 0; i < 8; ++i) acc[i] += cf > 0 ? f[i] : -f[i];
+          }
         }
+        *reinterpret_cast<uint4*>(dst + t * plane) =
+            make_uint4(pack2(acc[0], acc[1], P.is_bf16), pack2(acc[2], acc[3], P.is_bf16),
+                       pack2(acc[4], acc[5], P.is_bf16), pack2(acc[6], acc[7], P.is_bf16));
       }
-      *reinterpret_cast<uint4*>(dst + t * plane) =
-          make_uint4(pack2(acc[0], acc[1], P.is_bf16), pack2(acc[2], acc[3], P.is_bf16),
-                     pack2(acc[4], acc[5], P.is_bf16), pack2(acc[6], acc[7], P.is_bf16));
     }
   }
 }
@@ -110,137 +129,175 @@ struct LcmaCfg {
   static constexpr int kStages = BN == 256 ? 6 : 8;
   static constexpr int kTmemCols = BN == 256 ? 512 : 256;
   static constexpr int kBarBytes = 1024;
-  // After the barriers: per epilogue warp two 4 KB buffers of 32 rows x 32
-  // fp32 values, the sources of the bulk stores / reduce-adds of the fold.
-  // The region is longer than a B half, so even a full-width MMA read of the
-  // last stage stays inside this CTA's shared memory.
-  static constexpr int kStagingOff = kStages * kStageBytes + kBarBytes;
-  static constexpr int kStagingBytes = 4 * 2 * 4096;
-  static constexpr int kSmemBytes = 1024 + kStagingOff + kStagingBytes;
+  // After the barriers, one B half of slack: even a full-width MMA read of
+  // the last stage stays inside this CTA's shared memory.
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kBBytes;
   static constexpr int kChunks = BN / 32;
   static constexpr int kBlocks = 4;  // output blocks of one level
-  static_assert(kStagingBytes >= kBBytes, "slack past the last stage");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(2 * BN <= kTmemCols, "two accumulator buffers must fit in TMEM");
   static_assert((2 * kStages + 5) * 8 + 4 <= kBarBytes, "barrier area too small");
 };
 
-// The contiguous range of units [lo, hi) of pair c (equal shares, +-1).
-__device__ __forceinline__ void lcma_range(long long units, int pairs, int c, long long& lo,
-                                           long long& hi) {
-  lo = static_cast<long long>(c) * units / pairs;
-  hi = static_cast<long long>(c + 1) * units / pairs;
-}
+// The schedule.  With P pairs and `positions` output positions (256 x BN
+// tiles of the half-size block space, in rasterised order), the first
+// W = floor(positions / P) waves are whole positions: pair c runs positions
+// c, c + P, c + 2P, ..., each through products 0 .. 6 in order, so that at
+// any moment the pairs work on neighbouring positions and on the same
+// product and share its operand panels in the L2, as a classical wave does.
+// The T = positions - W P positions of the partial last wave are cut into
+// their 7 T units (product, position), product-major (unit t: product
+// t / T, position W P + t mod T), shared out in equal contiguous ranges, one
+// per pair, after its whole positions.  A tail unit stores its accumulator;
+// the last of a position's seven units to finish combines them.
+struct LcmaItem {
+  long long pos;   // output position (unit_coords order)
+  int pr;          // product
+  long long tail;  // tail unit index, or -1 for a product of a whole position
+};
 
-// Partial slot of output position `pos` on a pair whose units are [lo, hi):
-// 0 for its first position, 1 for its last, 2 for the ones between.
-__device__ __forceinline__ int lcma_slot(long long lo, long long hi, int np, long long pos) {
-  if (pos == lo / np) return 0;
-  if (pos == (hi - 1) / np) return 1;
-  return 2;
-}
+struct LcmaSchedule {
+  long long whole;   // W: whole positions per pair
+  long long tail0;   // W * P: the first tail position
+  long long tail_n;  // T: tail positions
+  long long tlo, thi;  // this pair's tail units [tlo, thi)
+  __device__ LcmaSchedule(long long positions, int pairs, int np, int c) {
+    whole = positions / pairs;
+    tail0 = whole * pairs;
+    tail_n = positions - tail0;
+    const long long ut = tail_n * np;
+    tlo = static_cast<long long>(c) * ut / pairs;
+    thi = static_cast<long long>(c + 1) * ut / pairs;
+  }
+  __device__ long long items(int np) const { return whole * np + (thi - tlo); }
+  __device__ LcmaItem item(long long n, int np, int pairs, int c) const {
+    LcmaItem it;
+    if (n < whole * np) {
+      it.pos = c + (n / np) * pairs;
+      it.pr = static_cast<int>(n % np);
+      it.tail = -1;
+    } else {
+      it.tail = tlo + (n - whole * np);
+      it.pr = static_cast<int>(it.tail / tail_n);
+      it.pos = tail0 + it.tail % tail_n;
+    }
+    return it;
+  }
+};
 
-__device__ __forceinline__ long long lmax(long long a, long long b) { return a > b ? a : b; }
-__device__ __forceinline__ long long lmin(long long a, long long b) { return a < b ? a : b; }
-
-// Output blocks that products [k0, k1) of the scheme feed.
-__device__ __forceinline__ uint32_t lcma_block_mask(const LcmaParams& L, int k0, int k1) {
-  uint32_t m = 0;
-  for (int k = k0; k < k1; ++k)
-    for (int t = 0; t < L.prod[k].nc; ++t) m |= 1u << (L.prod[k].c[t] & kTermIndexMask);
-  return m;
-}
-
-// The 32 x 32 fp32 values warp `ew` of CTA `cta` holds for chunk c of output
-// block blk in slot s: 4 KB, row lane at lane * 32.
+// fp32 tiles in global memory (a CTA's partial of one output block, or the
+// accumulator of a tail unit): 128 rows x BN, laid out [32-column chunk]
+// [column quad: 8][row: 128][4], so that a warp's 16-byte accesses to one
+// (chunk, quad) cover 512 contiguous bytes.  These return the chunk's base;
+// row r's quad q is at index q * 128 + r.
 template <int BN>
-__device__ __forceinline__ float* lcma_part(float* ws, int cta, int s, int blk, int c, int ew) {
+__device__ __forceinline__ float4* lcma_part(float* ws, int cta, int blk, int c) {
   using LC = LcmaCfg<BN>;
-  const size_t per_cta = static_cast<size_t>(3) * LC::kBlocks * kBM * BN;
-  return ws + static_cast<size_t>(cta) * per_cta +
-         ((static_cast<size_t>(s) * LC::kBlocks + blk) * LC::kChunks + c) * (kBM * 32) +
-         static_cast<size_t>(ew) * 1024;
+  return reinterpret_cast<float4*>(ws + static_cast<size_t>(cta) * (LC::kBlocks * kBM * BN) +
+                                   (static_cast<size_t>(blk) * LC::kChunks + c) * (kBM * 32));
 }
 
-// v[j] (+)= row `lane` of a 32 x 32 partial.
-__device__ __forceinline__ void lcma_load_row(const float* part, int lane, float (&v)[32], bool add) {
-  const float4* src = reinterpret_cast<const float4*>(part + lane * 32);
+template <int BN>
+__device__ __forceinline__ float4* lcma_tail_part(float* ws, long long t, uint32_t rank, int c) {
+  return reinterpret_cast<float4*>(ws + (static_cast<size_t>(t) * 2 + rank) * (kBM * BN) +
+                                   static_cast<size_t>(c) * (kBM * 32));
+}
+
+// v[j] = (add ? v[j] : 0) + sg * row r of a 32-column chunk.
+__device__ __forceinline__ void lcma_load_row(const float4* chunk, int r, float (&v)[32], bool add,
+                                              float sg) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    const float4 f = __ldcg(src + q);
+    const float4 f = __ldcg(chunk + q * kBM + r);
     if (add) {
-      v[4 * q + 0] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
+      v[4 * q + 0] += sg * f.x; v[4 * q + 1] += sg * f.y; v[4 * q + 2] += sg * f.z; v[4 * q + 3] += sg * f.w;
     } else {
-      v[4 * q + 0] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+      v[4 * q + 0] = sg * f.x; v[4 * q + 1] = sg * f.y; v[4 * q + 2] = sg * f.z; v[4 * q + 3] = sg * f.w;
     }
   }
 }
 
-// Finishes output position (tm, tn) for this warp's 32 rows of this CTA:
-// for every output block and 32-column chunk, the sum in pair order of the
-// partials of pairs [c0, c1] that fed the block, then alpha / bias /
-// activation and the store of C.  Every pair's partial lies in its slot for
-// this position.
+// Stores (or, add == true, atomically adds) sg * v (fp32 bit patterns) as
+// row r of a chunk.  Every address of a partial is only ever written by one
+// thread, whose operations on it take effect in program order, so the fp32
+// additions happen in product order whatever the timing.
+__device__ __forceinline__ void lcma_put_row(float4* chunk, int r, const uint32_t (&v)[32], float sg,
+                                             bool add) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 f = make_float4(sg * __uint_as_float(v[4 * q + 0]), sg * __uint_as_float(v[4 * q + 1]),
+                                 sg * __uint_as_float(v[4 * q + 2]), sg * __uint_as_float(v[4 * q + 3]));
+    if (add)
+      atomicAdd(chunk + q * kBM + r, f);
+    else
+      __stcg(chunk + q * kBM + r, f);
+  }
+}
+
+// alpha / bias / activation of output block blk (or, for SwiGLU, of gate
+// block 2 sr and up block 2 sr + 1 given as g and u) for 32 columns of chunk
+// c of position (tm, tn), and the store of C by this thread's row.
 template <int BN>
-__device__ void lcma_finish(const LcmaParams& L, int pairs, int c0, int c1, long long pos, int tm,
-                            int tn, uint32_t rank, int ew) {
+__device__ __forceinline__ void lcma_emit(const KernelParams& p, int blk, int c, int tm, int tn,
+                                          uint32_t rank, int r, float (&v)[32]) {
+  const int col0 = (blk & 1) * p.sub_n + tn * BN + c * 32;
+  float b[32];
+  bias32(p, 0, col0, b);
+  finish_plain(p, b, v);
+  store_row32(p, (blk >> 1) * p.sub_m + tm * (2 * kBM) + static_cast<int>(rank) * kBM + r, col0, v);
+}
+
+template <int BN>
+__device__ __forceinline__ void lcma_emit_swiglu(const KernelParams& p, int sr, int c, int tm, int tn,
+                                                 uint32_t rank, int r, float (&g)[32], const float (&u)[32]) {
+  const int col0 = tn * BN + c * 32;
+  finish_swiglu_warp(p, col0, g, u);
+  store_row32(p, sr * p.sub_m + tm * (2 * kBM) + static_cast<int>(rank) * kBM + r, col0, g);
+}
+
+// Finishes output group g of a tail position (its index among the T tail
+// positions) for this warp's 32 rows of this CTA: output block g, or for
+// SwiGLU block row g (gate block 2g, up block 2g + 1).  Every block is the
+// sum, in product order with the scheme's signs, of the stored accumulators
+// of the products that feed it, so the result does not depend on which unit
+// finished last.
+template <int BN>
+__device__ void lcma_finish_tail(const LcmaParams& L, long long tail_pos, long long tail_n, int g, int tm,
+                                 int tn, uint32_t rank, int ew) {
   using LC = LcmaCfg<BN>;
   const KernelParams& p = L.k;
-  const int lane = threadIdx.x & 31;
+  const int r = ew * 32 + (threadIdx.x & 31);
   const int np = p.num_products;
-  int slot[8];
-  uint32_t mask[8];
-  const int ns = c1 - c0 + 1;  // at most 8 pairs share a position (7 products)
-  for (int i = 0; i < ns; ++i) {
-    long long lo, hi;
-    lcma_range(L.units, pairs, c0 + i, lo, hi);
-    const long long u0 = pos * np;
-    const int k0 = static_cast<int>(lmax(lo, u0) - u0);
-    const int k1 = static_cast<int>(lmin(hi, u0 + np) - u0);
-    slot[i] = lcma_slot(lo, hi, np, pos);
-    mask[i] = lcma_block_mask(L, k0, k1);
-  }
   auto gather = [&](int blk, int c, float (&v)[32]) {
     bool any = false;
-    for (int i = 0; i < ns; ++i) {
-      if (!((mask[i] >> blk) & 1u)) continue;
-      const int cta = 2 * (c0 + i) + static_cast<int>(rank);
-      lcma_load_row(lcma_part<BN>(p.workspace, cta, slot[i], blk, c, ew), lane, v, any);
-      any = true;
+    for (int k = 0; k < np; ++k) {
+      for (int t = 0; t < L.prod[k].nc; ++t) {
+        const uint8_t code = L.prod[k].c[t];
+        if ((code & kTermIndexMask) != blk) continue;
+        lcma_load_row(lcma_tail_part<BN>(p.split_ws, k * tail_n + tail_pos, rank, c), r, v, any,
+                      (code & kTermNeg) ? -1.0f : 1.0f);
+        any = true;
+      }
     }
     if (!any) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0.0f;
     }
   };
-  const int row_in = tm * (2 * kBM) + static_cast<int>(rank) * kBM + ew * 32 + lane;
   if (p.epi == kEpiSwiglu) {
-    // gate = output blocks (r, 0), up = (r, 1): the halves of the N split
 #pragma unroll 1
-    for (int sr = 0; sr < 2; ++sr) {
-#pragma unroll 1
-      for (int c = 0; c < LC::kChunks; ++c) {
-        float g[32], u[32];
-        gather(sr * 2, c, g);
-        gather(sr * 2 + 1, c, u);
-        const int col0 = tn * BN + c * 32;
-        finish_swiglu_warp(p, col0, g, u);
-        store_row32(p, sr * p.sub_m + row_in, col0, g);
-      }
+    for (int c = 0; c < LC::kChunks; ++c) {
+      float gv[32], uv[32];
+      gather(g * 2, c, gv);
+      gather(g * 2 + 1, c, uv);
+      lcma_emit_swiglu<BN>(p, g, c, tm, tn, rank, r, gv, uv);
     }
   } else {
 #pragma unroll 1
-    for (int blk = 0; blk < LC::kBlocks; ++blk) {
-#pragma unroll 1
-      for (int c = 0; c < LC::kChunks; ++c) {
-        float v[32];
-        gather(blk, c, v);
-        const int col0 = (blk & 1) * p.sub_n + tn * BN + c * 32;
-        float b[32];
-        bias32(p, 0, col0, b);
-        finish_plain(p, b, v);
-        store_row32(p, (blk >> 1) * p.sub_m + row_in, col0, v);
-      }
+    for (int c = 0; c < LC::kChunks; ++c) {
+      float v[32];
+      gather(g, c, v);
+      lcma_emit<BN>(p, g, c, tm, tn, rank, r, v);
     }
   }
 }
@@ -272,8 +329,8 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
   const int cluster = blockIdx.x >> 1;
   const int pairs = gridDim.x >> 1;
   const int np = p.num_products;
-  long long lo, hi;
-  lcma_range(L.units, pairs, cluster, lo, hi);
+  const LcmaSchedule sched(p.num_units, pairs, np, cluster);
+  const long long n_items = sched.items(np);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -306,20 +363,47 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (long long u = lo; ok && u < hi; ++u) {
-        const long long pos = u / np;
-        const LcmaProduct& P = L.prod[u - pos * np];
+      // Where item n's operand tiles come from: the tensor maps and the
+      // coordinates of this CTA's first K block.
+      struct Src {
+        const CUtensorMap* amap;
+        const CUtensorMap* bmap;
+        int ax, ay, bx, by;
+      };
+      auto source = [&](long long n) {
+        const LcmaItem it = sched.item(n, np, pairs, cluster);
+        const LcmaProduct& P = L.prod[it.pr];
         int tm, tn;
-        unit_coords(p, static_cast<int>(pos), tm, tn);
-        const CUtensorMap* amap = P.a_temp ? &L.tmap_ta : &p.tmap_a;
-        const CUtensorMap* bmap = P.b_temp ? &L.tmap_tb : &p.tmap_b;
-        const int ay = (P.a_temp ? P.a_idx : (P.a_idx >> 1)) * p.sub_m + tm * (2 * kBM) +
-                       static_cast<int>(rank) * kBM;
-        const int ax = P.a_temp ? 0 : (P.a_idx & 1) * p.sub_k;
-        const int by = (P.b_temp ? P.b_idx : (P.b_idx >> 1)) * p.sub_k;
-        const int bx = (P.b_temp ? 0 : (P.b_idx & 1) * p.sub_n) + tn * BN +
-                       static_cast<int>(rank) * (BN / 2);
+        unit_coords(p, static_cast<int>(it.pos), tm, tn);
+        Src o;
+        o.amap = P.a_temp ? &L.tmap_ta : &p.tmap_a;
+        o.bmap = P.b_temp ? &L.tmap_tb : &p.tmap_b;
+        o.ay = (P.a_temp ? P.a_idx : (P.a_idx >> 1)) * p.sub_m + tm * (2 * kBM) + static_cast<int>(rank) * kBM;
+        o.ax = P.a_temp ? 0 : (P.a_idx & 1) * p.sub_k;
+        o.by = (P.b_temp ? P.b_idx : (P.b_idx >> 1)) * p.sub_k;
+        o.bx = (P.b_temp ? 0 : (P.b_idx & 1) * p.sub_n) + tn * BN + static_cast<int>(rank) * (BN / 2);
+        return o;
+      };
+      // Every pair moves to new operand panels at about the same time, so
+      // the first K blocks of a unit would all miss the L2 at once: the L2
+      // is asked for them kPrefetchAhead K blocks before the current unit
+      // ends.
+      constexpr int kPrefetchAhead = 16, kPrefetchBlocks = 8;
+      for (long long n = 0; ok && n < n_items; ++n) {
+        const Src cur = source(n);
+        const CUtensorMap* amap = cur.amap;
+        const CUtensorMap* bmap = cur.bmap;
+        const int ax = cur.ax, ay = cur.ay, bx = cur.bx, by = cur.by;
+        const int pf_at = n + 1 < n_items ? max(0, p.k_blocks - kPrefetchAhead) : -1;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (kb == pf_at) {
+            const Src nx = source(n + 1);
+            for (int j = 0; j < kPrefetchBlocks && j < p.k_blocks; ++j) {
+              ptx::tma_prefetch_2d(nx.amap, nx.ax + j * kBK, nx.ay);
+#pragma unroll
+              for (int q = 0; q < BN / 128; ++q) ptx::tma_prefetch_2d(nx.bmap, nx.bx + q * 64, nx.by + j * kBK);
+            }
+          }
           if (!wait_one(empty(s), ph ^ 1u, p, 0)) {
             ok = false;
             break;
@@ -353,7 +437,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
       int s = 0;
       uint32_t ph = 0, acc_it = 0;
       bool ok = true;
-      for (long long u = lo; ok && u < hi; ++u) {
+      for (long long n = 0; ok && n < n_items; ++n) {
         const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
         ++acc_it;
         if (!wait_one(tempty(buf), aph ^ 1u, p, 1)) {
@@ -389,98 +473,102 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
   } else if (warp >= 4) {
     // ------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 4;
-    uint8_t* stg = base_ptr + LC::kStagingOff + ew * 8192;
-    const uint32_t stg_addr = base + LC::kStagingOff + ew * 8192;
-    uint32_t acc_it = 0, nbulk = 0;
-    uint32_t written = 0;  // output blocks of the current position this pair has stored
+    const int r = ew * 32 + lane;
+    uint32_t acc_it = 0;
     bool ok = true;
-    for (long long u = lo; ok && u < hi; ++u) {
-      const long long pos = u / np;
-      const int pr = static_cast<int>(u - pos * np);
-      const long long u0 = pos * np;
-      const int k_lo = static_cast<int>(lmax(lo, u0) - u0);
-      const int k_hi = static_cast<int>(lmin(hi, u0 + np) - u0);
-      const int slot = lcma_slot(lo, hi, np, pos);
+    for (long long n = 0; ok && n < n_items; ++n) {
+      const LcmaItem it = sched.item(n, np, pairs, cluster);
       const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
       ++acc_it;
-      if (pr == k_lo) written = 0;
-      // the previous product's bulk operations have landed before this one
-      // adds to the same partials (a fixed order of the fp32 additions)
-      if (lane == 0) ptx::bulk_wait<0>();
-      __syncwarp();
       if (!wait_warp(tfull(buf), aph, p, 2)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * BN;
-      const LcmaProduct& P = L.prod[pr];
+      const LcmaProduct& P = L.prod[it.pr];
       const int nc = P.nc;
-      uint32_t first_bits = 0;
-      for (int t = 0; t < nc; ++t) {
-        const int blk = P.c[t] & kTermIndexMask;
-        if (!((written >> blk) & 1u)) first_bits |= 1u << t;
-        written |= 1u << blk;
-      }
+      int tm, tn;
+      unit_coords(p, static_cast<int>(it.pos), tm, tn);
 #pragma unroll 1
       for (int c = 0; c < LC::kChunks; ++c) {
         uint32_t ar[32];
         ptx::tmem_ld_32x32b_x32(tbase + c * 32, ar);
         ptx::tmem_wait_ld();
         ptx::tmem_regs_ready(ar);
-#pragma unroll 1
+        if (it.tail >= 0) {  // a tail unit keeps its accumulator as it is
+          lcma_put_row(lcma_tail_part<BN>(p.split_ws, it.tail, rank, c), r, ar, 1.0f, false);
+          continue;
+        }
+        // fold into the partials of the blocks this product feeds, except
+        // where it is the block's last contribution (finished below)
         for (int t = 0; t < nc; ++t) {
-          const uint32_t sb = nbulk & 1u;
-          // the bulk operation that read this buffer two operations ago is done reading
-          if (lane == 0) ptx::bulk_wait_read<1>();
-          __syncwarp();
-          const float sg = (P.c[t] & kTermNeg) ? -1.0f : 1.0f;
-          float4* row = reinterpret_cast<float4*>(stg + sb * 4096 + lane * 128);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            row[q] = make_float4(sg * __uint_as_float(ar[4 * q + 0]), sg * __uint_as_float(ar[4 * q + 1]),
-                                 sg * __uint_as_float(ar[4 * q + 2]), sg * __uint_as_float(ar[4 * q + 3]));
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            float* dst = lcma_part<BN>(p.workspace, static_cast<int>(blockIdx.x), slot,
-                                       P.c[t] & kTermIndexMask, c, ew);
-            if ((first_bits >> t) & 1u)
-              ptx::bulk_store(dst, stg_addr + sb * 4096, 4096);
-            else
-              ptx::bulk_reduce_add_f32(dst, stg_addr + sb * 4096, 4096);
-            ptx::bulk_commit();
+          const uint8_t code = P.c[t];
+          if (code & kTermLast) continue;
+          lcma_put_row(lcma_part<BN>(p.workspace, static_cast<int>(blockIdx.x), code & kTermIndexMask, c), r, ar,
+                       (code & kTermNeg) ? -1.0f : 1.0f, !(code & kTermFirst));
+        }
+        if (!P.fin) continue;
+        // the value of block blk once this product is in: its partial (the
+        // earlier products, in order) plus this product's share, if any (the
+        // chunk is read from TMEM again, so no copy of it stays live here)
+        auto final_block = [&](int blk, float (&v)[32]) {
+          bool fed = false, first = false;
+          float sg = 1.0f;
+          for (int t = 0; t < nc; ++t) {
+            if ((P.c[t] & kTermIndexMask) != blk) continue;
+            fed = true;
+            first = (P.c[t] & kTermFirst) != 0;
+            sg = (P.c[t] & kTermNeg) ? -1.0f : 1.0f;
           }
-          ++nbulk;
+          if (!first) lcma_load_row(lcma_part<BN>(p.workspace, static_cast<int>(blockIdx.x), blk, c), r, v, false, 1.0f);
+          if (fed) {
+            uint32_t x[32];
+            ptx::tmem_ld_32x32b_x32(tbase + c * 32, x);
+            ptx::tmem_wait_ld();
+            ptx::tmem_regs_ready(x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = first ? sg * __uint_as_float(x[j]) : v[j] + sg * __uint_as_float(x[j]);
+          }
+        };
+        if (p.epi == kEpiSwiglu) {
+#pragma unroll 1
+          for (int sr = 0; sr < 2; ++sr) {
+            if (!((P.fin >> sr) & 1u)) continue;
+            float g[32], u[32];
+            final_block(sr * 2, g);
+            final_block(sr * 2 + 1, u);
+            lcma_emit_swiglu<BN>(p, sr, c, tm, tn, rank, r, g, u);
+          }
+        } else {
+#pragma unroll 1
+          for (int blk = 0; blk < LC::kBlocks; ++blk) {
+            if (!((P.fin >> blk) & 1u)) continue;
+            float v[32];
+            final_block(blk, v);
+            lcma_emit<BN>(p, blk, c, tm, tn, rank, r, v);
+          }
         }
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty(buf), 0));
-      if (pr != k_hi - 1) continue;
-      // the pair's last product of this position: its partials are complete
-      if (lane == 0) ptx::bulk_wait<0>();
+      if (it.tail < 0) continue;
+      // a tail unit: for every output group (block, or SwiGLU block row) it
+      // feeds, the last of the group's feeding units to finish combines them
+      const long long tail_pos = it.pos - sched.tail0;
+      __threadfence();
       __syncwarp();
-      ptx::fence_proxy_async_global();
-      int tm, tn;
-      unit_coords(p, static_cast<int>(pos), tm, tn);
-      if (k_lo == 0 && k_hi == np) {
-        lcma_finish<BN>(L, pairs, cluster, cluster, pos, tm, tn, rank, ew);
-        continue;
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        if (!((P.groups >> g) & 1u)) continue;
+        const bool last = count_arrival(
+            p, p.split_ctr + ((static_cast<size_t>(tail_pos) * 4 + g) * 2 + rank) * 4 + ew, L.group_pieces[g]);
+        if (!last) continue;
+        __threadfence();
+        lcma_finish_tail<BN>(L, tail_pos, sched.tail_n, g, tm, tn, rank, ew);
       }
-      const int c0 = stream_k_owner(u0, L.units, pairs);
-      const int c1 = stream_k_owner(u0 + np - 1, L.units, pairs);
-      __threadfence();
-      __syncwarp();
-      const bool last = count_arrival(p, p.split_ctr + (static_cast<size_t>(pos) * 2 + rank) * 4 + ew,
-                                      c1 - c0 + 1);
-      if (!last) continue;
-      __threadfence();
-      ptx::fence_proxy_async_global();
-      lcma_finish<BN>(L, pairs, c0, c1, pos, tm, tn, rank, ew);
     }
-    if (lane == 0) ptx::bulk_wait<0>();
-    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -544,7 +632,7 @@ cudaError_t launch_lcma_pair_t(const LcmaParams& L, int clusters, cudaStream_t s
   int fit = 0;
   cudaError_t e = lcma_config<BN>(cfg, attr, fit, stream);
   if (e != cudaSuccess) return e;
-  if (clusters < 1 || clusters > fit || static_cast<long long>(clusters) > L.units)
+  if (clusters < 1 || clusters > fit || clusters > L.k.num_units * L.k.num_products)
     return cudaErrorInvalidValue;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   return cudaLaunchKernelEx(&cfg, fgemm_kernel_pair_lcma<BN>, L);

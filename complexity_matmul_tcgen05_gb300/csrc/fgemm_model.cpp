@@ -293,8 +293,10 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     // One level on CTA pairs with the summed operands streamed through HBM:
     // a pre-pass reads A and B once and writes each summed operand once
     // (Strassen: 5 + 5 of the 4 + 4 blocks, Winograd: 4 + 4), then the seven
-    // block products run on the classical pair mainloop, their (position,
-    // product) units shared out evenly over the pairs.
+    // block products run on the classical pair mainloop: whole positions in
+    // waves over the pairs, the partial last wave's positions as separate
+    // product units shared out evenly, whose combination costs about one
+    // more fill.
     const bool wino = algo == FGEMM_ALGO_WINOGRAD1;
     const int64_t sub_m = M / 2, sub_n = N / 2, sub_k = K / 2;
     const double temps = wino ? 4.0 : 5.0;
@@ -306,12 +308,14 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     const int64_t positions = fgemm_model_tiles(sub_m, sub_n, 256, tile_n);
     const int32_t pairs = std::max(1, dev->num_sms / 2);
     const int64_t units = positions * 7;
+    const int64_t used = std::min<int64_t>(pairs, units);
+    const int64_t tail_units = (positions % used) * 7;
     const double eff = std::max(dev->eff_strassen_pair[tile_n == 128 ? 0 : 1], 1e-3);
     const double pair_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms * 2.0;
     const double k_pad = static_cast<double>(ceil_div(sub_k, fgemm::kBK) * fgemm::kBK);
     const double t_unit = 2.0 * 256.0 * tile_n * k_pad / (pair_flop_per_us * eff);
-    const double t_compute = static_cast<double>(ceil_div(units, std::min<int64_t>(pairs, units))) * t_unit +
-                             dev->tile_fill_us;
+    const double per_pair = static_cast<double>((positions / used) * 7 + ceil_div(tail_units, used));
+    const double t_compute = per_pair * t_unit + dev->tile_fill_us * (tail_units > 0 ? 2.0 : 1.0);
     if (predicted_us) *predicted_us = t_pre + t_compute + dev->launch_us;
     return FGEMM_OK;
   }
