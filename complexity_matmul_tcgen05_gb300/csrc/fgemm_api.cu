@@ -1078,9 +1078,24 @@ extern "C" fgemm_status_t fgemm_calibrate_ex(fgemm_handle_t h, int64_t n, const 
       }
     }
     for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
+      // one level on CTA pairs: a pre-pass plus the product kernel, so the
+      // product kernel's rate is the one under which the model predicts the
+      // measured time (found by bisection; the prediction falls as it rises)
       double us = 0;
-      if (!time_gemm(n, n, n, FGEMM_ALGO_STRASSEN1, 256, i == 0 ? 128 : 256, &us)) break;
-      m.eff_strassen_pair[i] = flops * 7.0 / 8.0 / (us * 1e6) / m.peak_tflops;
+      const int32_t tn = i == 0 ? 128 : 256;
+      if (!time_gemm(n, n, n, FGEMM_ALGO_STRASSEN1, 256, tn, &us)) break;
+      double lo = 1e-3, hi = 4.0;
+      for (int it = 0; it < 60; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        m.eff_strassen_pair[i] = mid;
+        double pred = 0;
+        fgemm_model_predict(&m, n, n, n, FGEMM_EPI_NONE, FGEMM_ALGO_STRASSEN1, 256, tn, &pred);
+        if (pred > us)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      m.eff_strassen_pair[i] = 0.5 * (lo + hi);
     }
     for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
       double us = 0;

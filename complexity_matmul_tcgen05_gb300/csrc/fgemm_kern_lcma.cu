@@ -384,26 +384,12 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
         o.bx = (P.b_temp ? 0 : (P.b_idx & 1) * p.sub_n) + tn * BN + static_cast<int>(rank) * (BN / 2);
         return o;
       };
-      // Every pair moves to new operand panels at about the same time, so
-      // the first K blocks of a unit would all miss the L2 at once: the L2
-      // is asked for them kPrefetchAhead K blocks before the current unit
-      // ends.
-      constexpr int kPrefetchAhead = 16, kPrefetchBlocks = 8;
       for (long long n = 0; ok && n < n_items; ++n) {
         const Src cur = source(n);
         const CUtensorMap* amap = cur.amap;
         const CUtensorMap* bmap = cur.bmap;
         const int ax = cur.ax, ay = cur.ay, bx = cur.bx, by = cur.by;
-        const int pf_at = n + 1 < n_items ? max(0, p.k_blocks - kPrefetchAhead) : -1;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (kb == pf_at) {
-            const Src nx = source(n + 1);
-            for (int j = 0; j < kPrefetchBlocks && j < p.k_blocks; ++j) {
-              ptx::tma_prefetch_2d(nx.amap, nx.ax + j * kBK, nx.ay);
-#pragma unroll
-              for (int q = 0; q < BN / 128; ++q) ptx::tma_prefetch_2d(nx.bmap, nx.bx + q * 64, nx.by + j * kBK);
-            }
-          }
           if (!wait_one(empty(s), ph ^ 1u, p, 0)) {
             ok = false;
             break;

@@ -215,31 +215,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
           else
             bx[q] = tn * BN + qc;
         }
-        // the next item's first K blocks are asked of the L2 kPrefetchAhead
-        // K blocks before this one ends (every pair moves to new panels at
-        // about the same time)
-        constexpr int kPrefetchAhead = 16, kPrefetchBlocks = 8;
-        WorkItem nw;
-        const bool has_next =
-            work_item(p.num_units, p.split_tiles, p.split_pieces, nclusters, p.k_blocks, cluster, n + 1, nw);
-        const int pf_at = has_next ? max(w.k0, w.k1 - kPrefetchAhead) : -1;
         for (int kb = w.k0; kb < w.k1; ++kb) {
-          if (kb == pf_at) {
-            int ntm, ntn;
-            unit_coords(p, nw.unit, ntm, ntn);
-            const int nay = ntm * (2 * kBM) + static_cast<int>(rank) * kBM;
-            for (int j = nw.k0; j < nw.k1 && j < nw.k0 + kPrefetchBlocks; ++j) {
-              ptx::tma_prefetch_2d(&p.tmap_a, j * kBK, nay);
-#pragma unroll
-              for (int q = 0; q < BN / 128; ++q) {
-                const int qc = static_cast<int>(rank) * HALF + q * 64;
-                const int nbx = p.epi == kEpiSwiglu
-                                    ? (qc < HALF ? ntn * HALF + qc : p.n_out + ntn * HALF + (qc - HALF))
-                                    : ntn * BN + qc;
-                ptx::tma_prefetch_2d(&p.tmap_b, nbx, j * kBK);
-              }
-            }
-          }
           if (!wait_one(empty(s), ph ^ 1u, p, 0)) {
             ok = false;
             break;

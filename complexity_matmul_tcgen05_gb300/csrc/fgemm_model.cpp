@@ -111,9 +111,12 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   m.eff_strassen[1][0] = rate(76.5);
   m.eff_strassen[1][1] = rate(105.8);
   // one level on CTA pairs, summed operands streamed through HBM: the rate
-  // of its product kernel (executed MACs)
-  m.eff_strassen_pair[0] = rate(675.0);   // 256 x 128
-  m.eff_strassen_pair[1] = rate(675.0);   // 256 x 256
+  // of its product kernel (executed MACs) under which the model predicts the
+  // measured times (16384^3: 5.34 ms at 256 x 256 and 7.5 ms at 256 x 128,
+  // against 4.80 ms classical, sustained clocks, scaled to the classical
+  // rate above)
+  m.eff_strassen_pair[0] = rate(1121.0);  // 256 x 128
+  m.eff_strassen_pair[1] = rate(1620.0);  // 256 x 256
   // launch: back-to-back calls of a one-kernel product; fill: the first
   // MMA about 1.5 us after the start, the last 256 x 256 tile's epilogue
   // about 5 us after the last MMA (timestamps of an instrumented build)
