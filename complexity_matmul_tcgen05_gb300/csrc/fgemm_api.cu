@@ -401,24 +401,29 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
       last_of[blk] = pr;
     }
   }
-  // first and last contribution to each block, and where each output is complete
+  // where each output is complete (fin: the block, or for SwiGLU the block
+  // row, whose value is known once this product is in), the first
+  // contribution to each block (stored, not added) and the contribution
+  // that completes a block's output (kTermLast: kept out of the partial, the
+  // output is finished from the partial and the accumulator).  For SwiGLU a
+  // block's last contribution can come before its row is complete (C12's
+  // M5 before the gate's M7): it is folded like any other.
+  const bool swiglu = p.epi == FGEMM_EPI_SWIGLU;
   for (int pr = 0; pr < np; ++pr) {
     fgemm::LcmaProduct& P = L.prod[pr];
-    for (int t = 0; t < P.nc; ++t) {
-      const int blk = P.c[t] & fgemm::kTermIndexMask;
-      if (first_of[blk] == pr) P.c[t] |= fgemm::kTermFirst;
-      if (last_of[blk] == pr) P.c[t] |= fgemm::kTermLast;
-    }
     P.fin = 0;
     P.groups = 0;
     for (int b = 0; b < 4; ++b)
-      if (p.epi != FGEMM_EPI_SWIGLU && last_of[b] == pr) P.fin |= static_cast<uint8_t>(1u << b);
+      if (!swiglu && last_of[b] == pr) P.fin |= static_cast<uint8_t>(1u << b);
     for (int sr = 0; sr < 2; ++sr)
-      if (p.epi == FGEMM_EPI_SWIGLU && std::max(last_of[2 * sr], last_of[2 * sr + 1]) == pr)
+      if (swiglu && std::max(last_of[2 * sr], last_of[2 * sr + 1]) == pr)
         P.fin |= static_cast<uint8_t>(1u << sr);
     for (int t = 0; t < P.nc; ++t) {
       const int blk = P.c[t] & fgemm::kTermIndexMask;
-      P.groups |= static_cast<uint8_t>(1u << (p.epi == FGEMM_EPI_SWIGLU ? blk >> 1 : blk));
+      const int group = swiglu ? blk >> 1 : blk;
+      if (first_of[blk] == pr) P.c[t] |= fgemm::kTermFirst;
+      if (last_of[blk] == pr && ((P.fin >> group) & 1u)) P.c[t] |= fgemm::kTermLast;
+      P.groups |= static_cast<uint8_t>(1u << group);
     }
   }
   for (int g = 0; g < 4; ++g) {

@@ -91,6 +91,41 @@ def test_exact_ternary_lcma_cta_pair(M, N, K, tile, algo, dtype):
     assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
 
 
+# Enough output positions for whole waves on the pairs (the positions every
+# pair runs through all seven products, folding and finishing them itself)
+# besides a partial last wave: 4096 x 5120 has 8 x 10 positions of 256 x 256
+# in its 2048 x 2560 blocks (SwiGLU: 8 x 5), 8 x 20 at tile 128.
+@pytest.mark.parametrize("algo", ["strassen1", "winograd1"])
+@pytest.mark.parametrize("tile", [256, 128])
+@pytest.mark.parametrize("epilogue,alpha", [("none", 1.0), ("scale_bias", 0.75), ("silu", 1.25),
+                                            ("swiglu", 1.0)])
+def test_lcma_cta_pair_whole_positions_every_entry(algo, tile, epilogue, alpha):
+    M, N, K = 4096, 5120 if epilogue != "swiglu" else 10240, 128
+    A = inputs.matrix(M, K, "uniform", "bf16", 72, DEV)
+    B = inputs.matrix(K, N, "uniform", "bf16", 73, DEV)
+    bias = inputs.matrix(1, N, "normal_0.02", "bf16", 74, DEV)[0] if epilogue != "none" else None
+    _full_check(A, B, algo, "bf16", epilogue, alpha, bias, tile, 1, tile_m=256)
+
+
+@pytest.mark.parametrize("algo", ["strassen1", "winograd1"])
+@pytest.mark.parametrize("epilogue", ["scale_bias", "swiglu"])
+def test_exact_ternary_lcma_cta_pair_whole_positions(algo, epilogue):
+    M, N, K = 4096, 5120 if epilogue != "swiglu" else 10240, 384
+    A, B, bias = _ternary(M, N, K, "bf16", seed=75)
+    C = run(A, B, algo=algo, epilogue=epilogue, bias=bias, tile_n=256, tile_m=256)
+    if epilogue == "scale_bias":
+        assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, "bf16"))
+    else:
+        # gate and up are exact integers, so silu(gate) * up is the classical
+        # kernel's, evaluated by the same fp32 operations: the same bits; and
+        # each entry within the per-entry rule of the oracle's
+        C0 = run(A, B, algo="classical", epilogue="swiglu", bias=bias, tile_n=256, tile_m=256)
+        assert torch.equal(C.view(torch.int16), C0.view(torch.int16))
+        Av, Bv, bv = values(A), values(B), values(bias)
+        _act_entries_ok(values(C), "swiglu", oracle.gemm(Av, Bv), oracle.gemm(np.abs(Av), np.abs(Bv)), K,
+                        1.0, bv, "bf16")
+
+
 @pytest.mark.parametrize("algo", ["strassen1", "winograd1"])
 def test_lcma_cta_pair_deterministic_and_graph_replay(algo):
     """Positions shared by two pairs are summed in pair order: two launches
