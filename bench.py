@@ -208,7 +208,7 @@ def roofline_bound(M, N, K, n_out, bias_elems, tflops, gbs):
 KERNEL_SOURCES = ("fgemm_kernel.cuh", "fgemm_kernel_pair.cuh", "fgemm_ptx.cuh",
                   "fgemm_internal.h", "fgemm_kern_classical.cu", "fgemm_kern_pair.cu",
                   "fgemm_kern_strassen1.cu", "fgemm_kern_strassen2.cu", "fgemm_kern_winograd1.cu",
-                  "fgemm_kern_skinny.cu")
+                  "fgemm_kern_skinny.cu", "fgemm_kern_lcma.cu")
 
 
 def kernel_source_hash():
@@ -323,8 +323,10 @@ def run_reference(args, rank, world):
 
 
 def launches_per_call(algo, tile_m):
-    """Kernels of this library one fgemm_matmul_ex call launches."""
-    return 1
+    """Kernels of this library one fgemm_matmul_ex call launches: two for one
+    Strassen-like level on CTA pairs (the operand-sum pre-pass and the
+    product kernel), one otherwise."""
+    return 2 if algo in ("strassen1", "winograd1") and tile_m == 256 else 1
 
 
 def time_calls(fn, n, stream):
@@ -344,23 +346,38 @@ def time_calls(fn, n, stream):
     return statistics.mean(a.elapsed_time(b) for a, b in ev), t0.elapsed_time(t1)
 
 
-def time_form(A, B, C, bias, epi, algo, handle, stream, target_ms=400.0, max_calls=50):
-    """One LCMA or classical form on the workload: the model's best tile of
-    that form, timed over enough calls for about target_ms (at least 3)."""
+def time_forms(A, B, C, bias, epi, algos, handle, stream, target_ms=1500.0, max_rounds=60):
+    """The given forms on the same inputs, each with the model's best tile of
+    that form, timed round-robin: every round runs each form once (CUDA
+    events around each call), so the forms see the same clocks and power
+    state; rounds continue for about target_ms.  Returns {algo: (median ms,
+    calls)}."""
     from complexity_matmul_tcgen05_gb300 import fgemm
 
-    def call(i):
+    def call(algo):
         fgemm.matmul(A, B, out=C, epilogue=epi, bias=bias, algo=algo, handle=handle)
 
-    call(0)
-    call(1)
+    for algo in algos:
+        call(algo)
+        call(algo)
     torch.cuda.synchronize()
-    one, _ = time_calls(call, 1, stream)
-    n = int(max(3, min(max_calls, math.ceil(target_ms / max(one, 1e-3)))))
-    mean_ms, _ = time_calls(call, n, stream)
+    times = {a: [] for a in algos}
+    elapsed = 0.0
+    rounds = 0
+    while rounds < 3 or (elapsed < target_ms and rounds < max_rounds):
+        for algo in algos:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(algo)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            times[algo].append(ms)
+            elapsed += ms
+        rounds += 1
     if handle.get_error() != fgemm.OK:
-        raise SystemExit(f"device error timing {algo}: {handle.last_message()}")
-    return mean_ms, n
+        raise SystemExit(f"device error timing {algos}: {handle.last_message()}")
+    return {a: (statistics.median(t), len(t)) for a, t in times.items()}
 
 
 def run_fgemm(args, rank, world):
@@ -439,6 +456,7 @@ def run_fgemm(args, rank, world):
     forms = {}
     if rank == 0 and not args.no_forms:
         w = inputs_mod().WORKLOADS.get(args.workload, {})
+        legal, tiles = [], {}
         for form in ("classical", "strassen1", "strassen2", "winograd1"):
             if form not in w.get("algos", ()) and not (form == "classical"):
                 continue
@@ -446,14 +464,28 @@ def run_fgemm(args, rank, world):
                               fgemm.make_epilogue(epi, 1.0, 16 if bias0 is not None else None),
                               form) != fgemm.OK:
                 continue
-            f_algo, f_tm, f_tn, _ = handle.plan(M, N, K, fgemm._dtype_code(A0.dtype),
-                                                fgemm.make_epilogue(epi), algo=form)
-            ms, n = time_form(As[0], Bs[0], Cs[0], biases[0], epi, form, handle, stream)
-            eff = flops / (ms * 1e-3) / 1e12
-            executed = eff * (7.0 / 8.0) ** depth[form]
-            forms[form] = {"tile_m": f_tm, "tile_n": f_tn, "ms_per_call": ms, "calls": n,
-                           "effective_tflops": eff, "executed_tflops": executed,
-                           "executed_frac_of_peak": executed / peak if peak else None}
+            _, f_tm, f_tn, f_us = handle.plan(M, N, K, fgemm._dtype_code(A0.dtype),
+                                              fgemm.make_epilogue(epi), algo=form)
+            legal.append(form)
+            tiles[form] = (f_tm, f_tn, f_us)
+        # forms within a few times of the fastest prediction share the rounds;
+        # much slower ones (two Strassen levels on one-CTA tiles) get their own
+        fast = min(tiles[f][2] for f in legal) if legal else 0.0
+        groups = [[f for f in legal if tiles[f][2] <= 3.0 * fast],
+                  [f for f in legal if tiles[f][2] > 3.0 * fast]]
+        for g in groups:
+            if not g:
+                continue
+            res = time_forms(As[0], Bs[0], Cs[0], biases[0], epi, g, handle, stream,
+                             target_ms=1500.0 if len(g) > 1 else 400.0)
+            for form, (ms, n) in res.items():
+                eff = flops / (ms * 1e-3) / 1e12
+                executed = eff * (7.0 / 8.0) ** depth[form]
+                forms[form] = {"tile_m": tiles[form][0], "tile_n": tiles[form][1],
+                               "ms_per_call": ms, "calls": n, "predicted_ms": tiles[form][2] / 1e3,
+                               "effective_tflops": eff, "executed_tflops": executed,
+                               "executed_frac_of_peak": executed / peak if peak else None,
+                               "timing": "median of per-call CUDA events, forms round-robin"}
         if "classical" in forms:
             for f, d in forms.items():
                 d["vs_classical"] = d["effective_tflops"] / forms["classical"]["effective_tflops"]
