@@ -437,9 +437,12 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   const long long positions = p.num_units;
   L.units = positions * np;
   const int clusters = static_cast<int>(std::min<long long>(fit, L.units));
-  // the positions of the partial last wave run as separate product units
+  // the positions of the partial last wave run as separate product units;
+  // every CTA keeps the partials of each of its whole positions
   const long long tail_positions = positions % clusters;
-  const size_t slot_bytes = static_cast<size_t>(2) * clusters * fgemm::lcma_slot_floats(bn) * sizeof(float);
+  const long long whole = positions / clusters;
+  const size_t slot_bytes = static_cast<size_t>(2) * clusters * static_cast<size_t>(std::max<long long>(whole, 1)) *
+                            fgemm::lcma_slot_floats(bn) * sizeof(float);
   const size_t tail_bytes =
       static_cast<size_t>(tail_positions) * np * 2 * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float);
   const size_t ta_elems = static_cast<size_t>(ntA) * p.sub_m * p.sub_k;

@@ -258,8 +258,8 @@ inline size_t lcma_slot_floats(int bn) { return static_cast<size_t>(4) * 128 * s
 cudaError_t launch_lcma_form(const LcmaFormParams& f, int num_sms, cudaStream_t stream);
 
 // The product kernel for one Strassen-like level on `clusters` CTA pairs
-// (bn = 128 or 256).  p.k.workspace holds 2 * clusters * lcma_slot_floats
-// partials; the T = positions mod clusters positions of the partial last
+// (bn = 128 or 256).  p.k.workspace holds 2 * clusters * W * lcma_slot_floats
+// partials (W = positions / clusters whole positions per pair); the T = positions mod clusters positions of the partial last
 // wave run as 7 T separate product units, whose accumulators (128 x bn fp32
 // per unit and CTA) go to p.k.split_ws, with 32 counters per such position
 // (4 output groups x 2 CTAs x 4 epilogue warps) in p.k.split_ctr tagged with

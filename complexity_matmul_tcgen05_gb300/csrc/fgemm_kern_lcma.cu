@@ -51,57 +51,61 @@ __device__ __forceinline__ const uint4* form_src(const LcmaFormJob& J, int q, in
   return reinterpret_cast<const uint4*>(base);
 }
 
-// One warp per row and 32 column groups of 8 elements (16 bytes) per warp:
-// the four blocks' 16 bytes are loaded once, every temporary's 16 bytes
-// formed and stored.  blockIdx.z selects the matrix (A or B).  The source
-// blocks are read through the read-only path and the temporaries written
-// once; the sums of a row's group are independent of every other group.
+// Forms every temporary of job J at rows r0 and r1 (r1 may lie past the
+// last row: then only r0) for the 16-byte column group c8: the source
+// blocks' 16 bytes are loaded once (eight loads in flight), each temporary's
+// 16 bytes formed in fp32 (sum of the exact 16-bit values, one RNE rounding)
+// and stored.  The sums of one group are independent of every other group.
+__device__ __forceinline__ void form_rows(const LcmaFormJob& J, int is_bf16, int r0, int r1, int c8) {
+  const long long plane = static_cast<long long>(J.rows) * J.cols;
+  uint4 raw[2][4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = h == 0 ? r0 : r1;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      raw[h][q] = (r < J.rows && ((J.block_mask >> q) & 1u)) ? __ldg(form_src(J, q, r) + c8)
+                                                             : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = h == 0 ? r0 : r1;
+    if (r >= J.rows) break;
+    uint16_t* dst = J.dst + static_cast<long long>(r) * J.cols + c8 * 8;
+#pragma unroll 1
+    for (int t = 0; t < J.ntemp; ++t) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cf = J.coef[t][q];
+        if (cf != 0) {
+          float f[8];
+          unpack8(raw[h][q], f, is_bf16);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] += cf > 0 ? f[i] : -f[i];
+        }
+      }
+      *reinterpret_cast<uint4*>(dst + t * plane) =
+          make_uint4(pack2(acc[0], acc[1], is_bf16), pack2(acc[2], acc[3], is_bf16),
+                     pack2(acc[4], acc[5], is_bf16), pack2(acc[6], acc[7], is_bf16));
+    }
+  }
+}
+
+// The pre-pass as its own launch: one warp per pair of rows and 32 column
+// groups of 8 elements (16 bytes) per warp; blockIdx.z selects the matrix
+// (A or B).
 __global__ void __launch_bounds__(256) lcma_form_kernel(const __grid_constant__ LcmaFormParams P) {
   const LcmaFormJob& J = P.job[blockIdx.z];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cols8 = J.cols >> 3;
   const int c8 = blockIdx.x * 32 + lane;
   if (J.ntemp == 0 || c8 >= cols8) return;
-  const long long plane = static_cast<long long>(J.rows) * J.cols;
-  // two rows per iteration: eight 16-byte loads in flight per thread
   const int step = gridDim.y * 8;
 #pragma unroll 1
-  for (int r0 = blockIdx.y * 8 + warp; r0 < J.rows; r0 += 2 * step) {
-    uint4 raw[2][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = r0 + h * step;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        raw[h][q] = (r < J.rows && ((J.block_mask >> q) & 1u)) ? __ldg(form_src(J, q, r) + c8)
-                                                               : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = r0 + h * step;
-      if (r >= J.rows) break;
-      uint16_t* dst = J.dst + static_cast<long long>(r) * J.cols + c8 * 8;
-#pragma unroll 1
-      for (int t = 0; t < J.ntemp; ++t) {
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int cf = J.coef[t][q];
-          if (cf != 0) {
-            float f[8];
-            unpack8(raw[h][q], f, P.is_bf16);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] += cf > 0 ? f[i] : -f[i];
-          }
-        }
-        *reinterpret_cast<uint4*>(dst + t * plane) =
-            make_uint4(pack2(acc[0], acc[1], P.is_bf16), pack2(acc[2], acc[3], P.is_bf16),
-                       pack2(acc[4], acc[5], P.is_bf16), pack2(acc[6], acc[7], P.is_bf16));
-      }
-    }
-  }
+  for (int r0 = blockIdx.y * 8 + warp; r0 < J.rows; r0 += 2 * step) form_rows(J, P.is_bf16, r0, r0 + step, c8);
 }
 
 cudaError_t launch_lcma_form(const LcmaFormParams& f, int num_sms, cudaStream_t stream) {
@@ -141,10 +145,13 @@ struct LcmaCfg {
 
 // The schedule.  With P pairs and `positions` output positions (256 x BN
 // tiles of the half-size block space, in rasterised order), the first
-// W = floor(positions / P) waves are whole positions: pair c runs positions
-// c, c + P, c + 2P, ..., each through products 0 .. 6 in order, so that at
-// any moment the pairs work on neighbouring positions and on the same
-// product and share its operand panels in the L2, as a classical wave does.
+// W = floor(positions / P) waves are whole positions: pair c owns positions
+// c, c + P, c + 2P, ... and runs them product by product, product 0 for all
+// of them, then product 1, ...  At any moment the pairs work on the same
+// product and on neighbouring positions, and consecutive waves of one
+// product reuse its operand panels in the L2: each product is run like a
+// classical product of its two operands.  Every position still sees its
+// products in order, so its fold adds them in product order.
 // The T = positions - W P positions of the partial last wave are cut into
 // their 7 T units (product, position), product-major (unit t: product
 // t / T, position W P + t mod T), shared out in equal contiguous ranges, one
@@ -153,6 +160,7 @@ struct LcmaCfg {
 struct LcmaItem {
   long long pos;   // output position (unit_coords order)
   int pr;          // product
+  int slot;        // whole position: its index among the pair's whole positions
   long long tail;  // tail unit index, or -1 for a product of a whole position
 };
 
@@ -173,10 +181,12 @@ struct LcmaSchedule {
   __device__ LcmaItem item(long long n, int np, int pairs, int c) const {
     LcmaItem it;
     if (n < whole * np) {
-      it.pos = c + (n / np) * pairs;
-      it.pr = static_cast<int>(n % np);
+      it.slot = static_cast<int>(n % whole);
+      it.pos = c + it.slot * pairs;
+      it.pr = static_cast<int>(n / whole);
       it.tail = -1;
     } else {
+      it.slot = -1;
       it.tail = tlo + (n - whole * np);
       it.pr = static_cast<int>(it.tail / tail_n);
       it.pos = tail0 + it.tail % tail_n;
@@ -185,16 +195,18 @@ struct LcmaSchedule {
   }
 };
 
-// fp32 tiles in global memory (a CTA's partial of one output block, or the
-// accumulator of a tail unit): 128 rows x BN, laid out [32-column chunk]
-// [column quad: 8][row: 128][4], so that a warp's 16-byte accesses to one
-// (chunk, quad) cover 512 contiguous bytes.  These return the chunk's base;
-// row r's quad q is at index q * 128 + r.
+// fp32 tiles in global memory (a CTA's partial of one output block of one
+// of its whole positions, or the accumulator of a tail unit): 128 rows x BN,
+// laid out [32-column chunk][column quad: 8][row: 128][4], so that a warp's
+// 16-byte accesses to one (chunk, quad) cover 512 contiguous bytes.  These
+// return the chunk's base; row r's quad q is at index q * 128 + r.  A CTA's
+// partials: `whole` slots (its whole positions) of the four blocks.
 template <int BN>
-__device__ __forceinline__ float4* lcma_part(float* ws, int cta, int blk, int c) {
+__device__ __forceinline__ float4* lcma_part(float* ws, long long whole, int cta, int slot, int blk, int c) {
   using LC = LcmaCfg<BN>;
-  return reinterpret_cast<float4*>(ws + static_cast<size_t>(cta) * (LC::kBlocks * kBM * BN) +
-                                   (static_cast<size_t>(blk) * LC::kChunks + c) * (kBM * 32));
+  return reinterpret_cast<float4*>(
+      ws + ((static_cast<size_t>(cta) * whole + slot) * LC::kBlocks + blk) * (kBM * BN) +
+      static_cast<size_t>(c) * (kBM * 32));
 }
 
 template <int BN>
@@ -491,7 +503,9 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
         for (int t = 0; t < nc; ++t) {
           const uint8_t code = P.c[t];
           if (code & kTermLast) continue;
-          lcma_put_row(lcma_part<BN>(p.workspace, static_cast<int>(blockIdx.x), code & kTermIndexMask, c), r, ar,
+          lcma_put_row(lcma_part<BN>(p.workspace, sched.whole, static_cast<int>(blockIdx.x), it.slot,
+                                     code & kTermIndexMask, c),
+                       r, ar,
                        (code & kTermNeg) ? -1.0f : 1.0f, !(code & kTermFirst));
         }
         if (!P.fin) continue;
@@ -507,7 +521,9 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
             first = (P.c[t] & kTermFirst) != 0;
             sg = (P.c[t] & kTermNeg) ? -1.0f : 1.0f;
           }
-          if (!first) lcma_load_row(lcma_part<BN>(p.workspace, static_cast<int>(blockIdx.x), blk, c), r, v, false, 1.0f);
+          if (!first)
+            lcma_load_row(lcma_part<BN>(p.workspace, sched.whole, static_cast<int>(blockIdx.x), it.slot, blk, c),
+                          r, v, false, 1.0f);
           if (fed) {
             uint32_t x[32];
             ptx::tmem_ld_32x32b_x32(tbase + c * 32, x);
