@@ -132,6 +132,8 @@ struct fgemm_handle_s {
   size_t split_ctr_count = 0;
   unsigned int split_gen = 0;         // generation of the last split launch
   int split_mode = 1;                 // 0 never, 1 auto, 2 whenever possible
+  int lcma_formation = 0;             // 0 auto, 1 pre-pass launch, 2 inside the product kernel
+  unsigned int* form_ctr = nullptr;   // band counters of the in-kernel formation (3 words)
   unsigned long long spin_ns = 1000000000ull;
   fgemm_device_model_t model{};
   std::unordered_map<PlanKey, Plan, PlanKeyHash> plans;
@@ -364,7 +366,7 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   std::memset(&L, 0, sizeof(L));
   LcmaFormParams F;
   std::memset(&F, 0, sizeof(F));
-  const int np = 7;
+  const int np = fgemm::kLcmaProducts;
   // the distinct summed operands of each side (a single positive term is a
   // raw block of A or B, read in place)
   auto operand = [&](int n, const uint8_t* codes, fgemm::LcmaFormJob& J, uint8_t* is_temp,
@@ -374,14 +376,14 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
       *idx = codes[0] & fgemm::kTermIndexMask;
       return;
     }
-    int8_t coef[16] = {0};
+    int8_t coef[4] = {0};
     for (int i = 0; i < n; ++i)
       coef[codes[i] & fgemm::kTermIndexMask] += (codes[i] & fgemm::kTermNeg) ? -1 : 1;
     int t = 0;
     while (t < J.ntemp && std::memcmp(J.coef[t], coef, sizeof(coef)) != 0) ++t;
     if (t == J.ntemp) {
       std::memcpy(J.coef[t], coef, sizeof(coef));
-      for (int q = 0; q < 16; ++q)
+      for (int q = 0; q < 4; ++q)
         if (coef[q] != 0) J.block_mask |= 1u << q;
       ++J.ntemp;
     }
@@ -489,8 +491,35 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   F.job[1].dst = TB;
   F.job[1].rows = p.sub_k;
   F.job[1].cols = p.sub_n;
-  cudaError_t e = fgemm::launch_lcma_form(F, h->num_sms, h->stream);
-  if (e != cudaSuccess) return cuda_fail(h, e, "operand-sum pre-pass launch");
+  // Where the operands are formed: by the pre-pass launch, or inside the
+  // product kernel while the scheme's leading products that read only blocks
+  // of A and B run (their waves must cover the formation: auto asks for at
+  // least kFusedMinWaves of them).
+  int lead = 0;
+  while (lead < np && !L.prod[lead].a_temp && !L.prod[lead].b_temp) ++lead;
+  constexpr long long kFusedMinWaves = 16;
+  const bool whole_bands = F.job[0].rows % fgemm::kFormRows == 0 && F.job[1].rows % fgemm::kFormRows == 0;
+  const bool fused = lead > 0 && whole_bands &&
+                     (h->lcma_formation == 2 || (h->lcma_formation == 0 && lead * whole >= kFusedMinWaves));
+  cudaError_t e = cudaSuccess;
+  if (fused) {
+    if (!h->form_ctr) {
+      e = cudaMalloc(&h->form_ctr, 4 * sizeof(unsigned int));
+      if (e != cudaSuccess) {
+        h->form_ctr = nullptr;
+        return cuda_fail(h, e, "cudaMalloc(formation counters)");
+      }
+    }
+    e = cudaMemsetAsync(h->form_ctr, 0, 4 * sizeof(unsigned int), h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync(formation counters)");
+    L.form = F;
+    L.form_ctr = h->form_ctr;
+    for (int j = 0; j < 2; ++j)
+      L.form_tasks[j] = F.job[j].ntemp > 0 ? F.job[j].rows / fgemm::kFormRows : 0;
+  } else {
+    e = fgemm::launch_lcma_form(F, h->num_sms, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "operand-sum pre-pass launch");
+  }
   e = fgemm::launch_lcma_pair(bn, L, clusters, h->stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "Strassen pair kernel launch");
   return FGEMM_OK;
@@ -647,6 +676,7 @@ fgemm_status_t fgemm_destroy(fgemm_handle_t h) {
   cudaStreamSynchronize(h->stream);
   if (h->workspace) cudaFree(h->workspace);
   if (h->split_ctr) cudaFree(h->split_ctr);
+  if (h->form_ctr) cudaFree(h->form_ctr);
   if (h->mx_buf) cudaFree(h->mx_buf);
   if (h->d_err) cudaFree(h->d_err);
   delete h;
@@ -657,6 +687,13 @@ fgemm_status_t fgemm_set_split_mode(fgemm_handle_t h, int32_t mode) {
   if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
   if (mode < 0 || mode > 2) return set_msg(h, FGEMM_ERR_INVALID_ARG, "split mode must be 0, 1 or 2");
   h->split_mode = mode;
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_set_lcma_formation(fgemm_handle_t h, int32_t mode) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  if (mode < 0 || mode > 2) return set_msg(h, FGEMM_ERR_INVALID_ARG, "formation mode must be 0, 1 or 2");
+  h->lcma_formation = mode;
   return FGEMM_OK;
 }
 

@@ -222,19 +222,12 @@ struct LcmaProduct {
   uint8_t groups;  // output groups it feeds (bit g: block g, or for SwiGLU block row g)
 };
 
-struct LcmaParams {
-  KernelParams k;        // tmap_a / tmap_b map A and B; k.workspace holds the partial tiles
-  CUtensorMap tmap_ta;   // A temporaries: inner sub_k, outer ntemp_a * sub_m, box {64, 128}
-  CUtensorMap tmap_tb;   // B temporaries: inner sub_n, outer ntemp_b * sub_k, box {64, 64}
-  long long units;       // output positions * num_products (informational)
-  LcmaProduct prod[kMaxProducts];
-  uint8_t group_pieces[4];  // products feeding each output group
-};
-
-// One matrix of the pre-pass: the `rows` x `cols` blocks of src (block q at
-// block row q >> depth, block column q & (2^depth - 1)) are combined into
+// One matrix of the operand formation: the four `rows` x `cols` blocks of
+// src (block q at block row q >> 1, block column q & 1) are combined into
 // ntemp temporaries, temporary t = sum_q coef[t][q] * block_q (coef in
 // {-1, 0, 1}), stored one after another, each rows x cols with pitch cols.
+constexpr int kLcmaProducts = 7;  // one level: seven block products
+constexpr int kLcmaMaxTemps = 8;  // summed operands per side (Strassen 5, Winograd 4)
 struct LcmaFormJob {
   const uint16_t* src;
   long long ld;
@@ -242,12 +235,35 @@ struct LcmaFormJob {
   int rows, cols;
   int ntemp;
   uint32_t block_mask;  // blocks some temporary reads
-  int8_t coef[kMaxProducts][16];
+  int8_t coef[kLcmaMaxTemps][4];
 };
 
 struct LcmaFormParams {
   LcmaFormJob job[2];  // A and B
   int is_bf16;
+};
+
+// Rows of one matrix per formation task when the product kernel forms the
+// temporaries itself.
+constexpr int kFormRows = 8;
+
+struct LcmaParams {
+  KernelParams k;        // tmap_a / tmap_b map A and B; k.workspace holds the partial tiles
+  CUtensorMap tmap_ta;   // A temporaries: inner sub_k, outer ntemp_a * sub_m, box {64, 128}
+  CUtensorMap tmap_tb;   // B temporaries: inner sub_n, outer ntemp_b * sub_k, box {64, 64}
+  long long units;       // output positions * num_products (informational)
+  LcmaProduct prod[kLcmaProducts];
+  uint8_t group_pieces[4];  // products feeding each output group
+  // Temporaries formed inside the product kernel (form_tasks[0] +
+  // form_tasks[1] > 0; otherwise the pre-pass launch formed them): job j is
+  // cut into form_tasks[j] bands of kFormRows rows, claimed through
+  // form_ctr[0] by the CTAs' otherwise idle warps; form_ctr[1 + j] counts the
+  // bands of job j that are stored.  A producer issues the first load of a
+  // temporary of side j only once all of job j is stored.  The counters
+  // start at zero (the host clears them before the launch).
+  LcmaFormParams form;
+  unsigned int* form_ctr;
+  int form_tasks[2];
 };
 
 // Per-CTA partial tiles of the product kernel's whole positions: the four

@@ -51,25 +51,27 @@ __device__ __forceinline__ const uint4* form_src(const LcmaFormJob& J, int q, in
   return reinterpret_cast<const uint4*>(base);
 }
 
-// Forms every temporary of job J at rows r0 and r1 (r1 may lie past the
-// last row: then only r0) for the 16-byte column group c8: the source
-// blocks' 16 bytes are loaded once (eight loads in flight), each temporary's
-// 16 bytes formed in fp32 (sum of the exact 16-bit values, one RNE rounding)
-// and stored.  The sums of one group are independent of every other group.
-__device__ __forceinline__ void form_rows(const LcmaFormJob& J, int is_bf16, int r0, int r1, int c8) {
+// Forms every temporary of job J at the R rows r0, r0 + rstep, ... (rows
+// past the last are skipped) for the 16-byte column group c8: the source
+// blocks' 16 bytes are loaded once (4 R loads in flight), each temporary's
+// 16 bytes formed in fp32 (sum of the exact 16-bit values, one RNE
+// rounding) and stored.  The sums of one group are independent of every
+// other group.
+template <int R>
+__device__ __forceinline__ void form_rows(const LcmaFormJob& J, int is_bf16, int r0, int rstep, int c8) {
   const long long plane = static_cast<long long>(J.rows) * J.cols;
-  uint4 raw[2][4];
+  uint4 raw[R][4];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = h == 0 ? r0 : r1;
+  for (int h = 0; h < R; ++h) {
+    const int r = r0 + h * rstep;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       raw[h][q] = (r < J.rows && ((J.block_mask >> q) & 1u)) ? __ldg(form_src(J, q, r) + c8)
                                                              : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = h == 0 ? r0 : r1;
+  for (int h = 0; h < R; ++h) {
+    const int r = r0 + h * rstep;
     if (r >= J.rows) break;
     uint16_t* dst = J.dst + static_cast<long long>(r) * J.cols + c8 * 8;
 #pragma unroll 1
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(256) lcma_form_kernel(const __grid_constant__ 
   if (J.ntemp == 0 || c8 >= cols8) return;
   const int step = gridDim.y * 8;
 #pragma unroll 1
-  for (int r0 = blockIdx.y * 8 + warp; r0 < J.rows; r0 += 2 * step) form_rows(J, P.is_bf16, r0, r0 + step, c8);
+  for (int r0 = blockIdx.y * 8 + warp; r0 < J.rows; r0 += 2 * step) form_rows<2>(J, P.is_bf16, r0, step, c8);
 }
 
 cudaError_t launch_lcma_form(const LcmaFormParams& f, int num_sms, cudaStream_t stream) {
@@ -314,6 +316,60 @@ __device__ void lcma_finish_tail(const LcmaParams& L, long long tail_pos, long l
   }
 }
 
+// Operand formation inside the product kernel, by one warp: claims bands
+// of kFormRows rows (the jobs' row counts are multiples of it) of job 0
+// (A), then of job 1 (B), until none is left, forms each band's
+// temporaries over the full width (four rows in flight per lane) and counts
+// the band as stored.  The release: every lane's stores,
+// then its fences (async proxy, GPU scope), then the warp barrier, then lane
+// 0's increment.  A warp never waits for another CTA here, so every band a
+// running CTA has claimed is stored whatever else runs on the GPU.
+__device__ __forceinline__ void lcma_form_bands(const LcmaParams& L) {
+  const int lane = threadIdx.x & 31;
+  const int total = L.form_tasks[0] + L.form_tasks[1];
+#pragma unroll 1
+  while (true) {
+    int t = 0;
+    if (lane == 0) t = static_cast<int>(atomicAdd(L.form_ctr, 1u));
+    t = __shfl_sync(0xFFFFFFFFu, t, 0);
+    if (t >= total) break;
+    const int j = t < L.form_tasks[0] ? 0 : 1;
+    const LcmaFormJob& J = L.form.job[j];
+    const int r0 = (t - (j ? L.form_tasks[0] : 0)) * kFormRows;
+    const int r1 = r0 + kFormRows;  // the host asks for whole bands
+    const int cols8 = J.cols >> 3;
+#pragma unroll 1
+    for (int r = r0; r < r1; r += 4)
+#pragma unroll 1
+      for (int c8 = lane; c8 < cols8; c8 += 32) form_rows<4>(J, L.form.is_bf16, r, 1, c8);
+    ptx::fence_proxy_async_global();
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) atomicAdd(L.form_ctr + 1 + j, 1u);
+  }
+}
+
+// Bounded wait of a producer until every band of job j is stored (then its
+// later bulk-tensor loads see the temporaries).  Gives up when another role
+// latched an error, or latches a timeout of the operand-sum role.
+static __device__ __noinline__ bool lcma_wait_formed(const LcmaParams& L, int j) {
+  const KernelParams& p = L.k;
+  const unsigned int need = static_cast<unsigned int>(L.form_tasks[j]);
+  const unsigned int* ctr = L.form_ctr + 1 + j;
+  const uint64_t t0 = ptx::globaltimer();
+#pragma unroll 1
+  while (ptx::ld_acquire_gpu(ctr) < need) {
+    if (*reinterpret_cast<volatile unsigned int*>(p.err) != 0u) return false;
+    if (ptx::globaltimer() - t0 > p.spin_ns) {
+      atomicCAS(p.err, 0u, err_code(3));
+      return false;
+    }
+    __nanosleep(200);
+  }
+  ptx::fence_proxy_async_global();
+  return true;
+}
+
 template <int BN>
 __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_constant__ LcmaParams L) {
   using LC = LcmaCfg<BN>;
@@ -396,8 +452,20 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
         o.bx = (P.b_temp ? 0 : (P.b_idx & 1) * p.sub_n) + tn * BN + static_cast<int>(rank) * (BN / 2);
         return o;
       };
+      // sides whose temporaries this producer may read (the pre-pass formed
+      // them before the launch, or this kernel has finished forming them)
+      bool formed[2] = {L.form_tasks[0] == 0, L.form_tasks[1] == 0};
       for (long long n = 0; ok && n < n_items; ++n) {
         const Src cur = source(n);
+        for (int j = 0; j < 2; ++j) {
+          if (formed[j] || !(j == 0 ? cur.amap == &L.tmap_ta : cur.bmap == &L.tmap_tb)) continue;
+          if (!lcma_wait_formed(L, j)) {
+            ok = false;
+            break;
+          }
+          formed[j] = true;
+        }
+        if (!ok) break;
         const CUtensorMap* amap = cur.amap;
         const CUtensorMap* bmap = cur.bmap;
         const int ax = cur.ax, ay = cur.ay, bx = cur.bx, by = cur.by;
@@ -468,6 +536,9 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
       wait_bounded(drain, 0, p, err_code(1), false);
     }
     __syncwarp();
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------- operand formation (both CTAs)
+    if (L.form_tasks[0] + L.form_tasks[1] > 0) lcma_form_bands(L);
   } else if (warp >= 4) {
     // ------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 4;

@@ -129,6 +129,7 @@ def lib() -> ctypes.CDLL:
         L.fgemm_split_work_item.argtypes = [i64, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
         L.fgemm_split_work_item.restype = i32
         L.fgemm_set_split_mode.argtypes = [vp, i32]
+        L.fgemm_set_lcma_formation.argtypes = [vp, i32]
         L.fgemm_stream_k_work_item.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(i64)]
         L.fgemm_stream_k_work_item.restype = i32
         L.fgemm_small_m_grid.argtypes = [i64, i32, i32, ctypes.POINTER(i32)]
@@ -141,7 +142,7 @@ def lib() -> ctypes.CDLL:
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
                      "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout",
-                     "fgemm_set_split_mode", "fgemm_matmul_rms", "fgemm_matmul_mx",
+                     "fgemm_set_split_mode", "fgemm_set_lcma_formation", "fgemm_matmul_rms", "fgemm_matmul_mx",
                      "fgemm_mx_to_bf16", "fgemm_strassen_static_get_error",
                      "fgemm_strassen_static_selftest_timeout"):
             getattr(L, name).restype = st
@@ -150,6 +151,7 @@ def lib() -> ctypes.CDLL:
 
 
 SPLIT_MODES = {"off": 0, "auto": 1, "force": 2}
+FORMATION_MODES = {"auto": 0, "prepass": 1, "in_kernel": 2}
 
 
 def split_work_items(tiles: int, split_tiles: int, split_pieces: int, clusters: int,
@@ -246,6 +248,14 @@ class Handle:
         the default) or "force" (2, whenever possible)."""
         code = SPLIT_MODES[mode] if isinstance(mode, str) else int(mode)
         _check(lib().fgemm_set_split_mode(self._h, code), self._h)
+
+    def set_lcma_formation(self, mode):
+        """Where one-level Strassen-like launches on CTA pairs form their
+        summed operands: "auto" (0, the default), "prepass" (1, a separate
+        launch) or "in_kernel" (2, inside the product kernel while the
+        scheme's leading products that read only blocks of A and B run)."""
+        code = FORMATION_MODES[mode] if isinstance(mode, str) else int(mode)
+        _check(lib().fgemm_set_lcma_formation(self._h, code), self._h)
 
     def matmul_raw(self, M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, dtype: int,
                    epilogue: Epilogue | None = None, algo: str = "auto", tile_n: int = 0,

@@ -544,6 +544,20 @@ int32_t fgemm_stream_k_work_item(int64_t tiles, int32_t k_blocks, int32_t ctas, 
  */
 fgemm_status_t fgemm_set_split_mode(fgemm_handle_t h, int32_t mode);
 
+/*
+ * Where the handle's one-level Strassen-like launches on CTA pairs (tile_m
+ * 256) form their summed operands (FalconGEMM summary, "Methodology" item 3:
+ * the operand sums of the low-complexity scheme): 1 a streaming pre-pass
+ * launch before the product kernel; 2 inside the product kernel, by its two
+ * otherwise idle warps per CTA, while the scheme's leading products that
+ * read only blocks of A and B run (Winograd's A11 B11 and A12 B21; a scheme
+ * without such products, like Strassen's, always uses the pre-pass); 0 auto
+ * (the default): inside the product kernel when those products span at
+ * least 16 waves of the launch, else the pre-pass.  The result is the same
+ * bit for bit in every mode.  Returns FGEMM_ERR_INVALID_ARG for other modes.
+ */
+fgemm_status_t fgemm_set_lcma_formation(fgemm_handle_t h, int32_t mode);
+
 /* Copies the handle's current device model into *out. */
 fgemm_status_t fgemm_get_device_model(fgemm_handle_t h,
                                       fgemm_device_model_t* out);

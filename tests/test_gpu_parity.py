@@ -152,6 +152,80 @@ def test_lcma_cta_pair_deterministic_and_graph_replay(algo):
         assert torch.equal(C.view(torch.int16), C1.view(torch.int16))
 
 
+@pytest.fixture
+def formation():
+    """Sets the default handle's operand-formation mode for one test, then
+    restores auto."""
+    h = fgemm.default_handle()
+    yield h.set_lcma_formation
+    h.set_lcma_formation("auto")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K,tile", LCMA_PAIR_CASES)
+def test_exact_ternary_winograd_formed_in_kernel(M, N, K, tile, dtype, formation):
+    """Winograd's temporaries formed by the product kernel's own warps while
+    its first two products (A11 B11, A12 B21) run: RNE(exact C) bit for bit."""
+    formation("in_kernel")
+    A, B, bias = _ternary(M, N, K, dtype, seed=76)
+    C = run(A, B, algo="winograd1", epilogue="scale_bias", bias=bias, tile_n=tile, tile_m=256)
+    assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
+
+
+@pytest.mark.parametrize("algo", ["winograd1", "strassen1"])
+@pytest.mark.parametrize("M,N,K,tile,epilogue", [
+    (4096, 5120, 1024, 256, "none"),      # whole positions and a tail
+    (4096, 10240, 512, 256, "swiglu"),
+    (2048, 2048, 2048, 128, "silu"),      # tail units only
+    (1536, 768, 384, 128, "scale_bias"),
+])
+def test_lcma_formation_modes_give_the_same_bits(M, N, K, tile, epilogue, algo, formation):
+    """The temporaries hold the same values whoever forms them, so the
+    pre-pass and the in-kernel formation give the same C bit for bit
+    (Strassen's scheme has no leading product free of sums: it always uses
+    the pre-pass)."""
+    A = inputs.matrix(M, K, "uniform", "bf16", 77, DEV)
+    B = inputs.matrix(K, N, "uniform", "bf16", 78, DEV)
+    bias = inputs.matrix(1, N, "normal_0.02", "bf16", 79, DEV)[0] if epilogue != "none" else None
+    kw = dict(algo=algo, epilogue=epilogue, bias=bias, tile_n=tile, tile_m=256)
+    formation("prepass")
+    C1 = run(A, B, **kw)
+    formation("in_kernel")
+    C2 = run(A, B, **kw)
+    C3 = run(A, B, **kw)  # the band counters start from zero every launch
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+    assert torch.equal(C2.view(torch.int16), C3.view(torch.int16))
+
+
+def test_winograd_formed_in_kernel_graph_replay(formation):
+    """A captured launch with in-kernel formation replays with the same
+    result: the clearing of its band counters is part of the graph."""
+    formation("in_kernel")
+    M, N, K = 4096, 5120, 1024
+    A = inputs.matrix(M, K, "uniform", "bf16", 80, DEV)
+    B = inputs.matrix(K, N, "uniform", "bf16", 81, DEV)
+    kw = dict(algo="winograd1", tile_n=256, tile_m=256)
+    C1 = run(A, B, **kw)
+    C = torch.empty_like(C1)
+    fgemm.matmul(A, B, out=C, **kw)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fgemm.matmul(A, B, out=C, **kw)
+    for _ in range(3):
+        C.view(torch.int16).fill_(0x7F7B)
+        g.replay()
+        torch.cuda.synchronize()
+        assert fgemm.default_handle().get_error() == fgemm.OK
+        assert torch.equal(C.view(torch.int16), C1.view(torch.int16))
+    # the graph's B now changes: the replay forms the new temporaries
+    B2 = inputs.matrix(K, N, "uniform", "bf16", 82, DEV)
+    B.copy_(B2)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int16), run(A, B2, **kw).view(torch.int16))
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("M,N,K,tile", EXACT_PAIR_CASES)
 def test_exact_ternary_cta_pair(M, N, K, tile, dtype):
