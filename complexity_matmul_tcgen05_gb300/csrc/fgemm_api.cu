@@ -501,6 +501,13 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   const bool whole_bands = F.job[0].rows % fgemm::kFormRows == 0 && F.job[1].rows % fgemm::kFormRows == 0;
   const bool fused = lead > 0 && whole_bands &&
                      (h->lcma_formation == 2 || (h->lcma_formation == 0 && lead * whole >= kFusedMinWaves));
+  // A pair's tail units (positions of the partial last wave, one product
+  // each) run after its whole positions' first tail_at products, so that the
+  // combinations of their accumulators overlap the MMAs of the products that
+  // follow: first thing with the pre-pass, after two more products than the
+  // sum-free ones when this kernel forms the temporaries (then they are
+  // stored by the time the tail units read them).
+  L.tail_at = fused ? std::min(lead + 2, np) : 0;
   cudaError_t e = cudaSuccess;
   if (fused) {
     if (!h->form_ctr) {

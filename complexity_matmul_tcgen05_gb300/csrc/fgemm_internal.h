@@ -254,6 +254,7 @@ struct LcmaParams {
   long long units;       // output positions * num_products (informational)
   LcmaProduct prod[kLcmaProducts];
   uint8_t group_pieces[4];  // products feeding each output group
+  int tail_at;              // whole-position products a pair runs before its tail units
   // Temporaries formed inside the product kernel (form_tasks[0] +
   // form_tasks[1] > 0; otherwise the pre-pass launch formed them): job j is
   // cut into form_tasks[j] bands of kFormRows rows, claimed through

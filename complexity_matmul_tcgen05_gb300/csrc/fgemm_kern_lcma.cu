@@ -140,7 +140,13 @@ struct LcmaCfg {
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kBBytes;
   static constexpr int kChunks = BN / 32;
   static constexpr int kBlocks = 4;  // output blocks of one level
+  // The combination queue after the barriers: head, taken, epilogue warps
+  // done, then one word per job (a tail unit hands at most 4 groups x 4
+  // warps of combinations, and a pair has at most 7 tail units).
+  static constexpr int kQueueOff = 256;
+  static constexpr int kQueueCap = 128;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert(kQueueOff + 4 * (4 + kQueueCap) <= kBarBytes, "combination queue does not fit");
   static_assert(2 * BN <= kTmemCols, "two accumulator buffers must fit in TMEM");
   static_assert((2 * kStages + 5) * 8 + 4 <= kBarBytes, "barrier area too small");
 };
@@ -157,8 +163,13 @@ struct LcmaCfg {
 // The T = positions - W P positions of the partial last wave are cut into
 // their 7 T units (product, position), product-major (unit t: product
 // t / T, position W P + t mod T), shared out in equal contiguous ranges, one
-// per pair, after its whole positions.  A tail unit stores its accumulator;
-// the last of a position's seven units to finish combines them.
+// per pair.  A tail unit stores its accumulator; the last of a position's
+// seven units to finish combines them, a chain of dependent loads that is
+// long next to a unit's MMAs.  So a pair runs its tail units among its whole
+// positions, after the whole positions' first `tail_at` products: the
+// combinations then overlap the MMAs of the products that follow.  (With
+// the temporaries formed in this kernel, tail_at leaves time for them to be
+// stored first.)
 struct LcmaItem {
   long long pos;   // output position (unit_coords order)
   int pr;          // product
@@ -171,27 +182,31 @@ struct LcmaSchedule {
   long long tail0;   // W * P: the first tail position
   long long tail_n;  // T: tail positions
   long long tlo, thi;  // this pair's tail units [tlo, thi)
-  __device__ LcmaSchedule(long long positions, int pairs, int np, int c) {
+  long long head;    // whole-position items before the tail units: W * tail_at
+  __device__ LcmaSchedule(long long positions, int pairs, int np, int tail_at, int c) {
     whole = positions / pairs;
     tail0 = whole * pairs;
     tail_n = positions - tail0;
     const long long ut = tail_n * np;
     tlo = static_cast<long long>(c) * ut / pairs;
     thi = static_cast<long long>(c + 1) * ut / pairs;
+    head = whole * min(max(tail_at, 0), np);
   }
   __device__ long long items(int np) const { return whole * np + (thi - tlo); }
   __device__ LcmaItem item(long long n, int np, int pairs, int c) const {
     LcmaItem it;
-    if (n < whole * np) {
-      it.slot = static_cast<int>(n % whole);
-      it.pos = c + it.slot * pairs;
-      it.pr = static_cast<int>(n / whole);
-      it.tail = -1;
-    } else {
+    const long long nt = thi - tlo;
+    if (n >= head && n < head + nt) {
       it.slot = -1;
-      it.tail = tlo + (n - whole * np);
+      it.tail = tlo + (n - head);
       it.pr = static_cast<int>(it.tail / tail_n);
       it.pos = tail0 + it.tail % tail_n;
+    } else {
+      const long long w = n < head ? n : n - nt;  // index among the whole-position items
+      it.slot = static_cast<int>(w % whole);
+      it.pos = c + it.slot * pairs;
+      it.pr = static_cast<int>(w / whole);
+      it.tail = -1;
     }
     return it;
   }
@@ -370,6 +385,67 @@ static __device__ __noinline__ bool lcma_wait_formed(const LcmaParams& L, int j)
   return true;
 }
 
+// The combinations of tail positions, run by warps 2 and 3 (idle once the
+// operands are formed) so that the epilogue warps go on with the next
+// accumulator.  An epilogue warp that finds it has the last unit of an
+// output group appends a job (tail position, group, its warp index: the
+// 32 rows to combine) to the CTA's queue in shared memory; a helper claims
+// jobs in order and runs each.  The queue ends when all four epilogue
+// warps have said they are done and every appended job is taken.  A helper
+// may wait for its next job as long as the epilogue keeps finishing
+// accumulators (queue word 3 counts them): its bound restarts at each one.
+// It leaves on another role's error.
+template <int BN>
+__device__ __forceinline__ void lcma_tail_helper(const LcmaParams& L, volatile uint32_t* q,
+                                                 const LcmaSchedule& sched, uint32_t rank) {
+  using LC = LcmaCfg<BN>;
+  const KernelParams& p = L.k;
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  while (true) {
+    uint32_t i = 0, job = 0, quit = 0;
+    if (lane == 0) {
+      i = atomicAdd(const_cast<uint32_t*>(q + 1), 1u);
+      uint64_t t0 = ptx::globaltimer();
+      uint32_t beat = q[3];
+#pragma unroll 1
+      while (true) {
+        if (i < static_cast<uint32_t>(LC::kQueueCap)) {
+          job = q[4 + i];
+          if (job != 0u) break;
+        }
+        if (q[2] == 4u && i >= q[0]) {  // done flags first: then the head is final
+          quit = 1;
+          break;
+        }
+        if (*reinterpret_cast<volatile unsigned int*>(p.err) != 0u) {
+          quit = 1;
+          break;
+        }
+        const uint32_t b = q[3];
+        if (b != beat) {
+          beat = b;
+          t0 = ptx::globaltimer();
+        } else if (ptx::globaltimer() - t0 > p.spin_ns) {
+          atomicCAS(p.err, 0u, err_code(2));
+          quit = 1;
+          break;
+        }
+        __nanosleep(256);
+      }
+    }
+    quit = __shfl_sync(0xFFFFFFFFu, quit, 0);
+    job = __shfl_sync(0xFFFFFFFFu, job, 0);
+    if (quit) break;
+    __threadfence();  // the feeding units' stores, seen by the appending warp, are seen here
+    const long long tail_pos = static_cast<long long>((job & 0x7FFFFFFFu) >> 4);
+    int tm, tn;
+    unit_coords(p, static_cast<int>(sched.tail0 + tail_pos), tm, tn);
+    lcma_finish_tail<BN>(L, tail_pos, sched.tail_n, static_cast<int>((job >> 2) & 3u), tm, tn, rank,
+                         static_cast<int>(job & 3u));
+  }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_constant__ LcmaParams L) {
   using LC = LcmaCfg<BN>;
@@ -389,6 +465,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
   auto tfull = [&](uint32_t b) { return bar0 + 8u * (2 * S + b); };
   auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + 2 + b); };
   const uint32_t drain = bar0 + 8u * (2 * S + 4);
+  volatile uint32_t* queue = reinterpret_cast<volatile uint32_t*>(base_ptr + S * LC::kStageBytes + LC::kQueueOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -397,9 +474,10 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
   const int cluster = blockIdx.x >> 1;
   const int pairs = gridDim.x >> 1;
   const int np = p.num_products;
-  const LcmaSchedule sched(p.num_units, pairs, np, cluster);
+  const LcmaSchedule sched(p.num_units, pairs, np, L.tail_at, cluster);
   const long long n_items = sched.items(np);
 
+  if (threadIdx.x < 4 + LC::kQueueCap) queue[threadIdx.x] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full(s), 1);
@@ -539,6 +617,8 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------- operand formation (both CTAs)
     if (L.form_tasks[0] + L.form_tasks[1] > 0) lcma_form_bands(L);
+    // ------------------------------------------- tail combinations (both CTAs)
+    lcma_tail_helper<BN>(L, queue, sched, rank);
   } else if (warp >= 4) {
     // ------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 4;
@@ -626,6 +706,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty(buf), 0));
+      if (ew == 0 && lane == 0) queue[3] = static_cast<uint32_t>(n) + 1u;  // progress, for the helpers
       if (it.tail < 0) continue;
       // a tail unit: for every output group (block, or SwiGLU block row) it
       // feeds, the last of the group's feeding units to finish combines them
@@ -639,8 +720,21 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
             p, p.split_ctr + ((static_cast<size_t>(tail_pos) * 4 + g) * 2 + rank) * 4 + ew, L.group_pieces[g]);
         if (!last) continue;
         __threadfence();
-        lcma_finish_tail<BN>(L, tail_pos, sched.tail_n, g, tm, tn, rank, ew);
+        if (lane == 0) {
+          const uint32_t slot = atomicAdd(const_cast<uint32_t*>(queue), 1u);
+          if (slot < static_cast<uint32_t>(LC::kQueueCap))
+            queue[4 + slot] = 0x80000000u | (static_cast<uint32_t>(tail_pos) << 4) |
+                              (static_cast<uint32_t>(g) << 2) | static_cast<uint32_t>(ew);
+          else
+            atomicCAS(p.err, 0u, err_code(2));  // not reached: the host bounds the units per pair
+        }
+        __syncwarp();
       }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(const_cast<uint32_t*>(queue + 2), 1u);
     }
   }
 
