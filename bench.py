@@ -205,18 +205,34 @@ def roofline_bound(M, N, K, n_out, bias_elems, tflops, gbs):
     return alg_bytes, bool(tflops and gbs) and alg_bytes / (gbs * 1e9) > flops / (tflops * 1e12)
 
 
-KERNEL_SOURCES = ("fgemm_kernel.cuh", "fgemm_kernel_pair.cuh", "fgemm_ptx.cuh",
-                  "fgemm_internal.h", "fgemm_kern_classical.cu", "fgemm_kern_pair.cu",
-                  "fgemm_kern_strassen1.cu", "fgemm_kern_strassen2.cu", "fgemm_kern_winograd1.cu",
-                  "fgemm_kern_skinny.cu", "fgemm_kern_lcma.cu")
+# The device-code sources each form's kernels are built from.
+COMMON_SOURCES = ("fgemm_internal.h", "fgemm_ptx.cuh", "fgemm_kernel.cuh")
+FORM_SOURCES = {
+    "classical_pair": ("fgemm_kernel_pair.cuh", "fgemm_kern_pair.cu"),
+    "classical": ("fgemm_kern_classical.cu",),
+    "classical_small_m": ("fgemm_kern_skinny.cu",),
+    "lcma_pair": ("fgemm_kern_lcma.cu",),
+    "strassen1": ("fgemm_kern_strassen1.cu",),
+    "strassen2": ("fgemm_kern_strassen2.cu",),
+    "winograd1": ("fgemm_kern_winograd1.cu",),
+}
 
 
-def kernel_source_hash():
-    """Hash of the device-code sources: recorded ncu counters are used only
-    while the kernels they were taken on are unchanged."""
+def form_key(algo, tile_m):
+    if algo == "classical":
+        return "classical_pair" if tile_m == 256 else ("classical_small_m" if tile_m < 128 else "classical")
+    if tile_m == 256 and algo in ("strassen1", "winograd1"):
+        return "lcma_pair"
+    return algo
+
+
+def kernel_source_hash(algo="classical", tile_m=256):
+    """Hash of the device-code sources of one form's kernels: recorded ncu
+    counters are used only while the kernels they were taken on are
+    unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "complexity_matmul_tcgen05_gb300", "csrc")
-    for f in KERNEL_SOURCES:
+    for f in COMMON_SOURCES + FORM_SOURCES[form_key(algo, tile_m)]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
@@ -228,7 +244,7 @@ def ncu_traffic(workload, algo, tile_m, tile):
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(algo, tile_m)
     pat = re.compile(r"traffic_bytes_per_launch\s*:\s*(\d+)\s+workload=(\S+)\s+algo=(\S+)\s+"
                      r"tile=(\d+)x(\d+)\s+sources=(\w+)")
     for f in sorted(os.listdir(pdir)):

@@ -497,10 +497,9 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   // least kFusedMinWaves of them).
   int lead = 0;
   while (lead < np && !L.prod[lead].a_temp && !L.prod[lead].b_temp) ++lead;
-  constexpr long long kFusedMinWaves = 16;
   const bool whole_bands = F.job[0].rows % fgemm::kFormRows == 0 && F.job[1].rows % fgemm::kFormRows == 0;
   const bool fused = lead > 0 && whole_bands &&
-                     (h->lcma_formation == 2 || (h->lcma_formation == 0 && lead * whole >= kFusedMinWaves));
+                     (h->lcma_formation == 2 || (h->lcma_formation == 0 && lead * whole >= fgemm::kFusedMinWaves));
   // A pair's tail units (positions of the partial last wave, one product
   // each) run after its whole positions' first tail_at products, so that the
   // combinations of their accumulators overlap the MMAs of the products that

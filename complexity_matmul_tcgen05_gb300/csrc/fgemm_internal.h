@@ -246,6 +246,9 @@ struct LcmaFormParams {
 // Rows of one matrix per formation task when the product kernel forms the
 // temporaries itself.
 constexpr int kFormRows = 8;
+// The kernel forms them itself (automatic mode) when the scheme's leading
+// products that read only blocks of A and B span at least this many waves.
+constexpr long long kFusedMinWaves = 16;
 
 struct LcmaParams {
   KernelParams k;        // tmap_a / tmap_b map A and B; k.workspace holds the partial tiles

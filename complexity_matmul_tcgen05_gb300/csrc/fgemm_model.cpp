@@ -116,7 +116,7 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   // against 4.80 ms classical, sustained clocks, scaled to the classical
   // rate above)
   m.eff_strassen_pair[0] = rate(1121.0);  // 256 x 128
-  m.eff_strassen_pair[1] = rate(1620.0);  // 256 x 256
+  m.eff_strassen_pair[1] = rate(1650.0);  // 256 x 256
   // launch: back-to-back calls of a one-kernel product; fill: the first
   // MMA about 1.5 us after the start, the last 256 x 256 tile's epilogue
   // about 5 us after the last MMA (timestamps of an instrumented build)
@@ -141,6 +141,14 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   // 16 x 16384^2 on 128 CTAs of one whole tile each: 537 MB in 83.7 us, and
   // 16 x 8192^2 on 128 CTAs of half a tile: 32.7 us (CUDA events)
   m.small_m_aligned_eff = 7663.0 / m.hbm_gbs;
+  // Winograd's operands formed by the pair kernel's two idle warps per CTA
+  // beside its first products: 2.05 GB in about 1.9 ms at 16384^3, while the
+  // products of that time ran about 6 % slower
+  m.form_in_kernel_eff = 1080.0 / m.hbm_gbs;
+  m.form_in_kernel_drag = 0.063;
+  // the low-complexity forms round their operand sums: AUTO takes one only
+  // for a clear predicted gain, larger than the model's own error
+  m.lcma_margin = 0.03;
   *out = m;
 }
 
@@ -306,18 +314,31 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     const double pre_bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
                                     temps * (static_cast<double>(sub_m) * sub_k +
                                              static_cast<double>(sub_k) * sub_n));
-    const double t_pre = pre_bytes / (dev->hbm_gbs * 1e3 * std::max(dev->hbm_stream_eff, 1e-3)) +
-                         dev->launch_us;
+    double t_pre = pre_bytes / (dev->hbm_gbs * 1e3 * std::max(dev->hbm_stream_eff, 1e-3)) +
+                   dev->launch_us;
     const int64_t positions = fgemm_model_tiles(sub_m, sub_n, 256, tile_n);
     const int32_t pairs = std::max(1, dev->num_sms / 2);
     const int64_t units = positions * 7;
     const int64_t used = std::min<int64_t>(pairs, units);
+    const int64_t whole = positions / used;
     const int64_t tail_units = (positions % used) * 7;
     const double eff = std::max(dev->eff_strassen_pair[tile_n == 128 ? 0 : 1], 1e-3);
     const double pair_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms * 2.0;
     const double k_pad = static_cast<double>(ceil_div(sub_k, fgemm::kBK) * fgemm::kBK);
     const double t_unit = 2.0 * 256.0 * tile_n * k_pad / (pair_flop_per_us * eff);
-    const double per_pair = static_cast<double>((positions / used) * 7 + ceil_div(tail_units, used));
+    // Winograd's first two products read only blocks of A and B: with at
+    // least kFusedMinWaves waves of them the kernel forms the sums itself (A's, then
+    // B's) while they run, and the pre-pass launch goes.  What shows is the
+    // products' drag during the formation, and any part of it still running
+    // when the first product that reads B's sums (the fourth) starts.
+    const int64_t lead = wino ? 2 : 0;
+    if (lead > 0 && lead * whole >= fgemm::kFusedMinWaves && sub_m % fgemm::kFormRows == 0 && sub_k % fgemm::kFormRows == 0) {
+      const double t_form = pre_bytes / (dev->hbm_gbs * 1e3 * std::max(dev->form_in_kernel_eff, 1e-3));
+      const double drag = std::max(dev->form_in_kernel_drag, 0.0);
+      const double w = static_cast<double>(whole) * t_unit;
+      t_pre = drag * t_form + std::max(0.0, t_form - (1.0 + drag) * static_cast<double>(lead + 1) * w);
+    }
+    const double per_pair = static_cast<double>(whole * 7 + ceil_div(tail_units, used));
     const double t_compute = per_pair * t_unit + dev->tile_fill_us * (tail_units > 0 ? 2.0 : 1.0);
     if (predicted_us) *predicted_us = t_pre + t_compute + dev->launch_us;
     return FGEMM_OK;
@@ -402,11 +423,16 @@ fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M, int6
   double best = INFINITY;
   fgemm_algo_t best_algo = FGEMM_ALGO_CLASSICAL;
   int32_t best_m = 0, best_n = 0;
+  // the classical forms first; a low-complexity form must then beat the
+  // best of them by the margin
+  const double margin = std::min(std::max(dev->lcma_margin, 0.0), 0.9);
   for (fgemm_algo_t a : algos) {
+    const double scale = a == FGEMM_ALGO_CLASSICAL ? 1.0 : 1.0 / (1.0 - margin);
     for (int32_t tm : tms) {
       for (int32_t tn : tns) {
         double us = 0;
         if (fgemm_model_predict(dev, M, N, K, epi_kind, a, tm, tn, &us) != FGEMM_OK) continue;
+        us *= scale;
         if (us < best) {
           best = us;
           best_algo = a;
@@ -420,7 +446,8 @@ fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M, int6
   if (algo_out) *algo_out = best_algo;
   if (tile_m) *tile_m = best_m;
   if (tile_n) *tile_n = best_n;
-  if (predicted_us) *predicted_us = best;
+  if (predicted_us)
+    *predicted_us = best_algo == FGEMM_ALGO_CLASSICAL ? best : best * (1.0 - margin);
   return FGEMM_OK;
 }
 
@@ -460,6 +487,9 @@ std::vector<std::pair<const char*, double*>> model_fields(fgemm_device_model_t& 
       {"small_m_stream_eff", &m.small_m_stream_eff},
       {"small_m_fix_us", &m.small_m_fix_us},
       {"small_m_aligned_eff", &m.small_m_aligned_eff},
+      {"form_in_kernel_eff", &m.form_in_kernel_eff},
+      {"form_in_kernel_drag", &m.form_in_kernel_drag},
+      {"lcma_margin", &m.lcma_margin},
   };
 }
 
@@ -514,7 +544,8 @@ extern "C" fgemm_status_t fgemm_model_load_json(const char* path, fgemm_device_m
                       &m.eff_small_m[0], &m.eff_small_m[1], &m.eff_small_m[2]})
       *e *= r;
     const double rb = old_bw / m.hbm_gbs;
-    for (double* e : {&m.hbm_stream_eff, &m.small_m_stream_eff, &m.small_m_aligned_eff}) *e *= rb;
+    for (double* e : {&m.hbm_stream_eff, &m.small_m_stream_eff, &m.small_m_aligned_eff, &m.form_in_kernel_eff})
+      *e *= rb;
     m.peak_tflops = tf;
     ++found;
   }

@@ -57,7 +57,10 @@ class DeviceModel(ctypes.Structure):
                 ("eff_winograd", ctypes.c_double * 2),
                 ("eff_small_m", ctypes.c_double * 3), ("hbm_stream_eff", ctypes.c_double),
                 ("small_m_stream_eff", ctypes.c_double), ("small_m_fix_us", ctypes.c_double),
-                ("small_m_aligned_eff", ctypes.c_double)]
+                ("small_m_aligned_eff", ctypes.c_double),
+                ("form_in_kernel_eff", ctypes.c_double),
+                ("form_in_kernel_drag", ctypes.c_double),
+                ("lcma_margin", ctypes.c_double)]
 
 
 _lib = None

@@ -55,7 +55,8 @@ typedef enum {
                              * products whose operands are sums of up to four
                              * blocks (FalconGEMM summary, "Methodology" item 1
                              * names it; standard identities). One-CTA tiles
-                             * only (tile_m 128, tile_n 128 or 256). */
+                             * (tile_m 128) or CTA pairs (tile_m 256), tile_n
+                             * 128 or 256. */
 } fgemm_algo_t;
 
 /*
@@ -413,6 +414,14 @@ typedef struct {
   double small_m_aligned_eff; /* fraction of hbm_gbs the small-M kernel reaches on
                                * a grid whose shares start at no more than 4 K
                                * offsets of a tile (fgemm_small_m_grid) */
+  double form_in_kernel_eff; /* fraction of hbm_gbs at which a one-level pair
+                              * launch's own idle warps form the summed operands
+                              * beside the products (fgemm_set_lcma_formation) */
+  double form_in_kernel_drag; /* time the products lose to that formation, as a
+                               * fraction of the formation's duration */
+  double lcma_margin;      /* AUTO picks a low-complexity form only when its
+                            * prediction is below (1 - lcma_margin) times the
+                            * best classical one */
 } fgemm_device_model_t;
 
 /*
