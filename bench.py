@@ -338,13 +338,6 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def launches_per_call(algo, tile_m):
-    """Kernels of this library one fgemm_matmul_ex call launches: two for one
-    Strassen-like level on CTA pairs (the operand-sum pre-pass and the
-    product kernel), one otherwise."""
-    return 2 if algo in ("strassen1", "winograd1") and tile_m == 256 else 1
-
-
 def time_calls(fn, n, stream):
     """Mean ms of n back-to-back calls of fn(i) (CUDA events around each on
     `stream`), and the ms of the whole run."""
@@ -422,11 +415,14 @@ def run_fgemm(args, rank, world):
     handle.set_split_mode(args.split)
     stream = torch.cuda.current_stream(dev)
     algo, tile, tile_m = args.algo, args.tile, args.tile_m
-    if algo == "auto":
-        plan_algo, plan_tm, plan_tile, pred_us = handle.plan(M, N, K, fgemm._dtype_code(A0.dtype),
-                                                             fgemm.make_epilogue(epi))
-    else:
-        plan_algo, plan_tm, plan_tile, pred_us = algo, tile_m, tile, None
+    # the form and tile the calls run (AUTO's choice, or the forced form with
+    # the model's best tile of it where none is given), and the kernels each
+    # call launches
+    plan_algo, plan_tm, plan_tile, pred_us = handle.plan(M, N, K, fgemm._dtype_code(A0.dtype),
+                                                         fgemm.make_epilogue(epi), algo=algo,
+                                                         tile_m=tile_m, tile_n=tile)
+    per_call = handle.call_launches(M, N, K, fgemm.make_epilogue(epi), algo=algo, tile_m=tile_m,
+                                    tile_n=tile)
 
     def step(i):
         fgemm.matmul(As[i % sets], Bs[i % sets], out=Cs[i % sets], epilogue=epi,
@@ -591,7 +587,7 @@ def run_fgemm(args, rank, world):
         "parallelism": f"replicas x{world}",
         "roofline": roof,
         "forms": forms,
-        "gpu_launches": args.steps * launches_per_call(plan_algo, plan_tm),
+        "gpu_launches": args.steps * per_call,
         "clocks": clk.summary(),
     }
     if small is not None:

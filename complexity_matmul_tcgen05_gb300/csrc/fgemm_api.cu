@@ -358,6 +358,30 @@ fgemm_status_t prepare_split(fgemm_handle_t h, KernelParams* p, int split, int p
 // (formed by one pre-pass launch), the product kernel reads every operand
 // through a tensor map of A, B or the temporaries.  Workspace layout: the
 // product kernel's partial tiles, then the A and the B temporaries.
+// The scheme's leading products whose operands are both raw blocks of A and
+// B (a single positive term each): Winograd's A11 B11 and A12 B21, none of
+// Strassen's.
+int lcma_lead_products(const StrassenTable& tab) {
+  auto raw = [](int n, const uint8_t* c) { return n == 1 && !(c[0] & fgemm::kTermNeg); };
+  int lead = 0;
+  while (lead < fgemm::kLcmaProducts && raw(tab.na[lead], tab.a[lead]) && raw(tab.nb[lead], tab.b[lead])) ++lead;
+  return lead;
+}
+
+// Whether a one-level pair launch forms its summed operands inside the
+// product kernel: the scheme has leading products without sums, the
+// matrices cut into whole formation bands, and the handle asks for it (mode
+// 2) or leaves it to the rule (mode 0: those products span at least
+// kFusedMinWaves waves of the `clusters` pairs over `positions`).
+bool lcma_forms_in_kernel(fgemm_handle_t h, const StrassenTable& tab, long long positions, int clusters,
+                          int sub_m, int sub_k) {
+  const int lead = lcma_lead_products(tab);
+  const long long whole = positions / std::max(clusters, 1);
+  const bool whole_bands = sub_m % fgemm::kFormRows == 0 && sub_k % fgemm::kFormRows == 0;
+  return lead > 0 && whole_bands &&
+         (h->lcma_formation == 2 || (h->lcma_formation == 0 && lead * whole >= fgemm::kFusedMinWaves));
+}
+
 fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTable& tab, int bn,
                            const void* A, int64_t lda, const void* B, int64_t ldb) {
   using fgemm::LcmaFormParams;
@@ -495,11 +519,8 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   // product kernel while the scheme's leading products that read only blocks
   // of A and B run (their waves must cover the formation: auto asks for at
   // least kFusedMinWaves of them).
-  int lead = 0;
-  while (lead < np && !L.prod[lead].a_temp && !L.prod[lead].b_temp) ++lead;
-  const bool whole_bands = F.job[0].rows % fgemm::kFormRows == 0 && F.job[1].rows % fgemm::kFormRows == 0;
-  const bool fused = lead > 0 && whole_bands &&
-                     (h->lcma_formation == 2 || (h->lcma_formation == 0 && lead * whole >= fgemm::kFusedMinWaves));
+  const int lead = lcma_lead_products(tab);
+  const bool fused = lcma_forms_in_kernel(h, tab, positions, clusters, p.sub_m, p.sub_k);
   // A pair's tail units (positions of the partial last wave, one product
   // each) run after its whole positions' first tail_at products, so that the
   // combinations of their accumulators overlap the MMAs of the products that
@@ -748,6 +769,40 @@ fgemm_status_t fgemm_plan_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
   if (tile_m) *tile_m = p.tile_m;
   if (tile_n) *tile_n = p.tile_n;
   if (predicted_us) *predicted_us = p.predicted_us;
+  return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_call_launches(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                   const fgemm_epilogue_t* epi, fgemm_algo_t algo, int32_t tile_m_in,
+                                   int32_t tile_n_in, int32_t* launches) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  if (!launches) return set_msg(h, FGEMM_ERR_INVALID_ARG, "launches is NULL");
+  if (algo < FGEMM_ALGO_AUTO || algo > FGEMM_ALGO_WINOGRAD1)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "unknown algorithm");
+  const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
+  const int64_t n_out = kind == FGEMM_EPI_SWIGLU ? N / 2 : N;
+  if (M == 0 || n_out == 0) {
+    *launches = 0;
+    return FGEMM_OK;
+  }
+  if (K == 0) {
+    *launches = 1;  // the bias / zero fill
+    return FGEMM_OK;
+  }
+  Plan p;
+  fgemm_status_t s = choose_plan(h, M, N, K, kind, algo, tile_m_in, tile_n_in, &p);
+  if (s != FGEMM_OK) return s;
+  *launches = 1;
+  if (p.tile_m == 256 && depth_of(p.algo) == 1) {
+    const int sub_m = static_cast<int>(M / 2), sub_n = static_cast<int>(N / 2), sub_k = static_cast<int>(K / 2);
+    const long long positions = fgemm_model_tiles(sub_m, sub_n, 256, p.tile_n);
+    const int fit = fgemm::lcma_pair_clusters_fit(p.tile_n);
+    if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the Strassen pair launch");
+    const int clusters = static_cast<int>(std::min<long long>(fit, positions * fgemm::kLcmaProducts));
+    const StrassenTable& tab =
+        p.algo == FGEMM_ALGO_WINOGRAD1 ? fgemm::winograd_table() : fgemm::strassen_table(1);
+    if (!lcma_forms_in_kernel(h, tab, positions, clusters, sub_m, sub_k)) *launches = 2;
+  }
   return FGEMM_OK;
 }
 

@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
                                     ctypes.POINTER(i32), ctypes.POINTER(i32),
                                     ctypes.POINTER(ctypes.c_double)]
         L.fgemm_get_error.argtypes = [vp]
+        L.fgemm_call_launches.argtypes = [vp, i64, i64, i64, epi_p, st, i32, i32, ctypes.POINTER(i32)]
         L.fgemm_selftest_wait_timeout.argtypes = [vp, i32]
         L.fgemm_calibrate.argtypes = [vp, ctypes.c_char_p]
         L.fgemm_calibrate_ex.argtypes = [vp, i64, ctypes.c_char_p]
@@ -145,7 +146,7 @@ def lib() -> ctypes.CDLL:
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
                      "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout",
-                     "fgemm_set_split_mode", "fgemm_set_lcma_formation", "fgemm_matmul_rms", "fgemm_matmul_mx",
+                     "fgemm_set_split_mode", "fgemm_set_lcma_formation", "fgemm_call_launches", "fgemm_matmul_rms", "fgemm_matmul_mx",
                      "fgemm_mx_to_bf16", "fgemm_strassen_static_get_error",
                      "fgemm_strassen_static_selftest_timeout"):
             getattr(L, name).restype = st
@@ -289,6 +290,16 @@ class Handle:
                                    ALGOS[algo], tile_m, tile_n, ctypes.byref(a), ctypes.byref(tm),
                                    ctypes.byref(tn), ctypes.byref(us)), self._h)
         return ALGO_NAMES[a.value], tm.value, tn.value, us.value
+
+    def call_launches(self, M, N, K, epilogue: Epilogue | None = None, algo: str = "auto",
+                      tile_m: int = 0, tile_n: int = 0) -> int:
+        """Kernels of this library one matmul call with these arguments
+        launches on this handle (host only)."""
+        n = ctypes.c_int32()
+        _check(lib().fgemm_call_launches(self._h, M, N, K,
+                                         ctypes.byref(epilogue) if epilogue is not None else None,
+                                         ALGOS[algo], tile_m, tile_n, ctypes.byref(n)), self._h)
+        return n.value
 
     def get_error(self) -> int:
         return lib().fgemm_get_error(self._h)

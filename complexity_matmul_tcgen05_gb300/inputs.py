@@ -12,7 +12,9 @@ Workloads (dense GEMMs shaped like LLM projection / FFN layers):
                         per-column bias ~ N(0, 0.02^2), alpha = 1
   ffn_up_swiglu_bf16    M=8192, N=28672 (gate | up, 2 x 14336), K=4096, bf16,
                         A ~ N(0,1), B ~ N(0,1/K), SwiGLU output M x 14336
+  square_8192_bf16      M=N=K=8192, bf16, A,B ~ U[-1,1]
   square_16384_bf16     M=N=K=16384, bf16, A,B ~ U[-1,1]
+  square_24576_bf16     M=N=K=24576, bf16, A,B ~ U[-1,1]
   sweep                 bf16, M in {16,128,1024,8192} x N=K in
                         {2048,4096,8192,16384}, plus M=65536, N=K=1024;
                         A,B ~ N(0,1) / sqrt(K)
@@ -34,9 +36,15 @@ WORKLOADS = {
     "ffn_up_swiglu_bf16": dict(M=8192, N=28672, K=4096, dtype="bf16", a="normal",
                                b="normal_inv_k", epi="swiglu", bias=None,
                                algos=("classical", "strassen1", "auto")),
+    "square_8192_bf16": dict(M=8192, N=8192, K=8192, dtype="bf16", a="uniform",
+                             b="uniform", epi="none", bias=None,
+                             algos=("classical", "strassen1", "winograd1", "auto")),
     "square_16384_bf16": dict(M=16384, N=16384, K=16384, dtype="bf16", a="uniform",
                               b="uniform", epi="none", bias=None,
                               algos=("classical", "strassen1", "strassen2", "winograd1", "auto")),
+    "square_24576_bf16": dict(M=24576, N=24576, K=24576, dtype="bf16", a="uniform",
+                              b="uniform", epi="none", bias=None,
+                              algos=("classical", "strassen1", "winograd1", "auto")),
 }
 
 SWEEP_SHAPES = [(m, nk, nk) for m in (16, 128, 1024, 8192)

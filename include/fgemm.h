@@ -276,6 +276,20 @@ fgemm_status_t fgemm_plan_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
 fgemm_status_t fgemm_get_error(fgemm_handle_t h);
 
 /*
+ * How many kernels of this library one fgemm_matmul_ex call with these
+ * arguments launches on the handle with its current settings (the plan AUTO
+ * or the forced form resolves to; for one Strassen-like level on CTA pairs,
+ * the operand pre-pass unless the product kernel forms the sums itself, see
+ * fgemm_set_lcma_formation). Host only: launches nothing. Writes *launches;
+ * returns the plan's errors (FGEMM_ERR_UNSUPPORTED for an illegal forced
+ * form) or FGEMM_ERR_INVALID_ARG for a NULL handle, a NULL output or an
+ * unknown algorithm.
+ */
+fgemm_status_t fgemm_call_launches(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                   const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                                   int32_t tile_m, int32_t tile_n, int32_t* launches);
+
+/*
  * Measures the device (tensor throughput of each classical tile width and
  * of each Strassen form, streaming bandwidth) with the library's own
  * kernels, updates the handle's device model, and writes it as JSON to

@@ -115,6 +115,16 @@ def test_square_16384(algo, tile_m):
     _sampled_check("square_16384", A, B, None, algo, "none", "bf16", tile_m=tile_m)
 
 
+@pytest.mark.parametrize("algo,tile_m", [("classical", 0), ("winograd1", 256), ("strassen1", 256),
+                                         ("auto", 0)])
+def test_square_24576(algo, tile_m):
+    """The largest square workload the benchmark names: 30 whole waves of
+    output positions on the pairs plus a partial one, Winograd's sums formed
+    inside its product kernel."""
+    A, B, _ = inputs.workload_inputs("square_24576_bf16", DEV)
+    _sampled_check("square_24576", A, B, None, algo, "none", "bf16", tile_m=tile_m)
+
+
 @pytest.mark.parametrize("shape", inputs.SWEEP_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_sweep_shapes_every_legal_form(shape):
     M, N, K = shape

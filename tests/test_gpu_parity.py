@@ -197,6 +197,26 @@ def test_lcma_formation_modes_give_the_same_bits(M, N, K, tile, epilogue, algo, 
     assert torch.equal(C2.view(torch.int16), C3.view(torch.int16))
 
 
+def test_call_launches_follows_the_formation(formation):
+    """The launch count a call reports: one kernel, except one level on CTA
+    pairs whose operand sums a pre-pass forms (Strassen always; Winograd
+    when its sum-free products span fewer than 16 waves, or when asked)."""
+    h = fgemm.default_handle()
+    assert h.call_launches(4096, 4096, 4096, algo="classical", tile_m=256, tile_n=256) == 1
+    assert h.call_launches(16384, 16384, 16384, algo="strassen1", tile_m=256, tile_n=256) == 2
+    assert h.call_launches(16384, 16384, 16384, algo="winograd1", tile_m=256, tile_n=256) == 1
+    assert h.call_launches(4096, 4096, 4096, algo="winograd1", tile_m=256, tile_n=256) == 2
+    assert h.call_launches(4096, 4096, 4096, algo="winograd1", tile_m=128, tile_n=256) == 1
+    assert h.call_launches(4096, 4096, 0, algo="classical") == 1
+    formation("prepass")
+    assert h.call_launches(16384, 16384, 16384, algo="winograd1", tile_m=256, tile_n=256) == 2
+    formation("in_kernel")
+    assert h.call_launches(4096, 4096, 4096, algo="winograd1", tile_m=256, tile_n=256) == 1
+    assert h.call_launches(16384, 16384, 16384, algo="strassen1", tile_m=256, tile_n=256) == 2
+    with pytest.raises(fgemm.FgemmError):
+        h.call_launches(384, 256, 128, algo="strassen1", tile_m=256, tile_n=256)
+
+
 def test_winograd_formed_in_kernel_graph_replay(formation):
     """A captured launch with in-kernel formation replays with the same
     result: the clearing of its band counters is part of the graph."""
