@@ -523,9 +523,11 @@ def run_fgemm(args, rank, world):
         if handle.get_error() != fgemm.OK:
             raise SystemExit(f"device error in the 256^3 case: {handle.last_message()}")
 
-    # End to end through the library's host-buffer path: fgemm.matmul on
-    # pinned CPU tensors uploads A, B (and the bias), runs the product and
-    # downloads C into a pinned host tensor, every step.
+    # End to end through the library's host-buffer call: fgemm.matmul on
+    # pinned CPU tensors (fgemm_matmul_host) uploads B (and the bias), then
+    # streams A's row blocks up while earlier blocks are multiplied and their
+    # C blocks come down into a pinned host tensor; every step is a whole call
+    # that returns with C written.
     e2e = None
     if not args.no_e2e:
         hA = A0.cpu().pin_memory()
@@ -552,8 +554,9 @@ def run_fgemm(args, rank, world):
         h2d = hA.numel() * 2 + hB.numel() * 2 + (0 if hbias is None else hbias.numel() * 2)
         e2e = {"value": flops * world * n_e2e / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hC.numel() * 2,
-               "steps": n_e2e, "path": "fgemm.matmul on pinned host tensors (upload, product, "
-               "download each step, host wall clock)"}
+               "steps": n_e2e, "path": "fgemm.matmul on pinned host tensors: fgemm_matmul_host "
+               "(B up, then A row blocks up / products / C blocks down, pipelined), one "
+               "whole call per step, host wall clock"}
 
     if rank != 0:
         return

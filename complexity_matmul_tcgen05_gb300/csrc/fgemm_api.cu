@@ -134,6 +134,14 @@ struct fgemm_handle_s {
   int split_mode = 1;                 // 0 never, 1 auto, 2 whenever possible
   int lcma_formation = 0;             // 0 auto, 1 pre-pass launch, 2 inside the product kernel
   unsigned int* form_ctr = nullptr;   // band counters of the in-kernel formation (3 words)
+  // fgemm_matmul_host: device copies of B, the bias and two slots each of A
+  // and C row blocks; an upload and a download stream; the events that
+  // order them with the handle's stream
+  void* host_buf = nullptr;
+  size_t host_bytes = 0;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_a[2] = {nullptr, nullptr}, ev_c[2] = {nullptr, nullptr},
+              ev_d[2] = {nullptr, nullptr};
   unsigned long long spin_ns = 1000000000ull;
   fgemm_device_model_t model{};
   std::unordered_map<PlanKey, Plan, PlanKeyHash> plans;
@@ -704,6 +712,12 @@ fgemm_status_t fgemm_destroy(fgemm_handle_t h) {
   if (h->workspace) cudaFree(h->workspace);
   if (h->split_ctr) cudaFree(h->split_ctr);
   if (h->form_ctr) cudaFree(h->form_ctr);
+  if (h->host_buf) cudaFree(h->host_buf);
+  for (cudaStream_t st : {h->up, h->down})
+    if (st) cudaStreamDestroy(st);
+  for (cudaEvent_t ev : {h->ev_start, h->ev_b, h->ev_a[0], h->ev_a[1], h->ev_c[0], h->ev_c[1], h->ev_d[0],
+                         h->ev_d[1]})
+    if (ev) cudaEventDestroy(ev);
   if (h->mx_buf) cudaFree(h->mx_buf);
   if (h->d_err) cudaFree(h->d_err);
   delete h;
@@ -933,6 +947,123 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
                                int32_t tile_m, int32_t tile_n) {
   if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
   return matmul_impl(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_m, tile_n, nullptr);
+}
+
+// C = epi(alpha A B + bias) with A, B, C and the bias in host memory.  B (and
+// the bias) go up first; A is cut into row blocks that go up on the upload
+// stream while earlier blocks are multiplied on the handle's stream and their
+// C blocks come down on the download stream, two slots of each.  Everything
+// is ordered on the handle's stream when the call returns.
+fgemm_status_t fgemm_matmul_host(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                                 int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                                 fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                                 int32_t tile_m, int32_t tile_n) {
+  if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
+  if (dtype != FGEMM_F16 && dtype != FGEMM_BF16)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "dtype must be FGEMM_F16 or FGEMM_BF16");
+  if (M < 0 || N < 0 || K < 0) return set_msg(h, FGEMM_ERR_INVALID_ARG, "negative size");
+  const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
+  const int64_t n_out = kind == FGEMM_EPI_SWIGLU ? N / 2 : N;
+  if (M == 0 || n_out == 0) return FGEMM_OK;
+  if ((K > 0 && (!A || !B)) || !C) return set_msg(h, FGEMM_ERR_INVALID_ARG, "NULL host matrix");
+  if ((K > 0 && (lda < K || ldb < N)) || ldc < n_out)
+    return set_msg(h, FGEMM_ERR_INVALID_ARG, "leading dimension smaller than the row");
+  // row blocks: at least ~6 waves of 256 x 256 pair tiles each, at most 8
+  // blocks, a multiple of 512 rows that divides M (so every block takes the
+  // same form); otherwise one block
+  int64_t mb = M;
+  const int64_t min_rows = std::max<int64_t>(512, (6 * 76 * 65536 + N - 1) / std::max<int64_t>(N, 1));
+  for (int nb = 8; nb >= 2; --nb) {
+    if (M % nb != 0) continue;
+    const int64_t r = M / nb;
+    if (r % 512 == 0 && r >= min_rows) {
+      mb = r;
+      break;
+    }
+  }
+  const int64_t nblocks = M / mb;
+  const size_t esz = 2;
+  auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  // device row pitches: multiples of 8 elements (16 bytes), as the kernels need
+  const int64_t pk = (std::max<int64_t>(K, 1) + 7) / 8 * 8, pn = (N + 7) / 8 * 8, po = (n_out + 7) / 8 * 8;
+  const size_t b_bytes = al(static_cast<size_t>(K) * pn * esz), bias_bytes = al(static_cast<size_t>(N) * esz);
+  const size_t a_bytes = al(static_cast<size_t>(mb) * pk * esz), c_bytes = al(static_cast<size_t>(mb) * po * esz);
+  const size_t need = b_bytes + bias_bytes + 2 * a_bytes + 2 * c_bytes;
+  cudaError_t e = cudaSuccess;
+  if (need > h->host_bytes) {
+    e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+    if (h->host_buf) cudaFree(h->host_buf);
+    h->host_buf = nullptr;
+    h->host_bytes = 0;
+    e = cudaMalloc(&h->host_buf, need);
+    if (e != cudaSuccess) {
+      h->host_buf = nullptr;
+      return cuda_fail(h, e, "cudaMalloc(host-call buffers)");
+    }
+    h->host_bytes = need;
+  }
+  if (!h->up) {
+    e = cudaStreamCreateWithFlags(&h->up, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->down, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&h->ev_start, &h->ev_b, &h->ev_a[0], &h->ev_a[1], &h->ev_c[0], &h->ev_c[1],
+                            &h->ev_d[0], &h->ev_d[1]})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(h, e, "creating the host-call streams and events");
+  }
+  uint8_t* base = static_cast<uint8_t*>(h->host_buf);
+  uint8_t* dB = base;
+  uint8_t* dbias = dB + b_bytes;
+  uint8_t* dA[2] = {dbias + bias_bytes, dbias + bias_bytes + a_bytes};
+  uint8_t* dC[2] = {dA[1] + a_bytes, dA[1] + a_bytes + c_bytes};
+  fgemm_epilogue_t dev_epi{kind, epi ? epi->alpha : 1.0f, nullptr};
+  // the copy streams start after everything already on the handle's stream
+  e = cudaEventRecord(h->ev_start, h->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->up, h->ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->down, h->ev_start, 0);
+  if (e == cudaSuccess && K > 0)
+    e = cudaMemcpy2DAsync(dB, static_cast<size_t>(pn) * esz, B, static_cast<size_t>(ldb) * esz,
+                          static_cast<size_t>(N) * esz, static_cast<size_t>(K), cudaMemcpyHostToDevice, h->up);
+  if (e == cudaSuccess && epi && epi->bias) {
+    e = cudaMemcpyAsync(dbias, epi->bias, static_cast<size_t>(N) * esz, cudaMemcpyHostToDevice, h->up);
+    dev_epi.bias = dbias;
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_b, h->up);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->stream, h->ev_b, 0);
+  if (e != cudaSuccess) return cuda_fail(h, e, "host-call upload of B");
+  for (int64_t i = 0; i < nblocks; ++i) {
+    const int sl = static_cast<int>(i & 1);
+    const uint8_t* Ai = static_cast<const uint8_t*>(A) + static_cast<size_t>(i * mb) * lda * esz;
+    uint8_t* Ci = static_cast<uint8_t*>(C) + static_cast<size_t>(i * mb) * ldc * esz;
+    // A block i into its slot once block i - 2's product has read it
+    if (i >= 2) e = cudaStreamWaitEvent(h->up, h->ev_c[sl], 0);
+    if (e == cudaSuccess && K > 0)
+      e = cudaMemcpy2DAsync(dA[sl], static_cast<size_t>(pk) * esz, Ai, static_cast<size_t>(lda) * esz,
+                            static_cast<size_t>(K) * esz, static_cast<size_t>(mb), cudaMemcpyHostToDevice, h->up);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_a[sl], h->up);
+    // the product, once A block i is up and C block i - 2 is down
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->stream, h->ev_a[sl], 0);
+    if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(h->stream, h->ev_d[sl], 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "host-call upload of A");
+    fgemm_status_t s = matmul_impl(h, mb, N, K, dA[sl], pk, dB, pn, dC[sl], po, dtype, &dev_epi, algo, tile_m,
+                                   tile_n, nullptr);
+    if (s != FGEMM_OK) return s;
+    e = cudaEventRecord(h->ev_c[sl], h->stream);
+    // C block i down
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->down, h->ev_c[sl], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(Ci, static_cast<size_t>(ldc) * esz, dC[sl], static_cast<size_t>(po) * esz,
+                            static_cast<size_t>(n_out) * esz, static_cast<size_t>(mb), cudaMemcpyDeviceToHost,
+                            h->down);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_d[sl], h->down);
+    if (e != cudaSuccess) return cuda_fail(h, e, "host-call download of C");
+  }
+  // the handle's stream ends after the last download
+  for (int sl = 0; sl < 2 && sl < nblocks; ++sl) {
+    e = cudaStreamWaitEvent(h->stream, h->ev_d[sl], 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamWaitEvent");
+  }
+  return FGEMM_OK;
 }
 
 fgemm_status_t fgemm_matmul_rms(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,

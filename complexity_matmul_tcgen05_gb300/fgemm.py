@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
                                     ctypes.POINTER(i32), ctypes.POINTER(i32),
                                     ctypes.POINTER(ctypes.c_double)]
         L.fgemm_get_error.argtypes = [vp]
+        L.fgemm_matmul_host.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, st, epi_p, st, i32, i32]
         L.fgemm_call_launches.argtypes = [vp, i64, i64, i64, epi_p, st, i32, i32, ctypes.POINTER(i32)]
         L.fgemm_selftest_wait_timeout.argtypes = [vp, i32]
         L.fgemm_calibrate.argtypes = [vp, ctypes.c_char_p]
@@ -146,7 +147,7 @@ def lib() -> ctypes.CDLL:
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
                      "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout",
-                     "fgemm_set_split_mode", "fgemm_set_lcma_formation", "fgemm_call_launches", "fgemm_matmul_rms", "fgemm_matmul_mx",
+                     "fgemm_set_split_mode", "fgemm_set_lcma_formation", "fgemm_call_launches", "fgemm_matmul_host", "fgemm_matmul_rms", "fgemm_matmul_mx",
                      "fgemm_mx_to_bf16", "fgemm_strassen_static_get_error",
                      "fgemm_strassen_static_selftest_timeout"):
             getattr(L, name).restype = st
@@ -356,16 +357,7 @@ def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
     call) scales accumulator row i by 1/sqrt(sum / norm_width + rms_eps).
     """
     if A.device.type == "cpu" and B.device.type == "cpu":
-        dev = torch.device("cuda", torch.cuda.current_device())
-        Ad = A.to(dev, non_blocking=True)
-        Bd = B.to(dev, non_blocking=True)
-        bd = None if bias is None else bias.to(dev, non_blocking=True)
-        Cd = matmul(Ad, Bd, epilogue=epilogue, alpha=alpha, bias=bd, algo=algo, tile_n=tile_n,
-                    tile_m=tile_m, handle=handle)
-        if out is not None:
-            out.copy_(Cd)
-            return out
-        return Cd.cpu()
+        return _matmul_host(A, B, out, epilogue, alpha, bias, algo, tile_n, tile_m, handle)
     _check_matrix(A, "A")
     _check_matrix(B, "B")
     if not (A.is_cuda and B.is_cuda):
@@ -416,6 +408,44 @@ def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
         s = h.matmul_rms_raw(M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc, dt,
                              epi, algo, tile_n, tile_m, rms)
     _check(s, h.ptr)
+    return out
+
+
+def _matmul_host(A, B, out, epilogue, alpha, bias, algo, tile_n, tile_m, handle):
+    """Host tensors through fgemm_matmul_host (pipelined copies; they overlap
+    when the tensors are pinned); returns once C is written."""
+    for t, name in ((A, "A"), (B, "B")):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise FgemmError(ERR_INVALID_ARG, f"{name} must be a 2-D tensor with unit column stride")
+    if A.dtype != B.dtype:
+        raise FgemmError(ERR_INVALID_ARG, "A and B must have the same dtype")
+    dt = _dtype_code(A.dtype)
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise FgemmError(ERR_INVALID_ARG, f"inner dimensions differ: {K} vs {K2}")
+    n_out = N // 2 if epilogue == "swiglu" else N
+    if out is None:
+        out = torch.empty((M, n_out), dtype=A.dtype, pin_memory=A.is_pinned())
+    elif (out.device.type != "cpu" or out.dtype != A.dtype or tuple(out.shape) != (M, n_out)
+          or out.stride(1) != 1):
+        raise FgemmError(ERR_INVALID_ARG, "out must be a host tensor of the right dtype and shape")
+    bias_ptr = None
+    if bias is not None:
+        if bias.device.type != "cpu" or bias.dtype != A.dtype or bias.numel() != N:
+            raise FgemmError(ERR_INVALID_ARG, "bias must be a host vector of N entries, same dtype")
+        bias = bias.contiguous()
+        bias_ptr = bias.data_ptr()
+    h = handle if handle is not None else default_handle()
+    h.set_stream(torch.cuda.current_stream().cuda_stream)
+    epi = make_epilogue(epilogue, alpha, bias_ptr)
+    s = lib().fgemm_matmul_host(h.ptr, M, N, K, A.data_ptr(), A.stride(0) if M > 1 else max(K, 1),
+                                B.data_ptr(), B.stride(0) if K > 1 else max(N, 1), out.data_ptr(),
+                                out.stride(0) if M > 1 else max(n_out, 1), dt, ctypes.byref(epi),
+                                ALGOS[algo], tile_m, tile_n)
+    _check(s, h.ptr)
+    torch.cuda.current_stream().synchronize()
+    _check(h.get_error(), h.ptr)
     return out
 
 

@@ -193,6 +193,32 @@ typedef struct {
 } fgemm_rms_t;
 
 /*
+ * fgemm_matmul_ex with A, B, C and the bias (epi->bias) in HOST memory: the
+ * call a user with host buffers makes (PingPong GEMM / CODA note: keep the
+ * tensor cores busy during data movement). B and the bias are copied to the
+ * device first; A is cut into row blocks (up to 8, each a multiple of 512
+ * rows and at least about six waves of 256 x 256 tiles; one block when M does
+ * not divide so) that are uploaded on the handle's upload stream while the
+ * earlier blocks are multiplied on the handle's stream and their C blocks are
+ * downloaded on its download stream, two device slots of each, ordered by
+ * events. Every block runs the same form (AUTO's plan for the block's shape,
+ * or the forced algo / tile). The copies overlap only for page-locked host
+ * memory (cudaHostAlloc / cudaHostRegister); pageable memory works but
+ * serialises. Returns once everything is enqueued: C is written when the
+ * handle's stream reaches this point (cudaStreamSynchronize on it), and the
+ * host buffers must stay valid until then. lda >= K, ldb >= N, ldc >= N_out
+ * (any alignment). The device copies live in handle-owned buffers (grown on
+ * demand; B, the bias, two A and two C row blocks). Errors as for
+ * fgemm_matmul_ex, plus FGEMM_ERR_CUDA for a failed copy. RMSNorm statistics
+ * are not offered here.
+ */
+fgemm_status_t fgemm_matmul_host(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                 const void* A, int64_t lda, const void* B, int64_t ldb,
+                                 void* C, int64_t ldc, fgemm_dtype_t dtype,
+                                 const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                                 int32_t tile_m, int32_t tile_n);
+
+/*
  * As fgemm_matmul_ex, with RMSNorm statistics (rms may be NULL). Classical
  * form on one-CTA or CTA-pair tiles only (tile_m 128 or 256; AUTO chooses
  * among those), never with the last-wave K split; K >= 1. Other forced forms

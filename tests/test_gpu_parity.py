@@ -905,3 +905,76 @@ def test_calibrate_reduced_size_and_reload(tmp_path, monkeypatch):
         fgemm.Handle()
     h.close()
     h2.close()
+
+
+# ------------------------------------------- host buffers (fgemm_matmul_host)
+
+def _host(t, pinned):
+    h = t.cpu()
+    return h.pin_memory() if pinned else h
+
+
+@pytest.mark.parametrize("M,N,K,pinned", [
+    (8192, 16384, 512, True),    # four row blocks of 2048, pipelined
+    (4096, 16384, 256, True),    # two row blocks
+    (300, 520, 100, False),      # one ragged block, K and N off the 8-element pitch, pageable
+    (1, 1, 1, True),
+])
+def test_host_path_exact_ternary(M, N, K, pinned):
+    """A, B, C and the bias in host memory: RNE(exact C) bit for bit."""
+    A, B, bias = _ternary(M, N, K, "bf16", seed=90)
+    hA, hB, hbias = _host(A, pinned), _host(B, pinned), _host(bias, pinned)
+    C = fgemm.matmul(hA, hB, epilogue="scale_bias", bias=hbias)
+    assert C.device.type == "cpu"
+    assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, "bf16"))
+
+
+def test_host_path_strided_views_and_guard_band():
+    """Host views with leading dimensions past the row (lda > K, ldb > N,
+    ldc > N_out): the result lands in the view, the columns around it keep
+    their values."""
+    M, N, K = 4096, 16384, 136
+    A, B, bias = _ternary(M, N, K, "bf16", seed=91)
+    hA = torch.zeros(M, K + 40, dtype=torch.bfloat16).pin_memory()
+    hA[:, 8:8 + K] = A.cpu()
+    hB = torch.zeros(K, N + 24, dtype=torch.bfloat16).pin_memory()
+    hB[:, :N] = B.cpu()
+    hC = torch.full((M, N + 16), 7.0, dtype=torch.bfloat16).pin_memory()
+    out = hC[:, 16:]
+    fgemm.matmul(hA[:, 8:8 + K], hB[:, :N], out=out, epilogue="scale_bias", bias=bias.cpu())
+    assert np.array_equal(gpu_bits(out), _exact_reference(A, B, bias, "bf16"))
+    assert torch.all(hC[:, :16] == 7.0)
+
+
+@pytest.mark.parametrize("algo,tile_m,epilogue", [("classical", 256, "swiglu"),
+                                                  ("classical", 128, "silu"),
+                                                  ("winograd1", 256, "none")])
+def test_host_path_matches_the_device_path(algo, tile_m, epilogue, split_mode):
+    """Uniform inputs: the host call's row blocks run the device path's kernel
+    on the same rows; with the last-wave K split off every entry is summed in
+    the same order, so C is the same bit for bit."""
+    split_mode("off")
+    M, N, K = 8192, 16384, 1024
+    A = inputs.matrix(M, K, "uniform", "bf16", 92, DEV)
+    B = inputs.matrix(K, N, "uniform", "bf16", 93, DEV)
+    bias = inputs.matrix(1, N, "normal_0.02", "bf16", 94, DEV)[0] if epilogue != "none" else None
+    kw = dict(epilogue=epilogue, algo=algo, tile_m=tile_m, tile_n=256)
+    hC = fgemm.matmul(A.cpu().pin_memory(), B.cpu().pin_memory(),
+                      bias=None if bias is None else bias.cpu(), **kw)
+    # the device path on the same 2048-row blocks (the host call's blocks)
+    Cd = torch.empty(M, hC.shape[1], dtype=torch.bfloat16, device=DEV)
+    for i in range(0, M, 2048):
+        fgemm.matmul(A[i:i + 2048], B, out=Cd[i:i + 2048], bias=bias, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(hC.view(torch.int16), Cd.cpu().view(torch.int16))
+
+
+def test_host_path_rejects_bad_arguments():
+    hA = torch.zeros(64, 64, dtype=torch.bfloat16)
+    hB = torch.zeros(64, 64, dtype=torch.float16)
+    with pytest.raises(fgemm.FgemmError):
+        fgemm.matmul(hA, hB)
+    with pytest.raises(fgemm.FgemmError):
+        fgemm.matmul(hA, torch.zeros(32, 64, dtype=torch.bfloat16))
+    with pytest.raises(fgemm.FgemmError):
+        fgemm.matmul(hA, hA, out=torch.zeros(64, 32, dtype=torch.bfloat16))
