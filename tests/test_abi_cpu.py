@@ -554,3 +554,69 @@ def test_model_json_rejects_bad_files_and_keeps_the_model(L, tmp_path):
         fgemm.ERR_CALIBRATION
     assert L.fgemm_model_load_json(None, ctypes.byref(m)) == fgemm.ERR_INVALID_ARG
     assert _flat(m) == ref
+
+
+def test_model_in_kernel_formation_term(L):
+    """One Winograd level on CTA pairs: with at least 16 waves of its two
+    sum-free products the model charges the in-kernel formation (its drag,
+    and what outlasts the first three products) instead of the pre-pass;
+    Strassen's scheme, which has no sum-free product, keeps the pre-pass."""
+    m = _model(L)
+    m.eff_strassen_pair[1] = m.eff_pair[1] * 7.0 / 8.0  # products at the classical rate
+
+    def parts(n, algo):
+        s, t = _predict(L, m, n, n, n, algo, 256, tile_m=256)
+        assert s == fgemm.OK
+        return t
+
+    def with_formation(n, eff, drag):
+        m.form_in_kernel_eff, m.form_in_kernel_drag = eff, drag
+        return parts(n, "winograd1")
+
+    base_eff, base_drag = m.form_in_kernel_eff, m.form_in_kernel_drag
+    # 16384^3: 1024 positions on 76 pairs, 13 whole waves: 26 >= 16 -> in-kernel.
+    # A free, infinitely fast formation leaves the product time alone...
+    t_free = with_formation(16384, 1e9, 0.0)
+    # ...drag is charged on the formation's duration...
+    t_drag = with_formation(16384, 1e9 / 16384.0, 0.1)
+    assert t_drag > t_free
+    # ...and a slow formation shows once it outlasts three products' waves
+    t_slow = with_formation(16384, 0.01, 0.0)
+    assert t_slow > t_free + 1000.0
+    m.form_in_kernel_eff, m.form_in_kernel_drag = base_eff, base_drag
+    # Strassen at the same size is charged the pre-pass, which does not
+    # depend on the in-kernel formation's rate
+    ts1 = parts(16384, "strassen1")
+    m.form_in_kernel_eff = 1e-3
+    assert parts(16384, "strassen1") == ts1
+    m.form_in_kernel_eff = base_eff
+    # 8192^3: 3 whole waves (6 < 16): the pre-pass, whatever the in-kernel rate
+    tw = parts(8192, "winograd1")
+    m.form_in_kernel_eff = 1e-3
+    assert parts(8192, "winograd1") == tw
+
+
+def test_model_plan_margin_for_low_complexity_forms(L):
+    """AUTO takes a low-complexity form only when it beats the best classical
+    prediction by lcma_margin."""
+    m = _model(L)
+    a = ctypes.c_int()
+    tm, tn, us = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+
+    def pick():
+        assert L.fgemm_model_plan(ctypes.byref(m), 32768, 32768, 32768, 0, ctypes.byref(a),
+                                  ctypes.byref(tm), ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
+        return fgemm.ALGO_NAMES[a.value], us.value
+
+    _, tc = _predict(L, m, 32768, 32768, 32768, "classical", 256, tile_m=256)
+    # Winograd's pair products 5 % faster per MAC than the classical kernel's
+    m.eff_strassen_pair[1] = m.eff_pair[1] * 1.05
+    _, tw = _predict(L, m, 32768, 32768, 32768, "winograd1", 256, tile_m=256)
+    gain = 1.0 - tw / tc
+    assert gain > 0.03
+    m.lcma_margin = gain + 0.01          # not enough: classical stays
+    algo, t = pick()
+    assert algo == "classical" and abs(t - tc) < 1e-6 * tc
+    m.lcma_margin = gain - 0.01          # enough: the low-complexity form, its own prediction
+    algo, t = pick()
+    assert algo in ("winograd1", "strassen1") and t <= tw * (1 + 1e-9)
