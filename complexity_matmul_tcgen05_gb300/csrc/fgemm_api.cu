@@ -134,14 +134,17 @@ struct fgemm_handle_s {
   int split_mode = 1;                 // 0 never, 1 auto, 2 whenever possible
   int lcma_formation = 0;             // 0 auto, 1 pre-pass launch, 2 inside the product kernel
   unsigned int* form_ctr = nullptr;   // band counters of the in-kernel formation (3 words)
-  // fgemm_matmul_host: device copies of B, the bias and two slots each of A
-  // and C row blocks; an upload and a download stream; the events that
-  // order them with the handle's stream
+  // fgemm_matmul_host: two device slots each of B (with the bias), of A row
+  // blocks and of C row blocks; an upload and a download stream; the events
+  // that order them with the handle's stream; the host ranges of C the last
+  // two calls write, with the events that mark them written
   void* host_buf = nullptr;
   size_t host_bytes = 0;
   cudaStream_t up = nullptr, down = nullptr;
   cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_a[2] = {nullptr, nullptr}, ev_c[2] = {nullptr, nullptr},
-              ev_d[2] = {nullptr, nullptr};
+              ev_d[2] = {nullptr, nullptr}, ev_bfree[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr};
+  unsigned long long host_calls = 0, host_blocks = 0;
+  uintptr_t c_lo[2] = {0, 0}, c_hi[2] = {0, 0};
   unsigned long long spin_ns = 1000000000ull;
   fgemm_device_model_t model{};
   std::unordered_map<PlanKey, Plan, PlanKeyHash> plans;
@@ -716,7 +719,7 @@ fgemm_status_t fgemm_destroy(fgemm_handle_t h) {
   for (cudaStream_t st : {h->up, h->down})
     if (st) cudaStreamDestroy(st);
   for (cudaEvent_t ev : {h->ev_start, h->ev_b, h->ev_a[0], h->ev_a[1], h->ev_c[0], h->ev_c[1], h->ev_d[0],
-                         h->ev_d[1]})
+                         h->ev_d[1], h->ev_bfree[0], h->ev_bfree[1], h->ev_done[0], h->ev_done[1]})
     if (ev) cudaEventDestroy(ev);
   if (h->mx_buf) cudaFree(h->mx_buf);
   if (h->d_err) cudaFree(h->d_err);
@@ -949,18 +952,33 @@ fgemm_status_t fgemm_matmul_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
   return matmul_impl(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_m, tile_n, nullptr);
 }
 
+// Byte span [lo, hi) of a rows x cols matrix of 2-byte elements with row
+// pitch ld elements at p (empty when p is null or the matrix is).
+static void host_span(const void* p, int64_t rows, int64_t cols, int64_t ld, uintptr_t& lo, uintptr_t& hi) {
+  lo = hi = 0;
+  if (!p || rows <= 0 || cols <= 0) return;
+  lo = reinterpret_cast<uintptr_t>(p);
+  hi = lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 2);
+}
+
 // C = epi(alpha A B + bias) with A, B, C and the bias in host memory.  B (and
-// the bias) go up first; A is cut into row blocks that go up on the upload
-// stream while earlier blocks are multiplied on the handle's stream and their
-// C blocks come down on the download stream, two slots of each.  Everything
-// is ordered on the handle's stream when the call returns.
-fgemm_status_t fgemm_matmul_host(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
-                                 int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
-                                 fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
-                                 int32_t tile_m, int32_t tile_n) {
+// the bias) go up first into one of two device slots; A is cut into row
+// blocks that go up on the upload stream while earlier blocks are multiplied
+// on the handle's stream and their C blocks come down on the download
+// stream, two slots each of A and C.  Every slot is reused only after the
+// event that marks its last reader or writer done.  Everything is ordered on
+// the handle's stream when the call returns.  With FGEMM_HOST_OVERLAP the
+// uploads start without waiting for earlier work on the handle's stream
+// (only for the slots they reuse, and for the earlier calls whose C they
+// read), so they run under the previous call's products.
+fgemm_status_t fgemm_matmul_host_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                                    int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                                    fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                                    int32_t tile_m, int32_t tile_n, int32_t flags) {
   if (!h) return set_msg(nullptr, FGEMM_ERR_INVALID_ARG, "handle is NULL");
   if (dtype != FGEMM_F16 && dtype != FGEMM_BF16)
     return set_msg(h, FGEMM_ERR_INVALID_ARG, "dtype must be FGEMM_F16 or FGEMM_BF16");
+  if (flags & ~FGEMM_HOST_OVERLAP) return set_msg(h, FGEMM_ERR_INVALID_ARG, "unknown flags");
   if (M < 0 || N < 0 || K < 0) return set_msg(h, FGEMM_ERR_INVALID_ARG, "negative size");
   const int32_t kind = epi ? epi->kind : FGEMM_EPI_NONE;
   const int64_t n_out = kind == FGEMM_EPI_SWIGLU ? N / 2 : N;
@@ -986,12 +1004,14 @@ fgemm_status_t fgemm_matmul_host(fgemm_handle_t h, int64_t M, int64_t N, int64_t
   auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   // device row pitches: multiples of 8 elements (16 bytes), as the kernels need
   const int64_t pk = (std::max<int64_t>(K, 1) + 7) / 8 * 8, pn = (N + 7) / 8 * 8, po = (n_out + 7) / 8 * 8;
-  const size_t b_bytes = al(static_cast<size_t>(K) * pn * esz), bias_bytes = al(static_cast<size_t>(N) * esz);
+  const size_t b_bytes = al(static_cast<size_t>(K) * pn * esz) + al(static_cast<size_t>(N) * esz);
   const size_t a_bytes = al(static_cast<size_t>(mb) * pk * esz), c_bytes = al(static_cast<size_t>(mb) * po * esz);
-  const size_t need = b_bytes + bias_bytes + 2 * a_bytes + 2 * c_bytes;
+  const size_t need = 2 * (b_bytes + a_bytes + c_bytes);
   cudaError_t e = cudaSuccess;
   if (need > h->host_bytes) {
     e = cudaStreamSynchronize(h->stream);
+    for (cudaStream_t st : {h->up, h->down})
+      if (e == cudaSuccess && st) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
     if (h->host_buf) cudaFree(h->host_buf);
     h->host_buf = nullptr;
@@ -1007,20 +1027,39 @@ fgemm_status_t fgemm_matmul_host(fgemm_handle_t h, int64_t M, int64_t N, int64_t
     e = cudaStreamCreateWithFlags(&h->up, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->down, cudaStreamNonBlocking);
     for (cudaEvent_t* ev : {&h->ev_start, &h->ev_b, &h->ev_a[0], &h->ev_a[1], &h->ev_c[0], &h->ev_c[1],
-                            &h->ev_d[0], &h->ev_d[1]})
+                            &h->ev_d[0], &h->ev_d[1], &h->ev_bfree[0], &h->ev_bfree[1], &h->ev_done[0],
+                            &h->ev_done[1]})
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) return cuda_fail(h, e, "creating the host-call streams and events");
   }
+  const int bs = static_cast<int>(h->host_calls & 1u);  // this call's B slot
   uint8_t* base = static_cast<uint8_t*>(h->host_buf);
-  uint8_t* dB = base;
-  uint8_t* dbias = dB + b_bytes;
-  uint8_t* dA[2] = {dbias + bias_bytes, dbias + bias_bytes + a_bytes};
-  uint8_t* dC[2] = {dA[1] + a_bytes, dA[1] + a_bytes + c_bytes};
+  uint8_t* dB = base + bs * b_bytes;
+  uint8_t* dbias = dB + al(static_cast<size_t>(K) * pn * esz);
+  uint8_t* dA[2] = {base + 2 * b_bytes, base + 2 * b_bytes + a_bytes};
+  uint8_t* dC[2] = {base + 2 * b_bytes + 2 * a_bytes, base + 2 * b_bytes + 2 * a_bytes + c_bytes};
   fgemm_epilogue_t dev_epi{kind, epi ? epi->alpha : 1.0f, nullptr};
-  // the copy streams start after everything already on the handle's stream
-  e = cudaEventRecord(h->ev_start, h->stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->up, h->ev_start, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->down, h->ev_start, 0);
+  if (!(flags & FGEMM_HOST_OVERLAP)) {
+    // the uploads start after everything already on the handle's stream
+    e = cudaEventRecord(h->ev_start, h->stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->up, h->ev_start, 0);
+  } else {
+    // ... or only after the earlier calls (of the last two) whose C this
+    // call's inputs overlap have written it
+    uintptr_t lo[3], hi[3];
+    host_span(A, M, K, lda, lo[0], hi[0]);
+    host_span(B, K, N, ldb, lo[1], hi[1]);
+    host_span(epi ? epi->bias : nullptr, 1, N, N, lo[2], hi[2]);
+    for (int j = 0; j < 2 && e == cudaSuccess; ++j)
+      for (int t = 0; t < 3; ++t)
+        if (lo[t] < h->c_hi[j] && h->c_lo[j] < hi[t]) {
+          e = cudaStreamWaitEvent(h->up, h->ev_done[j], 0);
+          break;
+        }
+  }
+  // B (and the bias) into this call's slot once the products of the call
+  // that used the slot last are done
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->up, h->ev_bfree[bs], 0);
   if (e == cudaSuccess && K > 0)
     e = cudaMemcpy2DAsync(dB, static_cast<size_t>(pn) * esz, B, static_cast<size_t>(ldb) * esz,
                           static_cast<size_t>(N) * esz, static_cast<size_t>(K), cudaMemcpyHostToDevice, h->up);
@@ -1032,18 +1071,20 @@ fgemm_status_t fgemm_matmul_host(fgemm_handle_t h, int64_t M, int64_t N, int64_t
   if (e == cudaSuccess) e = cudaStreamWaitEvent(h->stream, h->ev_b, 0);
   if (e != cudaSuccess) return cuda_fail(h, e, "host-call upload of B");
   for (int64_t i = 0; i < nblocks; ++i) {
-    const int sl = static_cast<int>(i & 1);
+    // the slots alternate over all blocks of the handle's calls: a block
+    // uses the slot the previous block (of this or the last call) did not
+    const int sl = static_cast<int>(h->host_blocks++ & 1u);
     const uint8_t* Ai = static_cast<const uint8_t*>(A) + static_cast<size_t>(i * mb) * lda * esz;
     uint8_t* Ci = static_cast<uint8_t*>(C) + static_cast<size_t>(i * mb) * ldc * esz;
-    // A block i into its slot once block i - 2's product has read it
-    if (i >= 2) e = cudaStreamWaitEvent(h->up, h->ev_c[sl], 0);
+    // A block i into its slot once the last product that read the slot is done
+    e = cudaStreamWaitEvent(h->up, h->ev_c[sl], 0);
     if (e == cudaSuccess && K > 0)
       e = cudaMemcpy2DAsync(dA[sl], static_cast<size_t>(pk) * esz, Ai, static_cast<size_t>(lda) * esz,
                             static_cast<size_t>(K) * esz, static_cast<size_t>(mb), cudaMemcpyHostToDevice, h->up);
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_a[sl], h->up);
-    // the product, once A block i is up and C block i - 2 is down
+    // the product, once A block i is up and the slot's last C block is down
     if (e == cudaSuccess) e = cudaStreamWaitEvent(h->stream, h->ev_a[sl], 0);
-    if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(h->stream, h->ev_d[sl], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->stream, h->ev_d[sl], 0);
     if (e != cudaSuccess) return cuda_fail(h, e, "host-call upload of A");
     fgemm_status_t s = matmul_impl(h, mb, N, K, dA[sl], pk, dB, pn, dC[sl], po, dtype, &dev_epi, algo, tile_m,
                                    tile_n, nullptr);
@@ -1058,12 +1099,23 @@ fgemm_status_t fgemm_matmul_host(fgemm_handle_t h, int64_t M, int64_t N, int64_t
     if (e == cudaSuccess) e = cudaEventRecord(h->ev_d[sl], h->down);
     if (e != cudaSuccess) return cuda_fail(h, e, "host-call download of C");
   }
-  // the handle's stream ends after the last download
-  for (int sl = 0; sl < 2 && sl < nblocks; ++sl) {
-    e = cudaStreamWaitEvent(h->stream, h->ev_d[sl], 0);
-    if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamWaitEvent");
-  }
+  // B's slot is free once this call's products are done; C is written once
+  // the last download is done, and the handle's stream ends there
+  const int dj = static_cast<int>(h->host_calls & 1u);
+  e = cudaEventRecord(h->ev_bfree[bs], h->stream);
+  if (e == cudaSuccess) e = cudaEventRecord(h->ev_done[dj], h->down);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(h->stream, h->ev_done[dj], 0);
+  if (e != cudaSuccess) return cuda_fail(h, e, "host-call completion events");
+  host_span(C, M, n_out, ldc, h->c_lo[dj], h->c_hi[dj]);
+  ++h->host_calls;
   return FGEMM_OK;
+}
+
+fgemm_status_t fgemm_matmul_host(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,
+                                 int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                                 fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                                 int32_t tile_m, int32_t tile_n) {
+  return fgemm_matmul_host_ex(h, M, N, K, A, lda, B, ldb, C, ldc, dtype, epi, algo, tile_m, tile_n, 0);
 }
 
 fgemm_status_t fgemm_matmul_rms(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A,

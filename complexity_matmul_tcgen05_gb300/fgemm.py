@@ -98,6 +98,8 @@ def lib() -> ctypes.CDLL:
                                     ctypes.POINTER(ctypes.c_double)]
         L.fgemm_get_error.argtypes = [vp]
         L.fgemm_matmul_host.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, st, epi_p, st, i32, i32]
+        L.fgemm_matmul_host_ex.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, st, epi_p, st, i32,
+                                           i32, i32]
         L.fgemm_call_launches.argtypes = [vp, i64, i64, i64, epi_p, st, i32, i32, ctypes.POINTER(i32)]
         L.fgemm_selftest_wait_timeout.argtypes = [vp, i32]
         L.fgemm_calibrate.argtypes = [vp, ctypes.c_char_p]
@@ -147,7 +149,7 @@ def lib() -> ctypes.CDLL:
                      "fgemm_validate", "fgemm_model_predict", "fgemm_model_plan",
                      "fgemm_get_device_model", "fgemm_set_device_model",
                      "fgemm_strassen_matmul_static", "fgemm_selftest_wait_timeout",
-                     "fgemm_set_split_mode", "fgemm_set_lcma_formation", "fgemm_call_launches", "fgemm_matmul_host", "fgemm_matmul_rms", "fgemm_matmul_mx",
+                     "fgemm_set_split_mode", "fgemm_set_lcma_formation", "fgemm_call_launches", "fgemm_matmul_host", "fgemm_matmul_host_ex", "fgemm_matmul_rms", "fgemm_matmul_mx",
                      "fgemm_mx_to_bf16", "fgemm_strassen_static_get_error",
                      "fgemm_strassen_static_selftest_timeout"):
             getattr(L, name).restype = st
@@ -345,7 +347,7 @@ def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
            algo: str = "auto", tile_n: int = 0, tile_m: int = 0,
            handle: Handle | None = None, sumsq_out: torch.Tensor | None = None,
            sumsq_in: torch.Tensor | None = None, norm_width: int = 0,
-           rms_eps: float = 1e-6) -> torch.Tensor:
+           rms_eps: float = 1e-6, blocking: bool = True) -> torch.Tensor:
     """C = epi(alpha * A @ B + bias) through fgemm_matmul_ex.
 
     A is M x K, B is K x N (row-major), bias has N entries; for
@@ -355,9 +357,17 @@ def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
     [ceil(N_out/64), M]) receives each row's sums of squares of the stored
     outputs per 64-column block; ``sumsq_in`` (fp32 [parts, M], from an earlier
     call) scales accumulator row i by 1/sqrt(sum / norm_width + rms_eps).
+
+    A and B on the host (CPU tensors, pinned for overlapped copies): the
+    product goes through fgemm_matmul_host and ``out`` (or the returned
+    tensor) is on the host.  With ``blocking=False`` the call returns once it
+    is enqueued (fgemm_matmul_host_ex with FGEMM_HOST_OVERLAP: its uploads may
+    run under the previous host call's products); C is written once the
+    current CUDA stream has reached the call, and the inputs must not be
+    written by other work still pending on that stream.
     """
     if A.device.type == "cpu" and B.device.type == "cpu":
-        return _matmul_host(A, B, out, epilogue, alpha, bias, algo, tile_n, tile_m, handle)
+        return _matmul_host(A, B, out, epilogue, alpha, bias, algo, tile_n, tile_m, handle, blocking)
     _check_matrix(A, "A")
     _check_matrix(B, "B")
     if not (A.is_cuda and B.is_cuda):
@@ -411,9 +421,13 @@ def matmul(A: torch.Tensor, B: torch.Tensor, *, out: torch.Tensor | None = None,
     return out
 
 
-def _matmul_host(A, B, out, epilogue, alpha, bias, algo, tile_n, tile_m, handle):
-    """Host tensors through fgemm_matmul_host (pipelined copies; they overlap
-    when the tensors are pinned); returns once C is written."""
+HOST_OVERLAP = 1
+
+
+def _matmul_host(A, B, out, epilogue, alpha, bias, algo, tile_n, tile_m, handle, blocking=True):
+    """Host tensors through fgemm_matmul_host_ex (pipelined copies; they
+    overlap when the tensors are pinned); returns once C is written, or
+    (blocking=False) once the call is enqueued."""
     for t, name in ((A, "A"), (B, "B")):
         if t.dim() != 2 or t.stride(1) != 1:
             raise FgemmError(ERR_INVALID_ARG, f"{name} must be a 2-D tensor with unit column stride")
@@ -434,18 +448,21 @@ def _matmul_host(A, B, out, epilogue, alpha, bias, algo, tile_n, tile_m, handle)
     if bias is not None:
         if bias.device.type != "cpu" or bias.dtype != A.dtype or bias.numel() != N:
             raise FgemmError(ERR_INVALID_ARG, "bias must be a host vector of N entries, same dtype")
+        if not blocking and not bias.is_contiguous():
+            raise FgemmError(ERR_INVALID_ARG, "a non-blocking call needs a contiguous bias")
         bias = bias.contiguous()
         bias_ptr = bias.data_ptr()
     h = handle if handle is not None else default_handle()
     h.set_stream(torch.cuda.current_stream().cuda_stream)
     epi = make_epilogue(epilogue, alpha, bias_ptr)
-    s = lib().fgemm_matmul_host(h.ptr, M, N, K, A.data_ptr(), A.stride(0) if M > 1 else max(K, 1),
-                                B.data_ptr(), B.stride(0) if K > 1 else max(N, 1), out.data_ptr(),
-                                out.stride(0) if M > 1 else max(n_out, 1), dt, ctypes.byref(epi),
-                                ALGOS[algo], tile_m, tile_n)
+    s = lib().fgemm_matmul_host_ex(h.ptr, M, N, K, A.data_ptr(), A.stride(0) if M > 1 else max(K, 1),
+                                   B.data_ptr(), B.stride(0) if K > 1 else max(N, 1), out.data_ptr(),
+                                   out.stride(0) if M > 1 else max(n_out, 1), dt, ctypes.byref(epi),
+                                   ALGOS[algo], tile_m, tile_n, 0 if blocking else HOST_OVERLAP)
     _check(s, h.ptr)
-    torch.cuda.current_stream().synchronize()
-    _check(h.get_error(), h.ptr)
+    if blocking:
+        torch.cuda.current_stream().synchronize()
+        _check(h.get_error(), h.ptr)
     return out
 
 

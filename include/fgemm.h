@@ -208,15 +208,33 @@ typedef struct {
  * handle's stream reaches this point (cudaStreamSynchronize on it), and the
  * host buffers must stay valid until then. lda >= K, ldb >= N, ldc >= N_out
  * (any alignment). The device copies live in handle-owned buffers (grown on
- * demand; B, the bias, two A and two C row blocks). Errors as for
- * fgemm_matmul_ex, plus FGEMM_ERR_CUDA for a failed copy. RMSNorm statistics
- * are not offered here.
+ * demand; two slots each of B with the bias, of A row blocks and of C row
+ * blocks). Errors as for fgemm_matmul_ex, plus FGEMM_ERR_CUDA for a failed
+ * copy. RMSNorm statistics are not offered here.
  */
 fgemm_status_t fgemm_matmul_host(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
                                  const void* A, int64_t lda, const void* B, int64_t ldb,
                                  void* C, int64_t ldc, fgemm_dtype_t dtype,
                                  const fgemm_epilogue_t* epi, fgemm_algo_t algo,
                                  int32_t tile_m, int32_t tile_n);
+
+/*
+ * fgemm_matmul_host with flags. FGEMM_HOST_OVERLAP: the call's uploads do not
+ * wait for work already on the handle's stream, only for the device slots
+ * they reuse (two each of B, A blocks and C blocks, cycled over calls) and
+ * for the last two host calls on this handle whose C overlaps this call's A,
+ * B or bias; so the next call's uploads run under this call's products.
+ * The caller then guarantees that no other pending work on the handle's
+ * stream writes this call's host inputs. C is still written when the
+ * handle's stream reaches the point after the call. Unknown flags ->
+ * FGEMM_ERR_INVALID_ARG.
+ */
+#define FGEMM_HOST_OVERLAP 1
+fgemm_status_t fgemm_matmul_host_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                    const void* A, int64_t lda, const void* B, int64_t ldb,
+                                    void* C, int64_t ldc, fgemm_dtype_t dtype,
+                                    const fgemm_epilogue_t* epi, fgemm_algo_t algo,
+                                    int32_t tile_m, int32_t tile_n, int32_t flags);
 
 /*
  * As fgemm_matmul_ex, with RMSNorm statistics (rms may be NULL). Classical

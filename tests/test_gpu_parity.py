@@ -978,3 +978,43 @@ def test_host_path_rejects_bad_arguments():
         fgemm.matmul(hA, torch.zeros(32, 64, dtype=torch.bfloat16))
     with pytest.raises(fgemm.FgemmError):
         fgemm.matmul(hA, hA, out=torch.zeros(64, 32, dtype=torch.bfloat16))
+
+
+def test_host_overlap_chained_calls_wait_for_their_inputs():
+    """Non-blocking host calls whose input is an earlier call's output: the
+    second call's upload waits for the first call's C to be on the host
+    (ternary inputs keep C1 exact, so C2 = RNE(C1 B2) bit for bit)."""
+    M, N, K = 8192, 2048, 64
+    A, B, _ = _ternary(M, N, K, "bf16", seed=95)
+    B2 = inputs.matrix(N, 512, "ternary", "bf16", 96, DEV)
+    hA, hB, hB2 = A.cpu().pin_memory(), B.cpu().pin_memory(), B2.cpu().pin_memory()
+    hC1 = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    hC2 = torch.empty(M, 512, dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        hC1.view(torch.int16).fill_(0x7F7B)
+        fgemm.matmul(hA, hB, out=hC1, blocking=False)
+        fgemm.matmul(hC1, hB2, out=hC2, blocking=False)
+        torch.cuda.current_stream().synchronize()
+        assert fgemm.default_handle().get_error() == fgemm.OK
+        zero = torch.zeros(N, dtype=torch.bfloat16, device=DEV)
+        assert np.array_equal(gpu_bits(hC1), _exact_reference(A, B, zero, "bf16"))
+        C1 = hC1.to(DEV)
+        assert np.array_equal(gpu_bits(hC2), _exact_reference(C1, B2, zero[:512], "bf16"))
+
+
+def test_host_overlap_back_to_back_calls():
+    """Six non-blocking host calls in a row over the handle's two slots of B,
+    A blocks and C blocks (different inputs and outputs each): every C is the
+    exact product."""
+    M, N, K = 4096, 16384, 256
+    calls = []
+    for j in range(6):
+        A, B, bias = _ternary(M, N, K, "bf16", seed=100 + 3 * j)
+        calls.append((A, B, bias, A.cpu().pin_memory(), B.cpu().pin_memory(), bias.cpu().pin_memory(),
+                      torch.empty(M, N, dtype=torch.bfloat16).pin_memory()))
+    for (_, _, _, hA, hB, hbias, hC) in calls:
+        fgemm.matmul(hA, hB, out=hC, epilogue="scale_bias", bias=hbias, blocking=False)
+    torch.cuda.current_stream().synchronize()
+    assert fgemm.default_handle().get_error() == fgemm.OK
+    for (A, B, bias, _, _, _, hC) in calls:
+        assert np.array_equal(gpu_bits(hC), _exact_reference(A, B, bias, "bf16"))
