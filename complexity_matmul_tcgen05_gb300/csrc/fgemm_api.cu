@@ -139,7 +139,7 @@ struct fgemm_handle_s {
   // that order them with the handle's stream; the host ranges of C the last
   // two calls write, with the events that mark them written
   void* host_buf = nullptr;
-  size_t host_bytes = 0;
+  size_t host_cap_b = 0, host_cap_a = 0, host_cap_c = 0;  // bytes of one slot of each kind
   cudaStream_t up = nullptr, down = nullptr;
   cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_a[2] = {nullptr, nullptr}, ev_c[2] = {nullptr, nullptr},
               ev_d[2] = {nullptr, nullptr}, ev_bfree[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr};
@@ -1006,22 +1006,26 @@ fgemm_status_t fgemm_matmul_host_ex(fgemm_handle_t h, int64_t M, int64_t N, int6
   const int64_t pk = (std::max<int64_t>(K, 1) + 7) / 8 * 8, pn = (N + 7) / 8 * 8, po = (n_out + 7) / 8 * 8;
   const size_t b_bytes = al(static_cast<size_t>(K) * pn * esz) + al(static_cast<size_t>(N) * esz);
   const size_t a_bytes = al(static_cast<size_t>(mb) * pk * esz), c_bytes = al(static_cast<size_t>(mb) * po * esz);
-  const size_t need = 2 * (b_bytes + a_bytes + c_bytes);
+  // The slots keep fixed places (their capacities) from call to call, since
+  // earlier calls may still be using theirs; they grow, after everything in
+  // flight is done, only when a call needs more.
   cudaError_t e = cudaSuccess;
-  if (need > h->host_bytes) {
+  if (!h->host_buf || b_bytes > h->host_cap_b || a_bytes > h->host_cap_a || c_bytes > h->host_cap_c) {
     e = cudaStreamSynchronize(h->stream);
     for (cudaStream_t st : {h->up, h->down})
       if (e == cudaSuccess && st) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
     if (h->host_buf) cudaFree(h->host_buf);
     h->host_buf = nullptr;
-    h->host_bytes = 0;
-    e = cudaMalloc(&h->host_buf, need);
+    h->host_cap_b = std::max(h->host_cap_b, b_bytes);
+    h->host_cap_a = std::max(h->host_cap_a, a_bytes);
+    h->host_cap_c = std::max(h->host_cap_c, c_bytes);
+    e = cudaMalloc(&h->host_buf, 2 * (h->host_cap_b + h->host_cap_a + h->host_cap_c));
     if (e != cudaSuccess) {
       h->host_buf = nullptr;
+      h->host_cap_b = h->host_cap_a = h->host_cap_c = 0;
       return cuda_fail(h, e, "cudaMalloc(host-call buffers)");
     }
-    h->host_bytes = need;
   }
   if (!h->up) {
     e = cudaStreamCreateWithFlags(&h->up, cudaStreamNonBlocking);
@@ -1034,10 +1038,11 @@ fgemm_status_t fgemm_matmul_host_ex(fgemm_handle_t h, int64_t M, int64_t N, int6
   }
   const int bs = static_cast<int>(h->host_calls & 1u);  // this call's B slot
   uint8_t* base = static_cast<uint8_t*>(h->host_buf);
-  uint8_t* dB = base + bs * b_bytes;
+  const size_t cb = h->host_cap_b, ca = h->host_cap_a, cc = h->host_cap_c;
+  uint8_t* dB = base + bs * cb;
   uint8_t* dbias = dB + al(static_cast<size_t>(K) * pn * esz);
-  uint8_t* dA[2] = {base + 2 * b_bytes, base + 2 * b_bytes + a_bytes};
-  uint8_t* dC[2] = {base + 2 * b_bytes + 2 * a_bytes, base + 2 * b_bytes + 2 * a_bytes + c_bytes};
+  uint8_t* dA[2] = {base + 2 * cb, base + 2 * cb + ca};
+  uint8_t* dC[2] = {base + 2 * cb + 2 * ca, base + 2 * cb + 2 * ca + cc};
   fgemm_epilogue_t dev_epi{kind, epi ? epi->alpha : 1.0f, nullptr};
   if (!(flags & FGEMM_HOST_OVERLAP)) {
     // the uploads start after everything already on the handle's stream

@@ -38,7 +38,7 @@ struct PairCfg {
   static constexpr int kSmemBytes = 1024 + kStagingOff + kSlackBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(2 * BN <= kTmemCols, "two accumulator buffers must fit in TMEM");
-  static_assert((2 * kStages + 5) * 8 + 4 <= kBarBytes, "barrier area too small");
+  static_assert((2 * kStages + 6) * 8 + 4 <= kBarBytes, "barrier area too small");
   static_assert(kStageBytes >= 4096, "the last tile's second half stages in the pipeline buffers");
 };
 
@@ -155,12 +155,18 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
   const uint32_t sA0 = base;
   const uint32_t sB0 = base + S * PC::kABytes;
   const uint32_t bar0 = base + S * PC::kStageBytes;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + S * PC::kStageBytes + 8 * (2 * S + 5));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + S * PC::kStageBytes + 8 * (2 * S + 6));
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (S + s); };
   auto tfull = [&](uint32_t b) { return bar0 + 8u * (2 * S + b); };
   auto tempty = [&](uint32_t b) { return bar0 + 8u * (2 * S + 2 + b); };
   const uint32_t drain = bar0 + 8u * (2 * S + 4);
+  // completes (once per launch, in both CTAs) when every MMA of the pair's
+  // last work item is done: what the warps helping with the last tile wait
+  // for.  A parity wait on tfull could not serve them: with short K they get
+  // there while that barrier is still two phases behind, and a parity wait
+  // that far back returns at once.
+  const uint32_t lastfull = bar0 + 8u * (2 * S + 5);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -180,6 +186,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
       ptx::mbar_init(tempty(b), 8);
     }
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(lastfull, 1);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -280,6 +287,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
         }
         if (ok) ptx::mma_commit_pair(tfull(buf), 0x3);
       }
+      if (ok && n_items > 0) ptx::mma_commit_pair(lastfull, 0x3);
       ptx::mma_commit_pair(drain, 0x1);
       wait_bounded(drain, 0, p, err_code(1), false);
     }
@@ -332,8 +340,8 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair(const __grid_constan
     work_item(p.num_units, p.split_tiles, p.split_pieces, nclusters, p.k_blocks, cluster, n_items - 1, w);
     if (w.npieces == 1) {
       const uint32_t it = static_cast<uint32_t>(n_items - 1);
-      const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
-      if (wait_warp(tfull(buf), aph, p, 2)) {
+      const uint32_t buf = it & 1u;
+      if (wait_warp(lastfull, 0, p, 2)) {
         ptx::tc_fence_after();
         int tm, tn;
         unit_coords(p, w.unit, tm, tn);

@@ -246,6 +246,22 @@ def test_winograd_formed_in_kernel_graph_replay(formation):
     assert torch.equal(C.view(torch.int16), run(A, B2, **kw).view(torch.int16))
 
 
+@pytest.mark.parametrize("M,N,K,tile", [
+    (8192, 2048, 64, 256), (8192, 2048, 64, 128), (8192, 4096, 64, 256), (8192, 2048, 128, 256),
+    (16384, 4096, 64, 256), (8192, 2048, 192, 256),
+])
+def test_exact_ternary_cta_pair_short_k_many_tiles(M, N, K, tile):
+    """One or two K blocks and three to fourteen tiles per pair: the warps
+    that help with a pair's last tile get there while the MMAs of its earlier
+    tiles still run (they must wait for the last tile itself); five launches
+    in a row, each bit for bit."""
+    A, B, bias = _ternary(M, N, K, "bf16", seed=110)
+    ref = _exact_reference(A, B, bias, "bf16")
+    for _ in range(5):
+        C = run(A, B, algo="classical", epilogue="scale_bias", bias=bias, tile_n=tile, tile_m=256)
+        assert np.array_equal(gpu_bits(C), ref)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("M,N,K,tile", EXACT_PAIR_CASES)
 def test_exact_ternary_cta_pair(M, N, K, tile, dtype):
@@ -1002,13 +1018,19 @@ def test_host_overlap_chained_calls_wait_for_their_inputs():
         assert np.array_equal(gpu_bits(hC2), _exact_reference(C1, B2, zero[:512], "bf16"))
 
 
-def test_host_overlap_back_to_back_calls():
+@pytest.mark.parametrize("shapes", [
+    [(4096, 16384, 256)] * 6,
+    # shapes that change from call to call (the slots keep their places while
+    # earlier calls still use them), and a larger one that makes them grow
+    [(4096, 16384, 256), (8192, 2048, 64), (512, 4096, 1024), (4096, 16384, 256), (8192, 2048, 64),
+     (8192, 16384, 512)],
+], ids=["same", "mixed"])
+def test_host_overlap_back_to_back_calls(shapes):
     """Six non-blocking host calls in a row over the handle's two slots of B,
     A blocks and C blocks (different inputs and outputs each): every C is the
     exact product."""
-    M, N, K = 4096, 16384, 256
     calls = []
-    for j in range(6):
+    for j, (M, N, K) in enumerate(shapes):
         A, B, bias = _ternary(M, N, K, "bf16", seed=100 + 3 * j)
         calls.append((A, B, bias, A.cpu().pin_memory(), B.cpu().pin_memory(), bias.cpu().pin_memory(),
                       torch.empty(M, N, dtype=torch.bfloat16).pin_memory()))
