@@ -78,7 +78,8 @@ def test_exact_ternary(algo, M, N, K, tile, dtype):
 # 2048^2 at 256 has 16 (112 units over 76 pairs); 4096 x 4096 x 512 has 64
 # (448 units: about 6 per pair, positions shared at every range boundary).
 LCMA_PAIR_CASES = [(512, 512, 128, 128), (512, 1024, 256, 256), (1024, 2048, 640, 256),
-                   (1536, 768, 384, 128), (2048, 2048, 256, 256), (4096, 4096, 512, 256)]
+                   (1536, 768, 384, 128), (2048, 2048, 256, 256), (4096, 4096, 512, 256),
+                   (8192, 8192, 128, 256)]  # one K block per product, 3 whole waves per pair
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
