@@ -99,23 +99,6 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
   return v;
 }
 
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
-// from this CTA's shared memory to global memory, in the thread's current
-// bulk async-group.
-__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-               ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-
-// As bulk_store, but each fp32 element is added to the one in global memory
-// (an atomic reduction performed at the L2), in the current bulk async-group.
-__device__ __forceinline__ void bulk_reduce_add_f32(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
-               ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-
 // ---------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
