@@ -2,32 +2,35 @@
 // scheme) on CTA pairs, with the summed operands streamed through HBM
 // (FalconGEMM summary, "Methodology" items 1 and 3).
 //
-// Two launches:
-//  1. lcma_form_kernel forms every summed operand of the scheme once from the
-//     2 x 2 blocks of A and B (e.g. A11 + A22, B12 - B22): each element is the
-//     fp32 sum of the exact 16-bit inputs, rounded once to the input type,
-//     written to handle-owned temporaries.  It reads A and B once and writes
-//     each temporary once: a streaming, HBM-bound kernel.
+// Two steps:
+//  1. Every summed operand of the scheme is formed once from the 2 x 2 blocks
+//     of A and B (e.g. A11 + A22, B12 - B22): each element is the fp32 sum of
+//     the exact 16-bit inputs, rounded once to the input type, written to
+//     handle-owned temporaries, A and B read once and each temporary written
+//     once.  Either lcma_form_kernel does it as a streaming launch before the
+//     products, or, for a scheme whose first products read only blocks of A
+//     and B (Winograd's A11 B11 and A12 B21), the product kernel's idle warps
+//     do it while those run (lcma_form_bands).
 //  2. fgemm_kernel_pair_lcma runs the seven block products in one persistent
 //     launch on CTA pairs: 256 x BN tiles of the half-size block space, on
 //     the classical pair mainloop (TMA -> 128-byte-swizzled shared-memory ring
 //     -> tcgen05.mma cta_group::2 -> double-buffered TMEM), so the tensor
 //     pipe sees the same operand stream as a classical product.  Each pair
-//     runs whole output positions in waves (all seven products of one
-//     position, the pairs in step on the same product, so neighbouring
-//     positions share its operand panels in the L2).  The epilogue warps
+//     runs whole output positions product by product (product 1 of all its
+//     positions, then product 2, ...; the pairs in step on the same product,
+//     so neighbouring positions share its operand panels in the L2, and
+//     consecutive waves reuse them).  The epilogue warps
 //     fold each product's accumulator into per-CTA fp32 partial tiles of the
 //     output blocks it feeds (C11 = M1 + M4 - M5 + M7, ...): the first
 //     contribution to a block is stored, the next ones are added by vector
 //     atomic reductions performed at the L2 (no load latency in the fold),
 //     and at a block's last contribution the epilogue reads the partial,
 //     adds the accumulator, applies alpha / bias / activation and stores C.
-//     The
-//     partial last wave's positions run as separate (product, position)
+//     The partial last wave's positions run as separate (product, position)
 //     units shared out evenly over the pairs: each stores its accumulator,
 //     and the last of a position's seven to finish (a generation-tagged
-//     counter) combines them in product order, so the result does not
-//     depend on timing.
+//     counter) has them combined in product order, by the idle warps, so the
+//     result does not depend on timing.
 //
 // Why the sums go through HBM on this chip: the classical 256 x 256 pair
 // mainloop already keeps the shared-memory port and the tensor pipe near
