@@ -369,28 +369,49 @@ fgemm_status_t prepare_split(fgemm_handle_t h, KernelParams* p, int split, int p
 // (formed by one pre-pass launch), the product kernel reads every operand
 // through a tensor map of A, B or the temporaries.  Workspace layout: the
 // product kernel's partial tiles, then the A and the B temporaries.
-// The scheme's leading products whose operands are both raw blocks of A and
-// B (a single positive term each): Winograd's A11 B11 and A12 B21, none of
-// Strassen's.
-int lcma_lead_products(const StrassenTable& tab) {
-  auto raw = [](int n, const uint8_t* c) { return n == 1 && !(c[0] & fgemm::kTermNeg); };
-  int lead = 0;
-  while (lead < fgemm::kLcmaProducts && raw(tab.na[lead], tab.a[lead]) && raw(tab.nb[lead], tab.b[lead])) ++lead;
-  return lead;
+// Whether product k of the table reads a sum of A's blocks (bit 0) and of
+// B's (bit 1); a single positive term is a raw block, read in place.
+int lcma_needs(const StrassenTable& tab, int k) {
+  auto sum = [](int n, const uint8_t* c) { return !(n == 1 && !(c[0] & fgemm::kTermNeg)); };
+  return (sum(tab.na[k], tab.a[k]) ? 1 : 0) | (sum(tab.nb[k], tab.b[k]) ? 2 : 0);
 }
 
-// Whether a one-level pair launch forms its summed operands inside the
-// product kernel: the scheme has leading products without sums, the
-// matrices cut into whole formation bands, and the handle asks for it (mode
-// 2) or leaves it to the rule (mode 0: those products span at least
-// kFusedMinWaves waves of the `clusters` pairs over `positions`).
-bool lcma_forms_in_kernel(fgemm_handle_t h, const StrassenTable& tab, long long positions, int clusters,
-                          int sub_m, int sub_k) {
-  const int lead = lcma_lead_products(tab);
+// The order in which the pair kernel runs a scheme's products (and folds
+// them): those that read no sum first, then those that read sums of A only,
+// then of B only, then of both, each group in table order.  Winograd's
+// stays as it is (A11 B11, A12 B21 first); Strassen's becomes M2, M5, M3,
+// M4, M1, M6, M7.  The order is the same whoever forms the sums, so the
+// result is too.
+void lcma_order(const StrassenTable& tab, int (&order)[fgemm::kLcmaProducts]) {
+  int n = 0;
+  for (int key = 0; key < 4; ++key)
+    for (int k = 0; k < fgemm::kLcmaProducts; ++k)
+      if (lcma_needs(tab, k) == key) order[n++] = k;
+}
+
+// Which sides' sums the product kernel forms itself (bit 0: A's, bit 1:
+// B's; the pre-pass forms the others), and how many products run before the
+// first that reads one of them (*lead).  Both sides when the scheme has
+// products that read no sum (Winograd), else B's side alone when it has
+// products that read no sum of B (Strassen: M2 and M5).  Mode 2 of the
+// handle asks for it whenever possible, mode 0 (auto) when those products
+// span at least kFusedMinWaves waves; the matrices must cut into whole
+// formation bands.
+int lcma_formation_plan(fgemm_handle_t h, const StrassenTable& tab, long long positions, int clusters, int sub_m,
+                        int sub_k, int* lead) {
+  int order[fgemm::kLcmaProducts];
+  lcma_order(tab, order);
+  int none = 0, no_b = 0;
+  while (none < fgemm::kLcmaProducts && lcma_needs(tab, order[none]) == 0) ++none;
+  while (no_b < fgemm::kLcmaProducts && !(lcma_needs(tab, order[no_b]) & 2)) ++no_b;
+  const int mask = none > 0 ? 3 : (no_b > 0 ? 2 : 0);
+  const int ld = none > 0 ? none : no_b;
+  if (lead) *lead = ld;
   const long long whole = positions / std::max(clusters, 1);
   const bool whole_bands = sub_m % fgemm::kFormRows == 0 && sub_k % fgemm::kFormRows == 0;
-  return lead > 0 && whole_bands &&
-         (h->lcma_formation == 2 || (h->lcma_formation == 0 && lead * whole >= fgemm::kFusedMinWaves));
+  if (mask == 0 || !whole_bands || h->lcma_formation == 1) return 0;
+  if (h->lcma_formation == 2 || ld * whole >= fgemm::kFusedMinWaves) return mask;
+  return 0;
 }
 
 fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTable& tab, int bn,
@@ -425,14 +446,19 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
     *is_temp = 1;
     *idx = static_cast<uint8_t>(t);
   };
+  // the products in the kernel's order (lcma_order): L.prod[pr] is table
+  // product order[pr]
+  int order[fgemm::kLcmaProducts];
+  lcma_order(tab, order);
   int first_of[4] = {-1, -1, -1, -1}, last_of[4] = {-1, -1, -1, -1};  // product per output block
   for (int pr = 0; pr < np; ++pr) {
     fgemm::LcmaProduct& P = L.prod[pr];
-    operand(tab.na[pr], tab.a[pr], F.job[0], &P.a_temp, &P.a_idx);
-    operand(tab.nb[pr], tab.b[pr], F.job[1], &P.b_temp, &P.b_idx);
-    P.nc = tab.nc[pr];
+    const int k = order[pr];
+    operand(tab.na[k], tab.a[k], F.job[0], &P.a_temp, &P.a_idx);
+    operand(tab.nb[k], tab.b[k], F.job[1], &P.b_temp, &P.b_idx);
+    P.nc = tab.nc[k];
     for (int t = 0; t < P.nc; ++t) {
-      P.c[t] = static_cast<uint8_t>(tab.c[pr][t] & (fgemm::kTermIndexMask | fgemm::kTermNeg));
+      P.c[t] = static_cast<uint8_t>(tab.c[k][t] & (fgemm::kTermIndexMask | fgemm::kTermNeg));
       const int blk = P.c[t] & fgemm::kTermIndexMask;
       if (first_of[blk] < 0) first_of[blk] = pr;
       last_of[blk] = pr;
@@ -526,20 +552,28 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   F.job[1].dst = TB;
   F.job[1].rows = p.sub_k;
   F.job[1].cols = p.sub_n;
-  // Where the operands are formed: by the pre-pass launch, or inside the
-  // product kernel while the scheme's leading products that read only blocks
-  // of A and B run (their waves must cover the formation: auto asks for at
-  // least kFusedMinWaves of them).
-  const int lead = lcma_lead_products(tab);
-  const bool fused = lcma_forms_in_kernel(h, tab, positions, clusters, p.sub_m, p.sub_k);
+  // Where the operands are formed: each side by the pre-pass launch, or
+  // inside the product kernel while the leading products that do not read
+  // that side's sums run (lcma_formation_plan).
+  int lead = 0;
+  const int mask = lcma_formation_plan(h, tab, positions, clusters, p.sub_m, p.sub_k, &lead);
+  const bool fused = mask != 0;
   // A pair's tail units (positions of the partial last wave, one product
   // each) run after its whole positions' first tail_at products, so that the
   // combinations of their accumulators overlap the MMAs of the products that
-  // follow: first thing with the pre-pass, after two more products than the
-  // sum-free ones when this kernel forms the temporaries (then they are
-  // stored by the time the tail units read them).
+  // follow: first thing when the pre-pass formed every sum, else after two
+  // more products than those that read no sum the kernel forms (then they
+  // are stored by the time the tail units read them).
   L.tail_at = fused ? std::min(lead + 2, np) : 0;
   cudaError_t e = cudaSuccess;
+  // the pre-pass forms the sides the product kernel does not
+  LcmaFormParams pre = F;
+  for (int j = 0; j < 2; ++j)
+    if ((mask >> j) & 1) pre.job[j].ntemp = 0;
+  if (pre.job[0].ntemp > 0 || pre.job[1].ntemp > 0) {
+    e = fgemm::launch_lcma_form(pre, h->num_sms, h->stream);
+    if (e != cudaSuccess) return cuda_fail(h, e, "operand-sum pre-pass launch");
+  }
   if (fused) {
     if (!h->form_ctr) {
       e = cudaMalloc(&h->form_ctr, 4 * sizeof(unsigned int));
@@ -553,10 +587,7 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
     L.form = F;
     L.form_ctr = h->form_ctr;
     for (int j = 0; j < 2; ++j)
-      L.form_tasks[j] = F.job[j].ntemp > 0 ? F.job[j].rows / fgemm::kFormRows : 0;
-  } else {
-    e = fgemm::launch_lcma_form(F, h->num_sms, h->stream);
-    if (e != cudaSuccess) return cuda_fail(h, e, "operand-sum pre-pass launch");
+      L.form_tasks[j] = ((mask >> j) & 1) && F.job[j].ntemp > 0 ? F.job[j].rows / fgemm::kFormRows : 0;
   }
   e = fgemm::launch_lcma_pair(bn, L, clusters, h->stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "Strassen pair kernel launch");
@@ -818,7 +849,8 @@ fgemm_status_t fgemm_call_launches(fgemm_handle_t h, int64_t M, int64_t N, int64
     const int clusters = static_cast<int>(std::min<long long>(fit, positions * fgemm::kLcmaProducts));
     const StrassenTable& tab =
         p.algo == FGEMM_ALGO_WINOGRAD1 ? fgemm::winograd_table() : fgemm::strassen_table(1);
-    if (!lcma_forms_in_kernel(h, tab, positions, clusters, sub_m, sub_k)) *launches = 2;
+    // the pre-pass runs unless the product kernel forms both sides' sums
+    if (lcma_formation_plan(h, tab, positions, clusters, sub_m, sub_k, nullptr) != 3) *launches = 2;
   }
   return FGEMM_OK;
 }

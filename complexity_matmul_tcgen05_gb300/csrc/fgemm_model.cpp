@@ -326,17 +326,28 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     const double pair_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms * 2.0;
     const double k_pad = static_cast<double>(ceil_div(sub_k, fgemm::kBK) * fgemm::kBK);
     const double t_unit = 2.0 * 256.0 * tile_n * k_pad / (pair_flop_per_us * eff);
-    // Winograd's first two products read only blocks of A and B: with at
-    // least kFusedMinWaves waves of them the kernel forms the sums itself (A's, then
-    // B's) while they run, and the pre-pass launch goes.  What shows is the
-    // products' drag during the formation, and any part of it still running
-    // when the first product that reads B's sums (the fourth) starts.
-    const int64_t lead = wino ? 2 : 0;
-    if (lead > 0 && lead * whole >= fgemm::kFusedMinWaves && sub_m % fgemm::kFormRows == 0 && sub_k % fgemm::kFormRows == 0) {
-      const double t_form = pre_bytes / (dev->hbm_gbs * 1e3 * std::max(dev->form_in_kernel_eff, 1e-3));
+    // The product kernel forms sums itself while the products that do not
+    // read them run first: Winograd's two sum-free products (A11 B11, A12 B21)
+    // cover both sides' sums, formed A's then B's; Strassen's M2 and M5 read
+    // no sum of B, so B's sums are formed in the kernel and A's by a pre-pass
+    // half the size.  With at least kFusedMinWaves waves of those products
+    // this is done; what shows is the products' drag during the formation,
+    // and any part of it still running when the first product that reads
+    // the last side formed starts.
+    const int64_t lead = 2;
+    if (lead * whole >= fgemm::kFusedMinWaves && sub_m % fgemm::kFormRows == 0 &&
+        sub_k % fgemm::kFormRows == 0) {
+      const double a_bytes = 2.0 * (static_cast<double>(M) * K + temps * static_cast<double>(sub_m) * sub_k);
+      const double b_bytes = 2.0 * (static_cast<double>(K) * N + temps * static_cast<double>(sub_k) * sub_n);
+      const double in_kernel = wino ? a_bytes + b_bytes : b_bytes;
+      const double t_form = in_kernel / (dev->hbm_gbs * 1e3 * std::max(dev->form_in_kernel_eff, 1e-3));
       const double drag = std::max(dev->form_in_kernel_drag, 0.0);
       const double w = static_cast<double>(whole) * t_unit;
-      t_pre = drag * t_form + std::max(0.0, t_form - (1.0 + drag) * static_cast<double>(lead + 1) * w);
+      // the first product that needs the in-kernel side's (last) sums
+      const double needed_at = static_cast<double>(wino ? lead + 1 : lead) * w;
+      t_pre = drag * t_form + std::max(0.0, t_form - (1.0 + drag) * needed_at);
+      if (!wino)  // A's sums by the pre-pass
+        t_pre += a_bytes / (dev->hbm_gbs * 1e3 * std::max(dev->hbm_stream_eff, 1e-3)) + dev->launch_us;
     }
     const double per_pair = static_cast<double>(whole * 7 + ceil_div(tail_units, used));
     const double t_compute = per_pair * t_unit + dev->tile_fill_us * (tail_units > 0 ? 2.0 : 1.0);

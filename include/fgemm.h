@@ -616,11 +616,12 @@ fgemm_status_t fgemm_set_split_mode(fgemm_handle_t h, int32_t mode);
  * 256) form their summed operands (FalconGEMM summary, "Methodology" item 3:
  * the operand sums of the low-complexity scheme): 1 a streaming pre-pass
  * launch before the product kernel; 2 inside the product kernel, by its two
- * otherwise idle warps per CTA, while the scheme's leading products that
- * read only blocks of A and B run (Winograd's A11 B11 and A12 B21; a scheme
- * without such products, like Strassen's, always uses the pre-pass); 0 auto
- * (the default): inside the product kernel when those products span at
- * least 16 waves of the launch, else the pre-pass.  The result is the same
+ * otherwise idle warps per CTA, while the products that do not read those
+ * sums run first: both sides' sums for Winograd's scheme (its A11 B11 and
+ * A12 B21 read none), B's for Strassen's (its M2 and M5 read no sum of B;
+ * A's then come from a pre-pass of half the size); 0 auto (the default):
+ * mode 2 when those products span at least 16 waves of the launch, else
+ * mode 1.  The result is the same
  * bit for bit in every mode.  Returns FGEMM_ERR_INVALID_ARG for other modes.
  */
 fgemm_status_t fgemm_set_lcma_formation(fgemm_handle_t h, int32_t mode);

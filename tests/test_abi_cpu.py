@@ -584,12 +584,16 @@ def test_model_in_kernel_formation_term(L):
     t_slow = with_formation(16384, 0.01, 0.0)
     assert t_slow > t_free + 1000.0
     m.form_in_kernel_eff, m.form_in_kernel_drag = base_eff, base_drag
-    # Strassen at the same size is charged the pre-pass, which does not
-    # depend on the in-kernel formation's rate
-    ts1 = parts(16384, "strassen1")
-    m.form_in_kernel_eff = 1e-3
-    assert parts(16384, "strassen1") == ts1
-    m.form_in_kernel_eff = base_eff
+    # Strassen at the same size: B's sums in the kernel (its M2 and M5 read
+    # none), A's by a pre-pass half the full one; so even a free in-kernel
+    # formation leaves the half pre-pass, and a slow one shows
+    m.form_in_kernel_eff, m.form_in_kernel_drag = 1e9, 0.0
+    ts_free = parts(16384, "strassen1")
+    tw_free = parts(16384, "winograd1")
+    assert ts_free > tw_free + 50.0   # the A-side pre-pass (1.15 GB at 16384^3)
+    m.form_in_kernel_eff = 0.01
+    assert parts(16384, "strassen1") > ts_free + 1000.0
+    m.form_in_kernel_eff, m.form_in_kernel_drag = base_eff, base_drag
     # 8192^3: 3 whole waves (6 < 16): the pre-pass, whatever the in-kernel rate
     tw = parts(8192, "winograd1")
     m.form_in_kernel_eff = 1e-3

@@ -181,10 +181,11 @@ def test_exact_ternary_winograd_formed_in_kernel(M, N, K, tile, dtype, formation
     (1536, 768, 384, 128, "scale_bias"),
 ])
 def test_lcma_formation_modes_give_the_same_bits(M, N, K, tile, epilogue, algo, formation):
-    """The temporaries hold the same values whoever forms them, so the
-    pre-pass and the in-kernel formation give the same C bit for bit
-    (Strassen's scheme has no leading product free of sums: it always uses
-    the pre-pass)."""
+    """The temporaries hold the same values whoever forms them, and the
+    products run in the same order, so the pre-pass and the in-kernel
+    formation give the same C bit for bit (Winograd: both sides' sums in the
+    kernel; Strassen: B's in the kernel while M2 and M5 run, A's by the
+    pre-pass)."""
     A = inputs.matrix(M, K, "uniform", "bf16", 77, DEV)
     B = inputs.matrix(K, N, "uniform", "bf16", 78, DEV)
     bias = inputs.matrix(1, N, "normal_0.02", "bf16", 79, DEV)[0] if epilogue != "none" else None
