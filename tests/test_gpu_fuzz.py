@@ -64,8 +64,25 @@ def _case(rng):
                 split=split, formation=formation)
 
 
+def _many_case(rng):
+    """Many tiles (or output positions) per pair with a short K: launches whose
+    roles run far apart (the producer done long before the epilogue)."""
+    dtype = rng.choice(["bf16", "f16"])
+    split = rng.choice(["auto", "off", "force"])
+    formation = rng.choice(["auto", "prepass", "in_kernel"])
+    if rng.random() < 0.5:
+        tn = rng.choice([128, 256])
+        return dict(kind="pair_many", algo="classical", tile_m=256, tile_n=tn, M=rng.randrange(4096, 16385),
+                    N=tn * rng.randrange(8, 33), K=8 * rng.randrange(1, 33), dtype=dtype,
+                    epi=rng.choice(["scale_bias", "none"]), split=split, formation=formation)
+    tn = rng.choice([128, 256])
+    return dict(kind="lcma_many", algo=rng.choice(["strassen1", "winograd1"]), tile_m=256, tile_n=tn,
+                M=512 * rng.randrange(8, 17), N=2 * tn * rng.randrange(8, 17), K=128 * rng.randrange(1, 5),
+                dtype=dtype, epi=rng.choice(["scale_bias", "none"]), split=split, formation=formation)
+
+
 _RNG = random.Random(20260603)
-CASES = [_case(_RNG) for _ in range(192)]
+CASES = [_case(_RNG) for _ in range(192)] + [_many_case(_RNG) for _ in range(32)]
 
 
 def _id(c):
