@@ -149,6 +149,11 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   // the low-complexity forms round their operand sums: AUTO takes one only
   // for a clear predicted gain, larger than the model's own error
   m.lcma_margin = 0.03;
+  // operand panels re-read from DRAM once a wave's panels outgrow the L2
+  // (fitted to the classical pair kernel's full-clock times at 16384^3 and
+  // 24576^3)
+  m.dram_miss_slope = 1.0;
+  m.dram_exposed = 0.065 * m.hbm_gbs / 6789.0;  // 0.065 of that time at the measured copy rate
   *out = m;
 }
 
@@ -265,6 +270,32 @@ int32_t fgemm_small_m_grid(int64_t tiles, int32_t k_blocks, int32_t num_sms, int
   return static_cast<int32_t>(best);
 }
 
+namespace {
+
+// Time the operand panels' DRAM re-reads add to a persistent GEMM launch
+// (microseconds).  The tiles of one wave (rows x cols of the tile grid in
+// flight, rasterised in groups of 8 tile rows) share the A panels of their
+// rows and the B panels of their columns, each K long.  Once those panels
+// outgrow the L2, the part beyond it is re-read from DRAM by the tiles that
+// share it: a share min(1, dram_miss_slope * (panels / L2 - 1)) of the tiled
+// reads, of whose DRAM time a part (dram_exposed) is not hidden behind the
+// MMAs.  Fitted to the classical pair kernel's full-clock times (16384^3:
+// panels 1.09 L2, no visible cost; 24576^3: 1.63 L2, about 1.4 ms of 17).
+// `products`: launches of that shape in sequence (the block products of a
+// Strassen-like level, each with its own half-size panels).
+double operand_dram_us(const fgemm_device_model_t* dev, int64_t tiles_m, int64_t tiles_n, int32_t tile_m,
+                       int32_t tile_n, double k, int32_t slots, double products) {
+  if (dev->dram_exposed <= 0.0 || dev->dram_miss_slope <= 0.0 || dev->l2_bytes <= 0.0) return 0.0;
+  const int64_t rows = std::min<int64_t>(tiles_m, 8);
+  const int64_t cols = std::min<int64_t>(tiles_n, ceil_div(slots, std::max<int64_t>(rows, 1)));
+  const double panels = (static_cast<double>(rows) * tile_m + static_cast<double>(cols) * tile_n) * k * 2.0;
+  const double tiled = static_cast<double>(tiles_m) * tiles_n * (tile_m + tile_n) * k * 2.0 * products;
+  const double miss = std::min(1.0, dev->dram_miss_slope * std::max(0.0, panels / dev->l2_bytes - 1.0));
+  return dev->dram_exposed * tiled * miss / (dev->hbm_gbs * 1e3);
+}
+
+}  // namespace
+
 fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, int64_t N,
                                    int64_t K, int32_t epi_kind, fgemm_algo_t algo, int32_t tile_m,
                                    int32_t tile_n, double* predicted_us) {
@@ -350,7 +381,9 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
         t_pre += a_bytes / (dev->hbm_gbs * 1e3 * std::max(dev->hbm_stream_eff, 1e-3)) + dev->launch_us;
     }
     const double per_pair = static_cast<double>(whole * 7 + ceil_div(tail_units, used));
-    const double t_compute = per_pair * t_unit + dev->tile_fill_us * (tail_units > 0 ? 2.0 : 1.0);
+    const double t_compute = per_pair * t_unit + dev->tile_fill_us * (tail_units > 0 ? 2.0 : 1.0) +
+                             operand_dram_us(dev, ceil_div(sub_m, 256), ceil_div(sub_n, tile_n), 256, tile_n,
+                                             k_pad, pairs, 7.0);
     if (predicted_us) *predicted_us = t_pre + t_compute + dev->launch_us;
     return FGEMM_OK;
   }
@@ -393,6 +426,12 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
       t_compute = (static_cast<double>(tiles / slots) + 1.0 / s) * t_tile + dev->split_fix_us * (s - 1);
   }
   t_compute += dev->tile_fill_us;
+  {
+    const int32_t tn_eff = (d == 0 && swiglu) ? tile_n / 2 : tile_n;
+    const int64_t cols = d == 0 && swiglu ? n_out : sub_n;
+    t_compute += operand_dram_us(dev, ceil_div(sub_m, tile_m), ceil_div(cols, tn_eff), tile_m, tile_n, k_pad,
+                                 slots, static_cast<double>(products));
+  }
   double bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
                         static_cast<double>(M) * n_out);
   if (d > 0) {
@@ -501,6 +540,8 @@ std::vector<std::pair<const char*, double*>> model_fields(fgemm_device_model_t& 
       {"form_in_kernel_eff", &m.form_in_kernel_eff},
       {"form_in_kernel_drag", &m.form_in_kernel_drag},
       {"lcma_margin", &m.lcma_margin},
+      {"dram_miss_slope", &m.dram_miss_slope},
+      {"dram_exposed", &m.dram_exposed},
   };
 }
 
@@ -557,6 +598,7 @@ extern "C" fgemm_status_t fgemm_model_load_json(const char* path, fgemm_device_m
     const double rb = old_bw / m.hbm_gbs;
     for (double* e : {&m.hbm_stream_eff, &m.small_m_stream_eff, &m.small_m_aligned_eff, &m.form_in_kernel_eff})
       *e *= rb;
+    m.dram_exposed /= rb;  // a share of bytes / hbm_gbs: the same time
     m.peak_tflops = tf;
     ++found;
   }

@@ -60,7 +60,9 @@ class DeviceModel(ctypes.Structure):
                 ("small_m_aligned_eff", ctypes.c_double),
                 ("form_in_kernel_eff", ctypes.c_double),
                 ("form_in_kernel_drag", ctypes.c_double),
-                ("lcma_margin", ctypes.c_double)]
+                ("lcma_margin", ctypes.c_double),
+                ("dram_miss_slope", ctypes.c_double),
+                ("dram_exposed", ctypes.c_double)]
 
 
 _lib = None

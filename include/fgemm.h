@@ -480,6 +480,10 @@ typedef struct {
   double lcma_margin;      /* AUTO picks a low-complexity form only when its
                             * prediction is below (1 - lcma_margin) times the
                             * best classical one */
+  double dram_miss_slope;  /* share of the tiled operand reads re-read from
+                            * DRAM per unit of (panel bytes of one wave / L2 - 1),
+                            * capped at 1 */
+  double dram_exposed;     /* part of that DRAM time not hidden by the MMAs */
 } fgemm_device_model_t;
 
 /*

@@ -624,3 +624,33 @@ def test_model_plan_margin_for_low_complexity_forms(L):
     m.lcma_margin = gain - 0.01          # enough: the low-complexity form, its own prediction
     algo, t = pick()
     assert algo in ("winograd1", "strassen1") and t <= tw * (1 + 1e-9)
+
+
+def test_model_operand_dram_term_and_the_large_cube_picks(L):
+    """The operand panels' DRAM re-reads: no cost while a wave's panels fit
+    the L2 (8192^3), a cost beyond it (24576^3); with it the defaults pick one
+    Winograd level on CTA pairs from 24576^3 up (measured 5 % ahead there in
+    long runs) and keep the classical kernel at 16384^3 (within the margin)."""
+    m = _model(L)
+
+    def classical(n):
+        return _predict(L, m, n, n, n, "classical", 256, tile_m=256)[1]
+
+    def pick(n):
+        a = ctypes.c_int()
+        tm, tn, us = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+        assert L.fgemm_model_plan(ctypes.byref(m), n, n, n, 0, ctypes.byref(a), ctypes.byref(tm),
+                                  ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
+        return fgemm.ALGO_NAMES[a.value], tm.value, tn.value
+
+    with_term = [classical(n) for n in (8192, 24576)]
+    assert pick(16384) == ("classical", 256, 256)
+    assert pick(24576) == ("winograd1", 256, 256)
+    assert pick(32768) == ("winograd1", 256, 256)
+    exposed = m.dram_exposed
+    m.dram_exposed = 0.0
+    without = [classical(n) for n in (8192, 24576)]
+    assert with_term[0] == without[0]                 # 8192^3: the panels fit
+    assert with_term[1] > without[1] * 1.05           # 24576^3: about 1.4 ms of 17
+    assert pick(24576)[0] == "classical"              # and without it AUTO stays classical
+    m.dram_exposed = exposed
