@@ -598,6 +598,13 @@ def run_fgemm(args, rank, world):
         "gpu_launches": args.steps * per_call,
         "clocks": clk.summary(),
     }
+    if forms and algo == "auto" and plan_algo in forms:
+        # AUTO's pick against the fastest form timed in the same run (a pick
+        # inside the model's margin of a faster form shows here as < 1)
+        fastest = max(forms, key=lambda f: forms[f]["effective_tflops"])
+        line["decision"] = {"auto": plan_algo, "fastest_form": fastest,
+                            "auto_vs_fastest": forms[plan_algo]["effective_tflops"] /
+                            forms[fastest]["effective_tflops"]}
     if small is not None:
         line["small_case"] = small
     if e2e is not None:
