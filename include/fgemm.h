@@ -479,7 +479,11 @@ typedef struct {
                                * fraction of the formation's duration */
   double lcma_margin;      /* AUTO picks a low-complexity form only when its
                             * prediction is below (1 - lcma_margin) times the
-                            * best classical one */
+                            * best classical one (clamped to [0, 0.9]; 0.9 keeps
+                            * AUTO on the classical forms: the Strassen-like
+                            * forms carry their larger rounding error, e.g.
+                            * 6.4e-3 normwise for one Winograd level against
+                            * 2.5e-4 classical on U[-1,1] bf16 inputs) */
   double dram_miss_slope;  /* share of the tiled operand reads re-read from
                             * DRAM per unit of (panel bytes of one wave / L2 - 1),
                             * capped at 1 */
