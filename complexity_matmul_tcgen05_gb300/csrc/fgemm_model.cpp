@@ -116,7 +116,7 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   // against 4.80 ms classical, sustained clocks, scaled to the classical
   // rate above)
   m.eff_strassen_pair[0] = rate(1121.0);  // 256 x 128
-  m.eff_strassen_pair[1] = rate(1650.0);  // 256 x 256
+  m.eff_strassen_pair[1] = rate(1720.0);  // 256 x 256: the product kernel at 16384^3, 4.51 ms at full clocks
   // launch: back-to-back calls of a one-kernel product; fill: the first
   // MMA about 1.5 us after the start, the last 256 x 256 tile's epilogue
   // about 5 us after the last MMA (timestamps of an instrumented build)

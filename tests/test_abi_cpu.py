@@ -629,8 +629,9 @@ def test_model_plan_margin_for_low_complexity_forms(L):
 def test_model_operand_dram_term_and_the_large_cube_picks(L):
     """The operand panels' DRAM re-reads: no cost while a wave's panels fit
     the L2 (8192^3), a cost beyond it (24576^3); with it the defaults pick one
-    Winograd level on CTA pairs from 24576^3 up (measured 5 % ahead there in
-    long runs) and keep the classical kernel at 16384^3 (within the margin)."""
+    Winograd level on CTA pairs from 20480^3 up (measured 4-5 % ahead from there
+    on in long runs) and keep the classical kernel at 12288^3 (12 % behind) and
+    16384^3 (2 % ahead, within the margin)."""
     m = _model(L)
 
     def classical(n):
@@ -644,7 +645,9 @@ def test_model_operand_dram_term_and_the_large_cube_picks(L):
         return fgemm.ALGO_NAMES[a.value], tm.value, tn.value
 
     with_term = [classical(n) for n in (8192, 24576)]
+    assert pick(12288) == ("classical", 256, 256)
     assert pick(16384) == ("classical", 256, 256)
+    assert pick(20480) == ("winograd1", 256, 256)
     assert pick(24576) == ("winograd1", 256, 256)
     assert pick(32768) == ("winograd1", 256, 256)
     exposed = m.dram_exposed
