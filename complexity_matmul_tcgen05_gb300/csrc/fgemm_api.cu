@@ -24,7 +24,15 @@
 namespace fgemm {
 bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo_t algo,
                    int32_t tile_m, int32_t tile_n);
-
+// The decision: the form and tile of least predicted time among those that
+// `algo` (AUTO: every form), `tile_m` / `tile_n` (0: any) and `min_tile_m`
+// allow; under AUTO a low-complexity form only when its prediction is below
+// (1 - lcma_margin) times the best classical one.  The time returned is the
+// pick's own prediction.  FGEMM_ERR_UNSUPPORTED when nothing is legal.
+fgemm_status_t model_search(const fgemm_device_model_t* dev, int64_t M, int64_t N, int64_t K,
+                            int32_t epi_kind, fgemm_algo_t algo, int32_t tile_m, int32_t tile_n,
+                            int32_t min_tile_m, fgemm_algo_t* algo_out, int32_t* tm_out, int32_t* tn_out,
+                            double* us_out);
 }
 
 using fgemm::KernelParams;
@@ -272,23 +280,12 @@ fgemm_status_t choose_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, in
     return FGEMM_OK;
   }
   Plan p{FGEMM_ALGO_CLASSICAL, 0, 0, INFINITY};
-  for (fgemm_algo_t a : kForms) {
-    if (algo != FGEMM_ALGO_AUTO && a != algo) continue;
-    if (wide_classical && a != FGEMM_ALGO_CLASSICAL) continue;
-    for (int32_t tm : {16, 32, 64, 128, 256}) {
-      if (tile_m != 0 && tm != tile_m) continue;
-      if (wide_classical && tm < 128) continue;
-      for (int32_t tn : {64, 128, 256}) {
-        if (tile_n != 0 && tn != tile_n) continue;
-        double us;
-        if (fgemm_model_predict(&h->model, M, N, K, kind, a, tm, tn, &us) == FGEMM_OK &&
-            us < p.predicted_us) {
-          p = Plan{a, tm, tn, us};
-        }
-      }
-    }
-  }
-  if (p.tile_n == 0) return set_msg(h, FGEMM_ERR_UNSUPPORTED, "no legal form/tile for this shape");
+  // the same decision as fgemm_model_plan (under AUTO, the margin a
+  // low-complexity form must win by)
+  if (fgemm::model_search(&h->model, M, N, K, kind, wide_classical ? FGEMM_ALGO_CLASSICAL : algo, tile_m,
+                          tile_n, wide_classical ? 128 : 0, &p.algo, &p.tile_m, &p.tile_n,
+                          &p.predicted_us) != FGEMM_OK)
+    return set_msg(h, FGEMM_ERR_UNSUPPORTED, "no legal form/tile for this shape");
   if (h->plans.size() > 4096) h->plans.clear();
   h->plans.emplace(key, p);
   *out = p;

@@ -296,6 +296,52 @@ double operand_dram_us(const fgemm_device_model_t* dev, int64_t tiles_m, int64_t
 
 }  // namespace
 
+extern "C++" {
+namespace fgemm {
+
+fgemm_status_t model_search(const fgemm_device_model_t* dev, int64_t M, int64_t N, int64_t K,
+                            int32_t epi_kind, fgemm_algo_t algo, int32_t tile_m, int32_t tile_n,
+                            int32_t min_tile_m, fgemm_algo_t* algo_out, int32_t* tm_out, int32_t* tn_out,
+                            double* us_out) {
+  if (!dev) return FGEMM_ERR_INVALID_ARG;
+  const fgemm_algo_t forms[4] = {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2,
+                                 FGEMM_ALGO_WINOGRAD1};
+  // the classical forms first; under AUTO a low-complexity form must then
+  // beat the best of them by the margin
+  const double margin = std::min(std::max(dev->lcma_margin, 0.0), 0.9);
+  double best = INFINITY, best_us = INFINITY;
+  fgemm_algo_t best_algo = FGEMM_ALGO_CLASSICAL;
+  int32_t best_m = 0, best_n = 0;
+  for (fgemm_algo_t a : forms) {
+    if (algo != FGEMM_ALGO_AUTO && a != algo) continue;
+    const double scale = (algo == FGEMM_ALGO_AUTO && a != FGEMM_ALGO_CLASSICAL) ? 1.0 / (1.0 - margin) : 1.0;
+    for (int32_t tm : {16, 32, 64, 128, 256}) {
+      if ((tile_m != 0 && tm != tile_m) || tm < min_tile_m) continue;
+      for (int32_t tn : {64, 128, 256}) {
+        if (tile_n != 0 && tn != tile_n) continue;
+        double us = 0;
+        if (fgemm_model_predict(dev, M, N, K, epi_kind, a, tm, tn, &us) != FGEMM_OK) continue;
+        if (us * scale < best) {
+          best = us * scale;
+          best_us = us;
+          best_algo = a;
+          best_m = tm;
+          best_n = tn;
+        }
+      }
+    }
+  }
+  if (best_n == 0) return FGEMM_ERR_UNSUPPORTED;
+  if (algo_out) *algo_out = best_algo;
+  if (tm_out) *tm_out = best_m;
+  if (tn_out) *tn_out = best_n;
+  if (us_out) *us_out = best_us;
+  return FGEMM_OK;
+}
+
+}  // namespace fgemm
+}  // extern "C++"
+
 fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, int64_t N,
                                    int64_t K, int32_t epi_kind, fgemm_algo_t algo, int32_t tile_m,
                                    int32_t tile_n, double* predicted_us) {
@@ -465,40 +511,8 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
 fgemm_status_t fgemm_model_plan(const fgemm_device_model_t* dev, int64_t M, int64_t N, int64_t K,
                                 int32_t epi_kind, fgemm_algo_t* algo_out, int32_t* tile_m,
                                 int32_t* tile_n, double* predicted_us) {
-  if (!dev) return FGEMM_ERR_INVALID_ARG;
-  const fgemm_algo_t algos[4] = {FGEMM_ALGO_CLASSICAL, FGEMM_ALGO_STRASSEN1, FGEMM_ALGO_STRASSEN2,
-                                 FGEMM_ALGO_WINOGRAD1};
-  const int32_t tms[5] = {16, 32, 64, 128, 256};
-  const int32_t tns[3] = {64, 128, 256};
-  double best = INFINITY;
-  fgemm_algo_t best_algo = FGEMM_ALGO_CLASSICAL;
-  int32_t best_m = 0, best_n = 0;
-  // the classical forms first; a low-complexity form must then beat the
-  // best of them by the margin
-  const double margin = std::min(std::max(dev->lcma_margin, 0.0), 0.9);
-  for (fgemm_algo_t a : algos) {
-    const double scale = a == FGEMM_ALGO_CLASSICAL ? 1.0 : 1.0 / (1.0 - margin);
-    for (int32_t tm : tms) {
-      for (int32_t tn : tns) {
-        double us = 0;
-        if (fgemm_model_predict(dev, M, N, K, epi_kind, a, tm, tn, &us) != FGEMM_OK) continue;
-        us *= scale;
-        if (us < best) {
-          best = us;
-          best_algo = a;
-          best_m = tm;
-          best_n = tn;
-        }
-      }
-    }
-  }
-  if (best_n == 0) return FGEMM_ERR_UNSUPPORTED;
-  if (algo_out) *algo_out = best_algo;
-  if (tile_m) *tile_m = best_m;
-  if (tile_n) *tile_n = best_n;
-  if (predicted_us)
-    *predicted_us = best_algo == FGEMM_ALGO_CLASSICAL ? best : best * (1.0 - margin);
-  return FGEMM_OK;
+  return fgemm::model_search(dev, M, N, K, epi_kind, FGEMM_ALGO_AUTO, 0, 0, 0, algo_out, tile_m, tile_n,
+                             predicted_us);
 }
 
 }  // extern "C"

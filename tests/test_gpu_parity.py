@@ -4,6 +4,8 @@ Small and mid sizes are checked on every output entry; the full-size
 workloads on 4096 stratified sampled entries computed one by one by the
 oracle, in the same launch configuration the benchmark times.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -482,6 +484,40 @@ def test_plan_is_legal_and_launchable():
             C = run(A, B, algo=algo, tile_n=tile, tile_m=tile_m)
             ref = A.float() @ B.float()
             assert torch.equal(C.float(), ref.to(torch.bfloat16).float())
+
+
+def test_auto_takes_the_model_decision_with_its_margin():
+    """A handle's AUTO is fgemm_model_plan on the handle's model: a
+    low-complexity form only when predicted faster than the best classical
+    form by the margin (on the planned cubes and the 17 sweep shapes), and
+    never with a margin of 0.9; with a margin of 0 the fastest prediction."""
+    L = fgemm.lib()
+    h = fgemm.Handle()
+    m = h.device_model()
+    shapes = [(n, n, n) for n in (4096, 8192, 12288, 16384, 20480, 24576, 32768)] + \
+        [(M, n, n) for M in (16, 128, 1024, 8192) for n in (2048, 4096, 8192, 16384)] + [(65536, 1024, 1024)]
+
+    def model_pick(model, M, N, K):
+        a, tm, tn, us = ctypes.c_int(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+        assert L.fgemm_model_plan(ctypes.byref(model), M, N, K, 0, ctypes.byref(a), ctypes.byref(tm),
+                                  ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
+        return fgemm.ALGO_NAMES[a.value], tm.value, tn.value, us.value
+
+    try:
+        for margin in (m.lcma_margin, 0.9, 0.0):
+            m.lcma_margin = margin
+            h.set_device_model(m)
+            for (M, N, K) in shapes:
+                got = h.plan(M, N, K)
+                want = model_pick(m, M, N, K)
+                assert got[:3] == want[:3] and abs(got[3] - want[3]) <= 1e-9 * want[3], (margin, M, N, K, got, want)
+                if margin == 0.9:
+                    assert got[0] == "classical", (M, N, K, got)
+                if got[0] != "classical":
+                    best_classical = h.plan(M, N, K, algo="classical")[3]
+                    assert got[3] < (1.0 - margin) * best_classical, (margin, M, N, K, got, best_classical)
+    finally:
+        h.close()
 
 
 def test_host_buffers_end_to_end():
