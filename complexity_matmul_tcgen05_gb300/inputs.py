@@ -14,6 +14,7 @@ Workloads (dense GEMMs shaped like LLM projection / FFN layers):
                         A ~ N(0,1), B ~ N(0,1/K), SwiGLU output M x 14336
   square_8192_bf16      M=N=K=8192, bf16, A,B ~ U[-1,1]
   square_16384_bf16     M=N=K=16384, bf16, A,B ~ U[-1,1]
+  square_20480_bf16     M=N=K=20480, bf16, A,B ~ U[-1,1]
   square_24576_bf16     M=N=K=24576, bf16, A,B ~ U[-1,1]
   sweep                 bf16, M in {16,128,1024,8192} x N=K in
                         {2048,4096,8192,16384}, plus M=65536, N=K=1024;
@@ -42,6 +43,9 @@ WORKLOADS = {
     "square_16384_bf16": dict(M=16384, N=16384, K=16384, dtype="bf16", a="uniform",
                               b="uniform", epi="none", bias=None,
                               algos=("classical", "strassen1", "strassen2", "winograd1", "auto")),
+    "square_20480_bf16": dict(M=20480, N=20480, K=20480, dtype="bf16", a="uniform",
+                              b="uniform", epi="none", bias=None,
+                              algos=("classical", "strassen1", "winograd1", "auto")),
     "square_24576_bf16": dict(M=24576, N=24576, K=24576, dtype="bf16", a="uniform",
                               b="uniform", epi="none", bias=None,
                               algos=("classical", "strassen1", "winograd1", "auto")),

@@ -296,7 +296,8 @@ fgemm_status_t fgemm_matmul_mx(fgemm_handle_t h, int64_t M, int64_t N, int64_t K
 /*
  * Runs the decision model (no launch): the algorithm, tile and predicted
  * time AUTO would use for this shape (FalconGEMM summary, "Methodology"
- * items 4 and 5). Output pointers may be NULL.
+ * items 4 and 5): the same choice as fgemm_model_plan on the handle's model,
+ * lcma_margin included. Output pointers may be NULL.
  */
 fgemm_status_t fgemm_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
                           fgemm_dtype_t dtype, const fgemm_epilogue_t* epi,
@@ -307,8 +308,9 @@ fgemm_status_t fgemm_plan(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * As fgemm_plan, with the choice restricted: algo (FGEMM_ALGO_AUTO: any
  * form), tile_m_in and tile_n_in (0: any) constrain the candidates the model
  * ranks, as a forced form or tile in fgemm_matmul_ex does; the result is
- * what that call would launch. FGEMM_ERR_UNSUPPORTED if no candidate is
- * legal for the shape.
+ * what that call would launch (under AUTO a low-complexity candidate must
+ * beat the best classical one by lcma_margin). FGEMM_ERR_UNSUPPORTED if no
+ * candidate is legal for the shape.
  */
 fgemm_status_t fgemm_plan_ex(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
                              fgemm_dtype_t dtype, const fgemm_epilogue_t* epi, fgemm_algo_t algo,

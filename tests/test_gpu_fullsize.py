@@ -115,6 +115,15 @@ def test_square_16384(algo, tile_m):
     _sampled_check("square_16384", A, B, None, algo, "none", "bf16", tile_m=tile_m)
 
 
+@pytest.mark.parametrize("algo,tile_m", [("winograd1", 256), ("auto", 0)])
+def test_square_20480(algo, tile_m):
+    """The smallest cube on which AUTO takes one Winograd level on CTA pairs:
+    21 whole waves of output positions plus 4 positions as product units
+    shared out over the pairs."""
+    A, B, _ = inputs.workload_inputs("square_20480_bf16", DEV)
+    _sampled_check("square_20480", A, B, None, algo, "none", "bf16", tile_m=tile_m)
+
+
 @pytest.mark.parametrize("algo,tile_m", [("classical", 0), ("winograd1", 256), ("strassen1", 256),
                                          ("auto", 0)])
 def test_square_24576(algo, tile_m):
