@@ -221,7 +221,7 @@ FORM_SOURCES = {
 def form_key(algo, tile_m):
     if algo == "classical":
         return "classical_pair" if tile_m == 256 else ("classical_small_m" if tile_m < 128 else "classical")
-    if tile_m == 256 and algo in ("strassen1", "winograd1"):
+    if tile_m == 256 and algo in ("strassen1", "strassen2", "winograd1"):
         return "lcma_pair"
     return algo
 
@@ -628,7 +628,8 @@ CANDIDATES = [("classical", 16, 128), ("classical", 32, 128), ("classical", 64, 
               ("classical", 128, 64), ("classical", 128, 128), ("classical", 128, 256),
               ("classical", 256, 128), ("classical", 256, 256), ("strassen1", 128, 128),
               ("strassen1", 128, 256), ("strassen1", 256, 128), ("strassen1", 256, 256),
-              ("strassen2", 128, 128), ("strassen2", 128, 256), ("winograd1", 128, 128),
+              ("strassen2", 128, 128), ("strassen2", 128, 256), ("strassen2", 256, 128),
+              ("strassen2", 256, 256), ("winograd1", 128, 128),
               ("winograd1", 128, 256), ("winograd1", 256, 128), ("winograd1", 256, 256)]
 
 

@@ -379,10 +379,10 @@ int lcma_needs(const StrassenTable& tab, int k) {
 // stays as it is (A11 B11, A12 B21 first); Strassen's becomes M2, M5, M3,
 // M4, M1, M6, M7.  The order is the same whoever forms the sums, so the
 // result is too.
-void lcma_order(const StrassenTable& tab, int (&order)[fgemm::kLcmaProducts]) {
+void lcma_order(const StrassenTable& tab, int np, int (&order)[fgemm::kLcmaProducts]) {
   int n = 0;
   for (int key = 0; key < 4; ++key)
-    for (int k = 0; k < fgemm::kLcmaProducts; ++k)
+    for (int k = 0; k < np; ++k)
       if (lcma_needs(tab, k) == key) order[n++] = k;
 }
 
@@ -396,11 +396,12 @@ void lcma_order(const StrassenTable& tab, int (&order)[fgemm::kLcmaProducts]) {
 // formation bands.
 int lcma_formation_plan(fgemm_handle_t h, const StrassenTable& tab, long long positions, int clusters, int sub_m,
                         int sub_k, int* lead) {
+  constexpr int np = 7;  // one level (two levels always take the pre-pass)
   int order[fgemm::kLcmaProducts];
-  lcma_order(tab, order);
+  lcma_order(tab, np, order);
   int none = 0, no_b = 0;
-  while (none < fgemm::kLcmaProducts && lcma_needs(tab, order[none]) == 0) ++none;
-  while (no_b < fgemm::kLcmaProducts && !(lcma_needs(tab, order[no_b]) & 2)) ++no_b;
+  while (none < np && lcma_needs(tab, order[none]) == 0) ++none;
+  while (no_b < np && !(lcma_needs(tab, order[no_b]) & 2)) ++no_b;
   const int mask = none > 0 ? 3 : (no_b > 0 ? 2 : 0);
   const int ld = none > 0 ? none : no_b;
   if (lead) *lead = ld;
@@ -411,7 +412,7 @@ int lcma_formation_plan(fgemm_handle_t h, const StrassenTable& tab, long long po
   return 0;
 }
 
-fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTable& tab, int bn,
+fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTable& tab, int depth, int bn,
                            const void* A, int64_t lda, const void* B, int64_t ldb) {
   using fgemm::LcmaFormParams;
   using fgemm::LcmaParams;
@@ -419,7 +420,8 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   std::memset(&L, 0, sizeof(L));
   LcmaFormParams F;
   std::memset(&F, 0, sizeof(F));
-  const int np = fgemm::kLcmaProducts;
+  const int np = depth == 1 ? 7 : 49;
+  const int nblk = 1 << (2 * depth);  // blocks of each matrix, and output blocks
   // the distinct summed operands of each side (a single positive term is a
   // raw block of A or B, read in place)
   auto operand = [&](int n, const uint8_t* codes, fgemm::LcmaFormJob& J, uint8_t* is_temp,
@@ -429,14 +431,14 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
       *idx = codes[0] & fgemm::kTermIndexMask;
       return;
     }
-    int8_t coef[4] = {0};
+    int8_t coef[fgemm::kLcmaMaxBlocks] = {0};
     for (int i = 0; i < n; ++i)
       coef[codes[i] & fgemm::kTermIndexMask] += (codes[i] & fgemm::kTermNeg) ? -1 : 1;
     int t = 0;
     while (t < J.ntemp && std::memcmp(J.coef[t], coef, sizeof(coef)) != 0) ++t;
     if (t == J.ntemp) {
       std::memcpy(J.coef[t], coef, sizeof(coef));
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < nblk; ++q)
         if (coef[q] != 0) J.block_mask |= 1u << q;
       ++J.ntemp;
     }
@@ -445,9 +447,15 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   };
   // the products in the kernel's order (lcma_order): L.prod[pr] is table
   // product order[pr]
+  // (two levels: table order; every product but four reads sums, all
+  // formed by the pre-pass)
   int order[fgemm::kLcmaProducts];
-  lcma_order(tab, order);
-  int first_of[4] = {-1, -1, -1, -1}, last_of[4] = {-1, -1, -1, -1};  // product per output block
+  if (depth == 1)
+    lcma_order(tab, np, order);
+  else
+    for (int k = 0; k < np; ++k) order[k] = k;
+  int first_of[fgemm::kLcmaMaxBlocks], last_of[fgemm::kLcmaMaxBlocks];  // product per output block
+  for (int b = 0; b < fgemm::kLcmaMaxBlocks; ++b) first_of[b] = last_of[b] = -1;
   for (int pr = 0; pr < np; ++pr) {
     fgemm::LcmaProduct& P = L.prod[pr];
     const int k = order[pr];
@@ -473,36 +481,64 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
     fgemm::LcmaProduct& P = L.prod[pr];
     P.fin = 0;
     P.groups = 0;
-    for (int b = 0; b < 4; ++b)
-      if (!swiglu && last_of[b] == pr) P.fin |= static_cast<uint8_t>(1u << b);
+    for (int b = 0; b < nblk; ++b)
+      if (!swiglu && last_of[b] == pr) P.fin |= static_cast<uint16_t>(1u << b);
     for (int sr = 0; sr < 2; ++sr)
       if (swiglu && std::max(last_of[2 * sr], last_of[2 * sr + 1]) == pr)
-        P.fin |= static_cast<uint8_t>(1u << sr);
+        P.fin |= static_cast<uint16_t>(1u << sr);
     for (int t = 0; t < P.nc; ++t) {
       const int blk = P.c[t] & fgemm::kTermIndexMask;
       const int group = swiglu ? blk >> 1 : blk;
       if (first_of[blk] == pr) P.c[t] |= fgemm::kTermFirst;
       if (last_of[blk] == pr && ((P.fin >> group) & 1u)) P.c[t] |= fgemm::kTermLast;
-      P.groups |= static_cast<uint8_t>(1u << group);
+      P.groups |= static_cast<uint16_t>(1u << group);
     }
   }
-  for (int g = 0; g < 4; ++g) {
+  for (int g = 0; g < nblk; ++g) {
     int n = 0;
     for (int pr = 0; pr < np; ++pr) n += (L.prod[pr].groups >> g) & 1u;
     L.group_pieces[g] = static_cast<uint8_t>(n);
   }
+  if (depth == 2) {
+    // the two-level pre-pass forms product (p, q)'s operand as the inner
+    // combination q of the outer combination p (fgemm::strassen_coef): it
+    // must be the table's operand
+    for (int side = 0; side < 2; ++side) {
+      fgemm::LcmaFormJob& J = F.job[side];
+      for (int k = 0; k < np; ++k) {
+        const fgemm::LcmaProduct& P = L.prod[k];
+        const int n = side == 0 ? tab.na[k] : tab.nb[k];
+        const uint8_t* codes = side == 0 ? tab.a[k] : tab.b[k];
+        int8_t want[fgemm::kLcmaMaxBlocks] = {0}, got[fgemm::kLcmaMaxBlocks] = {0};
+        for (int i = 0; i < n; ++i)
+          want[codes[i] & fgemm::kTermIndexMask] += (codes[i] & fgemm::kTermNeg) ? -1 : 1;
+        for (int i = 0; i < 4; ++i)
+          for (int j = 0; j < 4; ++j)
+            got[(2 * (i >> 1) + (j >> 1)) * 4 + 2 * (i & 1) + (j & 1)] = static_cast<int8_t>(
+                fgemm::strassen_coef(side, k / 7, i) * fgemm::strassen_coef(side, k % 7, j));
+        if (std::memcmp(want, got, sizeof(want)) != 0)
+          return set_msg(h, FGEMM_ERR_UNSUPPORTED, "two-level operand table does not match the pre-pass");
+        const bool temp = side == 0 ? P.a_temp : P.b_temp;
+        J.leaf_temp[k] = temp ? static_cast<int8_t>(side == 0 ? P.a_idx : P.b_idx) : static_cast<int8_t>(-1);
+      }
+    }
+  }
   const int ntA = F.job[0].ntemp, ntB = F.job[1].ntemp;
-  const int fit = fgemm::lcma_pair_clusters_fit(bn);
+  const int fit = fgemm::lcma_pair_clusters_fit(bn, depth);
   if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the Strassen pair launch");
   const long long positions = p.num_units;
   L.units = positions * np;
-  const int clusters = static_cast<int>(std::min<long long>(fit, L.units));
+  // two levels with fewer positions than pairs: one pair per position, each
+  // running its position whole (a partial wave cut into 49 units per
+  // position would leave 49-way combinations to the helper warps)
+  const int clusters = depth == 2 && positions < fit ? static_cast<int>(positions)
+                                                     : static_cast<int>(std::min<long long>(fit, L.units));
   // the positions of the partial last wave run as separate product units;
   // every CTA keeps the partials of each of its whole positions
   const long long tail_positions = positions % clusters;
   const long long whole = positions / clusters;
   const size_t slot_bytes = static_cast<size_t>(2) * clusters * static_cast<size_t>(std::max<long long>(whole, 1)) *
-                            fgemm::lcma_slot_floats(bn) * sizeof(float);
+                            fgemm::lcma_slot_floats(bn, depth) * sizeof(float);
   const size_t tail_bytes =
       static_cast<size_t>(tail_positions) * np * 2 * fgemm::kBM * static_cast<size_t>(bn) * sizeof(float);
   const size_t ta_elems = static_cast<size_t>(ntA) * p.sub_m * p.sub_k;
@@ -512,8 +548,8 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   const size_t ta_off = tail_off + align(tail_bytes), tb_off = ta_off + align(ta_elems * 2);
   fgemm_status_t s = ensure_workspace(h, tb_off + align(tb_elems * 2));
   if (s != FGEMM_OK) return s;
-  // 4 output groups x 2 CTAs x 4 epilogue warps per tail position
-  s = ensure_counters(h, static_cast<size_t>(std::max<long long>(tail_positions, 1)) * 32);
+  // 4^depth output groups x 2 CTAs x 4 epilogue warps per tail position
+  s = ensure_counters(h, static_cast<size_t>(std::max<long long>(tail_positions, 1)) * nblk * 8);
   if (s != FGEMM_OK) return s;
   uint8_t* ws = reinterpret_cast<uint8_t*>(h->workspace);
   uint16_t* TA = reinterpret_cast<uint16_t*>(ws + ta_off);
@@ -553,7 +589,7 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   // inside the product kernel while the leading products that do not read
   // that side's sums run (lcma_formation_plan).
   int lead = 0;
-  const int mask = lcma_formation_plan(h, tab, positions, clusters, p.sub_m, p.sub_k, &lead);
+  const int mask = depth == 1 ? lcma_formation_plan(h, tab, positions, clusters, p.sub_m, p.sub_k, &lead) : 0;
   const bool fused = mask != 0;
   // A pair's tail units (positions of the partial last wave, one product
   // each) run after its whole positions' first tail_at products, so that the
@@ -568,7 +604,7 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   for (int j = 0; j < 2; ++j)
     if ((mask >> j) & 1) pre.job[j].ntemp = 0;
   if (pre.job[0].ntemp > 0 || pre.job[1].ntemp > 0) {
-    e = fgemm::launch_lcma_form(pre, h->num_sms, h->stream);
+    e = fgemm::launch_lcma_form(pre, depth, h->num_sms, h->stream);
     if (e != cudaSuccess) return cuda_fail(h, e, "operand-sum pre-pass launch");
   }
   if (fused) {
@@ -586,7 +622,7 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
     for (int j = 0; j < 2; ++j)
       L.form_tasks[j] = ((mask >> j) & 1) && F.job[j].ntemp > 0 ? F.job[j].rows / fgemm::kFormRows : 0;
   }
-  e = fgemm::launch_lcma_pair(bn, L, clusters, h->stream);
+  e = fgemm::launch_lcma_pair(bn, depth, L, clusters, h->stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "Strassen pair kernel launch");
   return FGEMM_OK;
 }
@@ -838,12 +874,14 @@ fgemm_status_t fgemm_call_launches(fgemm_handle_t h, int64_t M, int64_t N, int64
   fgemm_status_t s = choose_plan(h, M, N, K, kind, algo, tile_m_in, tile_n_in, &p);
   if (s != FGEMM_OK) return s;
   *launches = 1;
-  if (p.tile_m == 256 && depth_of(p.algo) == 1) {
+  if (p.tile_m == 256 && depth_of(p.algo) == 2) {
+    *launches = 2;  // the pre-pass, then the products
+  } else if (p.tile_m == 256 && depth_of(p.algo) == 1) {
     const int sub_m = static_cast<int>(M / 2), sub_n = static_cast<int>(N / 2), sub_k = static_cast<int>(K / 2);
     const long long positions = fgemm_model_tiles(sub_m, sub_n, 256, p.tile_n);
-    const int fit = fgemm::lcma_pair_clusters_fit(p.tile_n);
+    const int fit = fgemm::lcma_pair_clusters_fit(p.tile_n, 1);
     if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the Strassen pair launch");
-    const int clusters = static_cast<int>(std::min<long long>(fit, positions * fgemm::kLcmaProducts));
+    const int clusters = static_cast<int>(std::min<long long>(fit, positions * 7));
     const StrassenTable& tab =
         p.algo == FGEMM_ALGO_WINOGRAD1 ? fgemm::winograd_table() : fgemm::strassen_table(1);
     // the pre-pass runs unless the product kernel forms both sides' sums
@@ -936,7 +974,7 @@ fgemm_status_t matmul_impl(fgemm_handle_t h, int64_t M, int64_t N, int64_t K, co
                   static_cast<uint64_t>(ldb), fgemm::kBK, p.is_bf16);
   if (s != FGEMM_OK) return s;
 
-  if (bm == 256 && d == 1) return launch_lcma(h, p, tab, bn, A, lda, B, ldb);
+  if (bm == 256 && d >= 1) return launch_lcma(h, p, tab, d, bn, A, lda, B, ldb);
   if (bm == 256) {
     const int fit = fgemm::gemm_pair_clusters_fit(bn);
     if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the CTA-pair launch");
@@ -1400,25 +1438,31 @@ extern "C" fgemm_status_t fgemm_calibrate_ex(fgemm_handle_t h, int64_t n, const 
         m.eff_strassen[d - 1][i] = executed / (us * 1e6) / m.peak_tflops;
       }
     }
-    for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
-      // one level on CTA pairs: a pre-pass plus the product kernel, so the
-      // product kernel's rate is the one under which the model predicts the
-      // measured time (found by bisection; the prediction falls as it rises)
-      double us = 0;
-      const int32_t tn = i == 0 ? 128 : 256;
-      if (!time_gemm(n, n, n, FGEMM_ALGO_STRASSEN1, 256, tn, &us)) break;
-      double lo = 1e-3, hi = 4.0;
-      for (int it = 0; it < 60; ++it) {
-        const double mid = 0.5 * (lo + hi);
-        m.eff_strassen_pair[i] = mid;
-        double pred = 0;
-        fgemm_model_predict(&m, n, n, n, FGEMM_EPI_NONE, FGEMM_ALGO_STRASSEN1, 256, tn, &pred);
-        if (pred > us)
-          lo = mid;
-        else
-          hi = mid;
+    for (int d = 1; d <= 2 && status == FGEMM_OK; ++d) {
+      for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
+        // one or two levels on CTA pairs: a pre-pass plus the product
+        // kernel, so the product kernel's rate is the one under which the
+        // model predicts the measured time (found by bisection; the
+        // prediction falls as it rises)
+        const fgemm_algo_t a = d == 1 ? FGEMM_ALGO_STRASSEN1 : FGEMM_ALGO_STRASSEN2;
+        const int32_t tn = i == 0 ? 128 : 256;
+        if (!fgemm::form_is_legal(n, n, n, FGEMM_EPI_NONE, a, 256, tn)) continue;
+        double us = 0;
+        if (!time_gemm(n, n, n, a, 256, tn, &us)) break;
+        double* eff = d == 1 ? &m.eff_strassen_pair[i] : &m.eff_strassen2_pair[i];
+        double lo = 1e-3, hi = 4.0;
+        for (int it = 0; it < 60; ++it) {
+          const double mid = 0.5 * (lo + hi);
+          *eff = mid;
+          double pred = 0;
+          fgemm_model_predict(&m, n, n, n, FGEMM_EPI_NONE, a, 256, tn, &pred);
+          if (pred > us)
+            lo = mid;
+          else
+            hi = mid;
+        }
+        *eff = 0.5 * (lo + hi);
       }
-      m.eff_strassen_pair[i] = 0.5 * (lo + hi);
     }
     for (int i = 0; i < 2 && status == FGEMM_OK; ++i) {
       double us = 0;

@@ -213,21 +213,24 @@ struct StrassenParams {
 // marking the first and the last contribution to each block in product
 // order).  fin: the output blocks (bit b) whose value is complete once this
 // product is in, or for SwiGLU the block rows (bit r: gate block 2r, up
-// block 2r + 1) complete with it.
+// block 2r + 1) complete with it.  Block indices as in StrassenTable: block
+// (r, c) of the 2^depth x 2^depth split is r << depth | c.
 struct LcmaProduct {
   uint8_t a_temp, a_idx, b_temp, b_idx;
   uint8_t nc;
   uint8_t c[kMaxTerms];
-  uint8_t fin;
-  uint8_t groups;  // output groups it feeds (bit g: block g, or for SwiGLU block row g)
+  uint16_t fin;
+  uint16_t groups;  // output groups it feeds (bit g: block g, or for SwiGLU block row g)
 };
 
-// One matrix of the operand formation: the four `rows` x `cols` blocks of
-// src (block q at block row q >> 1, block column q & 1) are combined into
-// ntemp temporaries, temporary t = sum_q coef[t][q] * block_q (coef in
-// {-1, 0, 1}), stored one after another, each rows x cols with pitch cols.
-constexpr int kLcmaProducts = 7;  // one level: seven block products
-constexpr int kLcmaMaxTemps = 8;  // summed operands per side (Strassen 5, Winograd 4)
+// One matrix of the operand formation: the 4^depth `rows` x `cols` blocks
+// of src (block q at block row q >> depth, block column q & (2^depth - 1))
+// are combined into ntemp temporaries, temporary t = sum_q coef[t][q] *
+// block_q (coef in {-1, 0, 1}), stored one after another, each rows x cols
+// with pitch cols.
+constexpr int kLcmaProducts = 49;   // up to two levels: 7^depth block products
+constexpr int kLcmaMaxTemps = 49;   // summed operands per side (one level: Strassen 5, Winograd 4)
+constexpr int kLcmaMaxBlocks = 16;  // 4^depth blocks of each matrix
 struct LcmaFormJob {
   const uint16_t* src;
   long long ld;
@@ -235,8 +238,24 @@ struct LcmaFormJob {
   int rows, cols;
   int ntemp;
   uint32_t block_mask;  // blocks some temporary reads
-  int8_t coef[kLcmaMaxTemps][4];
+  int8_t coef[kLcmaMaxTemps][kLcmaMaxBlocks];
+  // two levels: the temporary that holds product p's operand on this side
+  // (-1: a raw block, read in place)
+  int8_t leaf_temp[kLcmaProducts];
 };
+
+// One Strassen level's operand coefficients (side 0: A, 1: B) over the
+// blocks 11, 12, 21, 22 (index i = r * 2 + c) for the products p = M1 .. M7: the two-level pre-pass forms
+// product (p, q)'s operand on a side as the inner combination q of the outer
+// combination p of the quarter blocks.  The host checks them against the
+// scheme's two-level table before it uses that pre-pass.
+FGEMM_HD constexpr int strassen_coef(int side, int p, int i) {
+  constexpr int8_t a[7][4] = {{1, 0, 0, 1}, {0, 0, 1, 1}, {1, 0, 0, 0}, {0, 0, 0, 1},
+                              {1, 1, 0, 0}, {-1, 0, 1, 0}, {0, 1, 0, -1}};
+  constexpr int8_t b[7][4] = {{1, 0, 0, 1}, {1, 0, 0, 0}, {0, 1, 0, -1}, {-1, 0, 1, 0},
+                              {0, 0, 0, 1}, {1, 1, 0, 0}, {0, 0, 1, 1}};
+  return side == 0 ? a[p][i] : b[p][i];
+}
 
 struct LcmaFormParams {
   LcmaFormJob job[2];  // A and B
@@ -256,7 +275,7 @@ struct LcmaParams {
   CUtensorMap tmap_tb;   // B temporaries: inner sub_n, outer ntemp_b * sub_k, box {64, 64}
   long long units;       // output positions * num_products (informational)
   LcmaProduct prod[kLcmaProducts];
-  uint8_t group_pieces[4];  // products feeding each output group
+  uint8_t group_pieces[kLcmaMaxBlocks];  // products feeding each output group
   int tail_at;              // whole-position products a pair runs before its tail units
   // Temporaries formed inside the product kernel (form_tasks[0] +
   // form_tasks[1] > 0; otherwise the pre-pass launch formed them): job j is
@@ -270,24 +289,29 @@ struct LcmaParams {
   int form_tasks[2];
 };
 
-// Per-CTA partial tiles of the product kernel's whole positions: the four
-// output blocks of one level, 128 x bn fp32 each.
-inline size_t lcma_slot_floats(int bn) { return static_cast<size_t>(4) * 128 * static_cast<size_t>(bn); }
+// Per-CTA partial tiles of the product kernel's whole positions: the 4^depth
+// output blocks, 128 x bn fp32 each.
+inline size_t lcma_slot_floats(int bn, int depth) {
+  return (static_cast<size_t>(1) << (2 * depth)) * 128 * static_cast<size_t>(bn);
+}
 
-// The pre-pass (depth 1) over both jobs in one launch.
-cudaError_t launch_lcma_form(const LcmaFormParams& f, int num_sms, cudaStream_t stream);
+// The pre-pass over both jobs in one launch (depth 1 or 2).
+cudaError_t launch_lcma_form(const LcmaFormParams& f, int depth, int num_sms, cudaStream_t stream);
 
-// The product kernel for one Strassen-like level on `clusters` CTA pairs
-// (bn = 128 or 256).  p.k.workspace holds 2 * clusters * W * lcma_slot_floats
-// partials (W = positions / clusters whole positions per pair); the T = positions mod clusters positions of the partial last
-// wave run as 7 T separate product units, whose accumulators (128 x bn fp32
-// per unit and CTA) go to p.k.split_ws, with 32 counters per such position
-// (4 output groups x 2 CTAs x 4 epilogue warps) in p.k.split_ctr tagged with
-// p.k.split_gen.
-cudaError_t launch_lcma_pair(int bn, const LcmaParams& p, int clusters, cudaStream_t stream);
+// The product kernel for `depth` Strassen-like levels on `clusters` CTA pairs
+// (bn = 128 or 256).  p.k.workspace holds 2 * clusters * W *
+// lcma_slot_floats(bn, depth) partials (W = positions / clusters whole
+// positions per pair); the T = positions mod clusters positions of the
+// partial last wave run as 7^depth T separate product units, whose
+// accumulators (128 x bn fp32 per unit and CTA) go to p.k.split_ws, with
+// 4^depth x 2 x 4 counters per such position (output groups x CTAs x
+// epilogue warps) in p.k.split_ctr tagged with p.k.split_gen.  Two levels
+// take the operands from the pre-pass (no in-kernel formation) and no
+// SwiGLU.
+cudaError_t launch_lcma_pair(int bn, int depth, const LcmaParams& p, int clusters, cudaStream_t stream);
 
 // How many clusters of the product kernel fit on the current device.
-int lcma_pair_clusters_fit(int bn);
+int lcma_pair_clusters_fit(int bn, int depth);
 
 // Error word layout written by a kernel whose bounded wait ran out.
 constexpr unsigned int kErrTimeout = 0x80000000u;

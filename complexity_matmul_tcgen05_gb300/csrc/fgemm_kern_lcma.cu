@@ -47,18 +47,20 @@ namespace fgemm {
 
 // ------------------------------------------------------ operand formation
 
-// Block (q >> 1, q & 1) of a 2 x 2 split of a rows x cols sub-block grid.
+// Row r of block (q >> D, q & (2^D - 1)) of a 2^D x 2^D split of src into
+// rows x cols blocks.
+template <int D>
 __device__ __forceinline__ const uint4* form_src(const LcmaFormJob& J, int q, int r) {
-  const uint16_t* base = J.src + static_cast<long long>((q >> 1) * J.rows + r) * J.ld +
-                         static_cast<long long>(q & 1) * J.cols;
+  const uint16_t* base = J.src + static_cast<long long>((q >> D) * J.rows + r) * J.ld +
+                         static_cast<long long>(q & ((1 << D) - 1)) * J.cols;
   return reinterpret_cast<const uint4*>(base);
 }
 
-// Forms every temporary of job J at the R rows r0, r0 + rstep, ... (rows
-// past the last are skipped) for the 16-byte column group c8: the source
-// blocks' 16 bytes are loaded once (4 R loads in flight), each temporary's
-// 16 bytes formed in fp32 (sum of the exact 16-bit values, one RNE
-// rounding) and stored.  The sums of one group are independent of every
+// One level: forms every temporary of job J at the R rows r0, r0 + rstep,
+// ... (rows past the last are skipped) for the 16-byte column group c8: the
+// source blocks' 16 bytes are loaded once (4 R loads in flight), each
+// temporary's 16 bytes formed in fp32 (sum of the exact 16-bit values, one
+// RNE rounding) and stored.  The sums of one group are independent of every
 // other group.
 template <int R>
 __device__ __forceinline__ void form_rows(const LcmaFormJob& J, int is_bf16, int r0, int rstep, int c8) {
@@ -69,7 +71,7 @@ __device__ __forceinline__ void form_rows(const LcmaFormJob& J, int is_bf16, int
     const int r = r0 + h * rstep;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      raw[h][q] = (r < J.rows && ((J.block_mask >> q) & 1u)) ? __ldg(form_src(J, q, r) + c8)
+      raw[h][q] = (r < J.rows && ((J.block_mask >> q) & 1u)) ? __ldg(form_src<1>(J, q, r) + c8)
                                                              : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
@@ -99,9 +101,9 @@ __device__ __forceinline__ void form_rows(const LcmaFormJob& J, int is_bf16, int
   }
 }
 
-// The pre-pass as its own launch: one warp per pair of rows and 32 column
-// groups of 8 elements (16 bytes) per warp; blockIdx.z selects the matrix
-// (A or B).
+// The one-level pre-pass as its own launch: one warp per pair of rows and
+// 32 column groups of 8 elements (16 bytes) per warp; blockIdx.z selects the
+// matrix (A or B).
 __global__ void __launch_bounds__(256) lcma_form_kernel(const __grid_constant__ LcmaFormParams P) {
   const LcmaFormJob& J = P.job[blockIdx.z];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -113,7 +115,77 @@ __global__ void __launch_bounds__(256) lcma_form_kernel(const __grid_constant__ 
   for (int r0 = blockIdx.y * 8 + warp; r0 < J.rows; r0 += 2 * step) form_rows<2>(J, P.is_bf16, r0, step, c8);
 }
 
-cudaError_t launch_lcma_form(const LcmaFormParams& f, int num_sms, cudaStream_t stream) {
+// Two Strassen levels: product (p, q)'s operand on one side is
+// sum_{i, j} c[p][i] c[q][j] X(i, j), X(i, j) quarter block (2 ri + rj,
+// 2 ci + cj) for outer block i = (ri, ci) and inner block j = (rj, cj).  One
+// thread per row and 16-byte column group: the 16 quarter blocks' 16 bytes
+// are loaded once; for each outer combination p the four inner blocks
+// Y_j = sum_i c[p][i] X(i, j) are summed in fp32, then each inner combination
+// q of them, rounded once to the input type and stored as the temporary that
+// holds (p, q) (the four operands that are a single block are read in
+// place).  The coefficients are compile-time constants, so only the nonzero
+// terms are added.
+template <int Side>
+__device__ __forceinline__ void form2_group(const LcmaFormJob& J, int is_bf16, int r, int c8) {
+  uint4 raw[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) raw[q] = __ldg(form_src<2>(J, q, r) + c8);
+  const long long plane = static_cast<long long>(J.rows) * J.cols;
+  uint16_t* dst = J.dst + static_cast<long long>(r) * J.cols + c8 * 8;
+#pragma unroll
+  for (int p = 0; p < 7; ++p) {
+    float y[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[j][e] = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = strassen_coef(Side, p, i);
+        if (c == 0) continue;
+        const int q16 = (2 * (i >> 1) + (j >> 1)) * 4 + 2 * (i & 1) + (j & 1);
+        float f[8];
+        unpack8(raw[q16], f, is_bf16);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[j][e] += c > 0 ? f[e] : -f[e];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 7; ++q) {
+      const int t = J.leaf_temp[p * 7 + q];
+      if (t < 0) continue;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = strassen_coef(Side, q, j);
+        if (c == 0) continue;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += c > 0 ? y[j][e] : -y[j][e];
+      }
+      *reinterpret_cast<uint4*>(dst + t * plane) =
+          make_uint4(pack2(acc[0], acc[1], is_bf16), pack2(acc[2], acc[3], is_bf16),
+                     pack2(acc[4], acc[5], is_bf16), pack2(acc[6], acc[7], is_bf16));
+    }
+  }
+}
+
+// The two-level pre-pass: one warp per row and 32 column groups;
+// blockIdx.z selects the matrix (A or B).
+__global__ void __launch_bounds__(256) lcma_form2_kernel(const __grid_constant__ LcmaFormParams P) {
+  const LcmaFormJob& J = P.job[blockIdx.z];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c8 = blockIdx.x * 32 + lane;
+  const int r = blockIdx.y * 8 + warp;
+  if (J.ntemp == 0 || c8 >= (J.cols >> 3) || r >= J.rows) return;
+  if (blockIdx.z == 0)
+    form2_group<0>(J, P.is_bf16, r, c8);
+  else
+    form2_group<1>(J, P.is_bf16, r, c8);
+}
+
+cudaError_t launch_lcma_form(const LcmaFormParams& f, int depth, int num_sms, cudaStream_t stream) {
   int max_cols8 = 0, max_rows = 0;
   for (int j = 0; j < 2; ++j) {
     if (f.job[j].ntemp == 0) continue;
@@ -122,34 +194,43 @@ cudaError_t launch_lcma_form(const LcmaFormParams& f, int num_sms, cudaStream_t 
   }
   if (max_cols8 == 0) return cudaSuccess;
   const int gx = (max_cols8 + 31) / 32;
+  if (depth == 2) {
+    if ((max_rows + 7) / 8 > 65535) return cudaErrorInvalidValue;
+    lcma_form2_kernel<<<dim3(gx, (max_rows + 7) / 8, 2), 256, 0, stream>>>(f);
+    return cudaGetLastError();
+  }
   // about 16 blocks of 8 warps per SM over both matrices, each warp looping over rows
   const int gy = std::max(1, std::min((max_rows + 7) / 8, std::max(1, num_sms * 8 / gx)));
+  if (depth != 1) return cudaErrorInvalidValue;
   lcma_form_kernel<<<dim3(gx, std::min(gy, 65535), 2), 256, 0, stream>>>(f);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------- product kernel
 
-template <int BN>
+template <int BN, int D>
 struct LcmaCfg {
   static constexpr int kABytes = kBM * kBK * 2;        // this CTA's 128 rows of A
   static constexpr int kBBytes = kBK * (BN / 2) * 2;   // this CTA's BN/2 columns of B
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = BN == 256 ? 6 : 8;
   static constexpr int kTmemCols = BN == 256 ? 512 : 256;
-  static constexpr int kBarBytes = 1024;
+  // The combination queue after the barriers: head, taken, epilogue warps
+  // done, progress, then one word per job.  A tail unit hands at most
+  // kMaxTerms groups x 4 warps of combinations, and a pair has fewer than
+  // 7^D tail units.
+  static constexpr int kQueueOff = 256;
+  static constexpr int kQueueCap = D == 1 ? 128 : 1024;
+  static constexpr int kBarBytes = D == 1 ? 1024 : 5120;
   // After the barriers, one B half of slack: even a full-width MMA read of
   // the last stage stays inside this CTA's shared memory.
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kBBytes;
   static constexpr int kChunks = BN / 32;
-  static constexpr int kBlocks = 4;  // output blocks of one level
-  // The combination queue after the barriers: head, taken, epilogue warps
-  // done, then one word per job (a tail unit hands at most 4 groups x 4
-  // warps of combinations, and a pair has at most 7 tail units).
-  static constexpr int kQueueOff = 256;
-  static constexpr int kQueueCap = 128;
+  static constexpr int kBlocks = 1 << (2 * D);  // output blocks of D levels
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(kQueueOff + 4 * (4 + kQueueCap) <= kBarBytes, "combination queue does not fit");
+  static_assert(kMaxTerms * 4 * 7 <= kQueueCap && (D == 1 || kMaxTerms * 4 * 49 <= kQueueCap),
+                "a pair's tail jobs must fit the queue");
   static_assert(2 * BN <= kTmemCols, "two accumulator buffers must fit in TMEM");
   static_assert((2 * kStages + 5) * 8 + 4 <= kBarBytes, "barrier area too small");
 };
@@ -221,9 +302,9 @@ struct LcmaSchedule {
 // 16-byte accesses to one (chunk, quad) cover 512 contiguous bytes.  These
 // return the chunk's base; row r's quad q is at index q * 128 + r.  A CTA's
 // partials: `whole` slots (its whole positions) of the four blocks.
-template <int BN>
+template <int BN, int D>
 __device__ __forceinline__ float4* lcma_part(float* ws, long long whole, int cta, int slot, int blk, int c) {
-  using LC = LcmaCfg<BN>;
+  using LC = LcmaCfg<BN, D>;
   return reinterpret_cast<float4*>(
       ws + ((static_cast<size_t>(cta) * whole + slot) * LC::kBlocks + blk) * (kBM * BN) +
       static_cast<size_t>(c) * (kBM * 32));
@@ -269,14 +350,14 @@ __device__ __forceinline__ void lcma_put_row(float4* chunk, int r, const uint32_
 // alpha / bias / activation of output block blk (or, for SwiGLU, of gate
 // block 2 sr and up block 2 sr + 1 given as g and u) for 32 columns of chunk
 // c of position (tm, tn), and the store of C by this thread's row.
-template <int BN>
+template <int BN, int D>
 __device__ __forceinline__ void lcma_emit(const KernelParams& p, int blk, int c, int tm, int tn,
                                           uint32_t rank, int r, float (&v)[32]) {
-  const int col0 = (blk & 1) * p.sub_n + tn * BN + c * 32;
+  const int col0 = (blk & ((1 << D) - 1)) * p.sub_n + tn * BN + c * 32;
   float b[32];
   bias32(p, 0, col0, b);
   finish_plain(p, b, v);
-  store_row32(p, (blk >> 1) * p.sub_m + tm * (2 * kBM) + static_cast<int>(rank) * kBM + r, col0, v);
+  store_row32(p, (blk >> D) * p.sub_m + tm * (2 * kBM) + static_cast<int>(rank) * kBM + r, col0, v);
 }
 
 template <int BN>
@@ -293,10 +374,10 @@ __device__ __forceinline__ void lcma_emit_swiglu(const KernelParams& p, int sr, 
 // sum, in product order with the scheme's signs, of the stored accumulators
 // of the products that feed it, so the result does not depend on which unit
 // finished last.
-template <int BN>
+template <int BN, int D>
 __device__ void lcma_finish_tail(const LcmaParams& L, long long tail_pos, long long tail_n, int g, int tm,
                                  int tn, uint32_t rank, int ew) {
-  using LC = LcmaCfg<BN>;
+  using LC = LcmaCfg<BN, D>;
   const KernelParams& p = L.k;
   const int r = ew * 32 + (threadIdx.x & 31);
   const int np = p.num_products;
@@ -316,7 +397,7 @@ __device__ void lcma_finish_tail(const LcmaParams& L, long long tail_pos, long l
       for (int j = 0; j < 32; ++j) v[j] = 0.0f;
     }
   };
-  if (p.epi == kEpiSwiglu) {
+  if (D == 1 && p.epi == kEpiSwiglu) {
 #pragma unroll 1
     for (int c = 0; c < LC::kChunks; ++c) {
       float gv[32], uv[32];
@@ -329,7 +410,7 @@ __device__ void lcma_finish_tail(const LcmaParams& L, long long tail_pos, long l
     for (int c = 0; c < LC::kChunks; ++c) {
       float v[32];
       gather(g, c, v);
-      lcma_emit<BN>(p, g, c, tm, tn, rank, r, v);
+      lcma_emit<BN, D>(p, g, c, tm, tn, rank, r, v);
     }
   }
 }
@@ -398,10 +479,10 @@ static __device__ __noinline__ bool lcma_wait_formed(const LcmaParams& L, int j)
 // may wait for its next job as long as the epilogue keeps finishing
 // accumulators (queue word 3 counts them): its bound restarts at each one.
 // It leaves on another role's error.
-template <int BN>
+template <int BN, int D>
 __device__ __forceinline__ void lcma_tail_helper(const LcmaParams& L, volatile uint32_t* q,
                                                  const LcmaSchedule& sched, uint32_t rank) {
-  using LC = LcmaCfg<BN>;
+  using LC = LcmaCfg<BN, D>;
   const KernelParams& p = L.k;
   const int lane = threadIdx.x & 31;
 #pragma unroll 1
@@ -441,17 +522,17 @@ __device__ __forceinline__ void lcma_tail_helper(const LcmaParams& L, volatile u
     job = __shfl_sync(0xFFFFFFFFu, job, 0);
     if (quit) break;
     __threadfence();  // the feeding units' stores, seen by the appending warp, are seen here
-    const long long tail_pos = static_cast<long long>((job & 0x7FFFFFFFu) >> 4);
+    const long long tail_pos = static_cast<long long>((job & 0x7FFFFFFFu) >> 6);
     int tm, tn;
     unit_coords(p, static_cast<int>(sched.tail0 + tail_pos), tm, tn);
-    lcma_finish_tail<BN>(L, tail_pos, sched.tail_n, static_cast<int>((job >> 2) & 3u), tm, tn, rank,
-                         static_cast<int>(job & 3u));
+    lcma_finish_tail<BN, D>(L, tail_pos, sched.tail_n, static_cast<int>((job >> 2) & 15u), tm, tn, rank,
+                            static_cast<int>(job & 3u));
   }
 }
 
-template <int BN>
+template <int BN, int D>
 __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_constant__ LcmaParams L) {
-  using LC = LcmaCfg<BN>;
+  using LC = LcmaCfg<BN, D>;
   constexpr int S = LC::kStages;
   const KernelParams& p = L.k;
 
@@ -480,7 +561,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
   const LcmaSchedule sched(p.num_units, pairs, np, L.tail_at, cluster);
   const long long n_items = sched.items(np);
 
-  if (threadIdx.x < 4 + LC::kQueueCap) queue[threadIdx.x] = 0u;
+  for (int i = threadIdx.x; i < 4 + LC::kQueueCap; i += blockDim.x) queue[i] = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(full(s), 1);
@@ -527,10 +608,11 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
         Src o;
         o.amap = P.a_temp ? &L.tmap_ta : &p.tmap_a;
         o.bmap = P.b_temp ? &L.tmap_tb : &p.tmap_b;
-        o.ay = (P.a_temp ? P.a_idx : (P.a_idx >> 1)) * p.sub_m + tm * (2 * kBM) + static_cast<int>(rank) * kBM;
-        o.ax = P.a_temp ? 0 : (P.a_idx & 1) * p.sub_k;
-        o.by = (P.b_temp ? P.b_idx : (P.b_idx >> 1)) * p.sub_k;
-        o.bx = (P.b_temp ? 0 : (P.b_idx & 1) * p.sub_n) + tn * BN + static_cast<int>(rank) * (BN / 2);
+        constexpr int kCol = (1 << D) - 1;
+        o.ay = (P.a_temp ? P.a_idx : (P.a_idx >> D)) * p.sub_m + tm * (2 * kBM) + static_cast<int>(rank) * kBM;
+        o.ax = P.a_temp ? 0 : (P.a_idx & kCol) * p.sub_k;
+        o.by = (P.b_temp ? P.b_idx : (P.b_idx >> D)) * p.sub_k;
+        o.bx = (P.b_temp ? 0 : (P.b_idx & kCol) * p.sub_n) + tn * BN + static_cast<int>(rank) * (BN / 2);
         return o;
       };
       // sides whose temporaries this producer may read (the pre-pass formed
@@ -621,7 +703,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
     // ------------------------------------------- operand formation (both CTAs)
     if (L.form_tasks[0] + L.form_tasks[1] > 0) lcma_form_bands(L);
     // ------------------------------------------- tail combinations (both CTAs)
-    lcma_tail_helper<BN>(L, queue, sched, rank);
+    lcma_tail_helper<BN, D>(L, queue, sched, rank);
   } else if (warp >= 4) {
     // ------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 4;
@@ -657,8 +739,8 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
         for (int t = 0; t < nc; ++t) {
           const uint8_t code = P.c[t];
           if (code & kTermLast) continue;
-          lcma_put_row(lcma_part<BN>(p.workspace, sched.whole, static_cast<int>(blockIdx.x), it.slot,
-                                     code & kTermIndexMask, c),
+          lcma_put_row(lcma_part<BN, D>(p.workspace, sched.whole, static_cast<int>(blockIdx.x), it.slot,
+                                        code & kTermIndexMask, c),
                        r, ar,
                        (code & kTermNeg) ? -1.0f : 1.0f, !(code & kTermFirst));
         }
@@ -676,7 +758,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
             sg = (P.c[t] & kTermNeg) ? -1.0f : 1.0f;
           }
           if (!first)
-            lcma_load_row(lcma_part<BN>(p.workspace, sched.whole, static_cast<int>(blockIdx.x), it.slot, blk, c),
+            lcma_load_row(lcma_part<BN, D>(p.workspace, sched.whole, static_cast<int>(blockIdx.x), it.slot, blk, c),
                           r, v, false, 1.0f);
           if (fed) {
             uint32_t x[32];
@@ -687,7 +769,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
             for (int j = 0; j < 32; ++j) v[j] = first ? sg * __uint_as_float(x[j]) : v[j] + sg * __uint_as_float(x[j]);
           }
         };
-        if (p.epi == kEpiSwiglu) {
+        if (D == 1 && p.epi == kEpiSwiglu) {
 #pragma unroll 1
           for (int sr = 0; sr < 2; ++sr) {
             if (!((P.fin >> sr) & 1u)) continue;
@@ -702,7 +784,7 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
             if (!((P.fin >> blk) & 1u)) continue;
             float v[32];
             final_block(blk, v);
-            lcma_emit<BN>(p, blk, c, tm, tn, rank, r, v);
+            lcma_emit<BN, D>(p, blk, c, tm, tn, rank, r, v);
           }
         }
       }
@@ -717,16 +799,17 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
       __threadfence();
       __syncwarp();
 #pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < LC::kBlocks; ++g) {
         if (!((P.groups >> g) & 1u)) continue;
         const bool last = count_arrival(
-            p, p.split_ctr + ((static_cast<size_t>(tail_pos) * 4 + g) * 2 + rank) * 4 + ew, L.group_pieces[g]);
+            p, p.split_ctr + ((static_cast<size_t>(tail_pos) * LC::kBlocks + g) * 2 + rank) * 4 + ew,
+            L.group_pieces[g]);
         if (!last) continue;
         __threadfence();
         if (lane == 0) {
           const uint32_t slot = atomicAdd(const_cast<uint32_t*>(queue), 1u);
           if (slot < static_cast<uint32_t>(LC::kQueueCap))
-            queue[4 + slot] = 0x80000000u | (static_cast<uint32_t>(tail_pos) << 4) |
+            queue[4 + slot] = 0x80000000u | (static_cast<uint32_t>(tail_pos) << 6) |
                               (static_cast<uint32_t>(g) << 2) | static_cast<uint32_t>(ew);
           else
             atomicCAS(p.err, 0u, err_code(2));  // not reached: the host bounds the units per pair
@@ -747,11 +830,11 @@ __global__ void __launch_bounds__(256, 1) fgemm_kernel_pair_lcma(const __grid_co
   if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, LC::kTmemCols);
 }
 
-template <int BN>
+template <int BN, int D>
 cudaError_t lcma_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1], int& fit,
                         cudaStream_t stream) {
-  auto kern = fgemm_kernel_pair_lcma<BN>;
-  constexpr int smem = LcmaCfg<BN>::kSmemBytes;
+  auto kern = fgemm_kernel_pair_lcma<BN, D>;
+  constexpr int smem = LcmaCfg<BN, D>::kSmemBytes;
   static unsigned long long configured = 0;
   static int clusters_fit[64] = {0};
   int dev = 0;
@@ -785,35 +868,40 @@ cudaError_t lcma_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[1],
   return cudaSuccess;
 }
 
-int lcma_pair_clusters_fit(int bn) {
+int lcma_pair_clusters_fit(int bn, int depth) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   int fit = 0;
-  cudaError_t e = bn == 256   ? lcma_config<256>(cfg, attr, fit, nullptr)
-                  : bn == 128 ? lcma_config<128>(cfg, attr, fit, nullptr)
-                              : cudaErrorInvalidValue;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (depth == 1)
+    e = bn == 256 ? lcma_config<256, 1>(cfg, attr, fit, nullptr)
+                  : (bn == 128 ? lcma_config<128, 1>(cfg, attr, fit, nullptr) : cudaErrorInvalidValue);
+  else if (depth == 2)
+    e = bn == 256 ? lcma_config<256, 2>(cfg, attr, fit, nullptr)
+                  : (bn == 128 ? lcma_config<128, 2>(cfg, attr, fit, nullptr) : cudaErrorInvalidValue);
   return e == cudaSuccess ? fit : 0;
 }
 
-template <int BN>
+template <int BN, int D>
 cudaError_t launch_lcma_pair_t(const LcmaParams& L, int clusters, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   int fit = 0;
-  cudaError_t e = lcma_config<BN>(cfg, attr, fit, stream);
+  cudaError_t e = lcma_config<BN, D>(cfg, attr, fit, stream);
   if (e != cudaSuccess) return e;
-  if (clusters < 1 || clusters > fit || clusters > L.k.num_units * L.k.num_products)
+  if (clusters < 1 || clusters > fit || clusters > L.k.num_units * L.k.num_products ||
+      L.k.num_products != (D == 1 ? 7 : 49) || (D == 2 && L.k.epi == kEpiSwiglu))
     return cudaErrorInvalidValue;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  return cudaLaunchKernelEx(&cfg, fgemm_kernel_pair_lcma<BN>, L);
+  return cudaLaunchKernelEx(&cfg, fgemm_kernel_pair_lcma<BN, D>, L);
 }
 
-cudaError_t launch_lcma_pair(int bn, const LcmaParams& L, int clusters, cudaStream_t stream) {
-  switch (bn) {
-    case 128: return launch_lcma_pair_t<128>(L, clusters, stream);
-    case 256: return launch_lcma_pair_t<256>(L, clusters, stream);
-    default: return cudaErrorInvalidValue;
-  }
+cudaError_t launch_lcma_pair(int bn, int depth, const LcmaParams& L, int clusters, cudaStream_t stream) {
+  if (depth == 1 && bn == 128) return launch_lcma_pair_t<128, 1>(L, clusters, stream);
+  if (depth == 1 && bn == 256) return launch_lcma_pair_t<256, 1>(L, clusters, stream);
+  if (depth == 2 && bn == 128) return launch_lcma_pair_t<128, 2>(L, clusters, stream);
+  if (depth == 2 && bn == 256) return launch_lcma_pair_t<256, 2>(L, clusters, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fgemm

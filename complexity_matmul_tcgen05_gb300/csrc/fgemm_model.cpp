@@ -70,7 +70,8 @@ bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo
   if (tile_m != 128 && tile_m != 256) return false;
   if (epi_kind == FGEMM_EPI_SWIGLU && tile_n == 64) return false;
   const int d = depth_of(algo);
-  if (tile_m == 256 && (tile_n < 128 || d == 2)) return false;
+  if (tile_m == 256 && tile_n < 128) return false;
+  if (tile_m == 256 && d == 2 && epi_kind == FGEMM_EPI_SWIGLU) return false;
   if (d == 0) return true;
   if (tile_n == 64) return false;
   const int64_t g = int64_t{1} << d;
@@ -117,6 +118,13 @@ void fgemm_model_default(fgemm_device_model_t* out, int32_t num_sms, double peak
   // rate above)
   m.eff_strassen_pair[0] = rate(1121.0);  // 256 x 128
   m.eff_strassen_pair[1] = rate(1720.0);  // 256 x 256: the product kernel at 16384^3, 4.51 ms at full clocks
+  // two levels on CTA pairs: the same product kernel (its MMAs at the
+  // one-level rate), each unit's fold into about three of the 16 output
+  // blocks about 30 us at 256 columns (fitted to 4096 x 19456 x {4096,
+  // 16384}, 16384^3 and 32768^3: 33, 45, 48 and 64 us per unit)
+  m.eff_strassen2_pair[0] = rate(1121.0);  // 256 x 128
+  m.eff_strassen2_pair[1] = rate(1720.0);  // 256 x 256
+  m.fold2_unit_us = 30.0;
   // launch: back-to-back calls of a one-kernel product; fill: the first
   // MMA about 1.5 us after the start, the last 256 x 256 tile's epilogue
   // about 5 us after the last MMA (timestamps of an instrumented build)
@@ -377,17 +385,18 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
   const int d = depth_of(algo);
   const bool swiglu = epi_kind == FGEMM_EPI_SWIGLU;
   const bool pair = tile_m == 256;
-  if (pair && d == 1) {
-    // One level on CTA pairs with the summed operands streamed through HBM:
-    // a pre-pass reads A and B once and writes each summed operand once
-    // (Strassen: 5 + 5 of the 4 + 4 blocks, Winograd: 4 + 4), then the seven
-    // block products run on the classical pair mainloop: whole positions in
-    // waves over the pairs, the partial last wave's positions as separate
-    // product units shared out evenly, whose combination costs about one
-    // more fill.
+  if (pair && d >= 1) {
+    // One or two levels on CTA pairs with the summed operands streamed
+    // through HBM: a pre-pass reads A and B once and writes each summed
+    // operand once (one level: Strassen 5 + 5 of the 4 + 4 blocks, Winograd
+    // 4 + 4; two levels: 45 + 45 of the 16 + 16), then the 7^d block
+    // products run on the classical pair mainloop: whole positions in waves
+    // over the pairs, the partial last wave's positions as separate product
+    // units shared out evenly, whose combination costs about one more fill.
     const bool wino = algo == FGEMM_ALGO_WINOGRAD1;
-    const int64_t sub_m = M / 2, sub_n = N / 2, sub_k = K / 2;
-    const double temps = wino ? 4.0 : 5.0;
+    const int64_t sub_m = M >> d, sub_n = N >> d, sub_k = K >> d;
+    const int64_t np = d == 1 ? 7 : 49;
+    const double temps = d == 2 ? 45.0 : (wino ? 4.0 : 5.0);
     const double pre_bytes = 2.0 * (static_cast<double>(M) * K + static_cast<double>(K) * N +
                                     temps * (static_cast<double>(sub_m) * sub_k +
                                              static_cast<double>(sub_k) * sub_n));
@@ -395,14 +404,25 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
                    dev->launch_us;
     const int64_t positions = fgemm_model_tiles(sub_m, sub_n, 256, tile_n);
     const int32_t pairs = std::max(1, dev->num_sms / 2);
-    const int64_t units = positions * 7;
-    const int64_t used = std::min<int64_t>(pairs, units);
+    const int64_t units = positions * np;
+    // (two levels with fewer positions than pairs: one pair per position)
+    const int64_t used = d == 2 && positions < pairs ? positions : std::min<int64_t>(pairs, units);
     const int64_t whole = positions / used;
-    const int64_t tail_units = (positions % used) * 7;
-    const double eff = std::max(dev->eff_strassen_pair[tile_n == 128 ? 0 : 1], 1e-3);
+    const int64_t tail_units = (positions % used) * np;
+    const double eff = std::max(d == 2 ? dev->eff_strassen2_pair[tile_n == 128 ? 0 : 1]
+                                       : dev->eff_strassen_pair[tile_n == 128 ? 0 : 1],
+                                1e-3);
     const double pair_flop_per_us = dev->peak_tflops * 1e6 / dev->num_sms * 2.0;
     const double k_pad = static_cast<double>(ceil_div(sub_k, fgemm::kBK) * fgemm::kBK);
-    const double t_unit = 2.0 * 256.0 * tile_n * k_pad / (pair_flop_per_us * eff);
+    double t_unit = 2.0 * 256.0 * tile_n * k_pad / (pair_flop_per_us * eff);
+    if (d == 2) {
+      // the fold of a unit into its output blocks (fp32 reductions at the
+      // L2) overlaps its MMAs only in part: the longer of the two, plus a
+      // share kFoldOverlap of the shorter
+      constexpr double kFoldOverlap = 0.55;
+      const double fold = std::max(dev->fold2_unit_us, 0.0) * tile_n / 256.0;
+      t_unit = std::max(t_unit, fold) + kFoldOverlap * std::min(t_unit, fold);
+    }
     // The product kernel forms sums itself while the products that do not
     // read them run first: Winograd's two sum-free products (A11 B11, A12 B21)
     // cover both sides' sums, formed A's then B's; Strassen's M2 and M5 read
@@ -412,7 +432,7 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
     // and any part of it still running when the first product that reads
     // the last side formed starts.
     const int64_t lead = 2;
-    if (lead * whole >= fgemm::kFusedMinWaves && sub_m % fgemm::kFormRows == 0 &&
+    if (d == 1 && lead * whole >= fgemm::kFusedMinWaves && sub_m % fgemm::kFormRows == 0 &&
         sub_k % fgemm::kFormRows == 0) {
       const double a_bytes = 2.0 * (static_cast<double>(M) * K + temps * static_cast<double>(sub_m) * sub_k);
       const double b_bytes = 2.0 * (static_cast<double>(K) * N + temps * static_cast<double>(sub_k) * sub_n);
@@ -426,10 +446,10 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
       if (!wino)  // A's sums by the pre-pass
         t_pre += a_bytes / (dev->hbm_gbs * 1e3 * std::max(dev->hbm_stream_eff, 1e-3)) + dev->launch_us;
     }
-    const double per_pair = static_cast<double>(whole * 7 + ceil_div(tail_units, used));
+    const double per_pair = static_cast<double>(whole * np + ceil_div(tail_units, used));
     const double t_compute = per_pair * t_unit + dev->tile_fill_us * (tail_units > 0 ? 2.0 : 1.0) +
                              operand_dram_us(dev, ceil_div(sub_m, 256), ceil_div(sub_n, tile_n), 256, tile_n,
-                                             k_pad, pairs, 7.0);
+                                             k_pad, pairs, static_cast<double>(np));
     if (predicted_us) *predicted_us = t_pre + t_compute + dev->launch_us;
     return FGEMM_OK;
   }
@@ -537,6 +557,9 @@ std::vector<std::pair<const char*, double*>> model_fields(fgemm_device_model_t& 
       {"eff_strassen2_256", &m.eff_strassen[1][1]},
       {"eff_strassen1_pair_128", &m.eff_strassen_pair[0]},
       {"eff_strassen1_pair_256", &m.eff_strassen_pair[1]},
+      {"eff_strassen2_pair_128", &m.eff_strassen2_pair[0]},
+      {"eff_strassen2_pair_256", &m.eff_strassen2_pair[1]},
+      {"fold2_unit_us", &m.fold2_unit_us},
       {"launch_us", &m.launch_us},
       {"tile_fill_us", &m.tile_fill_us},
       {"l2_bytes", &m.l2_bytes},
@@ -606,7 +629,8 @@ extern "C" fgemm_status_t fgemm_model_load_json(const char* path, fgemm_device_m
     for (double* e : {&m.eff_classical[0], &m.eff_classical[1], &m.eff_classical[2], &m.eff_pair[0],
                       &m.eff_pair[1], &m.eff_strassen[0][0], &m.eff_strassen[0][1],
                       &m.eff_strassen[1][0], &m.eff_strassen[1][1], &m.eff_strassen_pair[0],
-                      &m.eff_strassen_pair[1], &m.eff_winograd[0], &m.eff_winograd[1],
+                      &m.eff_strassen_pair[1], &m.eff_strassen2_pair[0], &m.eff_strassen2_pair[1],
+                      &m.eff_winograd[0], &m.eff_winograd[1],
                       &m.eff_small_m[0], &m.eff_small_m[1], &m.eff_small_m[2]})
       *e *= r;
     const double rb = old_bw / m.hbm_gbs;

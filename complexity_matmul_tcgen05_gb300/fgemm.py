@@ -62,7 +62,9 @@ class DeviceModel(ctypes.Structure):
                 ("form_in_kernel_drag", ctypes.c_double),
                 ("lcma_margin", ctypes.c_double),
                 ("dram_miss_slope", ctypes.c_double),
-                ("dram_exposed", ctypes.c_double)]
+                ("dram_exposed", ctypes.c_double),
+                ("eff_strassen2_pair", ctypes.c_double * 2),
+                ("fold2_unit_us", ctypes.c_double)]
 
 
 _lib = None

@@ -50,7 +50,11 @@ typedef enum {
   FGEMM_ALGO_AUTO = 0,
   FGEMM_ALGO_CLASSICAL = 1,
   FGEMM_ALGO_STRASSEN1 = 2, /* one Strassen level: 7 half-size products */
-  FGEMM_ALGO_STRASSEN2 = 3, /* two levels: 49 quarter-size products */
+  FGEMM_ALGO_STRASSEN2 = 3, /* two levels: 49 quarter-size products. One-CTA
+                             * tiles (tile_m 128, sums formed on chip) or CTA
+                             * pairs (tile_m 256: the 49 leaf operands of each
+                             * side formed by a pre-pass, each from the 16
+                             * quarter blocks with one rounding; no SWIGLU) */
   FGEMM_ALGO_WINOGRAD1 = 4  /* one level of Winograd's variant: 7 half-size
                              * products whose operands are sums of up to four
                              * blocks (FalconGEMM summary, "Methodology" item 1
@@ -146,13 +150,13 @@ fgemm_status_t fgemm_matmul(fgemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * As fgemm_matmul, with the output tile forced (used for exhaustive timing of
  * the decision model's choices). tile_m = 128: one CTA per tile, tile_n in
  * {64, 128, 256}; tile_m = 256: a pair of CTAs (one M = 256 tensor-core
- * operation across two SMs), tile_n in {128, 256}, classical and one-level
- * Strassen forms; tile_m = 16, 32 or 64: the small-M kernel for M <= tile_m
+ * operation across two SMs), tile_n in {128, 256}, every form (two
+ * Strassen levels without SWIGLU); tile_m = 16, 32 or 64: the small-M kernel for M <= tile_m
  * (classical, no SWIGLU, tile_n = 128 columns of C per tile): it computes
  * C^T = B^T A^T so that the tensor-core rows run over N, and shares the K
  * blocks of all tiles evenly over the CTAs of the grid fgemm_small_m_grid
  * picks (pieces of a tile are summed in a fixed order). SWIGLU needs tile_n >= 128; the Strassen forms use tile_n in
- * {128, 256}, two levels only with tile_m = 128. tile_m = tile_n = 0 lets
+ * {128, 256}. tile_m = tile_n = 0 lets
  * the model choose; a zero in only one of them lets the model choose the
  * other.
  */
@@ -326,7 +330,8 @@ fgemm_status_t fgemm_get_error(fgemm_handle_t h);
  * arguments launches on the handle with its current settings (the plan AUTO
  * or the forced form resolves to; for one Strassen-like level on CTA pairs,
  * the operand pre-pass unless the product kernel forms the sums itself, see
- * fgemm_set_lcma_formation). Host only: launches nothing. Writes *launches;
+ * fgemm_set_lcma_formation; for two levels on CTA pairs, always the
+ * pre-pass and the product kernel). Host only: launches nothing. Writes *launches;
  * returns the plan's errors (FGEMM_ERR_UNSUPPORTED for an illegal forced
  * form) or FGEMM_ERR_INVALID_ARG for a NULL handle, a NULL output or an
  * unknown algorithm.
@@ -490,6 +495,12 @@ typedef struct {
                             * DRAM per unit of (panel bytes of one wave / L2 - 1),
                             * capped at 1 */
   double dram_exposed;     /* part of that DRAM time not hidden by the MMAs */
+  double eff_strassen2_pair[2]; /* two levels on CTA pairs, 256 x {128, 256}:
+                                 * the product kernel's MMA rate */
+  double fold2_unit_us;    /* two levels on CTA pairs: the epilogue's fold of
+                            * one 256 x 256 product unit into its ~3 output
+                            * blocks (fp32 reductions at the L2), which
+                            * overlaps the unit's MMAs only in part */
 } fgemm_device_model_t;
 
 /*

@@ -92,12 +92,16 @@ def test_validation_codes(L):
     assert _v(256, 256, 96, lda=96, algo="strassen1") == fgemm.ERR_UNSUPPORTED
     assert _v(512, 512, 256, algo="strassen2", tile=128) == ok
     assert _v(256, 512, 256, algo="strassen2") == fgemm.ERR_UNSUPPORTED
-    # CTA-pair tiles: 256 x {128, 256}, classical and one-level Strassen
+    # CTA-pair tiles: 256 x {128, 256}, classical and one or two Strassen levels
     assert _v(512, 512, 256, tile_m=256, tile=128) == ok
     assert _v(512, 512, 256, tile_m=256, tile=64) == fgemm.ERR_UNSUPPORTED
     assert _v(512, 512, 256, algo="strassen1", tile_m=256) == ok
     assert _v(256, 512, 256, algo="strassen1", tile_m=256) == fgemm.ERR_UNSUPPORTED  # 2 x 256 rows
-    assert _v(1024, 1024, 512, algo="strassen2", tile_m=256) == fgemm.ERR_UNSUPPORTED
+    assert _v(1024, 1024, 512, algo="strassen2", tile_m=256) == ok   # 4 x 256 rows, 4 x 256 columns
+    assert _v(512, 1024, 512, algo="strassen2", tile_m=256) == fgemm.ERR_UNSUPPORTED
+    assert _v(1024, 1024, 128, algo="strassen2", tile_m=256) == fgemm.ERR_UNSUPPORTED  # K / 4 < 64
+    assert _v(1024, 2048, 512, algo="strassen2", tile_m=256,
+              epi=fgemm.make_epilogue("swiglu", 1.0, None)) == fgemm.ERR_UNSUPPORTED
     assert _v(512, 512, 256, tile_m=192) == fgemm.ERR_INVALID_ARG
     assert _v(100, 512, 256, tile_m=256) == ok                     # ragged rows are fine
 
@@ -657,3 +661,40 @@ def test_model_operand_dram_term_and_the_large_cube_picks(L):
     assert with_term[1] > without[1] * 1.05           # 24576^3: about 1.4 ms of 17
     assert pick(24576)[0] == "classical"              # and without it AUTO stays classical
     m.dram_exposed = exposed
+
+
+def test_model_two_levels_on_pairs_fold_term_and_picks(L):
+    """Two Strassen levels on CTA pairs: each product unit's fold (about
+    three fp32 output-block reductions) overlaps its MMAs only in part, so a
+    unit costs the longer of the two plus a share of the shorter: the
+    prediction grows with the fold time and is at least the fold time per
+    unit; with fewer positions than pairs each pair runs one position whole.
+    AUTO takes the form on none of the cubes or sweep shapes (it is slower
+    than the classical kernel up to 32768^3 and than one Winograd level)."""
+    m = _model(L, peak=0.0, bw=0.0)
+    n = 16384
+    s, base = _predict(L, m, n, n, n, "strassen2", 256, tile_m=256)
+    assert s == fgemm.OK
+    m.fold2_unit_us = 60.0
+    _, slower = _predict(L, m, n, n, n, "strassen2", 256, tile_m=256)
+    assert slower > base
+    units_per_pair = 3 * 49 + -(-(28 * 49) // 76)  # 256 positions: 3 whole waves + 28 positions as units
+    assert slower >= units_per_pair * 60.0
+    m.fold2_unit_us = 30.0
+    # 4096 x 16384: 64 positions on 76 pairs -> 49 units per pair, no tail
+    _, t64 = _predict(L, m, 4096, 16384, 16384, "strassen2", 256, tile_m=256)
+    _, t76 = _predict(L, m, 4096, 19456, 16384, "strassen2", 256, tile_m=256)
+    assert abs(t64 - t76) < 0.05 * t76
+    assert _predict(L, m, 4096, 4096, 4096, "strassen2", 256, epi=3, tile_m=256)[0] == fgemm.ERR_UNSUPPORTED
+
+    def pick(M, N, K):
+        a = ctypes.c_int()
+        tm, tn, us = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+        assert L.fgemm_model_plan(ctypes.byref(m), M, N, K, 0, ctypes.byref(a), ctypes.byref(tm),
+                                  ctypes.byref(tn), ctypes.byref(us)) == fgemm.OK
+        return fgemm.ALGO_NAMES[a.value], tm.value
+
+    shapes = [(c, c, c) for c in (4096, 8192, 16384, 24576, 32768, 49152)] + \
+        [(M, k, k) for M in (16, 128, 1024, 8192) for k in (2048, 4096, 8192, 16384)]
+    for shape in shapes:
+        assert pick(*shape)[0] != "strassen2", shape

@@ -108,8 +108,8 @@ def test_ffn_up_swiglu(algo, tile_m):
 
 
 @pytest.mark.parametrize("algo,tile_m", [("classical", 0), ("strassen1", 256), ("strassen1", 128),
-                                         ("strassen2", 128), ("winograd1", 256), ("winograd1", 128),
-                                         ("auto", 0)])
+                                         ("strassen2", 128), ("strassen2", 256), ("winograd1", 256),
+                                         ("winograd1", 128), ("auto", 0)])
 def test_square_16384(algo, tile_m):
     A, B, _ = inputs.workload_inputs("square_16384_bf16", DEV)
     _sampled_check("square_16384", A, B, None, algo, "none", "bf16", tile_m=tile_m)

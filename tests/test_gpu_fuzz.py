@@ -81,8 +81,19 @@ def _many_case(rng):
                 dtype=dtype, epi=rng.choice(["scale_bias", "none"]), split=split, formation=formation)
 
 
+def _strassen2_pair_case(rng):
+    """Two Strassen levels on CTA pairs (the operands from the pre-pass)."""
+    tn = rng.choice([128, 256])
+    return dict(kind="strassen2_pair", algo="strassen2", tile_m=256, tile_n=tn, M=1024 * rng.randrange(1, 4),
+                N=4 * tn * rng.randrange(1, 4), K=256 * rng.randrange(1, 4), dtype=rng.choice(["bf16", "f16"]),
+                epi=rng.choice(["scale_bias", "none"]), split=rng.choice(["auto", "off", "force"]),
+                formation=rng.choice(["auto", "prepass", "in_kernel"]))
+
+
 _RNG = random.Random(20260603)
-CASES = [_case(_RNG) for _ in range(192)] + [_many_case(_RNG) for _ in range(32)]
+_RNG2 = random.Random(20261203)
+CASES = [_case(_RNG) for _ in range(192)] + [_many_case(_RNG) for _ in range(32)] + \
+    [_strassen2_pair_case(_RNG2) for _ in range(24)]
 
 
 def _id(c):

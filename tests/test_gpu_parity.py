@@ -155,6 +155,76 @@ def test_lcma_cta_pair_deterministic_and_graph_replay(algo):
         assert torch.equal(C.view(torch.int16), C1.view(torch.int16))
 
 
+# Two Strassen levels on CTA pairs: the 49 leaf operands of each side formed
+# by the pre-pass (each from the 16 quarter blocks, one rounding), 49
+# quarter-size products per position, folded into 16 output blocks.
+# 1024^2 x 256 at 256 has one position (49 units over 49 pairs); 2048 x 4096
+# has 8 positions (392 units over the pairs); 8192^2 at tile 128 has 128
+# positions: one whole wave over the pairs plus a partial one; 16384 x 8192
+# at tile 128 has 256: three whole waves (each pair's positions run outer
+# product by outer product, the seven inner products back to back).
+LCMA2_PAIR_CASES = [(1024, 1024, 256, 256), (1024, 1024, 256, 128), (2048, 4096, 512, 256),
+                    (4096, 4096, 1024, 256), (8192, 8192, 256, 128), (16384, 8192, 256, 128)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("M,N,K,tile", LCMA2_PAIR_CASES)
+def test_exact_ternary_strassen2_cta_pair(M, N, K, tile, dtype):
+    """Two Strassen levels on CTA pairs: RNE(exact C) bit for bit (operand
+    sums in [-4, 4], products and folds exact in fp32)."""
+    A, B, bias = _ternary(M, N, K, dtype)
+    C = run(A, B, algo="strassen2", epilogue="scale_bias", bias=bias, tile_n=tile, tile_m=256)
+    assert np.array_equal(gpu_bits(C), _exact_reference(A, B, bias, dtype))
+
+
+@pytest.mark.parametrize("tile", [256, 128])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("epilogue,alpha", [("none", 1.0), ("silu", 1.25)])
+def test_strassen2_cta_pair_every_entry_and_emulation(tile, dtype, epilogue, alpha):
+    """Every entry within the two-level budget, and the tight pin against the
+    oracle's emulated two-level Strassen (leaf operands rounded once)."""
+    M, N, K = 1024, 2048, 1024
+    A = inputs.matrix(M, K, "uniform", dtype, 80, DEV)
+    B = inputs.matrix(K, N, "uniform", dtype, 81, DEV)
+    bias = inputs.matrix(1, N, "normal_0.02", dtype, 82, DEV)[0] if epilogue != "none" else None
+    _full_check(A, B, "strassen2", dtype, epilogue, alpha, bias, tile, 2, tile_m=256)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_strassen2_cta_pair_whole_positions_emulation(dtype):
+    """Three whole waves of positions (the two-stage fold) besides a partial
+    one: every entry against the oracle's emulated two-level Strassen."""
+    M, N, K = 16384, 8192, 256
+    A = inputs.matrix(M, K, "uniform", dtype, 85, DEV)
+    B = inputs.matrix(K, N, "uniform", dtype, 86, DEV)
+    _full_check(A, B, "strassen2", dtype, "none", 1.0, None, 128, 2, tile_m=256)
+
+
+def test_strassen2_cta_pair_deterministic_and_graph_replay():
+    """Two launches give the same bits; a captured graph (pre-pass and
+    product kernel) replays with the same result."""
+    M, N, K = 4096, 4096, 1024
+    A = inputs.matrix(M, K, "uniform", "bf16", 83, DEV)
+    B = inputs.matrix(K, N, "uniform", "bf16", 84, DEV)
+    kw = dict(algo="strassen2", tile_n=256, tile_m=256)
+    assert fgemm.default_handle().call_launches(M, N, K, **kw) == 2
+    C1 = run(A, B, **kw)
+    C2 = run(A, B, **kw)
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+    C = torch.empty_like(C1)
+    fgemm.matmul(A, B, out=C, **kw)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fgemm.matmul(A, B, out=C, **kw)
+    for _ in range(3):
+        C.view(torch.int16).fill_(0x7F7B)
+        g.replay()
+        torch.cuda.synchronize()
+        assert fgemm.default_handle().get_error() == fgemm.OK
+        assert torch.equal(C.view(torch.int16), C1.view(torch.int16))
+
+
 @pytest.fixture
 def formation():
     """Sets the default handle's operand-formation mode for one test, then
