@@ -528,11 +528,7 @@ fgemm_status_t launch_lcma(fgemm_handle_t h, KernelParams& p, const StrassenTabl
   if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the Strassen pair launch");
   const long long positions = p.num_units;
   L.units = positions * np;
-  // two levels with fewer positions than pairs: one pair per position, each
-  // running its position whole (a partial wave cut into 49 units per
-  // position would leave 49-way combinations to the helper warps)
-  const int clusters = depth == 2 && positions < fit ? static_cast<int>(positions)
-                                                     : static_cast<int>(std::min<long long>(fit, L.units));
+  const int clusters = static_cast<int>(fgemm_lcma_pair_clusters(positions, depth, fit));
   // the positions of the partial last wave run as separate product units;
   // every CTA keeps the partials of each of its whole positions
   const long long tail_positions = positions % clusters;

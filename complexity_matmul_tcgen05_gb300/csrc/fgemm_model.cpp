@@ -350,6 +350,24 @@ fgemm_status_t model_search(const fgemm_device_model_t* dev, int64_t M, int64_t 
 }  // namespace fgemm
 }  // extern "C++"
 
+int64_t fgemm_lcma_pair_clusters(int64_t positions, int32_t depth, int32_t fit) {
+  if (positions <= 0 || fit <= 0) return 0;
+  const int64_t units = positions * (depth == 2 ? 49 : 7);
+  if (depth != 2) return std::min<int64_t>(fit, units);
+  // Two levels: each position of a partial last wave becomes 49 product
+  // units whose combinations the helper warps run.  With fewer positions
+  // than pairs, one pair per position; with more than 24 such units per pair
+  // (8192 x 16384^2 at 256 x 256: 34 per pair, 14.6 ms against 4.6 at
+  // 256 x 128), the most pairs, down to half of them, that divide the
+  // positions into whole waves.
+  if (positions < fit) return positions;
+  const int64_t tail = positions % fit;
+  if ((tail * 49 + fit - 1) / fit <= 24) return fit;
+  for (int64_t c = fit; 2 * c >= fit; --c)
+    if (positions % c == 0) return c;
+  return fit;
+}
+
 fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, int64_t N,
                                    int64_t K, int32_t epi_kind, fgemm_algo_t algo, int32_t tile_m,
                                    int32_t tile_n, double* predicted_us) {
@@ -404,9 +422,7 @@ fgemm_status_t fgemm_model_predict(const fgemm_device_model_t* dev, int64_t M, i
                    dev->launch_us;
     const int64_t positions = fgemm_model_tiles(sub_m, sub_n, 256, tile_n);
     const int32_t pairs = std::max(1, dev->num_sms / 2);
-    const int64_t units = positions * np;
-    // (two levels with fewer positions than pairs: one pair per position)
-    const int64_t used = d == 2 && positions < pairs ? positions : std::min<int64_t>(pairs, units);
+    const int64_t used = fgemm_lcma_pair_clusters(positions, d, pairs);
     const int64_t whole = positions / used;
     const int64_t tail_units = (positions % used) * np;
     const double eff = std::max(d == 2 ? dev->eff_strassen2_pair[tile_n == 128 ? 0 : 1]

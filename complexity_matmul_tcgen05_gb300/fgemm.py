@@ -145,6 +145,8 @@ def lib() -> ctypes.CDLL:
         L.fgemm_stream_k_work_item.restype = i32
         L.fgemm_small_m_grid.argtypes = [i64, i32, i32, ctypes.POINTER(i32)]
         L.fgemm_small_m_grid.restype = i32
+        L.fgemm_lcma_pair_clusters.argtypes = [i64, i32, i32]
+        L.fgemm_lcma_pair_clusters.restype = i64
         L.fgemm_get_device_model.argtypes = [vp, model_p]
         L.fgemm_set_device_model.argtypes = [vp, model_p]
         for name in ("fgemm_create", "fgemm_destroy", "fgemm_set_stream", "fgemm_matmul",

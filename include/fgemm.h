@@ -519,6 +519,19 @@ typedef struct {
 int32_t fgemm_small_m_grid(int64_t tiles, int32_t k_blocks, int32_t num_sms, int32_t* phases_out);
 
 /*
+ * CTA pairs a Strassen-like launch on CTA pairs uses for `positions` output
+ * positions (256 x tile_n tiles of the 2^-depth-size block space) when `fit`
+ * pairs fit on the device. One level: min(fit, 7 positions). Two levels:
+ * every pair while the positions of the partial last wave, cut into 49
+ * product units each, give at most 24 units per pair; with fewer positions
+ * than pairs, one pair per position; otherwise the largest pair count from
+ * fit down to fit / 2 that divides the positions into whole waves, if any
+ * (else fit). Returns 0 for positions <= 0 or fit <= 0.
+ * Host-only.
+ */
+int64_t fgemm_lcma_pair_clusters(int64_t positions, int32_t depth, int32_t fit);
+
+/*
  * Default model for a device with the given SM count: the mainloop, launch
  * and streaming rates fgemm_calibrate measured on a GB300 (for 152 SMs,
  * scaled by the SM count), expressed as efficiencies against peak_tflops

@@ -698,3 +698,21 @@ def test_model_two_levels_on_pairs_fold_term_and_picks(L):
         [(M, k, k) for M in (16, 128, 1024, 8192) for k in (2048, 4096, 8192, 16384)]
     for shape in shapes:
         assert pick(*shape)[0] != "strassen2", shape
+
+
+def test_lcma_pair_clusters(L):
+    """Pairs of a Strassen-like launch on CTA pairs: one level every pair that
+    has work; two levels one pair per position below the pair count, every
+    pair while the partial wave's units stay within 24 per pair, else the
+    most pairs (down to half) that divide the positions into whole waves."""
+    f = L.fgemm_lcma_pair_clusters
+    assert f(0, 1, 76) == 0 and f(10, 2, 0) == 0
+    assert f(1, 1, 76) == 7 and f(64, 1, 76) == 76 and f(1024, 1, 76) == 76
+    assert f(64, 2, 76) == 64                      # fewer positions than pairs
+    assert f(76, 2, 76) == 76 and f(152, 2, 76) == 76
+    assert f(256, 2, 76) == 76                     # 28 positions left: 19 units per pair
+    assert f(80, 2, 76) == 76                      # 4 positions left: 3 units per pair
+    assert f(128, 2, 76) == 64                     # 52 left would be 34 units per pair: 2 waves of 64
+    assert f(1024, 2, 76) == 76                    # 36 left: 24 units per pair
+    assert f(200, 2, 76) == 50                     # 48 left would be 31 per pair: 4 waves of 50
+    assert f(151, 2, 76) == 76                     # 75 left, and no pair count from 38 to 76 divides 151
