@@ -72,6 +72,9 @@ bool form_is_legal(int64_t M, int64_t N, int64_t K, int32_t epi_kind, fgemm_algo
   const int d = depth_of(algo);
   if (tile_m == 256 && tile_n < 128) return false;
   if (tile_m == 256 && d == 2 && epi_kind == FGEMM_EPI_SWIGLU) return false;
+  // (two levels on pairs: the leaf-operand pre-pass runs a block of 8 rows
+  // per grid row, at most 65535 of them)
+  if (tile_m == 256 && d == 2 && (M / 4 > 8 * 65535 || K / 4 > 8 * 65535)) return false;
   if (d == 0) return true;
   if (tile_n == 64) return false;
   const int64_t g = int64_t{1} << d;

@@ -100,6 +100,7 @@ def test_validation_codes(L):
     assert _v(1024, 1024, 512, algo="strassen2", tile_m=256) == ok   # 4 x 256 rows, 4 x 256 columns
     assert _v(512, 1024, 512, algo="strassen2", tile_m=256) == fgemm.ERR_UNSUPPORTED
     assert _v(1024, 1024, 128, algo="strassen2", tile_m=256) == fgemm.ERR_UNSUPPORTED  # K / 4 < 64
+    assert _v(4 * 8 * 65536, 1024, 1024, algo="strassen2", tile_m=256) == fgemm.ERR_UNSUPPORTED  # pre-pass grid
     assert _v(1024, 2048, 512, algo="strassen2", tile_m=256,
               epi=fgemm.make_epilogue("swiglu", 1.0, None)) == fgemm.ERR_UNSUPPORTED
     assert _v(512, 512, 256, tile_m=192) == fgemm.ERR_INVALID_ARG
