@@ -480,11 +480,13 @@ def run_fgemm(args, rank, world):
                                               fgemm.make_epilogue(epi), algo=form)
             legal.append(form)
             tiles[form] = (f_tm, f_tn, f_us)
-        # forms within a few times of the fastest prediction share the rounds;
-        # much slower ones (two Strassen levels on one-CTA tiles) get their own
+        # forms predicted within 1.5x of the fastest share the rounds; each
+        # slower one (two Strassen levels) is timed in rounds of its own, so
+        # that its long, DRAM-heavy calls do not sit between the calls of
+        # the forms compared with each other
         fast = min(tiles[f][2] for f in legal) if legal else 0.0
-        groups = [[f for f in legal if tiles[f][2] <= 3.0 * fast],
-                  [f for f in legal if tiles[f][2] > 3.0 * fast]]
+        groups = [[f for f in legal if tiles[f][2] <= 1.5 * fast]] + \
+            [[f] for f in legal if tiles[f][2] > 1.5 * fast]
         for g in groups:
             if not g:
                 continue
@@ -497,7 +499,8 @@ def run_fgemm(args, rank, world):
                                "ms_per_call": ms, "calls": n, "predicted_ms": tiles[form][2] / 1e3,
                                "effective_tflops": eff, "executed_tflops": executed,
                                "executed_frac_of_peak": executed / peak if peak else None,
-                               "timing": "median of per-call CUDA events, forms round-robin"}
+                               "timing": "median of per-call CUDA events, " +
+                                         ("forms round-robin" if len(g) > 1 else "in rounds of its own")}
         if "classical" in forms:
             for f, d in forms.items():
                 d["vs_classical"] = d["effective_tflops"] / forms["classical"]["effective_tflops"]
