@@ -1,6 +1,10 @@
 // fgemm_kern_lcma.cu -- one Strassen-like level (Strassen's or Winograd's
-// scheme) on CTA pairs, with the summed operands streamed through HBM
-// (FalconGEMM summary, "Methodology" items 1 and 3).
+// scheme), or two Strassen levels, on CTA pairs, with the summed operands
+// streamed through HBM (FalconGEMM summary, "Methodology" items 1 and 3).
+// Two levels (D == 2) follow the same two steps with the 16 quarter blocks:
+// lcma_form2_kernel forms each side's 49 leaf operands (one rounding each),
+// and the product kernel runs 49 quarter-size products per position and
+// folds them into the 16 output blocks.
 //
 // Two steps:
 //  1. Every summed operand of the scheme is formed once from the 2 x 2 blocks
