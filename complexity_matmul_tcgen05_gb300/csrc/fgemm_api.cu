@@ -877,7 +877,7 @@ fgemm_status_t fgemm_call_launches(fgemm_handle_t h, int64_t M, int64_t N, int64
     const long long positions = fgemm_model_tiles(sub_m, sub_n, 256, p.tile_n);
     const int fit = fgemm::lcma_pair_clusters_fit(p.tile_n, 1);
     if (fit <= 0) return set_msg(h, FGEMM_ERR_CUDA, "cannot size the Strassen pair launch");
-    const int clusters = static_cast<int>(std::min<long long>(fit, positions * 7));
+    const int clusters = static_cast<int>(fgemm_lcma_pair_clusters(positions, 1, fit));
     const StrassenTable& tab =
         p.algo == FGEMM_ALGO_WINOGRAD1 ? fgemm::winograd_table() : fgemm::strassen_table(1);
     // the pre-pass runs unless the product kernel forms both sides' sums
